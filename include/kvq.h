@@ -1,0 +1,190 @@
+/*
+ * kvq.h -- C ABI of the compressed-KV-cache attention library (sm_103a).
+ *
+ * The cache follows "KV殘差窗口：最近Token一定值得高精度嗎？" (huhohoo.com,
+ * kv-residual-window), section 固定預算，先問它保護了誰: the tokens before the
+ * last R are stored as grouped symmetric int4 (group 32, no zero point, K per
+ * channel over 32-token groups, V per token over 32-feature groups) and the
+ * last R tokens stay in floating point. Attention always covers the whole
+ * context, or exactly a listed set of candidate keys (MiniCPM5-2B study,
+ * bjdmk.com.cn/news/5855973, sections 6 and 9). The chunk layout and the
+ * per-row region mass follow "Catnip Week 10 KV Cache Attention Study"
+ * (cappuccino.cafe/kv-attn.html), section "KV Cache 的实际作用"; MXFP8 Q/K
+ * (E4M3 elements, one E8M0 scale per 32 along the head dim) follows its section
+ * "Q/K 与 probability quantization 的影响".
+ *
+ * Conventions for every call:
+ *  - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *    never allocates, never frees and never synchronises. Every pointer must be
+ *    16-byte aligned (else KVQ_ERR_ALIGN).
+ *  - Tensors are dense, row-major, in the index order written beside them.
+ *  - GQA: query head h reads KV head h / (q_heads / kv_heads); q_heads must be
+ *    a multiple of kv_heads.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default
+ *    stream) and runs asynchronously.
+ *  - Argument errors are returned before anything is enqueued. Errors a kernel
+ *    detects are OR-ed as KVQ_DEV_* bits into *dev_status (a device int32 the
+ *    caller zeroes beforehand and reads after synchronising); kernels never
+ *    trap and every wait in them is bounded.
+ *  - sm_scale <= 0 selects 1/sqrt(head_dim). There is no mask.
+ *  - head_dim is a multiple of 32 in [32, 256].
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define KVQ_API __attribute__((visibility("default")))
+#else
+#define KVQ_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *kvq_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+  KVQ_OK = 0,
+  KVQ_ERR_ARG = 1,         /* bad shape, dtype, count or NULL pointer */
+  KVQ_ERR_ALIGN = 2,       /* a pointer is not 16-byte aligned */
+  KVQ_ERR_UNSUPPORTED = 3, /* a valid combination this build has no kernel for */
+  KVQ_ERR_WORKSPACE = 4,   /* workspace given but smaller than required */
+  KVQ_ERR_CUDA = 5         /* a launch failed (cudaGetLastError) */
+} kvq_status;
+
+/* Bits OR-ed into *dev_status by kernels. */
+enum {
+  KVQ_DEV_INDEX = 1,   /* a candidate index outside [0, n_tokens) (that key is skipped) */
+  KVQ_DEV_DUP = 2,     /* a candidate list holds the same index twice (validate only) */
+  KVQ_DEV_TIMEOUT = 4, /* a bounded wait ran out; the outputs of that launch are invalid */
+  KVQ_DEV_BOUNDS = 8   /* an internal index check failed; outputs invalid */
+};
+
+typedef enum { KVQ_F32 = 0, KVQ_BF16 = 1, KVQ_MXFP8 = 2 } kvq_dtype;
+
+/*
+ * A packed cache of `batch` sequences x `kv_heads` heads, each holding
+ * `n_tokens` (N) tokens of `head_dim` (D) features, the last `recent` (R)
+ * tokens kept in the window. With cut = N - R and Gk = ceil(cut / 32):
+ *
+ *   k_codes  [batch][kv_heads][Gk][32][D/2]   uint8: token-group major; byte i
+ *            of a token row holds channels 2i (low nibble) and 2i+1 (high
+ *            nibble) as code + 8 (codes in [-7, 7]); padding tokens of the last
+ *            group hold code 0.
+ *   k_scales [batch][kv_heads][Gk][D]         float: one scale per (group, channel).
+ *   v_codes  [batch][kv_heads][cut][D/2]      uint8: same nibble order, per token.
+ *   v_scales [batch][kv_heads][cut][D/32]     float: one scale per (token, 32 features).
+ *   k_window [batch][kv_heads][R][D]          kwin_dtype: F32, BF16, or MXFP8
+ *            (E4M3 bytes, with k_window_e8m0 [batch][kv_heads][R][D/32] holding
+ *            the E8M0 block-scale bytes, exponent + 127).
+ *   v_window [batch][kv_heads][R][D]          vwin_dtype: F32 or BF16.
+ *   header   {N, D, R, 32}: the 16 bytes of shape metadata, filled by kv_pack.
+ *
+ * Pointers for empty arrays (cut == 0 or R == 0) may be NULL.
+ */
+typedef struct kvq_cache {
+  int32_t batch, kv_heads, n_tokens, head_dim, recent;
+  int32_t kwin_dtype, vwin_dtype;
+  uint8_t *k_codes;
+  float *k_scales;
+  uint8_t *v_codes;
+  float *v_scales;
+  void *k_window;
+  void *v_window;
+  uint8_t *k_window_e8m0;
+  uint32_t header[4];
+} kvq_cache;
+
+/* Array sizes of a cache, in bytes (host only, no GPU needed):
+ * sizes[0..7] = k_codes, k_scales, v_codes, v_scales, k_window, v_window,
+ * k_window_e8m0, header. Returns KVQ_ERR_ARG for an invalid shape. */
+KVQ_API kvq_status kvq_cache_sizes(int32_t batch, int32_t kv_heads, int32_t n_tokens,
+                                   int32_t head_dim, int32_t recent, int32_t kwin_dtype,
+                                   int32_t vwin_dtype, size_t sizes[8]);
+
+/* Total payload in bytes: the sum of kvq_cache_sizes (header included). */
+KVQ_API size_t kvq_cache_bytes(int32_t batch, int32_t kv_heads, int32_t n_tokens,
+                               int32_t head_dim, int32_t recent, int32_t kwin_dtype,
+                               int32_t vwin_dtype);
+
+/*
+ * kv_pack -- quantize K and V into `cache` (residual-window page, section
+ * 固定預算). k, v: [batch][kv_heads][N][D] in in_dtype (F32 or BF16), device.
+ * For each (sequence, head): tokens [0, cut) are quantized, tokens [cut, N)
+ * are copied into the window (rounded to nearest even when the window type is
+ * narrower; E4M3 with an E8M0 scale per 32 features for an MXFP8 K window).
+ * int4 rule: scale = amax / 7 rounded to fp32, code = clamp(rint(x / scale),
+ * -7, 7) with the division correctly rounded in fp32 and ties to even; a zero
+ * scale gives all-zero codes. The cache's shape fields and array pointers are
+ * read; header[] is written. dev_status may be NULL.
+ */
+KVQ_API kvq_status kv_pack(const void *k, const void *v, int32_t in_dtype, kvq_cache *cache,
+                           int32_t *dev_status, kvq_stream_t stream);
+
+/*
+ * kv_attend -- O = softmax(sm_scale * Q K^T) V over all N tokens of the cache,
+ * with K, V dequantized (int4 part) or taken from the window.
+ * q:   [batch][q_heads][n_q][D] in q_dtype (F32 or BF16), device.
+ * out: [batch][q_heads][n_q][D] in out_dtype (F32 or BF16), device.
+ * region_bounds: HOST array of n_regions + 1 increasing token positions
+ *   starting at 0 and ending at N, or NULL; region_mass: device float
+ *   [batch][q_heads][n_q][n_regions] receiving, per query row, the softmax
+ *   mass on tokens [b_k, b_{k+1}) (n_regions <= 16). For an MXFP8 K window, Q
+ *   is quantized the same way (E4M3 + E8M0 per 32) before QK^T.
+ * workspace: device scratch of *ws_bytes bytes. With workspace == NULL the
+ *   call only stores the required size in *ws_bytes and returns KVQ_OK
+ *   (enqueueing nothing); to run, pass a non-NULL workspace even when the
+ *   required size is 0.
+ * Kernel choice: one query row per (sequence, head) with 8 query heads per KV
+ *   head and D = 128 runs the split-K decode kernels; a bf16 or MXFP8 window
+ *   covering all tokens with many queries runs the tensor-core chunk kernel;
+ *   everything else runs the fp32 kernel.
+ */
+KVQ_API kvq_status kv_attend(const kvq_cache *cache, const void *q, int32_t q_dtype,
+                             int32_t q_heads, int32_t n_q, float sm_scale, void *out,
+                             int32_t out_dtype, const int32_t *region_bounds, int32_t n_regions,
+                             float *region_mass, void *workspace, size_t *ws_bytes,
+                             int32_t *dev_status, kvq_stream_t stream);
+
+/*
+ * kv_attend_candidates -- exact attention of each query row over its own
+ * candidate keys only (MiniCPM5-2B study, sections 6 and 9): row (b, h, i)
+ * attends the n_cand token positions idx[b][h][i][:] (int32, device) and no
+ * other key. Lists hold distinct positions in any order. An index outside
+ * [0, N) is skipped and flagged KVQ_DEV_INDEX; with validate != 0 duplicate
+ * positions are flagged KVQ_DEV_DUP (the output of that row is then invalid).
+ * An MXFP8 K window is not supported here (KVQ_ERR_UNSUPPORTED). Other
+ * arguments as for kv_attend.
+ */
+KVQ_API kvq_status kv_attend_candidates(const kvq_cache *cache, const void *q, int32_t q_dtype,
+                                        int32_t q_heads, int32_t n_q, const int32_t *idx,
+                                        int32_t n_cand, int32_t validate, float sm_scale,
+                                        void *out, int32_t out_dtype, void *workspace,
+                                        size_t *ws_bytes, int32_t *dev_status,
+                                        kvq_stream_t stream);
+
+/* Number of kernel launches the last successful call on this thread enqueued. */
+KVQ_API int32_t kvq_last_launch_count(void);
+
+/* Name of the kernel family the last successful call on this thread used
+ * ("pack", "decode", "chunk_bf16", "chunk_mxfp8", "generic", "candidates");
+ * a static string. */
+KVQ_API const char *kvq_last_path(void);
+
+/*
+ * Test hook: bound every mbarrier wait of the next launches on this thread to
+ * `wait_limit_ns` nanoseconds (0 restores the default of one second), and,
+ * when drop_item >= 0, make the decode kernel's loader skip the copy of that
+ * work item so that the wait on it can only run out. Used by the failure tests.
+ */
+KVQ_API void kvq_debug_set(uint32_t wait_limit_ns, int32_t drop_item);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H */

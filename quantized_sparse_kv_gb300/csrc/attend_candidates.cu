@@ -1,0 +1,206 @@
+// Candidate attention: each query row attends exactly the keys listed for it.
+//
+// MiniCPM5-2B study (bjdmk.com.cn/news/5855973), section 6 (score -> top-C
+// candidates -> exact attention inside the candidates) and section 9 (the
+// decode kernel gathers the listed K/V rows and runs an online softmax). Here
+// the gathered rows come from the int4 cache (dequantized on the fly) or from
+// the float window.
+//
+// Layout: one CTA per (query row, query head, sequence), 8 warps. Warp w
+// takes candidates w, w+8, ...; lane l owns features [l*F, (l+1)*F) with
+// F = D/32, so one candidate's K codes, K scales, V codes and V scales are
+// read as contiguous warp-wide segments. Each warp keeps an online softmax in
+// fp32; the 8 warp states are merged through shared memory at the end.
+#include <math_constants.h>
+
+#include "kvq_internal.h"
+
+namespace kvq {
+namespace {
+
+constexpr int kWarps = 8;
+
+struct CandArgs {
+  const uint8_t *k_codes;
+  const float *k_scales;
+  const uint8_t *v_codes;
+  const float *v_scales;
+  const void *k_window;
+  const void *v_window;
+  int kwin, vwin;
+  int Hkv, N, R, cut, Gk;
+  int Hq, group, n_q, C, validate;
+  const void *q;
+  int q_dtype;
+  const int32_t *idx;
+  void *out;
+  int out_dtype;
+  float scale_log2;
+  KernelCtl ctl;
+};
+
+__device__ __forceinline__ float wval(const void *w, int dtype, long i) {
+  return dtype == KVQ_F32 ? static_cast<const float *>(w)[i]
+                          : bf16_to_f32(static_cast<const uint16_t *>(w)[i]);
+}
+
+template <int F>
+__global__ void __launch_bounds__(kWarps * 32) cand_kernel(const CandArgs a) {
+  constexpr int D = F * 32;
+  __shared__ float red_o[kWarps][D];
+  __shared__ float red_m[kWarps], red_l[kWarps];
+  extern __shared__ int32_t list[];  // the row's C indices (validate only)
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int i = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const long u = static_cast<long>(b) * a.Hkv + h / a.group;
+  const long row = (static_cast<long>(b) * a.Hq + h) * a.n_q + i;
+  const int32_t *cand = a.idx + row * a.C;
+  const int d0 = lane * F;
+
+  float q[F];
+#pragma unroll
+  for (int k = 0; k < F; ++k) {
+    const long gi = row * D + d0 + k;
+    q[k] = (a.q_dtype == KVQ_F32 ? static_cast<const float *>(a.q)[gi]
+                                 : bf16_to_f32(static_cast<const uint16_t *>(a.q)[gi])) *
+           a.scale_log2;
+  }
+
+  if (a.validate) {
+    for (int j = threadIdx.x; j < a.C; j += blockDim.x) list[j] = cand[j];
+    __syncthreads();
+    for (int j = threadIdx.x; j < a.C; j += blockDim.x) {
+      const int32_t x = list[j];
+      for (int jj = 0; jj < j; ++jj)
+        if (list[jj] == x) {
+          flag_error(a.ctl, KVQ_DEV_DUP);
+          break;
+        }
+    }
+  }
+
+  float m = -CUDART_INF_F, l = 0.0f, o[F];
+#pragma unroll
+  for (int k = 0; k < F; ++k) o[k] = 0.0f;
+
+  for (int c = warp; c < a.C; c += kWarps) {
+    const int t = cand[c];
+    if (t < 0 || t >= a.N) {
+      if (lane == 0) flag_error(a.ctl, KVQ_DEV_INDEX);
+      continue;
+    }
+    float kv[F], vv[F];
+    if (t < a.cut) {
+      const int g = t / kGroup, r = t % kGroup;
+      const uint8_t *kc = a.k_codes + ((u * a.Gk + g) * kGroup + r) * (D / 2);
+      const float *ks = a.k_scales + (u * a.Gk + g) * D;
+      const uint8_t *vc = a.v_codes + (u * a.cut + t) * (D / 2);
+      const float *vs = a.v_scales + (u * a.cut + t) * (D / 32);
+#pragma unroll
+      for (int k = 0; k < F; ++k) {
+        const int d = d0 + k;
+        const uint8_t kb = kc[d >> 1], vb = vc[d >> 1];
+        kv[k] = static_cast<float>(static_cast<int>((d & 1) ? (kb >> 4) : (kb & 15)) - 8) * ks[d];
+        vv[k] = static_cast<float>(static_cast<int>((d & 1) ? (vb >> 4) : (vb & 15)) - 8) *
+                vs[d / 32];
+      }
+    } else {
+      const long wr = u * a.R + (t - a.cut);
+#pragma unroll
+      for (int k = 0; k < F; ++k) {
+        const long wi = wr * D + d0 + k;
+        kv[k] = wval(a.k_window, a.kwin, wi);
+        vv[k] = wval(a.v_window, a.vwin, wi);
+      }
+    }
+    float s = 0.0f;
+#pragma unroll
+    for (int k = 0; k < F; ++k) s = fmaf(q[k], kv[k], s);
+    s = warp_sum(s);
+    const float mn = fmaxf(m, s);
+    const float corr = exp2f(m - mn), p = exp2f(s - mn);
+    l = l * corr + p;
+#pragma unroll
+    for (int k = 0; k < F; ++k) o[k] = o[k] * corr + p * vv[k];
+    m = mn;
+  }
+
+  if (lane == 0) {
+    red_m[warp] = m;
+    red_l[warp] = l;
+  }
+#pragma unroll
+  for (int k = 0; k < F; ++k) red_o[warp][d0 + k] = o[k];
+  __syncthreads();
+  for (int d = threadIdx.x; d < D; d += blockDim.x) {
+    float mx = -CUDART_INF_F;
+    for (int w = 0; w < kWarps; ++w) mx = fmaxf(mx, red_m[w]);
+    float acc = 0.0f, ls = 0.0f;
+    for (int w = 0; w < kWarps; ++w) {
+      if (red_m[w] == -CUDART_INF_F) continue;
+      const float c = exp2f(red_m[w] - mx);
+      acc += c * red_o[w][d];
+      ls += c * red_l[w];
+    }
+    const float x = acc / ls;
+    if (a.out_dtype == KVQ_F32)
+      static_cast<float *>(a.out)[row * D + d] = x;
+    else
+      static_cast<__nv_bfloat16 *>(a.out)[row * D + d] = __float2bfloat16_rn(x);
+  }
+}
+
+template <int F>
+void launch_f(const CandArgs &a, int B, cudaStream_t s) {
+  dim3 grid(a.n_q, a.Hq, B);
+  const size_t smem = a.validate ? sizeof(int32_t) * a.C : 0;
+  cand_kernel<F><<<grid, kWarps * 32, smem, s>>>(a);
+}
+
+}  // namespace
+
+int launch_attend_candidates(const kvq_cache &c, const void *q, int q_dtype, int Hq, int n_q,
+                             const int32_t *idx, int n_cand, int validate, float scale_log2,
+                             void *out, int out_dtype, const KernelCtl &ctl, cudaStream_t s) {
+  const CacheDims d = dims_of(c);
+  CandArgs a;
+  a.k_codes = c.k_codes;
+  a.k_scales = c.k_scales;
+  a.v_codes = c.v_codes;
+  a.v_scales = c.v_scales;
+  a.k_window = c.k_window;
+  a.v_window = c.v_window;
+  a.kwin = c.kwin_dtype;
+  a.vwin = c.vwin_dtype;
+  a.Hkv = d.Hkv;
+  a.N = d.N;
+  a.R = d.R;
+  a.cut = d.cut;
+  a.Gk = d.Gk;
+  a.Hq = Hq;
+  a.group = Hq / d.Hkv;
+  a.n_q = n_q;
+  a.C = n_cand;
+  a.validate = validate;
+  a.q = q;
+  a.q_dtype = q_dtype;
+  a.idx = idx;
+  a.out = out;
+  a.out_dtype = out_dtype;
+  a.scale_log2 = scale_log2;
+  a.ctl = ctl;
+  switch (d.D / 32) {
+    case 1: launch_f<1>(a, d.B, s); break;
+    case 2: launch_f<2>(a, d.B, s); break;
+    case 3: launch_f<3>(a, d.B, s); break;
+    case 4: launch_f<4>(a, d.B, s); break;
+    case 5: launch_f<5>(a, d.B, s); break;
+    case 6: launch_f<6>(a, d.B, s); break;
+    case 7: launch_f<7>(a, d.B, s); break;
+    default: launch_f<8>(a, d.B, s); break;
+  }
+  return 1;
+}
+
+}  // namespace kvq

@@ -1,0 +1,251 @@
+// fp32 CUDA-core attention over a packed cache, for any supported shape.
+//
+// O = softmax(sm_scale * Q K^T) V over every token, K/V dequantized on the
+// fly (int4 part) or read from the window, with per-row region masses
+// (Catnip study, section "KV Cache 的实际作用": mass per region, all regions
+// summing to 1). This is the exact path of the small head-dim workloads of the
+// residual-window page (head dim 32, 16 queries, N up to 512) and of any shape
+// the specialised kernels do not take.
+//
+// Layout: one CTA per (16 query rows, query head, sequence); 4 warps, 4 rows
+// each. Keys stream through shared memory 32 at a time as fp32; lane j scores
+// key j, the warp keeps an online softmax (running max, rescaled sum) and each
+// lane owns D/32 output features.
+#include <cuda_fp8.h>
+#include <math_constants.h>
+
+#include "kvq_internal.h"
+
+namespace kvq {
+namespace {
+
+constexpr int kTileKeys = 32;
+constexpr int kWarps = 4;
+constexpr int kRowsPerWarp = 4;
+constexpr int kRowsPerCta = kWarps * kRowsPerWarp;
+
+struct GenericArgs {
+  const uint8_t *k_codes;
+  const float *k_scales;
+  const uint8_t *v_codes;
+  const float *v_scales;
+  const void *k_window;
+  const void *v_window;
+  const uint8_t *k_e8m0;
+  int kwin, vwin;
+  int Hkv, N, D, R, cut, Gk;
+  int Hq, group, n_q;
+  const void *q;
+  int q_dtype;
+  void *out;
+  int out_dtype;
+  float *mass;
+  float sm_scale;
+  Regions reg;
+};
+
+__device__ __forceinline__ float nib(uint8_t byte, int odd) {
+  return static_cast<float>(static_cast<int>(odd ? (byte >> 4) : (byte & 15)) - 8);
+}
+
+__device__ __forceinline__ float window_value(const void *w, int dtype, long i) {
+  return dtype == KVQ_F32 ? static_cast<const float *>(w)[i]
+                          : bf16_to_f32(static_cast<const uint16_t *>(w)[i]);
+}
+
+// Round x to MXFP8 inside a warp (lane = position in the 32-block) and return
+// the dequantized value: the same rule kv_pack applies to an MXFP8 K window.
+__device__ __forceinline__ float mxfp8_round_warp(float x) {
+  const float amax = warp_max(fabsf(x));
+  int e = -127;
+  if (amax > 0.0f) {
+    int ex;
+    frexpf(amax, &ex);
+    e = max(-127, min(127, ex - 1 - 8));
+  }
+  const uint8_t c =
+      static_cast<uint8_t>(__nv_cvt_float_to_fp8(ldexpf(x, -e), __NV_SATFINITE, __NV_E4M3));
+  return mxfp8_value(c, static_cast<uint8_t>(e + 127));
+}
+
+template <int DPL>
+__global__ void __launch_bounds__(kWarps * 32) generic_attend_kernel(GenericArgs a) {
+  constexpr int D = DPL * 32;
+  extern __shared__ float sm[];
+  float *Ks = sm;                        // [32][D+1]
+  float *Vs = Ks + kTileKeys * (D + 1);  // [32][D]
+  float *Qs = Vs + kTileKeys * D;        // [16][D]
+  float *Ps = Qs + kRowsPerCta * D;      // [16][32]
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int h = blockIdx.y, b = blockIdx.z;
+  const long u = static_cast<long>(b) * a.Hkv + h / a.group;
+  const int q0 = blockIdx.x * kRowsPerCta;
+  const long qbase = (static_cast<long>(b) * a.Hq + h) * a.n_q;
+
+  for (int i = tid; i < kRowsPerCta * D; i += blockDim.x) {
+    const int r = i / D, d = i % D;
+    float x = 0.0f;
+    if (q0 + r < a.n_q) {
+      const long gi = (qbase + q0 + r) * D + d;
+      x = a.q_dtype == KVQ_F32 ? static_cast<const float *>(a.q)[gi]
+                               : bf16_to_f32(static_cast<const uint16_t *>(a.q)[gi]);
+    }
+    Qs[i] = x;
+  }
+  __syncthreads();
+  if (a.kwin == KVQ_MXFP8) {  // Q takes the same MXFP8 rounding as the K window
+    for (int r = warp; r < kRowsPerCta; r += kWarps)
+      for (int j = 0; j < D / 32; ++j)
+        Qs[r * D + 32 * j + lane] = mxfp8_round_warp(Qs[r * D + 32 * j + lane]);
+    __syncthreads();
+  }
+
+  float m[kRowsPerWarp], l[kRowsPerWarp], rm[kRowsPerWarp], o[kRowsPerWarp][DPL];
+#pragma unroll
+  for (int r = 0; r < kRowsPerWarp; ++r) {
+    m[r] = -CUDART_INF_F;
+    l[r] = 0.0f;
+    rm[r] = 0.0f;
+#pragma unroll
+    for (int k = 0; k < DPL; ++k) o[r][k] = 0.0f;
+  }
+
+  for (int t0 = 0; t0 < a.N; t0 += kTileKeys) {
+    __syncthreads();
+    for (int i = tid; i < kTileKeys * D; i += blockDim.x) {
+      const int j = i / D, d = i % D, t = t0 + j;
+      float kv = 0.0f, vv = 0.0f;
+      if (t < a.cut) {
+        const int g = t / kGroup, r = t % kGroup;
+        const long kb = ((u * a.Gk + g) * kGroup + r) * (D / 2) + d / 2;
+        kv = nib(a.k_codes[kb], d & 1) * a.k_scales[(u * a.Gk + g) * D + d];
+        const long vb = (u * a.cut + t) * (D / 2) + d / 2;
+        vv = nib(a.v_codes[vb], d & 1) * a.v_scales[(u * a.cut + t) * (D / 32) + d / 32];
+      } else if (t < a.N) {
+        const long wi = (u * a.R + (t - a.cut)) * D + d;
+        if (a.kwin == KVQ_MXFP8)
+          kv = mxfp8_value(static_cast<const uint8_t *>(a.k_window)[wi],
+                           a.k_e8m0[(u * a.R + (t - a.cut)) * (D / 32) + d / 32]);
+        else
+          kv = window_value(a.k_window, a.kwin, wi);
+        vv = window_value(a.v_window, a.vwin, wi);
+      }
+      Ks[j * (D + 1) + d] = kv;
+      Vs[j * D + d] = vv;
+    }
+    __syncthreads();
+
+    const bool valid = t0 + lane < a.N;
+#pragma unroll
+    for (int r = 0; r < kRowsPerWarp; ++r) {
+      const float *qr = Qs + (warp * kRowsPerWarp + r) * D;
+      const float *kr = Ks + lane * (D + 1);
+      float s = 0.0f;
+#pragma unroll 8
+      for (int d = 0; d < D; ++d) s = fmaf(qr[d], kr[d], s);
+      s = valid ? s * a.sm_scale : -CUDART_INF_F;
+      const float m_new = fmaxf(m[r], warp_max(s));
+      const float corr = expf(m[r] - m_new);
+      const float p = valid ? expf(s - m_new) : 0.0f;
+      l[r] = l[r] * corr + warp_sum(p);
+      rm[r] *= corr;
+      for (int k = 0; k < a.reg.n; ++k) {
+        if (a.reg.b[k] < t0 + kTileKeys && a.reg.b[k + 1] > t0) {
+          const int t = t0 + lane;
+          const float ps = warp_sum((t >= a.reg.b[k] && t < a.reg.b[k + 1]) ? p : 0.0f);
+          if (lane == k) rm[r] += ps;
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < DPL; ++k) o[r][k] *= corr;
+      m[r] = m_new;
+      Ps[(warp * kRowsPerWarp + r) * kTileKeys + lane] = p;
+    }
+    __syncwarp();
+#pragma unroll
+    for (int r = 0; r < kRowsPerWarp; ++r) {
+      const float *pr = Ps + (warp * kRowsPerWarp + r) * kTileKeys;
+      for (int j = 0; j < kTileKeys; ++j) {
+        const float pj = pr[j];
+#pragma unroll
+        for (int k = 0; k < DPL; ++k) o[r][k] = fmaf(pj, Vs[j * D + lane + 32 * k], o[r][k]);
+      }
+    }
+  }
+
+#pragma unroll
+  for (int r = 0; r < kRowsPerWarp; ++r) {
+    const int row = q0 + warp * kRowsPerWarp + r;
+    if (row >= a.n_q) continue;
+    const float inv = 1.0f / l[r];
+    const long ob = (qbase + row) * D;
+#pragma unroll
+    for (int k = 0; k < DPL; ++k) {
+      const float x = o[r][k] * inv;
+      if (a.out_dtype == KVQ_F32)
+        static_cast<float *>(a.out)[ob + lane + 32 * k] = x;
+      else
+        static_cast<__nv_bfloat16 *>(a.out)[ob + lane + 32 * k] = __float2bfloat16_rn(x);
+    }
+    if (a.mass && lane < a.reg.n) a.mass[(qbase + row) * a.reg.n + lane] = rm[r] * inv;
+  }
+}
+
+template <int DPL>
+void launch_dpl(const GenericArgs &a, int B, cudaStream_t s) {
+  constexpr int D = DPL * 32;
+  const size_t smem = sizeof(float) * (kTileKeys * (D + 1) + kTileKeys * D + kRowsPerCta * D +
+                                       kRowsPerCta * kTileKeys);
+  cudaFuncSetAttribute(generic_attend_kernel<DPL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       static_cast<int>(smem));
+  dim3 grid((a.n_q + kRowsPerCta - 1) / kRowsPerCta, a.Hq, B);
+  generic_attend_kernel<DPL><<<grid, kWarps * 32, smem, s>>>(a);
+}
+
+}  // namespace
+
+int launch_attend_generic(const kvq_cache &c, const void *q, int q_dtype, int Hq, int n_q,
+                          float sm_scale, void *out, int out_dtype, const int32_t *bounds,
+                          int n_regions, float *mass, const KernelCtl &, cudaStream_t s) {
+  const CacheDims d = dims_of(c);
+  GenericArgs a;
+  a.k_codes = c.k_codes;
+  a.k_scales = c.k_scales;
+  a.v_codes = c.v_codes;
+  a.v_scales = c.v_scales;
+  a.k_window = c.k_window;
+  a.v_window = c.v_window;
+  a.k_e8m0 = c.k_window_e8m0;
+  a.kwin = c.kwin_dtype;
+  a.vwin = c.vwin_dtype;
+  a.Hkv = d.Hkv;
+  a.N = d.N;
+  a.D = d.D;
+  a.R = d.R;
+  a.cut = d.cut;
+  a.Gk = d.Gk;
+  a.Hq = Hq;
+  a.group = Hq / d.Hkv;
+  a.n_q = n_q;
+  a.q = q;
+  a.q_dtype = q_dtype;
+  a.out = out;
+  a.out_dtype = out_dtype;
+  a.mass = mass;
+  a.sm_scale = sm_scale;
+  a.reg = make_regions(bounds, n_regions);
+  switch (d.D / 32) {
+    case 1: launch_dpl<1>(a, d.B, s); break;
+    case 2: launch_dpl<2>(a, d.B, s); break;
+    case 3: launch_dpl<3>(a, d.B, s); break;
+    case 4: launch_dpl<4>(a, d.B, s); break;
+    case 5: launch_dpl<5>(a, d.B, s); break;
+    case 6: launch_dpl<6>(a, d.B, s); break;
+    case 7: launch_dpl<7>(a, d.B, s); break;
+    default: launch_dpl<8>(a, d.B, s); break;
+  }
+  return 1;
+}
+
+}  // namespace kvq

@@ -1,0 +1,236 @@
+// C ABI entry points: argument checks, kernel choice, launch accounting.
+// Declarations and the meaning of every argument are in include/kvq.h.
+#include <math.h>
+
+#include "kvq_internal.h"
+
+namespace {
+
+thread_local int32_t g_last_launches = 0;
+thread_local const char *g_last_path = "";
+thread_local uint64_t g_wait_limit_ns = 0;
+thread_local int32_t g_drop_item = -1;
+
+constexpr uint64_t kDefaultWaitNs = 1000000000ull;  // one second
+constexpr double kLog2e = 1.4426950408889634;
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int sm_count() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 148;
+  if (dev < 64 && cache[dev] > 0) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    n = 148;
+  if (dev < 64) cache[dev] = n;
+  return n;
+}
+
+kvq::KernelCtl make_ctl(int32_t *dev_status) {
+  kvq::KernelCtl c;
+  c.dev_status = dev_status;
+  c.wait_limit_ns = g_wait_limit_ns ? g_wait_limit_ns : kDefaultWaitNs;
+  c.drop_item = g_drop_item;
+  return c;
+}
+
+bool shape_ok(int32_t batch, int32_t kv_heads, int32_t n_tokens, int32_t head_dim, int32_t recent,
+              int32_t kwin, int32_t vwin) {
+  if (batch < 1 || kv_heads < 1 || n_tokens < 1) return false;
+  if (head_dim < 32 || head_dim > 256 || head_dim % 32) return false;
+  if (recent < 0 || recent > n_tokens) return false;
+  if (kwin != KVQ_F32 && kwin != KVQ_BF16 && kwin != KVQ_MXFP8) return false;
+  if (vwin != KVQ_F32 && vwin != KVQ_BF16) return false;
+  return true;
+}
+
+size_t elem_bytes(int32_t dt) { return dt == KVQ_F32 ? 4 : dt == KVQ_BF16 ? 2 : 1; }
+
+// Validates the cache descriptor's shape and the pointers its arrays need.
+kvq_status check_cache(const kvq_cache *c) {
+  if (!c) return KVQ_ERR_ARG;
+  if (!shape_ok(c->batch, c->kv_heads, c->n_tokens, c->head_dim, c->recent, c->kwin_dtype,
+                c->vwin_dtype))
+    return KVQ_ERR_ARG;
+  const int cut = c->n_tokens - c->recent;
+  if (cut > 0) {
+    if (!c->k_codes || !c->k_scales || !c->v_codes || !c->v_scales) return KVQ_ERR_ARG;
+    if (!aligned16(c->k_codes) || !aligned16(c->k_scales) || !aligned16(c->v_codes) ||
+        !aligned16(c->v_scales))
+      return KVQ_ERR_ALIGN;
+  }
+  if (c->recent > 0) {
+    if (!c->k_window || !c->v_window) return KVQ_ERR_ARG;
+    if (c->kwin_dtype == KVQ_MXFP8 && !c->k_window_e8m0) return KVQ_ERR_ARG;
+    if (!aligned16(c->k_window) || !aligned16(c->v_window)) return KVQ_ERR_ALIGN;
+    if (c->kwin_dtype == KVQ_MXFP8 && !aligned16(c->k_window_e8m0)) return KVQ_ERR_ALIGN;
+  }
+  return KVQ_OK;
+}
+
+kvq_status finish(int launches, const char *path) {
+  if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
+  g_last_launches = launches;
+  g_last_path = path;
+  return KVQ_OK;
+}
+
+float resolve_scale(float sm_scale, int head_dim) {
+  return sm_scale > 0.0f ? sm_scale
+                         : static_cast<float>(1.0 / sqrt(static_cast<double>(head_dim)));
+}
+
+}  // namespace
+
+extern "C" {
+
+kvq_status kvq_cache_sizes(int32_t batch, int32_t kv_heads, int32_t n_tokens, int32_t head_dim,
+                           int32_t recent, int32_t kwin_dtype, int32_t vwin_dtype,
+                           size_t sizes[8]) {
+  if (!sizes || !shape_ok(batch, kv_heads, n_tokens, head_dim, recent, kwin_dtype, vwin_dtype))
+    return KVQ_ERR_ARG;
+  const size_t units = static_cast<size_t>(batch) * kv_heads;
+  const size_t cut = static_cast<size_t>(n_tokens - recent);
+  const size_t gk = (cut + 31) / 32;
+  const size_t d = static_cast<size_t>(head_dim);
+  sizes[0] = units * gk * 32 * d / 2;                 // k_codes
+  sizes[1] = units * gk * d * sizeof(float);          // k_scales
+  sizes[2] = units * cut * d / 2;                     // v_codes
+  sizes[3] = units * cut * (d / 32) * sizeof(float);  // v_scales
+  sizes[4] = units * recent * d * elem_bytes(kwin_dtype);
+  sizes[5] = units * recent * d * elem_bytes(vwin_dtype);
+  sizes[6] = kwin_dtype == KVQ_MXFP8 ? units * recent * (d / 32) : 0;
+  sizes[7] = 16;                                      // {N, D, R, 32}
+  return KVQ_OK;
+}
+
+size_t kvq_cache_bytes(int32_t batch, int32_t kv_heads, int32_t n_tokens, int32_t head_dim,
+                       int32_t recent, int32_t kwin_dtype, int32_t vwin_dtype) {
+  size_t s[8];
+  if (kvq_cache_sizes(batch, kv_heads, n_tokens, head_dim, recent, kwin_dtype, vwin_dtype, s) !=
+      KVQ_OK)
+    return 0;
+  size_t total = 0;
+  for (int i = 0; i < 8; ++i) total += s[i];
+  return total;
+}
+
+kvq_status kv_pack(const void *k, const void *v, int32_t in_dtype, kvq_cache *cache,
+                   int32_t *dev_status, kvq_stream_t stream) {
+  const kvq_status st = check_cache(cache);
+  if (st != KVQ_OK) return st;
+  if (in_dtype != KVQ_F32 && in_dtype != KVQ_BF16) return KVQ_ERR_ARG;
+  if (!k || !v) return KVQ_ERR_ARG;
+  if (!aligned16(k) || !aligned16(v) || (dev_status && !aligned16(dev_status)))
+    return KVQ_ERR_ALIGN;
+  cache->header[0] = static_cast<uint32_t>(cache->n_tokens);
+  cache->header[1] = static_cast<uint32_t>(cache->head_dim);
+  cache->header[2] = static_cast<uint32_t>(cache->recent);
+  cache->header[3] = 32u;
+  const int n = kvq::launch_pack(k, v, in_dtype, *cache, make_ctl(dev_status),
+                                 reinterpret_cast<cudaStream_t>(stream));
+  return finish(n, "pack");
+}
+
+kvq_status kv_attend(const kvq_cache *cache, const void *q, int32_t q_dtype, int32_t q_heads,
+                     int32_t n_q, float sm_scale, void *out, int32_t out_dtype,
+                     const int32_t *region_bounds, int32_t n_regions, float *region_mass,
+                     void *workspace, size_t *ws_bytes, int32_t *dev_status,
+                     kvq_stream_t stream) {
+  kvq_status st = check_cache(cache);
+  if (st != KVQ_OK) return st;
+  if (!ws_bytes) return KVQ_ERR_ARG;
+  if (q_heads < 1 || q_heads % cache->kv_heads || n_q < 1) return KVQ_ERR_ARG;
+  if ((q_dtype != KVQ_F32 && q_dtype != KVQ_BF16) ||
+      (out_dtype != KVQ_F32 && out_dtype != KVQ_BF16))
+    return KVQ_ERR_ARG;
+  if (region_bounds) {
+    if (n_regions < 1 || n_regions > 16 || !region_mass) return KVQ_ERR_ARG;
+    if (region_bounds[0] != 0 || region_bounds[n_regions] != cache->n_tokens) return KVQ_ERR_ARG;
+    for (int i = 0; i < n_regions; ++i)
+      if (region_bounds[i + 1] <= region_bounds[i]) return KVQ_ERR_ARG;
+    if (!aligned16(region_mass)) return KVQ_ERR_ALIGN;
+  }
+  const bool regions = region_bounds != nullptr;
+  const float scale = resolve_scale(sm_scale, cache->head_dim);
+  const int sms = sm_count();
+
+  enum { GENERIC, DECODE, CHUNK } path = GENERIC;
+  if (kvq::chunk_supported(*cache, q_dtype, q_heads, n_q))
+    path = CHUNK;
+  else if (!regions && kvq::decode_supported(*cache, q_dtype, q_heads, n_q))
+    path = DECODE;
+  size_t need = 0;
+  if (path == DECODE) need = kvq::decode_workspace_bytes(*cache, q_heads, sms);
+  if (path == CHUNK) need = kvq::chunk_workspace_bytes(*cache, q_heads, n_q);
+  if (!workspace) {
+    *ws_bytes = need;
+    return KVQ_OK;
+  }
+  if (*ws_bytes < need) return KVQ_ERR_WORKSPACE;
+  if (!q || !out) return KVQ_ERR_ARG;
+  if (!aligned16(q) || !aligned16(out) || !aligned16(workspace) ||
+      (dev_status && !aligned16(dev_status)))
+    return KVQ_ERR_ALIGN;
+
+  const kvq::KernelCtl ctl = make_ctl(dev_status);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (path == CHUNK) {
+    const int n = kvq::launch_attend_chunk(*cache, q, q_heads, n_q,
+                                           static_cast<float>(scale * kLog2e), out, out_dtype,
+                                           region_bounds, n_regions, region_mass, workspace, ctl, s);
+    return finish(n, cache->kwin_dtype == KVQ_MXFP8 ? "chunk_mxfp8" : "chunk_bf16");
+  }
+  if (path == DECODE) {
+    const int n = kvq::launch_attend_decode(*cache, q, q_dtype,
+                                            static_cast<float>(scale * kLog2e), out, out_dtype,
+                                            workspace, ctl, sms, s);
+    return finish(n, "decode");
+  }
+  const int n = kvq::launch_attend_generic(*cache, q, q_dtype, q_heads, n_q, scale, out,
+                                           out_dtype, region_bounds, n_regions, region_mass, ctl, s);
+  return finish(n, "generic");
+}
+
+kvq_status kv_attend_candidates(const kvq_cache *cache, const void *q, int32_t q_dtype,
+                                int32_t q_heads, int32_t n_q, const int32_t *idx,
+                                int32_t n_cand, int32_t validate, float sm_scale, void *out,
+                                int32_t out_dtype, void *workspace, size_t *ws_bytes,
+                                int32_t *dev_status, kvq_stream_t stream) {
+  kvq_status st = check_cache(cache);
+  if (st != KVQ_OK) return st;
+  if (!ws_bytes) return KVQ_ERR_ARG;
+  if (q_heads < 1 || q_heads % cache->kv_heads || n_q < 1 || n_cand < 1) return KVQ_ERR_ARG;
+  if ((q_dtype != KVQ_F32 && q_dtype != KVQ_BF16) ||
+      (out_dtype != KVQ_F32 && out_dtype != KVQ_BF16))
+    return KVQ_ERR_ARG;
+  if (cache->recent > 0 && cache->kwin_dtype == KVQ_MXFP8) return KVQ_ERR_UNSUPPORTED;
+  if (n_cand > 65536) return KVQ_ERR_UNSUPPORTED;
+  if (!workspace) {
+    *ws_bytes = 0;
+    return KVQ_OK;
+  }
+  if (!q || !out || !idx) return KVQ_ERR_ARG;
+  if (!aligned16(q) || !aligned16(out) || !aligned16(idx) ||
+      (dev_status && !aligned16(dev_status)))
+    return KVQ_ERR_ALIGN;
+  const float scale = resolve_scale(sm_scale, cache->head_dim);
+  const int n = kvq::launch_attend_candidates(*cache, q, q_dtype, q_heads, n_q, idx, n_cand,
+                                              validate, static_cast<float>(scale * kLog2e), out,
+                                              out_dtype, make_ctl(dev_status),
+                                              reinterpret_cast<cudaStream_t>(stream));
+  return finish(n, "candidates");
+}
+
+int32_t kvq_last_launch_count(void) { return g_last_launches; }
+
+const char *kvq_last_path(void) { return g_last_path; }
+
+void kvq_debug_set(uint32_t wait_limit_ns, int32_t drop_item) {
+  g_wait_limit_ns = wait_limit_ns;
+  g_drop_item = drop_item;
+}
+
+}  // extern "C"

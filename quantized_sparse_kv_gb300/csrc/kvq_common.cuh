@@ -1,0 +1,140 @@
+// Device helpers shared by the kvq kernels: error reporting, bounded mbarrier
+// waits, 1-D bulk copies (TMA) and small conversions. sm_103a only.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kvq.h"
+
+namespace kvq {
+
+constexpr int kGroup = 32;
+
+// Launch-wide settings every kernel receives by value.
+struct KernelCtl {
+  int32_t *dev_status;      // may be nullptr
+  uint64_t wait_limit_ns;   // bound of every mbarrier wait
+  int32_t drop_item;        // test hook: loader skips this work item (-1: none)
+};
+
+__device__ __forceinline__ void flag_error(const KernelCtl &ctl, int bit) {
+  if (ctl.dev_status) atomicOr(ctl.dev_status, bit);
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ------------------------------------------------------------------ mbarrier
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for the phase with the given parity to complete, for at most
+// limit_ns nanoseconds of global time. Returns false when the limit ran out.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t spin = 1;; ++spin) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((spin & 63u) == 0 && global_ns() - t0 > limit_ns) return false;
+  }
+}
+
+// ------------------------------------------------------------------ bulk copy
+// 1-D global -> shared copy completing on an mbarrier (tx bytes). Both
+// addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes,
+                                         uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// ------------------------------------------------------------------ conversions
+__device__ __forceinline__ float bf16_to_f32(uint16_t b) {
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+template <typename T>
+__device__ __forceinline__ float load_f32(const T *p);
+template <>
+__device__ __forceinline__ float load_f32<float>(const float *p) {
+  return *p;
+}
+template <>
+__device__ __forceinline__ float load_f32<__nv_bfloat16>(const __nv_bfloat16 *p) {
+  return __bfloat162float(*p);
+}
+
+template <typename T>
+__device__ __forceinline__ void store_from_f32(T *p, float x);
+template <>
+__device__ __forceinline__ void store_from_f32<float>(float *p, float x) {
+  *p = x;
+}
+template <>
+__device__ __forceinline__ void store_from_f32<__nv_bfloat16>(__nv_bfloat16 *p, float x) {
+  *p = __float2bfloat16_rn(x);
+}
+
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+  return x;
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+// Value of an E4M3 byte times 2^(e8m0 - 127), computed exactly in fp32
+// (E4M3 has 3 mantissa bits; the power of two is applied with ldexpf).
+__device__ __forceinline__ float mxfp8_value(uint8_t code, uint8_t e8m0) {
+  const int e = (code >> 3) & 0xF;
+  const int m = code & 0x7;
+  float mag = (e == 0) ? ldexpf(static_cast<float>(m), -9)
+                       : ldexpf(static_cast<float>(8 + m), e - 10);
+  if ((code & 0x7F) == 0x7F) mag = __int_as_float(0x7fc00000);
+  return ldexpf((code & 0x80) ? -mag : mag, static_cast<int>(e8m0) - 127);
+}
+
+}  // namespace kvq

@@ -1,0 +1,73 @@
+// Host-side launchers implemented by the kernel files and called by the C ABI
+// layer (kvq_api.cu). Arguments are already validated when these run.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/kvq.h"
+#include "kvq_common.cuh"
+
+namespace kvq {
+
+// Shape of a cache, derived once from a kvq_cache.
+struct CacheDims {
+  int B, Hkv, N, D, R, cut, Gk;
+};
+
+inline CacheDims dims_of(const kvq_cache &c) {
+  CacheDims d;
+  d.B = c.batch;
+  d.Hkv = c.kv_heads;
+  d.N = c.n_tokens;
+  d.D = c.head_dim;
+  d.R = c.recent;
+  d.cut = c.n_tokens - c.recent;
+  d.Gk = (d.cut + kGroup - 1) / kGroup;
+  return d;
+}
+
+// Region bounds live in a small by-value struct so kernels need no extra copy.
+struct Regions {
+  int n;      // number of regions, 0 = none
+  int b[17];  // bounds b[0] = 0 < ... < b[n] = N
+};
+
+inline Regions make_regions(const int32_t *bounds, int n) {
+  Regions r{};
+  r.n = bounds ? n : 0;
+  if (bounds)
+    for (int i = 0; i <= r.n && i < 17; ++i) r.b[i] = bounds[i];
+  return r;
+}
+
+// pack.cu
+int launch_pack(const void *k, const void *v, int in_dtype, const kvq_cache &c,
+                const KernelCtl &ctl, cudaStream_t s);
+
+// attend_generic.cu: fp32 CUDA-core attention for any supported shape.
+int launch_attend_generic(const kvq_cache &c, const void *q, int q_dtype, int Hq, int n_q,
+                          float sm_scale, void *out, int out_dtype, const int32_t *bounds,
+                          int n_regions, float *mass, const KernelCtl &ctl, cudaStream_t s);
+
+// attend_decode.cu: split-K decode for D = 128, 8 query heads per KV head, one query.
+bool decode_supported(const kvq_cache &c, int q_dtype, int Hq, int n_q);
+size_t decode_workspace_bytes(const kvq_cache &c, int Hq, int num_sms);
+int launch_attend_decode(const kvq_cache &c, const void *q, int q_dtype, float scale_log2,
+                         void *out, int out_dtype, void *ws, const KernelCtl &ctl, int num_sms,
+                         cudaStream_t s);
+
+// attend_candidates.cu
+int launch_attend_candidates(const kvq_cache &c, const void *q, int q_dtype, int Hq, int n_q,
+                             const int32_t *idx, int n_cand, int validate, float scale_log2,
+                             void *out, int out_dtype, const KernelCtl &ctl, cudaStream_t s);
+
+// attend_chunk.cu: tcgen05 chunk attention over an all-window bf16 / MXFP8 cache.
+bool chunk_supported(const kvq_cache &c, int q_dtype, int Hq, int n_q);
+size_t chunk_workspace_bytes(const kvq_cache &c, int Hq, int n_q);
+int launch_attend_chunk(const kvq_cache &c, const void *q, int Hq, int n_q, float scale_log2,
+                        void *out, int out_dtype, const int32_t *bounds, int n_regions,
+                        float *mass, void *ws, const KernelCtl &ctl, cudaStream_t s);
+
+}  // namespace kvq

@@ -1,0 +1,183 @@
+// kv_pack kernels: grouped symmetric int4 for the tokens before the window and
+// a copy (or MXFP8 encoding) of the last R tokens.
+//
+// Residual-window page ("KV殘差窗口", section 固定預算): group size 32, K per
+// channel over 32-token groups, V per token over 32-feature groups, the last R
+// tokens kept in floating point. Rounding: scale = amax / 7 rounded once to
+// fp32; code = clamp(rint(x / scale), -7, 7) with the division correctly
+// rounded (__fdiv_rn) and ties to even (__float2int_rn); a zero scale gives
+// zero codes. MXFP8 K window: Catnip study, section "Q/K 与 probability
+// quantization 的影响" (E4M3, E8M0 scale per 32 along the head dim).
+#include <cuda_fp8.h>
+
+#include <algorithm>
+
+#include "kvq_internal.h"
+
+namespace kvq {
+namespace {
+
+__device__ __forceinline__ float int4_scale(float amax) { return __fdiv_rn(amax, 7.0f); }
+
+__device__ __forceinline__ int int4_code(float x, float scale) {
+  if (scale == 0.0f) return 0;
+  int c = __float2int_rn(__fdiv_rn(x, scale));
+  return max(-7, min(7, c));
+}
+
+// One CTA per (sequence*head, K group): loads 32 tokens x D, writes the
+// group's nibbles [32][D/2] and its D per-channel scales.
+template <typename T>
+__global__ void __launch_bounds__(256) pack_k_kernel(const T *__restrict__ k, int N, int D,
+                                                     int cut, int Gk,
+                                                     uint8_t *__restrict__ k_codes,
+                                                     float *__restrict__ k_scales) {
+  extern __shared__ float tile[];  // [32][D] values, then [32][D] int8 codes
+  int8_t *codes = reinterpret_cast<int8_t *>(tile + kGroup * D);
+  const int g = blockIdx.x % Gk;
+  const long u = blockIdx.x / Gk;
+  const T *src = k + (u * N + static_cast<long>(g) * kGroup) * D;
+  const int valid = min(kGroup, cut - g * kGroup);
+  for (int i = threadIdx.x; i < kGroup * D; i += blockDim.x) {
+    const int t = i / D;
+    tile[i] = (t < valid) ? load_f32(src + i) : 0.0f;
+  }
+  __syncthreads();
+  for (int c = threadIdx.x; c < D; c += blockDim.x) {
+    float amax = 0.0f;
+    for (int t = 0; t < kGroup; ++t) amax = fmaxf(amax, fabsf(tile[t * D + c]));
+    const float s = int4_scale(amax);
+    k_scales[(u * Gk + g) * D + c] = s;
+    for (int t = 0; t < kGroup; ++t)
+      codes[t * D + c] = static_cast<int8_t>(int4_code(tile[t * D + c], s));
+  }
+  __syncthreads();
+  uint8_t *dst = k_codes + (u * Gk + g) * (kGroup * D / 2);
+  for (int i = threadIdx.x; i < kGroup * D / 2; i += blockDim.x) {
+    const int t = i / (D / 2), b = i % (D / 2);
+    const int lo = codes[t * D + 2 * b] + 8, hi = codes[t * D + 2 * b + 1] + 8;
+    dst[i] = static_cast<uint8_t>(lo | (hi << 4));
+  }
+}
+
+// One warp per (token, 32-feature group) of the quantized part of V.
+template <typename T>
+__global__ void __launch_bounds__(256) pack_v_kernel(const T *__restrict__ v, long rows, int N,
+                                                     int D, int cut,
+                                                     uint8_t *__restrict__ v_codes,
+                                                     float *__restrict__ v_scales) {
+  const int groups = D / kGroup;
+  const long task = static_cast<long>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32;
+  if (task >= rows * groups) return;
+  const int lane = threadIdx.x & 31;
+  const long row = task / groups;  // over (unit, token < cut)
+  const int j = static_cast<int>(task % groups);
+  const long u = row / cut;
+  const long t = row % cut;
+  const float x = load_f32(v + (u * N + t) * D + j * kGroup + lane);
+  const float amax = warp_max(fabsf(x));
+  const float s = int4_scale(amax);
+  const int code = int4_code(x, s) + 8;
+  const int hi = __shfl_down_sync(0xffffffffu, code, 1);
+  if ((lane & 1) == 0)
+    v_codes[row * (D / 2) + j * (kGroup / 2) + lane / 2] = static_cast<uint8_t>(code | (hi << 4));
+  if (lane == 0) v_scales[row * groups + j] = s;
+}
+
+// Window copy with dtype change (fp32 <-> bf16, nearest even).
+template <typename TI, typename TO>
+__global__ void window_copy_kernel(const TI *__restrict__ x, long rows, int N, int D, int R,
+                                   TO *__restrict__ w) {
+  const long n = rows * D;
+  for (long i = blockIdx.x * static_cast<long>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<long>(gridDim.x) * blockDim.x) {
+    const long row = i / D, d = i % D;
+    const long u = row / R, t = row % R;
+    store_from_f32(w + i, load_f32(x + (u * N + (N - R) + t) * D + d));
+  }
+}
+
+// MXFP8 window: one warp per (token, 32-feature block). Block exponent
+// e = floor(log2 amax) - 8 clamped to [-127, 127] (-127 for a zero block);
+// elements x * 2^-e rounded to E4M3, nearest even, saturating at 448.
+template <typename TI>
+__global__ void __launch_bounds__(256) window_mxfp8_kernel(const TI *__restrict__ x, long rows,
+                                                           int N, int D, int R,
+                                                           uint8_t *__restrict__ codes,
+                                                           uint8_t *__restrict__ e8m0) {
+  const int groups = D / kGroup;
+  const long task = static_cast<long>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32;
+  if (task >= rows * groups) return;
+  const int lane = threadIdx.x & 31;
+  const long row = task / groups;
+  const int j = static_cast<int>(task % groups);
+  const long u = row / R, t = row % R;
+  const float val = load_f32(x + (u * N + (N - R) + t) * D + j * kGroup + lane);
+  const float amax = warp_max(fabsf(val));
+  int e = -127;
+  if (amax > 0.0f) {
+    int ex;
+    frexpf(amax, &ex);  // amax = f * 2^ex, f in [0.5, 1)
+    e = max(-127, min(127, ex - 1 - 8));
+  }
+  const float y = ldexpf(val, -e);
+  const __nv_fp8_storage_t c = __nv_cvt_float_to_fp8(y, __NV_SATFINITE, __NV_E4M3);
+  codes[row * D + j * kGroup + lane] = static_cast<uint8_t>(c);
+  if (lane == 0) e8m0[row * groups + j] = static_cast<uint8_t>(e + 127);
+}
+
+template <typename T>
+int pack_typed(const T *k, const T *v, const kvq_cache &c, cudaStream_t s) {
+  const CacheDims d = dims_of(c);
+  const long units = static_cast<long>(d.B) * d.Hkv;
+  int launches = 0;
+  if (d.cut > 0) {
+    const size_t smem = static_cast<size_t>(kGroup) * d.D * (sizeof(float) + 1);
+    cudaFuncSetAttribute(pack_k_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         static_cast<int>(smem));
+    pack_k_kernel<T><<<static_cast<unsigned>(units * d.Gk), 256, smem, s>>>(
+        k, d.N, d.D, d.cut, d.Gk, c.k_codes, c.k_scales);
+    const long rows = units * d.cut;
+    const long tasks = rows * (d.D / kGroup);
+    pack_v_kernel<T><<<static_cast<unsigned>((tasks + 7) / 8), 256, 0, s>>>(
+        v, rows, d.N, d.D, d.cut, c.v_codes, c.v_scales);
+    launches += 2;
+  }
+  if (d.R > 0) {
+    const long rows = units * d.R;
+    const unsigned blocks =
+        static_cast<unsigned>(std::min<long>((rows * d.D + 255) / 256, 1L << 20));
+    if (c.kwin_dtype == KVQ_MXFP8) {
+      const long tasks = rows * (d.D / kGroup);
+      window_mxfp8_kernel<T><<<static_cast<unsigned>((tasks + 7) / 8), 256, 0, s>>>(
+          k, rows, d.N, d.D, d.R, static_cast<uint8_t *>(c.k_window), c.k_window_e8m0);
+    } else if (c.kwin_dtype == KVQ_F32) {
+      window_copy_kernel<T, float><<<blocks, 256, 0, s>>>(k, rows, d.N, d.D, d.R,
+                                                          static_cast<float *>(c.k_window));
+    } else {
+      window_copy_kernel<T, __nv_bfloat16><<<blocks, 256, 0, s>>>(
+          k, rows, d.N, d.D, d.R, static_cast<__nv_bfloat16 *>(c.k_window));
+    }
+    if (c.vwin_dtype == KVQ_F32) {
+      window_copy_kernel<T, float><<<blocks, 256, 0, s>>>(v, rows, d.N, d.D, d.R,
+                                                          static_cast<float *>(c.v_window));
+    } else {
+      window_copy_kernel<T, __nv_bfloat16><<<blocks, 256, 0, s>>>(
+          v, rows, d.N, d.D, d.R, static_cast<__nv_bfloat16 *>(c.v_window));
+    }
+    launches += 2;
+  }
+  return launches;
+}
+
+}  // namespace
+
+int launch_pack(const void *k, const void *v, int in_dtype, const kvq_cache &c,
+                const KernelCtl &, cudaStream_t s) {
+  if (in_dtype == KVQ_F32)
+    return pack_typed(static_cast<const float *>(k), static_cast<const float *>(v), c, s);
+  return pack_typed(static_cast<const __nv_bfloat16 *>(k), static_cast<const __nv_bfloat16 *>(v),
+                    c, s);
+}
+
+}  // namespace kvq

@@ -1,0 +1,264 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle.
+
+kv_pack must match the oracle byte for byte; attention must match within
+relative L2 1e-5 on the fp32 path and 1e-2 on the bf16 / MXFP8 paths (the
+tolerances the workload statement fixes); region masses within 1e-4.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import kvq_oracle as O
+from quantized_sparse_kv_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+TOL_F32 = 1e-5
+TOL_BF16 = 1e-2
+TOL_MASS = 1e-4
+
+
+@pytest.fixture(scope="module")
+def kvq():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from quantized_sparse_kv_gb300 import kvq as k
+    k.load_library()
+    return k
+
+
+def to_np(t):
+    return t.detach().float().cpu().numpy()
+
+
+def oracle_pack(k, v, recent, window):
+    """Oracle packing of (B, H, N, D) float arrays: serialised bytes per array."""
+    heads = O.pack(k, v, recent, window)
+    ser = [[O.serialize_head(p) for p in row] for row in heads]
+    stack = lambda key: np.stack([np.stack([s[key] for s in row]) for row in ser])  # noqa: E731
+    return heads, {key: stack(key) for key in ("k_codes", "k_scales", "v_codes", "v_scales",
+                                                "k_window", "v_window")}
+
+
+def _bytes(t):
+    t = t.detach().cpu()
+    if t.dtype == torch.bfloat16:
+        t = t.view(torch.int16)
+    return t.numpy().view(np.uint8)
+
+
+def assert_pack_bitexact(cache, ref):
+    for key in ("k_codes", "k_scales", "v_codes", "v_scales"):
+        got = _bytes(getattr(cache, key))
+        np.testing.assert_array_equal(got.reshape(-1), ref[key].view(np.uint8).reshape(-1),
+                                      err_msg=key)
+    if cache.recent:
+        for key in ("k_window", "v_window"):
+            got = _bytes(getattr(cache, key))
+            np.testing.assert_array_equal(got.reshape(-1), ref[key].view(np.uint8).reshape(-1),
+                                          err_msg=key)
+
+
+def bf16_cuda(x):
+    return torch.from_numpy(np.ascontiguousarray(x)).cuda().to(torch.bfloat16)
+
+
+# ------------------------------------------------------------------ kv_pack
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+@pytest.mark.parametrize("n", [128, 512])
+@pytest.mark.parametrize("recent", [0, 16, 64])
+def test_pack_residual_window_bitexact(kvq, seed, n, recent):
+    q, k, v = synth.residual_window_batch(seed, n, 1 if n == 128 else 32)
+    cache = kvq.pack(torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda(), recent, "f32")
+    _, ref = oracle_pack(k, v, recent, "f32")
+    assert_pack_bitexact(cache, ref)
+    assert cache.header == [n, 32, recent, 32]
+    if n == 128:
+        assert cache.payload_bytes() == {0: 5136, 16: 8912, 64: 18960}[recent]
+
+
+@pytest.mark.parametrize("shape,recent", [((2, 2, 100, 128), 7), ((1, 3, 65, 64), 0),
+                                          ((1, 2, 33, 96), 33), ((3, 1, 31, 256), 1)])
+def test_pack_ragged_bf16_bitexact(kvq, shape, recent):
+    k = O.round_to_bf16(synth.normal_numpy(10, shape) * 3)
+    v = O.round_to_bf16(synth.normal_numpy(11, shape))
+    cache = kvq.pack(bf16_cuda(k), bf16_cuda(v), recent, "bf16")
+    _, ref = oracle_pack(k, v, recent, "bf16")
+    assert_pack_bitexact(cache, ref)
+
+
+def test_pack_edge_values_bitexact(kvq):
+    # zero groups, exact .5 quotients, a negative amax, tiny and huge groups
+    k = np.zeros((1, 1, 96, 32), np.float32)
+    k[0, 0, :32, 0] = np.arange(-16, 16) * 0.5
+    k[0, 0, 32:64, 1] = -3.5
+    k[0, 0, 40, 2] = 1e-30
+    k[0, 0, 64:, 3] = np.linspace(-1e30, 1e30, 32)
+    v = np.ascontiguousarray(np.swapaxes(k, 2, 3)[:, :, :, :32].repeat(3, axis=2))
+    cache = kvq.pack(torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda(), 0, "f32")
+    _, ref = oracle_pack(k, v, 0, "f32")
+    assert_pack_bitexact(cache, ref)
+
+
+def test_pack_mxfp8_window_bitexact(kvq):
+    shape = (1, 2, 70, 128)
+    k = O.round_to_bf16(synth.normal_numpy(12, shape) * np.logspace(-3, 3, 128, dtype=np.float32))
+    k[0, 0, 5, :32] = 0.0
+    v = O.round_to_bf16(synth.normal_numpy(13, shape))
+    cache = kvq.pack(bf16_cuda(k), bf16_cuda(v), 70, "mxfp8", "bf16")
+    codes, sb = O.mxfp8_quantize(k.astype(np.float64))
+    np.testing.assert_array_equal(cache.k_window.cpu().numpy(), codes)
+    np.testing.assert_array_equal(cache.k_window_e8m0.cpu().numpy(), sb)
+
+
+# ------------------------------------------------------------------ fp32 attention (small D)
+
+
+@pytest.mark.parametrize("variant", ["clean", "early", "recent"])
+@pytest.mark.parametrize("n,heads", [(128, 1), (512, 32)])
+@pytest.mark.parametrize("recent", [0, 16, 64])
+def test_attend_residual_window_fp32(kvq, variant, n, heads, recent):
+    for seed in range(3):
+        q, k, v = synth.residual_window_batch(seed, n, heads, variant=variant)
+        cache = kvq.pack(torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda(), recent, "f32")
+        out, _, path = kvq.attend(cache, torch.from_numpy(q).cuda(), out_dtype="f32")
+        assert path == "generic"
+        ref, _ = O.attend(q, O.pack(k, v, recent, "f32"))
+        assert O.rel_l2(to_np(out), ref) <= TOL_F32
+
+
+def test_attend_region_mass_fp32(kvq):
+    q, k, v = synth.residual_window_batch(4, 512, 4, variant="recent")
+    bounds = [0, 100, 480, 496, 512]
+    cache = kvq.pack(torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda(), 16, "f32")
+    out, mass, _ = kvq.attend(cache, torch.from_numpy(q).cuda(), out_dtype="f32",
+                              region_bounds=bounds)
+    ref, ref_mass = O.attend(q, O.pack(k, v, 16, "f32"), region_bounds=bounds)
+    assert O.rel_l2(to_np(out), ref) <= TOL_F32
+    np.testing.assert_allclose(to_np(mass), ref_mass, atol=TOL_MASS, rtol=0)
+    np.testing.assert_allclose(to_np(mass).sum(-1), 1.0, atol=1e-5)
+
+
+# ------------------------------------------------------------------ decode (int4 + bf16 window)
+
+
+def decode_case(seed, batch, n, hkv=2, d=128):
+    q = O.round_to_bf16(synth.normal_numpy(seed, (batch, 8 * hkv, 1, d)))
+    k = O.round_to_bf16(synth.normal_numpy(seed + 1, (batch, hkv, n, d)))
+    v = O.round_to_bf16(synth.normal_numpy(seed + 2, (batch, hkv, n, d)))
+    return q, k, v
+
+
+@pytest.mark.parametrize("batch,n,recent", [(1, 1024, 128), (3, 1000, 128), (2, 333, 0),
+                                            (1, 128, 128), (2, 4109, 37), (1, 40, 17)])
+def test_decode_matches_oracle(kvq, batch, n, recent):
+    q, k, v = decode_case(20 + n, batch, n)
+    tq = bf16_cuda(q)
+    cache = kvq.pack(bf16_cuda(k), bf16_cuda(v), recent, "bf16")
+    ref, _ = O.attend(q, O.pack(k, v, recent, "bf16"))
+    for out_dtype in ("f32", "bf16"):
+        a = kvq.Attend(cache, tq, out_dtype=out_dtype)
+        a.run()
+        assert a.path == "decode"
+        assert kvq.read_status(a.status) == 0
+        err = O.rel_l2(to_np(a.out), ref)
+        assert err <= TOL_BF16, err
+        per_head = [O.rel_l2(to_np(a.out)[b, h], ref[b, h]) for b in range(batch) for h in range(16)]
+        assert max(per_head) <= 3 * TOL_BF16
+
+
+def test_decode_is_deterministic(kvq):
+    q, k, v = decode_case(5, 2, 2000)
+    cache = kvq.pack(bf16_cuda(k), bf16_cuda(v), 128, "bf16")
+    a = kvq.Attend(cache, bf16_cuda(q), out_dtype="f32")
+    first = a.run().clone()
+    second = a.run().clone()
+    assert torch.equal(first, second)
+
+
+# ------------------------------------------------------------------ candidates
+
+
+@pytest.mark.parametrize("n,recent,c,sort", [(4096, 128, 96, True), (1000, 128, 256, False),
+                                             (300, 0, 64, True), (5000, 37, 8, False)])
+def test_candidates_match_oracle(kvq, n, recent, c, sort):
+    batch = 2
+    q, k, v = decode_case(40 + c, batch, n)
+    idx = synth.candidate_indices(3, batch, 16, n, c, sort=sort)
+    cache = kvq.pack(bf16_cuda(k), bf16_cuda(v), recent, "bf16")
+    out, status = kvq.attend_candidates(cache, bf16_cuda(q), torch.from_numpy(idx).cuda(),
+                                        out_dtype="f32")
+    assert kvq.read_status(status) == 0
+    ref = O.attend_candidates(q, O.pack(k, v, recent, "bf16"), idx)
+    assert O.rel_l2(to_np(out), ref) <= TOL_BF16
+
+
+def test_candidates_over_all_keys_equal_dense(kvq):
+    q, k, v = decode_case(7, 1, 700)
+    cache = kvq.pack(bf16_cuda(k), bf16_cuda(v), 64, "bf16")
+    tq = bf16_cuda(q)
+    perm = np.stack([np.random.default_rng(h).permutation(700) for h in range(16)])
+    idx = torch.from_numpy(perm.astype(np.int32)).reshape(1, 16, 1, 700).cuda()
+    out_c, _ = kvq.attend_candidates(cache, tq, idx, out_dtype="f32")
+    out_d, _, _ = kvq.attend(cache, tq, out_dtype="f32")
+    assert O.rel_l2(to_np(out_c), to_np(out_d)) <= TOL_BF16
+
+
+def test_candidates_flag_bad_and_duplicate_indices(kvq):
+    q, k, v = decode_case(8, 1, 200)
+    cache = kvq.pack(bf16_cuda(k), bf16_cuda(v), 8, "bf16")
+    tq = bf16_cuda(q)
+    idx = torch.arange(16, dtype=torch.int32).repeat(1, 16, 1, 1).cuda()
+    idx[0, 3, 0, 5] = 200                    # out of range
+    _, status = kvq.attend_candidates(cache, tq, idx)
+    assert kvq.read_status(status) & kvq.DEV_INDEX
+    idx[0, 3, 0, 5] = 4                      # duplicate of position 4
+    _, status = kvq.attend_candidates(cache, tq, idx, validate=True)
+    assert kvq.read_status(status) & kvq.DEV_DUP
+    _, status = kvq.attend_candidates(cache, tq, idx, validate=False)
+    assert kvq.read_status(status) == 0
+
+
+# ------------------------------------------------------------------ argument errors and timeouts
+
+
+def test_argument_errors_return_before_launch(kvq):
+    k = torch.zeros((1, 2, 64, 32), device="cuda")
+    with pytest.raises(kvq.KvqError) as e:
+        kvq.pack(k, k, 65, "f32")                                            # R > N
+    assert e.value.status == 1
+    cache = kvq.pack(k, k, 0, "f32")
+    with pytest.raises(kvq.KvqError) as e:
+        kvq.attend(cache, torch.zeros((1, 3, 2, 32), device="cuda"))        # 3 q-heads, 2 KV heads
+    assert e.value.status == 1
+    with pytest.raises(kvq.KvqError) as e:
+        kvq.attend(cache, torch.zeros((1, 2, 2, 32), device="cuda"), region_bounds=[0, 70, 64])
+    assert e.value.status == 1
+    with pytest.raises(ValueError):                                         # caught by the binding
+        kvq.attend(cache, torch.zeros((1, 2, 2, 64), device="cuda"))
+    base = torch.zeros(2 * 64 * 32 + 4, device="cuda")
+    with pytest.raises(kvq.KvqError) as e:
+        kvq.pack(base[1:1 + 2 * 64 * 32].view(1, 2, 64, 32), k, 0, "f32")  # 4-byte offset
+    assert e.value.status == 2
+
+
+def test_decode_wait_runs_out_and_reports_timeout(kvq):
+    # the loader skips one item, so the wait on it can only end by its limit
+    q, k, v = decode_case(9, 1, 2048)
+    cache = kvq.pack(bf16_cuda(k), bf16_cuda(v), 128, "bf16")
+    a = kvq.Attend(cache, bf16_cuda(q))
+    try:
+        kvq.debug_set(wait_limit_ns=2_000_000, drop_item=3)
+        a.run()
+        st = kvq.read_status(a.status)
+    finally:
+        kvq.debug_set(0, -1)
+    assert st & kvq.DEV_TIMEOUT
+    # the context is still usable and a normal call succeeds afterwards
+    a.status.zero_()
+    a.run()
+    assert kvq.read_status(a.status) == 0
+    ref, _ = O.attend(q, O.pack(k, v, 128, "bf16"))
+    assert O.rel_l2(to_np(a.out), ref) <= TOL_BF16
