@@ -1,0 +1,491 @@
+"""Benchmark of the compressed-KV-cache attention path on GB300.
+
+Default (``--impl kvq``): the timed step is one GQA decode attention pass over a
+packed int4 cache -- 64 sequences, 16 query heads over 2 KV heads, head dim 128,
+context 32,768 with the last 128 tokens in bf16 -- through the C ABI
+(kv_attend: split-K decode kernel + log-sum-exp combine). The metric is
+attended keys per second (sequences x query heads x context / step time).
+The other hot-path rows (packing, fp32 small-head attention, chunk attention
+with region mass in bf16 and MXFP8, candidate attention) are timed the same
+way and reported under ``rows``.
+
+``--impl reference`` times the fp64 CPU oracle on a bounded sample of the same
+decode workload on the host cores (the reference arm).
+
+Prints ONE JSON line on rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+DECODE = dict(batch=64, q_heads=16, kv_heads=2, head_dim=128, context=32768, recent=128)
+CHUNK = dict(heads=32, n_q=2340, n_kv=6240, head_dim=128, bounds=(0, 1560, 3900, 6240))
+CAND = dict(batch=32, q_heads=16, kv_heads=2, head_dim=128, context=131072, recent=128, c=256)
+SMALL = dict(heads=32, n=512, head_dim=32, n_q=16, recent=16)
+L2_BYTES = 129 * 2 ** 20
+NOMINAL_HBM_GBS = 8000.0
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+# ---------------------------------------------------------------- algorithmic bytes
+
+def decode_bytes(batch, kv_heads, context, recent, head_dim=128, q_heads=16, out_bytes=2):
+    """Bytes one decode pass must move: the packed cache once, Q in, O out."""
+    cut = context - recent
+    gk = -(-cut // 32)
+    per_unit = gk * 32 * head_dim // 2 + gk * head_dim * 4 + cut * head_dim // 2 \
+        + cut * head_dim // 32 * 4 + 2 * recent * head_dim * 2
+    return batch * kv_heads * per_unit + batch * q_heads * head_dim * (2 + out_bytes)
+
+
+def candidate_unique_bytes(idx, context, recent, head_dim=128, kv_heads=2):
+    """Bytes a candidate pass must read at least: each distinct token row and
+    each distinct K-scale group once per (sequence, KV head), plus Q and O."""
+    import numpy as np
+    b, hq, nq, c = idx.shape
+    group = hq // kv_heads
+    cut = context - recent
+    total = 0
+    for bi in range(b):
+        for h in range(kv_heads):
+            toks = np.unique(idx[bi, h * group:(h + 1) * group].reshape(-1))
+            q = toks[toks < cut]
+            w = toks.size - q.size
+            total += q.size * (head_dim // 2 * 2 + head_dim // 32 * 4)   # K, V codes + V scales
+            total += np.unique(q // 32).size * head_dim * 4                # K scale groups
+            total += w * head_dim * 2 * 2                                 # bf16 window rows
+    return total + b * hq * nq * head_dim * 4
+
+
+# ---------------------------------------------------------------- clocks sampler
+
+class ClockSampler:
+    """Samples SM clock and throttle reasons with nvidia-smi while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        self.file.flush()
+        rows = []
+        with open(self.file.name) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[5:9]))
+                except ValueError:
+                    continue
+        os.unlink(self.file.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[3]) if v == "Active"})
+        loaded = [r for r in rows if r[2] > 200.0] or rows
+        return {"sm_mhz": statistics.median(r[0] for r in loaded),
+                "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons,
+                "samples": len(rows), "samples_under_load": len(loaded)}
+
+
+# ---------------------------------------------------------------- timing helpers
+
+def time_steps(fn, steps, warmup, flush=None):
+    """Mean ms per call with CUDA events on the current stream. Without
+    ``flush`` the calls run back to back inside one event pair; with it,
+    each call is bracketed by its own events and the flush runs outside them."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    s = torch.cuda.current_stream()
+    if flush is None:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for _ in range(steps):
+            fn()
+        e1.record(s)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps
+    total = 0.0
+    for _ in range(steps):
+        flush()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        fn()
+        e1.record(s)
+        torch.cuda.synchronize()
+        total += e0.elapsed_time(e1)
+    return total / steps
+
+
+def make_flush():
+    import torch
+    buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda")
+
+    def flush():
+        buf.fill_(1.0)
+    return flush
+
+
+# ---------------------------------------------------------------- rows
+
+def row_pack(kvq, synth, torch, steps, warmup, pk):
+    d = DECODE
+    q, k, v = synth.decode_inputs_torch(11, d["batch"], d["context"], "cuda")
+    cache = kvq.pack(k, v, d["recent"], "bf16")
+    ms = time_steps(lambda: kvq.pack(k, v, d["recent"], "bf16", out=cache), steps, warmup)
+    nbytes = 2 * k.numel() * 2 + cache.payload_bytes()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    tokens = d["batch"] * d["kv_heads"] * d["context"]
+    del q, k, v, cache
+    return {"workload": "kv_pack int4 K/V, 64 x 2 KV heads x 32768 tokens x 128, bf16 in, R=128",
+            "ms": ms, "tokens_per_s": tokens / (ms * 1e-3),
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / pk["hbm_gbs"], "traffic": None},
+            "launches": 4}
+
+
+def row_small(kvq, synth, torch, steps, warmup, pk):
+    import numpy as np
+    s = SMALL
+    q, k, v = synth.residual_window_batch(0, s["n"], s["heads"])
+    cache = kvq.pack(torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda(), s["recent"], "f32")
+    a = kvq.Attend(cache, torch.from_numpy(q).cuda(), out_dtype="f32")
+    ms = time_steps(a.run, steps, warmup, flush=make_flush())
+    keys = s["heads"] * s["n_q"] * s["n"]
+    nbytes = cache.payload_bytes() + 2 * q.nbytes
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"workload": "fp32 attention, 32 heads, N=512, D=32, 16 queries, R=16 fp32",
+            "ms": ms, "keys_per_s": keys / (ms * 1e-3), "path": a.path,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / pk["hbm_gbs"], "traffic": None},
+            "launches": a.launches(), "note": "latency-bound: 0.8 MB per call"}
+
+
+def row_chunk(kvq, synth, torch, steps, warmup, pk, kwin):
+    c = CHUNK
+    q, k, v = synth.chunk_inputs_torch(21, "cuda")
+    cache = kvq.pack(k, v, c["n_kv"], kwin, "bf16")
+    a = kvq.Attend(cache, q, out_dtype="bf16", region_bounds=c["bounds"])
+    ms = time_steps(a.run, steps, warmup, flush=make_flush())
+    flops = 4.0 * c["heads"] * c["n_q"] * c["n_kv"] * c["head_dim"]
+    tf = flops / (ms * 1e-3) / 1e12
+    peak = pk["bf16_tflops"] * (2.0 if kwin == "mxfp8" else 1.0)
+    keys = c["heads"] * c["n_q"] * c["n_kv"]
+    return {"workload": f"chunk attention {kwin} Q/K, 32 heads, 2340 queries over 6240 keys "
+                        "[sink 1560 | recent 2340 | current 2340], D=128, region mass",
+            "ms": ms, "keys_per_s": keys / (ms * 1e-3), "path": a.path,
+            "roofline": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s",
+                         "frac": tf / peak, "traffic": None,
+                         "peak_note": "bf16 measured" if kwin != "mxfp8"
+                         else "2 x measured bf16 (nominal fp8/bf16 ratio)"},
+            "launches": a.launches()}
+
+
+def row_candidates(kvq, synth, torch, steps, warmup, pk, context, c):
+    d = CAND
+    q, k, v = synth.decode_inputs_torch(31, d["batch"], context, "cuda")
+    cache = kvq.pack(k, v, d["recent"], "bf16")
+    del k, v
+    idx = synth.candidate_indices(5, d["batch"], d["q_heads"], context, c)
+    a = kvq.AttendCandidates(cache, q, torch.from_numpy(idx).cuda(), out_dtype="bf16")
+    ms = time_steps(a.run, steps, warmup, flush=make_flush())
+    nbytes = candidate_unique_bytes(idx, context, d["recent"])
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    keys = d["batch"] * d["q_heads"] * c
+    return {"workload": f"candidate attention, 32 x 16 heads, L={context}, C={c}, int4 + bf16 R=128",
+            "ms": ms, "keys_per_s": keys / (ms * 1e-3),
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / pk["hbm_gbs"], "traffic": None,
+                         "bytes_note": "distinct rows and K-scale groups per (sequence, KV head)"},
+            "launches": a.launches()}
+
+
+# ---------------------------------------------------------------- oracle (CPU) arm
+
+def _oracle_unit_worker(args):
+    """Time the oracle's attend on one (sequence, KV head) of the decode workload:
+    dequantize the packed unit and attend its 8 query heads."""
+    seed, context, recent = args
+    import numpy as np
+    from oracle import kvq_oracle as O
+    from quantized_sparse_kv_gb300 import synth
+    q = O.round_to_bf16(synth.normal_numpy(seed, (8, 1, 128)))
+    k = O.round_to_bf16(synth.normal_numpy(seed + 1, (context, 128)))
+    v = O.round_to_bf16(synth.normal_numpy(seed + 2, (context, 128)))
+    packed = O.pack_head(k, v, recent, "bf16")
+    t0 = time.perf_counter()
+    kh, vh = O.dequantize_head(packed)
+    for h in range(8):
+        O.attention(q[h], kh, vh)
+    return time.perf_counter() - t0
+
+
+def oracle_pool(workers):
+    import multiprocessing as mp
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[var] = "1"
+    return mp.get_context("spawn").Pool(workers)
+
+
+def oracle_sample(pool, units, workers, seed0=1000):
+    d = DECODE
+    t0 = time.perf_counter()
+    busy = pool.map(_oracle_unit_worker,
+                    [(seed0 + 3 * i, d["context"], d["recent"]) for i in range(units)])
+    wall = time.perf_counter() - t0
+    keys = units * 8 * d["context"]
+    cpu_s = sum(busy)
+    # each worker is one core; input generation and packing are not timed
+    return {"keys": keys, "wall_s": wall, "cpu_s": cpu_s, "keys_per_s": keys * workers / cpu_s}
+
+
+def cpu_workers():
+    try:
+        n = len(os.sched_getaffinity(0))
+    except AttributeError:
+        n = os.cpu_count() or 1
+    return max(1, min(16, n))
+
+
+# ---------------------------------------------------------------- main arms
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("gloo")
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_reference(args):
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return
+    workers = cpu_workers()
+    pool = oracle_pool(workers)
+    units = 2 * workers
+    for _ in range(args.warmup):
+        oracle_sample(pool, workers, workers)
+    res = [oracle_sample(pool, units, workers, seed0=2000 + 97 * i) for i in range(args.steps)]
+    pool.close()
+    keys = sum(r["keys"] for r in res)
+    busy = sum(r["cpu_s"] for r in res) / workers   # timed oracle seconds per core
+    wall = busy
+    value = keys / busy
+    d = DECODE
+    sample = (f"{units} of the 128 (sequence, KV head) units per step: oracle dequantize + "
+              f"fp64 attention of their 8 query heads over L={d['context']}")
+    line = {"metric": "attended keys/s (GQA decode over int4 KV cache)", "value": value,
+            "unit": "keys/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * wall / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic N(0,1), bf16-rounded",
+            "impl": "reference",
+            "config": {"workload": "decode B=64 Hq=16 Hkv=2 D=128 L=32768 R=128 (sampled units)"},
+            "cpu_baseline": {"value": value, "unit": "keys/s", "cores": workers, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "keys/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def run_kvq(args):
+    world, rank, local = dist_setup()
+    import numpy as np
+    import torch
+
+    from quantized_sparse_kv_gb300 import kvq, synth
+    kvq.load_library()
+    torch.cuda.set_device(local)
+    pk = peaks()
+    d = dict(DECODE)
+    if args.case == "small":
+        d["batch"] = 16   # 169 MB per step: still larger than L2, small enough for ncu sections
+
+    # CPU oracle baseline first (spawned before heavy GPU work), rank 0 only
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        workers = cpu_workers()
+        pool = oracle_pool(workers)
+        s = oracle_sample(pool, 8 * workers, workers)
+        pool.close()
+        cpu = {"value": s["keys_per_s"], "unit": "keys/s", "cores": workers, "kind": "oracle",
+               "sample": f"{8 * workers} (sequence, KV head) units of the decode workload "
+                         f"(8 query heads x L={d['context']} each), oracle dequantize + fp64 "
+                         f"attention, {s['cpu_s']:.1f} s of CPU work"}
+
+    q, k, v = synth.decode_inputs_torch(1 + rank, d["batch"], d["context"], "cuda")
+    cache = kvq.pack(k, v, d["recent"], "bf16")
+    del k, v
+    torch.cuda.synchronize()
+    att = kvq.Attend(cache, q, out_dtype="bf16")
+    att.run()
+    assert att.path == "decode", att.path
+    launches_per_step = att.launches()
+    nbytes = decode_bytes(d["batch"], d["kv_heads"], d["context"], d["recent"])
+
+    for _ in range(max(3, args.warmup)):
+        att.run()
+    torch.cuda.synchronize()
+    barrier(world)
+    s = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        torch.cuda.synchronize()
+        barrier(world)
+        e0.record(s)
+        for _ in range(args.steps):
+            att.run()
+        e1.record(s)
+        torch.cuda.synchronize()
+        barrier(world)
+        # keep the GPU busy a little longer so the sampler sees the loaded clock
+        for _ in range(args.steps):
+            att.run()
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    ms_max = max_over_ranks(ms, world)
+    clocks = clk.summary()
+    keys_per_step = d["batch"] * d["q_heads"] * d["context"]
+    value = world * keys_per_step / (ms_max * 1e-3)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+
+    # end to end through the same C call with host buffers: q from pinned host
+    # memory in, O back to pinned host memory, every step
+    q_host = q.cpu().pin_memory()
+    o_host = torch.empty(att.out.shape, dtype=att.out.dtype).pin_memory()
+
+    def e2e_step():
+        att.q.copy_(q_host, non_blocking=True)
+        att.run()
+        o_host.copy_(att.out, non_blocking=True)
+    e2e_ms = time_steps(e2e_step, args.steps, 3)
+    e2e = {"value": world * keys_per_step / (max_over_ranks(e2e_ms, world) * 1e-3),
+           "unit": "keys/s", "h2d_bytes_per_step": q_host.numel() * q_host.element_size(),
+           "d2h_bytes_per_step": o_host.numel() * o_host.element_size(),
+           "note": "KV cache resident in HBM; per step the query rows go in and the outputs come out"}
+
+    rows = {}
+    if rank == 0 and not args.no_rows:
+        rsteps = max(3, min(args.steps, 10))
+        rows["pack"] = row_pack(kvq, synth, torch, rsteps, 2, pk)
+        rows["small_d_fp32"] = row_small(kvq, synth, torch, rsteps, 2, pk)
+        rows["candidates_L131072_C256"] = row_candidates(kvq, synth, torch, rsteps, 2, pk, 131072, 256)
+        rows["candidates_L32768_C96"] = row_candidates(kvq, synth, torch, rsteps, 2, pk, 32768, 96)
+        rows["chunk_bf16"] = row_chunk(kvq, synth, torch, 3, 1, pk, "bf16")
+        rows["chunk_mxfp8"] = row_chunk(kvq, synth, torch, 3, 1, pk, "mxfp8")
+
+    if rank != 0:
+        return
+    line = {
+        "metric": "attended keys/s (GQA decode over int4 KV cache)",
+        "value": value, "unit": "keys/s", "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": ms_max, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int4 KV, bf16 Q/window, f16/f32 MMA",
+        "data": "synthetic N(0,1) bf16 Q/K/V, seeded",
+        "config": {"workload": f"decode: B={d['batch']} sequences, 16 query heads over 2 KV heads, "
+                               "D=128, L=32768, last R=128 tokens bf16, int4 groups of 32",
+                   "batch": d["batch"], "context": d["context"], "recent": d["recent"],
+                   "l2": f"inputs larger than L2 ({nbytes / 1e6:.0f} MB per step), no flush",
+                   "parallelism": f"replicas x{world}, each its own batch"},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": gbs / pk["hbm_gbs"], "traffic": None,
+                     "kernel": "decode_kernel + combine_kernel (one kv_attend call)",
+                     "algorithmic_bytes": nbytes, "peak_source": pk["source"],
+                     "frac_of_nominal_8tbs": gbs / NOMINAL_HBM_GBS},
+        "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
+        "gpu_launches": launches_per_step * args.steps,
+        "rows": rows,
+    }
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["kvq", "reference"], default="kvq")
+    ap.add_argument("--no-rows", action="store_true", help="time only the decode step")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--case", choices=["full", "small"], default="full",
+                    help="small: 16 sequences instead of 64 (for profiler captures)")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_kvq(args)
+
+
+if __name__ == "__main__":
+    main()
