@@ -167,6 +167,35 @@ KVQ_API kvq_status kv_attend_candidates(const kvq_cache *cache, const void *q, i
                                         size_t *ws_bytes, int32_t *dev_status,
                                         kvq_stream_t stream);
 
+/*
+ * kv_attend_decode_static -- the decode case of kv_attend (one query row per
+ * sequence and head, 8 query heads per KV head, D = 128, bf16 or no window)
+ * for callers that cannot allocate device memory: a serving runtime that has
+ * already handed all free HBM to its KV-cache pool (any further cudaMalloc
+ * fails), or a latency-critical caller that cannot afford cudaMalloc's
+ * implicit device synchronisation. The pages have no counterpart; it exists
+ * only for those callers.
+ * Same q / out / dtype / dev_status / stream rules as kv_attend; no
+ * workspace argument. The split-K partials go to a scratch array of
+ * KVQ_DECODE_STATIC_SCRATCH_BYTES (8 MiB) that the library keeps in device
+ * memory on every GPU that loads it, until the process exits. A call whose
+ * partials need more (roughly batch * kv_heads above about 1,300 on a
+ * 152-SM GPU) returns KVQ_ERR_WORKSPACE and enqueues nothing; other
+ * unsupported shapes return KVQ_ERR_UNSUPPORTED. Nothing is allocated, by
+ * the library or by any library it calls.
+ * The first call on a device looks up the scratch array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture. Every call reads scratch it wrote itself in the
+ * same call, so nothing needs clearing between calls, but all calls share
+ * the one array: calls that overlap on the GPU (different streams, no
+ * ordering between them) race and corrupt each other's results.
+ */
+#define KVQ_DECODE_STATIC_SCRATCH_BYTES (8u << 20)
+KVQ_API kvq_status kv_attend_decode_static(const kvq_cache *cache, const void *q,
+                                           int32_t q_dtype, int32_t q_heads, float sm_scale,
+                                           void *out, int32_t out_dtype, int32_t *dev_status,
+                                           kvq_stream_t stream);
+
 /* Number of kernel launches the last successful call on this thread enqueued. */
 KVQ_API int32_t kvq_last_launch_count(void);
 

@@ -32,6 +32,7 @@
 #include <math_constants.h>
 
 #include <algorithm>
+#include <mutex>
 
 #include "kvq_internal.h"
 
@@ -617,6 +618,37 @@ int launch_attend_decode(const kvq_cache &c, const void *q, int q_dtype, float s
     combine_kernel<__nv_bfloat16><<<units, kHeads * 32, 0, s>>>(
         a, static_cast<__nv_bfloat16 *>(out));
   return 2;
+}
+
+// ------------------------------------------------------------------ library-owned scratch
+// Scratch of kv_attend_decode_static: the split-K partials live in this
+// file-scope device array instead of a caller-provided workspace. Every GPU
+// that loads this module keeps the array until the process exits.
+namespace {
+constexpr size_t kStaticScratchBytes = size_t(8) << 20;  // 8 MiB
+static __device__ __align__(256) unsigned char g_decode_scratch[kStaticScratchBytes];
+std::mutex g_scratch_mu;
+void *g_scratch_addr[64] = {};
+}  // namespace
+
+size_t decode_static_scratch_limit() { return kStaticScratchBytes; }
+
+// In host code `g_decode_scratch` is only a host-side stand-in; the kernel
+// needs its device address, resolved once per device with that device current.
+cudaError_t decode_static_scratch(void **ptr) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_addr[dev]) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_decode_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_addr[dev] = p;
+  }
+  *ptr = g_scratch_addr[dev];
+  return cudaSuccess;
 }
 
 }  // namespace kvq

@@ -224,6 +224,31 @@ kvq_status kv_attend_candidates(const kvq_cache *cache, const void *q, int32_t q
   return finish(n, "candidates");
 }
 
+kvq_status kv_attend_decode_static(const kvq_cache *cache, const void *q, int32_t q_dtype,
+                                   int32_t q_heads, float sm_scale, void *out,
+                                   int32_t out_dtype, int32_t *dev_status, kvq_stream_t stream) {
+  kvq_status st = check_cache(cache);
+  if (st != KVQ_OK) return st;
+  if (q_heads < 1 || q_heads % cache->kv_heads) return KVQ_ERR_ARG;
+  if ((q_dtype != KVQ_F32 && q_dtype != KVQ_BF16) ||
+      (out_dtype != KVQ_F32 && out_dtype != KVQ_BF16))
+    return KVQ_ERR_ARG;
+  if (!kvq::decode_supported(*cache, q_dtype, q_heads, 1)) return KVQ_ERR_UNSUPPORTED;
+  if (!q || !out) return KVQ_ERR_ARG;
+  if (!aligned16(q) || !aligned16(out) || (dev_status && !aligned16(dev_status)))
+    return KVQ_ERR_ALIGN;
+  const int sms = sm_count();
+  if (kvq::decode_workspace_bytes(*cache, q_heads, sms) > kvq::decode_static_scratch_limit())
+    return KVQ_ERR_WORKSPACE;
+  void *scratch = nullptr;
+  if (kvq::decode_static_scratch(&scratch) != cudaSuccess) return KVQ_ERR_CUDA;
+  const float scale = resolve_scale(sm_scale, cache->head_dim);
+  const int n = kvq::launch_attend_decode(*cache, q, q_dtype, static_cast<float>(scale * kLog2e),
+                                          out, out_dtype, scratch, make_ctl(dev_status), sms,
+                                          reinterpret_cast<cudaStream_t>(stream));
+  return finish(n, "decode_static");
+}
+
 int32_t kvq_last_launch_count(void) { return g_last_launches; }
 
 const char *kvq_last_path(void) { return g_last_path; }

@@ -58,6 +58,11 @@ int launch_attend_decode(const kvq_cache &c, const void *q, int q_dtype, float s
                          void *out, int out_dtype, void *ws, const KernelCtl &ctl, int num_sms,
                          cudaStream_t s);
 
+// attend_decode.cu: the same decode kernels with the partials in a static
+// device array (kv_attend_decode_static).
+size_t decode_static_scratch_limit();
+cudaError_t decode_static_scratch(void **ptr);
+
 // attend_candidates.cu
 int launch_attend_candidates(const kvq_cache &c, const void *q, int q_dtype, int Hq, int n_q,
                              const int32_t *idx, int n_cand, int validate, float scale_log2,
