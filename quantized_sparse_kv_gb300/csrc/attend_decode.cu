@@ -6,24 +6,25 @@
 // read from the bf16 window of the last R tokens; no mask.
 //
 // Work split. The cache of one (sequence, KV head) -- a "unit" -- is a list
-// of items: its int4 groups (32 tokens: 2 KB K codes, 512 B K scales, 2 KB V
-// codes, 512 B V scales) followed by its window tiles (16 tokens of bf16 K and
-// V). All items of all units are laid end to end and the persistent grid
-// (2 CTAs per SM) takes equal contiguous slices, so every SM streams the same
-// number of bytes. A CTA emits one partial (running max m, sum l, unnormalised
-// O for 8 heads) per unit its slice touches; combine_kernel merges them with
-// the log-sum-exp rule.
+// of items: its int4 groups taken four at a time (128 tokens: 8 KB K codes,
+// 2 KB K scales, 8 KB V codes, 2 KB V scales, one bulk copy each) followed by
+// its window tiles (40 tokens of bf16 K and V). All items of all units are
+// laid end to end and the persistent grid (3 CTAs per SM) takes equal
+// contiguous slices, so every SM streams the same number of bytes. A CTA
+// emits one partial (running max m, sum l, unnormalised O for 8 heads) per
+// unit its slice touches; combine_kernel merges them with the log-sum-exp rule.
 //
-// Inside a CTA. Warp 4 is the loader: one lane issues cp.async.bulk copies of
-// each item into an 8-stage shared-memory ring, completing on mbarriers.
-// Warps 0-3 take the items round robin. Scores use mma.sync m16n8k16 with the
-// 16 tokens of a tile as M and the 8 query heads as N: the K scales of a group
-// are folded into q (q' = q * s_k * sm_scale * log2 e, fp16), the nibbles are
-// turned into fp16 codes with two bit masks and one subtraction, so the MMA sees
-// codes in [-7, 7] exactly. P (fp16) is transposed in registers with movmatrix
-// and multiplies V^T (features as M) whose codes are scaled by the token's V
-// scale in fp16. The bf16 window uses bf16 MMAs with q and P split into
-// hi + lo bf16 parts. Softmax runs in the log2 domain with fp32 state.
+// Inside a CTA. Warp 4 is the loader: one lane issues the copies of each item
+// into a 3-stage shared-memory ring, completing on mbarriers. Consumer warp w
+// takes group w of every item (window rows 10w..10w+9). Scores use mma.sync
+// m16n8k16 with the 16 tokens of a tile as M and the 8 query heads as N: the
+// K scales of a group are folded into q (q' = q * sm_scale * log2 e * s_k,
+// fp16), the nibbles are turned into fp16 codes with two bit masks and one
+// subtraction, so the MMA sees codes in [-7, 7] exactly. P (fp16) is
+// transposed in registers with movmatrix and multiplies V^T (features as M)
+// whose codes are scaled by the token's V scale in fp16. The bf16 window uses
+// bf16 MMAs with q and P split into hi + lo bf16 parts. Softmax runs in the
+// log2 domain with fp32 state.
 //
 // Feature order. Within a thread, features are visited in a fixed permutation
 // (the one that makes a 16-byte row slice of nibbles a ready MMA operand); the
@@ -43,12 +44,24 @@ constexpr int kD = 128;
 constexpr int kHeads = 8;              // query heads per KV head
 constexpr int kConsumers = 4;          // consumer warps
 constexpr int kThreads = (kConsumers + 1) * 32;
-constexpr int kStages = 8;
-constexpr int kStageBytes = 8192;
-constexpr int kWinTile = 16;           // window tokens per item
+#ifndef KVQ_DECODE_CTAS_PER_SM
+#define KVQ_DECODE_CTAS_PER_SM 3
+#endif
+#ifndef KVQ_DECODE_STAGES
+#define KVQ_DECODE_STAGES 3
+#endif
+constexpr int kStages = KVQ_DECODE_STAGES;          // ring depth per CTA
+constexpr int kCtasPerSm = KVQ_DECODE_CTAS_PER_SM;  // resident CTAs per SM
+constexpr int kGroupsPerItem = kConsumers;          // one K group per consumer warp
+constexpr int kWinTile = 10;                        // window tokens per consumer warp
+constexpr int kWinItem = kWinTile * kConsumers;     // window tokens per item
 constexpr int kPartFloats = kD + 4;    // O[128], m, l per head, padded to 16 bytes
-// int4 item layout inside a stage
-constexpr int kOffKScale = 2048, kOffVCode = 2560, kOffVScale = 4608;
+// int4 item (4 K groups = 128 tokens): K codes [4][2048], K scales [4][512],
+// V codes [128][64], V scales [128][16]
+constexpr int kOffKScale = 8192, kOffVCode = 10240, kOffVScale = 18432;
+constexpr int kStageBytes = 20480;
+// window item (40 tokens): K rows [40][256 B] at 0, V rows at kOffVWin
+constexpr int kOffVWin = 10240;
 
 struct DecodeArgs {
   const uint8_t *k_codes;
@@ -59,8 +72,9 @@ struct DecodeArgs {
   const uint16_t *v_window;
   const void *q;
   int q_dtype;
-  int Hkv, N, R, cut, Gk, Wt, ipu;  // ipu: items per unit = Gk + Wt
-  long total_items;
+  int Hkv, N, R, cut, Gk, Wt, ipu;  // ipu: items per unit = ceil(Gk / 4) + Wt
+  int Gi;                           // int4 items per unit = ceil(Gk / 4)
+  int total_items;
   int num_ctas, max_units;
   float scale_log2;
   float *partials;                  // [num_ctas][max_units][8][132]
@@ -182,46 +196,45 @@ __device__ __forceinline__ void softmax_update(WarpState &st, float (&s)[NT][4])
 
 // ------------------------------------------------------------------ item bodies
 // int4 group: 32 tokens (two m-tiles), `valid` of them real.
-__device__ __forceinline__ void do_int4_item(WarpState &st, const uint8_t *stage,
-                                             const float (&qr)[32], int valid, int g, int t) {
-  const float *ks = reinterpret_cast<const float *>(stage + kOffKScale);
-  // q' fragments for this group (features 32t .. 32t+31 of head g)
+// q of this thread: head g, features 32t + 8i + j, held as fp16 pairs
+// qh[i][j] = (q[8i + j], q[8i + 4 + j]) in the MMA's feature order.
+__device__ __forceinline__ void do_int4_item(WarpState &st, const uint8_t *kc, const float *ks,
+                                             const uint8_t *vc, const float *vs,
+                                             const uint32_t (&qh)[4][4], int valid, int g, int t) {
+  // q' = q * (K scale of the channel) for this group, as fp16 B fragments
   uint32_t bq[8][2];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const float4 s0 = *reinterpret_cast<const float4 *>(ks + 32 * t + 8 * i);
     const float4 s1 = *reinterpret_cast<const float4 *>(ks + 32 * t + 8 * i + 4);
-    const float x0 = qr[8 * i + 0] * s0.x, x1 = qr[8 * i + 1] * s0.y, x2 = qr[8 * i + 2] * s0.z,
-                x3 = qr[8 * i + 3] * s0.w, x4 = qr[8 * i + 4] * s1.x, x5 = qr[8 * i + 5] * s1.y,
-                x6 = qr[8 * i + 6] * s1.z, x7 = qr[8 * i + 7] * s1.w;
-    bq[2 * i][0] = pack_h2(x0, x4);
-    bq[2 * i][1] = pack_h2(x1, x5);
-    bq[2 * i + 1][0] = pack_h2(x2, x6);
-    bq[2 * i + 1][1] = pack_h2(x3, x7);
+    bq[2 * i][0] = as_u32(__hmul2(as_h2(qh[i][0]), __floats2half2_rn(s0.x, s1.x)));
+    bq[2 * i][1] = as_u32(__hmul2(as_h2(qh[i][1]), __floats2half2_rn(s0.y, s1.y)));
+    bq[2 * i + 1][0] = as_u32(__hmul2(as_h2(qh[i][2]), __floats2half2_rn(s0.z, s1.z)));
+    bq[2 * i + 1][1] = as_u32(__hmul2(as_h2(qh[i][3]), __floats2half2_rn(s0.w, s1.w)));
   }
   float s[2][4];
 #pragma unroll
   for (int mt = 0; mt < 2; ++mt) {
     const int r0 = 16 * mt + g;
-    const uint4 ka = *reinterpret_cast<const uint4 *>(stage + r0 * 64 + 16 * t);
-    const uint4 kb = *reinterpret_cast<const uint4 *>(stage + (r0 + 8) * 64 + 16 * t);
+    const uint4 ka = *reinterpret_cast<const uint4 *>(kc + r0 * 64 + 16 * t);
+    const uint4 kb = *reinterpret_cast<const uint4 *>(kc + (r0 + 8) * 64 + 16 * t);
     const uint32_t wa[4] = {ka.x, ka.y, ka.z, ka.w}, wb[4] = {kb.x, kb.y, kb.z, kb.w};
-    s[mt][0] = s[mt][1] = s[mt][2] = s[mt][3] = 0.0f;
+    float e[4] = {0.0f, 0.0f, 0.0f, 0.0f}, o[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // two MMA chains
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      mma_f16(s[mt], dq_lo(wa[i]), dq_lo(wb[i]), dq_hi(wa[i]), dq_hi(wb[i]), bq[2 * i][0],
+      mma_f16(e, dq_lo(wa[i]), dq_lo(wb[i]), dq_hi(wa[i]), dq_hi(wb[i]), bq[2 * i][0],
               bq[2 * i][1]);
       const uint32_t a8 = wa[i] >> 8, b8 = wb[i] >> 8;
-      mma_f16(s[mt], dq_lo(a8), dq_lo(b8), dq_hi(a8), dq_hi(b8), bq[2 * i + 1][0],
+      mma_f16(o, dq_lo(a8), dq_lo(b8), dq_hi(a8), dq_hi(b8), bq[2 * i + 1][0],
               bq[2 * i + 1][1]);
     }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) s[mt][j] = e[j] + o[j];
     if (r0 >= valid) s[mt][0] = s[mt][1] = -CUDART_INF_F;
     if (r0 + 8 >= valid) s[mt][2] = s[mt][3] = -CUDART_INF_F;
   }
   softmax_update<2>(st, s);
 
-  const uint8_t *vc = stage + kOffVCode;
-  const float *vs = reinterpret_cast<const float *>(stage + kOffVScale);
   const uint2 zero8 = make_uint2(0x88888888u, 0x88888888u);  // code 0 everywhere
 #pragma unroll
   for (int mt = 0; mt < 2; ++mt) {
@@ -238,36 +251,36 @@ __device__ __forceinline__ void do_int4_item(WarpState &st, const uint8_t *stage
     const float sc = vcv ? vs[(ta + 8) * 4 + (g >> 1)] : 0.0f;
     const float sd = vd ? vs[(ta + 9) * 4 + (g >> 1)] : 0.0f;
     const __half2 sab = __floats2half2_rn(sa, sb), scd = __floats2half2_rn(sc, sd);
-    // feature f of this thread's 16 (16g + f): pairs (ta, ta+1) and (ta+8, ta+9)
-    uint32_t pab[16], pcd[16];
-    const uint32_t wab[2][2] = {{prmt(za.x, zb.x, 0x5410), prmt(za.x, zb.x, 0x7632)},
-                                {prmt(za.y, zb.y, 0x5410), prmt(za.y, zb.y, 0x7632)}};
-    const uint32_t wcd[2][2] = {{prmt(zc.x, zd.x, 0x5410), prmt(zc.x, zd.x, 0x7632)},
-                                {prmt(zc.y, zd.y, 0x5410), prmt(zc.y, zd.y, 0x7632)}};
+    // Feature 16g + f of the token pair (ta, ta+1) comes from byte-permuted
+    // words: f = 8w + 4h + j, w = which 8-byte word, h = low/high 2 bytes,
+    // j = nibble position. M-tile f (f < 8) takes features 16g + f (row g)
+    // and 16g + 8 + f (row g+8), so the A operands of one m-tile are built
+    // right before its MMA.
 #pragma unroll
-    for (int w = 0; w < 2; ++w)
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t sel = h ? 0x7632u : 0x5410u;
+      const uint32_t xab0 = prmt(za.x, zb.x, sel), xab1 = prmt(za.y, zb.y, sel);
+      const uint32_t xcd0 = prmt(zc.x, zd.x, sel), xcd1 = prmt(zc.y, zd.y, sel);
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int f = 8 * w + 4 * h;
-        pab[f + 0] = as_u32(__hmul2(as_h2(dq_lo(wab[w][h])), sab));
-        pab[f + 1] = as_u32(__hmul2(as_h2(dq_hi(wab[w][h])), sab));
-        pab[f + 2] = as_u32(__hmul2(as_h2(dq_lo(wab[w][h] >> 8)), sab));
-        pab[f + 3] = as_u32(__hmul2(as_h2(dq_hi(wab[w][h] >> 8)), sab));
-        pcd[f + 0] = as_u32(__hmul2(as_h2(dq_lo(wcd[w][h])), scd));
-        pcd[f + 1] = as_u32(__hmul2(as_h2(dq_hi(wcd[w][h])), scd));
-        pcd[f + 2] = as_u32(__hmul2(as_h2(dq_lo(wcd[w][h] >> 8)), scd));
-        pcd[f + 3] = as_u32(__hmul2(as_h2(dq_hi(wcd[w][h] >> 8)), scd));
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t a0 = j < 2 ? xab0 : xab0 >> 8, a1 = j < 2 ? xab1 : xab1 >> 8;
+        const uint32_t c0 = j < 2 ? xcd0 : xcd0 >> 8, c1 = j < 2 ? xcd1 : xcd1 >> 8;
+        const bool hi_nib = j & 1;
+        const uint32_t r0 = as_u32(__hmul2(as_h2(hi_nib ? dq_hi(a0) : dq_lo(a0)), sab));
+        const uint32_t r1 = as_u32(__hmul2(as_h2(hi_nib ? dq_hi(a1) : dq_lo(a1)), sab));
+        const uint32_t r2 = as_u32(__hmul2(as_h2(hi_nib ? dq_hi(c0) : dq_lo(c0)), scd));
+        const uint32_t r3 = as_u32(__hmul2(as_h2(hi_nib ? dq_hi(c1) : dq_lo(c1)), scd));
+        mma_f16(st.o[4 * h + j], r0, r1, r2, r3, b0, b1);
       }
-#pragma unroll
-    for (int f = 0; f < 8; ++f) mma_f16(st.o[f], pab[f], pab[8 + f], pcd[f], pcd[8 + f], b0, b1);
+    }
   }
 }
 
 // bf16 window tile: 16 tokens, `valid` of them real.
-__device__ __forceinline__ void do_window_item(WarpState &st, const uint8_t *stage,
-                                               const float (&qr)[32], int valid, int g, int t) {
-  const uint32_t *kw = reinterpret_cast<const uint32_t *>(stage);         // [16][64] words
-  const uint32_t *vw = reinterpret_cast<const uint32_t *>(stage + 4096);  // [16][64] words
+__device__ __forceinline__ void do_window_item(WarpState &st, const uint32_t *kw,
+                                               const uint32_t *vw, const uint32_t (&qh)[4][4],
+                                               int valid, int g, int t) {
+  // kw, vw: this warp's token rows, 64 words (128 bf16) each; rows >= valid unread
   float s[1][4] = {{0.0f, 0.0f, 0.0f, 0.0f}};
   const bool ra = g < valid, rb = g + 8 < valid;
 #pragma unroll
@@ -277,8 +290,10 @@ __device__ __forceinline__ void do_window_item(WarpState &st, const uint8_t *sta
                        : make_uint4(0, 0, 0, 0);
     const uint4 b = rb ? *reinterpret_cast<const uint4 *>(kw + (g + 8) * 64 + 16 * t + 4 * i)
                        : make_uint4(0, 0, 0, 0);
-    const float q0 = qr[8 * i + 0], q1 = qr[8 * i + 1], q2 = qr[8 * i + 2], q3 = qr[8 * i + 3];
-    const float q4 = qr[8 * i + 4], q5 = qr[8 * i + 5], q6 = qr[8 * i + 6], q7 = qr[8 * i + 7];
+    const float2 f04 = __half22float2(as_h2(qh[i][0])), f15 = __half22float2(as_h2(qh[i][1]));
+    const float2 f26 = __half22float2(as_h2(qh[i][2])), f37 = __half22float2(as_h2(qh[i][3]));
+    const float q0 = f04.x, q4 = f04.y, q1 = f15.x, q5 = f15.y;
+    const float q2 = f26.x, q6 = f26.y, q3 = f37.x, q7 = f37.y;
     const uint32_t h04 = pack_bf2(q0, q4), h15 = pack_bf2(q1, q5);
     const uint32_t h26 = pack_bf2(q2, q6), h37 = pack_bf2(q3, q7);
     const uint32_t l04 = pack_bf2(q0 - bf_lo(h04), q4 - bf_hi(h04));
@@ -305,39 +320,32 @@ __device__ __forceinline__ void do_window_item(WarpState &st, const uint8_t *sta
   const uint32_t bh0 = movmatrix_t(xh0), bh1 = movmatrix_t(xh1);
   const uint32_t bl0 = movmatrix_t(xl0), bl1 = movmatrix_t(xl1);
   const int ta = 2 * t;
-  uint32_t zab[16], zcd[16];  // feature 16g + f, token pairs (ta, ta+1) and (ta+8, ta+9)
+  // Word j of a token row slice holds features 16g + 2j, 2j+1. M-tiles 2j and
+  // 2j+1 need words j (rows g) and 4 + j (rows g+8) of the tokens ta, ta+1,
+  // ta+8, ta+9; invalid tokens read as zero.
+  const bool v0 = ta < valid, v1 = ta + 1 < valid, v2 = ta + 8 < valid, v3 = ta + 9 < valid;
+  const uint32_t *r0 = vw + ta * 64 + 8 * g, *r1 = r0 + 64, *r2 = r0 + 8 * 64, *r3 = r0 + 9 * 64;
 #pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    const int tk = ta + 8 * half;
-    const bool v0 = tk < valid, v1 = tk + 1 < valid;
-    uint32_t w0[8], w1[8];
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t a_lo = v0 ? r0[j] : 0u, b_lo = v1 ? r1[j] : 0u;
+    const uint32_t a_hi = v0 ? r0[4 + j] : 0u, b_hi = v1 ? r1[4 + j] : 0u;
+    const uint32_t c_lo = v2 ? r2[j] : 0u, d_lo = v3 ? r3[j] : 0u;
+    const uint32_t c_hi = v2 ? r2[4 + j] : 0u, d_hi = v3 ? r3[4 + j] : 0u;
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const uint4 x = v0 ? *reinterpret_cast<const uint4 *>(vw + tk * 64 + 8 * g + 4 * j)
-                         : make_uint4(0, 0, 0, 0);
-      const uint4 y = v1 ? *reinterpret_cast<const uint4 *>(vw + (tk + 1) * 64 + 8 * g + 4 * j)
-                         : make_uint4(0, 0, 0, 0);
-      w0[4 * j + 0] = x.x; w0[4 * j + 1] = x.y; w0[4 * j + 2] = x.z; w0[4 * j + 3] = x.w;
-      w1[4 * j + 0] = y.x; w1[4 * j + 1] = y.y; w1[4 * j + 2] = y.z; w1[4 * j + 3] = y.w;
+    for (int e = 0; e < 2; ++e) {
+      const uint32_t sel = e ? 0x7632u : 0x5410u;
+      const uint32_t x0 = prmt(a_lo, b_lo, sel), x1 = prmt(a_hi, b_hi, sel);
+      const uint32_t x2 = prmt(c_lo, d_lo, sel), x3 = prmt(c_hi, d_hi, sel);
+      mma_bf16(st.o[2 * j + e], x0, x1, x2, x3, bh0, bh1);
+      mma_bf16(st.o[2 * j + e], x0, x1, x2, x3, bl0, bl1);
     }
-    uint32_t *z = half ? zcd : zab;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      z[2 * j] = prmt(w0[j], w1[j], 0x5410);
-      z[2 * j + 1] = prmt(w0[j], w1[j], 0x7632);
-    }
-  }
-#pragma unroll
-  for (int f = 0; f < 8; ++f) {
-    mma_bf16(st.o[f], zab[f], zab[8 + f], zcd[f], zcd[8 + f], bh0, bh1);
-    mma_bf16(st.o[f], zab[f], zab[8 + f], zcd[f], zcd[8 + f], bl0, bl1);
   }
 }
 
 // ------------------------------------------------------------------ the kernel
 struct __align__(16) DecodeSmem {
   uint8_t stage[kStages][kStageBytes];
-  float red_o[kConsumers][kHeads][kD];
+  float red_o[kConsumers][kHeads / 2][kD];  // one half of the heads at a time
   float red_m[kConsumers][kHeads];
   float red_l[kConsumers][kHeads];
   uint64_t full[kStages];
@@ -345,9 +353,10 @@ struct __align__(16) DecodeSmem {
   int abort_flag;
 };
 
-__device__ __forceinline__ void load_q(const DecodeArgs &a, long u, int g, int t,
-                                       float (&qr)[32]) {
-  const long row = u * kHeads + g;  // (b * Hkv + kvh) * 8 + g: query head kvh * 8 + g
+__device__ __forceinline__ void load_q(const DecodeArgs &a, int u, int g, int t,
+                                       uint32_t (&qh)[4][4]) {
+  const long row = static_cast<long>(u) * kHeads + g;  // query head kvh * 8 + g of sequence b
+  float qr[32];
   if (a.q_dtype == KVQ_F32) {
     const float *q = static_cast<const float *>(a.q) + row * kD + 32 * t;
 #pragma unroll
@@ -357,26 +366,57 @@ __device__ __forceinline__ void load_q(const DecodeArgs &a, long u, int g, int t
 #pragma unroll
     for (int i = 0; i < 32; ++i) qr[i] = bf16_to_f32(q[i]) * a.scale_log2;
   }
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) qh[i][j] = pack_h2(qr[8 * i + j], qr[8 * i + 4 + j]);
 }
 
 __device__ __forceinline__ bool aborted_flag(DecodeSmem &sm) {
   return *reinterpret_cast<volatile int *>(&sm.abort_flag) != 0;
 }
 
-__global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a) {
+// Issue the copies of item `item` (unit u, index j within the unit) into a stage.
+__device__ __forceinline__ void load_item(const DecodeArgs &a, int u, int j, uint32_t dst,
+                                          uint32_t bar) {
+  if (j < a.Gi) {
+    const int g0 = kGroupsPerItem * j;
+    const int ng = min(kGroupsPerItem, a.Gk - g0);
+    const int t0 = 32 * g0;
+    const int nt = min(32 * kGroupsPerItem, a.cut - t0);
+    const long gi = static_cast<long>(u) * a.Gk + g0;
+    const long ti = static_cast<long>(u) * a.cut + t0;
+    const uint32_t kb = 2048u * ng, sb = 512u * ng, vb = 64u * nt, wb = 16u * nt;
+    mbar_arrive_expect_tx(bar, kb + sb + vb + wb);
+    bulk_g2s(dst, a.k_codes + gi * 2048, kb, bar);
+    bulk_g2s(dst + kOffKScale, a.k_scales + gi * 128, sb, bar);
+    bulk_g2s(dst + kOffVCode, a.v_codes + ti * 64, vb, bar);
+    bulk_g2s(dst + kOffVScale, a.v_scales + ti * 4, wb, bar);
+  } else {
+    const int w0 = kWinItem * (j - a.Gi);
+    const int nt = min(kWinItem, a.R - w0);
+    const long wi = static_cast<long>(u) * a.R + w0;
+    const uint32_t bytes = 256u * nt;
+    mbar_arrive_expect_tx(bar, 2u * bytes);
+    bulk_g2s(dst, a.k_window + wi * 128, bytes, bar);
+    bulk_g2s(dst + kOffVWin, a.v_window + wi * 128, bytes, bar);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const DecodeArgs a) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   DecodeSmem &sm = *reinterpret_cast<DecodeSmem *>(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long cta = blockIdx.x;
-  const long lo = cta * a.total_items / a.num_ctas;
-  const long hi = (cta + 1) * a.total_items / a.num_ctas;
-  const long n_items = hi - lo;
-  const long u_first = lo / a.ipu;
+  const int cta = blockIdx.x;
+  const int lo = static_cast<int>(static_cast<long>(cta) * a.total_items / a.num_ctas);
+  const int hi = static_cast<int>(static_cast<long>(cta + 1) * a.total_items / a.num_ctas);
+  const int n_items = hi - lo;
+  const int u_first = lo / a.ipu;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&sm.full[s]), 1);
-      mbar_init(smem_u32(&sm.empty[s]), 1);
+      mbar_init(smem_u32(&sm.empty[s]), kConsumers);
     }
     sm.abort_flag = 0;
     fence_mbar_init();
@@ -384,47 +424,29 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a)
   __syncthreads();
 
   if (warp == kConsumers) {
-    // ---------------- loader
+    // ---------------- loader: one lane walks the CTA's items in order
     if (lane == 0) {
-      long k = 0;
+      int k = 0, u = u_first, j = lo - u_first * a.ipu;
       for (; k < n_items; ++k) {
-        const int st = static_cast<int>(k % kStages);
+        const int st = k % kStages;
         if (k >= kStages) {
           const uint32_t par = static_cast<uint32_t>((k / kStages - 1) & 1);
-          if (!mbar_wait(smem_u32(&sm.empty[st]), par, a.ctl.wait_limit_ns)) {
+          if (!mbar_wait_sleep(smem_u32(&sm.empty[st]), par, a.ctl.wait_limit_ns, 32)) {
             flag_error(a.ctl, KVQ_DEV_TIMEOUT);
             *reinterpret_cast<volatile int *>(&sm.abort_flag) = 1;
             break;
           }
         }
         if (aborted_flag(sm)) break;
-        const long item = lo + k;
-        if (item == a.ctl.drop_item) continue;  // test hook: this stage is never filled
-        const long u = item / a.ipu;
-        const int j = static_cast<int>(item % a.ipu);
-        const uint32_t dst = smem_u32(sm.stage[st]);
-        const uint32_t bar = smem_u32(&sm.full[st]);
-        if (j < a.Gk) {
-          const int valid = min(32, a.cut - 32 * j);
-          const uint32_t vbytes = static_cast<uint32_t>(valid) * 64u;
-          const uint32_t sbytes = static_cast<uint32_t>(valid) * 16u;
-          mbar_arrive_expect_tx(bar, 2048u + 512u + vbytes + sbytes);
-          bulk_g2s(dst, a.k_codes + (u * a.Gk + j) * 2048L, 2048u, bar);
-          bulk_g2s(dst + kOffKScale, a.k_scales + (u * a.Gk + j) * 128L, 512u, bar);
-          bulk_g2s(dst + kOffVCode, a.v_codes + (u * a.cut + 32L * j) * 64L, vbytes, bar);
-          bulk_g2s(dst + kOffVScale, a.v_scales + (u * a.cut + 32L * j) * 4L, sbytes, bar);
-        } else {
-          const int w = j - a.Gk;
-          const int valid = min(kWinTile, a.R - kWinTile * w);
-          const uint32_t bytes = static_cast<uint32_t>(valid) * 256u;
-          mbar_arrive_expect_tx(bar, 2u * bytes);
-          bulk_g2s(dst, a.k_window + (u * a.R + kWinTile * w) * 128L, bytes, bar);
-          bulk_g2s(dst + 4096, a.v_window + (u * a.R + kWinTile * w) * 128L, bytes, bar);
+        if (lo + k != a.ctl.drop_item)  // test hook: a dropped stage is never filled
+          load_item(a, u, j, smem_u32(sm.stage[st]), smem_u32(&sm.full[st]));
+        if (++j == a.ipu) {
+          j = 0;
+          ++u;
         }
       }
       // drain: copies still in flight must land before the CTA exits
-      const long issued = k;
-      for (long d = std::max(0L, issued - kStages); d < issued; ++d) {
+      for (int d = max(0, k - kStages); d < k; ++d) {
         if (lo + d == a.ctl.drop_item) continue;
         mbar_wait(smem_u32(&sm.full[d % kStages]), static_cast<uint32_t>((d / kStages) & 1),
                   2000000000ull);
@@ -433,22 +455,23 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a)
     return;
   }
 
-  // ---------------- consumers
+  // ---------------- consumers: warp w takes group w (or window rows 10w..) of every item
   const int g = lane >> 2, t = lane & 3;
   WarpState st;
-  float qr[32];
-  long k = warp;  // this warp's next item (CTA-relative)
-  for (long u = u_first; u * a.ipu < hi; ++u) {
+  uint32_t qh[4][4];
+  int k = 0;  // CTA-relative item index
+  for (int u = u_first; u * a.ipu < hi; ++u) {
     state_reset(st);
-    load_q(a, u, g, t, qr);
-    const long u_end = std::min(hi, (u + 1) * a.ipu) - lo;  // CTA-relative end of unit u
+    load_q(a, u, g, t, qh);
+    const int u_end = min(hi, (u + 1) * a.ipu) - lo;  // CTA-relative end of unit u
+    int j = lo + k - u * a.ipu;                        // item index within unit u
     bool aborted = false;
-    for (; k < u_end; k += kConsumers) {
+    for (; k < u_end; ++k, ++j) {
       if (aborted_flag(sm)) {
         aborted = true;
         break;
       }
-      const int s = static_cast<int>(k % kStages);
+      const int s = k % kStages;
       if (!mbar_wait(smem_u32(&sm.full[s]), static_cast<uint32_t>((k / kStages) & 1),
                      a.ctl.wait_limit_ns)) {
         if (lane == 0) {
@@ -458,11 +481,22 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a)
         aborted = true;
         break;
       }
-      const int j = static_cast<int>((lo + k) % a.ipu);
-      if (j < a.Gk)
-        do_int4_item(st, sm.stage[s], qr, min(32, a.cut - 32 * j), g, t);
-      else
-        do_window_item(st, sm.stage[s], qr, min(kWinTile, a.R - kWinTile * (j - a.Gk)), g, t);
+      const uint8_t *stg = sm.stage[s];
+      if (j < a.Gi) {
+        const int grp = kGroupsPerItem * j + warp;
+        if (grp < a.Gk)
+          do_int4_item(st, stg + warp * 2048,
+                       reinterpret_cast<const float *>(stg + kOffKScale + warp * 512),
+                       stg + kOffVCode + warp * 2048,
+                       reinterpret_cast<const float *>(stg + kOffVScale + warp * 512), qh,
+                       min(32, a.cut - 32 * grp), g, t);
+      } else {
+        const int r0 = kWinItem * (j - a.Gi) + kWinTile * warp;
+        if (r0 < a.R)
+          do_window_item(st, reinterpret_cast<const uint32_t *>(stg + warp * kWinTile * 256),
+                         reinterpret_cast<const uint32_t *>(stg + kOffVWin + warp * kWinTile * 256),
+                         qh, min(kWinTile, a.R - r0), g, t);
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&sm.empty[s]));
     }
@@ -479,34 +513,42 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a)
       sm.red_l[warp][2 * t] = l0;
       sm.red_l[warp][2 * t + 1] = l1;
     }
+    // heads 0-3 live in lanes with t < 2, heads 4-7 in lanes with t >= 2:
+    // merge one half at a time through red_o
+    for (int half = 0; half < 2; ++half) {
+      if ((t >> 1) == half) {
+        const int h0 = 2 * t - 4 * half;
 #pragma unroll
-    for (int f = 0; f < 8; ++f) {
-      sm.red_o[warp][2 * t][16 * g + f] = st.o[f][0];
-      sm.red_o[warp][2 * t + 1][16 * g + f] = st.o[f][1];
-      sm.red_o[warp][2 * t][16 * g + 8 + f] = st.o[f][2];
-      sm.red_o[warp][2 * t + 1][16 * g + 8 + f] = st.o[f][3];
-    }
-    asm volatile("bar.sync 1, %0;" ::"n"(kConsumers * 32));
-    float *part = a.partials + ((cta * a.max_units + (u - u_first)) * kHeads) * kPartFloats;
-    for (int i = threadIdx.x; i < kHeads * kD; i += kConsumers * 32) {
-      const int h = i / kD, d = i % kD;
-      float mx = -CUDART_INF_F;
-#pragma unroll
-      for (int w = 0; w < kConsumers; ++w) mx = fmaxf(mx, sm.red_m[w][h]);
-      float acc = 0.0f, lsum = 0.0f;
-#pragma unroll
-      for (int w = 0; w < kConsumers; ++w) {
-        const float c = (sm.red_m[w][h] == -CUDART_INF_F) ? 0.0f : exp2f(sm.red_m[w][h] - mx);
-        acc += c * sm.red_o[w][h][d];
-        lsum += c * sm.red_l[w][h];
+        for (int f = 0; f < 8; ++f) {
+          sm.red_o[warp][h0][16 * g + f] = st.o[f][0];
+          sm.red_o[warp][h0 + 1][16 * g + f] = st.o[f][1];
+          sm.red_o[warp][h0][16 * g + 8 + f] = st.o[f][2];
+          sm.red_o[warp][h0 + 1][16 * g + 8 + f] = st.o[f][3];
+        }
       }
-      part[h * kPartFloats + d] = acc;
-      if (d == 0) {
-        part[h * kPartFloats + kD] = mx;
-        part[h * kPartFloats + kD + 1] = lsum;
+      asm volatile("bar.sync 1, %0;" ::"n"(kConsumers * 32));
+      float *part =
+          a.partials + ((static_cast<long>(cta) * a.max_units + (u - u_first)) * kHeads) * kPartFloats;
+      for (int i = threadIdx.x; i < (kHeads / 2) * kD; i += kConsumers * 32) {
+        const int hh = i / kD, d = i % kD, h = 4 * half + hh;
+        float mx = -CUDART_INF_F;
+#pragma unroll
+        for (int w = 0; w < kConsumers; ++w) mx = fmaxf(mx, sm.red_m[w][h]);
+        float acc = 0.0f, lsum = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kConsumers; ++w) {
+          const float c = (sm.red_m[w][h] == -CUDART_INF_F) ? 0.0f : exp2f(sm.red_m[w][h] - mx);
+          acc += c * sm.red_o[w][hh][d];
+          lsum += c * sm.red_l[w][h];
+        }
+        part[h * kPartFloats + d] = acc;
+        if (d == 0) {
+          part[h * kPartFloats + kD] = mx;
+          part[h * kPartFloats + kD + 1] = lsum;
+        }
       }
+      asm volatile("bar.sync 1, %0;" ::"n"(kConsumers * 32));
     }
-    asm volatile("bar.sync 1, %0;" ::"n"(kConsumers * 32));
     if (aborted || aborted_flag(sm)) break;
   }
 }
@@ -551,18 +593,20 @@ __global__ void __launch_bounds__(256) combine_kernel(const DecodeArgs a, OT *__
 }
 
 struct Plan {
-  long total_items;
-  int ipu, Wt, num_ctas, max_units;
+  int total_items;
+  int ipu, Gi, Wt, num_ctas, max_units;
 };
 
 Plan make_plan(const kvq_cache &c, int num_sms) {
   const CacheDims d = dims_of(c);
   Plan p;
-  p.Wt = (d.R + kWinTile - 1) / kWinTile;
-  p.ipu = d.Gk + p.Wt;
-  p.total_items = static_cast<long>(d.B) * d.Hkv * p.ipu;
-  p.num_ctas = static_cast<int>(std::min<long>(p.total_items, 2L * num_sms));
-  const long per = (p.total_items + p.num_ctas - 1) / p.num_ctas;
+  p.Gi = (d.Gk + kGroupsPerItem - 1) / kGroupsPerItem;
+  p.Wt = (d.R + kWinItem - 1) / kWinItem;
+  p.ipu = p.Gi + p.Wt;
+  const long total = static_cast<long>(d.B) * d.Hkv * p.ipu;
+  p.total_items = static_cast<int>(std::min<long>(total, 1L << 30));
+  p.num_ctas = static_cast<int>(std::min<long>(total, static_cast<long>(kCtasPerSm) * num_sms));
+  const long per = (total + p.num_ctas - 1) / p.num_ctas;
   p.max_units = static_cast<int>((per + p.ipu - 1) / p.ipu + 1);
   return p;
 }
@@ -571,8 +615,11 @@ Plan make_plan(const kvq_cache &c, int num_sms) {
 
 bool decode_supported(const kvq_cache &c, int q_dtype, int Hq, int n_q) {
   const bool win_ok = c.recent == 0 || (c.kwin_dtype == KVQ_BF16 && c.vwin_dtype == KVQ_BF16);
+  const long items = static_cast<long>(c.batch) * c.kv_heads *
+                    ((c.n_tokens - c.recent + 32 * kGroupsPerItem - 1) / (32 * kGroupsPerItem) +
+                     (c.recent + kWinItem - 1) / kWinItem);
   return c.head_dim == kD && n_q == 1 && Hq == kHeads * c.kv_heads && win_ok &&
-         (q_dtype == KVQ_BF16 || q_dtype == KVQ_F32) && c.n_tokens > 0;
+         (q_dtype == KVQ_BF16 || q_dtype == KVQ_F32) && c.n_tokens > 0 && items < (1L << 30);
 }
 
 size_t decode_workspace_bytes(const kvq_cache &c, int, int num_sms) {
@@ -600,6 +647,7 @@ int launch_attend_decode(const kvq_cache &c, const void *q, int q_dtype, float s
   a.cut = d.cut;
   a.Gk = d.Gk;
   a.Wt = p.Wt;
+  a.Gi = p.Gi;
   a.ipu = p.ipu;
   a.total_items = p.total_items;
   a.num_ctas = p.num_ctas;

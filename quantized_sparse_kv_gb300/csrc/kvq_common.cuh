@@ -75,6 +75,19 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
   }
 }
 
+// As mbar_wait, but sleeps between polls: for a warp whose waiting should not
+// take issue slots from the warps that do the work.
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                                uint32_t sleep_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (;;) {
+    __nanosleep(sleep_ns);
+    if (mbar_try_wait(bar, parity)) return true;
+    if (global_ns() - t0 > limit_ns) return false;
+  }
+}
+
 // ------------------------------------------------------------------ bulk copy
 // 1-D global -> shared copy completing on an mbarrier (tx bytes). Both
 // addresses 16-byte aligned, bytes a multiple of 16.
