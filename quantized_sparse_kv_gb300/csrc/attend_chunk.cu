@@ -1,16 +1,505 @@
-// Chunk attention on the fifth-generation tensor cores: not built yet; every
-// chunk-shaped call runs the fp32 kernel meanwhile.
+// Chunk attention on the fifth-generation tensor cores (tcgen05 + TMEM + TMA).
+//
+// What it computes: for every query row of a chunk, O = softmax(sm_scale * Q
+// K^T) V over all keys of a cache whose window holds every token (bf16 K and
+// V), plus the per-row softmax mass on each key region -- the Catnip study's
+// chunk of 2,340 queries (6 latent frames) over 6,240 keys laid out [sink 1560
+// | recent 2340 | current 2340] (section "KV Cache 的实际作用"), no mask.
+//
+// One CTA per (128 query rows, query head); 8 warps:
+//   warp 0      TMA producer: Q once, then K and V tiles of 128 keys into a
+//               2-stage ring (128B-swizzled, 64-feature boxes);
+//   warp 1      allocates 512 TMEM columns and one lane issues the MMAs:
+//               S_j = Q K_j^T into TMEM buffer j % 2 (M=128, N=128, K=128 as 8
+//               k-steps of 16), then O += P_{j-1} V_{j-1} into TMEM O (V is the
+//               MN-major B operand);
+//   warps 4-7   softmax: thread r owns query row r (TMEM lane r). It loads its
+//               S row, releases the S buffer, exponentiates in the log2 domain
+//               against a running max that is only moved when it grows by more
+//               than 8 (then O and the sums are rescaled), accumulates the row
+//               sum and the region sums, and writes P (bf16, swizzled) to
+//               shared memory for the next PV MMA. At the end it reads O from
+//               TMEM, normalises and stores O and the region masses.
+// Every mbarrier wait is bounded; on timeout the CTA flags KVQ_DEV_TIMEOUT,
+// stops, drains its copies and MMAs and frees TMEM.
+#include <cuda.h>
+#include <math_constants.h>
+
+#include <mutex>
+
 #include "kvq_internal.h"
 
 namespace kvq {
+namespace {
 
-bool chunk_supported(const kvq_cache &, int, int, int) { return false; }
+constexpr int kBM = 128;          // query rows per CTA
+constexpr int kBN = 128;          // keys per tile
+constexpr int kDim = 128;         // head dim
+constexpr int kKvStages = 2;
+constexpr int kMaxRegions = 4;
+constexpr uint32_t kTileBytes = kBN * kDim * 2;  // 32 KB, one K or V tile (bf16)
+constexpr uint32_t kHalfBytes = kTileBytes / 2;  // 16 KB: 128 rows x 64 features
+constexpr float kRescaleThreshold = 8.0f;         // log2 units
+
+struct __align__(1024) ChunkSmem {
+  uint8_t q[kTileBytes];                    // 2 x [128 rows][128 B], swizzled
+  uint8_t k[kKvStages][kTileBytes];
+  uint8_t v[kKvStages][kTileBytes];
+  uint8_t p[kTileBytes];                    // P (bf16) as the K-major A operand
+  uint64_t q_full;
+  uint64_t kv_full[kKvStages], kv_empty[kKvStages];
+  uint64_t s_full[2], s_free[2];
+  uint64_t p_full, o_done, mma_done;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+struct ChunkArgs {
+  int n_q, n_kv, q_heads, kv_group, n_tiles;
+  float scale_log2;
+  void *out;
+  int out_dtype;
+  float *mass;
+  Regions reg;
+  KernelCtl ctl;
+};
+
+// ------------------------------------------------------------------ PTX wrappers
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int x, int y,
+                                            int z, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+      "%3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                           uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// 32 consecutive TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+      "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+      "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+      "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+      "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: 128B swizzle, version 1 (bits 46-48).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = static_cast<uint64_t>((addr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;  // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor, kind::f16: bf16 A and B, fp32 accumulator, M=128,
+// N=128, A K-major, B K-major (b_mn_major = 0) or MN-major (1).
+__host__ __device__ constexpr uint32_t idesc_bf16(uint32_t b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (b_mn_major << 16) | ((128u >> 3) << 17) |
+         ((128u >> 4) << 24);
+}
+
+__device__ __forceinline__ bool cta_aborted(ChunkSmem &sm) {
+  return *reinterpret_cast<volatile int *>(&sm.abort_flag) != 0;
+}
+
+__device__ __forceinline__ bool wait_or_abort(ChunkSmem &sm, uint32_t bar, uint32_t parity,
+                                              const KernelCtl &ctl) {
+  if (mbar_wait(bar, parity, ctl.wait_limit_ns)) return true;
+  flag_error(ctl, KVQ_DEV_TIMEOUT);
+  *reinterpret_cast<volatile int *>(&sm.abort_flag) = 1;
+  return false;
+}
+
+// Byte offset of 16-byte chunk c (0..7) of row r inside a 128B-swizzled
+// [rows][128 B] region that starts on a 1024-byte boundary.
+__device__ __forceinline__ uint32_t swz(uint32_t r, uint32_t c) {
+  return r * 128u + ((c ^ (r & 7u)) << 4);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&b);
+}
+
+__global__ void __launch_bounds__(256, 1)
+    chunk_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
+                      const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v, const ChunkArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // dynamic shared memory is only 16-byte aligned: round up to 1024
+  const uint32_t base = smem_u32(smem_raw);
+  ChunkSmem &sm = *reinterpret_cast<ChunkSmem *>(smem_raw + (((base + 1023u) & ~1023u) - base));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int q0 = blockIdx.x * kBM;
+  const int hq = blockIdx.y;                 // b * q_heads + h
+  const int hkv = (hq / a.q_heads) * (a.q_heads / a.kv_group) + (hq % a.q_heads) / a.kv_group;
+  const int nt = a.n_tiles;
+
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&sm.q_full), 1);
+    for (int s = 0; s < kKvStages; ++s) {
+      mbar_init(smem_u32(&sm.kv_full[s]), 1);
+      mbar_init(smem_u32(&sm.kv_empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&sm.s_full[b]), 1);
+      mbar_init(smem_u32(&sm.s_free[b]), 128);
+    }
+    mbar_init(smem_u32(&sm.p_full), 128);
+    mbar_init(smem_u32(&sm.o_done), 1);
+    mbar_init(smem_u32(&sm.mma_done), 1);
+    sm.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(
+                     smem_u32(&sm.tmem_base))
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+  const uint32_t t_s[2] = {tmem, tmem + 128u};
+  const uint32_t t_o = tmem + 256u;
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint32_t qb = smem_u32(&sm.q_full);
+      mbar_arrive_expect_tx(qb, kTileBytes);
+      tma_load_3d(smem_u32(sm.q), &tm_q, 0, q0, hq, qb);
+      tma_load_3d(smem_u32(sm.q) + kHalfBytes, &tm_q, 64, q0, hq, qb);
+      int j = 0;
+      for (; j < nt; ++j) {
+        const int st = j % kKvStages;
+        if (j >= kKvStages &&
+            !wait_or_abort(sm, smem_u32(&sm.kv_empty[st]), ((j / kKvStages) - 1) & 1, a.ctl))
+          break;
+        if (cta_aborted(sm)) break;
+        const uint32_t fb = smem_u32(&sm.kv_full[st]);
+        mbar_arrive_expect_tx(fb, 2 * kTileBytes);
+        tma_load_3d(smem_u32(sm.k[st]), &tm_k, 0, j * kBN, hkv, fb);
+        tma_load_3d(smem_u32(sm.k[st]) + kHalfBytes, &tm_k, 64, j * kBN, hkv, fb);
+        tma_load_3d(smem_u32(sm.v[st]), &tm_v, 0, j * kBN, hkv, fb);
+        tma_load_3d(smem_u32(sm.v[st]) + kHalfBytes, &tm_v, 64, j * kBN, hkv, fb);
+      }
+      // drain: the copies of the last stages must land before the CTA exits
+      mbar_wait(qb, 0, 2000000000ull);
+      for (int d = (j > kKvStages ? j - kKvStages : 0); d < j; ++d)
+        mbar_wait(smem_u32(&sm.kv_full[d % kKvStages]), (d / kKvStages) & 1, 2000000000ull);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t id_qk = idesc_bf16(0), id_pv = idesc_bf16(1);
+      const uint32_t qa = smem_u32(sm.q), pa = smem_u32(sm.p);
+      bool ok = wait_or_abort(sm, smem_u32(&sm.q_full), 0, a.ctl);
+      auto issue_pv = [&](int i) -> bool {
+        if (!wait_or_abort(sm, smem_u32(&sm.p_full), i & 1, a.ctl)) return false;
+        tc_fence_after();
+        const uint32_t va = smem_u32(sm.v[i % kKvStages]);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t ad = smem_desc(pa + (kk >> 2) * kHalfBytes + (kk & 3) * 32u, 16, 1024);
+          const uint64_t bd = smem_desc(va + kk * 2048u, kHalfBytes, 1024);
+          tc_mma_f16(t_o, ad, bd, id_pv, (i > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc_commit(smem_u32(&sm.o_done));
+        tc_commit(smem_u32(&sm.kv_empty[i % kKvStages]));
+        return true;
+      };
+      for (int j = 0; ok && j < nt; ++j) {
+        const int st = j % kKvStages, b = j & 1;
+        if (!wait_or_abort(sm, smem_u32(&sm.kv_full[st]), (j / kKvStages) & 1, a.ctl)) break;
+        if (j >= 2 && !wait_or_abort(sm, smem_u32(&sm.s_free[b]), ((j >> 1) - 1) & 1, a.ctl))
+          break;
+        tc_fence_after();
+        const uint32_t ka = smem_u32(sm.k[st]);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32u;
+          tc_mma_f16(t_s[b], smem_desc(qa + off, 16, 1024), smem_desc(ka + off, 16, 1024), id_qk,
+                     kk > 0 ? 1u : 0u);
+        }
+        tc_commit(smem_u32(&sm.s_full[b]));
+        if (j >= 1 && !issue_pv(j - 1)) {
+          ok = false;
+          break;
+        }
+      }
+      if (ok && !cta_aborted(sm)) issue_pv(nt - 1);
+      // all MMAs of this CTA complete before TMEM is released
+      tc_commit(smem_u32(&sm.mma_done));
+      mbar_wait(smem_u32(&sm.mma_done), 0, 2000000000ull);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------ softmax + epilogue
+    const int quad = warp - 4;               // TMEM lanes 32*quad .. +31
+    const int row = quad * 32 + lane;        // query row within the tile
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    float m_used = -CUDART_INF_F, l = 0.0f;
+    float rsum[kMaxRegions] = {0.0f, 0.0f, 0.0f, 0.0f};
+    bool ok = true;
+    for (int j = 0; j < nt; ++j) {
+      const int b = j & 1;
+      if (!wait_or_abort(sm, smem_u32(&sm.s_full[b]), (j >> 1) & 1, a.ctl)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float s[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        float v[32];
+        tmem_ld32(t_s[b] + lane_off + 32u * c, v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s[32 * c + i] = v[i];
+      }
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(smem_u32(&sm.s_free[b]));
+      const int valid = min(kBN, a.n_kv - j * kBN);
+      float mx = -CUDART_INF_F;
+#pragma unroll
+      for (int i = 0; i < 128; ++i) {
+        s[i] = (i < valid) ? s[i] * a.scale_log2 : -CUDART_INF_F;
+        mx = fmaxf(mx, s[i]);
+      }
+      // move the running max only when it grows by more than the threshold
+      float factor = 1.0f;
+      const bool grow = mx > m_used + kRescaleThreshold;
+      if (grow) {
+        factor = exp2f(m_used - mx);  // 0 on the first tile
+        m_used = mx;
+      }
+      l *= factor;
+#pragma unroll
+      for (int k = 0; k < kMaxRegions; ++k) rsum[k] *= factor;
+      float ps = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 128; ++i) {
+        s[i] = exp2f(s[i] - m_used);
+        ps += s[i];
+      }
+      l += ps;
+      // region sums: bounds inside this tile split the row
+      const int t0 = j * kBN;
+      for (int k = 0; k < a.reg.n && k < kMaxRegions; ++k) {
+        const int lo = a.reg.b[k] - t0, hi = a.reg.b[k + 1] - t0;
+        if (hi <= 0 || lo >= kBN) continue;
+        if (lo <= 0 && hi >= kBN) {
+          rsum[k] += ps;
+          continue;
+        }
+        float part = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 128; ++i) part += (i >= lo && i < hi) ? s[i] : 0.0f;
+        rsum[k] += part;
+      }
+      // PV_{j-1} must be complete before P is overwritten or O is rescaled
+      if (j >= 1 && !wait_or_abort(sm, smem_u32(&sm.o_done), (j - 1) & 1, a.ctl)) {
+        ok = false;
+        break;
+      }
+      if (j >= 1 && __any_sync(0xffffffffu, factor != 1.0f)) {
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          float v[32];
+          tmem_ld32(t_o + lane_off + 32u * c, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] *= factor;
+          tmem_st32(t_o + lane_off + 32u * c, v);
+        }
+        tmem_wait_st();
+      }
+      // P row -> shared memory, bf16, 128B-swizzled K-major layout
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const int half = c >> 3, chunk = c & 7;
+        uint4 w;
+        w.x = pack_bf16x2(s[8 * c + 0], s[8 * c + 1]);
+        w.y = pack_bf16x2(s[8 * c + 2], s[8 * c + 3]);
+        w.z = pack_bf16x2(s[8 * c + 4], s[8 * c + 5]);
+        w.w = pack_bf16x2(s[8 * c + 6], s[8 * c + 7]);
+        *reinterpret_cast<uint4 *>(sm.p + half * kHalfBytes + swz(row, chunk)) = w;
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      tc_fence_before();
+      mbar_arrive(smem_u32(&sm.p_full));
+    }
+    // ---- epilogue: O / l and region masses
+    if (ok && wait_or_abort(sm, smem_u32(&sm.o_done), (nt - 1) & 1, a.ctl)) {
+      tc_fence_after();
+      const int qrow = q0 + row;
+      const float inv = 1.0f / l;
+      const long obase = (static_cast<long>(hq) * a.n_q + qrow) * kDim;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        float v[32];
+        tmem_ld32(t_o + lane_off + 32u * c, v);
+        tmem_wait_ld();
+        if (qrow < a.n_q) {
+          if (a.out_dtype == KVQ_F32) {
+            float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(a.out) + obase + 32 * c);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              o[i] = make_float4(v[4 * i] * inv, v[4 * i + 1] * inv, v[4 * i + 2] * inv,
+                                 v[4 * i + 3] * inv);
+          } else {
+            uint4 *o = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.out) + obase + 32 * c);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              o[i] = make_uint4(pack_bf16x2(v[8 * i] * inv, v[8 * i + 1] * inv),
+                                pack_bf16x2(v[8 * i + 2] * inv, v[8 * i + 3] * inv),
+                                pack_bf16x2(v[8 * i + 4] * inv, v[8 * i + 5] * inv),
+                                pack_bf16x2(v[8 * i + 6] * inv, v[8 * i + 7] * inv));
+          }
+        }
+      }
+      if (a.mass && qrow < a.n_q)
+        for (int k = 0; k < a.reg.n; ++k)
+          a.mass[(static_cast<long>(hq) * a.n_q + qrow) * a.reg.n + k] = rsum[k] * inv;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem) : "memory");
+  }
+}
+
+// ------------------------------------------------------------------ host side
+using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                 const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                 const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                 CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encoder() {
+  static EncodeTiled fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiled>(p);
+  });
+  return fn;
+}
+
+// [heads][rows][128] bf16 as a 3-D map, box 64 features x 128 rows x 1 head.
+bool make_map(CUtensorMap *m, const void *ptr, int rows, int heads) {
+  EncodeTiled enc = encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kDim), static_cast<cuuint64_t>(rows),
+                              static_cast<cuuint64_t>(heads)};
+  const cuuint64_t strides[2] = {kDim * 2ull, static_cast<cuuint64_t>(rows) * kDim * 2ull};
+  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool chunk_supported(const kvq_cache &c, int q_dtype, int Hq, int n_q) {
+  return c.recent == c.n_tokens && c.head_dim == kDim && c.kwin_dtype == KVQ_BF16 &&
+         c.vwin_dtype == KVQ_BF16 && q_dtype == KVQ_BF16 && n_q >= 64 && Hq % c.kv_heads == 0 &&
+         encoder() != nullptr;
+}
 
 size_t chunk_workspace_bytes(const kvq_cache &, int, int) { return 0; }
 
-int launch_attend_chunk(const kvq_cache &, const void *, int, int, float, void *, int,
-                        const int32_t *, int, float *, void *, const KernelCtl &, cudaStream_t) {
-  return 0;
+int chunk_max_regions() { return kMaxRegions; }
+
+int launch_attend_chunk(const kvq_cache &c, const void *q, int Hq, int n_q, float scale_log2,
+                        void *out, int out_dtype, const int32_t *bounds, int n_regions,
+                        float *mass, void *, const KernelCtl &ctl, cudaStream_t s) {
+  CUtensorMap tq, tk, tv;
+  if (!make_map(&tq, q, n_q, c.batch * Hq) || !make_map(&tk, c.k_window, c.n_tokens, c.batch * c.kv_heads) ||
+      !make_map(&tv, c.v_window, c.n_tokens, c.batch * c.kv_heads))
+    return -1;
+  ChunkArgs a;
+  a.n_q = n_q;
+  a.n_kv = c.n_tokens;
+  a.q_heads = Hq;
+  a.kv_group = Hq / c.kv_heads;
+  a.n_tiles = (c.n_tokens + kBN - 1) / kBN;
+  a.scale_log2 = scale_log2;
+  a.out = out;
+  a.out_dtype = out_dtype;
+  a.mass = mass;
+  a.reg = make_regions(bounds, n_regions);
+  a.ctl = ctl;
+  const size_t smem = sizeof(ChunkSmem) + 1024;
+  cudaFuncSetAttribute(chunk_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       static_cast<int>(smem));
+  dim3 grid((n_q + kBM - 1) / kBM, c.batch * Hq);
+  chunk_bf16_kernel<<<grid, 256, smem, s>>>(tq, tk, tv, a);
+  return 1;
 }
 
 }  // namespace kvq

@@ -554,37 +554,46 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const Deco
 }
 
 // One warp per (unit, query head): merge the partials of every CTA whose
-// slice overlaps the unit (log-sum-exp), normalise, store.
+// slice overlaps the unit (log-sum-exp), normalise, store. Lanes first read
+// the CTAs' running maxima and sums in parallel; the O rows are then summed
+// with independent loads.
 template <typename OT>
 __global__ void __launch_bounds__(256) combine_kernel(const DecodeArgs a, OT *__restrict__ out) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long u = blockIdx.x;
   const int h = warp;
   const long start = u * a.ipu, end = start + a.ipu;
-  long c = start * a.num_ctas / a.total_items;
-  while (c > 0 && (c * a.total_items / a.num_ctas) > start) --c;
-  float m = -CUDART_INF_F, l = 0.0f, acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-  for (; c < a.num_ctas; ++c) {
-    const long clo = c * a.total_items / a.num_ctas, chi = (c + 1) * a.total_items / a.num_ctas;
-    if (clo >= end) break;
-    if (chi <= start) continue;
-    const long slot = u - clo / a.ipu;
-    if (slot < 0 || slot >= a.max_units) {
-      if (lane == 0) flag_error(a.ctl, KVQ_DEV_BOUNDS);
-      continue;
-    }
-    const float *p = a.partials + ((c * a.max_units + slot) * kHeads + h) * kPartFloats;
+  long c0 = start * a.num_ctas / a.total_items;
+  while (c0 > 0 && (c0 * a.total_items / a.num_ctas) > start) --c0;
+  while ((c0 + 1) * a.total_items / a.num_ctas <= start) ++c0;  // first CTA ending past start
+  long c1 = c0;                                                  // one past the last overlapping CTA
+  while (c1 < a.num_ctas && c1 * a.total_items / a.num_ctas < end) ++c1;
+  auto part = [&](long c) -> const float * {
+    const long slot = u - (c * a.total_items / a.num_ctas) / a.ipu;
+    return a.partials + ((c * a.max_units + slot) * kHeads + h) * kPartFloats;
+  };
+  float m = -CUDART_INF_F, l = 0.0f;
+  for (long c = c0 + lane; c < c1; c += 32) {
+    const float *p = part(c);
     const float pm = p[kD], pl = p[kD + 1];
     if (pm == -CUDART_INF_F) continue;
     const float nm = fmaxf(m, pm);
-    const float c_old = exp2f(m - nm), c_new = exp2f(pm - nm);
-    const float4 po = *reinterpret_cast<const float4 *>(p + 4 * lane);
-    acc[0] = acc[0] * c_old + po.x * c_new;
-    acc[1] = acc[1] * c_old + po.y * c_new;
-    acc[2] = acc[2] * c_old + po.z * c_new;
-    acc[3] = acc[3] * c_old + po.w * c_new;
-    l = l * c_old + pl * c_new;
+    l = l * exp2f(m - nm) + pl * exp2f(pm - nm);
     m = nm;
+  }
+  const float mx = warp_max(m);
+  l = warp_sum(m == -CUDART_INF_F ? 0.0f : l * exp2f(m - mx));
+  float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll 4
+  for (long c = c0; c < c1; ++c) {
+    const float *p = part(c);
+    const float pm = p[kD];
+    const float w = pm == -CUDART_INF_F ? 0.0f : exp2f(pm - mx);
+    const float4 po = *reinterpret_cast<const float4 *>(p + 4 * lane);
+    acc[0] += w * po.x;
+    acc[1] += w * po.y;
+    acc[2] += w * po.z;
+    acc[3] += w * po.w;
   }
   const float inv = 1.0f / l;
   OT *o = out + (u * kHeads + h) * kD + 4 * lane;

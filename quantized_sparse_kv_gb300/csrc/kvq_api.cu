@@ -158,7 +158,8 @@ kvq_status kv_attend(const kvq_cache *cache, const void *q, int32_t q_dtype, int
   const int sms = sm_count();
 
   enum { GENERIC, DECODE, CHUNK } path = GENERIC;
-  if (kvq::chunk_supported(*cache, q_dtype, q_heads, n_q))
+  if (kvq::chunk_supported(*cache, q_dtype, q_heads, n_q) &&
+      (!regions || n_regions <= kvq::chunk_max_regions()))
     path = CHUNK;
   else if (!regions && kvq::decode_supported(*cache, q_dtype, q_heads, n_q))
     path = DECODE;
@@ -181,6 +182,7 @@ kvq_status kv_attend(const kvq_cache *cache, const void *q, int32_t q_dtype, int
     const int n = kvq::launch_attend_chunk(*cache, q, q_heads, n_q,
                                            static_cast<float>(scale * kLog2e), out, out_dtype,
                                            region_bounds, n_regions, region_mass, workspace, ctl, s);
+    if (n < 0) return KVQ_ERR_CUDA;
     return finish(n, cache->kwin_dtype == KVQ_MXFP8 ? "chunk_mxfp8" : "chunk_bf16");
   }
   if (path == DECODE) {

@@ -71,6 +71,7 @@ int launch_attend_candidates(const kvq_cache &c, const void *q, int q_dtype, int
 // attend_chunk.cu: tcgen05 chunk attention over an all-window bf16 / MXFP8 cache.
 bool chunk_supported(const kvq_cache &c, int q_dtype, int Hq, int n_q);
 size_t chunk_workspace_bytes(const kvq_cache &c, int Hq, int n_q);
+int chunk_max_regions();
 int launch_attend_chunk(const kvq_cache &c, const void *q, int Hq, int n_q, float scale_log2,
                         void *out, int out_dtype, const int32_t *bounds, int n_regions,
                         float *mass, void *ws, const KernelCtl &ctl, cudaStream_t s);

@@ -262,3 +262,54 @@ def test_decode_wait_runs_out_and_reports_timeout(kvq):
     assert kvq.read_status(a.status) == 0
     ref, _ = O.attend(q, O.pack(k, v, 128, "bf16"))
     assert O.rel_l2(to_np(a.out), ref) <= TOL_BF16
+
+
+# ------------------------------------------------------------------ chunk attention (tcgen05)
+
+
+def chunk_case(seed, heads_q, heads_kv, n_q, n_kv, concentrated=0.0):
+    rng = np.random.default_rng(seed)
+    q = rng.standard_normal((1, heads_q, n_q, 128))
+    k = rng.standard_normal((1, heads_kv, n_kv, 128))
+    v = rng.standard_normal((1, heads_kv, n_kv, 128))
+    if concentrated:
+        u = rng.standard_normal((1, heads_kv, 1, 128))
+        u /= np.linalg.norm(u, axis=-1, keepdims=True)
+        k = k + concentrated * u
+        q = q + concentrated * np.repeat(u, heads_q // heads_kv, axis=1)
+    return (O.round_to_bf16(q.astype(np.float32)), O.round_to_bf16(k.astype(np.float32)),
+            O.round_to_bf16(v.astype(np.float32)))
+
+
+@pytest.mark.parametrize("hq,hkv,n_q,n_kv,bounds,conc", [
+    (2, 2, 200, 300, [0, 100, 250, 300], 0.0),
+    (4, 2, 128, 128, [0, 64, 128], 0.0),
+    (1, 1, 64, 1000, [0, 390, 999, 1000], 6.0),
+    (2, 1, 333, 777, None, 3.0),
+])
+def test_chunk_bf16_matches_oracle(kvq, hq, hkv, n_q, n_kv, bounds, conc):
+    q, k, v = chunk_case(60 + n_kv, hq, hkv, n_q, n_kv, conc)
+    cache = kvq.pack(bf16_cuda(k), bf16_cuda(v), n_kv, "bf16")
+    for out_dtype in ("f32", "bf16"):
+        out, mass, path = kvq.attend(cache, bf16_cuda(q), out_dtype=out_dtype, region_bounds=bounds)
+        assert path == "chunk_bf16"
+        ref, ref_mass = O.attend(q, O.pack(k, v, n_kv, "bf16"), region_bounds=bounds)
+        err = O.rel_l2(to_np(out), ref)
+        assert err <= TOL_BF16, err
+        if bounds is not None:
+            np.testing.assert_allclose(to_np(mass), ref_mass, atol=TOL_MASS, rtol=0)
+
+
+def test_chunk_bf16_full_size_sampled_heads(kvq):
+    # the video chunk: 32 heads, 2,340 queries over 6,240 keys [1560 | 2340 | 2340]
+    bounds = list(synth.CHUNK_REGION_BOUNDS)
+    q, k, v = synth.chunk_inputs_torch(7, "cuda")
+    cache = kvq.pack(k, v, bounds[-1], "bf16")
+    out, mass, path = kvq.attend(cache, q, out_dtype="f32", region_bounds=bounds)
+    assert path == "chunk_bf16"
+    qn, kn, vn = to_np(q), to_np(k), to_np(v)
+    for h in (0, 17, 31):
+        ref, _, ref_mass = O.attention(qn[0, h], kn[0, h], vn[0, h], region_bounds=bounds)
+        assert O.rel_l2(to_np(out)[0, h], ref) <= TOL_BF16
+        np.testing.assert_allclose(to_np(mass)[0, h], ref_mass, atol=TOL_MASS, rtol=0)
+    np.testing.assert_allclose(to_np(mass).sum(-1), 1.0, atol=1e-4)
