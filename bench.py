@@ -438,12 +438,8 @@ def run_kvq(args):
     rows = {}
     if rank == 0 and not args.no_rows:
         rsteps = max(3, min(args.steps, 10))
-        rows["pack"] = row_pack(kvq, synth, torch, rsteps, 2, pk)
-        rows["small_d_fp32"] = row_small(kvq, synth, torch, rsteps, 2, pk)
-        rows["candidates_L131072_C256"] = row_candidates(kvq, synth, torch, rsteps, 2, pk, 131072, 256)
-        rows["candidates_L32768_C96"] = row_candidates(kvq, synth, torch, rsteps, 2, pk, 32768, 96)
-        rows["chunk_bf16"] = row_chunk(kvq, synth, torch, 3, 1, pk, "bf16")
-        rows["chunk_mxfp8"] = row_chunk(kvq, synth, torch, 3, 1, pk, "mxfp8")
+        for name, fn in ROWS.items():
+            rows[name] = fn(kvq, synth, torch, rsteps, 2, pk)
 
     if rank != 0:
         return
@@ -470,6 +466,29 @@ def run_kvq(args):
     print(json.dumps(line))
 
 
+ROWS = {
+    "pack": lambda kvq, synth, torch, st, w, pk: row_pack(kvq, synth, torch, st, w, pk),
+    "small_d_fp32": lambda kvq, synth, torch, st, w, pk: row_small(kvq, synth, torch, st, w, pk),
+    "candidates_L131072_C256": lambda kvq, synth, torch, st, w, pk:
+        row_candidates(kvq, synth, torch, st, w, pk, 131072, 256),
+    "candidates_L32768_C96": lambda kvq, synth, torch, st, w, pk:
+        row_candidates(kvq, synth, torch, st, w, pk, 32768, 96),
+    "chunk_bf16": lambda kvq, synth, torch, st, w, pk: row_chunk(kvq, synth, torch, st, w, pk, "bf16"),
+    "chunk_mxfp8": lambda kvq, synth, torch, st, w, pk:
+        row_chunk(kvq, synth, torch, st, w, pk, "mxfp8"),
+}
+
+
+def run_row(args):
+    """Time one hot-path row alone (for profiling); prints its JSON object."""
+    import torch
+
+    from quantized_sparse_kv_gb300 import kvq, synth
+    kvq.load_library()
+    res = ROWS[args.row](kvq, synth, torch, args.steps, args.warmup, peaks())
+    print(json.dumps({"row": args.row, **res}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -480,8 +499,11 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--case", choices=["full", "small"], default="full",
                     help="small: 16 sequences instead of 64 (for profiler captures)")
+    ap.add_argument("--row", choices=sorted(ROWS), help="time only this hot-path row")
     args = ap.parse_args()
-    if args.impl == "reference":
+    if args.row:
+        run_row(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_kvq(args)

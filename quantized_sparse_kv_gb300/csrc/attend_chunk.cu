@@ -154,6 +154,14 @@ __host__ __device__ constexpr uint32_t idesc_bf16(uint32_t b_mn_major) {
          ((128u >> 4) << 24);
 }
 
+// 2^x with the SFU (ex2.approx: about 2 ulp, flushes subnormal results to 0;
+// 2^-inf = 0). P is rounded to bf16 afterwards, far coarser than that.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ bool cta_aborted(ChunkSmem &sm) {
   return *reinterpret_cast<volatile int *>(&sm.abort_flag) != 0;
 }
@@ -317,28 +325,34 @@ __global__ void __launch_bounds__(256, 1)
       tc_fence_before();
       mbar_arrive(smem_u32(&sm.s_free[b]));
       const int valid = min(kBN, a.n_kv - j * kBN);
-      float mx = -CUDART_INF_F;
+      if (valid < kBN) {  // ragged last tile: keys past the end get -inf
 #pragma unroll
-      for (int i = 0; i < 128; ++i) {
-        s[i] = (i < valid) ? s[i] * a.scale_log2 : -CUDART_INF_F;
-        mx = fmaxf(mx, s[i]);
+        for (int i = 0; i < 128; ++i) s[i] = (i < valid) ? s[i] : -CUDART_INF_F;
       }
+      float mx0 = s[0], mx1 = s[1];
+#pragma unroll
+      for (int i = 2; i < 128; i += 2) {
+        mx0 = fmaxf(mx0, s[i]);
+        mx1 = fmaxf(mx1, s[i + 1]);
+      }
+      const float mx = fmaxf(mx0, mx1) * a.scale_log2;  // scale > 0 keeps the order
       // move the running max only when it grows by more than the threshold
       float factor = 1.0f;
-      const bool grow = mx > m_used + kRescaleThreshold;
-      if (grow) {
+      if (mx > m_used + kRescaleThreshold) {
         factor = exp2f(m_used - mx);  // 0 on the first tile
         m_used = mx;
       }
       l *= factor;
 #pragma unroll
       for (int k = 0; k < kMaxRegions; ++k) rsum[k] *= factor;
-      float ps = 0.0f;
+      const float neg_m = -m_used;
+      float ps4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
       for (int i = 0; i < 128; ++i) {
-        s[i] = exp2f(s[i] - m_used);
-        ps += s[i];
+        s[i] = fast_exp2(fmaf(s[i], a.scale_log2, neg_m));
+        ps4[i & 3] += s[i];
       }
+      const float ps = (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
       l += ps;
       // region sums: bounds inside this tile split the row
       const int t0 = j * kBN;
