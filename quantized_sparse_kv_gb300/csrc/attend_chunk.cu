@@ -6,20 +6,21 @@
 // chunk of 2,340 queries (6 latent frames) over 6,240 keys laid out [sink 1560
 // | recent 2340 | current 2340] (section "KV Cache 的实际作用"), no mask.
 //
-// One CTA per (128 query rows, query head); 8 warps:
-//   warp 0      TMA producer: Q once, then K and V tiles of 128 keys into a
-//               2-stage ring (128B-swizzled, 64-feature boxes);
-//   warp 1      allocates 512 TMEM columns and one lane issues the MMAs:
-//               S_j = Q K_j^T into TMEM buffer j % 2 (M=128, N=128, K=128 as 8
-//               k-steps of 16), then O += P_{j-1} V_{j-1} into TMEM O (V is the
-//               MN-major B operand);
-//   warps 4-7   softmax: thread r owns query row r (TMEM lane r). It loads its
-//               S row, releases the S buffer, exponentiates in the log2 domain
-//               against a running max that is only moved when it grows by more
-//               than 8 (then O and the sums are rescaled), accumulates the row
-//               sum and the region sums, and writes P (bf16, swizzled) to
-//               shared memory for the next PV MMA. At the end it reads O from
-//               TMEM, normalises and stores O and the region masses.
+// One CTA per (128 query rows, query head); 12 warps:
+//   warp 0      TMA producer: Q once, then 128-key K tiles (one slot: K is
+//               free once its QK MMA ends) and V tiles (two slots), all
+//               128B-swizzled in 64-feature boxes;
+//   warp 1      allocates 512 TMEM columns and one lane issues the MMAs;
+//   warps 4-7   softmax group A: key tiles 0, 2, 4, ...
+//   warps 8-11  softmax group B: key tiles 1, 3, 5, ...
+// Each softmax group g owns TMEM S_g (128 columns) and O_g (128 columns) and
+// a P buffer in shared memory; its chain per tile is S = Q K^T (MMA) ->
+// softmax (thread r owns query row r = TMEM lane r) -> O_g += P V (MMA, V as
+// the MN-major operand), and the two groups' chains interleave so the tensor
+// core works on one group while the other exponentiates. A group's running
+// max only moves when it grows by more than 8 (then O_g and its sums are
+// rescaled). At the end group A merges both (max, sum, O, region sums)
+// states of its rows, normalises and stores O and the region masses.
 // Every mbarrier wait is bounded; on timeout the CTA flags KVQ_DEV_TIMEOUT,
 // stops, drains its copies and MMAs and frees TMEM.
 #include <cuda.h>
@@ -35,7 +36,8 @@ namespace {
 constexpr int kBM = 128;          // query rows per CTA
 constexpr int kBN = 128;          // keys per tile
 constexpr int kDim = 128;         // head dim
-constexpr int kKvStages = 2;
+constexpr int kKStages = 1;   // K is released as soon as its QK MMA completes
+constexpr int kVStages = 2;
 constexpr int kMaxRegions = 4;
 constexpr uint32_t kTileBytes = kBN * kDim * 2;  // 32 KB, one K or V tile (bf16)
 constexpr uint32_t kHalfBytes = kTileBytes / 2;  // 16 KB: 128 rows x 64 features
@@ -43,13 +45,14 @@ constexpr float kRescaleThreshold = 8.0f;         // log2 units
 
 struct __align__(1024) ChunkSmem {
   uint8_t q[kTileBytes];                    // 2 x [128 rows][128 B], swizzled
-  uint8_t k[kKvStages][kTileBytes];
-  uint8_t v[kKvStages][kTileBytes];
-  uint8_t p[kTileBytes];                    // P (bf16) as the K-major A operand
+  uint8_t k[kKStages][kTileBytes];
+  uint8_t v[kVStages][kTileBytes];
+  uint8_t p[2][kTileBytes];                 // P (bf16) of group A and B, K-major A operand
+  float merge_m[kBM], merge_l[kBM];         // group B's row state for the final merge
+  float merge_r[kMaxRegions][kBM];
   uint64_t q_full;
-  uint64_t kv_full[kKvStages], kv_empty[kKvStages];
-  uint64_t s_full[2], s_free[2];
-  uint64_t p_full, o_done, mma_done;
+  uint64_t k_full[kKStages], k_empty[kKStages], v_full[kVStages], v_empty[kVStages];
+  uint64_t s_full[2], p_full[2], o_done[2], mma_done;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -185,7 +188,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t *>(&b);
 }
 
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(384, 1)
     chunk_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const ChunkArgs a) {
@@ -201,16 +204,19 @@ __global__ void __launch_bounds__(256, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&sm.q_full), 1);
-    for (int s = 0; s < kKvStages; ++s) {
-      mbar_init(smem_u32(&sm.kv_full[s]), 1);
-      mbar_init(smem_u32(&sm.kv_empty[s]), 1);
+    for (int s = 0; s < kKStages; ++s) {
+      mbar_init(smem_u32(&sm.k_full[s]), 1);
+      mbar_init(smem_u32(&sm.k_empty[s]), 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(smem_u32(&sm.s_full[b]), 1);
-      mbar_init(smem_u32(&sm.s_free[b]), 128);
+    for (int s = 0; s < kVStages; ++s) {
+      mbar_init(smem_u32(&sm.v_full[s]), 1);
+      mbar_init(smem_u32(&sm.v_empty[s]), 1);
     }
-    mbar_init(smem_u32(&sm.p_full), 128);
-    mbar_init(smem_u32(&sm.o_done), 1);
+    for (int g = 0; g < 2; ++g) {
+      mbar_init(smem_u32(&sm.s_full[g]), 1);
+      mbar_init(smem_u32(&sm.p_full[g]), 128);
+      mbar_init(smem_u32(&sm.o_done[g]), 1);
+    }
     mbar_init(smem_u32(&sm.mma_done), 1);
     sm.abort_flag = 0;
     fence_mbar_init();
@@ -225,8 +231,9 @@ __global__ void __launch_bounds__(256, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
-  const uint32_t t_s[2] = {tmem, tmem + 128u};
-  const uint32_t t_o = tmem + 256u;
+  // group g: S at columns 256g, O at 256g + 128
+  const uint32_t t_s[2] = {tmem, tmem + 256u};
+  const uint32_t t_o[2] = {tmem + 128u, tmem + 384u};
 
   if (warp == 0) {
     // ------------------------------------------------ TMA producer
@@ -235,108 +242,124 @@ __global__ void __launch_bounds__(256, 1)
       mbar_arrive_expect_tx(qb, kTileBytes);
       tma_load_3d(smem_u32(sm.q), &tm_q, 0, q0, hq, qb);
       tma_load_3d(smem_u32(sm.q) + kHalfBytes, &tm_q, 64, q0, hq, qb);
-      int j = 0;
-      for (; j < nt; ++j) {
-        const int st = j % kKvStages;
-        if (j >= kKvStages &&
-            !wait_or_abort(sm, smem_u32(&sm.kv_empty[st]), ((j / kKvStages) - 1) & 1, a.ctl))
-          break;
+      // K tile j then V tile j, each into its own ring; a slot is reused once
+      // the MMA reading it has completed
+      int kj = 0, vj = 0;
+      while (vj < nt) {
+        if (kj == vj) {
+          const int st = kj % kKStages, use = kj / kKStages;
+          if (use > 0 && !wait_or_abort(sm, smem_u32(&sm.k_empty[st]), (use - 1) & 1, a.ctl)) break;
+          if (cta_aborted(sm)) break;
+          const uint32_t fb = smem_u32(&sm.k_full[st]);
+          mbar_arrive_expect_tx(fb, kTileBytes);
+          tma_load_3d(smem_u32(sm.k[st]), &tm_k, 0, kj * kBN, hkv, fb);
+          tma_load_3d(smem_u32(sm.k[st]) + kHalfBytes, &tm_k, 64, kj * kBN, hkv, fb);
+          ++kj;
+        }
+        const int st = vj % kVStages, use = vj / kVStages;
+        if (use > 0 && !wait_or_abort(sm, smem_u32(&sm.v_empty[st]), (use - 1) & 1, a.ctl)) break;
         if (cta_aborted(sm)) break;
-        const uint32_t fb = smem_u32(&sm.kv_full[st]);
-        mbar_arrive_expect_tx(fb, 2 * kTileBytes);
-        tma_load_3d(smem_u32(sm.k[st]), &tm_k, 0, j * kBN, hkv, fb);
-        tma_load_3d(smem_u32(sm.k[st]) + kHalfBytes, &tm_k, 64, j * kBN, hkv, fb);
-        tma_load_3d(smem_u32(sm.v[st]), &tm_v, 0, j * kBN, hkv, fb);
-        tma_load_3d(smem_u32(sm.v[st]) + kHalfBytes, &tm_v, 64, j * kBN, hkv, fb);
+        const uint32_t fb = smem_u32(&sm.v_full[st]);
+        mbar_arrive_expect_tx(fb, kTileBytes);
+        tma_load_3d(smem_u32(sm.v[st]), &tm_v, 0, vj * kBN, hkv, fb);
+        tma_load_3d(smem_u32(sm.v[st]) + kHalfBytes, &tm_v, 64, vj * kBN, hkv, fb);
+        ++vj;
       }
-      // drain: the copies of the last stages must land before the CTA exits
+      // drain: the copies of the last slots must land before the CTA exits
       mbar_wait(qb, 0, 2000000000ull);
-      for (int d = (j > kKvStages ? j - kKvStages : 0); d < j; ++d)
-        mbar_wait(smem_u32(&sm.kv_full[d % kKvStages]), (d / kKvStages) & 1, 2000000000ull);
+      for (int d = (kj > kKStages ? kj - kKStages : 0); d < kj; ++d)
+        mbar_wait(smem_u32(&sm.k_full[d % kKStages]), (d / kKStages) & 1, 2000000000ull);
+      for (int d = (vj > kVStages ? vj - kVStages : 0); d < vj; ++d)
+        mbar_wait(smem_u32(&sm.v_full[d % kVStages]), (d / kVStages) & 1, 2000000000ull);
     }
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t id_qk = idesc_bf16(0), id_pv = idesc_bf16(1);
-      const uint32_t qa = smem_u32(sm.q), pa = smem_u32(sm.p);
+      const uint32_t qa = smem_u32(sm.q);
       bool ok = wait_or_abort(sm, smem_u32(&sm.q_full), 0, a.ctl);
-      auto issue_pv = [&](int i) -> bool {
-        if (!wait_or_abort(sm, smem_u32(&sm.p_full), i & 1, a.ctl)) return false;
-        tc_fence_after();
-        const uint32_t va = smem_u32(sm.v[i % kKvStages]);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t ad = smem_desc(pa + (kk >> 2) * kHalfBytes + (kk & 3) * 32u, 16, 1024);
-          const uint64_t bd = smem_desc(va + kk * 2048u, kHalfBytes, 1024);
-          tc_mma_f16(t_o, ad, bd, id_pv, (i > 0 || kk > 0) ? 1u : 0u);
-        }
-        tc_commit(smem_u32(&sm.o_done));
-        tc_commit(smem_u32(&sm.kv_empty[i % kKvStages]));
-        return true;
-      };
-      for (int j = 0; ok && j < nt; ++j) {
-        const int st = j % kKvStages, b = j & 1;
-        if (!wait_or_abort(sm, smem_u32(&sm.kv_full[st]), (j / kKvStages) & 1, a.ctl)) break;
-        if (j >= 2 && !wait_or_abort(sm, smem_u32(&sm.s_free[b]), ((j >> 1) - 1) & 1, a.ctl))
-          break;
+      // S_j = Q K_j^T into group j % 2's S
+      auto issue_s = [&](int j) -> bool {
+        const int st = j % kKStages, g = j & 1;
+        if (!wait_or_abort(sm, smem_u32(&sm.k_full[st]), (j / kKStages) & 1, a.ctl)) return false;
         tc_fence_after();
         const uint32_t ka = smem_u32(sm.k[st]);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32u;
-          tc_mma_f16(t_s[b], smem_desc(qa + off, 16, 1024), smem_desc(ka + off, 16, 1024), id_qk,
+          tc_mma_f16(t_s[g], smem_desc(qa + off, 16, 1024), smem_desc(ka + off, 16, 1024), id_qk,
                      kk > 0 ? 1u : 0u);
         }
-        tc_commit(smem_u32(&sm.s_full[b]));
-        if (j >= 1 && !issue_pv(j - 1)) {
+        tc_commit(smem_u32(&sm.s_full[g]));
+        tc_commit(smem_u32(&sm.k_empty[st]));
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      if (ok && nt > 1) ok = issue_s(1);
+      for (int j = 0; ok && j < nt; ++j) {
+        const int st = j % kVStages, g = j & 1, i = j >> 1;
+        // O_g += P_g V_j once group g has written P for tile j
+        if (!wait_or_abort(sm, smem_u32(&sm.p_full[g]), i & 1, a.ctl) ||
+            !wait_or_abort(sm, smem_u32(&sm.v_full[st]), (j / kVStages) & 1, a.ctl)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t pa = smem_u32(sm.p[g]), va = smem_u32(sm.v[st]);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t ad = smem_desc(pa + (kk >> 2) * kHalfBytes + (kk & 3) * 32u, 16, 1024);
+          const uint64_t bd = smem_desc(va + kk * 2048u, kHalfBytes, 1024);
+          tc_mma_f16(t_o[g], ad, bd, id_pv, (i > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc_commit(smem_u32(&sm.o_done[g]));
+        tc_commit(smem_u32(&sm.v_empty[st]));
+        // group g has read S for tile j (it wrote P after), so S_g can take tile j + 2
+        if (j + 2 < nt && !issue_s(j + 2)) {
           ok = false;
           break;
         }
       }
-      if (ok && !cta_aborted(sm)) issue_pv(nt - 1);
       // all MMAs of this CTA complete before TMEM is released
       tc_commit(smem_u32(&sm.mma_done));
       mbar_wait(smem_u32(&sm.mma_done), 0, 2000000000ull);
     }
   } else if (warp >= 4) {
-    // ------------------------------------------------ softmax + epilogue
-    const int quad = warp - 4;               // TMEM lanes 32*quad .. +31
+    // ------------------------------------------------ softmax groups
+    const int g = (warp - 4) >> 2;           // 0: even tiles, 1: odd tiles
+    const int quad = warp & 3;               // TMEM lanes 32*quad .. +31
     const int row = quad * 32 + lane;        // query row within the tile
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const int my_tiles = (nt - g + 1) >> 1;  // tiles g, g+2, ...
     float m_used = -CUDART_INF_F, l = 0.0f;
     float rsum[kMaxRegions] = {0.0f, 0.0f, 0.0f, 0.0f};
     bool ok = true;
-    for (int j = 0; j < nt; ++j) {
-      const int b = j & 1;
-      if (!wait_or_abort(sm, smem_u32(&sm.s_full[b]), (j >> 1) & 1, a.ctl)) {
+    for (int i = 0; i < my_tiles; ++i) {
+      const int j = 2 * i + g;
+      if (!wait_or_abort(sm, smem_u32(&sm.s_full[g]), i & 1, a.ctl)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      float s[128];
-#pragma unroll
+      const int valid = min(kBN, a.n_kv - j * kBN);
+      // pass 1: row max of the raw scores
+      float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F;
+#pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         float v[32];
-        tmem_ld32(t_s[b] + lane_off + 32u * c, v);
+        tmem_ld32(t_s[g] + lane_off + 32u * c, v);
+        tmem_wait_ld();
+        if (valid < kBN) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) s[32 * c + i] = v[i];
-      }
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(smem_u32(&sm.s_free[b]));
-      const int valid = min(kBN, a.n_kv - j * kBN);
-      if (valid < kBN) {  // ragged last tile: keys past the end get -inf
+          for (int e = 0; e < 32; ++e) v[e] = (32 * c + e < valid) ? v[e] : -CUDART_INF_F;
+        }
 #pragma unroll
-        for (int i = 0; i < 128; ++i) s[i] = (i < valid) ? s[i] : -CUDART_INF_F;
-      }
-      float mx0 = s[0], mx1 = s[1];
-#pragma unroll
-      for (int i = 2; i < 128; i += 2) {
-        mx0 = fmaxf(mx0, s[i]);
-        mx1 = fmaxf(mx1, s[i + 1]);
+        for (int e = 0; e < 32; e += 2) {
+          mx0 = fmaxf(mx0, v[e]);
+          mx1 = fmaxf(mx1, v[e + 1]);
+        }
       }
       const float mx = fmaxf(mx0, mx1) * a.scale_log2;  // scale > 0 keeps the order
-      // move the running max only when it grows by more than the threshold
       float factor = 1.0f;
       if (mx > m_used + kRescaleThreshold) {
         factor = exp2f(m_used - mx);  // 0 on the first tile
@@ -345,94 +368,134 @@ __global__ void __launch_bounds__(256, 1)
       l *= factor;
 #pragma unroll
       for (int k = 0; k < kMaxRegions; ++k) rsum[k] *= factor;
-      const float neg_m = -m_used;
-      float ps4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-      for (int i = 0; i < 128; ++i) {
-        s[i] = fast_exp2(fmaf(s[i], a.scale_log2, neg_m));
-        ps4[i & 3] += s[i];
-      }
-      const float ps = (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
-      l += ps;
-      // region sums: bounds inside this tile split the row
-      const int t0 = j * kBN;
-      for (int k = 0; k < a.reg.n && k < kMaxRegions; ++k) {
-        const int lo = a.reg.b[k] - t0, hi = a.reg.b[k + 1] - t0;
-        if (hi <= 0 || lo >= kBN) continue;
-        if (lo <= 0 && hi >= kBN) {
-          rsum[k] += ps;
-          continue;
-        }
-        float part = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 128; ++i) part += (i >= lo && i < hi) ? s[i] : 0.0f;
-        rsum[k] += part;
-      }
-      // PV_{j-1} must be complete before P is overwritten or O is rescaled
-      if (j >= 1 && !wait_or_abort(sm, smem_u32(&sm.o_done), (j - 1) & 1, a.ctl)) {
+      // O_g += P V of the previous tile must be done before P_g is rewritten
+      // or O_g is rescaled
+      if (i >= 1 && !wait_or_abort(sm, smem_u32(&sm.o_done[g]), (i - 1) & 1, a.ctl)) {
         ok = false;
         break;
       }
-      if (j >= 1 && __any_sync(0xffffffffu, factor != 1.0f)) {
+      if (i >= 1 && __any_sync(0xffffffffu, factor != 1.0f)) {
         tc_fence_after();
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           float v[32];
-          tmem_ld32(t_o + lane_off + 32u * c, v);
+          tmem_ld32(t_o[g] + lane_off + 32u * c, v);
           tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] *= factor;
-          tmem_st32(t_o + lane_off + 32u * c, v);
+          for (int e = 0; e < 32; ++e) v[e] *= factor;
+          tmem_st32(t_o[g] + lane_off + 32u * c, v);
         }
         tmem_wait_st();
       }
-      // P row -> shared memory, bf16, 128B-swizzled K-major layout
+      // pass 2: P = 2^(s * scale - m), row and region sums, P -> shared memory
+      const float neg_m = -m_used;
+      const int t0 = j * kBN;
+      float ps = 0.0f;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        float v[32];
+        tmem_ld32(t_s[g] + lane_off + 32u * c, v);
+        tmem_wait_ld();
+        float ps4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        if (valid == kBN) {
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const int half = c >> 3, chunk = c & 7;
-        uint4 w;
-        w.x = pack_bf16x2(s[8 * c + 0], s[8 * c + 1]);
-        w.y = pack_bf16x2(s[8 * c + 2], s[8 * c + 3]);
-        w.z = pack_bf16x2(s[8 * c + 4], s[8 * c + 5]);
-        w.w = pack_bf16x2(s[8 * c + 6], s[8 * c + 7]);
-        *reinterpret_cast<uint4 *>(sm.p + half * kHalfBytes + swz(row, chunk)) = w;
+          for (int e = 0; e < 32; ++e) {
+            v[e] = fast_exp2(fmaf(v[e], a.scale_log2, neg_m));
+            ps4[e & 3] += v[e];
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            v[e] = (32 * c + e < valid) ? fast_exp2(fmaf(v[e], a.scale_log2, neg_m)) : 0.0f;
+            ps4[e & 3] += v[e];
+          }
+        }
+        const float cs = (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
+        ps += cs;
+        for (int k = 0; k < a.reg.n && k < kMaxRegions; ++k) {
+          const int lo = a.reg.b[k] - t0 - 32 * c, hi = a.reg.b[k + 1] - t0 - 32 * c;
+          if (hi <= 0 || lo >= 32) continue;
+          if (lo <= 0 && hi >= 32) {
+            rsum[k] += cs;
+            continue;
+          }
+          float part = 0.0f;
+#pragma unroll
+          for (int e = 0; e < 32; ++e) part += (e >= lo && e < hi) ? v[e] : 0.0f;
+          rsum[k] += part;
+        }
+#pragma unroll
+        for (int q8 = 0; q8 < 4; ++q8) {
+          const int chunk = 4 * c + q8;  // 16-byte chunk of the row, 0..15
+          uint4 w;
+          w.x = pack_bf16x2(v[8 * q8 + 0], v[8 * q8 + 1]);
+          w.y = pack_bf16x2(v[8 * q8 + 2], v[8 * q8 + 3]);
+          w.z = pack_bf16x2(v[8 * q8 + 4], v[8 * q8 + 5]);
+          w.w = pack_bf16x2(v[8 * q8 + 6], v[8 * q8 + 7]);
+          *reinterpret_cast<uint4 *>(sm.p[g] + (chunk >> 3) * kHalfBytes + swz(row, chunk & 7)) = w;
+        }
       }
+      l += ps;
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       tc_fence_before();
-      mbar_arrive(smem_u32(&sm.p_full));
+      mbar_arrive(smem_u32(&sm.p_full[g]));
     }
-    // ---- epilogue: O / l and region masses
-    if (ok && wait_or_abort(sm, smem_u32(&sm.o_done), (nt - 1) & 1, a.ctl)) {
+    // ---- epilogue: group B hands its row state to group A, A merges and stores
+    const bool last_ok =
+        ok && my_tiles > 0 &&
+        wait_or_abort(sm, smem_u32(&sm.o_done[g]), (my_tiles - 1) & 1, a.ctl);
+    if (g == 1) {
+      sm.merge_m[row] = last_ok ? m_used : -CUDART_INF_F;
+      sm.merge_l[row] = last_ok ? l : 0.0f;
+#pragma unroll
+      for (int k = 0; k < kMaxRegions; ++k) sm.merge_r[k][row] = last_ok ? rsum[k] : 0.0f;
+    }
+    tc_fence_before();
+    asm volatile("bar.sync 2, 256;" ::: "memory");
+    const int tiles_b = nt >> 1;
+    if (g == 0 && last_ok &&
+        (tiles_b == 0 ||
+         wait_or_abort(sm, smem_u32(&sm.o_done[1]), (tiles_b - 1) & 1, a.ctl))) {
       tc_fence_after();
+      const float mb = sm.merge_m[row];
+      const bool have_b = nt > 1;  // group B processed at least one tile
+      const float mm = fmaxf(m_used, mb);
+      const float fa = exp2f(m_used - mm);
+      const float fb = have_b ? exp2f(mb - mm) : 0.0f;
+      const float lt = fa * l + fb * sm.merge_l[row];
+      const float inv = 1.0f / lt;
       const int qrow = q0 + row;
-      const float inv = 1.0f / l;
       const long obase = (static_cast<long>(hq) * a.n_q + qrow) * kDim;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        float v[32];
-        tmem_ld32(t_o + lane_off + 32u * c, v);
+        float va[32], vb[32];
+        tmem_ld32(t_o[0] + lane_off + 32u * c, va);
+        if (have_b) tmem_ld32(t_o[1] + lane_off + 32u * c, vb);
         tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) va[e] = (fa * va[e] + (have_b ? fb * vb[e] : 0.0f)) * inv;
         if (qrow < a.n_q) {
           if (a.out_dtype == KVQ_F32) {
             float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(a.out) + obase + 32 * c);
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              o[i] = make_float4(v[4 * i] * inv, v[4 * i + 1] * inv, v[4 * i + 2] * inv,
-                                 v[4 * i + 3] * inv);
+            for (int e = 0; e < 8; ++e)
+              o[e] = make_float4(va[4 * e], va[4 * e + 1], va[4 * e + 2], va[4 * e + 3]);
           } else {
-            uint4 *o = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.out) + obase + 32 * c);
+            uint4 *o =
+                reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.out) + obase + 32 * c);
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              o[i] = make_uint4(pack_bf16x2(v[8 * i] * inv, v[8 * i + 1] * inv),
-                                pack_bf16x2(v[8 * i + 2] * inv, v[8 * i + 3] * inv),
-                                pack_bf16x2(v[8 * i + 4] * inv, v[8 * i + 5] * inv),
-                                pack_bf16x2(v[8 * i + 6] * inv, v[8 * i + 7] * inv));
+            for (int e = 0; e < 4; ++e)
+              o[e] = make_uint4(pack_bf16x2(va[8 * e], va[8 * e + 1]),
+                                pack_bf16x2(va[8 * e + 2], va[8 * e + 3]),
+                                pack_bf16x2(va[8 * e + 4], va[8 * e + 5]),
+                                pack_bf16x2(va[8 * e + 6], va[8 * e + 7]));
           }
         }
       }
       if (a.mass && qrow < a.n_q)
-        for (int k = 0; k < a.reg.n; ++k)
-          a.mass[(static_cast<long>(hq) * a.n_q + qrow) * a.reg.n + k] = rsum[k] * inv;
+        for (int k = 0; k < a.reg.n && k < kMaxRegions; ++k)
+          a.mass[(static_cast<long>(hq) * a.n_q + qrow) * a.reg.n + k] =
+              (fa * rsum[k] + fb * sm.merge_r[k][row]) * inv;
     }
   }
   tc_fence_before();
@@ -512,7 +575,7 @@ int launch_attend_chunk(const kvq_cache &c, const void *q, int Hq, int n_q, floa
   cudaFuncSetAttribute(chunk_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        static_cast<int>(smem));
   dim3 grid((n_q + kBM - 1) / kBM, c.batch * Hq);
-  chunk_bf16_kernel<<<grid, 256, smem, s>>>(tq, tk, tv, a);
+  chunk_bf16_kernel<<<grid, 384, smem, s>>>(tq, tk, tv, a);
   return 1;
 }
 
