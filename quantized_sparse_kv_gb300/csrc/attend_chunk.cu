@@ -136,6 +136,19 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
+
+// Registers written by tcgen05.ld hold valid data only after tcgen05.wait::ld;
+// this empty asm, placed after the wait, keeps the compiler from moving any
+// use of them above it.
+__device__ __forceinline__ void reg_fence(float (&v)[32]) {
+  asm volatile(""
+               : "+f"(v[0]), "+f"(v[1]), "+f"(v[2]), "+f"(v[3]), "+f"(v[4]), "+f"(v[5]),
+                 "+f"(v[6]), "+f"(v[7]), "+f"(v[8]), "+f"(v[9]), "+f"(v[10]), "+f"(v[11]),
+                 "+f"(v[12]), "+f"(v[13]), "+f"(v[14]), "+f"(v[15]), "+f"(v[16]), "+f"(v[17]),
+                 "+f"(v[18]), "+f"(v[19]), "+f"(v[20]), "+f"(v[21]), "+f"(v[22]), "+f"(v[23]),
+                 "+f"(v[24]), "+f"(v[25]), "+f"(v[26]), "+f"(v[27]), "+f"(v[28]), "+f"(v[29]),
+                 "+f"(v[30]), "+f"(v[31])::"memory");
+}
 __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -349,6 +362,7 @@ __global__ void __launch_bounds__(384, 1)
         float v[32];
         tmem_ld32(t_s[g] + lane_off + 32u * c, v);
         tmem_wait_ld();
+        reg_fence(v);
         if (valid < kBN) {
 #pragma unroll
           for (int e = 0; e < 32; ++e) v[e] = (32 * c + e < valid) ? v[e] : -CUDART_INF_F;
@@ -381,6 +395,7 @@ __global__ void __launch_bounds__(384, 1)
           float v[32];
           tmem_ld32(t_o[g] + lane_off + 32u * c, v);
           tmem_wait_ld();
+          reg_fence(v);
 #pragma unroll
           for (int e = 0; e < 32; ++e) v[e] *= factor;
           tmem_st32(t_o[g] + lane_off + 32u * c, v);
@@ -396,6 +411,7 @@ __global__ void __launch_bounds__(384, 1)
         float v[32];
         tmem_ld32(t_s[g] + lane_off + 32u * c, v);
         tmem_wait_ld();
+        reg_fence(v);
         float ps4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
         if (valid == kBN) {
 #pragma unroll
@@ -472,6 +488,8 @@ __global__ void __launch_bounds__(384, 1)
         tmem_ld32(t_o[0] + lane_off + 32u * c, va);
         if (have_b) tmem_ld32(t_o[1] + lane_off + 32u * c, vb);
         tmem_wait_ld();
+        reg_fence(va);
+        if (have_b) reg_fence(vb);
 #pragma unroll
         for (int e = 0; e < 32; ++e) va[e] = (fa * va[e] + (have_b ? fb * vb[e] : 0.0f)) * inv;
         if (qrow < a.n_q) {
