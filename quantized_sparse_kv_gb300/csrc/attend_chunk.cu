@@ -26,6 +26,7 @@
 #include <cuda.h>
 #include <math_constants.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "kvq_internal.h"
@@ -524,6 +525,59 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
+// ------------------------------------------------------------------ MXFP8 Q/K prologue
+// The MXFP8 path (Catnip study, section "Q/K 与 probability quantization 的影响":
+// E4M3 elements with an E8M0 scale per 32 features) rounds Q to MXFP8 with the
+// same rule kv_pack applies to the K window, and expands both to bf16. Every
+// MXFP8 value (at most 4 significant bits times a power of two) is exact in
+// bf16 unless its exponent falls below bf16's subnormal range, so the bf16
+// tensor-core products equal the E4M3 products and the fp32 accumulation is
+// the same.
+
+// 2^(e - 127) as an exact float for an E8M0 byte e (e = 255, NaN, is not produced by kv_pack).
+__device__ __forceinline__ float e8m0_scale(uint32_t e) {
+  return e ? __uint_as_float(e << 23) : __uint_as_float(0x00400000u);  // 2^-127 is subnormal
+}
+
+// K window: E4M3 codes + E8M0 block bytes -> bf16, 16 codes (one half block)
+// per thread. cvt from e4m3x2 to f16x2 is exact; the power of two is exact.
+__global__ void mxfp8_to_bf16_kernel(const uint8_t *__restrict__ codes,
+                                     const uint8_t *__restrict__ e8m0, long n16,
+                                     __nv_bfloat16 *__restrict__ out) {
+  for (long i = blockIdx.x * static_cast<long>(blockDim.x) + threadIdx.x; i < n16;
+       i += static_cast<long>(gridDim.x) * blockDim.x) {
+    const uint4 c = reinterpret_cast<const uint4 *>(codes)[i];
+    const float sc = e8m0_scale(e8m0[i >> 1]);
+    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+    uint32_t o[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const unsigned short pair = static_cast<unsigned short>(w[k] >> (16 * h));
+        uint32_t f16x2;
+        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(f16x2) : "h"(pair));
+        const float2 f = __half22float2(*reinterpret_cast<__half2 *>(&f16x2));
+        __nv_bfloat162 b = __floats2bfloat162_rn(f.x * sc, f.y * sc);
+        o[2 * k + h] = *reinterpret_cast<uint32_t *>(&b);
+      }
+    }
+    uint4 *dst = reinterpret_cast<uint4 *>(out) + 2 * i;
+    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+  }
+}
+
+// Q: bf16 -> MXFP8 rounding -> bf16, one warp per 32-feature block.
+__global__ void __launch_bounds__(256) q_mxfp8_round_kernel(const __nv_bfloat16 *__restrict__ q,
+                                                            long blocks,
+                                                            __nv_bfloat16 *__restrict__ out) {
+  const long task = static_cast<long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  if (task >= blocks) return;
+  const long i = task * 32 + (threadIdx.x & 31);
+  out[i] = __float2bfloat16_rn(mxfp8_round_warp(__bfloat162float(q[i])));
+}
+
 // ------------------------------------------------------------------ host side
 using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
@@ -561,20 +615,44 @@ bool make_map(CUtensorMap *m, const void *ptr, int rows, int heads) {
 }  // namespace
 
 bool chunk_supported(const kvq_cache &c, int q_dtype, int Hq, int n_q) {
-  return c.recent == c.n_tokens && c.head_dim == kDim && c.kwin_dtype == KVQ_BF16 &&
-         c.vwin_dtype == KVQ_BF16 && q_dtype == KVQ_BF16 && n_q >= 64 && Hq % c.kv_heads == 0 &&
-         encoder() != nullptr;
+  return c.recent == c.n_tokens && c.head_dim == kDim &&
+         (c.kwin_dtype == KVQ_BF16 || c.kwin_dtype == KVQ_MXFP8) && c.vwin_dtype == KVQ_BF16 &&
+         q_dtype == KVQ_BF16 && n_q >= 64 && Hq % c.kv_heads == 0 && encoder() != nullptr;
 }
 
-size_t chunk_workspace_bytes(const kvq_cache &, int, int) { return 0; }
+// MXFP8: bf16 copies of K and of the MXFP8-rounded Q, each 256-byte aligned.
+size_t chunk_workspace_bytes(const kvq_cache &c, int Hq, int n_q) {
+  if (c.kwin_dtype != KVQ_MXFP8) return 0;
+  const size_t kb = static_cast<size_t>(c.batch) * c.kv_heads * c.n_tokens * kDim * 2;
+  const size_t qb = static_cast<size_t>(c.batch) * Hq * n_q * kDim * 2;
+  return ((kb + 255) & ~size_t(255)) + qb;
+}
 
 int chunk_max_regions() { return kMaxRegions; }
 
 int launch_attend_chunk(const kvq_cache &c, const void *q, int Hq, int n_q, float scale_log2,
                         void *out, int out_dtype, const int32_t *bounds, int n_regions,
-                        float *mass, void *, const KernelCtl &ctl, cudaStream_t s) {
+                        float *mass, void *ws, const KernelCtl &ctl, cudaStream_t s) {
+  int launches = 1;
+  const void *kptr = c.k_window, *qptr = q;
+  if (c.kwin_dtype == KVQ_MXFP8) {
+    const long kn = static_cast<long>(c.batch) * c.kv_heads * c.n_tokens * kDim;
+    const long qn = static_cast<long>(c.batch) * Hq * n_q * kDim;
+    __nv_bfloat16 *kb = static_cast<__nv_bfloat16 *>(ws);
+    __nv_bfloat16 *qb = reinterpret_cast<__nv_bfloat16 *>(static_cast<uint8_t *>(ws) +
+                                                          ((kn * 2 + 255) & ~255L));
+    mxfp8_to_bf16_kernel<<<static_cast<unsigned>(std::min<long>((kn / 16 + 255) / 256, 1L << 20)),
+                           256, 0, s>>>(static_cast<const uint8_t *>(c.k_window), c.k_window_e8m0,
+                                        kn / 16, kb);
+    q_mxfp8_round_kernel<<<static_cast<unsigned>((qn / 32 + 7) / 8), 256, 0, s>>>(
+        static_cast<const __nv_bfloat16 *>(q), qn / 32, qb);
+    kptr = kb;
+    qptr = qb;
+    launches += 2;
+  }
   CUtensorMap tq, tk, tv;
-  if (!make_map(&tq, q, n_q, c.batch * Hq) || !make_map(&tk, c.k_window, c.n_tokens, c.batch * c.kv_heads) ||
+  if (!make_map(&tq, qptr, n_q, c.batch * Hq) ||
+      !make_map(&tk, kptr, c.n_tokens, c.batch * c.kv_heads) ||
       !make_map(&tv, c.v_window, c.n_tokens, c.batch * c.kv_heads))
     return -1;
   ChunkArgs a;
@@ -594,7 +672,7 @@ int launch_attend_chunk(const kvq_cache &c, const void *q, int Hq, int n_q, floa
                        static_cast<int>(smem));
   dim3 grid((n_q + kBM - 1) / kBM, c.batch * Hq);
   chunk_bf16_kernel<<<grid, 384, smem, s>>>(tq, tk, tv, a);
-  return 1;
+  return launches;
 }
 
 }  // namespace kvq

@@ -53,21 +53,6 @@ __device__ __forceinline__ float window_value(const void *w, int dtype, long i) 
                           : bf16_to_f32(static_cast<const uint16_t *>(w)[i]);
 }
 
-// Round x to MXFP8 inside a warp (lane = position in the 32-block) and return
-// the dequantized value: the same rule kv_pack applies to an MXFP8 K window.
-__device__ __forceinline__ float mxfp8_round_warp(float x) {
-  const float amax = warp_max(fabsf(x));
-  int e = -127;
-  if (amax > 0.0f) {
-    int ex;
-    frexpf(amax, &ex);
-    e = max(-127, min(127, ex - 1 - 8));
-  }
-  const uint8_t c =
-      static_cast<uint8_t>(__nv_cvt_float_to_fp8(ldexpf(x, -e), __NV_SATFINITE, __NV_E4M3));
-  return mxfp8_value(c, static_cast<uint8_t>(e + 127));
-}
-
 template <int DPL>
 __global__ void __launch_bounds__(kWarps * 32) generic_attend_kernel(GenericArgs a) {
   constexpr int D = DPL * 32;

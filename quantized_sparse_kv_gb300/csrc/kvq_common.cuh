@@ -4,6 +4,7 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -148,6 +149,21 @@ __device__ __forceinline__ float mxfp8_value(uint8_t code, uint8_t e8m0) {
                        : ldexpf(static_cast<float>(8 + m), e - 10);
   if ((code & 0x7F) == 0x7F) mag = __int_as_float(0x7fc00000);
   return ldexpf((code & 0x80) ? -mag : mag, static_cast<int>(e8m0) - 127);
+}
+
+// Round x to MXFP8 inside a warp (lane = position in the 32-block) and return
+// the dequantized value: the same rule kv_pack applies to an MXFP8 K window.
+__device__ __forceinline__ float mxfp8_round_warp(float x) {
+  const float amax = warp_max(fabsf(x));
+  int e = -127;
+  if (amax > 0.0f) {
+    int ex;
+    frexpf(amax, &ex);
+    e = max(-127, min(127, ex - 1 - 8));
+  }
+  const uint8_t c =
+      static_cast<uint8_t>(__nv_cvt_float_to_fp8(ldexpf(x, -e), __NV_SATFINITE, __NV_E4M3));
+  return mxfp8_value(c, static_cast<uint8_t>(e + 127));
 }
 
 }  // namespace kvq

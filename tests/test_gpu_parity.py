@@ -313,3 +313,39 @@ def test_chunk_bf16_full_size_sampled_heads(kvq):
         assert O.rel_l2(to_np(out)[0, h], ref) <= TOL_BF16
         np.testing.assert_allclose(to_np(mass)[0, h], ref_mass, atol=TOL_MASS, rtol=0)
     np.testing.assert_allclose(to_np(mass).sum(-1), 1.0, atol=1e-4)
+
+
+@pytest.mark.parametrize("hq,hkv,n_q,n_kv,bounds", [
+    (2, 2, 200, 300, [0, 100, 250, 300]),
+    (4, 2, 130, 1000, [0, 390, 999, 1000]),
+])
+def test_chunk_mxfp8_matches_oracle(kvq, hq, hkv, n_q, n_kv, bounds):
+    q, k, v = chunk_case(80 + n_kv, hq, hkv, n_q, n_kv, 2.0)
+    cache = kvq.pack(bf16_cuda(k), bf16_cuda(v), n_kv, "mxfp8", "bf16")
+    out, mass, path = kvq.attend(cache, bf16_cuda(q), out_dtype="f32", region_bounds=bounds)
+    assert path == "chunk_mxfp8"
+    # oracle: Q and K rounded to MXFP8 (E4M3 + E8M0 per 32 features), V as given
+    qc, qs = O.mxfp8_quantize(q.astype(np.float64))
+    kc, ks = O.mxfp8_quantize(k.astype(np.float64))
+    qh, kh = O.mxfp8_dequantize(qc, qs), O.mxfp8_dequantize(kc, ks)
+    for h in range(hq):
+        ref, p_mx, ref_mass = O.attention(qh[0, h], kh[0, h // (hq // hkv)], v[0, h // (hq // hkv)],
+                                          region_bounds=bounds)
+        assert O.rel_l2(to_np(out)[0, h], ref) <= TOL_BF16
+        np.testing.assert_allclose(to_np(mass)[0, h], ref_mass, atol=TOL_MASS, rtol=0)
+    # the generic fp32 kernel, which applies the same rounding, agrees too
+    cache_g = kvq.pack(bf16_cuda(k), bf16_cuda(v), n_kv, "mxfp8", "bf16")
+    out_g, _, path_g = kvq.attend(cache_g, bf16_cuda(q[:, :, :63]), out_dtype="f32")
+    assert path_g == "generic"
+    assert O.rel_l2(to_np(out_g), to_np(out)[:, :, :63]) <= TOL_BF16
+
+
+def test_chunk_mxfp8_changes_probabilities_little(kvq):
+    # reported, not a parity pin: total variation of MXFP8 vs bf16 softmax rows
+    q, k, v = chunk_case(90, 1, 1, 64, 512, 0.0)
+    qc, qs = O.mxfp8_quantize(q.astype(np.float64))
+    kc, ks = O.mxfp8_quantize(k.astype(np.float64))
+    _, p_mx, _ = O.attention(O.mxfp8_dequantize(qc, qs)[0, 0], O.mxfp8_dequantize(kc, ks)[0, 0], v[0, 0])
+    _, p_bf, _ = O.attention(q[0, 0], k[0, 0], v[0, 0])
+    tv = O.probability_tv(p_mx, p_bf)
+    assert np.median(tv) < 0.05
