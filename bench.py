@@ -143,12 +143,15 @@ class ClockSampler:
 def time_steps(fn, steps, warmup, flush=None):
     """Mean ms per call with CUDA events on the current stream. Without
     ``flush`` the calls run back to back inside one event pair; with it,
-    each call is bracketed by its own events and the flush runs outside them."""
+    each call is bracketed by its own events and the flush runs outside them.
+    The stream is first held by a short spin kernel while every call, flush
+    and event is enqueued, so the GPU never waits for the host inside a pair."""
     import torch
     for _ in range(warmup):
         fn()
     torch.cuda.synchronize()
     s = torch.cuda.current_stream()
+    torch.cuda._sleep(int(2e6 + 4e5 * steps))  # about a millisecond, plus per-step room
     if flush is None:
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(s)
@@ -157,24 +160,28 @@ def time_steps(fn, steps, warmup, flush=None):
         e1.record(s)
         torch.cuda.synchronize()
         return e0.elapsed_time(e1) / steps
-    total = 0.0
+    pairs = []
     for _ in range(steps):
         flush()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(s)
         fn()
         e1.record(s)
-        torch.cuda.synchronize()
-        total += e0.elapsed_time(e1)
-    return total / steps
+        pairs.append((e0, e1))
+    torch.cuda.synchronize()
+    return sum(e0.elapsed_time(e1) for e0, e1 in pairs) / steps
 
 
 def make_flush():
+    """Evict L2 between timed calls by READING a buffer of twice its size: a
+    write-based flush would leave L2 full of dirty lines whose write-back
+    then lands inside the next timed call."""
     import torch
-    buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda")
+    buf = torch.ones(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda")
+    sink = torch.empty((), dtype=torch.float32, device="cuda")
 
     def flush():
-        buf.fill_(1.0)
+        torch.amax(buf, dim=0, out=sink)
     return flush
 
 

@@ -6,7 +6,7 @@
 // the gathered rows come from the int4 cache (dequantized on the fly) or from
 // the float window.
 //
-// Layout: one CTA per (query row, query head, sequence), 8 warps. Warp w
+// Layout (any head dim): one CTA per (query row, query head, sequence), 8 warps. Warp w
 // takes candidates w, w+8, ...; lane l owns features [l*F, (l+1)*F) with
 // F = D/32, so one candidate's K codes, K scales, V codes and V scales are
 // read as contiguous warp-wide segments. Each warp keeps an online softmax in
@@ -151,6 +151,176 @@ __global__ void __launch_bounds__(kWarps * 32) cand_kernel(const CandArgs a) {
   }
 }
 
+// Head dim 128 (4 features per lane): the row's index list is staged in shared
+// memory, and each warp gathers kUnroll candidates per step with independent
+// vector loads, so many rows are in flight per SM; the kUnroll dot products
+// are reduced together and enter the online softmax as one update.
+constexpr int kUnroll = 4;
+
+__global__ void __launch_bounds__(kWarps * 32) cand128_kernel(const CandArgs a) {
+  constexpr int D = 128;
+  __shared__ float red_o[kWarps][D];
+  __shared__ float red_m[kWarps], red_l[kWarps];
+  extern __shared__ int32_t list[];  // the row's C indices
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int i = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const long u = static_cast<long>(b) * a.Hkv + h / a.group;
+  const long row = (static_cast<long>(b) * a.Hq + h) * a.n_q + i;
+  const int32_t *cand = a.idx + row * a.C;
+  for (int j = threadIdx.x; j < a.C; j += blockDim.x) list[j] = cand[j];
+
+  float q[4];
+  if (a.q_dtype == KVQ_F32) {
+    const float4 x = reinterpret_cast<const float4 *>(static_cast<const float *>(a.q) + row * D)[lane];
+    q[0] = x.x; q[1] = x.y; q[2] = x.z; q[3] = x.w;
+  } else {
+    const uint2 x = reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(a.q) + row * D)[lane];
+    q[0] = bf16_to_f32(x.x & 0xffffu); q[1] = bf16_to_f32(x.x >> 16);
+    q[2] = bf16_to_f32(x.y & 0xffffu); q[3] = bf16_to_f32(x.y >> 16);
+  }
+#pragma unroll
+  for (int k = 0; k < 4; ++k) q[k] *= a.scale_log2;
+  __syncthreads();
+
+  if (a.validate) {
+    for (int j = threadIdx.x; j < a.C; j += blockDim.x) {
+      const int32_t x = list[j];
+      for (int jj = 0; jj < j; ++jj)
+        if (list[jj] == x) {
+          flag_error(a.ctl, KVQ_DEV_DUP);
+          break;
+        }
+    }
+  }
+
+  const uint8_t *kc_u = a.k_codes + u * a.Gk * kGroup * (D / 2);
+  const float *ks_u = a.k_scales + u * a.Gk * D;
+  const uint8_t *vc_u = a.v_codes + u * a.cut * (D / 2);
+  const float *vs_u = a.v_scales + u * a.cut * (D / 32);
+  const long wbase = u * a.R;
+
+  float m = -CUDART_INF_F, l = 0.0f, o[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  const int tq_max = a.cut > 0 ? a.cut - 1 : 0;
+  for (int c0 = warp * kUnroll; c0 < a.C; c0 += kWarps * kUnroll) {
+    int tk[kUnroll];
+    bool ok[kUnroll];
+    bool any_win = false;
+#pragma unroll
+    for (int x = 0; x < kUnroll; ++x) {
+      const int c = c0 + x;
+      tk[x] = c < a.C ? list[c] : -1;
+      ok[x] = c < a.C && tk[x] >= 0 && tk[x] < a.N;
+      if (c < a.C && !ok[x] && lane == 0) flag_error(a.ctl, KVQ_DEV_INDEX);
+      any_win |= ok[x] && tk[x] >= a.cut;
+    }
+    // int4 rows for every slot, branch-free: out-of-range or window slots read
+    // a clamped, valid int4 row that is overwritten or masked below, so all
+    // 4 x kUnroll loads are in flight together
+    uint32_t kb[kUnroll], vb[kUnroll];
+    float4 ks[kUnroll];
+    float vs[kUnroll];
+    if (a.cut > 0) {
+#pragma unroll
+      for (int x = 0; x < kUnroll; ++x) {
+        const int t = min(max(tk[x], 0), tq_max);
+        const int g = t / kGroup, r = t % kGroup;
+        kb[x] = reinterpret_cast<const uint16_t *>(kc_u + (static_cast<long>(g) * kGroup + r) * (D / 2))[lane];
+        ks[x] = reinterpret_cast<const float4 *>(ks_u + static_cast<long>(g) * D)[lane];
+        vb[x] = reinterpret_cast<const uint16_t *>(vc_u + static_cast<long>(t) * (D / 2))[lane];
+        vs[x] = vs_u[static_cast<long>(t) * (D / 32) + (lane >> 3)];
+      }
+    }
+    float kv[kUnroll][4], vv[kUnroll][4], s[kUnroll];
+#pragma unroll
+    for (int x = 0; x < kUnroll; ++x) {
+      if (a.cut > 0) {
+        kv[x][0] = static_cast<float>(static_cast<int>(kb[x] & 15) - 8) * ks[x].x;
+        kv[x][1] = static_cast<float>(static_cast<int>((kb[x] >> 4) & 15) - 8) * ks[x].y;
+        kv[x][2] = static_cast<float>(static_cast<int>((kb[x] >> 8) & 15) - 8) * ks[x].z;
+        kv[x][3] = static_cast<float>(static_cast<int>((kb[x] >> 12) & 15) - 8) * ks[x].w;
+        vv[x][0] = static_cast<float>(static_cast<int>(vb[x] & 15) - 8) * vs[x];
+        vv[x][1] = static_cast<float>(static_cast<int>((vb[x] >> 4) & 15) - 8) * vs[x];
+        vv[x][2] = static_cast<float>(static_cast<int>((vb[x] >> 8) & 15) - 8) * vs[x];
+        vv[x][3] = static_cast<float>(static_cast<int>((vb[x] >> 12) & 15) - 8) * vs[x];
+      } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) kv[x][k] = vv[x][k] = 0.0f;
+      }
+    }
+    if (any_win) {  // rare: rows of the float window
+#pragma unroll
+      for (int x = 0; x < kUnroll; ++x) {
+        if (!(ok[x] && tk[x] >= a.cut)) continue;
+        const long wr = (wbase + (tk[x] - a.cut)) * D;
+        if (a.kwin == KVQ_F32) {
+          const float4 kf = reinterpret_cast<const float4 *>(static_cast<const float *>(a.k_window) + wr)[lane];
+          kv[x][0] = kf.x; kv[x][1] = kf.y; kv[x][2] = kf.z; kv[x][3] = kf.w;
+        } else {
+          const uint2 kw = reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(a.k_window) + wr)[lane];
+          kv[x][0] = bf16_to_f32(kw.x & 0xffffu); kv[x][1] = bf16_to_f32(kw.x >> 16);
+          kv[x][2] = bf16_to_f32(kw.y & 0xffffu); kv[x][3] = bf16_to_f32(kw.y >> 16);
+        }
+        if (a.vwin == KVQ_F32) {
+          const float4 vf = reinterpret_cast<const float4 *>(static_cast<const float *>(a.v_window) + wr)[lane];
+          vv[x][0] = vf.x; vv[x][1] = vf.y; vv[x][2] = vf.z; vv[x][3] = vf.w;
+        } else {
+          const uint2 vw = reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(a.v_window) + wr)[lane];
+          vv[x][0] = bf16_to_f32(vw.x & 0xffffu); vv[x][1] = bf16_to_f32(vw.x >> 16);
+          vv[x][2] = bf16_to_f32(vw.y & 0xffffu); vv[x][3] = bf16_to_f32(vw.y >> 16);
+        }
+      }
+    }
+#pragma unroll
+    for (int x = 0; x < kUnroll; ++x)
+      s[x] = q[0] * kv[x][0] + q[1] * kv[x][1] + q[2] * kv[x][2] + q[3] * kv[x][3];
+#pragma unroll
+    for (int off = 16; off; off >>= 1)
+#pragma unroll
+      for (int x = 0; x < kUnroll; ++x) s[x] += __shfl_xor_sync(0xffffffffu, s[x], off);
+    float mn = m;
+#pragma unroll
+    for (int x = 0; x < kUnroll; ++x)
+      if (ok[x]) mn = fmaxf(mn, s[x]);
+    if (mn == -CUDART_INF_F) continue;  // nothing valid in this step
+    const float corr = exp2f(m - mn);
+    l *= corr;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) o[k] *= corr;
+#pragma unroll
+    for (int x = 0; x < kUnroll; ++x) {
+      const float p = ok[x] ? exp2f(s[x] - mn) : 0.0f;
+      l += p;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) o[k] = fmaf(p, vv[x][k], o[k]);
+    }
+    m = mn;
+  }
+
+  if (lane == 0) {
+    red_m[warp] = m;
+    red_l[warp] = l;
+  }
+  reinterpret_cast<float4 *>(red_o[warp])[lane] = make_float4(o[0], o[1], o[2], o[3]);
+  __syncthreads();
+  for (int d = threadIdx.x; d < D; d += blockDim.x) {
+    float mx = -CUDART_INF_F;
+    for (int w = 0; w < kWarps; ++w) mx = fmaxf(mx, red_m[w]);
+    float acc = 0.0f, ls = 0.0f;
+    for (int w = 0; w < kWarps; ++w) {
+      if (red_m[w] == -CUDART_INF_F) continue;
+      const float c = exp2f(red_m[w] - mx);
+      acc += c * red_o[w][d];
+      ls += c * red_l[w];
+    }
+    const float x = acc / ls;
+    if (a.out_dtype == KVQ_F32)
+      static_cast<float *>(a.out)[row * D + d] = x;
+    else
+      static_cast<__nv_bfloat16 *>(a.out)[row * D + d] = __float2bfloat16_rn(x);
+  }
+}
+
 template <int F>
 void launch_f(const CandArgs &a, int B, cudaStream_t s) {
   dim3 grid(a.n_q, a.Hq, B);
@@ -190,6 +360,10 @@ int launch_attend_candidates(const kvq_cache &c, const void *q, int q_dtype, int
   a.out_dtype = out_dtype;
   a.scale_log2 = scale_log2;
   a.ctl = ctl;
+  if (d.D == 128) {
+    cand128_kernel<<<dim3(n_q, Hq, d.B), kWarps * 32, sizeof(int32_t) * n_cand, s>>>(a);
+    return 1;
+  }
   switch (d.D / 32) {
     case 1: launch_f<1>(a, d.B, s); break;
     case 2: launch_f<2>(a, d.B, s); break;

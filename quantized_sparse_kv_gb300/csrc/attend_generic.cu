@@ -98,6 +98,18 @@ __global__ void __launch_bounds__(kWarps * 32) generic_attend_kernel(GenericArgs
 
   for (int t0 = 0; t0 < a.N; t0 += kTileKeys) {
     __syncthreads();
+    if (t0 + kTileKeys <= a.cut) {
+      // whole tile in the int4 part: branch-free, so all its loads are in flight together
+#pragma unroll 4
+      for (int i = tid; i < kTileKeys * D; i += blockDim.x) {
+        const int j = i / D, d = i % D, t = t0 + j;
+        const int g = t / kGroup, r = t % kGroup;
+        const long kb = ((u * a.Gk + g) * kGroup + r) * (D / 2) + d / 2;
+        const long vb = (u * a.cut + t) * (D / 2) + d / 2;
+        Ks[j * (D + 1) + d] = nib(a.k_codes[kb], d & 1) * a.k_scales[(u * a.Gk + g) * D + d];
+        Vs[j * D + d] = nib(a.v_codes[vb], d & 1) * a.v_scales[(u * a.cut + t) * (D / 32) + d / 32];
+      }
+    } else
     for (int i = tid; i < kTileKeys * D; i += blockDim.x) {
       const int j = i / D, d = i % D, t = t0 + j;
       float kv = 0.0f, vv = 0.0f;
