@@ -7,8 +7,8 @@
 // residual-window page (head dim 32, 16 queries, N up to 512) and of any shape
 // the specialised kernels do not take.
 //
-// Layout: one CTA per (16 query rows, query head, sequence); 4 warps, 4 rows
-// each. Keys stream through shared memory 32 at a time as fp32; lane j scores
+// Layout (head dims above 64, or an MXFP8 K window): one CTA per (16 query
+// rows, query head, sequence); 4 warps, 4 rows each. Keys stream through shared memory 32 at a time as fp32; lane j scores
 // key j, the warp keeps an online softmax (running max, rescaled sum) and each
 // lane owns D/32 output features.
 #include <cuda_fp8.h>
@@ -189,6 +189,126 @@ __global__ void __launch_bounds__(kWarps * 32) generic_attend_kernel(GenericArgs
   }
 }
 
+// Head dim 32, fp32 or bf16 windows, at most 4 regions: one warp per query row,
+// lane j takes key t0 + j of each 32-key chunk, dequantizes it in registers
+// and scores it against the whole q row; the chunk's max and the running
+// softmax state are shared across the warp, each lane keeps partial sums of
+// O and of the region masses, and O is reduced across lanes once at the end
+// through shared memory. Every query row is independent, so the grid has one
+// warp per row instead of one CTA per head.
+constexpr int kSmallWarps = 4;
+constexpr int kSmallRegions = 4;
+
+template <int D>
+__global__ void __launch_bounds__(kSmallWarps * 32) small_attend_kernel(GenericArgs a, long rows) {
+  __shared__ float red[kSmallWarps][32][D + 1];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long row = static_cast<long>(blockIdx.x) * kSmallWarps + warp;  // over (b, h, i)
+  if (row >= rows) return;                                               // warp-uniform
+  const long bh = row / a.n_q;
+  const int h = static_cast<int>(bh % a.Hq);
+  const long b = bh / a.Hq;
+  const long u = b * a.Hkv + h / a.group;
+
+  float q[D];
+#pragma unroll
+  for (int d = 0; d < D; d += 4) {
+    if (a.q_dtype == KVQ_F32) {
+      const float4 x = *reinterpret_cast<const float4 *>(static_cast<const float *>(a.q) + row * D + d);
+      q[d] = x.x; q[d + 1] = x.y; q[d + 2] = x.z; q[d + 3] = x.w;
+    } else {
+      const uint2 x = *reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(a.q) + row * D + d);
+      q[d] = bf16_to_f32(x.x & 0xffffu); q[d + 1] = bf16_to_f32(x.x >> 16);
+      q[d + 2] = bf16_to_f32(x.y & 0xffffu); q[d + 3] = bf16_to_f32(x.y >> 16);
+    }
+  }
+
+  float m = -CUDART_INF_F, l = 0.0f, o[D], rm[kSmallRegions];
+#pragma unroll
+  for (int d = 0; d < D; ++d) o[d] = 0.0f;
+#pragma unroll
+  for (int k = 0; k < kSmallRegions; ++k) rm[k] = 0.0f;
+
+  for (int t0 = 0; t0 < a.N; t0 += 32) {
+    const int t = t0 + lane;
+    float kv[D], vv[D];
+    if (t < a.cut) {
+      const int g = t / kGroup, r = t % kGroup;
+      const uint32_t *kc = reinterpret_cast<const uint32_t *>(a.k_codes + ((u * a.Gk + g) * kGroup + r) * (D / 2));
+      const float *ks = a.k_scales + (u * a.Gk + g) * D;
+      const uint32_t *vc = reinterpret_cast<const uint32_t *>(a.v_codes + (u * a.cut + t) * (D / 2));
+      const float *vs = a.v_scales + (u * a.cut + t) * (D / 32);
+#pragma unroll
+      for (int w = 0; w < D / 8; ++w) {
+        const uint32_t kw = kc[w], vw = vc[w];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int d = 8 * w + e;
+          kv[d] = static_cast<float>(static_cast<int>((kw >> (4 * e)) & 15u) - 8) * ks[d];
+          vv[d] = static_cast<float>(static_cast<int>((vw >> (4 * e)) & 15u) - 8) * vs[d / 32];
+        }
+      }
+    } else if (t < a.N) {
+      const long wi = (u * a.R + (t - a.cut)) * D;
+#pragma unroll
+      for (int d = 0; d < D; ++d) {
+        kv[d] = window_value(a.k_window, a.kwin, wi + d);
+        vv[d] = window_value(a.v_window, a.vwin, wi + d);
+      }
+    } else {
+#pragma unroll
+      for (int d = 0; d < D; ++d) kv[d] = vv[d] = 0.0f;
+    }
+    float s0 = 0.0f, s1 = 0.0f;
+#pragma unroll
+    for (int d = 0; d < D; d += 2) {
+      s0 = fmaf(q[d], kv[d], s0);
+      s1 = fmaf(q[d + 1], kv[d + 1], s1);
+    }
+    const bool valid = t < a.N;
+    const float sc = valid ? (s0 + s1) * a.sm_scale : -CUDART_INF_F;
+    const float m_new = fmaxf(m, warp_max(sc));
+    const float p = valid ? expf(sc - m_new) : 0.0f;
+    if (m_new != m) {  // warp-uniform
+      const float corr = expf(m - m_new);
+      l *= corr;
+#pragma unroll
+      for (int d = 0; d < D; ++d) o[d] *= corr;
+#pragma unroll
+      for (int k = 0; k < kSmallRegions; ++k) rm[k] *= corr;
+      m = m_new;
+    }
+    l += p;
+#pragma unroll
+    for (int d = 0; d < D; ++d) o[d] = fmaf(p, vv[d], o[d]);
+#pragma unroll
+    for (int k = 0; k < kSmallRegions; ++k)
+      if (k < a.reg.n) rm[k] += (t >= a.reg.b[k] && t < a.reg.b[k + 1]) ? p : 0.0f;
+  }
+
+  // reduce the lanes' partial O through shared memory: lane d sums feature d
+#pragma unroll
+  for (int d = 0; d < D; ++d) red[warp][lane][d] = o[d];
+  __syncwarp();
+  const float inv = 1.0f / warp_sum(l);
+  for (int d = lane; d < D; d += 32) {
+    float acc = 0.0f;
+#pragma unroll 8
+    for (int j = 0; j < 32; ++j) acc += red[warp][j][d];
+    const float x = acc * inv;
+    if (a.out_dtype == KVQ_F32)
+      static_cast<float *>(a.out)[row * D + d] = x;
+    else
+      static_cast<__nv_bfloat16 *>(a.out)[row * D + d] = __float2bfloat16_rn(x);
+  }
+#pragma unroll
+  for (int k = 0; k < kSmallRegions; ++k) {
+    if (k >= a.reg.n) break;
+    const float mk = warp_sum(rm[k]);
+    if (a.mass && lane == 0) a.mass[row * a.reg.n + k] = mk * inv;
+  }
+}
+
 template <int DPL>
 void launch_dpl(const GenericArgs &a, int B, cudaStream_t s) {
   constexpr int D = DPL * 32;
@@ -232,6 +352,12 @@ int launch_attend_generic(const kvq_cache &c, const void *q, int q_dtype, int Hq
   a.mass = mass;
   a.sm_scale = sm_scale;
   a.reg = make_regions(bounds, n_regions);
+  if (d.D == 32 && c.kwin_dtype != KVQ_MXFP8 && a.reg.n <= kSmallRegions) {
+    const long rows = static_cast<long>(d.B) * Hq * n_q;
+    const unsigned blocks = static_cast<unsigned>((rows + kSmallWarps - 1) / kSmallWarps);
+    small_attend_kernel<32><<<blocks, kSmallWarps * 32, 0, s>>>(a, rows);
+    return 1;
+  }
   switch (d.D / 32) {
     case 1: launch_dpl<1>(a, d.B, s); break;
     case 2: launch_dpl<2>(a, d.B, s); break;

@@ -25,63 +25,70 @@ __device__ __forceinline__ int int4_code(float x, float scale) {
   return max(-7, min(7, c));
 }
 
-// One CTA per (sequence*head, K group): loads 32 tokens x D, writes the
-// group's nibbles [32][D/2] and its D per-channel scales.
+// K: one thread per (sequence*head, K group, channel pair). A warp's threads
+// read adjacent channel pairs of the same token (coalesced), keep the 32 x 2
+// values in registers, and write the pair's byte for each of the 32 tokens
+// (adjacent threads -> adjacent bytes) and its two scales.
 template <typename T>
-__global__ void __launch_bounds__(256) pack_k_kernel(const T *__restrict__ k, int N, int D,
-                                                     int cut, int Gk,
+__global__ void __launch_bounds__(256) pack_k_kernel(const T *__restrict__ k, long tasks, int N,
+                                                     int D, int cut, int Gk,
                                                      uint8_t *__restrict__ k_codes,
                                                      float *__restrict__ k_scales) {
-  extern __shared__ float tile[];  // [32][D] values, then [32][D] int8 codes
-  int8_t *codes = reinterpret_cast<int8_t *>(tile + kGroup * D);
-  const int g = blockIdx.x % Gk;
-  const long u = blockIdx.x / Gk;
-  const T *src = k + (u * N + static_cast<long>(g) * kGroup) * D;
+  const long task = blockIdx.x * static_cast<long>(blockDim.x) + threadIdx.x;
+  if (task >= tasks) return;
+  const int pairs = D / 2;
+  const int p = static_cast<int>(task % pairs);
+  const long ug = task / pairs;  // unit * Gk + g
+  const int g = static_cast<int>(ug % Gk);
+  const long u = ug / Gk;
   const int valid = min(kGroup, cut - g * kGroup);
-  for (int i = threadIdx.x; i < kGroup * D; i += blockDim.x) {
-    const int t = i / D;
-    tile[i] = (t < valid) ? load_f32(src + i) : 0.0f;
+  const T *src = k + (u * N + static_cast<long>(g) * kGroup) * D + 2 * p;
+  float x0[kGroup], x1[kGroup];
+  float a0 = 0.0f, a1 = 0.0f;
+#pragma unroll
+  for (int t = 0; t < kGroup; ++t) {
+    x0[t] = t < valid ? load_f32(src + static_cast<long>(t) * D) : 0.0f;
+    x1[t] = t < valid ? load_f32(src + static_cast<long>(t) * D + 1) : 0.0f;
+    a0 = fmaxf(a0, fabsf(x0[t]));
+    a1 = fmaxf(a1, fabsf(x1[t]));
   }
-  __syncthreads();
-  for (int c = threadIdx.x; c < D; c += blockDim.x) {
-    float amax = 0.0f;
-    for (int t = 0; t < kGroup; ++t) amax = fmaxf(amax, fabsf(tile[t * D + c]));
-    const float s = int4_scale(amax);
-    k_scales[(u * Gk + g) * D + c] = s;
-    for (int t = 0; t < kGroup; ++t)
-      codes[t * D + c] = static_cast<int8_t>(int4_code(tile[t * D + c], s));
-  }
-  __syncthreads();
-  uint8_t *dst = k_codes + (u * Gk + g) * (kGroup * D / 2);
-  for (int i = threadIdx.x; i < kGroup * D / 2; i += blockDim.x) {
-    const int t = i / (D / 2), b = i % (D / 2);
-    const int lo = codes[t * D + 2 * b] + 8, hi = codes[t * D + 2 * b + 1] + 8;
-    dst[i] = static_cast<uint8_t>(lo | (hi << 4));
-  }
+  const float s0 = int4_scale(a0), s1 = int4_scale(a1);
+  *reinterpret_cast<float2 *>(k_scales + ug * D + 2 * p) = make_float2(s0, s1);
+  uint8_t *dst = k_codes + ug * (kGroup * D / 2) + p;
+#pragma unroll
+  for (int t = 0; t < kGroup; ++t)
+    dst[t * (D / 2)] = static_cast<uint8_t>((int4_code(x0[t], s0) + 8) | ((int4_code(x1[t], s1) + 8) << 4));
 }
 
-// One warp per (token, 32-feature group) of the quantized part of V.
+// V: one thread per (token, 32-feature group) of the quantized part; 32 values
+// in, 16 code bytes and one scale out.
 template <typename T>
 __global__ void __launch_bounds__(256) pack_v_kernel(const T *__restrict__ v, long rows, int N,
                                                      int D, int cut,
                                                      uint8_t *__restrict__ v_codes,
                                                      float *__restrict__ v_scales) {
   const int groups = D / kGroup;
-  const long task = static_cast<long>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32;
+  const long task = blockIdx.x * static_cast<long>(blockDim.x) + threadIdx.x;
   if (task >= rows * groups) return;
-  const int lane = threadIdx.x & 31;
   const long row = task / groups;  // over (unit, token < cut)
   const int j = static_cast<int>(task % groups);
   const long u = row / cut;
   const long t = row % cut;
-  const float x = load_f32(v + (u * N + t) * D + j * kGroup + lane);
-  const float amax = warp_max(fabsf(x));
+  const T *src = v + (u * N + t) * D + j * kGroup;
+  float x[kGroup];
+  float amax = 0.0f;
+#pragma unroll
+  for (int e = 0; e < kGroup; ++e) {
+    x[e] = load_f32(src + e);
+    amax = fmaxf(amax, fabsf(x[e]));
+  }
   const float s = int4_scale(amax);
-  const int code = int4_code(x, s) + 8;
-  const int hi = __shfl_down_sync(0xffffffffu, code, 1);
-  if ((lane & 1) == 0)
-    v_codes[row * (D / 2) + j * (kGroup / 2) + lane / 2] = static_cast<uint8_t>(code | (hi << 4));
-  if (lane == 0) v_scales[row * groups + j] = s;
+  uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+  for (int e = 0; e < kGroup; ++e)
+    w[e >> 3] |= static_cast<uint32_t>(int4_code(x[e], s) + 8) << (4 * (e & 7));
+  *reinterpret_cast<uint4 *>(v_codes + row * (D / 2) + j * (kGroup / 2)) = make_uint4(w[0], w[1], w[2], w[3]);
+  v_scales[row * groups + j] = s;
 }
 
 // Window copy with dtype change (fp32 <-> bf16, nearest even).
@@ -132,14 +139,12 @@ int pack_typed(const T *k, const T *v, const kvq_cache &c, cudaStream_t s) {
   const long units = static_cast<long>(d.B) * d.Hkv;
   int launches = 0;
   if (d.cut > 0) {
-    const size_t smem = static_cast<size_t>(kGroup) * d.D * (sizeof(float) + 1);
-    cudaFuncSetAttribute(pack_k_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         static_cast<int>(smem));
-    pack_k_kernel<T><<<static_cast<unsigned>(units * d.Gk), 256, smem, s>>>(
-        k, d.N, d.D, d.cut, d.Gk, c.k_codes, c.k_scales);
+    const long ktasks = units * d.Gk * (d.D / 2);
+    pack_k_kernel<T><<<static_cast<unsigned>((ktasks + 255) / 256), 256, 0, s>>>(
+        k, ktasks, d.N, d.D, d.cut, d.Gk, c.k_codes, c.k_scales);
     const long rows = units * d.cut;
-    const long tasks = rows * (d.D / kGroup);
-    pack_v_kernel<T><<<static_cast<unsigned>((tasks + 7) / 8), 256, 0, s>>>(
+    const long vtasks = rows * (d.D / kGroup);
+    pack_v_kernel<T><<<static_cast<unsigned>((vtasks + 255) / 256), 256, 0, s>>>(
         v, rows, d.N, d.D, d.cut, c.v_codes, c.v_scales);
     launches += 2;
   }

@@ -349,3 +349,19 @@ def test_chunk_mxfp8_changes_probabilities_little(kvq):
     _, p_bf, _ = O.attention(q[0, 0], k[0, 0], v[0, 0])
     tv = O.probability_tv(p_mx, p_bf)
     assert np.median(tv) < 0.05
+
+
+@pytest.mark.parametrize("n,heads,n_q,hq_per_kv", [(512, 4, 33, 1), (77, 2, 5, 3), (1000, 1, 40, 2)])
+def test_attend_small_head_dim_kernel_edges(kvq, n, heads, n_q, hq_per_kv):
+    # ragged key chunks, many or few queries, GQA, bf16 window, region masses
+    rng = np.random.default_rng(n)
+    q = O.round_to_bf16(rng.standard_normal((2, heads * hq_per_kv, n_q, 32)).astype(np.float32) * 2)
+    k = O.round_to_bf16(rng.standard_normal((2, heads, n, 32)).astype(np.float32))
+    v = O.round_to_bf16(rng.standard_normal((2, heads, n, 32)).astype(np.float32))
+    bounds = [0, n // 3, n - 5, n]
+    cache = kvq.pack(bf16_cuda(k), bf16_cuda(v), 21, "bf16")
+    out, mass, path = kvq.attend(cache, bf16_cuda(q), out_dtype="f32", region_bounds=bounds)
+    assert path == "generic"
+    ref, ref_mass = O.attend(q, O.pack(k, v, 21, "bf16"), region_bounds=bounds)
+    assert O.rel_l2(to_np(out), ref) <= TOL_F32
+    np.testing.assert_allclose(to_np(mass), ref_mass, atol=TOL_MASS, rtol=0)
