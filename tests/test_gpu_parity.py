@@ -365,3 +365,45 @@ def test_attend_small_head_dim_kernel_edges(kvq, n, heads, n_q, hq_per_kv):
     ref, ref_mass = O.attend(q, O.pack(k, v, 21, "bf16"), region_bounds=bounds)
     assert O.rel_l2(to_np(out), ref) <= TOL_F32
     np.testing.assert_allclose(to_np(mass), ref_mass, atol=TOL_MASS, rtol=0)
+
+
+# ------------------------------------------------------------------ full-size workloads, sampled
+
+
+def _unit_np(t, b, h):
+    return t[b, h].float().cpu().numpy()
+
+
+def test_decode_full_size_sampled_units(kvq):
+    # the timed decode workload: 64 sequences, 16 q-heads / 2 KV heads, D=128, L=32768, R=128
+    q, k, v = synth.decode_inputs_torch(1, 64, 32768, "cuda")
+    cache = kvq.pack(k, v, 128, "bf16")
+    a = kvq.Attend(cache, q, out_dtype="bf16")
+    a.run()
+    assert a.path == "decode" and kvq.read_status(a.status) == 0
+    out = a.out.float().cpu().numpy()
+    for b, kvh in ((0, 0), (17, 1), (63, 1)):
+        kn, vn = _unit_np(k, b, kvh), _unit_np(v, b, kvh)
+        p = O.pack_head(kn, vn, 128, "bf16")
+        ser = O.serialize_head(p)
+        np.testing.assert_array_equal(cache.k_codes[b, kvh].cpu().numpy().reshape(-1), ser["k_codes"].reshape(-1))
+        np.testing.assert_array_equal(cache.v_scales[b, kvh].cpu().numpy(), ser["v_scales"])
+        kh, vh = O.dequantize_head(p)
+        for h in range(8 * kvh, 8 * kvh + 8):
+            ref, _, _ = O.attention(q[b, h].float().cpu().numpy(), kh, vh)
+            assert O.rel_l2(out[b, h], ref) <= TOL_BF16
+
+
+def test_candidates_full_size_sampled_rows(kvq):
+    # the timed candidate workload: 32 sequences, L=131072, C=256
+    q, k, v = synth.decode_inputs_torch(31, 32, 131072, "cuda")
+    cache = kvq.pack(k, v, 128, "bf16")
+    idx = synth.candidate_indices(5, 32, 16, 131072, 256)
+    out, status = kvq.attend_candidates(cache, q, torch.from_numpy(idx).cuda(), out_dtype="f32")
+    assert kvq.read_status(status) == 0
+    out = out.cpu().numpy()
+    for b, h in ((0, 0), (9, 7), (31, 15)):
+        kvh = h // 8
+        kh, vh = O.dequantize_head(O.pack_head(_unit_np(k, b, kvh), _unit_np(v, b, kvh), 128, "bf16"))
+        ref = O.candidate_attention(q[b, h].float().cpu().numpy(), kh, vh, idx[b, h])
+        assert O.rel_l2(out[b, h], ref) <= TOL_BF16
