@@ -51,6 +51,22 @@ def peaks():
                 "source": "fallback"}
 
 
+def profile_traffic(summary):
+    """DRAM bytes per full-size launch recorded in a profiles/ summary, or None
+    when the kernel source has changed since those counters were taken."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", summary)
+    try:
+        fields = dict(line.split(": ", 1) for line in open(path).read().splitlines()
+                      if line.startswith(("source: ", "source_sha256: ", "traffic_bytes_per_full_launch: ")))
+        src = open(os.path.join(ROOT, fields["source"].strip()), "rb").read()
+        if hashlib.sha256(src).hexdigest() != fields["source_sha256"].strip():
+            return None
+        return int(fields["traffic_bytes_per_full_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
 # ---------------------------------------------------------------- algorithmic bytes
 
 def decode_bytes(batch, kv_heads, context, recent, head_dim=128, q_heads=16, out_bytes=2):
@@ -235,7 +251,9 @@ def row_chunk(kvq, synth, torch, steps, warmup, pk, kwin):
                         "[sink 1560 | recent 2340 | current 2340], D=128, region mass",
             "ms": ms, "keys_per_s": keys / (ms * 1e-3), "path": a.path,
             "roofline": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s",
-                         "frac": tf / peak, "traffic": None,
+                         "frac": tf / peak,
+                         "traffic": (profile_traffic("chunk_bf16_kernel_H32_Q2340_K6240.md")
+                                     if kwin == "bf16" else None),
                          "peak_note": "bf16 measured" if kwin != "mxfp8"
                          else "bf16 measured: MXFP8 Q/K expanded exactly to bf16, bf16 MMA"},
             "launches": a.launches()}
@@ -255,7 +273,9 @@ def row_candidates(kvq, synth, torch, steps, warmup, pk, context, c):
     return {"workload": f"candidate attention, 32 x 16 heads, L={context}, C={c}, int4 + bf16 R=128",
             "ms": ms, "keys_per_s": keys / (ms * 1e-3),
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                         "frac": gbs / pk["hbm_gbs"], "traffic": None,
+                         "frac": gbs / pk["hbm_gbs"],
+                         "traffic": (profile_traffic("candidates_kernel_B32_L131072_C256.md")
+                                     if (context, c) == (131072, 256) else None),
                          "bytes_note": "distinct rows and K-scale groups per (sequence, KV head)"},
             "launches": a.launches()}
 
@@ -408,8 +428,16 @@ def run_kvq(args):
     barrier(world)
     s = torch.cuda.current_stream()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    def busy(seconds):
+        # untimed steps, so that the clock sampler sees the GPU under this load
+        t_end = time.perf_counter() + seconds
+        while time.perf_counter() < t_end:
+            for _ in range(20):
+                att.run()
+            torch.cuda.synchronize()
+
     with ClockSampler(local) as clk:
-        torch.cuda.synchronize()
+        busy(0.5)
         barrier(world)
         e0.record(s)
         for _ in range(args.steps):
@@ -417,10 +445,7 @@ def run_kvq(args):
         e1.record(s)
         torch.cuda.synchronize()
         barrier(world)
-        # keep the GPU busy a little longer so the sampler sees the loaded clock
-        for _ in range(args.steps):
-            att.run()
-        torch.cuda.synchronize()
+        busy(0.5)
     ms = e0.elapsed_time(e1) / args.steps
     ms_max = max_over_ranks(ms, world)
     clocks = clk.summary()
@@ -463,7 +488,9 @@ def run_kvq(args):
                    "l2": f"inputs larger than L2 ({nbytes / 1e6:.0f} MB per step), no flush",
                    "parallelism": f"replicas x{world}, each its own batch"},
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                     "frac": gbs / pk["hbm_gbs"], "traffic": None,
+                     "frac": gbs / pk["hbm_gbs"],
+                     "traffic": (profile_traffic("decode_kernel_B16_L32768.md")
+                                 if d["batch"] == 64 else None),
                      "kernel": "decode_kernel + combine_kernel (one kv_attend call)",
                      "algorithmic_bytes": nbytes, "peak_source": pk["source"],
                      "frac_of_nominal_8tbs": gbs / NOMINAL_HBM_GBS},
