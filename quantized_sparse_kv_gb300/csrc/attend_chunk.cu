@@ -171,14 +171,6 @@ __host__ __device__ constexpr uint32_t idesc_bf16(uint32_t b_mn_major) {
          ((128u >> 4) << 24);
 }
 
-// 2^x with the SFU (ex2.approx: about 2 ulp, flushes subnormal results to 0;
-// 2^-inf = 0). P is rounded to bf16 afterwards, far coarser than that.
-__device__ __forceinline__ float fast_exp2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
 __device__ __forceinline__ bool cta_aborted(ChunkSmem &sm) {
   return *reinterpret_cast<volatile int *>(&sm.abort_flag) != 0;
 }

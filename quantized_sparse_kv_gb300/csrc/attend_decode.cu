@@ -115,14 +115,22 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
 __device__ __forceinline__ uint32_t as_u32(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
 __device__ __forceinline__ __half2 as_h2(uint32_t u) { return *reinterpret_cast<__half2 *>(&u); }
 
+// (w & kMask) | kMagic as one three-input logic op.
+template <uint32_t kMask, uint32_t kMagic>
+__device__ __forceinline__ uint32_t and_or(uint32_t w) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(w), "n"(kMask), "n"(kMagic));
+  return d;
+}
+
 // Nibbles at bits 0-3 and 16-19 -> fp16 codes: 0x6400 | n is 1024 + n, n = code + 8.
 __device__ __forceinline__ uint32_t dq_lo(uint32_t w) {
-  const uint32_t x = (w & 0x000F000Fu) | 0x64006400u;
+  const uint32_t x = and_or<0x000F000Fu, 0x64006400u>(w);
   return as_u32(__hsub2(as_h2(x), as_h2(0x64086408u)));  // 1032
 }
 // Nibbles at bits 4-7 and 20-23: 0x5400 | n << 4 is 64 + n.
 __device__ __forceinline__ uint32_t dq_hi(uint32_t w) {
-  const uint32_t x = (w & 0x00F000F0u) | 0x54005400u;
+  const uint32_t x = and_or<0x00F000F0u, 0x54005400u>(w);
   return as_u32(__hsub2(as_h2(x), as_h2(0x54805480u)));  // 72
 }
 
@@ -168,16 +176,16 @@ __device__ __forceinline__ void softmax_update(WarpState &st, float (&s)[NT][4])
     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
   }
   const float n0 = fmaxf(st.m[0], mx0), n1 = fmaxf(st.m[1], mx1);
-  const float c0 = exp2f(st.m[0] - n0), c1 = exp2f(st.m[1] - n1);
+  const float c0 = fast_exp2(st.m[0] - n0), c1 = fast_exp2(st.m[1] - n1);
   st.m[0] = n0;
   st.m[1] = n1;
   float sum0 = 0.0f, sum1 = 0.0f;
 #pragma unroll
   for (int i = 0; i < NT; ++i) {
-    s[i][0] = exp2f(s[i][0] - n0);
-    s[i][1] = exp2f(s[i][1] - n1);
-    s[i][2] = exp2f(s[i][2] - n0);
-    s[i][3] = exp2f(s[i][3] - n1);
+    s[i][0] = fast_exp2(s[i][0] - n0);
+    s[i][1] = fast_exp2(s[i][1] - n1);
+    s[i][2] = fast_exp2(s[i][2] - n0);
+    s[i][3] = fast_exp2(s[i][3] - n1);
     sum0 += s[i][0] + s[i][2];
     sum1 += s[i][1] + s[i][3];
   }
@@ -195,9 +203,10 @@ __device__ __forceinline__ void softmax_update(WarpState &st, float (&s)[NT][4])
 }
 
 // ------------------------------------------------------------------ item bodies
-// int4 group: 32 tokens (two m-tiles), `valid` of them real.
+// int4 group: 32 tokens (two m-tiles), `valid` of them real; kFull: all 32.
 // q of this thread: head g, features 32t + 8i + j, held as fp16 pairs
 // qh[i][j] = (q[8i + j], q[8i + 4 + j]) in the MMA's feature order.
+template <bool kFull>
 __device__ __forceinline__ void do_int4_item(WarpState &st, const uint8_t *kc, const float *ks,
                                              const uint8_t *vc, const float *vs,
                                              const uint32_t (&qh)[4][4], int valid, int g, int t) {
@@ -230,8 +239,10 @@ __device__ __forceinline__ void do_int4_item(WarpState &st, const uint8_t *kc, c
     }
 #pragma unroll
     for (int j = 0; j < 4; ++j) s[mt][j] = e[j] + o[j];
-    if (r0 >= valid) s[mt][0] = s[mt][1] = -CUDART_INF_F;
-    if (r0 + 8 >= valid) s[mt][2] = s[mt][3] = -CUDART_INF_F;
+    if (!kFull) {
+      if (r0 >= valid) s[mt][0] = s[mt][1] = -CUDART_INF_F;
+      if (r0 + 8 >= valid) s[mt][2] = s[mt][3] = -CUDART_INF_F;
+    }
   }
   softmax_update<2>(st, s);
 
@@ -241,7 +252,8 @@ __device__ __forceinline__ void do_int4_item(WarpState &st, const uint8_t *kc, c
     const uint32_t b0 = movmatrix_t(pack_h2(s[mt][0], s[mt][1]));
     const uint32_t b1 = movmatrix_t(pack_h2(s[mt][2], s[mt][3]));
     const int ta = 16 * mt + 2 * t;  // tokens ta, ta+1, ta+8, ta+9
-    const bool va = ta < valid, vb = ta + 1 < valid, vcv = ta + 8 < valid, vd = ta + 9 < valid;
+    const bool va = kFull || ta < valid, vb = kFull || ta + 1 < valid;
+    const bool vcv = kFull || ta + 8 < valid, vd = kFull || ta + 9 < valid;
     const uint2 za = va ? *reinterpret_cast<const uint2 *>(vc + ta * 64 + 8 * g) : zero8;
     const uint2 zb = vb ? *reinterpret_cast<const uint2 *>(vc + (ta + 1) * 64 + 8 * g) : zero8;
     const uint2 zc = vcv ? *reinterpret_cast<const uint2 *>(vc + (ta + 8) * 64 + 8 * g) : zero8;
@@ -431,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const Deco
         const int st = k % kStages;
         if (k >= kStages) {
           const uint32_t par = static_cast<uint32_t>((k / kStages - 1) & 1);
-          if (!mbar_wait_sleep(smem_u32(&sm.empty[st]), par, a.ctl.wait_limit_ns, 32)) {
+          if (!mbar_wait(smem_u32(&sm.empty[st]), par, a.ctl.wait_limit_ns)) {
             flag_error(a.ctl, KVQ_DEV_TIMEOUT);
             *reinterpret_cast<volatile int *>(&sm.abort_flag) = 1;
             break;
@@ -484,12 +496,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const Deco
       const uint8_t *stg = sm.stage[s];
       if (j < a.Gi) {
         const int grp = kGroupsPerItem * j + warp;
-        if (grp < a.Gk)
-          do_int4_item(st, stg + warp * 2048,
-                       reinterpret_cast<const float *>(stg + kOffKScale + warp * 512),
-                       stg + kOffVCode + warp * 2048,
-                       reinterpret_cast<const float *>(stg + kOffVScale + warp * 512), qh,
-                       min(32, a.cut - 32 * grp), g, t);
+        const int valid = a.cut - 32 * grp;
+        const uint8_t *kc = stg + warp * 2048, *vc = stg + kOffVCode + warp * 2048;
+        const float *ks = reinterpret_cast<const float *>(stg + kOffKScale + warp * 512);
+        const float *vs = reinterpret_cast<const float *>(stg + kOffVScale + warp * 512);
+        if (valid >= 32)
+          do_int4_item<true>(st, kc, ks, vc, vs, qh, 32, g, t);
+        else if (valid > 0)
+          do_int4_item<false>(st, kc, ks, vc, vs, qh, valid, g, t);
       } else {
         const int r0 = kWinItem * (j - a.Gi) + kWinTile * warp;
         if (r0 < a.R)

@@ -65,28 +65,40 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for the phase with the given parity to complete, for at most
-// limit_ns nanoseconds of global time. Returns false when the limit ran out.
+// As mbar_try_wait, but a thread whose phase has not completed is suspended
+// until it completes or about hint_ns nanoseconds pass, instead of returning
+// at once: a waiting warp takes no issue slots from the warps doing the work.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity,
+                                                   uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for the phase with the given parity to complete, for at most about
+// limit_ns nanoseconds of global time (the last suspension may overshoot by
+// up to 100 us). Returns false when the limit ran out.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
-  for (uint32_t spin = 1;; ++spin) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((spin & 63u) == 0 && global_ns() - t0 > limit_ns) return false;
+  for (;;) {
+    if (mbar_try_wait_hint(bar, parity, 100000u)) return true;
+    if (global_ns() - t0 > limit_ns) return false;
   }
 }
 
-// As mbar_wait, but sleeps between polls: for a warp whose waiting should not
-// take issue slots from the warps that do the work.
-__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, uint64_t limit_ns,
-                                                uint32_t sleep_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_ns();
-  for (;;) {
-    __nanosleep(sleep_ns);
-    if (mbar_try_wait(bar, parity)) return true;
-    if (global_ns() - t0 > limit_ns) return false;
-  }
+// 2^x on the SFU (ex2.approx: about 2 ulp, subnormal results flushed to 0,
+// 2^-inf = 0). Every caller rounds the result to 16 bits afterwards.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 // ------------------------------------------------------------------ bulk copy
