@@ -179,7 +179,7 @@ KVQ_API kvq_status kv_attend_candidates(const kvq_cache *cache, const void *q, i
  * workspace argument. The split-K partials go to a scratch array of
  * KVQ_DECODE_STATIC_SCRATCH_BYTES (8 MiB) that the library keeps in device
  * memory on every GPU that loads it, until the process exits. A call whose
- * partials need more (roughly batch * kv_heads above about 1,300 on a
+ * partials need more (batch * kv_heads above 992 on a
  * 152-SM GPU) returns KVQ_ERR_WORKSPACE and enqueues nothing; other
  * unsupported shapes return KVQ_ERR_UNSUPPORTED. Nothing is allocated, by
  * the library or by any library it calls.

@@ -12,7 +12,9 @@
 // laid end to end and the persistent grid (3 CTAs per SM) takes equal
 // contiguous slices, so every SM streams the same number of bytes. A CTA
 // emits one partial (running max m, sum l, unnormalised O for 8 heads) per
-// unit its slice touches; combine_kernel merges them with the log-sum-exp rule.
+// unit its slice touches, into the unit's slot for that CTA; combine_kernel,
+// launched as a programmatic dependent of this grid, merges a unit's slots
+// with the log-sum-exp rule.
 //
 // Inside a CTA. Warp 4 is the loader: one lane issues the copies of each item
 // into a 3-stage shared-memory ring, completing on mbarriers. Consumer warp w
@@ -75,9 +77,9 @@ struct DecodeArgs {
   int Hkv, N, R, cut, Gk, Wt, ipu;  // ipu: items per unit = ceil(Gk / 4) + Wt
   int Gi;                           // int4 items per unit = ceil(Gk / 4)
   int total_items;
-  int num_ctas, max_units;
+  int num_ctas, max_ctas_per_unit;
   float scale_log2;
-  float *partials;                  // [num_ctas][max_units][8][132]
+  float *partials;                  // [units][max_ctas_per_unit][8][132]
   KernelCtl ctl;
 };
 
@@ -415,6 +417,16 @@ __device__ __forceinline__ void load_item(const DecodeArgs &a, int u, int j, uin
   }
 }
 
+// First CTA of the persistent grid whose slice holds item x: the largest c
+// with floor(c * T / C) <= x.
+__device__ __forceinline__ int cta_of_item(const DecodeArgs &a, int x) {
+  return static_cast<int>(((static_cast<long>(x) + 1) * a.num_ctas - 1) / a.total_items);
+}
+
+__device__ __forceinline__ float *partial_of(const DecodeArgs &a, int u, int slot) {
+  return a.partials + (static_cast<long>(u) * a.max_ctas_per_unit + slot) * (kHeads * kPartFloats);
+}
+
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const DecodeArgs a) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   DecodeSmem &sm = *reinterpret_cast<DecodeSmem *>(smem_raw);
@@ -424,6 +436,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const Deco
   const int hi = static_cast<int>(static_cast<long>(cta + 1) * a.total_items / a.num_ctas);
   const int n_items = hi - lo;
   const int u_first = lo / a.ipu;
+
+  // The combine launch may start placing its blocks as this grid drains; it
+  // waits for the whole grid before reading any partial.
+  asm volatile("griddepcontrol.launch_dependents;");
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -541,8 +557,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const Deco
         }
       }
       asm volatile("bar.sync 1, %0;" ::"n"(kConsumers * 32));
-      float *part =
-          a.partials + ((static_cast<long>(cta) * a.max_units + (u - u_first)) * kHeads) * kPartFloats;
+      float *part = partial_of(a, u, cta - cta_of_item(a, u * a.ipu));
       for (int i = threadIdx.x; i < (kHeads / 2) * kD; i += kConsumers * 32) {
         const int hh = i / kD, d = i % kD, h = 4 * half + hh;
         float mx = -CUDART_INF_F;
@@ -567,29 +582,21 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const Deco
   }
 }
 
-// One warp per (unit, query head): merge the partials of every CTA whose
-// slice overlaps the unit (log-sum-exp), normalise, store. Lanes first read
-// the CTAs' running maxima and sums in parallel; the O rows are then summed
-// with independent loads.
+// One warp per (unit, query head): merge the partials of the CTAs whose
+// slices overlap the unit (log-sum-exp), normalise, store. The partials of
+// unit u sit in consecutive slots, one per overlapping CTA.
 template <typename OT>
 __global__ void __launch_bounds__(256) combine_kernel(const DecodeArgs a, OT *__restrict__ out) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long u = blockIdx.x;
+  const int u = blockIdx.x;
   const int h = warp;
-  const long start = u * a.ipu, end = start + a.ipu;
-  long c0 = start * a.num_ctas / a.total_items;
-  while (c0 > 0 && (c0 * a.total_items / a.num_ctas) > start) --c0;
-  while ((c0 + 1) * a.total_items / a.num_ctas <= start) ++c0;  // first CTA ending past start
-  long c1 = c0;                                                  // one past the last overlapping CTA
-  while (c1 < a.num_ctas && c1 * a.total_items / a.num_ctas < end) ++c1;
-  auto part = [&](long c) -> const float * {
-    const long slot = u - (c * a.total_items / a.num_ctas) / a.ipu;
-    return a.partials + ((c * a.max_units + slot) * kHeads + h) * kPartFloats;
-  };
+  const int n = cta_of_item(a, (u + 1) * a.ipu - 1) - cta_of_item(a, u * a.ipu) + 1;
+  const float *base = partial_of(a, u, 0) + h * kPartFloats;
+  constexpr long kSlot = kHeads * kPartFloats;
   float m = -CUDART_INF_F, l = 0.0f;
-  for (long c = c0 + lane; c < c1; c += 32) {
-    const float *p = part(c);
-    const float pm = p[kD], pl = p[kD + 1];
+  for (int c = lane; c < n; c += 32) {
+    const float pm = base[c * kSlot + kD], pl = base[c * kSlot + kD + 1];
     if (pm == -CUDART_INF_F) continue;
     const float nm = fmaxf(m, pm);
     l = l * exp2f(m - nm) + pl * exp2f(pm - nm);
@@ -599,8 +606,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const DecodeArgs a, OT *__
   l = warp_sum(m == -CUDART_INF_F ? 0.0f : l * exp2f(m - mx));
   float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll 4
-  for (long c = c0; c < c1; ++c) {
-    const float *p = part(c);
+  for (int c = 0; c < n; ++c) {
+    const float *p = base + c * kSlot;
     const float pm = p[kD];
     const float w = pm == -CUDART_INF_F ? 0.0f : exp2f(pm - mx);
     const float4 po = *reinterpret_cast<const float4 *>(p + 4 * lane);
@@ -610,14 +617,15 @@ __global__ void __launch_bounds__(256) combine_kernel(const DecodeArgs a, OT *__
     acc[3] += w * po.w;
   }
   const float inv = 1.0f / l;
-  OT *o = out + (u * kHeads + h) * kD + 4 * lane;
+  OT *o = out + (static_cast<long>(u) * kHeads + h) * kD + 4 * lane;
 #pragma unroll
   for (int i = 0; i < 4; ++i) store_from_f32(o + i, acc[i] * inv);
 }
 
 struct Plan {
   int total_items;
-  int ipu, Gi, Wt, num_ctas, max_units;
+  int ipu, Gi, Wt, num_ctas, max_ctas_per_unit;
+  long units;
 };
 
 Plan make_plan(const kvq_cache &c, int num_sms) {
@@ -626,11 +634,14 @@ Plan make_plan(const kvq_cache &c, int num_sms) {
   p.Gi = (d.Gk + kGroupsPerItem - 1) / kGroupsPerItem;
   p.Wt = (d.R + kWinItem - 1) / kWinItem;
   p.ipu = p.Gi + p.Wt;
-  const long total = static_cast<long>(d.B) * d.Hkv * p.ipu;
+  p.units = static_cast<long>(d.B) * d.Hkv;
+  const long total = p.units * p.ipu;
   p.total_items = static_cast<int>(std::min<long>(total, 1L << 30));
   p.num_ctas = static_cast<int>(std::min<long>(total, static_cast<long>(kCtasPerSm) * num_sms));
-  const long per = (total + p.num_ctas - 1) / p.num_ctas;
-  p.max_units = static_cast<int>((per + p.ipu - 1) / p.ipu + 1);
+  // A unit's ipu items meet at most (ipu - 2) / min_per + 2 slices: the first
+  // and last hold at least one of its items, the ones between all of theirs.
+  const long min_per = total / p.num_ctas;
+  p.max_ctas_per_unit = p.ipu >= 2 ? static_cast<int>((p.ipu - 2) / min_per + 2) : 1;
   return p;
 }
 
@@ -647,7 +658,7 @@ bool decode_supported(const kvq_cache &c, int q_dtype, int Hq, int n_q) {
 
 size_t decode_workspace_bytes(const kvq_cache &c, int, int num_sms) {
   const Plan p = make_plan(c, num_sms);
-  return sizeof(float) * static_cast<size_t>(p.num_ctas) * p.max_units * kHeads * kPartFloats;
+  return sizeof(float) * static_cast<size_t>(p.units) * p.max_ctas_per_unit * kHeads * kPartFloats;
 }
 
 int launch_attend_decode(const kvq_cache &c, const void *q, int q_dtype, float scale_log2,
@@ -674,7 +685,7 @@ int launch_attend_decode(const kvq_cache &c, const void *q, int q_dtype, float s
   a.ipu = p.ipu;
   a.total_items = p.total_items;
   a.num_ctas = p.num_ctas;
-  a.max_units = p.max_units;
+  a.max_ctas_per_unit = p.max_ctas_per_unit;
   a.scale_log2 = scale_log2;
   a.partials = static_cast<float *>(ws);
   a.ctl = ctl;
@@ -682,12 +693,23 @@ int launch_attend_decode(const kvq_cache &c, const void *q, int q_dtype, float s
   cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        static_cast<int>(smem));
   decode_kernel<<<p.num_ctas, kThreads, smem, s>>>(a);
-  const unsigned units = static_cast<unsigned>(d.B) * d.Hkv;
+  // The combine kernel is a programmatic dependent launch: its blocks may be
+  // placed while the decode grid drains and wait for it on the device.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.units));
+  cfg.blockDim = dim3(kHeads * 32);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   if (out_dtype == KVQ_F32)
-    combine_kernel<float><<<units, kHeads * 32, 0, s>>>(a, static_cast<float *>(out));
+    cudaLaunchKernelEx(&cfg, combine_kernel<float>, a, static_cast<float *>(out));
   else
-    combine_kernel<__nv_bfloat16><<<units, kHeads * 32, 0, s>>>(
-        a, static_cast<__nv_bfloat16 *>(out));
+    cudaLaunchKernelEx(&cfg, combine_kernel<__nv_bfloat16>, a,
+                       static_cast<__nv_bfloat16 *>(out));
   return 2;
 }
 
