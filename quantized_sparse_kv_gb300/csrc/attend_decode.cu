@@ -164,6 +164,12 @@ __device__ __forceinline__ void state_reset(WarpState &st) {
 
 // Online-softmax update with NT m-tiles of scores s[NT][4] (rows g, g+8 x heads
 // 2t, 2t+1); masked scores are -inf. Turns s into probabilities in place.
+// The reference maximum m is only raised when some score of the tile exceeds
+// it by more than kLazy (log2 units), so most tiles need no cross-lane
+// reduction; probabilities are then at most 2^kLazy, well inside fp16, and
+// the result is unchanged because O and l share the reference.
+constexpr float kLazy = 8.0f;
+
 template <int NT>
 __device__ __forceinline__ void softmax_update(WarpState &st, float (&s)[NT][4]) {
   float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F;
@@ -172,28 +178,18 @@ __device__ __forceinline__ void softmax_update(WarpState &st, float (&s)[NT][4])
     mx0 = fmaxf(mx0, fmaxf(s[i][0], s[i][2]));
     mx1 = fmaxf(mx1, fmaxf(s[i][1], s[i][3]));
   }
+  if (__any_sync(0xffffffffu, mx0 > st.m[0] + kLazy || mx1 > st.m[1] + kLazy)) {
 #pragma unroll
-  for (int o = 4; o < 32; o <<= 1) {
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
-  }
-  const float n0 = fmaxf(st.m[0], mx0), n1 = fmaxf(st.m[1], mx1);
-  const float c0 = fast_exp2(st.m[0] - n0), c1 = fast_exp2(st.m[1] - n1);
-  st.m[0] = n0;
-  st.m[1] = n1;
-  float sum0 = 0.0f, sum1 = 0.0f;
-#pragma unroll
-  for (int i = 0; i < NT; ++i) {
-    s[i][0] = fast_exp2(s[i][0] - n0);
-    s[i][1] = fast_exp2(s[i][1] - n1);
-    s[i][2] = fast_exp2(s[i][2] - n0);
-    s[i][3] = fast_exp2(s[i][3] - n1);
-    sum0 += s[i][0] + s[i][2];
-    sum1 += s[i][1] + s[i][3];
-  }
-  st.l[0] = st.l[0] * c0 + sum0;
-  st.l[1] = st.l[1] * c1 + sum1;
-  if (!__all_sync(0xffffffffu, c0 == 1.0f && c1 == 1.0f)) {
+    for (int o = 4; o < 32; o <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+    }
+    const float n0 = fmaxf(st.m[0], mx0), n1 = fmaxf(st.m[1], mx1);
+    const float c0 = fast_exp2(st.m[0] - n0), c1 = fast_exp2(st.m[1] - n1);
+    st.m[0] = n0;
+    st.m[1] = n1;
+    st.l[0] *= c0;
+    st.l[1] *= c1;
 #pragma unroll
     for (int f = 0; f < 8; ++f) {
       st.o[f][0] *= c0;
@@ -202,6 +198,18 @@ __device__ __forceinline__ void softmax_update(WarpState &st, float (&s)[NT][4])
       st.o[f][3] *= c1;
     }
   }
+  float sum0 = 0.0f, sum1 = 0.0f;
+#pragma unroll
+  for (int i = 0; i < NT; ++i) {
+    s[i][0] = fast_exp2(s[i][0] - st.m[0]);
+    s[i][1] = fast_exp2(s[i][1] - st.m[1]);
+    s[i][2] = fast_exp2(s[i][2] - st.m[0]);
+    s[i][3] = fast_exp2(s[i][3] - st.m[1]);
+    sum0 += s[i][0] + s[i][2];
+    sum1 += s[i][1] + s[i][3];
+  }
+  st.l[0] += sum0;
+  st.l[1] += sum1;
 }
 
 // ------------------------------------------------------------------ item bodies
@@ -584,7 +592,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const Deco
 
 // One warp per (unit, query head): merge the partials of the CTAs whose
 // slices overlap the unit (log-sum-exp), normalise, store. The partials of
-// unit u sit in consecutive slots, one per overlapping CTA.
+// unit u sit in consecutive slots, one per overlapping CTA; they are read
+// eight at a time with all loads of a batch in flight together.
 template <typename OT>
 __global__ void __launch_bounds__(256) combine_kernel(const DecodeArgs a, OT *__restrict__ out) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -593,33 +602,48 @@ __global__ void __launch_bounds__(256) combine_kernel(const DecodeArgs a, OT *__
   const int h = warp;
   const int n = cta_of_item(a, (u + 1) * a.ipu - 1) - cta_of_item(a, u * a.ipu) + 1;
   const float *base = partial_of(a, u, 0) + h * kPartFloats;
-  constexpr long kSlot = kHeads * kPartFloats;
+  constexpr int kSlot = kHeads * kPartFloats;
+  constexpr int kBatch = 8;
   float m = -CUDART_INF_F, l = 0.0f;
-  for (int c = lane; c < n; c += 32) {
-    const float pm = base[c * kSlot + kD], pl = base[c * kSlot + kD + 1];
-    if (pm == -CUDART_INF_F) continue;
-    const float nm = fmaxf(m, pm);
-    l = l * exp2f(m - nm) + pl * exp2f(pm - nm);
+  float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  for (int c0 = 0; c0 < n; c0 += kBatch) {
+    float pm[kBatch], pl[kBatch];
+    float4 po[kBatch];
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      const float *p = base + static_cast<long>(min(c0 + i, n - 1)) * kSlot;
+      const float2 ml = *reinterpret_cast<const float2 *>(p + kD);
+      pm[i] = c0 + i < n ? ml.x : -CUDART_INF_F;
+      pl[i] = ml.y;
+      po[i] = *reinterpret_cast<const float4 *>(p + 4 * lane);
+    }
+    float nm = m;
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) nm = fmaxf(nm, pm[i]);
+    if (nm == -CUDART_INF_F) continue;
+    const float r = exp2f(m - nm);  // 0 while m is -inf
+    l *= r;
+    acc.x *= r;
+    acc.y *= r;
+    acc.z *= r;
+    acc.w *= r;
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      const float w = exp2f(pm[i] - nm);  // 0 for empty and padded slots
+      l += w * pl[i];
+      acc.x += w * po[i].x;
+      acc.y += w * po[i].y;
+      acc.z += w * po[i].z;
+      acc.w += w * po[i].w;
+    }
     m = nm;
-  }
-  const float mx = warp_max(m);
-  l = warp_sum(m == -CUDART_INF_F ? 0.0f : l * exp2f(m - mx));
-  float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll 4
-  for (int c = 0; c < n; ++c) {
-    const float *p = base + c * kSlot;
-    const float pm = p[kD];
-    const float w = pm == -CUDART_INF_F ? 0.0f : exp2f(pm - mx);
-    const float4 po = *reinterpret_cast<const float4 *>(p + 4 * lane);
-    acc[0] += w * po.x;
-    acc[1] += w * po.y;
-    acc[2] += w * po.z;
-    acc[3] += w * po.w;
   }
   const float inv = 1.0f / l;
   OT *o = out + (static_cast<long>(u) * kHeads + h) * kD + 4 * lane;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) store_from_f32(o + i, acc[i] * inv);
+  store_from_f32(o + 0, acc.x * inv);
+  store_from_f32(o + 1, acc.y * inv);
+  store_from_f32(o + 2, acc.z * inv);
+  store_from_f32(o + 3, acc.w * inv);
 }
 
 struct Plan {
