@@ -43,13 +43,14 @@ constexpr int kMaxRegions = 4;
 constexpr uint32_t kTileBytes = kBN * kDim * 2;  // 32 KB, one K or V tile (bf16)
 constexpr uint32_t kHalfBytes = kTileBytes / 2;  // 16 KB: 128 rows x 64 features
 constexpr float kRescaleThreshold = 8.0f;         // log2 units
+constexpr float kRedoThreshold = 64.0f;           // log2 units: P stays below 2^64
 
 struct __align__(1024) ChunkSmem {
   uint8_t q[kTileBytes];                    // 2 x [128 rows][128 B], swizzled
   uint8_t k[kKStages][kTileBytes];
   uint8_t v[kVStages][kTileBytes];
   uint8_t p[2][kTileBytes];                 // P (bf16) of group A and B, K-major A operand
-  float merge_m[kBM], merge_l[kBM];         // group B's row state for the final merge
+  float merge_m[kBM], merge_l[kBM], merge_p[kBM];  // group B's row state for the final merge
   float merge_r[kMaxRegions][kBM];
   uint64_t q_full;
   uint64_t k_full[kKStages], k_empty[kKStages], v_full[kVStages], v_empty[kVStages];
@@ -194,6 +195,129 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t *>(&b);
 }
 
+// Scale 128 fp32 TMEM columns of this thread's lane by f.
+__device__ __forceinline__ void scale_tmem_row(uint32_t taddr, float f) {
+#pragma unroll 1
+  for (int c = 0; c < 4; ++c) {
+    float v[32];
+    tmem_ld32(taddr + 32u * c, v);
+    tmem_wait_ld();
+    reg_fence(v);
+#pragma unroll
+    for (int e = 0; e < 32; ++e) v[e] *= f;
+    tmem_st32(taddr + 32u * c, v);
+  }
+  tmem_wait_st();
+}
+
+// Maximum of the first `valid` of this lane's 128 score columns.
+__device__ __forceinline__ float row_max(uint32_t taddr, int valid) {
+  float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F;
+#pragma unroll 1
+  for (int c = 0; c < 4; ++c) {
+    float v[32];
+    tmem_ld32(taddr + 32u * c, v);
+    tmem_wait_ld();
+    reg_fence(v);
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) {
+      mx0 = fmaxf(mx0, 32 * c + e < valid ? v[e] : -CUDART_INF_F);
+      mx1 = fmaxf(mx1, 32 * c + e + 1 < valid ? v[e + 1] : -CUDART_INF_F);
+    }
+  }
+  return fmaxf(mx0, mx1);
+}
+
+// 32 columns of the pass: P = 2^(s * scale + neg_m) for the valid ones (0
+// beyond), raw maximum, P to shared memory as bf16, the chunk's sum. Region
+// sums are left to the caller unless kSplit (the tile straddles a region
+// bound), when they are taken here element by element.
+template <bool kSplit>
+__device__ __forceinline__ void softmax_chunk(float (&v)[32], int c, int valid, int t0,
+                                              float scale, float neg_m, const Regions &reg,
+                                              uint8_t *p, int row, float &cs,
+                                              float (&part)[kMaxRegions], float &mx0, float &mx1) {
+  float ps4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  if (32 * c + 32 <= valid) {
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) {
+      mx0 = fmaxf(mx0, v[e]);
+      mx1 = fmaxf(mx1, v[e + 1]);
+    }
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      v[e] = fast_exp2(fmaf(v[e], scale, neg_m));
+      ps4[e & 3] += v[e];
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      const bool in = 32 * c + e < valid;
+      if (e & 1)
+        mx1 = fmaxf(mx1, in ? v[e] : -CUDART_INF_F);
+      else
+        mx0 = fmaxf(mx0, in ? v[e] : -CUDART_INF_F);
+      v[e] = in ? fast_exp2(fmaf(v[e], scale, neg_m)) : 0.0f;
+      ps4[e & 3] += v[e];
+    }
+  }
+#pragma unroll
+  for (int q8 = 0; q8 < 4; ++q8) {
+    const int chunk = 4 * c + q8;  // 16-byte chunk of the row, 0..15
+    uint4 w;
+    w.x = pack_bf16x2(v[8 * q8 + 0], v[8 * q8 + 1]);
+    w.y = pack_bf16x2(v[8 * q8 + 2], v[8 * q8 + 3]);
+    w.z = pack_bf16x2(v[8 * q8 + 4], v[8 * q8 + 5]);
+    w.w = pack_bf16x2(v[8 * q8 + 6], v[8 * q8 + 7]);
+    *reinterpret_cast<uint4 *>(p + (chunk >> 3) * kHalfBytes + swz(row, chunk & 7)) = w;
+  }
+  cs = (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
+  if (kSplit) {
+    const int start = t0 + 32 * c;
+#pragma unroll
+    for (int k = 0; k < kMaxRegions; ++k) {
+      if (k >= reg.n) break;
+      const int lo = reg.b[k] - start, hi = reg.b[k + 1] - start;
+      if (hi <= 0 || lo >= 32) continue;
+      float pk = 0.0f;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) pk += (e >= lo && e < hi) ? v[e] : 0.0f;
+      part[k] += pk;
+    }
+  }
+}
+
+// One pass over the 128 score columns of this thread's row; the TMEM load
+// of the next 32 columns is in flight while the current ones are processed.
+// cs[c]: sum of chunk c; part: region sums (kSplit only).
+template <bool kSplit>
+__device__ __forceinline__ void softmax_pass(uint32_t taddr, int valid, int t0, float scale,
+                                             float neg_m, const Regions &reg, uint8_t *p, int row,
+                                             float (&cs)[4], float (&part)[kMaxRegions],
+                                             float &mx) {
+#pragma unroll
+  for (int k = 0; k < kMaxRegions; ++k) part[k] = 0.0f;
+  float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F;
+  float va[32], vb[32];
+  tmem_ld32(taddr, va);
+  tmem_wait_ld();
+  reg_fence(va);
+  tmem_ld32(taddr + 32u, vb);
+  softmax_chunk<kSplit>(va, 0, valid, t0, scale, neg_m, reg, p, row, cs[0], part, mx0, mx1);
+  tmem_wait_ld();
+  reg_fence(vb);
+  tmem_ld32(taddr + 64u, va);
+  softmax_chunk<kSplit>(vb, 1, valid, t0, scale, neg_m, reg, p, row, cs[1], part, mx0, mx1);
+  tmem_wait_ld();
+  reg_fence(va);
+  tmem_ld32(taddr + 96u, vb);
+  softmax_chunk<kSplit>(va, 2, valid, t0, scale, neg_m, reg, p, row, cs[2], part, mx0, mx1);
+  tmem_wait_ld();
+  reg_fence(vb);
+  softmax_chunk<kSplit>(vb, 3, valid, t0, scale, neg_m, reg, p, row, cs[3], part, mx0, mx1);
+  mx = fmaxf(mx0, mx1);
+}
+
 __global__ void __launch_bounds__(384, 1)
     chunk_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
@@ -238,8 +362,8 @@ __global__ void __launch_bounds__(384, 1)
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
   // group g: S at columns 256g, O at 256g + 128
-  const uint32_t t_s[2] = {tmem, tmem + 256u};
-  const uint32_t t_o[2] = {tmem + 128u, tmem + 384u};
+  auto t_s = [&](int g) { return tmem + 256u * g; };
+  auto t_o = [&](int g) { return tmem + 256u * g + 128u; };
 
   if (warp == 0) {
     // ------------------------------------------------ TMA producer
@@ -293,7 +417,7 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32u;
-          tc_mma_f16(t_s[g], smem_desc(qa + off, 16, 1024), smem_desc(ka + off, 16, 1024), id_qk,
+          tc_mma_f16(t_s(g), smem_desc(qa + off, 16, 1024), smem_desc(ka + off, 16, 1024), id_qk,
                      kk > 0 ? 1u : 0u);
         }
         tc_commit(smem_u32(&sm.s_full[g]));
@@ -316,7 +440,7 @@ __global__ void __launch_bounds__(384, 1)
         for (int kk = 0; kk < 8; ++kk) {
           const uint64_t ad = smem_desc(pa + (kk >> 2) * kHalfBytes + (kk & 3) * 32u, 16, 1024);
           const uint64_t bd = smem_desc(va + kk * 2048u, kHalfBytes, 1024);
-          tc_mma_f16(t_o[g], ad, bd, id_pv, (i > 0 || kk > 0) ? 1u : 0u);
+          tc_mma_f16(t_o(g), ad, bd, id_pv, (i > 0 || kk > 0) ? 1u : 0u);
         }
         tc_commit(smem_u32(&sm.o_done[g]));
         tc_commit(smem_u32(&sm.v_empty[st]));
@@ -336,8 +460,13 @@ __global__ void __launch_bounds__(384, 1)
     const int quad = warp & 3;               // TMEM lanes 32*quad .. +31
     const int row = quad * 32 + lane;        // query row within the tile
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t s_row = t_s(g) + lane_off, o_row = t_o(g) + lane_off;
     const int my_tiles = (nt - g + 1) >> 1;  // tiles g, g+2, ...
-    float m_used = -CUDART_INF_F, l = 0.0f;
+    // Row state: P of a tile is taken against the reference m_used fixed when
+    // the tile starts; a tile whose maximum passes m_used + kRescaleThreshold
+    // raises the reference for the following tiles (l and the region sums are
+    // rescaled at once, O_g once its pending MMA is done: `pend`).
+    float m_used = -CUDART_INF_F, l = 0.0f, pend = 1.0f;
     float rsum[kMaxRegions] = {0.0f, 0.0f, 0.0f, 0.0f};
     bool ok = true;
     for (int i = 0; i < my_tiles; ++i) {
@@ -348,106 +477,84 @@ __global__ void __launch_bounds__(384, 1)
       }
       tc_fence_after();
       const int valid = min(kBN, a.n_kv - j * kBN);
-      // pass 1: row max of the raw scores
-      float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F;
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        float v[32];
-        tmem_ld32(t_s[g] + lane_off + 32u * c, v);
-        tmem_wait_ld();
-        reg_fence(v);
-        if (valid < kBN) {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) v[e] = (32 * c + e < valid) ? v[e] : -CUDART_INF_F;
-        }
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          mx0 = fmaxf(mx0, v[e]);
-          mx1 = fmaxf(mx1, v[e + 1]);
-        }
-      }
-      const float mx = fmaxf(mx0, mx1) * a.scale_log2;  // scale > 0 keeps the order
-      float factor = 1.0f;
-      if (mx > m_used + kRescaleThreshold) {
-        factor = exp2f(m_used - mx);  // 0 on the first tile
-        m_used = mx;
-      }
-      l *= factor;
-#pragma unroll
-      for (int k = 0; k < kMaxRegions; ++k) rsum[k] *= factor;
+      const int t0 = j * kBN;
       // O_g += P V of the previous tile must be done before P_g is rewritten
       // or O_g is rescaled
-      if (i >= 1 && !wait_or_abort(sm, smem_u32(&sm.o_done[g]), (i - 1) & 1, a.ctl)) {
-        ok = false;
-        break;
+      if (i >= 1) {
+        if (!wait_or_abort(sm, smem_u32(&sm.o_done[g]), (i - 1) & 1, a.ctl)) {
+          ok = false;
+          break;
+        }
+        if (__any_sync(0xffffffffu, pend != 1.0f)) {
+          tc_fence_after();
+          scale_tmem_row(o_row, pend);
+        }
+        pend = 1.0f;
       }
-      if (i >= 1 && __any_sync(0xffffffffu, factor != 1.0f)) {
-        tc_fence_after();
+      if (i == 0) m_used = row_max(s_row, valid) * a.scale_log2;  // scale > 0 keeps the order
+      // regions: chunk c of the tile lies in region kc[c], unless the tile
+      // has a chunk across a bound (split: sums taken per element)
+      int kc[4] = {0, 0, 0, 0};
+      bool split = false;
+      if (a.reg.n > 0) {
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          float v[32];
-          tmem_ld32(t_o[g] + lane_off + 32u * c, v);
-          tmem_wait_ld();
-          reg_fence(v);
+          const int start = t0 + 32 * c;
 #pragma unroll
-          for (int e = 0; e < 32; ++e) v[e] *= factor;
-          tmem_st32(t_o[g] + lane_off + 32u * c, v);
-        }
-        tmem_wait_st();
-      }
-      // pass 2: P = 2^(s * scale - m), row and region sums, P -> shared memory
-      const float neg_m = -m_used;
-      const int t0 = j * kBN;
-      float ps = 0.0f;
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        float v[32];
-        tmem_ld32(t_s[g] + lane_off + 32u * c, v);
-        tmem_wait_ld();
-        reg_fence(v);
-        float ps4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        if (valid == kBN) {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            v[e] = fast_exp2(fmaf(v[e], a.scale_log2, neg_m));
-            ps4[e & 3] += v[e];
-          }
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            v[e] = (32 * c + e < valid) ? fast_exp2(fmaf(v[e], a.scale_log2, neg_m)) : 0.0f;
-            ps4[e & 3] += v[e];
-          }
-        }
-        const float cs = (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
-        ps += cs;
-        for (int k = 0; k < a.reg.n && k < kMaxRegions; ++k) {
-          const int lo = a.reg.b[k] - t0 - 32 * c, hi = a.reg.b[k + 1] - t0 - 32 * c;
-          if (hi <= 0 || lo >= 32) continue;
-          if (lo <= 0 && hi >= 32) {
-            rsum[k] += cs;
-            continue;
-          }
-          float part = 0.0f;
-#pragma unroll
-          for (int e = 0; e < 32; ++e) part += (e >= lo && e < hi) ? v[e] : 0.0f;
-          rsum[k] += part;
-        }
-#pragma unroll
-        for (int q8 = 0; q8 < 4; ++q8) {
-          const int chunk = 4 * c + q8;  // 16-byte chunk of the row, 0..15
-          uint4 w;
-          w.x = pack_bf16x2(v[8 * q8 + 0], v[8 * q8 + 1]);
-          w.y = pack_bf16x2(v[8 * q8 + 2], v[8 * q8 + 3]);
-          w.z = pack_bf16x2(v[8 * q8 + 4], v[8 * q8 + 5]);
-          w.w = pack_bf16x2(v[8 * q8 + 6], v[8 * q8 + 7]);
-          *reinterpret_cast<uint4 *>(sm.p[g] + (chunk >> 3) * kHalfBytes + swz(row, chunk & 7)) = w;
+          for (int k = 1; k < kMaxRegions; ++k)
+            kc[c] += (k < a.reg.n && a.reg.b[k] <= start) ? 1 : 0;
+          const int end = min(start + 32, t0 + valid);
+          split |= start < end && end > a.reg.b[kc[c] + 1];
         }
       }
-      l += ps;
+      // one pass: P = 2^(s * scale - m_used) -> shared memory, sums, raw max
+      float cs[4], part[kMaxRegions], mx;
+      if (split)
+        softmax_pass<true>(s_row, valid, t0, a.scale_log2, -m_used, a.reg, sm.p[g], row, cs, part, mx);
+      else
+        softmax_pass<false>(s_row, valid, t0, a.scale_log2, -m_used, a.reg, sm.p[g], row, cs, part, mx);
+      const float mt = mx * a.scale_log2;  // scaled tile maximum
+      if (__any_sync(0xffffffffu, mt > m_used + kRedoThreshold)) {
+        // far above the reference for some row (P could overflow): the warp
+        // takes the tile maxima now and recomputes the tile (TMEM access is
+        // warp-wide); O_g is idle, its last MMA is done
+        const float m_new = fmaxf(m_used, mt);
+        const float f = fast_exp2(m_used - m_new);
+        m_used = m_new;
+        l *= f;
+#pragma unroll
+        for (int k = 0; k < kMaxRegions; ++k) rsum[k] *= f;
+        if (i >= 1) {
+          tc_fence_after();
+          scale_tmem_row(o_row, f);
+        }
+        if (split)
+          softmax_pass<true>(s_row, valid, t0, a.scale_log2, -m_used, a.reg, sm.p[g], row, cs, part, mx);
+        else
+          softmax_pass<false>(s_row, valid, t0, a.scale_log2, -m_used, a.reg, sm.p[g], row, cs, part, mx);
+      }
+      // P is complete: hand it to the MMA warp, then do the bookkeeping
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       tc_fence_before();
       mbar_arrive(smem_u32(&sm.p_full[g]));
+      l += (cs[0] + cs[1]) + (cs[2] + cs[3]);
+      if (!split) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int k = 0; k < kMaxRegions; ++k) part[k] += (kc[c] == k) ? cs[c] : 0.0f;
+      }
+      if (a.reg.n > 0) {
+#pragma unroll
+        for (int k = 0; k < kMaxRegions; ++k) rsum[k] += part[k];
+      }
+      if (mt > m_used + kRescaleThreshold) {
+        pend = fast_exp2(m_used - mt);
+        m_used = mt;
+        l *= pend;
+#pragma unroll
+        for (int k = 0; k < kMaxRegions; ++k) rsum[k] *= pend;
+      }
     }
     // ---- epilogue: group B hands its row state to group A, A merges and stores
     const bool last_ok =
@@ -456,6 +563,7 @@ __global__ void __launch_bounds__(384, 1)
     if (g == 1) {
       sm.merge_m[row] = last_ok ? m_used : -CUDART_INF_F;
       sm.merge_l[row] = last_ok ? l : 0.0f;
+      sm.merge_p[row] = pend;
 #pragma unroll
       for (int k = 0; k < kMaxRegions; ++k) sm.merge_r[k][row] = last_ok ? rsum[k] : 0.0f;
     }
@@ -473,18 +581,20 @@ __global__ void __launch_bounds__(384, 1)
       const float fb = have_b ? exp2f(mb - mm) : 0.0f;
       const float lt = fa * l + fb * sm.merge_l[row];
       const float inv = 1.0f / lt;
+      // O_A and O_B still owe their last reference change
+      const float oa = fa * pend, ob = fb * sm.merge_p[row];
       const int qrow = q0 + row;
       const long obase = (static_cast<long>(hq) * a.n_q + qrow) * kDim;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         float va[32], vb[32];
-        tmem_ld32(t_o[0] + lane_off + 32u * c, va);
-        if (have_b) tmem_ld32(t_o[1] + lane_off + 32u * c, vb);
+        tmem_ld32(t_o(0) + lane_off + 32u * c, va);
+        if (have_b) tmem_ld32(t_o(1) + lane_off + 32u * c, vb);
         tmem_wait_ld();
         reg_fence(va);
         if (have_b) reg_fence(vb);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) va[e] = (fa * va[e] + (have_b ? fb * vb[e] : 0.0f)) * inv;
+        for (int e = 0; e < 32; ++e) va[e] = (oa * va[e] + (have_b ? ob * vb[e] : 0.0f)) * inv;
         if (qrow < a.n_q) {
           if (a.out_dtype == KVQ_F32) {
             float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(a.out) + obase + 32 * c);

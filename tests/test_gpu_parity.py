@@ -300,6 +300,31 @@ def test_chunk_bf16_matches_oracle(kvq, hq, hkv, n_q, n_kv, bounds, conc):
             np.testing.assert_allclose(to_np(mass), ref_mass, atol=TOL_MASS, rtol=0)
 
 
+def test_chunk_bf16_growing_and_spiking_scores(kvq):
+    # scores that grow along the keys move the softmax reference several times,
+    # and a late block of keys far above everything before it (more than 2^64
+    # in probability) makes the kernel recompute that tile with a new reference
+    rng = np.random.default_rng(11)
+    n_q, n_kv = 130, 1100
+    u = rng.standard_normal(128)
+    u /= np.linalg.norm(u)
+    q = rng.standard_normal((1, 2, n_q, 128))
+    q += (3.0 - q @ u)[..., None] * u  # every row has the same component along u
+    k = rng.standard_normal((1, 1, n_kv, 128)) * (1.0 + 6.0 * np.arange(n_kv) / n_kv)[:, None]
+    k[0, 0, 900:910] = 300.0 * u + 0.1 * rng.standard_normal((10, 128))
+    v = rng.standard_normal((1, 1, n_kv, 128))
+    q, k, v = (O.round_to_bf16(x.astype(np.float32)) for x in (q, k, v))
+    bounds = [0, 500, 905, n_kv]
+    cache = kvq.pack(bf16_cuda(k), bf16_cuda(v), n_kv, "bf16")
+    out, mass, path = kvq.attend(cache, bf16_cuda(q), out_dtype="f32", region_bounds=bounds)
+    assert path == "chunk_bf16"
+    ref, ref_mass = O.attend(q, O.pack(k, v, n_kv, "bf16"), region_bounds=bounds)
+    assert O.rel_l2(to_np(out), ref) <= TOL_BF16
+    np.testing.assert_allclose(to_np(mass), ref_mass, atol=TOL_MASS, rtol=0)
+    # the spike takes almost all of the mass
+    assert (ref_mass[..., 1:].sum(-1) > 0.99).all()
+
+
 def test_chunk_bf16_full_size_sampled_heads(kvq):
     # the video chunk: 32 heads, 2,340 queries over 6,240 keys [1560 | 2340 | 2340]
     bounds = list(synth.CHUNK_REGION_BOUNDS)
