@@ -37,7 +37,7 @@ namespace {
 constexpr int kBM = 128;          // query rows per CTA
 constexpr int kBN = 128;          // keys per tile
 constexpr int kDim = 128;         // head dim
-constexpr int kKStages = 1;   // K is released as soon as its QK MMA completes
+constexpr int kKStages = 2;
 constexpr int kVStages = 2;
 constexpr int kMaxRegions = 4;
 constexpr uint32_t kTileBytes = kBN * kDim * 2;  // 32 KB, one K or V tile (bf16)
@@ -50,14 +50,20 @@ struct __align__(1024) ChunkSmem {
   uint8_t k[kKStages][kTileBytes];
   uint8_t v[kVStages][kTileBytes];
   uint8_t p[2][kTileBytes];                 // P (bf16) of group A and B, K-major A operand
-  float merge_m[kBM], merge_l[kBM], merge_p[kBM];  // group B's row state for the final merge
-  float merge_r[kMaxRegions][kBM];
   uint64_t q_full;
   uint64_t k_full[kKStages], k_empty[kKStages], v_full[kVStages], v_empty[kVStages];
-  uint64_t s_full[2], p_full[2], o_done[2], mma_done;
+  uint64_t s_full[2], s_free[2], p_full[2], o_done[2], mma_done;
   uint32_t tmem_base;
   int abort_flag;
 };
+
+// Group B's row state for the final merge, laid over K stage 0, which no copy
+// or MMA touches any more once group B has seen its last PV complete.
+struct MergeState {
+  float m[kBM], l[kBM], p[kBM];
+  float r[kMaxRegions][kBM];
+};
+static_assert(sizeof(MergeState) <= kTileBytes, "merge state fits a K stage");
 
 struct ChunkArgs {
   int n_q, n_kv, q_heads, kv_group, n_tiles;
@@ -228,35 +234,61 @@ __device__ __forceinline__ float row_max(uint32_t taddr, int valid) {
   return fmaxf(mx0, mx1);
 }
 
+// Paired fp32 arithmetic (one instruction for two lanes of work):
+// (y0, y1) = (x0, x1) * (s, s) + (n, n), and (a0, a1) += (x0, x1).
+__device__ __forceinline__ void fma2(float &y0, float &y1, float x0, float x1, float s, float n) {
+  asm("{\n\t.reg .b64 x, s, n, y;\n\t"
+      "mov.b64 x, {%2, %3};\n\tmov.b64 s, {%4, %4};\n\tmov.b64 n, {%5, %5};\n\t"
+      "fma.rn.f32x2 y, x, s, n;\n\tmov.b64 {%0, %1}, y;\n\t}"
+      : "=f"(y0), "=f"(y1)
+      : "f"(x0), "f"(x1), "f"(s), "f"(n));
+}
+__device__ __forceinline__ void add2(float &a0, float &a1, float x0, float x1) {
+  asm("{\n\t.reg .b64 a, x;\n\t"
+      "mov.b64 a, {%0, %1};\n\tmov.b64 x, {%2, %3};\n\t"
+      "add.rn.f32x2 a, a, x;\n\tmov.b64 {%0, %1}, a;\n\t}"
+      : "+f"(a0), "+f"(a1)
+      : "f"(x0), "f"(x1));
+}
+
 // 32 columns of the pass: P = 2^(s * scale + neg_m) for the valid ones (0
 // beyond), raw maximum, P to shared memory as bf16, the chunk's sum. Region
 // sums are left to the caller unless kSplit (the tile straddles a region
 // bound), when they are taken here element by element.
-template <bool kSplit>
+template <bool kSplit, bool kMax = true>
 __device__ __forceinline__ void softmax_chunk(float (&v)[32], int c, int valid, int t0,
                                               float scale, float neg_m, const Regions &reg,
                                               uint8_t *p, int row, float &cs,
                                               float (&part)[kMaxRegions], float &mx0, float &mx1) {
   float ps4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
   if (32 * c + 32 <= valid) {
+    if (kMax) {
 #pragma unroll
-    for (int e = 0; e < 32; e += 2) {
-      mx0 = fmaxf(mx0, v[e]);
-      mx1 = fmaxf(mx1, v[e + 1]);
+      for (int e = 0; e < 32; e += 2) {
+        mx0 = fmaxf(mx0, v[e]);
+        mx1 = fmaxf(mx1, v[e + 1]);
+      }
     }
 #pragma unroll
-    for (int e = 0; e < 32; ++e) {
-      v[e] = fast_exp2(fmaf(v[e], scale, neg_m));
-      ps4[e & 3] += v[e];
+    for (int e = 0; e < 32; e += 2) {
+      fma2(v[e], v[e + 1], v[e], v[e + 1], scale, neg_m);
+      v[e] = fast_exp2(v[e]);
+      v[e + 1] = fast_exp2(v[e + 1]);
+      if (e & 2)
+        add2(ps4[2], ps4[3], v[e], v[e + 1]);
+      else
+        add2(ps4[0], ps4[1], v[e], v[e + 1]);
     }
   } else {
 #pragma unroll
     for (int e = 0; e < 32; ++e) {
       const bool in = 32 * c + e < valid;
-      if (e & 1)
-        mx1 = fmaxf(mx1, in ? v[e] : -CUDART_INF_F);
-      else
-        mx0 = fmaxf(mx0, in ? v[e] : -CUDART_INF_F);
+      if (kMax) {
+        if (e & 1)
+          mx1 = fmaxf(mx1, in ? v[e] : -CUDART_INF_F);
+        else
+          mx0 = fmaxf(mx0, in ? v[e] : -CUDART_INF_F);
+      }
       v[e] = in ? fast_exp2(fmaf(v[e], scale, neg_m)) : 0.0f;
       ps4[e & 3] += v[e];
     }
@@ -287,34 +319,41 @@ __device__ __forceinline__ void softmax_chunk(float (&v)[32], int c, int valid, 
   }
 }
 
-// One pass over the 128 score columns of this thread's row; the TMEM load
-// of the next 32 columns is in flight while the current ones are processed.
+// The pass over the 128 score columns of this thread's row, up to the last
+// chunk: chunks 0-2 are exponentiated and stored while the TMEM load of the
+// next is in flight; chunk 3 is left raw in v3 and only folded into the
+// maximum, so that the caller can release S before finishing it.
 // cs[c]: sum of chunk c; part: region sums (kSplit only).
 template <bool kSplit>
-__device__ __forceinline__ void softmax_pass(uint32_t taddr, int valid, int t0, float scale,
-                                             float neg_m, const Regions &reg, uint8_t *p, int row,
-                                             float (&cs)[4], float (&part)[kMaxRegions],
-                                             float &mx) {
+__device__ __forceinline__ void softmax_pass_head(uint32_t taddr, int valid, int t0, float scale,
+                                                  float neg_m, const Regions &reg, uint8_t *p,
+                                                  int row, float (&cs)[4],
+                                                  float (&part)[kMaxRegions], float (&v3)[32],
+                                                  float &mx) {
 #pragma unroll
   for (int k = 0; k < kMaxRegions; ++k) part[k] = 0.0f;
   float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F;
-  float va[32], vb[32];
+  float va[32];
   tmem_ld32(taddr, va);
   tmem_wait_ld();
   reg_fence(va);
-  tmem_ld32(taddr + 32u, vb);
+  tmem_ld32(taddr + 32u, v3);
   softmax_chunk<kSplit>(va, 0, valid, t0, scale, neg_m, reg, p, row, cs[0], part, mx0, mx1);
   tmem_wait_ld();
-  reg_fence(vb);
+  reg_fence(v3);
   tmem_ld32(taddr + 64u, va);
-  softmax_chunk<kSplit>(vb, 1, valid, t0, scale, neg_m, reg, p, row, cs[1], part, mx0, mx1);
+  softmax_chunk<kSplit>(v3, 1, valid, t0, scale, neg_m, reg, p, row, cs[1], part, mx0, mx1);
   tmem_wait_ld();
   reg_fence(va);
-  tmem_ld32(taddr + 96u, vb);
+  tmem_ld32(taddr + 96u, v3);
   softmax_chunk<kSplit>(va, 2, valid, t0, scale, neg_m, reg, p, row, cs[2], part, mx0, mx1);
   tmem_wait_ld();
-  reg_fence(vb);
-  softmax_chunk<kSplit>(vb, 3, valid, t0, scale, neg_m, reg, p, row, cs[3], part, mx0, mx1);
+  reg_fence(v3);
+#pragma unroll
+  for (int e = 0; e < 32; e += 2) {
+    mx0 = fmaxf(mx0, 96 + e < valid ? v3[e] : -CUDART_INF_F);
+    mx1 = fmaxf(mx1, 97 + e < valid ? v3[e + 1] : -CUDART_INF_F);
+  }
   mx = fmaxf(mx0, mx1);
 }
 
@@ -344,6 +383,7 @@ __global__ void __launch_bounds__(384, 1)
     }
     for (int g = 0; g < 2; ++g) {
       mbar_init(smem_u32(&sm.s_full[g]), 1);
+      mbar_init(smem_u32(&sm.s_free[g]), 128);
       mbar_init(smem_u32(&sm.p_full[g]), 128);
       mbar_init(smem_u32(&sm.o_done[g]), 1);
     }
@@ -366,26 +406,33 @@ __global__ void __launch_bounds__(384, 1)
   auto t_o = [&](int g) { return tmem + 256u * g + 128u; };
 
   if (warp == 0) {
-    // ------------------------------------------------ TMA producer
+    // ------------------------------------------------ TMA producer: Q, then K tiles
     if (lane == 0) {
       const uint32_t qb = smem_u32(&sm.q_full);
       mbar_arrive_expect_tx(qb, kTileBytes);
       tma_load_3d(smem_u32(sm.q), &tm_q, 0, q0, hq, qb);
       tma_load_3d(smem_u32(sm.q) + kHalfBytes, &tm_q, 64, q0, hq, qb);
-      // K tile j then V tile j, each into its own ring; a slot is reused once
-      // the MMA reading it has completed
-      int kj = 0, vj = 0;
-      while (vj < nt) {
-        if (kj == vj) {
-          const int st = kj % kKStages, use = kj / kKStages;
-          if (use > 0 && !wait_or_abort(sm, smem_u32(&sm.k_empty[st]), (use - 1) & 1, a.ctl)) break;
-          if (cta_aborted(sm)) break;
-          const uint32_t fb = smem_u32(&sm.k_full[st]);
-          mbar_arrive_expect_tx(fb, kTileBytes);
-          tma_load_3d(smem_u32(sm.k[st]), &tm_k, 0, kj * kBN, hkv, fb);
-          tma_load_3d(smem_u32(sm.k[st]) + kHalfBytes, &tm_k, 64, kj * kBN, hkv, fb);
-          ++kj;
-        }
+      // a stage is reused once the MMA reading it has completed
+      int kj = 0;
+      for (; kj < nt; ++kj) {
+        const int st = kj % kKStages, use = kj / kKStages;
+        if (use > 0 && !wait_or_abort(sm, smem_u32(&sm.k_empty[st]), (use - 1) & 1, a.ctl)) break;
+        if (cta_aborted(sm)) break;
+        const uint32_t fb = smem_u32(&sm.k_full[st]);
+        mbar_arrive_expect_tx(fb, kTileBytes);
+        tma_load_3d(smem_u32(sm.k[st]), &tm_k, 0, kj * kBN, hkv, fb);
+        tma_load_3d(smem_u32(sm.k[st]) + kHalfBytes, &tm_k, 64, kj * kBN, hkv, fb);
+      }
+      // drain: the copies of the last stages must land before the CTA exits
+      mbar_wait(qb, 0, 2000000000ull);
+      for (int d = (kj > kKStages ? kj - kKStages : 0); d < kj; ++d)
+        mbar_wait(smem_u32(&sm.k_full[d % kKStages]), (d / kKStages) & 1, 2000000000ull);
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------ TMA producer: V tiles
+    if (lane == 0) {
+      int vj = 0;
+      for (; vj < nt; ++vj) {
         const int st = vj % kVStages, use = vj / kVStages;
         if (use > 0 && !wait_or_abort(sm, smem_u32(&sm.v_empty[st]), (use - 1) & 1, a.ctl)) break;
         if (cta_aborted(sm)) break;
@@ -393,12 +440,7 @@ __global__ void __launch_bounds__(384, 1)
         mbar_arrive_expect_tx(fb, kTileBytes);
         tma_load_3d(smem_u32(sm.v[st]), &tm_v, 0, vj * kBN, hkv, fb);
         tma_load_3d(smem_u32(sm.v[st]) + kHalfBytes, &tm_v, 64, vj * kBN, hkv, fb);
-        ++vj;
       }
-      // drain: the copies of the last slots must land before the CTA exits
-      mbar_wait(qb, 0, 2000000000ull);
-      for (int d = (kj > kKStages ? kj - kKStages : 0); d < kj; ++d)
-        mbar_wait(smem_u32(&sm.k_full[d % kKStages]), (d / kKStages) & 1, 2000000000ull);
       for (int d = (vj > kVStages ? vj - kVStages : 0); d < vj; ++d)
         mbar_wait(smem_u32(&sm.v_full[d % kVStages]), (d / kVStages) & 1, 2000000000ull);
     }
@@ -428,6 +470,13 @@ __global__ void __launch_bounds__(384, 1)
       if (ok && nt > 1) ok = issue_s(1);
       for (int j = 0; ok && j < nt; ++j) {
         const int st = j % kVStages, g = j & 1, i = j >> 1;
+        // S_g can take tile j + 2 as soon as group g holds tile j's scores in
+        // registers, before its P is written
+        if (j + 2 < nt && (!wait_or_abort(sm, smem_u32(&sm.s_free[g]), i & 1, a.ctl) ||
+                           !issue_s(j + 2))) {
+          ok = false;
+          break;
+        }
         // O_g += P_g V_j once group g has written P for tile j
         if (!wait_or_abort(sm, smem_u32(&sm.p_full[g]), i & 1, a.ctl) ||
             !wait_or_abort(sm, smem_u32(&sm.v_full[st]), (j / kVStages) & 1, a.ctl)) {
@@ -444,11 +493,6 @@ __global__ void __launch_bounds__(384, 1)
         }
         tc_commit(smem_u32(&sm.o_done[g]));
         tc_commit(smem_u32(&sm.v_empty[st]));
-        // group g has read S for tile j (it wrote P after), so S_g can take tile j + 2
-        if (j + 2 < nt && !issue_s(j + 2)) {
-          ok = false;
-          break;
-        }
       }
       // all MMAs of this CTA complete before TMEM is released
       tc_commit(smem_u32(&sm.mma_done));
@@ -508,16 +552,18 @@ __global__ void __launch_bounds__(384, 1)
         }
       }
       // one pass: P = 2^(s * scale - m_used) -> shared memory, sums, raw max
-      float cs[4], part[kMaxRegions], mx;
+      float cs[4], part[kMaxRegions], v3[32], mx, dummy0 = 0.0f, dummy1 = 0.0f;
       if (split)
-        softmax_pass<true>(s_row, valid, t0, a.scale_log2, -m_used, a.reg, sm.p[g], row, cs, part, mx);
+        softmax_pass_head<true>(s_row, valid, t0, a.scale_log2, -m_used, a.reg, sm.p[g], row, cs,
+                                part, v3, mx);
       else
-        softmax_pass<false>(s_row, valid, t0, a.scale_log2, -m_used, a.reg, sm.p[g], row, cs, part, mx);
+        softmax_pass_head<false>(s_row, valid, t0, a.scale_log2, -m_used, a.reg, sm.p[g], row, cs,
+                                 part, v3, mx);
       const float mt = mx * a.scale_log2;  // scaled tile maximum
       if (__any_sync(0xffffffffu, mt > m_used + kRedoThreshold)) {
         // far above the reference for some row (P could overflow): the warp
-        // takes the tile maxima now and recomputes the tile (TMEM access is
-        // warp-wide); O_g is idle, its last MMA is done
+        // takes the tile maxima now and redoes the tile from its scores, still
+        // in TMEM (TMEM access is warp-wide); O_g is idle, its last MMA is done
         const float m_new = fmaxf(m_used, mt);
         const float f = fast_exp2(m_used - m_new);
         m_used = m_new;
@@ -529,10 +575,21 @@ __global__ void __launch_bounds__(384, 1)
           scale_tmem_row(o_row, f);
         }
         if (split)
-          softmax_pass<true>(s_row, valid, t0, a.scale_log2, -m_used, a.reg, sm.p[g], row, cs, part, mx);
+          softmax_pass_head<true>(s_row, valid, t0, a.scale_log2, -m_used, a.reg, sm.p[g], row, cs,
+                                  part, v3, mx);
         else
-          softmax_pass<false>(s_row, valid, t0, a.scale_log2, -m_used, a.reg, sm.p[g], row, cs, part, mx);
+          softmax_pass_head<false>(s_row, valid, t0, a.scale_log2, -m_used, a.reg, sm.p[g], row,
+                                   cs, part, v3, mx);
       }
+      // every score of the tile is in registers: S_g may take the next tile
+      tc_fence_before();
+      mbar_arrive(smem_u32(&sm.s_free[g]));
+      if (split)
+        softmax_chunk<true, false>(v3, 3, valid, t0, a.scale_log2, -m_used, a.reg, sm.p[g], row,
+                                   cs[3], part, dummy0, dummy1);
+      else
+        softmax_chunk<false, false>(v3, 3, valid, t0, a.scale_log2, -m_used, a.reg, sm.p[g], row,
+                                    cs[3], part, dummy0, dummy1);
       // P is complete: hand it to the MMA warp, then do the bookkeeping
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       tc_fence_before();
@@ -560,12 +617,15 @@ __global__ void __launch_bounds__(384, 1)
     const bool last_ok =
         ok && my_tiles > 0 &&
         wait_or_abort(sm, smem_u32(&sm.o_done[g]), (my_tiles - 1) & 1, a.ctl);
-    if (g == 1) {
-      sm.merge_m[row] = last_ok ? m_used : -CUDART_INF_F;
-      sm.merge_l[row] = last_ok ? l : 0.0f;
-      sm.merge_p[row] = pend;
+    // only after its last PV completed may group B write over K stage 0 (a
+    // group B without tiles writes nothing; group A then ignores it)
+    MergeState &ms = *reinterpret_cast<MergeState *>(sm.k[0]);
+    if (g == 1 && last_ok) {
+      ms.m[row] = m_used;
+      ms.l[row] = l;
+      ms.p[row] = pend;
 #pragma unroll
-      for (int k = 0; k < kMaxRegions; ++k) sm.merge_r[k][row] = last_ok ? rsum[k] : 0.0f;
+      for (int k = 0; k < kMaxRegions; ++k) ms.r[k][row] = rsum[k];
     }
     tc_fence_before();
     asm volatile("bar.sync 2, 256;" ::: "memory");
@@ -574,15 +634,15 @@ __global__ void __launch_bounds__(384, 1)
         (tiles_b == 0 ||
          wait_or_abort(sm, smem_u32(&sm.o_done[1]), (tiles_b - 1) & 1, a.ctl))) {
       tc_fence_after();
-      const float mb = sm.merge_m[row];
       const bool have_b = nt > 1;  // group B processed at least one tile
+      const float mb = have_b ? ms.m[row] : -CUDART_INF_F;
       const float mm = fmaxf(m_used, mb);
       const float fa = exp2f(m_used - mm);
       const float fb = have_b ? exp2f(mb - mm) : 0.0f;
-      const float lt = fa * l + fb * sm.merge_l[row];
+      const float lt = fa * l + (have_b ? fb * ms.l[row] : 0.0f);
       const float inv = 1.0f / lt;
       // O_A and O_B still owe their last reference change
-      const float oa = fa * pend, ob = fb * sm.merge_p[row];
+      const float oa = fa * pend, ob = have_b ? fb * ms.p[row] : 0.0f;
       const int qrow = q0 + row;
       const long obase = (static_cast<long>(hq) * a.n_q + qrow) * kDim;
 #pragma unroll
@@ -616,7 +676,7 @@ __global__ void __launch_bounds__(384, 1)
       if (a.mass && qrow < a.n_q)
         for (int k = 0; k < a.reg.n && k < kMaxRegions; ++k)
           a.mass[(static_cast<long>(hq) * a.n_q + qrow) * a.reg.n + k] =
-              (fa * rsum[k] + fb * sm.merge_r[k][row]) * inv;
+              (fa * rsum[k] + (have_b ? fb * ms.r[k][row] : 0.0f)) * inv;
     }
   }
   tc_fence_before();
@@ -769,6 +829,7 @@ int launch_attend_chunk(const kvq_cache &c, const void *q, int Hq, int n_q, floa
   a.mass = mass;
   a.reg = make_regions(bounds, n_regions);
   a.ctl = ctl;
+  static_assert(sizeof(ChunkSmem) + 1024 <= 232448, "chunk kernel shared memory");
   const size_t smem = sizeof(ChunkSmem) + 1024;
   cudaFuncSetAttribute(chunk_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        static_cast<int>(smem));
