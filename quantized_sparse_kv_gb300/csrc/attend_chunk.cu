@@ -349,10 +349,18 @@ __device__ __forceinline__ void softmax_pass_head(uint32_t taddr, int valid, int
   softmax_chunk<kSplit>(va, 2, valid, t0, scale, neg_m, reg, p, row, cs[2], part, mx0, mx1);
   tmem_wait_ld();
   reg_fence(v3);
+  if (valid == kBN) {
 #pragma unroll
-  for (int e = 0; e < 32; e += 2) {
-    mx0 = fmaxf(mx0, 96 + e < valid ? v3[e] : -CUDART_INF_F);
-    mx1 = fmaxf(mx1, 97 + e < valid ? v3[e + 1] : -CUDART_INF_F);
+    for (int e = 0; e < 32; e += 2) {
+      mx0 = fmaxf(mx0, v3[e]);
+      mx1 = fmaxf(mx1, v3[e + 1]);
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) {
+      mx0 = fmaxf(mx0, 96 + e < valid ? v3[e] : -CUDART_INF_F);
+      mx1 = fmaxf(mx1, 97 + e < valid ? v3[e + 1] : -CUDART_INF_F);
+    }
   }
   mx = fmaxf(mx0, mx1);
 }
@@ -594,16 +602,21 @@ __global__ void __launch_bounds__(384, 1)
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       tc_fence_before();
       mbar_arrive(smem_u32(&sm.p_full[g]));
-      l += (cs[0] + cs[1]) + (cs[2] + cs[3]);
-      if (!split) {
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int k = 0; k < kMaxRegions; ++k) part[k] += (kc[c] == k) ? cs[c] : 0.0f;
-      }
+      const float tile_sum = (cs[0] + cs[1]) + (cs[2] + cs[3]);
+      l += tile_sum;
       if (a.reg.n > 0) {
+        if (split) {
 #pragma unroll
-        for (int k = 0; k < kMaxRegions; ++k) rsum[k] += part[k];
+          for (int k = 0; k < kMaxRegions; ++k) rsum[k] += part[k];
+        } else if (kc[0] == kc[3]) {  // the whole tile in one region
+#pragma unroll
+          for (int k = 0; k < kMaxRegions; ++k) rsum[k] += (kc[0] == k) ? tile_sum : 0.0f;
+        } else {
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int k = 0; k < kMaxRegions; ++k) rsum[k] += (kc[c] == k) ? cs[c] : 0.0f;
+        }
       }
       if (mt > m_used + kRescaleThreshold) {
         pend = fast_exp2(m_used - mt);

@@ -25,10 +25,58 @@ __device__ __forceinline__ int int4_code(float x, float scale) {
   return max(-7, min(7, c));
 }
 
+// 32 consecutive elements as floats, 16-byte loads.
+__device__ __forceinline__ void load32(const float *p, float (&x)[32]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float4 f = reinterpret_cast<const float4 *>(p)[i];
+    x[4 * i] = f.x;
+    x[4 * i + 1] = f.y;
+    x[4 * i + 2] = f.z;
+    x[4 * i + 3] = f.w;
+  }
+}
+__device__ __forceinline__ void load32(const __nv_bfloat16 *p, float (&x)[32]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint4 u = reinterpret_cast<const uint4 *>(p)[i];
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      x[8 * i + 2 * j] = __uint_as_float(w[j] << 16);
+      x[8 * i + 2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
+    }
+  }
+}
+
+// The K loads of one channel pair and token as they sit in memory: a bf16
+// pair stays packed in one register until it is used (half the registers
+// of two floats, so more groups are in flight per SM).
+struct PairBF16 {
+  uint32_t w;
+  __device__ __forceinline__ void load(const __nv_bfloat16 *p) {
+    w = *reinterpret_cast<const uint32_t *>(p);
+  }
+  __device__ __forceinline__ void zero() { w = 0u; }
+  __device__ __forceinline__ float lo() const { return __uint_as_float(w << 16); }
+  __device__ __forceinline__ float hi() const { return __uint_as_float(w & 0xffff0000u); }
+};
+struct PairF32 {
+  float2 f;
+  __device__ __forceinline__ void load(const float *p) { f = *reinterpret_cast<const float2 *>(p); }
+  __device__ __forceinline__ void zero() { f = make_float2(0.0f, 0.0f); }
+  __device__ __forceinline__ float lo() const { return f.x; }
+  __device__ __forceinline__ float hi() const { return f.y; }
+};
+template <typename T> struct PairOf;
+template <> struct PairOf<float> { using type = PairF32; };
+template <> struct PairOf<__nv_bfloat16> { using type = PairBF16; };
+
 // K: one thread per (sequence*head, K group, channel pair). A warp's threads
-// read adjacent channel pairs of the same token (coalesced), keep the 32 x 2
-// values in registers, and write the pair's byte for each of the 32 tokens
-// (adjacent threads -> adjacent bytes) and its two scales.
+// read adjacent channel pairs of the same token (one 128-byte line per load
+// for bf16), keep the group's 32 pairs in registers, and write the pair's
+// byte for each of the 32 tokens (adjacent threads -> adjacent bytes) and
+// its two scales.
 template <typename T>
 __global__ void __launch_bounds__(256) pack_k_kernel(const T *__restrict__ k, long tasks, int N,
                                                      int D, int cut, int Gk,
@@ -43,25 +91,31 @@ __global__ void __launch_bounds__(256) pack_k_kernel(const T *__restrict__ k, lo
   const long u = ug / Gk;
   const int valid = min(kGroup, cut - g * kGroup);
   const T *src = k + (u * N + static_cast<long>(g) * kGroup) * D + 2 * p;
-  float x0[kGroup], x1[kGroup];
+  typename PairOf<T>::type x[kGroup];
+#pragma unroll
+  for (int t = 0; t < kGroup; ++t) {
+    if (t < valid)
+      x[t].load(src + static_cast<long>(t) * D);
+    else
+      x[t].zero();
+  }
   float a0 = 0.0f, a1 = 0.0f;
 #pragma unroll
   for (int t = 0; t < kGroup; ++t) {
-    x0[t] = t < valid ? load_f32(src + static_cast<long>(t) * D) : 0.0f;
-    x1[t] = t < valid ? load_f32(src + static_cast<long>(t) * D + 1) : 0.0f;
-    a0 = fmaxf(a0, fabsf(x0[t]));
-    a1 = fmaxf(a1, fabsf(x1[t]));
+    a0 = fmaxf(a0, fabsf(x[t].lo()));
+    a1 = fmaxf(a1, fabsf(x[t].hi()));
   }
   const float s0 = int4_scale(a0), s1 = int4_scale(a1);
   *reinterpret_cast<float2 *>(k_scales + ug * D + 2 * p) = make_float2(s0, s1);
   uint8_t *dst = k_codes + ug * (kGroup * D / 2) + p;
 #pragma unroll
   for (int t = 0; t < kGroup; ++t)
-    dst[t * (D / 2)] = static_cast<uint8_t>((int4_code(x0[t], s0) + 8) | ((int4_code(x1[t], s1) + 8) << 4));
+    dst[t * (D / 2)] =
+        static_cast<uint8_t>((int4_code(x[t].lo(), s0) + 8) | ((int4_code(x[t].hi(), s1) + 8) << 4));
 }
 
 // V: one thread per (token, 32-feature group) of the quantized part; 32 values
-// in, 16 code bytes and one scale out.
+// in (16-byte loads), 16 code bytes and one scale out.
 template <typename T>
 __global__ void __launch_bounds__(256) pack_v_kernel(const T *__restrict__ v, long rows, int N,
                                                      int D, int cut,
@@ -74,14 +128,11 @@ __global__ void __launch_bounds__(256) pack_v_kernel(const T *__restrict__ v, lo
   const int j = static_cast<int>(task % groups);
   const long u = row / cut;
   const long t = row % cut;
-  const T *src = v + (u * N + t) * D + j * kGroup;
   float x[kGroup];
+  load32(v + (u * N + t) * D + j * kGroup, x);
   float amax = 0.0f;
 #pragma unroll
-  for (int e = 0; e < kGroup; ++e) {
-    x[e] = load_f32(src + e);
-    amax = fmaxf(amax, fabsf(x[e]));
-  }
+  for (int e = 0; e < kGroup; ++e) amax = fmaxf(amax, fabsf(x[e]));
   const float s = int4_scale(amax);
   uint32_t w[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
