@@ -49,6 +49,79 @@ __device__ __forceinline__ void load32(const __nv_bfloat16 *p, float (&x)[32]) {
   }
 }
 
+// 16 consecutive elements as floats (16-byte loads).
+__device__ __forceinline__ void load16(const float *p, float (&x)[16]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float4 f = reinterpret_cast<const float4 *>(p)[i];
+    x[4 * i] = f.x;
+    x[4 * i + 1] = f.y;
+    x[4 * i + 2] = f.z;
+    x[4 * i + 3] = f.w;
+  }
+}
+__device__ __forceinline__ void load16(const __nv_bfloat16 *p, float (&x)[16]) {
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const uint4 u = reinterpret_cast<const uint4 *>(p)[i];
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      x[8 * i + 2 * j] = __uint_as_float(w[j] << 16);
+      x[8 * i + 2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
+    }
+  }
+}
+
+// K, head dim 128: one CTA of 256 threads per (sequence*head, K group).
+// Thread (t, q) holds channels 16q..16q+15 of token t (two 16-byte loads for
+// bf16); the per-channel maximum over the 32 tokens is reduced over the four
+// tokens of a warp with shuffles and over the eight warps in shared memory;
+// every thread then writes the 8 code bytes of its 16 channels.
+template <typename T>
+__global__ void __launch_bounds__(256) pack_k128_kernel(const T *__restrict__ k, int N, int cut,
+                                                        int Gk, uint8_t *__restrict__ k_codes,
+                                                        float *__restrict__ k_scales) {
+  constexpr int D = 128;
+  __shared__ float part[8][D];
+  __shared__ float scale[D];
+  const long ug = blockIdx.x;  // unit * Gk + g
+  const int g = static_cast<int>(ug % Gk);
+  const long u = ug / Gk;
+  const int t = threadIdx.x >> 3, q = threadIdx.x & 7;  // token, 16-channel slice
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int valid = min(kGroup, cut - g * kGroup);
+  float x[16];
+  if (t < valid)
+    load16(k + (u * N + static_cast<long>(g) * kGroup + t) * D + 16 * q, x);
+  else
+#pragma unroll
+    for (int e = 0; e < 16; ++e) x[e] = 0.0f;
+  // lanes q, q+8, q+16, q+24 of a warp hold the same channels (4 tokens)
+#pragma unroll
+  for (int e = 0; e < 16; ++e) {
+    float m = fabsf(x[e]);
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+    if (lane < 8) part[warp][16 * q + e] = m;
+  }
+  __syncthreads();
+  if (threadIdx.x < D) {
+    float m = part[0][threadIdx.x];
+#pragma unroll
+    for (int w = 1; w < 8; ++w) m = fmaxf(m, part[w][threadIdx.x]);
+    const float sc = int4_scale(m);
+    scale[threadIdx.x] = sc;
+    k_scales[ug * D + threadIdx.x] = sc;
+  }
+  __syncthreads();
+  uint32_t w[2] = {0u, 0u};
+#pragma unroll
+  for (int e = 0; e < 16; ++e)
+    w[e >> 3] |= static_cast<uint32_t>(int4_code(x[e], scale[16 * q + e]) + 8) << (4 * (e & 7));
+  *reinterpret_cast<uint2 *>(k_codes + (ug * kGroup + t) * (D / 2) + 8 * q) = make_uint2(w[0], w[1]);
+}
+
 // The K loads of one channel pair and token as they sit in memory: a bf16
 // pair stays packed in one register until it is used (half the registers
 // of two floats, so more groups are in flight per SM).
@@ -190,9 +263,14 @@ int pack_typed(const T *k, const T *v, const kvq_cache &c, cudaStream_t s) {
   const long units = static_cast<long>(d.B) * d.Hkv;
   int launches = 0;
   if (d.cut > 0) {
-    const long ktasks = units * d.Gk * (d.D / 2);
-    pack_k_kernel<T><<<static_cast<unsigned>((ktasks + 255) / 256), 256, 0, s>>>(
-        k, ktasks, d.N, d.D, d.cut, d.Gk, c.k_codes, c.k_scales);
+    if (d.D == 128) {
+      pack_k128_kernel<T><<<static_cast<unsigned>(units * d.Gk), 256, 0, s>>>(
+          k, d.N, d.cut, d.Gk, c.k_codes, c.k_scales);
+    } else {
+      const long ktasks = units * d.Gk * (d.D / 2);
+      pack_k_kernel<T><<<static_cast<unsigned>((ktasks + 255) / 256), 256, 0, s>>>(
+          k, ktasks, d.N, d.D, d.cut, d.Gk, c.k_codes, c.k_scales);
+    }
     const long rows = units * d.cut;
     const long vtasks = rows * (d.D / kGroup);
     pack_v_kernel<T><<<static_cast<unsigned>((vtasks + 255) / 256), 256, 0, s>>>(
