@@ -25,101 +25,74 @@ __device__ __forceinline__ int int4_code(float x, float scale) {
   return max(-7, min(7, c));
 }
 
-// 32 consecutive elements as floats, 16-byte loads.
-__device__ __forceinline__ void load32(const float *p, float (&x)[32]) {
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const float4 f = reinterpret_cast<const float4 *>(p)[i];
-    x[4 * i] = f.x;
-    x[4 * i + 1] = f.y;
-    x[4 * i + 2] = f.z;
-    x[4 * i + 3] = f.w;
-  }
+// Four consecutive elements as floats (one 8- or 16-byte load).
+__device__ __forceinline__ void load4(const float *p, float (&x)[4]) {
+  const float4 f = *reinterpret_cast<const float4 *>(p);
+  x[0] = f.x;
+  x[1] = f.y;
+  x[2] = f.z;
+  x[3] = f.w;
 }
-__device__ __forceinline__ void load32(const __nv_bfloat16 *p, float (&x)[32]) {
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint4 u = reinterpret_cast<const uint4 *>(p)[i];
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      x[8 * i + 2 * j] = __uint_as_float(w[j] << 16);
-      x[8 * i + 2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
-    }
-  }
-}
-
-// 16 consecutive elements as floats (16-byte loads).
-__device__ __forceinline__ void load16(const float *p, float (&x)[16]) {
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float4 f = reinterpret_cast<const float4 *>(p)[i];
-    x[4 * i] = f.x;
-    x[4 * i + 1] = f.y;
-    x[4 * i + 2] = f.z;
-    x[4 * i + 3] = f.w;
-  }
-}
-__device__ __forceinline__ void load16(const __nv_bfloat16 *p, float (&x)[16]) {
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const uint4 u = reinterpret_cast<const uint4 *>(p)[i];
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      x[8 * i + 2 * j] = __uint_as_float(w[j] << 16);
-      x[8 * i + 2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
-    }
-  }
+__device__ __forceinline__ void load4(const __nv_bfloat16 *p, float (&x)[4]) {
+  const uint2 u = *reinterpret_cast<const uint2 *>(p);
+  x[0] = __uint_as_float(u.x << 16);
+  x[1] = __uint_as_float(u.x & 0xffff0000u);
+  x[2] = __uint_as_float(u.y << 16);
+  x[3] = __uint_as_float(u.y & 0xffff0000u);
 }
 
 // K, head dim 128: one CTA of 256 threads per (sequence*head, K group).
-// Thread (t, q) holds channels 16q..16q+15 of token t (two 16-byte loads for
-// bf16); the per-channel maximum over the 32 tokens is reduced over the four
-// tokens of a warp with shuffles and over the eight warps in shared memory;
-// every thread then writes the 8 code bytes of its 16 channels.
+// Warp w holds tokens 4w..4w+3 and lane l channels 4l..4l+3, so every load
+// of a warp is one whole token row; the per-channel maximum over the 32
+// tokens is taken over the thread's four tokens and then across the eight
+// warps in shared memory, and each thread writes 2 code bytes per token.
 template <typename T>
 __global__ void __launch_bounds__(256) pack_k128_kernel(const T *__restrict__ k, int N, int cut,
-                                                        int Gk, uint8_t *__restrict__ k_codes,
+                                                        int Gk, long u0,
+                                                        uint8_t *__restrict__ k_codes,
                                                         float *__restrict__ k_scales) {
   constexpr int D = 128;
-  __shared__ float part[8][D];
-  __shared__ float scale[D];
-  const long ug = blockIdx.x;  // unit * Gk + g
-  const int g = static_cast<int>(ug % Gk);
-  const long u = ug / Gk;
-  const int t = threadIdx.x >> 3, q = threadIdx.x & 7;  // token, 16-channel slice
+  __shared__ __align__(16) float part[8][D];
+  __shared__ __align__(16) float scale[D];
+  const int g = blockIdx.x;              // K group
+  const long u = u0 + blockIdx.y;        // (sequence, head)
+  const long ug = u * Gk + g;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int valid = min(kGroup, cut - g * kGroup);
-  float x[16];
-  if (t < valid)
-    load16(k + (u * N + static_cast<long>(g) * kGroup + t) * D + 16 * q, x);
-  else
+  const T *src = k + (u * N + static_cast<long>(g) * kGroup) * D + 4 * lane;
+  float x[4][4];
+  float m[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-    for (int e = 0; e < 16; ++e) x[e] = 0.0f;
-  // lanes q, q+8, q+16, q+24 of a warp hold the same channels (4 tokens)
+  for (int i = 0; i < 4; ++i) {
+    const int t = 4 * warp + i;
+    if (t < valid)
+      load4(src + static_cast<long>(t) * D, x[i]);
+    else
+      x[i][0] = x[i][1] = x[i][2] = x[i][3] = 0.0f;
 #pragma unroll
-  for (int e = 0; e < 16; ++e) {
-    float m = fabsf(x[e]);
-    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
-    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
-    if (lane < 8) part[warp][16 * q + e] = m;
+    for (int e = 0; e < 4; ++e) m[e] = fmaxf(m[e], fabsf(x[i][e]));
   }
+  *reinterpret_cast<float4 *>(&part[warp][4 * lane]) = make_float4(m[0], m[1], m[2], m[3]);
   __syncthreads();
   if (threadIdx.x < D) {
-    float m = part[0][threadIdx.x];
+    float mx = part[0][threadIdx.x];
 #pragma unroll
-    for (int w = 1; w < 8; ++w) m = fmaxf(m, part[w][threadIdx.x]);
-    const float sc = int4_scale(m);
+    for (int w = 1; w < 8; ++w) mx = fmaxf(mx, part[w][threadIdx.x]);
+    const float sc = int4_scale(mx);
     scale[threadIdx.x] = sc;
     k_scales[ug * D + threadIdx.x] = sc;
   }
   __syncthreads();
-  uint32_t w[2] = {0u, 0u};
+  const float4 sc = *reinterpret_cast<const float4 *>(&scale[4 * lane]);
+  const float s4[4] = {sc.x, sc.y, sc.z, sc.w};
 #pragma unroll
-  for (int e = 0; e < 16; ++e)
-    w[e >> 3] |= static_cast<uint32_t>(int4_code(x[e], scale[16 * q + e]) + 8) << (4 * (e & 7));
-  *reinterpret_cast<uint2 *>(k_codes + (ug * kGroup + t) * (D / 2) + 8 * q) = make_uint2(w[0], w[1]);
+  for (int i = 0; i < 4; ++i) {
+    uint32_t w = 0u;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) w |= static_cast<uint32_t>(int4_code(x[i][e], s4[e]) + 8) << (4 * e);
+    *reinterpret_cast<uint16_t *>(k_codes + (ug * kGroup + 4 * warp + i) * (D / 2) + 2 * lane) =
+        static_cast<uint16_t>(w);
+  }
 }
 
 // The K loads of one channel pair and token as they sit in memory: a bf16
@@ -187,32 +160,49 @@ __global__ void __launch_bounds__(256) pack_k_kernel(const T *__restrict__ k, lo
         static_cast<uint8_t>((int4_code(x[t].lo(), s0) + 8) | ((int4_code(x[t].hi(), s1) + 8) << 4));
 }
 
-// V: one thread per (token, 32-feature group) of the quantized part; 32 values
-// in (16-byte loads), 16 code bytes and one scale out.
+// V: four lanes per (token, 32-feature group) of the quantized part, each
+// with 8 consecutive values, so a warp's loads cover 8 whole groups
+// contiguously; the group maximum takes two shuffles, and each lane writes
+// its 4 code bytes (the leader also the scale).
 template <typename T>
-__global__ void __launch_bounds__(256) pack_v_kernel(const T *__restrict__ v, long rows, int N,
-                                                     int D, int cut,
+__global__ void __launch_bounds__(256) pack_v_kernel(const T *__restrict__ v, long u0, int t0,
+                                                     int nt, int N, int D, int cut,
                                                      uint8_t *__restrict__ v_codes,
                                                      float *__restrict__ v_scales) {
   const int groups = D / kGroup;
-  const long task = blockIdx.x * static_cast<long>(blockDim.x) + threadIdx.x;
-  if (task >= rows * groups) return;
-  const long row = task / groups;  // over (unit, token < cut)
-  const int j = static_cast<int>(task % groups);
-  const long u = row / cut;
-  const long t = row % cut;
-  float x[kGroup];
-  load32(v + (u * N + t) * D + j * kGroup, x);
+  const unsigned tid = blockIdx.x * blockDim.x + threadIdx.x;  // within the slice
+  const unsigned task = tid >> 2;                               // (token, group)
+  const int part = static_cast<int>(tid & 3);
+  const bool live = task < static_cast<unsigned>(nt) * groups;
+  const unsigned tk = live ? task : 0u;
+  const int t = t0 + static_cast<int>(tk / groups);  // token < cut
+  const int j = static_cast<int>(tk % groups);
+  const long u = u0 + blockIdx.y;
+  const long row = u * cut + t;  // over (unit, token < cut)
+  const T *src = v + (u * N + t) * D + j * kGroup + 8 * part;
+  float x[8];
+  {
+    float a4[4], b4[4];
+    load4(src, a4);
+    load4(src + 4, b4);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      x[e] = a4[e];
+      x[4 + e] = b4[e];
+    }
+  }
   float amax = 0.0f;
 #pragma unroll
-  for (int e = 0; e < kGroup; ++e) amax = fmaxf(amax, fabsf(x[e]));
+  for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(x[e]));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+  if (!live) return;
   const float s = int4_scale(amax);
-  uint32_t w[4] = {0u, 0u, 0u, 0u};
+  uint32_t w = 0u;
 #pragma unroll
-  for (int e = 0; e < kGroup; ++e)
-    w[e >> 3] |= static_cast<uint32_t>(int4_code(x[e], s) + 8) << (4 * (e & 7));
-  *reinterpret_cast<uint4 *>(v_codes + row * (D / 2) + j * (kGroup / 2)) = make_uint4(w[0], w[1], w[2], w[3]);
-  v_scales[row * groups + j] = s;
+  for (int e = 0; e < 8; ++e) w |= static_cast<uint32_t>(int4_code(x[e], s) + 8) << (4 * e);
+  *reinterpret_cast<uint32_t *>(v_codes + row * (D / 2) + j * (kGroup / 2) + 4 * part) = w;
+  if (part == 0) v_scales[row * groups + j] = s;
 }
 
 // Window copy with dtype change (fp32 <-> bf16, nearest even).
@@ -264,18 +254,31 @@ int pack_typed(const T *k, const T *v, const kvq_cache &c, cudaStream_t s) {
   int launches = 0;
   if (d.cut > 0) {
     if (d.D == 128) {
-      pack_k128_kernel<T><<<static_cast<unsigned>(units * d.Gk), 256, 0, s>>>(
-          k, d.N, d.cut, d.Gk, c.k_codes, c.k_scales);
+      for (long u0 = 0; u0 < units; u0 += 65535) {  // grid.y holds at most 65,535 units
+        const unsigned nu = static_cast<unsigned>(std::min<long>(65535, units - u0));
+        pack_k128_kernel<T><<<dim3(d.Gk, nu), 256, 0, s>>>(k, d.N, d.cut, d.Gk, u0, c.k_codes,
+                                                           c.k_scales);
+        ++launches;
+      }
     } else {
       const long ktasks = units * d.Gk * (d.D / 2);
       pack_k_kernel<T><<<static_cast<unsigned>((ktasks + 255) / 256), 256, 0, s>>>(
           k, ktasks, d.N, d.D, d.cut, d.Gk, c.k_codes, c.k_scales);
+      ++launches;
     }
-    const long rows = units * d.cut;
-    const long vtasks = rows * (d.D / kGroup);
-    pack_v_kernel<T><<<static_cast<unsigned>((vtasks + 255) / 256), 256, 0, s>>>(
-        v, rows, d.N, d.D, d.cut, c.v_codes, c.v_scales);
-    launches += 2;
+    // V: per launch at most 65,535 units (grid.y) and 2^24 tokens of each,
+    // so the thread index of a unit's slice fits 32 bits
+    constexpr int kSlice = 1 << 24;
+    for (long u0 = 0; u0 < units; u0 += 65535) {
+      const unsigned nu = static_cast<unsigned>(std::min<long>(65535, units - u0));
+      for (int t0 = 0; t0 < d.cut; t0 += kSlice) {
+        const int nt = std::min(kSlice, d.cut - t0);
+        const long vthreads = 4L * nt * (d.D / kGroup);
+        pack_v_kernel<T><<<dim3(static_cast<unsigned>((vthreads + 255) / 256), nu), 256, 0, s>>>(
+            v, u0, t0, nt, d.N, d.D, d.cut, c.v_codes, c.v_scales);
+        ++launches;
+      }
+    }
   }
   if (d.R > 0) {
     const long rows = units * d.R;
