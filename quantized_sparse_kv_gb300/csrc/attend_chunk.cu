@@ -743,14 +743,48 @@ __global__ void mxfp8_to_bf16_kernel(const uint8_t *__restrict__ codes,
   }
 }
 
-// Q: bf16 -> MXFP8 rounding -> bf16, one warp per 32-feature block.
+// Q: bf16 -> MXFP8 rounding -> bf16. Four lanes per 32-feature block, 8
+// values each (16-byte loads and stores); the block maximum takes two
+// shuffles, after which every value follows the rule kv_pack applies to an
+// MXFP8 K window (mxfp8_round_warp gives the same values with a lane each).
 __global__ void __launch_bounds__(256) q_mxfp8_round_kernel(const __nv_bfloat16 *__restrict__ q,
                                                             long blocks,
                                                             __nv_bfloat16 *__restrict__ out) {
-  const long task = static_cast<long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
-  if (task >= blocks) return;
-  const long i = task * 32 + (threadIdx.x & 31);
-  out[i] = __float2bfloat16_rn(mxfp8_round_warp(__bfloat162float(q[i])));
+  const long tid = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const bool live = (tid >> 2) < blocks;
+  const uint4 u = live ? reinterpret_cast<const uint4 *>(q)[tid] : make_uint4(0, 0, 0, 0);
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+  float x[8];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    x[2 * j] = __uint_as_float(w[j] << 16);
+    x[2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
+  }
+  float amax = 0.0f;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(x[e]));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+  if (!live) return;
+  int ex = -127;
+  if (amax > 0.0f) {
+    int f;
+    frexpf(amax, &f);
+    ex = max(-127, min(127, f - 1 - 8));
+  }
+  uint32_t o[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    float r[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint8_t c = static_cast<uint8_t>(
+          __nv_cvt_float_to_fp8(ldexpf(x[2 * j + h], -ex), __NV_SATFINITE, __NV_E4M3));
+      r[h] = mxfp8_value(c, static_cast<uint8_t>(ex + 127));
+    }
+    o[j] = pack_bf16x2(r[0], r[1]);
+  }
+  reinterpret_cast<uint4 *>(out)[tid] = make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 // ------------------------------------------------------------------ host side
@@ -819,7 +853,7 @@ int launch_attend_chunk(const kvq_cache &c, const void *q, int Hq, int n_q, floa
     mxfp8_to_bf16_kernel<<<static_cast<unsigned>(std::min<long>((kn / 16 + 255) / 256, 1L << 20)),
                            256, 0, s>>>(static_cast<const uint8_t *>(c.k_window), c.k_window_e8m0,
                                         kn / 16, kb);
-    q_mxfp8_round_kernel<<<static_cast<unsigned>((qn / 32 + 7) / 8), 256, 0, s>>>(
+    q_mxfp8_round_kernel<<<static_cast<unsigned>((qn / 8 + 255) / 256), 256, 0, s>>>(
         static_cast<const __nv_bfloat16 *>(q), qn / 32, qb);
     kptr = kb;
     qptr = qb;

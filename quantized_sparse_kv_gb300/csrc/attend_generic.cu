@@ -189,22 +189,22 @@ __global__ void __launch_bounds__(kWarps * 32) generic_attend_kernel(GenericArgs
   }
 }
 
-// Head dim 32, fp32 or bf16 windows, at most 4 regions: one warp per query row,
-// lane j takes key t0 + j of each 32-key chunk, dequantizes it in registers
-// and scores it against the whole q row; the chunk's max and the running
-// softmax state are shared across the warp, each lane keeps partial sums of
-// O and of the region masses, and O is reduced across lanes once at the end
-// through shared memory. Every query row is independent, so the grid has one
-// warp per row instead of one CTA per head.
-constexpr int kSmallWarps = 4;
+// Head dim 32, fp32 or bf16 windows, at most 4 regions: one CTA of 8 warps
+// per query row; warp w takes the 32-key chunks w, w + 8, ..., lane j key
+// t0 + j of a chunk, which it dequantizes on use and scores against the
+// whole q row; a chunk's max and the running softmax state are shared across
+// the warp, each lane keeps partial sums of O and of the region masses. At
+// the end O is reduced across lanes through shared memory and the 8 warps'
+// states are merged with the log-sum-exp rule.
+constexpr int kSmallWarps = 8;  // warps per query row: each takes every 8th block of 32 keys
 constexpr int kSmallRegions = 4;
 
 template <int D>
 __global__ void __launch_bounds__(kSmallWarps * 32) small_attend_kernel(GenericArgs a, long rows) {
   __shared__ float red[kSmallWarps][32][D + 1];
+  __shared__ float wm[kSmallWarps], wl[kSmallWarps], wr[kSmallWarps][kSmallRegions];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long row = static_cast<long>(blockIdx.x) * kSmallWarps + warp;  // over (b, h, i)
-  if (row >= rows) return;                                               // warp-uniform
+  const long row = blockIdx.x;  // over (b, h, i)
   const long bh = row / a.n_q;
   const int h = static_cast<int>(bh % a.Hq);
   const long b = bh / a.Hq;
@@ -229,41 +229,44 @@ __global__ void __launch_bounds__(kSmallWarps * 32) small_attend_kernel(GenericA
 #pragma unroll
   for (int k = 0; k < kSmallRegions; ++k) rm[k] = 0.0f;
 
-  for (int t0 = 0; t0 < a.N; t0 += 32) {
+  for (int t0 = 32 * warp; t0 < a.N; t0 += 32 * kSmallWarps) {
     const int t = t0 + lane;
-    float kv[D], vv[D];
-    if (t < a.cut) {
+    const bool in_codes = t < a.cut, in_win = !in_codes && t < a.N;
+    // the key's K and V nibbles stay packed until used (8 registers, not 2D)
+    uint32_t kw[D / 8], vw[D / 8];
+    const float *ks = a.k_scales;
+    float vs[D / 32];
+    long wi = 0;
+    if (in_codes) {
       const int g = t / kGroup, r = t % kGroup;
-      const uint32_t *kc = reinterpret_cast<const uint32_t *>(a.k_codes + ((u * a.Gk + g) * kGroup + r) * (D / 2));
-      const float *ks = a.k_scales + (u * a.Gk + g) * D;
-      const uint32_t *vc = reinterpret_cast<const uint32_t *>(a.v_codes + (u * a.cut + t) * (D / 2));
-      const float *vs = a.v_scales + (u * a.cut + t) * (D / 32);
+      const uint4 *kc = reinterpret_cast<const uint4 *>(a.k_codes + ((u * a.Gk + g) * kGroup + r) * (D / 2));
+      const uint4 *vc = reinterpret_cast<const uint4 *>(a.v_codes + (u * a.cut + t) * (D / 2));
 #pragma unroll
-      for (int w = 0; w < D / 8; ++w) {
-        const uint32_t kw = kc[w], vw = vc[w];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int d = 8 * w + e;
-          kv[d] = static_cast<float>(static_cast<int>((kw >> (4 * e)) & 15u) - 8) * ks[d];
-          vv[d] = static_cast<float>(static_cast<int>((vw >> (4 * e)) & 15u) - 8) * vs[d / 32];
-        }
+      for (int w = 0; w < D / 32; ++w) {
+        const uint4 x = kc[w], y = vc[w];
+        kw[4 * w] = x.x; kw[4 * w + 1] = x.y; kw[4 * w + 2] = x.z; kw[4 * w + 3] = x.w;
+        vw[4 * w] = y.x; vw[4 * w + 1] = y.y; vw[4 * w + 2] = y.z; vw[4 * w + 3] = y.w;
+        vs[w] = a.v_scales[(u * a.cut + t) * (D / 32) + w];
       }
-    } else if (t < a.N) {
-      const long wi = (u * a.R + (t - a.cut)) * D;
-#pragma unroll
-      for (int d = 0; d < D; ++d) {
-        kv[d] = window_value(a.k_window, a.kwin, wi + d);
-        vv[d] = window_value(a.v_window, a.vwin, wi + d);
-      }
+      ks = a.k_scales + (u * a.Gk + g) * D;  // the same group for the whole warp: broadcast loads
     } else {
-#pragma unroll
-      for (int d = 0; d < D; ++d) kv[d] = vv[d] = 0.0f;
+      wi = (u * a.R + (t - a.cut)) * D;
     }
     float s0 = 0.0f, s1 = 0.0f;
+    if (in_codes) {
 #pragma unroll
-    for (int d = 0; d < D; d += 2) {
-      s0 = fmaf(q[d], kv[d], s0);
-      s1 = fmaf(q[d + 1], kv[d + 1], s1);
+      for (int d = 0; d < D; d += 2) {
+        const uint32_t w = kw[d >> 3];
+        s0 = fmaf(q[d], static_cast<float>(static_cast<int>((w >> (4 * (d & 7))) & 15u) - 8) * ks[d], s0);
+        s1 = fmaf(q[d + 1],
+                  static_cast<float>(static_cast<int>((w >> (4 * ((d + 1) & 7))) & 15u) - 8) * ks[d + 1], s1);
+      }
+    } else if (in_win) {
+#pragma unroll
+      for (int d = 0; d < D; d += 2) {
+        s0 = fmaf(q[d], window_value(a.k_window, a.kwin, wi + d), s0);
+        s1 = fmaf(q[d + 1], window_value(a.k_window, a.kwin, wi + d + 1), s1);
+      }
     }
     const bool valid = t < a.N;
     const float sc = valid ? (s0 + s1) * a.sm_scale : -CUDART_INF_F;
@@ -279,33 +282,67 @@ __global__ void __launch_bounds__(kSmallWarps * 32) small_attend_kernel(GenericA
       m = m_new;
     }
     l += p;
+    if (in_codes) {
 #pragma unroll
-    for (int d = 0; d < D; ++d) o[d] = fmaf(p, vv[d], o[d]);
+      for (int d = 0; d < D; ++d) {
+        const float v = static_cast<float>(static_cast<int>((vw[d >> 3] >> (4 * (d & 7))) & 15u) - 8) * vs[d / 32];
+        o[d] = fmaf(p, v, o[d]);
+      }
+    } else if (in_win) {
+#pragma unroll
+      for (int d = 0; d < D; ++d) o[d] = fmaf(p, window_value(a.v_window, a.vwin, wi + d), o[d]);
+    }
 #pragma unroll
     for (int k = 0; k < kSmallRegions; ++k)
       if (k < a.reg.n) rm[k] += (t >= a.reg.b[k] && t < a.reg.b[k + 1]) ? p : 0.0f;
   }
 
-  // reduce the lanes' partial O through shared memory: lane d sums feature d
+  // each warp's state: O through shared memory (lane d later sums feature
+  // d), l and the region sums over the lanes
 #pragma unroll
   for (int d = 0; d < D; ++d) red[warp][lane][d] = o[d];
-  __syncwarp();
-  const float inv = 1.0f / warp_sum(l);
-  for (int d = lane; d < D; d += 32) {
+  const float lw = warp_sum(l);
+  float rw[kSmallRegions];
+#pragma unroll
+  for (int k = 0; k < kSmallRegions; ++k) rw[k] = warp_sum(rm[k]);
+  if (lane == 0) {
+    wm[warp] = m;
+    wl[warp] = lw;
+#pragma unroll
+    for (int k = 0; k < kSmallRegions; ++k) wr[warp][k] = rw[k];
+  }
+  __syncthreads();
+  // merge the warps (log-sum-exp); a warp that met no key has m = -inf
+  float mx = -CUDART_INF_F;
+#pragma unroll
+  for (int w = 0; w < kSmallWarps; ++w) mx = fmaxf(mx, wm[w]);
+  float cw[kSmallWarps], den = 0.0f;
+#pragma unroll
+  for (int w = 0; w < kSmallWarps; ++w) {
+    cw[w] = wm[w] == -CUDART_INF_F ? 0.0f : expf(wm[w] - mx);
+    den += cw[w] * wl[w];
+  }
+  const float inv = 1.0f / den;
+  for (int d = threadIdx.x; d < D; d += kSmallWarps * 32) {
     float acc = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kSmallWarps; ++w) {
+      float sw = 0.0f;
 #pragma unroll 8
-    for (int j = 0; j < 32; ++j) acc += red[warp][j][d];
+      for (int j = 0; j < 32; ++j) sw += red[w][j][d];
+      acc += cw[w] * sw;
+    }
     const float x = acc * inv;
     if (a.out_dtype == KVQ_F32)
       static_cast<float *>(a.out)[row * D + d] = x;
     else
       static_cast<__nv_bfloat16 *>(a.out)[row * D + d] = __float2bfloat16_rn(x);
   }
+  if (a.mass && threadIdx.x < a.reg.n && threadIdx.x < kSmallRegions) {
+    float acc = 0.0f;
 #pragma unroll
-  for (int k = 0; k < kSmallRegions; ++k) {
-    if (k >= a.reg.n) break;
-    const float mk = warp_sum(rm[k]);
-    if (a.mass && lane == 0) a.mass[row * a.reg.n + k] = mk * inv;
+    for (int w = 0; w < kSmallWarps; ++w) acc += cw[w] * wr[w][threadIdx.x];
+    a.mass[row * a.reg.n + threadIdx.x] = acc * inv;
   }
 }
 
@@ -353,9 +390,8 @@ int launch_attend_generic(const kvq_cache &c, const void *q, int q_dtype, int Hq
   a.sm_scale = sm_scale;
   a.reg = make_regions(bounds, n_regions);
   if (d.D == 32 && c.kwin_dtype != KVQ_MXFP8 && a.reg.n <= kSmallRegions) {
-    const long rows = static_cast<long>(d.B) * Hq * n_q;
-    const unsigned blocks = static_cast<unsigned>((rows + kSmallWarps - 1) / kSmallWarps);
-    small_attend_kernel<32><<<blocks, kSmallWarps * 32, 0, s>>>(a, rows);
+    const long rows = static_cast<long>(d.B) * Hq * n_q;  // one CTA per query row
+    small_attend_kernel<32><<<static_cast<unsigned>(rows), kSmallWarps * 32, 0, s>>>(a, rows);
     return 1;
   }
   switch (d.D / 32) {
