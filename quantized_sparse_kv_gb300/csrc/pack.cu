@@ -160,49 +160,42 @@ __global__ void __launch_bounds__(256) pack_k_kernel(const T *__restrict__ k, lo
         static_cast<uint8_t>((int4_code(x[t].lo(), s0) + 8) | ((int4_code(x[t].hi(), s1) + 8) << 4));
 }
 
-// V: four lanes per (token, 32-feature group) of the quantized part, each
-// with 8 consecutive values, so a warp's loads cover 8 whole groups
-// contiguously; the group maximum takes two shuffles, and each lane writes
-// its 4 code bytes (the leader also the scale).
+// V: one thread per (token, 32-feature group) of the quantized part; 32 values
+// in (16-byte loads), 16 code bytes and one scale out. The grid is (position
+// within a slice of the unit's tokens, unit), so indices stay 32-bit.
 template <typename T>
 __global__ void __launch_bounds__(256) pack_v_kernel(const T *__restrict__ v, long u0, int t0,
                                                      int nt, int N, int D, int cut,
                                                      uint8_t *__restrict__ v_codes,
                                                      float *__restrict__ v_scales) {
   const int groups = D / kGroup;
-  const unsigned tid = blockIdx.x * blockDim.x + threadIdx.x;  // within the slice
-  const unsigned task = tid >> 2;                               // (token, group)
-  const int part = static_cast<int>(tid & 3);
-  const bool live = task < static_cast<unsigned>(nt) * groups;
-  const unsigned tk = live ? task : 0u;
-  const int t = t0 + static_cast<int>(tk / groups);  // token < cut
-  const int j = static_cast<int>(tk % groups);
+  const unsigned task = blockIdx.x * blockDim.x + threadIdx.x;  // (token, group) in the slice
+  if (task >= static_cast<unsigned>(nt) * groups) return;
+  const int t = t0 + static_cast<int>(task / groups);  // token < cut
+  const int j = static_cast<int>(task % groups);
   const long u = u0 + blockIdx.y;
   const long row = u * cut + t;  // over (unit, token < cut)
-  const T *src = v + (u * N + t) * D + j * kGroup + 8 * part;
-  float x[8];
-  {
-    float a4[4], b4[4];
-    load4(src, a4);
-    load4(src + 4, b4);
+  const T *src = v + (u * N + t) * D + j * kGroup;
+  float x[kGroup];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      x[e] = a4[e];
-      x[4 + e] = b4[e];
-    }
+  for (int i = 0; i < kGroup / 4; ++i) {
+    float f[4];
+    load4(src + 4 * i, f);
+    x[4 * i] = f[0];
+    x[4 * i + 1] = f[1];
+    x[4 * i + 2] = f[2];
+    x[4 * i + 3] = f[3];
   }
   float amax = 0.0f;
 #pragma unroll
-  for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(x[e]));
-  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-  if (!live) return;
+  for (int e = 0; e < kGroup; ++e) amax = fmaxf(amax, fabsf(x[e]));
   const float s = int4_scale(amax);
-  uint32_t w = 0u;
+  uint32_t w[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-  for (int e = 0; e < 8; ++e) w |= static_cast<uint32_t>(int4_code(x[e], s) + 8) << (4 * e);
-  *reinterpret_cast<uint32_t *>(v_codes + row * (D / 2) + j * (kGroup / 2) + 4 * part) = w;
-  if (part == 0) v_scales[row * groups + j] = s;
+  for (int e = 0; e < kGroup; ++e)
+    w[e >> 3] |= static_cast<uint32_t>(int4_code(x[e], s) + 8) << (4 * (e & 7));
+  *reinterpret_cast<uint4 *>(v_codes + row * (D / 2) + j * (kGroup / 2)) = make_uint4(w[0], w[1], w[2], w[3]);
+  v_scales[row * groups + j] = s;
 }
 
 // Window copy with dtype change (fp32 <-> bf16, nearest even).
@@ -267,13 +260,13 @@ int pack_typed(const T *k, const T *v, const kvq_cache &c, cudaStream_t s) {
       ++launches;
     }
     // V: per launch at most 65,535 units (grid.y) and 2^24 tokens of each,
-    // so the thread index of a unit's slice fits 32 bits
+    // so the thread index within a unit's slice fits 32 bits
     constexpr int kSlice = 1 << 24;
     for (long u0 = 0; u0 < units; u0 += 65535) {
       const unsigned nu = static_cast<unsigned>(std::min<long>(65535, units - u0));
       for (int t0 = 0; t0 < d.cut; t0 += kSlice) {
         const int nt = std::min(kSlice, d.cut - t0);
-        const long vthreads = 4L * nt * (d.D / kGroup);
+        const long vthreads = static_cast<long>(nt) * (d.D / kGroup);
         pack_v_kernel<T><<<dim3(static_cast<unsigned>((vthreads + 255) / 256), nu), 256, 0, s>>>(
             v, u0, t0, nt, d.N, d.D, d.cut, c.v_codes, c.v_scales);
         ++launches;
