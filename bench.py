@@ -280,6 +280,28 @@ def row_candidates(kvq, synth, torch, steps, warmup, pk, context, c):
             "launches": a.launches()}
 
 
+def row_decode(kvq, synth, torch, steps, warmup, pk, batch, context):
+    """The decode step at another (batch, context) of the decode workload."""
+    d = dict(DECODE, batch=batch, context=context)
+    q, k, v = synth.decode_inputs_torch(1, batch, context, "cuda")
+    cache = kvq.pack(k, v, d["recent"], "bf16")
+    del k, v
+    a = kvq.Attend(cache, q, out_dtype="bf16")
+    a.run()
+    ms = time_steps(a.run, steps, warmup, flush=make_flush())
+    nbytes = decode_bytes(batch, d["kv_heads"], context, d["recent"])
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    keys = batch * d["q_heads"] * context
+    return {"workload": f"decode: B={batch}, 16 query heads over 2 KV heads, D=128, L={context}, "
+                        "R=128 bf16, int4 groups of 32",
+            "ms": ms, "keys_per_s": keys / (ms * 1e-3), "path": a.path,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / pk["hbm_gbs"], "traffic": None,
+                         "algorithmic_bytes": nbytes,
+                         "kernel": "decode_kernel + combine_kernel (one kv_attend call)"},
+            "launches": a.launches()}
+
+
 # ---------------------------------------------------------------- oracle (CPU) arm
 
 def _oracle_unit_worker(args):
@@ -470,9 +492,9 @@ def run_kvq(args):
 
     rows = {}
     if rank == 0 and not args.no_rows:
-        rsteps = max(3, min(args.steps, 10))
+        rsteps = max(3, min(args.steps, 20))
         for name, fn in ROWS.items():
-            rows[name] = fn(kvq, synth, torch, rsteps, 2, pk)
+            rows[name] = fn(kvq, synth, torch, rsteps, 3, pk)
 
     if rank != 0:
         return
@@ -502,6 +524,12 @@ def run_kvq(args):
 
 
 ROWS = {
+    "decode_B16_L32768": lambda kvq, synth, torch, st, w, pk:
+        row_decode(kvq, synth, torch, st, w, pk, 16, 32768),
+    "decode_B64_L8192": lambda kvq, synth, torch, st, w, pk:
+        row_decode(kvq, synth, torch, st, w, pk, 64, 8192),
+    "decode_B64_L1024": lambda kvq, synth, torch, st, w, pk:
+        row_decode(kvq, synth, torch, st, w, pk, 64, 1024),
     "pack": lambda kvq, synth, torch, st, w, pk: row_pack(kvq, synth, torch, st, w, pk),
     "small_d_fp32": lambda kvq, synth, torch, st, w, pk: row_small(kvq, synth, torch, st, w, pk),
     "candidates_L131072_C256": lambda kvq, synth, torch, st, w, pk:
