@@ -42,8 +42,8 @@ constexpr int kVStages = 2;
 constexpr int kMaxRegions = 4;
 constexpr uint32_t kTileBytes = kBN * kDim * 2;  // 32 KB, one K or V tile (bf16)
 constexpr uint32_t kHalfBytes = kTileBytes / 2;  // 16 KB: 128 rows x 64 features
-constexpr float kRescaleThreshold = 8.0f;         // log2 units
 constexpr float kRedoThreshold = 64.0f;           // log2 units: P stays below 2^64
+constexpr float kRedoBound = 18446744073709551616.0f;  // 2^64
 
 struct __align__(1024) ChunkSmem {
   uint8_t q[kTileBytes];                    // 2 x [128 rows][128 B], swizzled
@@ -60,7 +60,7 @@ struct __align__(1024) ChunkSmem {
 // Group B's row state for the final merge, laid over K stage 0, which no copy
 // or MMA touches any more once group B has seen its last PV complete.
 struct MergeState {
-  float m[kBM], l[kBM], p[kBM];
+  float m[kBM], l[kBM];
   float r[kMaxRegions][kBM];
 };
 static_assert(sizeof(MergeState) <= kTileBytes, "merge state fits a K stage");
@@ -321,9 +321,9 @@ __device__ __forceinline__ void softmax_chunk(float (&v)[32], int c, int valid, 
 
 // The pass over the 128 score columns of this thread's row, up to the last
 // chunk: chunks 0-2 are exponentiated and stored while the TMEM load of the
-// next is in flight; chunk 3 is left raw in v3 and only folded into the
-// maximum, so that the caller can release S before finishing it.
-// cs[c]: sum of chunk c; part: region sums (kSplit only).
+// next is in flight; chunk 3 is left raw in v3, and mx is its raw maximum, so
+// that the caller can release S before finishing it. cs[c]: sum of chunk c;
+// part: region sums (kSplit only).
 template <bool kSplit>
 __device__ __forceinline__ void softmax_pass_head(uint32_t taddr, int valid, int t0, float scale,
                                                   float neg_m, const Regions &reg, uint8_t *p,
@@ -338,15 +338,15 @@ __device__ __forceinline__ void softmax_pass_head(uint32_t taddr, int valid, int
   tmem_wait_ld();
   reg_fence(va);
   tmem_ld32(taddr + 32u, v3);
-  softmax_chunk<kSplit>(va, 0, valid, t0, scale, neg_m, reg, p, row, cs[0], part, mx0, mx1);
+  softmax_chunk<kSplit, false>(va, 0, valid, t0, scale, neg_m, reg, p, row, cs[0], part, mx0, mx1);
   tmem_wait_ld();
   reg_fence(v3);
   tmem_ld32(taddr + 64u, va);
-  softmax_chunk<kSplit>(v3, 1, valid, t0, scale, neg_m, reg, p, row, cs[1], part, mx0, mx1);
+  softmax_chunk<kSplit, false>(v3, 1, valid, t0, scale, neg_m, reg, p, row, cs[1], part, mx0, mx1);
   tmem_wait_ld();
   reg_fence(va);
   tmem_ld32(taddr + 96u, v3);
-  softmax_chunk<kSplit>(va, 2, valid, t0, scale, neg_m, reg, p, row, cs[2], part, mx0, mx1);
+  softmax_chunk<kSplit, false>(va, 2, valid, t0, scale, neg_m, reg, p, row, cs[2], part, mx0, mx1);
   tmem_wait_ld();
   reg_fence(v3);
   if (valid == kBN) {
@@ -514,11 +514,12 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t s_row = t_s(g) + lane_off, o_row = t_o(g) + lane_off;
     const int my_tiles = (nt - g + 1) >> 1;  // tiles g, g+2, ...
-    // Row state: P of a tile is taken against the reference m_used fixed when
-    // the tile starts; a tile whose maximum passes m_used + kRescaleThreshold
-    // raises the reference for the following tiles (l and the region sums are
-    // rescaled at once, O_g once its pending MMA is done: `pend`).
-    float m_used = -CUDART_INF_F, l = 0.0f, pend = 1.0f;
+    // Row state: P is taken against a reference m_used, set from the row's
+    // maximum over its first tile and kept while P stays below
+    // 2^kRedoThreshold (bf16 P and the fp32 sums have the range for it, so no
+    // running maximum is kept); a tile that would pass that bound raises the
+    // reference to its maximum and is redone.
+    float m_used = -CUDART_INF_F, l = 0.0f;
     float rsum[kMaxRegions] = {0.0f, 0.0f, 0.0f, 0.0f};
     bool ok = true;
     for (int i = 0; i < my_tiles; ++i) {
@@ -532,16 +533,9 @@ __global__ void __launch_bounds__(384, 1)
       const int t0 = j * kBN;
       // O_g += P V of the previous tile must be done before P_g is rewritten
       // or O_g is rescaled
-      if (i >= 1) {
-        if (!wait_or_abort(sm, smem_u32(&sm.o_done[g]), (i - 1) & 1, a.ctl)) {
-          ok = false;
-          break;
-        }
-        if (__any_sync(0xffffffffu, pend != 1.0f)) {
-          tc_fence_after();
-          scale_tmem_row(o_row, pend);
-        }
-        pend = 1.0f;
+      if (i >= 1 && !wait_or_abort(sm, smem_u32(&sm.o_done[g]), (i - 1) & 1, a.ctl)) {
+        ok = false;
+        break;
       }
       if (i == 0) m_used = row_max(s_row, valid) * a.scale_log2;  // scale > 0 keeps the order
       // regions: chunk c of the tile lies in region kc[c], unless the tile
@@ -559,7 +553,7 @@ __global__ void __launch_bounds__(384, 1)
           split |= start < end && end > a.reg.b[kc[c] + 1];
         }
       }
-      // one pass: P = 2^(s * scale - m_used) -> shared memory, sums, raw max
+      // one pass: P = 2^(s * scale - m_used) -> shared memory, sums
       float cs[4], part[kMaxRegions], v3[32], mx, dummy0 = 0.0f, dummy1 = 0.0f;
       if (split)
         softmax_pass_head<true>(s_row, valid, t0, a.scale_log2, -m_used, a.reg, sm.p[g], row, cs,
@@ -567,12 +561,14 @@ __global__ void __launch_bounds__(384, 1)
       else
         softmax_pass_head<false>(s_row, valid, t0, a.scale_log2, -m_used, a.reg, sm.p[g], row, cs,
                                  part, v3, mx);
-      const float mt = mx * a.scale_log2;  // scaled tile maximum
-      if (__any_sync(0xffffffffu, mt > m_used + kRedoThreshold)) {
+      // A chunk sum bounds each of its P values: chunks 0-2 are checked by
+      // their sums, chunk 3 by its raw maximum.
+      const float big = fmaxf(fmaxf(cs[0], cs[1]), cs[2]);
+      if (__any_sync(0xffffffffu, !(big <= kRedoBound) || mx * a.scale_log2 > m_used + kRedoThreshold)) {
         // far above the reference for some row (P could overflow): the warp
         // takes the tile maxima now and redoes the tile from its scores, still
         // in TMEM (TMEM access is warp-wide); O_g is idle, its last MMA is done
-        const float m_new = fmaxf(m_used, mt);
+        const float m_new = fmaxf(m_used, row_max(s_row, valid) * a.scale_log2);
         const float f = fast_exp2(m_used - m_new);
         m_used = m_new;
         l *= f;
@@ -618,13 +614,6 @@ __global__ void __launch_bounds__(384, 1)
             for (int k = 0; k < kMaxRegions; ++k) rsum[k] += (kc[c] == k) ? cs[c] : 0.0f;
         }
       }
-      if (mt > m_used + kRescaleThreshold) {
-        pend = fast_exp2(m_used - mt);
-        m_used = mt;
-        l *= pend;
-#pragma unroll
-        for (int k = 0; k < kMaxRegions; ++k) rsum[k] *= pend;
-      }
     }
     // ---- epilogue: group B hands its row state to group A, A merges and stores
     const bool last_ok =
@@ -636,7 +625,6 @@ __global__ void __launch_bounds__(384, 1)
     if (g == 1 && last_ok) {
       ms.m[row] = m_used;
       ms.l[row] = l;
-      ms.p[row] = pend;
 #pragma unroll
       for (int k = 0; k < kMaxRegions; ++k) ms.r[k][row] = rsum[k];
     }
@@ -654,8 +642,7 @@ __global__ void __launch_bounds__(384, 1)
       const float fb = have_b ? exp2f(mb - mm) : 0.0f;
       const float lt = fa * l + (have_b ? fb * ms.l[row] : 0.0f);
       const float inv = 1.0f / lt;
-      // O_A and O_B still owe their last reference change
-      const float oa = fa * pend, ob = have_b ? fb * ms.p[row] : 0.0f;
+      const float oa = fa, ob = have_b ? fb : 0.0f;
       const int qrow = q0 + row;
       const long obase = (static_cast<long>(hq) * a.n_q + qrow) * kDim;
 #pragma unroll
