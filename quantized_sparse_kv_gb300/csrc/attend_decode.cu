@@ -593,7 +593,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const Deco
 // One warp per (unit, query head): merge the partials of the CTAs whose
 // slices overlap the unit (log-sum-exp), normalise, store. The partials of
 // unit u sit in consecutive slots, one per overlapping CTA; they are read
-// eight at a time with all loads of a batch in flight together.
+// sixteen at a time with all loads of a batch in flight together.
 template <typename OT>
 __global__ void __launch_bounds__(256) combine_kernel(const DecodeArgs a, OT *__restrict__ out) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -603,7 +603,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const DecodeArgs a, OT *__
   const int n = cta_of_item(a, (u + 1) * a.ipu - 1) - cta_of_item(a, u * a.ipu) + 1;
   const float *base = partial_of(a, u, 0) + h * kPartFloats;
   constexpr int kSlot = kHeads * kPartFloats;
-  constexpr int kBatch = 8;
+  constexpr int kBatch = 16;
   float m = -CUDART_INF_F, l = 0.0f;
   float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
   for (int c0 = 0; c0 < n; c0 += kBatch) {
