@@ -260,13 +260,16 @@ def row_small(kvq, synth, torch, steps, warmup, pk):
 
 
 def row_chunk(kvq, synth, torch, steps, warmup, pk, kwin):
+    """kwin "bf16" / "mxfp8": every key in the window; "int4": the sink and
+    recent regions (3,900 tokens) as int4 groups, the current 2,340 in bf16."""
     c = CHUNK
+    recent = c["n_kv"] if kwin != "int4" else c["n_kv"] - c["bounds"][2]
     touched = 2 * c["heads"] * c["head_dim"] * (2 * c["n_q"] + 2 * c["n_kv"])
     n = rotation(touched)
     attends = []
     for i in range(n):
         q, k, v = synth.chunk_inputs_torch(21 + 5 * i, "cuda")
-        cache = kvq.pack(k, v, c["n_kv"], kwin, "bf16")
+        cache = kvq.pack(k, v, recent, "bf16" if kwin == "int4" else kwin, "bf16")
         del k, v
         attends.append(kvq.Attend(cache, q, out_dtype="bf16", region_bounds=c["bounds"]))
     a = attends[0]
@@ -276,15 +279,20 @@ def row_chunk(kvq, synth, torch, steps, warmup, pk, kwin):
     # the MXFP8 path expands Q/K exactly to bf16 and runs the bf16 tensor pipe
     peak = pk["bf16_tflops"]
     keys = c["heads"] * c["n_q"] * c["n_kv"]
-    return {"workload": f"chunk attention {kwin} Q/K, 32 heads, 2340 queries over 6240 keys "
+    what = {"bf16": "bf16 Q/K", "mxfp8": "mxfp8 Q/K",
+            "int4": "bf16 Q, int4 K/V for sink+recent (3900 tokens) and bf16 current window"}[kwin]
+    return {"workload": f"chunk attention {what}, 32 heads, 2340 queries over 6240 keys "
                         "[sink 1560 | recent 2340 | current 2340], D=128, region mass",
             "ms": ms, "keys_per_s": keys / (ms * 1e-3), "path": a.path, "l2": l2_note(n, touched),
             "roofline": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s",
                          "frac": tf / peak,
                          "traffic": (profile_traffic("chunk_bf16_kernel_H32_Q2340_K6240.md")
                                      if kwin == "bf16" else None),
-                         "peak_note": "bf16 measured" if kwin != "mxfp8"
-                         else "bf16 measured: MXFP8 Q/K expanded exactly to bf16, bf16 MMA"},
+                         "peak_note": {"bf16": "bf16 measured",
+                                       "mxfp8": "bf16 measured: MXFP8 Q/K expanded exactly to "
+                                                "bf16, bf16 MMA",
+                                       "int4": "bf16 measured: int4 history expanded to bf16 "
+                                               "(one pass, inside the timed call), bf16 MMA"}[kwin]},
             "launches": a.launches()}
 
 
@@ -577,6 +585,8 @@ ROWS = {
     "chunk_bf16": lambda kvq, synth, torch, st, w, pk: row_chunk(kvq, synth, torch, st, w, pk, "bf16"),
     "chunk_mxfp8": lambda kvq, synth, torch, st, w, pk:
         row_chunk(kvq, synth, torch, st, w, pk, "mxfp8"),
+    "chunk_int4_history": lambda kvq, synth, torch, st, w, pk:
+        row_chunk(kvq, synth, torch, st, w, pk, "int4"),
 }
 
 

@@ -774,6 +774,62 @@ __global__ void __launch_bounds__(256) q_mxfp8_round_kernel(const __nv_bfloat16 
   reinterpret_cast<uint4 *>(out)[tid] = make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// ------------------------------------------------------------------ int4 history
+// A cache whose older tokens are grouped int4 (residual-window page, section
+// 固定預算) and whose last R tokens are a bf16 window -- the layout of the
+// Catnip study's cache with the sink and recent regions compressed -- is
+// first expanded to contiguous bf16 K and V rows [unit][N][128] in workspace:
+// x = code * s, exact in fp32, rounded once to bf16 (the precision the tensor
+// cores take anyway). The chunk kernel then reads one key range.
+struct HistArgs {
+  const uint8_t *k_codes;   // [unit][Gk][32][64]
+  const float *k_scales;    // [unit][Gk][128]
+  const uint8_t *v_codes;   // [unit][cut][64]
+  const float *v_scales;    // [unit][cut][4]
+  const uint16_t *k_window, *v_window;  // [unit][R][128] bf16
+  uint16_t *k_out, *v_out;  // [unit][N][128] bf16
+  int N, R, cut, Gk;
+};
+
+__device__ __forceinline__ float nib(uint32_t w, int e) {
+  return static_cast<float>(static_cast<int>((w >> (4 * e)) & 0xFu) - 8);
+}
+
+// One thread per (token, 8 features) of unit blockIdx.y: 16-byte stores.
+__global__ void __launch_bounds__(256) history_to_bf16_kernel(const HistArgs a) {
+  const int i = blockIdx.x * 256 + threadIdx.x;
+  if (i >= a.N * 16) return;
+  const long u = blockIdx.y;
+  const int t = i >> 4, q = i & 15;  // token, feature slice 8q..8q+7
+  uint4 ko, vo;
+  if (t < a.cut) {
+    const long grp = u * a.Gk + (t >> 5);
+    // byte j of the slice holds features 8q + 2j (low nibble) and 8q + 2j + 1
+    const uint32_t kc =
+        *reinterpret_cast<const uint32_t *>(a.k_codes + (grp * 32 + (t & 31)) * 64 + 4 * q);
+    const float4 s0 = *reinterpret_cast<const float4 *>(a.k_scales + grp * 128 + 8 * q);
+    const float4 s1 = *reinterpret_cast<const float4 *>(a.k_scales + grp * 128 + 8 * q + 4);
+    ko = make_uint4(pack_bf16x2(nib(kc, 0) * s0.x, nib(kc, 1) * s0.y),
+                    pack_bf16x2(nib(kc, 2) * s0.z, nib(kc, 3) * s0.w),
+                    pack_bf16x2(nib(kc, 4) * s1.x, nib(kc, 5) * s1.y),
+                    pack_bf16x2(nib(kc, 6) * s1.z, nib(kc, 7) * s1.w));
+    const long row = u * a.cut + t;
+    const uint32_t vc = *reinterpret_cast<const uint32_t *>(a.v_codes + row * 64 + 4 * q);
+    const float vs = a.v_scales[row * 4 + (q >> 2)];
+    vo = make_uint4(pack_bf16x2(nib(vc, 0) * vs, nib(vc, 1) * vs),
+                    pack_bf16x2(nib(vc, 2) * vs, nib(vc, 3) * vs),
+                    pack_bf16x2(nib(vc, 4) * vs, nib(vc, 5) * vs),
+                    pack_bf16x2(nib(vc, 6) * vs, nib(vc, 7) * vs));
+  } else {
+    const long w = (u * a.R + (t - a.cut)) * 128 + 8 * q;
+    ko = *reinterpret_cast<const uint4 *>(a.k_window + w);
+    vo = *reinterpret_cast<const uint4 *>(a.v_window + w);
+  }
+  const long o = (u * a.N + t) * 128 + 8 * q;
+  *reinterpret_cast<uint4 *>(a.k_out + o) = ko;
+  *reinterpret_cast<uint4 *>(a.v_out + o) = vo;
+}
+
 // ------------------------------------------------------------------ host side
 using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
@@ -810,14 +866,27 @@ bool make_map(CUtensorMap *m, const void *ptr, int rows, int heads) {
 
 }  // namespace
 
+// All-window caches (bf16 K, or MXFP8 K) and int4-history caches whose window,
+// if any, is bf16.
 bool chunk_supported(const kvq_cache &c, int q_dtype, int Hq, int n_q) {
-  return c.recent == c.n_tokens && c.head_dim == kDim &&
-         (c.kwin_dtype == KVQ_BF16 || c.kwin_dtype == KVQ_MXFP8) && c.vwin_dtype == KVQ_BF16 &&
-         q_dtype == KVQ_BF16 && n_q >= 64 && Hq % c.kv_heads == 0 && encoder() != nullptr;
+  const bool all_window = c.recent == c.n_tokens &&
+                          (c.kwin_dtype == KVQ_BF16 || c.kwin_dtype == KVQ_MXFP8) &&
+                          c.vwin_dtype == KVQ_BF16;
+  const bool history = c.recent < c.n_tokens &&
+                       (c.recent == 0 || (c.kwin_dtype == KVQ_BF16 && c.vwin_dtype == KVQ_BF16));
+  return (all_window || history) && c.head_dim == kDim && q_dtype == KVQ_BF16 && n_q >= 64 &&
+         Hq % c.kv_heads == 0 && encoder() != nullptr;
 }
 
+static bool has_history(const kvq_cache &c) { return c.recent < c.n_tokens; }
+
 // MXFP8: bf16 copies of K and of the MXFP8-rounded Q, each 256-byte aligned.
+// int4 history: bf16 K and V of every token.
 size_t chunk_workspace_bytes(const kvq_cache &c, int Hq, int n_q) {
+  if (has_history(c)) {
+    const size_t kb = static_cast<size_t>(c.batch) * c.kv_heads * c.n_tokens * kDim * 2;
+    return 2 * ((kb + 255) & ~size_t(255));
+  }
   if (c.kwin_dtype != KVQ_MXFP8) return 0;
   const size_t kb = static_cast<size_t>(c.batch) * c.kv_heads * c.n_tokens * kDim * 2;
   const size_t qb = static_cast<size_t>(c.batch) * Hq * n_q * kDim * 2;
@@ -830,8 +899,30 @@ int launch_attend_chunk(const kvq_cache &c, const void *q, int Hq, int n_q, floa
                         void *out, int out_dtype, const int32_t *bounds, int n_regions,
                         float *mass, void *ws, const KernelCtl &ctl, cudaStream_t s) {
   int launches = 1;
-  const void *kptr = c.k_window, *qptr = q;
-  if (c.kwin_dtype == KVQ_MXFP8) {
+  const void *kptr = c.k_window, *vptr = c.v_window, *qptr = q;
+  if (has_history(c)) {
+    const CacheDims d = dims_of(c);
+    const size_t kb = (static_cast<size_t>(d.B) * d.Hkv * d.N * kDim * 2 + 255) & ~size_t(255);
+    HistArgs h;
+    h.k_codes = c.k_codes;
+    h.k_scales = c.k_scales;
+    h.v_codes = c.v_codes;
+    h.v_scales = c.v_scales;
+    h.k_window = static_cast<const uint16_t *>(c.k_window);
+    h.v_window = static_cast<const uint16_t *>(c.v_window);
+    h.k_out = static_cast<uint16_t *>(ws);
+    h.v_out = reinterpret_cast<uint16_t *>(static_cast<uint8_t *>(ws) + kb);
+    h.N = d.N;
+    h.R = d.R;
+    h.cut = d.cut;
+    h.Gk = d.Gk;
+    const dim3 grid(static_cast<unsigned>((d.N * 16 + 255) / 256),
+                    static_cast<unsigned>(d.B * d.Hkv));
+    history_to_bf16_kernel<<<grid, 256, 0, s>>>(h);
+    kptr = h.k_out;
+    vptr = h.v_out;
+    launches += 1;
+  } else if (c.kwin_dtype == KVQ_MXFP8) {
     const long kn = static_cast<long>(c.batch) * c.kv_heads * c.n_tokens * kDim;
     const long qn = static_cast<long>(c.batch) * Hq * n_q * kDim;
     __nv_bfloat16 *kb = static_cast<__nv_bfloat16 *>(ws);
@@ -849,7 +940,7 @@ int launch_attend_chunk(const kvq_cache &c, const void *q, int Hq, int n_q, floa
   CUtensorMap tq, tk, tv;
   if (!make_map(&tq, qptr, n_q, c.batch * Hq) ||
       !make_map(&tk, kptr, c.n_tokens, c.batch * c.kv_heads) ||
-      !make_map(&tv, c.v_window, c.n_tokens, c.batch * c.kv_heads))
+      !make_map(&tv, vptr, c.n_tokens, c.batch * c.kv_heads))
     return -1;
   ChunkArgs a;
   a.n_q = n_q;

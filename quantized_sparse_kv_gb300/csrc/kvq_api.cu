@@ -183,7 +183,9 @@ kvq_status kv_attend(const kvq_cache *cache, const void *q, int32_t q_dtype, int
                                            static_cast<float>(scale * kLog2e), out, out_dtype,
                                            region_bounds, n_regions, region_mass, workspace, ctl, s);
     if (n < 0) return KVQ_ERR_CUDA;
-    return finish(n, cache->kwin_dtype == KVQ_MXFP8 ? "chunk_mxfp8" : "chunk_bf16");
+    return finish(n, cache->recent < cache->n_tokens   ? "chunk_int4"
+                     : cache->kwin_dtype == KVQ_MXFP8 ? "chunk_mxfp8"
+                                                      : "chunk_bf16");
   }
   if (path == DECODE) {
     const int n = kvq::launch_attend_decode(*cache, q, q_dtype,

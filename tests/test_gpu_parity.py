@@ -340,6 +340,68 @@ def test_chunk_bf16_full_size_sampled_heads(kvq):
     np.testing.assert_allclose(to_np(mass).sum(-1), 1.0, atol=1e-4)
 
 
+def history_reference(q, k, v, recent, bounds):
+    """Oracle attention over an int4 history + bf16 window, two ways: with the
+    dequantized history exact (fp64), and with it rounded once to bf16, which is
+    the operand precision the tensor-core path takes."""
+    packed = O.pack(k, v, recent, "bf16")
+    exact, _ = O.attend(q, packed, region_bounds=bounds)
+    bsz, hq, _, _ = q.shape
+    hkv = len(packed[0])
+    cut = k.shape[2] - recent
+    o_bf = np.empty_like(exact)
+    m_bf = None if bounds is None else np.empty(exact.shape[:3] + (len(bounds) - 1,))
+    for b in range(bsz):
+        for h in range(hq):
+            kh, vh = O.dequantize_head(packed[b][h // (hq // hkv)])
+            kh[:cut] = O.round_to_bf16(kh[:cut])
+            vh[:cut] = O.round_to_bf16(vh[:cut])
+            o_bf[b, h], _, mb = O.attention(q[b, h], kh, vh, region_bounds=bounds)
+            if bounds is not None:
+                m_bf[b, h] = mb
+    return exact, o_bf, m_bf
+
+
+@pytest.mark.parametrize("hq,hkv,n_q,n_kv,recent,bounds,conc", [
+    (2, 2, 200, 600, 250, [0, 150, 350, 600], 0.0),
+    (4, 2, 130, 1000, 0, [0, 390, 999, 1000], 0.0),
+    (2, 1, 333, 777, 100, None, 3.0),
+])
+def test_chunk_int4_history_matches_oracle(kvq, hq, hkv, n_q, n_kv, recent, bounds, conc):
+    # int4 groups for the older tokens (a ragged last K group where N - R is
+    # not a multiple of 32), a bf16 window for the last R, tensor-core path
+    q, k, v = chunk_case(70 + n_kv, hq, hkv, n_q, n_kv, conc)
+    cache = kvq.pack(bf16_cuda(k), bf16_cuda(v), recent, "bf16")
+    exact, o_bf, m_bf = history_reference(q, k, v, recent, bounds)
+    for out_dtype in ("f32", "bf16"):
+        out, mass, path = kvq.attend(cache, bf16_cuda(q), out_dtype=out_dtype, region_bounds=bounds)
+        assert path == "chunk_int4"
+        assert O.rel_l2(to_np(out), exact) <= TOL_BF16
+        assert O.rel_l2(to_np(out), o_bf) <= TOL_BF16
+        if bounds is not None:
+            np.testing.assert_allclose(to_np(mass), m_bf, atol=TOL_MASS, rtol=0)
+            np.testing.assert_allclose(to_np(mass).sum(-1), 1.0, atol=1e-4)
+
+
+def test_chunk_int4_history_full_size_sampled_heads(kvq):
+    # the video chunk with its sink and recent regions (3,900 tokens) in int4
+    # and the current 2,340 in the bf16 window
+    bounds = list(synth.CHUNK_REGION_BOUNDS)
+    recent = bounds[-1] - bounds[2]
+    q, k, v = synth.chunk_inputs_torch(9, "cuda")
+    cache = kvq.pack(k, v, recent, "bf16")
+    out, mass, path = kvq.attend(cache, q, out_dtype="f32", region_bounds=bounds)
+    assert path == "chunk_int4"
+    heads = (0, 17, 31)
+    qn = to_np(q)[:, heads]
+    kn, vn = to_np(k)[:, heads], to_np(v)[:, heads]
+    exact, o_bf, m_bf = history_reference(qn, kn, vn, recent, bounds)
+    got, got_mass = to_np(out)[:, heads], to_np(mass)[:, heads]
+    assert O.rel_l2(got, exact) <= TOL_BF16
+    assert O.rel_l2(got, o_bf) <= TOL_BF16
+    np.testing.assert_allclose(got_mass, m_bf, atol=TOL_MASS, rtol=0)
+
+
 @pytest.mark.parametrize("hq,hkv,n_q,n_kv,bounds", [
     (2, 2, 200, 300, [0, 100, 250, 300]),
     (4, 2, 130, 1000, [0, 390, 999, 1000]),
