@@ -97,6 +97,15 @@ typedef struct kvq_cache {
   void *v_window;
   uint8_t *k_window_e8m0;
   uint32_t header[4];
+  /* Room reserved per (sequence, head) for kv_append; 0 and 0 = a tight cache
+   * whose arrays are exactly the sizes above. With cap_groups > 0 the
+   * per-(sequence, head) strides become cap_groups K groups (k_codes,
+   * k_scales), 32 * cap_groups V rows (v_codes, v_scales) and cap_window
+   * window rows (k_window, v_window, k_window_e8m0); rows past Gk, cut and R
+   * are unused. Both are then required, with cap_groups >= Gk and
+   * cap_window >= R. */
+  int32_t cap_groups;
+  int32_t cap_window;
 } kvq_cache;
 
 /* Array sizes of a cache, in bytes (host only, no GPU needed):
@@ -105,6 +114,15 @@ typedef struct kvq_cache {
 KVQ_API kvq_status kvq_cache_sizes(int32_t batch, int32_t kv_heads, int32_t n_tokens,
                                    int32_t head_dim, int32_t recent, int32_t kwin_dtype,
                                    int32_t vwin_dtype, size_t sizes[8]);
+
+/* Array sizes of a cache laid out for kv_append, with cap_groups >= 1 K groups
+ * (and 32 * cap_groups V rows) and cap_window window rows reserved per
+ * (sequence, head); same order as kvq_cache_sizes. KVQ_ERR_ARG for an invalid
+ * shape. */
+KVQ_API kvq_status kvq_cache_sizes_reserved(int32_t batch, int32_t kv_heads, int32_t head_dim,
+                                            int32_t kwin_dtype, int32_t vwin_dtype,
+                                            int32_t cap_groups, int32_t cap_window,
+                                            size_t sizes[8]);
 
 /* Total payload in bytes: the sum of kvq_cache_sizes (header included). */
 KVQ_API size_t kvq_cache_bytes(int32_t batch, int32_t kv_heads, int32_t n_tokens,
@@ -124,6 +142,34 @@ KVQ_API size_t kvq_cache_bytes(int32_t batch, int32_t kv_heads, int32_t n_tokens
  */
 KVQ_API kvq_status kv_pack(const void *k, const void *v, int32_t in_dtype, kvq_cache *cache,
                            int32_t *dev_status, kvq_stream_t stream);
+
+/*
+ * kv_append -- add n_new tokens per (sequence, head) to a cache laid out with
+ * reserved room (cap_groups > 0), as decoding produces them. The pages build
+ * the cache once and leave this online update out ("KV殘差窗口", section
+ * 適用邊界：本輪沒有測在線更新: the oldest window entries are not migrated
+ * into the quantized part token by token); this call is that update, with
+ * the cache layout and quantization rule of kv_pack.
+ * k_new, v_new: [batch][kv_heads][n_new][D] in in_dtype (F32 or BF16), device.
+ * The window grows by n_new; then, while it holds at least `window` + 32
+ * tokens, its oldest 32 become one more int4 K group and 32 more V rows (the
+ * kv_pack rule applied to the window's values, so the result equals kv_pack
+ * of the whole sequence whenever the window type holds the inputs exactly --
+ * BF16 inputs with a BF16 window, or an F32 window). Afterwards N - R is the
+ * largest multiple of 32 leaving at least `window` tokens in the window (and
+ * never less than before), so R lies in [window, window + 31] once
+ * N >= window.
+ * On success the call updates cache->n_tokens, cache->recent and header[]
+ * (host fields) and enqueues the kernels on `stream`.
+ * Errors: KVQ_ERR_UNSUPPORTED for a tight cache (cap_groups == 0), an MXFP8
+ * K window, an int4 part whose last K group is padded ((N - R) % 32 != 0) or
+ * more than 65,535 (sequence, head) pairs when groups migrate;
+ * KVQ_ERR_WORKSPACE when the reserved room (cap_groups, cap_window) is too
+ * small for the result; the cache is then left unchanged.
+ */
+KVQ_API kvq_status kv_append(kvq_cache *cache, const void *k_new, const void *v_new,
+                             int32_t in_dtype, int32_t n_new, int32_t window,
+                             int32_t *dev_status, kvq_stream_t stream);
 
 /*
  * kv_attend -- O = softmax(sm_scale * Q K^T) V over all N tokens of the cache,

@@ -29,6 +29,7 @@ struct CandArgs {
   const void *v_window;
   int kwin, vwin;
   int Hkv, N, R, cut, Gk;
+  int Gs, Vs, Ws;  // per-(sequence, head) strides: K groups, V rows, window rows
   int Hq, group, n_q, C, validate;
   const void *q;
   int q_dtype;
@@ -93,10 +94,10 @@ __global__ void __launch_bounds__(kWarps * 32) cand_kernel(const CandArgs a) {
     float kv[F], vv[F];
     if (t < a.cut) {
       const int g = t / kGroup, r = t % kGroup;
-      const uint8_t *kc = a.k_codes + ((u * a.Gk + g) * kGroup + r) * (D / 2);
-      const float *ks = a.k_scales + (u * a.Gk + g) * D;
-      const uint8_t *vc = a.v_codes + (u * a.cut + t) * (D / 2);
-      const float *vs = a.v_scales + (u * a.cut + t) * (D / 32);
+      const uint8_t *kc = a.k_codes + ((u * a.Gs + g) * kGroup + r) * (D / 2);
+      const float *ks = a.k_scales + (u * a.Gs + g) * D;
+      const uint8_t *vc = a.v_codes + (u * a.Vs + t) * (D / 2);
+      const float *vs = a.v_scales + (u * a.Vs + t) * (D / 32);
 #pragma unroll
       for (int k = 0; k < F; ++k) {
         const int d = d0 + k;
@@ -106,7 +107,7 @@ __global__ void __launch_bounds__(kWarps * 32) cand_kernel(const CandArgs a) {
                 vs[d / 32];
       }
     } else {
-      const long wr = u * a.R + (t - a.cut);
+      const long wr = u * a.Ws + (t - a.cut);
 #pragma unroll
       for (int k = 0; k < F; ++k) {
         const long wi = wr * D + d0 + k;
@@ -194,11 +195,11 @@ __global__ void __launch_bounds__(kWarps * 32) cand128_kernel(const CandArgs a) 
     }
   }
 
-  const uint8_t *kc_u = a.k_codes + u * a.Gk * kGroup * (D / 2);
-  const float *ks_u = a.k_scales + u * a.Gk * D;
-  const uint8_t *vc_u = a.v_codes + u * a.cut * (D / 2);
-  const float *vs_u = a.v_scales + u * a.cut * (D / 32);
-  const long wbase = u * a.R;
+  const uint8_t *kc_u = a.k_codes + u * a.Gs * kGroup * (D / 2);
+  const float *ks_u = a.k_scales + u * a.Gs * D;
+  const uint8_t *vc_u = a.v_codes + u * a.Vs * (D / 2);
+  const float *vs_u = a.v_scales + u * a.Vs * (D / 32);
+  const long wbase = u * a.Ws;
 
   float m = -CUDART_INF_F, l = 0.0f, o[4] = {0.0f, 0.0f, 0.0f, 0.0f};
   const int tq_max = a.cut > 0 ? a.cut - 1 : 0;
@@ -348,6 +349,9 @@ int launch_attend_candidates(const kvq_cache &c, const void *q, int q_dtype, int
   a.R = d.R;
   a.cut = d.cut;
   a.Gk = d.Gk;
+  a.Gs = d.Gs;
+  a.Vs = d.Vs;
+  a.Ws = d.Ws;
   a.Hq = Hq;
   a.group = Hq / d.Hkv;
   a.n_q = n_q;

@@ -789,6 +789,7 @@ struct HistArgs {
   const uint16_t *k_window, *v_window;  // [unit][R][128] bf16
   uint16_t *k_out, *v_out;  // [unit][N][128] bf16
   int N, R, cut, Gk;
+  int Gs, Vs, Ws;  // per-unit strides: K groups, V rows, window rows
 };
 
 __device__ __forceinline__ float nib(uint32_t w, int e) {
@@ -803,7 +804,7 @@ __global__ void __launch_bounds__(256) history_to_bf16_kernel(const HistArgs a) 
   const int t = i >> 4, q = i & 15;  // token, feature slice 8q..8q+7
   uint4 ko, vo;
   if (t < a.cut) {
-    const long grp = u * a.Gk + (t >> 5);
+    const long grp = u * a.Gs + (t >> 5);
     // byte j of the slice holds features 8q + 2j (low nibble) and 8q + 2j + 1
     const uint32_t kc =
         *reinterpret_cast<const uint32_t *>(a.k_codes + (grp * 32 + (t & 31)) * 64 + 4 * q);
@@ -813,7 +814,7 @@ __global__ void __launch_bounds__(256) history_to_bf16_kernel(const HistArgs a) 
                     pack_bf16x2(nib(kc, 2) * s0.z, nib(kc, 3) * s0.w),
                     pack_bf16x2(nib(kc, 4) * s1.x, nib(kc, 5) * s1.y),
                     pack_bf16x2(nib(kc, 6) * s1.z, nib(kc, 7) * s1.w));
-    const long row = u * a.cut + t;
+    const long row = u * a.Vs + t;
     const uint32_t vc = *reinterpret_cast<const uint32_t *>(a.v_codes + row * 64 + 4 * q);
     const float vs = a.v_scales[row * 4 + (q >> 2)];
     vo = make_uint4(pack_bf16x2(nib(vc, 0) * vs, nib(vc, 1) * vs),
@@ -821,7 +822,7 @@ __global__ void __launch_bounds__(256) history_to_bf16_kernel(const HistArgs a) 
                     pack_bf16x2(nib(vc, 4) * vs, nib(vc, 5) * vs),
                     pack_bf16x2(nib(vc, 6) * vs, nib(vc, 7) * vs));
   } else {
-    const long w = (u * a.R + (t - a.cut)) * 128 + 8 * q;
+    const long w = (u * a.Ws + (t - a.cut)) * 128 + 8 * q;
     ko = *reinterpret_cast<const uint4 *>(a.k_window + w);
     vo = *reinterpret_cast<const uint4 *>(a.v_window + w);
   }
@@ -850,13 +851,14 @@ EncodeTiled encoder() {
   return fn;
 }
 
-// [heads][rows][128] bf16 as a 3-D map, box 64 features x 128 rows x 1 head.
-bool make_map(CUtensorMap *m, const void *ptr, int rows, int heads) {
+// [heads][rows][128] bf16 as a 3-D map, box 64 features x 128 rows x 1 head;
+// consecutive heads are head_rows rows apart (>= rows).
+bool make_map(CUtensorMap *m, const void *ptr, int rows, int heads, long head_rows) {
   EncodeTiled enc = encoder();
   if (!enc) return false;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kDim), static_cast<cuuint64_t>(rows),
                               static_cast<cuuint64_t>(heads)};
-  const cuuint64_t strides[2] = {kDim * 2ull, static_cast<cuuint64_t>(rows) * kDim * 2ull};
+  const cuuint64_t strides[2] = {kDim * 2ull, static_cast<cuuint64_t>(head_rows) * kDim * 2ull};
   const cuuint32_t box[3] = {64, 128, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box,
@@ -869,9 +871,10 @@ bool make_map(CUtensorMap *m, const void *ptr, int rows, int heads) {
 // All-window caches (bf16 K, or MXFP8 K) and int4-history caches whose window,
 // if any, is bf16.
 bool chunk_supported(const kvq_cache &c, int q_dtype, int Hq, int n_q) {
-  const bool all_window = c.recent == c.n_tokens &&
-                          (c.kwin_dtype == KVQ_BF16 || c.kwin_dtype == KVQ_MXFP8) &&
-                          c.vwin_dtype == KVQ_BF16;
+  // (the MXFP8 expansion reads a tight window)
+  const bool all_window =
+      c.recent == c.n_tokens && c.vwin_dtype == KVQ_BF16 &&
+      (c.kwin_dtype == KVQ_BF16 || (c.kwin_dtype == KVQ_MXFP8 && dims_of(c).Ws == c.recent));
   const bool history = c.recent < c.n_tokens &&
                        (c.recent == 0 || (c.kwin_dtype == KVQ_BF16 && c.vwin_dtype == KVQ_BF16));
   return (all_window || history) && c.head_dim == kDim && q_dtype == KVQ_BF16 && n_q >= 64 &&
@@ -916,6 +919,9 @@ int launch_attend_chunk(const kvq_cache &c, const void *q, int Hq, int n_q, floa
     h.R = d.R;
     h.cut = d.cut;
     h.Gk = d.Gk;
+    h.Gs = d.Gs;
+    h.Vs = d.Vs;
+    h.Ws = d.Ws;
     const dim3 grid(static_cast<unsigned>((d.N * 16 + 255) / 256),
                     static_cast<unsigned>(d.B * d.Hkv));
     history_to_bf16_kernel<<<grid, 256, 0, s>>>(h);
@@ -938,9 +944,13 @@ int launch_attend_chunk(const kvq_cache &c, const void *q, int Hq, int n_q, floa
     launches += 2;
   }
   CUtensorMap tq, tk, tv;
-  if (!make_map(&tq, qptr, n_q, c.batch * Hq) ||
-      !make_map(&tk, kptr, c.n_tokens, c.batch * c.kv_heads) ||
-      !make_map(&tv, vptr, c.n_tokens, c.batch * c.kv_heads))
+  // expanded K and V (history, MXFP8) are tight; an all-window cache keeps
+  // its window stride
+  const long k_rows = kptr == c.k_window ? dims_of(c).Ws : c.n_tokens;
+  const long v_rows = vptr == c.v_window ? dims_of(c).Ws : c.n_tokens;
+  if (!make_map(&tq, qptr, n_q, c.batch * Hq, n_q) ||
+      !make_map(&tk, kptr, c.n_tokens, c.batch * c.kv_heads, k_rows) ||
+      !make_map(&tv, vptr, c.n_tokens, c.batch * c.kv_heads, v_rows))
     return -1;
   ChunkArgs a;
   a.n_q = n_q;

@@ -76,6 +76,7 @@ struct DecodeArgs {
   int q_dtype;
   int Hkv, N, R, cut, Gk, Wt, ipu;  // ipu: items per unit = ceil(Gk / 4) + Wt
   int Gi;                           // int4 items per unit = ceil(Gk / 4)
+  int Gs, Vs, Ws;                   // per-unit strides: K groups, V rows, window rows
   int total_items;
   int num_ctas, max_ctas_per_unit;
   float scale_log2;
@@ -406,8 +407,8 @@ __device__ __forceinline__ void load_item(const DecodeArgs &a, int u, int j, uin
     const int ng = min(kGroupsPerItem, a.Gk - g0);
     const int t0 = 32 * g0;
     const int nt = min(32 * kGroupsPerItem, a.cut - t0);
-    const long gi = static_cast<long>(u) * a.Gk + g0;
-    const long ti = static_cast<long>(u) * a.cut + t0;
+    const long gi = static_cast<long>(u) * a.Gs + g0;
+    const long ti = static_cast<long>(u) * a.Vs + t0;
     const uint32_t kb = 2048u * ng, sb = 512u * ng, vb = 64u * nt, wb = 16u * nt;
     mbar_arrive_expect_tx(bar, kb + sb + vb + wb);
     bulk_g2s(dst, a.k_codes + gi * 2048, kb, bar);
@@ -417,7 +418,7 @@ __device__ __forceinline__ void load_item(const DecodeArgs &a, int u, int j, uin
   } else {
     const int w0 = kWinItem * (j - a.Gi);
     const int nt = min(kWinItem, a.R - w0);
-    const long wi = static_cast<long>(u) * a.R + w0;
+    const long wi = static_cast<long>(u) * a.Ws + w0;
     const uint32_t bytes = 256u * nt;
     mbar_arrive_expect_tx(bar, 2u * bytes);
     bulk_g2s(dst, a.k_window + wi * 128, bytes, bar);
@@ -704,6 +705,9 @@ int launch_attend_decode(const kvq_cache &c, const void *q, int q_dtype, float s
   a.R = d.R;
   a.cut = d.cut;
   a.Gk = d.Gk;
+  a.Gs = d.Gs;
+  a.Vs = d.Vs;
+  a.Ws = d.Ws;
   a.Wt = p.Wt;
   a.Gi = p.Gi;
   a.ipu = p.ipu;

@@ -34,6 +34,7 @@ struct GenericArgs {
   const uint8_t *k_e8m0;
   int kwin, vwin;
   int Hkv, N, D, R, cut, Gk;
+  int Gs, Vs, Ws;  // per-(sequence, head) strides: K groups, V rows, window rows
   int Hq, group, n_q;
   const void *q;
   int q_dtype;
@@ -104,10 +105,10 @@ __global__ void __launch_bounds__(kWarps * 32) generic_attend_kernel(GenericArgs
       for (int i = tid; i < kTileKeys * D; i += blockDim.x) {
         const int j = i / D, d = i % D, t = t0 + j;
         const int g = t / kGroup, r = t % kGroup;
-        const long kb = ((u * a.Gk + g) * kGroup + r) * (D / 2) + d / 2;
-        const long vb = (u * a.cut + t) * (D / 2) + d / 2;
-        Ks[j * (D + 1) + d] = nib(a.k_codes[kb], d & 1) * a.k_scales[(u * a.Gk + g) * D + d];
-        Vs[j * D + d] = nib(a.v_codes[vb], d & 1) * a.v_scales[(u * a.cut + t) * (D / 32) + d / 32];
+        const long kb = ((u * a.Gs + g) * kGroup + r) * (D / 2) + d / 2;
+        const long vb = (u * a.Vs + t) * (D / 2) + d / 2;
+        Ks[j * (D + 1) + d] = nib(a.k_codes[kb], d & 1) * a.k_scales[(u * a.Gs + g) * D + d];
+        Vs[j * D + d] = nib(a.v_codes[vb], d & 1) * a.v_scales[(u * a.Vs + t) * (D / 32) + d / 32];
       }
     } else
     for (int i = tid; i < kTileKeys * D; i += blockDim.x) {
@@ -115,15 +116,15 @@ __global__ void __launch_bounds__(kWarps * 32) generic_attend_kernel(GenericArgs
       float kv = 0.0f, vv = 0.0f;
       if (t < a.cut) {
         const int g = t / kGroup, r = t % kGroup;
-        const long kb = ((u * a.Gk + g) * kGroup + r) * (D / 2) + d / 2;
-        kv = nib(a.k_codes[kb], d & 1) * a.k_scales[(u * a.Gk + g) * D + d];
-        const long vb = (u * a.cut + t) * (D / 2) + d / 2;
-        vv = nib(a.v_codes[vb], d & 1) * a.v_scales[(u * a.cut + t) * (D / 32) + d / 32];
+        const long kb = ((u * a.Gs + g) * kGroup + r) * (D / 2) + d / 2;
+        kv = nib(a.k_codes[kb], d & 1) * a.k_scales[(u * a.Gs + g) * D + d];
+        const long vb = (u * a.Vs + t) * (D / 2) + d / 2;
+        vv = nib(a.v_codes[vb], d & 1) * a.v_scales[(u * a.Vs + t) * (D / 32) + d / 32];
       } else if (t < a.N) {
-        const long wi = (u * a.R + (t - a.cut)) * D + d;
+        const long wi = (u * a.Ws + (t - a.cut)) * D + d;
         if (a.kwin == KVQ_MXFP8)
           kv = mxfp8_value(static_cast<const uint8_t *>(a.k_window)[wi],
-                           a.k_e8m0[(u * a.R + (t - a.cut)) * (D / 32) + d / 32]);
+                           a.k_e8m0[(u * a.Ws + (t - a.cut)) * (D / 32) + d / 32]);
         else
           kv = window_value(a.k_window, a.kwin, wi);
         vv = window_value(a.v_window, a.vwin, wi);
@@ -239,18 +240,18 @@ __global__ void __launch_bounds__(kSmallWarps * 32) small_attend_kernel(GenericA
     long wi = 0;
     if (in_codes) {
       const int g = t / kGroup, r = t % kGroup;
-      const uint4 *kc = reinterpret_cast<const uint4 *>(a.k_codes + ((u * a.Gk + g) * kGroup + r) * (D / 2));
-      const uint4 *vc = reinterpret_cast<const uint4 *>(a.v_codes + (u * a.cut + t) * (D / 2));
+      const uint4 *kc = reinterpret_cast<const uint4 *>(a.k_codes + ((u * a.Gs + g) * kGroup + r) * (D / 2));
+      const uint4 *vc = reinterpret_cast<const uint4 *>(a.v_codes + (u * a.Vs + t) * (D / 2));
 #pragma unroll
       for (int w = 0; w < D / 32; ++w) {
         const uint4 x = kc[w], y = vc[w];
         kw[4 * w] = x.x; kw[4 * w + 1] = x.y; kw[4 * w + 2] = x.z; kw[4 * w + 3] = x.w;
         vw[4 * w] = y.x; vw[4 * w + 1] = y.y; vw[4 * w + 2] = y.z; vw[4 * w + 3] = y.w;
-        vs[w] = a.v_scales[(u * a.cut + t) * (D / 32) + w];
+        vs[w] = a.v_scales[(u * a.Vs + t) * (D / 32) + w];
       }
-      ks = a.k_scales + (u * a.Gk + g) * D;  // the same group for the whole warp: broadcast loads
+      ks = a.k_scales + (u * a.Gs + g) * D;  // the same group for the whole warp: broadcast loads
     } else {
-      wi = (u * a.R + (t - a.cut)) * D;
+      wi = (u * a.Ws + (t - a.cut)) * D;
     }
     float s0 = 0.0f, s1 = 0.0f;
     if (in_codes) {
@@ -379,6 +380,9 @@ int launch_attend_generic(const kvq_cache &c, const void *q, int q_dtype, int Hq
   a.R = d.R;
   a.cut = d.cut;
   a.Gk = d.Gk;
+  a.Gs = d.Gs;
+  a.Vs = d.Vs;
+  a.Ws = d.Ws;
   a.Hq = Hq;
   a.group = Hq / d.Hkv;
   a.n_q = n_q;

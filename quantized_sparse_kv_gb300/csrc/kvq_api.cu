@@ -55,6 +55,10 @@ kvq_status check_cache(const kvq_cache *c) {
                 c->vwin_dtype))
     return KVQ_ERR_ARG;
   const int cut = c->n_tokens - c->recent;
+  if (c->cap_groups < 0 || c->cap_window < 0) return KVQ_ERR_ARG;
+  if (c->cap_groups > 0 && (c->cap_groups < (cut + 31) / 32 || c->cap_window < c->recent))
+    return KVQ_ERR_ARG;
+  if (c->cap_groups == 0 && c->cap_window != 0) return KVQ_ERR_ARG;
   if (cut > 0) {
     if (!c->k_codes || !c->k_scales || !c->v_codes || !c->v_scales) return KVQ_ERR_ARG;
     if (!aligned16(c->k_codes) || !aligned16(c->k_scales) || !aligned16(c->v_codes) ||
@@ -106,6 +110,26 @@ kvq_status kvq_cache_sizes(int32_t batch, int32_t kv_heads, int32_t n_tokens, in
   return KVQ_OK;
 }
 
+kvq_status kvq_cache_sizes_reserved(int32_t batch, int32_t kv_heads, int32_t head_dim,
+                                    int32_t kwin_dtype, int32_t vwin_dtype, int32_t cap_groups,
+                                    int32_t cap_window, size_t sizes[8]) {
+  if (!sizes || cap_groups < 1 || cap_window < 0 ||
+      !shape_ok(batch, kv_heads, 1, head_dim, 0, kwin_dtype, vwin_dtype))
+    return KVQ_ERR_ARG;
+  const size_t units = static_cast<size_t>(batch) * kv_heads;
+  const size_t gs = static_cast<size_t>(cap_groups), ws = static_cast<size_t>(cap_window);
+  const size_t d = static_cast<size_t>(head_dim);
+  sizes[0] = units * gs * 32 * d / 2;
+  sizes[1] = units * gs * d * sizeof(float);
+  sizes[2] = units * gs * 32 * d / 2;
+  sizes[3] = units * gs * 32 * (d / 32) * sizeof(float);
+  sizes[4] = units * ws * d * elem_bytes(kwin_dtype);
+  sizes[5] = units * ws * d * elem_bytes(vwin_dtype);
+  sizes[6] = kwin_dtype == KVQ_MXFP8 ? units * ws * (d / 32) : 0;
+  sizes[7] = 16;
+  return KVQ_OK;
+}
+
 size_t kvq_cache_bytes(int32_t batch, int32_t kv_heads, int32_t n_tokens, int32_t head_dim,
                        int32_t recent, int32_t kwin_dtype, int32_t vwin_dtype) {
   size_t s[8];
@@ -132,6 +156,41 @@ kvq_status kv_pack(const void *k, const void *v, int32_t in_dtype, kvq_cache *ca
   const int n = kvq::launch_pack(k, v, in_dtype, *cache, make_ctl(dev_status),
                                  reinterpret_cast<cudaStream_t>(stream));
   return finish(n, "pack");
+}
+
+kvq_status kv_append(kvq_cache *cache, const void *k_new, const void *v_new, int32_t in_dtype,
+                     int32_t n_new, int32_t window, int32_t *dev_status, kvq_stream_t stream) {
+  const kvq_status st = check_cache(cache);
+  if (st != KVQ_OK) return st;
+  if (in_dtype != KVQ_F32 && in_dtype != KVQ_BF16) return KVQ_ERR_ARG;
+  if (n_new < 1 || window < 0 || !k_new || !v_new) return KVQ_ERR_ARG;
+  if (!aligned16(k_new) || !aligned16(v_new) || (dev_status && !aligned16(dev_status)))
+    return KVQ_ERR_ALIGN;
+  if (cache->cap_groups <= 0) return KVQ_ERR_UNSUPPORTED;
+  if ((cache->kwin_dtype != KVQ_F32 && cache->kwin_dtype != KVQ_BF16) ||
+      (cache->vwin_dtype != KVQ_F32 && cache->vwin_dtype != KVQ_BF16))
+    return KVQ_ERR_UNSUPPORTED;
+  const int cut = cache->n_tokens - cache->recent;
+  if (cut % 32) return KVQ_ERR_UNSUPPORTED;  // a padded last K group cannot grow
+  if (n_new > 0x7fffffff - cache->n_tokens) return KVQ_ERR_ARG;
+  const int n2 = cache->n_tokens + n_new;
+  int cut2 = n2 > window ? 32 * ((n2 - window) / 32) : 0;
+  if (cut2 < cut) cut2 = cut;
+  const int r2 = n2 - cut2, m = (cut2 - cut) / 32;
+  if (cut2 / 32 > cache->cap_groups || r2 > cache->cap_window) return KVQ_ERR_WORKSPACE;
+  if (m > 0 && static_cast<long>(cache->batch) * cache->kv_heads > 65535)
+    return KVQ_ERR_UNSUPPORTED;
+  const int n = kvq::launch_append(*cache, k_new, v_new, in_dtype, n_new, m, r2,
+                                   reinterpret_cast<cudaStream_t>(stream));
+  const kvq_status done = finish(n, "append");
+  if (done != KVQ_OK) return done;
+  cache->n_tokens = n2;
+  cache->recent = r2;
+  cache->header[0] = static_cast<uint32_t>(n2);
+  cache->header[1] = static_cast<uint32_t>(cache->head_dim);
+  cache->header[2] = static_cast<uint32_t>(r2);
+  cache->header[3] = 32u;
+  return KVQ_OK;
 }
 
 kvq_status kv_attend(const kvq_cache *cache, const void *q, int32_t q_dtype, int32_t q_heads,

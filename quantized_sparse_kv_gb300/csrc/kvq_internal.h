@@ -11,9 +11,13 @@
 
 namespace kvq {
 
-// Shape of a cache, derived once from a kvq_cache.
+// Shape of a cache, derived once from a kvq_cache. Gs, Vs and Ws are the
+// per-(sequence, head) strides of the K-group, V-row and window arrays: the
+// sizes themselves for a tight cache, the reserved counts for one laid out
+// for kv_append.
 struct CacheDims {
   int B, Hkv, N, D, R, cut, Gk;
+  int Gs, Vs, Ws;
 };
 
 inline CacheDims dims_of(const kvq_cache &c) {
@@ -25,6 +29,9 @@ inline CacheDims dims_of(const kvq_cache &c) {
   d.R = c.recent;
   d.cut = c.n_tokens - c.recent;
   d.Gk = (d.cut + kGroup - 1) / kGroup;
+  d.Gs = c.cap_groups > 0 ? c.cap_groups : d.Gk;
+  d.Vs = c.cap_groups > 0 ? kGroup * c.cap_groups : d.cut;
+  d.Ws = c.cap_window > 0 ? c.cap_window : d.R;
   return d;
 }
 
@@ -45,6 +52,12 @@ inline Regions make_regions(const int32_t *bounds, int n) {
 // pack.cu
 int launch_pack(const void *k, const void *v, int in_dtype, const kvq_cache &c,
                 const KernelCtl &ctl, cudaStream_t s);
+
+// pack.cu: kv_append on a cache with reserved room: n_new tokens per
+// (sequence, head) after the current ones; m groups of the oldest window
+// tokens become int4 and the window becomes R_new rows.
+int launch_append(const kvq_cache &c, const void *k_new, const void *v_new, int in_dtype,
+                  int n_new, int m, int R_new, cudaStream_t s);
 
 // attend_generic.cu: fp32 CUDA-core attention for any supported shape.
 int launch_attend_generic(const kvq_cache &c, const void *q, int q_dtype, int Hq, int n_q,

@@ -48,7 +48,7 @@ __device__ __forceinline__ void load4(const __nv_bfloat16 *p, float (&x)[4]) {
 // warps in shared memory, and each thread writes 2 code bytes per token.
 template <typename T>
 __global__ void __launch_bounds__(256) pack_k128_kernel(const T *__restrict__ k, int N, int cut,
-                                                        int Gk, long u0,
+                                                        int Gs, long u0,
                                                         uint8_t *__restrict__ k_codes,
                                                         float *__restrict__ k_scales) {
   constexpr int D = 128;
@@ -56,7 +56,7 @@ __global__ void __launch_bounds__(256) pack_k128_kernel(const T *__restrict__ k,
   __shared__ __align__(16) float scale[D];
   const int g = blockIdx.x;              // K group
   const long u = u0 + blockIdx.y;        // (sequence, head)
-  const long ug = u * Gk + g;
+  const long ug = u * Gs + g;  // Gs: K groups per (sequence, head) in the arrays
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int valid = min(kGroup, cut - g * kGroup);
   const T *src = k + (u * N + static_cast<long>(g) * kGroup) * D + 4 * lane;
@@ -125,16 +125,17 @@ template <> struct PairOf<__nv_bfloat16> { using type = PairBF16; };
 // its two scales.
 template <typename T>
 __global__ void __launch_bounds__(256) pack_k_kernel(const T *__restrict__ k, long tasks, int N,
-                                                     int D, int cut, int Gk,
+                                                     int D, int cut, int Gk, int Gs,
                                                      uint8_t *__restrict__ k_codes,
                                                      float *__restrict__ k_scales) {
   const long task = blockIdx.x * static_cast<long>(blockDim.x) + threadIdx.x;
   if (task >= tasks) return;
   const int pairs = D / 2;
   const int p = static_cast<int>(task % pairs);
-  const long ug = task / pairs;  // unit * Gk + g
-  const int g = static_cast<int>(ug % Gk);
-  const long u = ug / Gk;
+  const long ugk = task / pairs;  // unit * Gk + g
+  const int g = static_cast<int>(ugk % Gk);
+  const long u = ugk / Gk;
+  const long ug = u * Gs + g;     // position in the arrays
   const int valid = min(kGroup, cut - g * kGroup);
   const T *src = k + (u * N + static_cast<long>(g) * kGroup) * D + 2 * p;
   typename PairOf<T>::type x[kGroup];
@@ -165,7 +166,7 @@ __global__ void __launch_bounds__(256) pack_k_kernel(const T *__restrict__ k, lo
 // within a slice of the unit's tokens, unit), so indices stay 32-bit.
 template <typename T>
 __global__ void __launch_bounds__(256) pack_v_kernel(const T *__restrict__ v, long u0, int t0,
-                                                     int nt, int N, int D, int cut,
+                                                     int nt, int N, int D, int Vs,
                                                      uint8_t *__restrict__ v_codes,
                                                      float *__restrict__ v_scales) {
   const int groups = D / kGroup;
@@ -174,7 +175,7 @@ __global__ void __launch_bounds__(256) pack_v_kernel(const T *__restrict__ v, lo
   const int t = t0 + static_cast<int>(task / groups);  // token < cut
   const int j = static_cast<int>(task % groups);
   const long u = u0 + blockIdx.y;
-  const long row = u * cut + t;  // over (unit, token < cut)
+  const long row = u * Vs + t;  // Vs: V rows per (sequence, head) in the arrays
   const T *src = v + (u * N + t) * D + j * kGroup;
   float x[kGroup];
 #pragma unroll
@@ -199,15 +200,16 @@ __global__ void __launch_bounds__(256) pack_v_kernel(const T *__restrict__ v, lo
 }
 
 // Window copy with dtype change (fp32 <-> bf16, nearest even).
+// Ws: window rows per (sequence, head) in the arrays.
 template <typename TI, typename TO>
 __global__ void window_copy_kernel(const TI *__restrict__ x, long rows, int N, int D, int R,
-                                   TO *__restrict__ w) {
+                                   int Ws, TO *__restrict__ w) {
   const long n = rows * D;
   for (long i = blockIdx.x * static_cast<long>(blockDim.x) + threadIdx.x; i < n;
        i += static_cast<long>(gridDim.x) * blockDim.x) {
     const long row = i / D, d = i % D;
     const long u = row / R, t = row % R;
-    store_from_f32(w + i, load_f32(x + (u * N + (N - R) + t) * D + d));
+    store_from_f32(w + (u * Ws + t) * D + d, load_f32(x + (u * N + (N - R) + t) * D + d));
   }
 }
 
@@ -216,7 +218,7 @@ __global__ void window_copy_kernel(const TI *__restrict__ x, long rows, int N, i
 // elements x * 2^-e rounded to E4M3, nearest even, saturating at 448.
 template <typename TI>
 __global__ void __launch_bounds__(256) window_mxfp8_kernel(const TI *__restrict__ x, long rows,
-                                                           int N, int D, int R,
+                                                           int N, int D, int R, int Ws,
                                                            uint8_t *__restrict__ codes,
                                                            uint8_t *__restrict__ e8m0) {
   const int groups = D / kGroup;
@@ -236,8 +238,9 @@ __global__ void __launch_bounds__(256) window_mxfp8_kernel(const TI *__restrict_
   }
   const float y = ldexpf(val, -e);
   const __nv_fp8_storage_t c = __nv_cvt_float_to_fp8(y, __NV_SATFINITE, __NV_E4M3);
-  codes[row * D + j * kGroup + lane] = static_cast<uint8_t>(c);
-  if (lane == 0) e8m0[row * groups + j] = static_cast<uint8_t>(e + 127);
+  const long dst = u * Ws + t;
+  codes[dst * D + j * kGroup + lane] = static_cast<uint8_t>(c);
+  if (lane == 0) e8m0[dst * groups + j] = static_cast<uint8_t>(e + 127);
 }
 
 template <typename T>
@@ -249,14 +252,14 @@ int pack_typed(const T *k, const T *v, const kvq_cache &c, cudaStream_t s) {
     if (d.D == 128) {
       for (long u0 = 0; u0 < units; u0 += 65535) {  // grid.y holds at most 65,535 units
         const unsigned nu = static_cast<unsigned>(std::min<long>(65535, units - u0));
-        pack_k128_kernel<T><<<dim3(d.Gk, nu), 256, 0, s>>>(k, d.N, d.cut, d.Gk, u0, c.k_codes,
+        pack_k128_kernel<T><<<dim3(d.Gk, nu), 256, 0, s>>>(k, d.N, d.cut, d.Gs, u0, c.k_codes,
                                                            c.k_scales);
         ++launches;
       }
     } else {
       const long ktasks = units * d.Gk * (d.D / 2);
       pack_k_kernel<T><<<static_cast<unsigned>((ktasks + 255) / 256), 256, 0, s>>>(
-          k, ktasks, d.N, d.D, d.cut, d.Gk, c.k_codes, c.k_scales);
+          k, ktasks, d.N, d.D, d.cut, d.Gk, d.Gs, c.k_codes, c.k_scales);
       ++launches;
     }
     // V: per launch at most 65,535 units (grid.y) and 2^24 tokens of each,
@@ -268,7 +271,7 @@ int pack_typed(const T *k, const T *v, const kvq_cache &c, cudaStream_t s) {
         const int nt = std::min(kSlice, d.cut - t0);
         const long vthreads = static_cast<long>(nt) * (d.D / kGroup);
         pack_v_kernel<T><<<dim3(static_cast<unsigned>((vthreads + 255) / 256), nu), 256, 0, s>>>(
-            v, u0, t0, nt, d.N, d.D, d.cut, c.v_codes, c.v_scales);
+            v, u0, t0, nt, d.N, d.D, d.Vs, c.v_codes, c.v_scales);
         ++launches;
       }
     }
@@ -280,24 +283,130 @@ int pack_typed(const T *k, const T *v, const kvq_cache &c, cudaStream_t s) {
     if (c.kwin_dtype == KVQ_MXFP8) {
       const long tasks = rows * (d.D / kGroup);
       window_mxfp8_kernel<T><<<static_cast<unsigned>((tasks + 7) / 8), 256, 0, s>>>(
-          k, rows, d.N, d.D, d.R, static_cast<uint8_t *>(c.k_window), c.k_window_e8m0);
+          k, rows, d.N, d.D, d.R, d.Ws, static_cast<uint8_t *>(c.k_window), c.k_window_e8m0);
     } else if (c.kwin_dtype == KVQ_F32) {
-      window_copy_kernel<T, float><<<blocks, 256, 0, s>>>(k, rows, d.N, d.D, d.R,
+      window_copy_kernel<T, float><<<blocks, 256, 0, s>>>(k, rows, d.N, d.D, d.R, d.Ws,
                                                           static_cast<float *>(c.k_window));
     } else {
       window_copy_kernel<T, __nv_bfloat16><<<blocks, 256, 0, s>>>(
-          k, rows, d.N, d.D, d.R, static_cast<__nv_bfloat16 *>(c.k_window));
+          k, rows, d.N, d.D, d.R, d.Ws, static_cast<__nv_bfloat16 *>(c.k_window));
     }
     if (c.vwin_dtype == KVQ_F32) {
-      window_copy_kernel<T, float><<<blocks, 256, 0, s>>>(v, rows, d.N, d.D, d.R,
+      window_copy_kernel<T, float><<<blocks, 256, 0, s>>>(v, rows, d.N, d.D, d.R, d.Ws,
                                                           static_cast<float *>(c.v_window));
     } else {
       window_copy_kernel<T, __nv_bfloat16><<<blocks, 256, 0, s>>>(
-          v, rows, d.N, d.D, d.R, static_cast<__nv_bfloat16 *>(c.v_window));
+          v, rows, d.N, d.D, d.R, d.Ws, static_cast<__nv_bfloat16 *>(c.v_window));
     }
     launches += 2;
   }
   return launches;
+}
+
+// ------------------------------------------------------------------ kv_append
+// The tokens of one (sequence, head) as an append sees them: the current
+// window rows followed by the new ones, S[i] = window row i for i < R_old and
+// new row i - R_old after. The oldest 32m of them become int4 groups
+// Gk_old .. Gk_old + m - 1 (and V rows cut_old .. cut_old + 32m - 1) by the
+// kv_pack rule; S[32m ..] is the new window.
+struct AppendArgs {
+  const void *k_new, *v_new;  // [units][T][D] in in_dtype
+  int in_dtype, kwin, vwin;
+  uint8_t *k_codes;
+  float *k_scales;
+  uint8_t *v_codes;
+  float *v_scales;
+  void *k_window, *v_window;
+  int D, T, R_old, m, Gk_old, cut_old, Gs, Vs, Ws;
+};
+
+__device__ __forceinline__ float load_as(const void *base, long i, int dt) {
+  return dt == KVQ_F32 ? static_cast<const float *>(base)[i]
+                       : load_f32(static_cast<const __nv_bfloat16 *>(base) + i);
+}
+
+__device__ __forceinline__ float seq_at(const AppendArgs &a, const void *win, const void *fresh,
+                                        int win_dt, long u, int i, int d) {
+  if (i < a.R_old) return load_as(win, (u * a.Ws + i) * a.D + d, win_dt);
+  return load_as(fresh, (u * a.T + (i - a.R_old)) * a.D + d, a.in_dtype);
+}
+
+// One CTA per (migrated group gi, unit). The group's 32 tokens are staged in
+// shared memory as floats ([32][D], K then V); K takes one thread per channel
+// pair, V one thread per (token, 32-feature block).
+__global__ void __launch_bounds__(128) append_migrate_kernel(const AppendArgs a) {
+  extern __shared__ float xs[];
+  const int gi = blockIdx.x;
+  const long u = blockIdx.y;
+  const long grp = u * a.Gs + a.Gk_old + gi;
+  const int D = a.D;
+  for (int e = threadIdx.x; e < kGroup * D; e += blockDim.x)
+    xs[e] = seq_at(a, a.k_window, a.k_new, a.kwin, u, kGroup * gi + e / D, e % D);
+  __syncthreads();
+  for (int p = threadIdx.x; p < D / 2; p += blockDim.x) {
+    float a0 = 0.0f, a1 = 0.0f;
+    for (int t = 0; t < kGroup; ++t) {
+      a0 = fmaxf(a0, fabsf(xs[t * D + 2 * p]));
+      a1 = fmaxf(a1, fabsf(xs[t * D + 2 * p + 1]));
+    }
+    const float s0 = int4_scale(a0), s1 = int4_scale(a1);
+    a.k_scales[grp * D + 2 * p] = s0;
+    a.k_scales[grp * D + 2 * p + 1] = s1;
+    for (int t = 0; t < kGroup; ++t)
+      a.k_codes[(grp * kGroup + t) * (D / 2) + p] = static_cast<uint8_t>(
+          (int4_code(xs[t * D + 2 * p], s0) + 8) | ((int4_code(xs[t * D + 2 * p + 1], s1) + 8) << 4));
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < kGroup * D; e += blockDim.x)
+    xs[e] = seq_at(a, a.v_window, a.v_new, a.vwin, u, kGroup * gi + e / D, e % D);
+  __syncthreads();
+  const int blocks = D / kGroup;
+  for (int task = threadIdx.x; task < kGroup * blocks; task += blockDim.x) {
+    const int t = task / blocks, j = task % blocks;
+    const long row = u * a.Vs + a.cut_old + kGroup * gi + t;
+    const float *x = xs + t * D + kGroup * j;
+    float amax = 0.0f;
+#pragma unroll
+    for (int e = 0; e < kGroup; ++e) amax = fmaxf(amax, fabsf(x[e]));
+    const float sc = int4_scale(amax);
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+    for (int e = 0; e < kGroup; ++e)
+      w[e >> 3] |= static_cast<uint32_t>(int4_code(x[e], sc) + 8) << (4 * (e & 7));
+    *reinterpret_cast<uint4 *>(a.v_codes + row * (D / 2) + j * (kGroup / 2)) =
+        make_uint4(w[0], w[1], w[2], w[3]);
+    a.v_scales[row * blocks + j] = sc;
+  }
+}
+
+__device__ __forceinline__ void store_as(void *base, long i, int dt, float x) {
+  if (dt == KVQ_F32)
+    static_cast<float *>(base)[i] = x;
+  else
+    store_from_f32(static_cast<__nv_bfloat16 *>(base) + i, x);
+}
+
+// The new window, rows [0, R_new) = S[32m ..], one CTA per unit, 32 rows per
+// step with a barrier between steps. With m > 0 a step reads rows at least 32
+// above those it writes, and a row written at step s was read at step s - m,
+// before the barrier; with m = 0 the old rows stay and only new ones are
+// written.
+__global__ void __launch_bounds__(256) append_window_kernel(const AppendArgs a, int R_new) {
+  const long u = blockIdx.x;
+  const int D = a.D;
+  for (int r0 = a.m == 0 ? a.R_old : 0; r0 < R_new; r0 += kGroup) {
+    const int rows = min(kGroup, R_new - r0);
+    for (int e = threadIdx.x; e < rows * D; e += blockDim.x) {
+      const int r = r0 + e / D, d = e % D;
+      const int i = kGroup * a.m + r;
+      const float kx = seq_at(a, a.k_window, a.k_new, a.kwin, u, i, d);
+      const float vx = seq_at(a, a.v_window, a.v_new, a.vwin, u, i, d);
+      const long o = (u * a.Ws + r) * D + d;
+      store_as(a.k_window, o, a.kwin, kx);
+      store_as(a.v_window, o, a.vwin, vx);
+    }
+    __syncthreads();
+  }
 }
 
 }  // namespace
@@ -308,6 +417,41 @@ int launch_pack(const void *k, const void *v, int in_dtype, const kvq_cache &c,
     return pack_typed(static_cast<const float *>(k), static_cast<const float *>(v), c, s);
   return pack_typed(static_cast<const __nv_bfloat16 *>(k), static_cast<const __nv_bfloat16 *>(v),
                     c, s);
+}
+
+int launch_append(const kvq_cache &c, const void *k_new, const void *v_new, int in_dtype,
+                  int n_new, int m, int R_new, cudaStream_t s) {
+  const CacheDims d = dims_of(c);
+  const long units = static_cast<long>(d.B) * d.Hkv;
+  AppendArgs a;
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.in_dtype = in_dtype;
+  a.kwin = c.kwin_dtype;
+  a.vwin = c.vwin_dtype;
+  a.k_codes = c.k_codes;
+  a.k_scales = c.k_scales;
+  a.v_codes = c.v_codes;
+  a.v_scales = c.v_scales;
+  a.k_window = c.k_window;
+  a.v_window = c.v_window;
+  a.D = d.D;
+  a.T = n_new;
+  a.R_old = d.R;
+  a.m = m;
+  a.Gk_old = d.Gk;
+  a.cut_old = d.cut;
+  a.Gs = d.Gs;
+  a.Vs = d.Vs;
+  a.Ws = d.Ws;
+  int launches = 0;
+  if (m > 0) {
+    append_migrate_kernel<<<dim3(static_cast<unsigned>(m), static_cast<unsigned>(units)), 128,
+                            sizeof(float) * kGroup * d.D, s>>>(a);
+    ++launches;
+  }
+  append_window_kernel<<<static_cast<unsigned>(units), 256, 0, s>>>(a, R_new);
+  return launches + 1;
 }
 
 }  // namespace kvq

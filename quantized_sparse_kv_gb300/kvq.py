@@ -42,6 +42,7 @@ class KvqCacheStruct(ctypes.Structure):
         ("k_window", ctypes.c_void_p), ("v_window", ctypes.c_void_p),
         ("k_window_e8m0", ctypes.c_void_p),
         ("header", ctypes.c_uint32 * 4),
+        ("cap_groups", ctypes.c_int32), ("cap_window", ctypes.c_int32),
     ]
 
 
@@ -60,6 +61,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     cp = ctypes.POINTER(KvqCacheStruct)
     lib.kvq_cache_sizes.argtypes = [i32, i32, i32, i32, i32, i32, i32, ctypes.POINTER(sz)]
     lib.kvq_cache_sizes.restype = i32
+    lib.kvq_cache_sizes_reserved.argtypes = [i32, i32, i32, i32, i32, i32, i32,
+                                             ctypes.POINTER(sz)]
+    lib.kvq_cache_sizes_reserved.restype = i32
+    lib.kv_append.argtypes = [cp, vp, vp, i32, i32, i32, vp, vp]
+    lib.kv_append.restype = i32
     lib.kvq_cache_bytes.argtypes = [i32, i32, i32, i32, i32, i32, i32]
     lib.kvq_cache_bytes.restype = sz
     lib.kv_pack.argtypes = [vp, vp, i32, cp, vp, vp]
@@ -99,6 +105,14 @@ def cache_sizes(batch, kv_heads, n_tokens, head_dim, recent, kwin=F32, vwin=F32)
     return list(out)
 
 
+def cache_sizes_reserved(batch, kv_heads, head_dim, kwin, vwin, cap_groups, cap_window) -> list[int]:
+    lib = load_library()
+    out = (ctypes.c_size_t * 8)()
+    _check(lib.kvq_cache_sizes_reserved(batch, kv_heads, head_dim, kwin, vwin, cap_groups,
+                                        cap_window, out), "kvq_cache_sizes_reserved")
+    return list(out)
+
+
 def cache_bytes(batch, kv_heads, n_tokens, head_dim, recent, kwin=F32, vwin=F32) -> int:
     return int(load_library().kvq_cache_bytes(batch, kv_heads, n_tokens, head_dim, recent, kwin,
                                               vwin))
@@ -117,33 +131,60 @@ def _ptr(t) -> ctypes.c_void_p:
 
 
 class PackedCache:
-    """Device arrays of one packed cache plus the C descriptor pointing at them."""
+    """Device arrays of one packed cache plus the C descriptor pointing at them.
+
+    ``reserve=(cap_groups, cap_window)`` lays the arrays out with room for
+    kv_append: cap_groups K groups (32 per group V rows) and cap_window window
+    rows per (sequence, head)."""
 
     def __init__(self, batch, kv_heads, n_tokens, head_dim, recent, kwin="f32", vwin="f32",
-                 device="cuda"):
+                 device="cuda", reserve=None):
         self.batch, self.kv_heads, self.n_tokens = batch, kv_heads, n_tokens
         self.head_dim, self.recent = head_dim, recent
         self.kwin, self.vwin = _dtype(kwin), _dtype(vwin)
         self.cut = n_tokens - recent
         self.gk = -(-self.cut // 32)
+        self.reserve = tuple(reserve) if reserve else (0, 0)
+        if reserve:
+            cap_g, cap_w = self.reserve
+            if cap_g < self.gk or cap_w < recent:
+                raise ValueError("reserve is smaller than the cache")
+            rows_g, rows_v, rows_w = cap_g, 32 * cap_g, cap_w
+        else:
+            rows_g, rows_v, rows_w = self.gk, self.cut, recent
         self.sizes = cache_sizes(batch, kv_heads, n_tokens, head_dim, recent, self.kwin, self.vwin)
         u8 = torch.uint8
         b, h, d = batch, kv_heads, head_dim
-        self.k_codes = torch.empty((b, h, self.gk, 32, d // 2), dtype=u8, device=device)
-        self.k_scales = torch.empty((b, h, self.gk, d), dtype=torch.float32, device=device)
-        self.v_codes = torch.empty((b, h, self.cut, d // 2), dtype=u8, device=device)
-        self.v_scales = torch.empty((b, h, self.cut, d // 32), dtype=torch.float32, device=device)
+        self.k_codes = torch.empty((b, h, rows_g, 32, d // 2), dtype=u8, device=device)
+        self.k_scales = torch.empty((b, h, rows_g, d), dtype=torch.float32, device=device)
+        self.v_codes = torch.empty((b, h, rows_v, d // 2), dtype=u8, device=device)
+        self.v_scales = torch.empty((b, h, rows_v, d // 32), dtype=torch.float32, device=device)
         kdt = u8 if self.kwin == MXFP8 else TORCH_OF[self.kwin]
-        self.k_window = torch.empty((b, h, recent, d), dtype=kdt, device=device)
-        self.v_window = torch.empty((b, h, recent, d), dtype=TORCH_OF[self.vwin], device=device)
-        self.k_window_e8m0 = torch.empty((b, h, recent, d // 32) if self.kwin == MXFP8 else (0,),
+        self.k_window = torch.empty((b, h, rows_w, d), dtype=kdt, device=device)
+        self.v_window = torch.empty((b, h, rows_w, d), dtype=TORCH_OF[self.vwin], device=device)
+        self.k_window_e8m0 = torch.empty((b, h, rows_w, d // 32) if self.kwin == MXFP8 else (0,),
                                          dtype=u8, device=device)
         self.struct = KvqCacheStruct(
             batch, kv_heads, n_tokens, head_dim, recent, self.kwin, self.vwin,
             _ptr(self.k_codes), _ptr(self.k_scales), _ptr(self.v_codes), _ptr(self.v_scales),
             _ptr(self.k_window), _ptr(self.v_window), _ptr(self.k_window_e8m0),
-            (ctypes.c_uint32 * 4)(0, 0, 0, 0))
+            (ctypes.c_uint32 * 4)(0, 0, 0, 0), self.reserve[0], self.reserve[1])
         self.ref = ctypes.byref(self.struct)
+
+    def _sync_shape(self):
+        """Take n_tokens and recent back from the descriptor (kv_append moves them)."""
+        self.n_tokens, self.recent = int(self.struct.n_tokens), int(self.struct.recent)
+        self.cut = self.n_tokens - self.recent
+        self.gk = -(-self.cut // 32)
+        self.sizes = cache_sizes(self.batch, self.kv_heads, self.n_tokens, self.head_dim,
+                                 self.recent, self.kwin, self.vwin)
+
+    def used(self) -> dict:
+        """Views of the filled part of every array (the tight layout's content)."""
+        return {"k_codes": self.k_codes[:, :, :self.gk], "k_scales": self.k_scales[:, :, :self.gk],
+                "v_codes": self.v_codes[:, :, :self.cut], "v_scales": self.v_scales[:, :, :self.cut],
+                "k_window": self.k_window[:, :, :self.recent],
+                "v_window": self.v_window[:, :, :self.recent]}
 
     @property
     def header(self):
@@ -164,10 +205,12 @@ def read_status(status: torch.Tensor) -> int:
 
 
 def pack(k: torch.Tensor, v: torch.Tensor, recent: int, kwin="f32", vwin=None,
-         status: torch.Tensor | None = None, out: PackedCache | None = None) -> PackedCache:
+         status: torch.Tensor | None = None, out: PackedCache | None = None,
+         reserve=None) -> PackedCache:
     """kv_pack: k, v (batch, kv_heads, N, D) fp32 or bf16 on the GPU.
 
-    ``out`` reuses the arrays of an existing cache of the same shape."""
+    ``out`` reuses the arrays of an existing cache of the same shape;
+    ``reserve=(cap_groups, cap_window)`` leaves room for kv_append."""
     if k.dtype not in (torch.float32, torch.bfloat16) or v.dtype != k.dtype:
         raise TypeError("k and v must both be float32 or bfloat16")
     k = k.contiguous()
@@ -175,7 +218,7 @@ def pack(k: torch.Tensor, v: torch.Tensor, recent: int, kwin="f32", vwin=None,
     b, h, n, d = k.shape
     if out is None:
         vw = vwin if vwin is not None else ("f32" if _dtype(kwin) == F32 else "bf16")
-        out = PackedCache(b, h, n, d, recent, kwin, vw, device=k.device)
+        out = PackedCache(b, h, n, d, recent, kwin, vw, device=k.device, reserve=reserve)
     in_dt = F32 if k.dtype == torch.float32 else BF16
     lib = load_library()
     _check(lib.kv_pack(_ptr(k), _ptr(v), in_dt, out.ref,
@@ -291,3 +334,22 @@ def attend_candidates(cache: PackedCache, q: torch.Tensor, idx: torch.Tensor,
 def debug_set(wait_limit_ns: int = 0, drop_item: int = -1):
     """Failure-test hook (see kvq_debug_set in include/kvq.h)."""
     load_library().kvq_debug_set(int(wait_limit_ns), int(drop_item))
+
+
+def append(cache: PackedCache, k_new: torch.Tensor, v_new: torch.Tensor, window: int,
+           status: torch.Tensor | None = None) -> PackedCache:
+    """kv_append: k_new, v_new (batch, kv_heads, T, D) fp32 or bf16 on the GPU,
+    added after the cache's tokens; the window keeps at least ``window`` tokens
+    and whole 32-token groups move from its oldest end into int4."""
+    if k_new.dtype not in (torch.float32, torch.bfloat16) or v_new.dtype != k_new.dtype:
+        raise TypeError("k_new and v_new must both be float32 or bfloat16")
+    k_new, v_new = k_new.contiguous(), v_new.contiguous()
+    b, h, t, d = k_new.shape
+    if (b, h, d) != (cache.batch, cache.kv_heads, cache.head_dim) or v_new.shape != k_new.shape:
+        raise ValueError("new tokens do not match the cache")
+    in_dt = F32 if k_new.dtype == torch.float32 else BF16
+    lib = load_library()
+    _check(lib.kv_append(cache.ref, _ptr(k_new), _ptr(v_new), in_dt, t, window,
+                         _ptr(status) if status is not None else None, _stream()), "kv_append")
+    cache._sync_shape()
+    return cache

@@ -89,3 +89,19 @@ def test_product_path_never_touches_the_oracle():
                 text = open(os.path.join(dirpath, f), encoding="utf-8").read()
                 assert not re.search(r"^\s*(from|import)\s+oracle", text, flags=re.M), f
                 assert "kvq_oracle" not in text, f
+
+
+def test_binding_struct_matches_header():
+    # the ctypes descriptor lists the header's kvq_cache fields in order
+    from quantized_sparse_kv_gb300 import kvq as k
+    text = open(k.HEADER, encoding="utf-8").read()
+    body = re.search(r"typedef struct kvq_cache \{(.*?)\} kvq_cache;", text, flags=re.S).group(1)
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    names = []
+    for decl in body.split(";"):
+        decl = decl.strip()
+        if not decl:
+            continue
+        for part in decl.split(","):
+            names.append(re.findall(r"(\w+)\s*(?:\[\d+\])?\s*$", part.strip())[0])
+    assert names == [f[0] for f in k.KvqCacheStruct._fields_]
