@@ -348,6 +348,38 @@ def row_decode(kvq, synth, torch, steps, warmup, pk, batch, context):
             "launches": a.launches()}
 
 
+def row_append(kvq, synth, torch, steps, warmup, pk):
+    """kv_append of one decoded token per (sequence, KV head) on the decode
+    cache (64 sequences x 2 KV heads, D = 128, window 128): every 32nd call
+    also moves a 32-token group from the window into int4."""
+    d = DECODE
+    n_calls = 32 * max(1, -(-steps // 32))
+    extra = n_calls + 32 * (warmup + 2)
+    q, k, v = synth.decode_inputs_torch(41, d["batch"], d["context"] + extra, "cuda")
+    n0 = d["context"]
+    cache = kvq.pack(k[:, :, :n0], v[:, :, :n0], d["recent"], "bf16",
+                     reserve=(-(-(n0 + extra) // 32), d["recent"] + 32))
+    news = [(k[:, :, t:t + 1].contiguous(), v[:, :, t:t + 1].contiguous())
+            for t in range(n0, n0 + extra)]
+    del q
+    state = {"i": 0}
+
+    def one():
+        kn, vn = news[state["i"]]
+        kvq.append(cache, kn, vn, d["recent"])
+        state["i"] += 1
+    ms = time_steps(one, n_calls, 32 * warmup)
+    nbytes = 2 * d["batch"] * d["kv_heads"] * d["head_dim"] * 2 * 2  # new rows in, window rows out
+    return {"workload": "kv_append: 1 token per (sequence, KV head), 64 x 2 heads, D=128, bf16, "
+                        "window 128, int4 groups of 32 (a group migrates every 32nd call)",
+            "ms": ms, "tokens_per_s": d["batch"] * d["kv_heads"] / (ms * 1e-3),
+            "roofline": {"bound": "latency", "achieved": nbytes / (ms * 1e-3) / 1e9,
+                         "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": nbytes / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], "traffic": None,
+                         "note": "64 KB of new rows per call: launch-latency bound"},
+            "launches": "1 per call, 2 on every 32nd"}
+
+
 # ---------------------------------------------------------------- oracle (CPU) arm
 
 def _oracle_unit_worker(args):
@@ -577,6 +609,7 @@ ROWS = {
     "decode_B64_L1024": lambda kvq, synth, torch, st, w, pk:
         row_decode(kvq, synth, torch, st, w, pk, 64, 1024),
     "pack": lambda kvq, synth, torch, st, w, pk: row_pack(kvq, synth, torch, st, w, pk),
+    "append": lambda kvq, synth, torch, st, w, pk: row_append(kvq, synth, torch, st, w, pk),
     "small_d_fp32": lambda kvq, synth, torch, st, w, pk: row_small(kvq, synth, torch, st, w, pk),
     "candidates_L131072_C256": lambda kvq, synth, torch, st, w, pk:
         row_candidates(kvq, synth, torch, st, w, pk, 131072, 256),
