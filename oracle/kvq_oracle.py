@@ -363,3 +363,101 @@ def mxfp8_dequantize(codes, scale_bytes) -> np.ndarray:
 def probability_tv(p, p_ref) -> np.ndarray:
     """Per-row total variation 0.5 * sum |p - p_ref| (reported only; parity unpinned)."""
     return 0.5 * np.abs(np.asarray(p) - np.asarray(p_ref)).sum(axis=-1)
+
+
+# --------------------------------------------------------------------------------------
+# Observer statistics of attention rows (Catnip study: section 实验设计, step 5 and
+# the Structural / Effective / Numerical MXFP8 notes; section "Q/K 与 probability
+# quantization 的影响" for the signed-H128 + MXFP8 Q/K path, the P-path proxy and
+# the argmax agreement)
+# --------------------------------------------------------------------------------------
+
+FP32_HALF_TINY = 2.0 ** -150   # fp64 values below this round to 0 in fp32
+
+
+def hadamard(n: int) -> np.ndarray:
+    """Sylvester Hadamard matrix of order n (a power of two), entries +-1."""
+    h = np.ones((1, 1))
+    while h.shape[0] < n:
+        h = np.block([[h, h], [h, -h]])
+    return h
+
+
+def signed_hadamard(x, signs) -> np.ndarray:
+    """x -> (x * signs) H / sqrt(D) along the last axis.
+
+    An orthogonal rotation (H / sqrt(D) is symmetric and orthogonal, signs are
+    +-1), so q . k is unchanged when both sides are rotated; it spreads a large
+    channel over all channels before MXFP8 rounding (the page's signed-H128)."""
+    x = np.asarray(x, dtype=np.float64)
+    d = x.shape[-1]
+    return (x * np.asarray(signs, dtype=np.float64)) @ hadamard(d) / math.sqrt(d)
+
+
+def mxfp8_round(x) -> np.ndarray:
+    """Every element's MXFP8 value, one scale per 32 along the last axis; a
+    partial last block is padded with zeros (which do not change its maximum)."""
+    x = np.asarray(x, dtype=np.float64)
+    d = x.shape[-1]
+    pad = (-d) % GROUP
+    if pad:
+        x = np.concatenate([x, np.zeros(x.shape[:-1] + (pad,))], axis=-1)
+    codes, scales = mxfp8_quantize(x)
+    return mxfp8_dequantize(codes, scales)[..., :d]
+
+
+def top_count(n: int, percent: int) -> int:
+    """ceil(percent% of n): how many of the largest probabilities a top-x% mass sums."""
+    return (n * percent + 99) // 100
+
+
+def row_statistics(s, s_mx=None) -> dict:
+    """Statistics of softmax rows over scores s (rows, N), already scaled.
+
+    entropy   H = -sum p ln p (nats, over p > 0)
+    support   exp(H) / N, the entropy-equivalent share of the keys
+    top1/5/10 mass of the top_count(N, 1 / 5 / 10) largest probabilities
+    zero      share of keys whose probability is 0 in fp32 (structural zeros)
+    p_zero    share of keys whose probability is nonzero in fp32 but 0 after
+              MXFP8 rounding along the keys (E4M3, one E8M0 scale per 32 keys)
+    p_tv      0.5 sum |p_mx - p|; p_sum = sum p_mx (the P-path proxy row sum)
+    With s_mx, the scores of the MXFP8 Q/K path for the same rows:
+    qk_tv     0.5 sum |softmax(s_mx) - p|
+    qk_agree  1 where argmax s_mx == argmax s (first index of the maximum)
+    """
+    s = np.asarray(s, dtype=np.float64)
+    n = s.shape[-1]
+    e = np.exp(s - s.max(axis=-1, keepdims=True))
+    p = e / e.sum(axis=-1, keepdims=True)
+    live = p >= FP32_HALF_TINY
+    plogp = np.where(p > 0, p * np.log(np.where(p > 0, p, 1.0)), 0.0)
+    h = -plogp.sum(axis=-1)
+    ps = -np.sort(-p, axis=-1)
+    out = {"entropy": h, "support": np.exp(h) / n,
+           "top1": ps[..., :top_count(n, 1)].sum(-1), "top5": ps[..., :top_count(n, 5)].sum(-1),
+           "top10": ps[..., :top_count(n, 10)].sum(-1),
+           "zero": (~live).sum(-1) / n}
+    p_mx = mxfp8_round(p)
+    out["p_zero"] = (live & (p_mx == 0)).sum(-1) / n
+    out["p_tv"] = 0.5 * np.abs(p_mx - p).sum(-1)
+    out["p_sum"] = p_mx.sum(-1)
+    if s_mx is not None:
+        s_mx = np.asarray(s_mx, dtype=np.float64)
+        e2 = np.exp(s_mx - s_mx.max(axis=-1, keepdims=True))
+        out["qk_tv"] = 0.5 * np.abs(e2 / e2.sum(axis=-1, keepdims=True) - p).sum(-1)
+        out["qk_agree"] = (np.argmax(s_mx, axis=-1) == np.argmax(s, axis=-1)).astype(np.float64)
+    return out
+
+
+def attention_statistics(q, k_hat, signs=None, sm_scale=None) -> dict:
+    """row_statistics of softmax(sm_scale q k_hat^T) for q (n_q, D) over k_hat (N, D),
+    with the MXFP8 Q/K path: q and k_hat rotated by signed_hadamard when signs
+    are given, then both rounded to MXFP8 along D."""
+    q = np.asarray(q, dtype=np.float64)
+    k_hat = np.asarray(k_hat, dtype=np.float64)
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(q.shape[-1])
+    qr, kr = (q, k_hat) if signs is None else (signed_hadamard(q, signs), signed_hadamard(k_hat, signs))
+    s = sm_scale * (q @ k_hat.T)
+    s_mx = sm_scale * (mxfp8_round(qr) @ mxfp8_round(kr).T)
+    return row_statistics(s, s_mx)

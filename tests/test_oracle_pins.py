@@ -407,3 +407,115 @@ def test_page_matched_focus_variants():
     assert max(err) - min(err) < 0.2
     for got, want in zip(err, rows["early"]["rel_l2_pct"]):
         assert abs(got - want) <= 1.5
+
+
+# ------------------------------------------------------------------ observer statistics
+# (Catnip study: entropy support, top-k mass, structural and MXFP8 numerical
+# zeros, P-path TV and row sum, signed-H128 + MXFP8 Q/K TV and argmax agreement)
+
+def test_statistics_of_a_uniform_row_in_closed_form():
+    n = 100
+    st = O.row_statistics(np.zeros((1, n)))
+    assert np.isclose(st["entropy"][0], math.log(n)) and np.isclose(st["support"][0], 1.0)
+    # ceil(1 %, 5 %, 10 % of 100) = 1, 5, 10 keys of mass 1/100 each
+    assert np.allclose([st["top1"][0], st["top5"][0], st["top10"][0]], [0.01, 0.05, 0.10])
+    assert st["zero"][0] == 0 and st["p_zero"][0] == 0
+    # 1/100 in a block whose scale is 2^(floor(log2 0.01) - 8) = 2^-15: 327.68 -> E4M3 320
+    assert np.isclose(st["p_sum"][0], 100 * 320 * 2.0 ** -15)
+    assert np.isclose(st["p_tv"][0], 0.5 * 100 * (0.01 - 320 * 2.0 ** -15))
+
+
+def test_statistics_of_a_one_hot_row():
+    n = 64
+    s = np.zeros((1, n))
+    s[0, 17] = 1000.0
+    st = O.row_statistics(s)
+    assert abs(st["entropy"][0]) < 1e-12 and np.isclose(st["support"][0], 1.0 / n)
+    assert st["top1"][0] == 1.0 and st["top10"][0] == 1.0
+    assert st["zero"][0] == (n - 1) / n        # e^-1000 is 0 in fp32
+    assert st["p_zero"][0] == 0 and st["p_sum"][0] == 1.0 and st["p_tv"][0] == 0
+
+
+def test_statistics_of_a_two_level_row():
+    # k keys at score a, n - k at 0: p_hi = e^a / Z, p_lo = 1 / Z
+    n, k, a = 200, 6, 3.0
+    s = np.zeros((1, n))
+    s[0, :k] = a
+    z = k * math.exp(a) + (n - k)
+    ph, pl = math.exp(a) / z, 1.0 / z
+    st = O.row_statistics(s)
+    h = -(k * ph * math.log(ph) + (n - k) * pl * math.log(pl))
+    assert np.isclose(st["entropy"][0], h) and np.isclose(st["support"][0], math.exp(h) / n)
+    assert np.isclose(st["top1"][0], 2 * ph)               # ceil(2.0) = 2 keys
+    assert np.isclose(st["top5"][0], k * ph + 4 * pl)      # 10 keys
+    assert np.isclose(st["top10"][0], k * ph + 14 * pl)    # 20 keys
+
+
+def test_top_count_rounds_up():
+    assert [O.top_count(6240, p) for p in (1, 5, 10)] == [63, 312, 624]
+    assert [O.top_count(100, p) for p in (1, 5, 10)] == [1, 5, 10]
+    assert O.top_count(101, 1) == 2
+
+
+def test_mxfp8_round_along_a_row():
+    # block max 1 -> scale 2^-8: 2^-17 is the smallest subnormal step (2^-9 * 2^-8),
+    # 2^-20 rounds to 0, 0.3 * 256 = 76.8 -> 80 (step 8 in [64, 128))
+    x = np.zeros(40)
+    x[:4] = [1.0, 2.0 ** -20, 2.0 ** -17, 0.3]
+    x[33] = 0.3                                   # partial second block, its own scale
+    y = O.mxfp8_round(x)
+    assert list(y[:4]) == [1.0, 0.0, 2.0 ** -17, 80 / 256]
+    # its own block: scale 2^(floor(log2 0.3) - 8) = 2^-10, 307.2 -> 320 (step 32)
+    assert y[33] == 320 * 2.0 ** -10
+
+
+def test_numerical_zeros_of_the_p_path():
+    # one dominant key and 31 at 2^-20 of it: after MXFP8 rounding (block scale
+    # 2^-8) the 31 small ones are 0 although they are not 0 in fp32
+    n = 32
+    s = np.full((1, n), -20 * math.log(2.0))
+    s[0, 0] = 0.0
+    st = O.row_statistics(s)
+    assert st["zero"][0] == 0 and st["p_zero"][0] == 31 / n
+    pmax = 1.0 / (1.0 + 31 * 2.0 ** -20)
+    assert np.isclose(st["p_sum"][0], O.mxfp8_round(np.array([pmax]))[0])
+
+
+def test_qk_path_identical_and_disagreeing():
+    rng = np.random.default_rng(3)
+    s = rng.standard_normal((4, 50))
+    st = O.row_statistics(s, s)
+    assert np.all(st["qk_tv"] == 0) and np.all(st["qk_agree"] == 1)
+    s2 = s.copy()
+    s2[0, np.argmin(s2[0])] = 100.0
+    st2 = O.row_statistics(s, s2)
+    # the spiked key takes almost all the mass on one side and little on the other
+    assert st2["qk_agree"][0] == 0 and st2["qk_tv"][0] > 0.9
+
+
+def test_signed_hadamard_is_orthogonal_and_keeps_dot_products():
+    h = O.hadamard(128)
+    assert np.array_equal(h @ h.T, 128 * np.eye(128))
+    assert np.array_equal(O.hadamard(2), np.array([[1, 1], [1, -1]]))
+    rng = np.random.default_rng(4)
+    signs = rng.choice([-1.0, 1.0], 128)
+    q, k = rng.standard_normal((3, 128)), rng.standard_normal((5, 128))
+    qr, kr = O.signed_hadamard(q, signs), O.signed_hadamard(k, signs)
+    assert np.allclose(qr @ kr.T, q @ k.T)
+    # a spike in one channel becomes a flat vector of magnitude 1/sqrt(128)
+    e = np.zeros(128)
+    e[5] = 1.0
+    assert np.allclose(np.abs(O.signed_hadamard(e, signs)), 1 / math.sqrt(128))
+    # H / sqrt(D) undoes itself; the signs then undo themselves
+    assert np.allclose(O.signed_hadamard(qr, np.ones(128)) * signs, q)
+
+
+def test_attention_statistics_reference_path_ignores_the_rotation():
+    rng = np.random.default_rng(6)
+    q, k = rng.standard_normal((2, 128)), rng.standard_normal((70, 128))
+    signs = rng.choice([-1.0, 1.0], 128)
+    a = O.attention_statistics(q, k, signs)
+    b = O.attention_statistics(q, k, None)
+    for key in ("entropy", "support", "top1", "zero", "p_zero", "p_tv", "p_sum"):
+        assert np.allclose(a[key], b[key])
+    assert np.all(a["qk_tv"] < 0.1) and np.all(b["qk_tv"] < 0.1)
