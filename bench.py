@@ -380,6 +380,32 @@ def row_append(kvq, synth, torch, steps, warmup, pk):
             "launches": "1 per call, 2 on every 32nd"}
 
 
+def row_stats(kvq, synth, torch, steps, warmup, pk):
+    """kv_attend_stats on the video chunk: 96 sampled query rows per head (the
+    pages' observer samples 96 queries per head), 32 heads over 6,240 keys,
+    with the signed-H128 MXFP8 Q/K path."""
+    import numpy as np
+    c = CHUNK
+    q, k, v = synth.chunk_inputs_torch(51, "cuda")
+    cache = kvq.pack(k, v, c["n_kv"], "bf16")
+    qs = q[:, :, ::c["n_q"] // 96][:, :, :96].contiguous()
+    signs = torch.from_numpy(np.random.default_rng(2).choice([-1.0, 1.0], c["head_dim"]))
+    kvq.attend_stats(cache, qs, signs)
+    sg = signs.cuda().float()
+    ms = time_steps(lambda: kvq.attend_stats(cache, qs, sg), steps, warmup)
+    rows = c["heads"] * 96
+    flops = rows * c["n_kv"] * 2 * (2 * c["head_dim"])   # the two score dot products
+    peak = 152 * 128 * 2 * 2.07e9 / 1e12                  # fp32 FMA issue rate at 2.07 GHz
+    tf = flops / (ms * 1e-3) / 1e12
+    return {"workload": "kv_attend_stats: 32 heads x 96 sampled queries over 6240 bf16 keys, "
+                        "signed-H128 MXFP8 Q/K path, MXFP8 P path, top-k by sort",
+            "ms": ms, "rows_per_s": rows / (ms * 1e-3),
+            "roofline": {"bound": "alu", "achieved": tf, "peak": peak, "unit": "TFLOP/s",
+                         "frac": tf / peak, "traffic": None,
+                         "peak_note": "fp32 FMA: 152 SMs x 128 lanes x 2 flop x 2.07 GHz"},
+            "launches": 1}
+
+
 # ---------------------------------------------------------------- oracle (CPU) arm
 
 def _oracle_unit_worker(args):
@@ -620,6 +646,7 @@ ROWS = {
         row_chunk(kvq, synth, torch, st, w, pk, "mxfp8"),
     "chunk_int4_history": lambda kvq, synth, torch, st, w, pk:
         row_chunk(kvq, synth, torch, st, w, pk, "int4"),
+    "stats_chunk_96q": lambda kvq, synth, torch, st, w, pk: row_stats(kvq, synth, torch, st, w, pk),
 }
 
 

@@ -196,6 +196,45 @@ KVQ_API kvq_status kv_attend(const kvq_cache *cache, const void *q, int32_t q_dt
                              float *region_mass, void *workspace, size_t *ws_bytes,
                              int32_t *dev_status, kvq_stream_t stream);
 
+/* Columns of kv_attend_stats' output, one row of KVQ_N_STATS floats per query. */
+enum {
+  KVQ_STAT_ENTROPY = 0,  /* H = -sum p ln p (nats) */
+  KVQ_STAT_SUPPORT = 1,  /* exp(H) / N: entropy-equivalent share of the keys */
+  KVQ_STAT_TOP1 = 2,     /* mass of the ceil(1 % of N) largest probabilities */
+  KVQ_STAT_TOP5 = 3,     /* ... ceil(5 %) */
+  KVQ_STAT_TOP10 = 4,    /* ... ceil(10 %) */
+  KVQ_STAT_ZERO = 5,     /* share of probabilities exactly 0 in fp32 */
+  KVQ_STAT_P_ZERO = 6,   /* share of keys nonzero in fp32 but 0 on the MXFP8 P path */
+  KVQ_STAT_P_TV = 7,     /* 0.5 sum |p_mx - p| on the MXFP8 P path */
+  KVQ_STAT_P_SUM = 8,    /* sum p_mx (the P-path proxy row sum) */
+  KVQ_STAT_QK_TV = 9,    /* 0.5 sum |p_qk - p|, p_qk from MXFP8 Q/K */
+  KVQ_STAT_QK_AGREE = 10, /* 1 when p_qk and p have the same argmax (first index), else 0 */
+  KVQ_N_STATS = 11
+};
+
+/*
+ * kv_attend_stats -- observer statistics of attention rows (Catnip study,
+ * "Catnip Week 10 KV Cache Attention Study", section 实验设计 step 5 with its
+ * Structural / Effective / Numerical MXFP8 notes, and section "Q/K 与
+ * probability quantization 的影响"). For each query row, p is the fp32
+ * softmax of sm_scale * q K^T over all N keys of the cache, K as kv_attend
+ * reads it. The MXFP8 P path rounds p to E4M3 with one E8M0 scale per 32
+ * consecutive keys (the scale rule of the MXFP8 K window). The MXFP8 Q/K path
+ * rotates q and every key by the signed Hadamard transform
+ * x -> (x * signs) H / sqrt(D) (H the Sylvester Hadamard matrix of order D)
+ * when hadamard_signs is not NULL, rounds both to MXFP8 along D and takes the
+ * softmax of their scores (p_qk).
+ * q: [batch][q_heads][n_q][D] in q_dtype (F32 or BF16), device; typically a
+ *   sample of query rows. hadamard_signs: device float [D] of +-1, or NULL.
+ * stats: device float [batch][q_heads][n_q][KVQ_N_STATS], see KVQ_STAT_*.
+ * Restrictions (else KVQ_ERR_UNSUPPORTED): D in {32, 64, 128, 256},
+ * N <= 16384. No workspace is needed.
+ */
+KVQ_API kvq_status kv_attend_stats(const kvq_cache *cache, const void *q, int32_t q_dtype,
+                                   int32_t q_heads, int32_t n_q, float sm_scale,
+                                   const float *hadamard_signs, float *stats,
+                                   int32_t *dev_status, kvq_stream_t stream);
+
 /*
  * kv_attend_candidates -- exact attention of each query row over its own
  * candidate keys only (MiniCPM5-2B study, sections 6 and 9): row (b, h, i)

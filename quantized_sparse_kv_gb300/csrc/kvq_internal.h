@@ -89,4 +89,9 @@ int launch_attend_chunk(const kvq_cache &c, const void *q, int Hq, int n_q, floa
                         void *out, int out_dtype, const int32_t *bounds, int n_regions,
                         float *mass, void *ws, const KernelCtl &ctl, cudaStream_t s);
 
+// attend_stats.cu: observer statistics of attention rows (kv_attend_stats).
+int stats_max_tokens();
+int launch_attend_stats(const kvq_cache &c, const void *q, int q_dtype, int Hq, int n_q,
+                        float sm_scale, const float *signs, float *stats, cudaStream_t s);
+
 }  // namespace kvq

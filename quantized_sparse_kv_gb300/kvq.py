@@ -20,6 +20,9 @@ TORCH_OF = {F32: torch.float32, BF16: torch.bfloat16}
 STATUS = {0: "KVQ_OK", 1: "KVQ_ERR_ARG", 2: "KVQ_ERR_ALIGN", 3: "KVQ_ERR_UNSUPPORTED",
           4: "KVQ_ERR_WORKSPACE", 5: "KVQ_ERR_CUDA"}
 DEV_INDEX, DEV_DUP, DEV_TIMEOUT, DEV_BOUNDS = 1, 2, 4, 8
+# columns of kv_attend_stats (include/kvq.h, KVQ_STAT_*)
+STATS = ("entropy", "support", "top1", "top5", "top10", "zero", "p_zero", "p_tv", "p_sum",
+         "qk_tv", "qk_agree")
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libkvq.so")
@@ -66,6 +69,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.kvq_cache_sizes_reserved.restype = i32
     lib.kv_append.argtypes = [cp, vp, vp, i32, i32, i32, vp, vp]
     lib.kv_append.restype = i32
+    lib.kv_attend_stats.argtypes = [cp, vp, i32, i32, i32, f32, vp, vp, vp, vp]
+    lib.kv_attend_stats.restype = i32
     lib.kvq_cache_bytes.argtypes = [i32, i32, i32, i32, i32, i32, i32]
     lib.kvq_cache_bytes.restype = sz
     lib.kv_pack.argtypes = [vp, vp, i32, cp, vp, vp]
@@ -353,3 +358,27 @@ def append(cache: PackedCache, k_new: torch.Tensor, v_new: torch.Tensor, window:
                          _ptr(status) if status is not None else None, _stream()), "kv_append")
     cache._sync_shape()
     return cache
+
+
+def attend_stats(cache: PackedCache, q: torch.Tensor, signs: torch.Tensor | None = None,
+                 sm_scale: float = 0.0, status: torch.Tensor | None = None) -> torch.Tensor:
+    """kv_attend_stats: observer statistics of the softmax rows of q over the
+    cache; returns float32 (batch, q_heads, n_q, len(STATS)), columns STATS.
+    ``signs`` (D,) of +-1 turns on the signed Hadamard rotation of the MXFP8
+    Q/K path."""
+    q = q.contiguous()
+    if q.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("q must be float32 or bfloat16")
+    b, hq, nq, d = q.shape
+    out = torch.empty((b, hq, nq, len(STATS)), dtype=torch.float32, device=q.device)
+    sg = None
+    if signs is not None:
+        sg = signs.to(device=q.device, dtype=torch.float32).contiguous()
+        if sg.shape != (d,):
+            raise ValueError("signs must have head_dim entries")
+    lib = load_library()
+    _check(lib.kv_attend_stats(cache.ref, _ptr(q), F32 if q.dtype == torch.float32 else BF16, hq,
+                               nq, float(sm_scale or 0.0), _ptr(sg), _ptr(out),
+                               _ptr(status) if status is not None else None, _stream()),
+           "kv_attend_stats")
+    return out
