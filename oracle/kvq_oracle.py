@@ -227,6 +227,28 @@ def candidate_attention(q, k_hat, v_hat, idx, sm_scale: float | None = None):
     return out
 
 
+def candidate_topk_select(q, k_hat, idx, top_k: int, sm_scale: float | None = None):
+    """The keys a two-stage candidate pass keeps (MiniCPM study, section 6:
+    a predictor proposes top-C candidates, then the true top-32 inside them is
+    taken by exact score): per row, the top_k listed keys by sm_scale q . k,
+    ties going to the key listed first. Returns (positions (n_q, top_k),
+    scores of every listed key (n_q, C))."""
+    q = np.asarray(q, dtype=np.float64)
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(q.shape[-1])
+    idx = np.asarray(idx, dtype=np.int64)
+    scores = np.stack([sm_scale * (k_hat[idx[i]] @ q[i]) for i in range(q.shape[0])])
+    order = np.argsort(-scores, axis=-1, kind="stable")[:, :top_k]
+    return np.take_along_axis(idx, order, axis=-1), scores
+
+
+def candidate_topk_attention(q, k_hat, v_hat, idx, top_k: int, sm_scale: float | None = None):
+    """Exact attention of each row over the top_k of its listed keys
+    (candidate_topk_select), and nothing else."""
+    keep, _ = candidate_topk_select(q, k_hat, idx, top_k, sm_scale)
+    return candidate_attention(q, k_hat, v_hat, keep, sm_scale)
+
+
 # --------------------------------------------------------------------------------------
 # Batched forms over (batch, head) in the library's tensor layout
 # --------------------------------------------------------------------------------------

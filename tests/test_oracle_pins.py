@@ -519,3 +519,38 @@ def test_attention_statistics_reference_path_ignores_the_rotation():
     for key in ("entropy", "support", "top1", "zero", "p_zero", "p_tv", "p_sum"):
         assert np.allclose(a[key], b[key])
     assert np.all(a["qk_tv"] < 0.1) and np.all(b["qk_tv"] < 0.1)
+
+
+# ------------------------------------------------------------------ exact top-k inside the candidates
+
+def test_topk_inside_candidates_reduces_to_known_cases():
+    rng = np.random.default_rng(12)
+    n, d = 300, 32
+    k, v = rng.standard_normal((n, d)), rng.standard_normal((n, d))
+    q = rng.standard_normal((3, d))
+    idx = np.stack([rng.choice(n, 40, replace=False) for _ in range(3)])
+    # keeping all C is plain candidate attention
+    assert np.allclose(O.candidate_topk_attention(q, k, v, idx, 40),
+                       O.candidate_attention(q, k, v, idx))
+    # keeping one is the value row of the best-scoring listed key (brute force)
+    best = [idx[i][np.argmax(k[idx[i]] @ q[i])] for i in range(3)]
+    assert np.allclose(O.candidate_topk_attention(q, k, v, idx, 1), v[best])
+    # the list's order does not matter
+    perm = rng.permutation(40)
+    assert np.allclose(O.candidate_topk_attention(q, k, v, idx[:, perm], 7),
+                       O.candidate_topk_attention(q, k, v, idx, 7))
+    # the kept keys are the 7 highest-scoring ones, found by brute force
+    keep, _ = O.candidate_topk_select(q, k, idx, 7)
+    for i in range(3):
+        s = {int(t): float(k[t] @ q[i]) for t in idx[i]}
+        top = sorted(s, key=lambda t: -s[t])[:7]
+        assert list(keep[i]) == top
+
+
+def test_topk_ties_go_to_the_key_listed_first():
+    k = np.zeros((6, 32))
+    k[:, 0] = [1.0, 3.0, 3.0, 2.0, 3.0, 0.0]
+    q = np.zeros((1, 32))
+    q[0, 0] = 1.0
+    keep, _ = O.candidate_topk_select(q, k, np.array([[4, 1, 2, 0]]), 2)
+    assert list(keep[0]) == [4, 1]
