@@ -322,6 +322,34 @@ def row_candidates(kvq, synth, torch, steps, warmup, pk, context, c):
             "launches": a.launches()}
 
 
+def row_candidates_topk(kvq, synth, torch, steps, warmup, pk, context, c, top_k):
+    """Two-stage candidates: exact scores of the C listed keys, attention over
+    their top_k (the pages' C -> top-32)."""
+    d = CAND
+    idx = synth.candidate_indices(5, d["batch"], d["q_heads"], context, c)
+    nbytes = candidate_unique_bytes(idx, context, d["recent"])
+    n = rotation(nbytes)
+    calls = []
+    for i in range(n):
+        q, k, v = synth.decode_inputs_torch(61 + 3 * i, d["batch"], context, "cuda")
+        cache = kvq.pack(k, v, d["recent"], "bf16")
+        del k, v
+        ti = torch.from_numpy(idx).cuda()
+        calls.append(lambda cache=cache, q=q, ti=ti:
+                     kvq.attend_candidates_topk(cache, q, ti, top_k, out_dtype="bf16"))
+    ms = time_steps(cycling(calls), steps, warmup)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"workload": f"candidate attention, exact top-{top_k} of C={c} listed keys, 32 x 16 "
+                        f"heads, L={context}, int4 + bf16 R=128",
+            "ms": ms, "keys_per_s": d["batch"] * d["q_heads"] * top_k / (ms * 1e-3),
+            "l2": l2_note(n, nbytes),
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / pk["hbm_gbs"], "traffic": None,
+                         "bytes_note": "distinct K rows of the lists once, V rows of the kept keys "
+                                       "counted as in the plain candidate row (upper bound)"},
+            "launches": 1}
+
+
 def row_decode(kvq, synth, torch, steps, warmup, pk, batch, context):
     """The decode step at another (batch, context) of the decode workload."""
     d = dict(DECODE, batch=batch, context=context)
@@ -641,6 +669,8 @@ ROWS = {
         row_candidates(kvq, synth, torch, st, w, pk, 131072, 256),
     "candidates_L32768_C96": lambda kvq, synth, torch, st, w, pk:
         row_candidates(kvq, synth, torch, st, w, pk, 32768, 96),
+    "candidates_top32_of_C256_L131072": lambda kvq, synth, torch, st, w, pk:
+        row_candidates_topk(kvq, synth, torch, st, w, pk, 131072, 256, 32),
     "chunk_bf16": lambda kvq, synth, torch, st, w, pk: row_chunk(kvq, synth, torch, st, w, pk, "bf16"),
     "chunk_mxfp8": lambda kvq, synth, torch, st, w, pk:
         row_chunk(kvq, synth, torch, st, w, pk, "mxfp8"),

@@ -253,6 +253,26 @@ KVQ_API kvq_status kv_attend_candidates(const kvq_cache *cache, const void *q, i
                                         kvq_stream_t stream);
 
 /*
+ * kv_attend_candidates_topk -- the two-stage form of candidate attention
+ * (MiniCPM5-2B study, section 6: a predictor proposes top-C candidates, then
+ * the true top-32 inside them is taken by exact score): each query row scores
+ * its n_cand listed keys exactly (sm_scale * q . k, keys as kv_attend reads
+ * them), keeps the top_k highest (equal scores: the key listed first) and
+ * attends exactly over those. q, idx, out as kv_attend_candidates; positions
+ * outside [0, N) score -inf (flagged KVQ_DEV_INDEX) and are never kept.
+ * selected: device int32 [batch][q_heads][n_q][top_k] receiving the kept
+ *   positions in score order (-1 past the valid ones), or NULL.
+ * Restrictions: 1 <= top_k <= n_cand <= 4096 (else KVQ_ERR_ARG /
+ * KVQ_ERR_UNSUPPORTED); an MXFP8 K window is not supported. No workspace.
+ */
+KVQ_API kvq_status kv_attend_candidates_topk(const kvq_cache *cache, const void *q,
+                                             int32_t q_dtype, int32_t q_heads, int32_t n_q,
+                                             const int32_t *idx, int32_t n_cand, int32_t top_k,
+                                             float sm_scale, void *out, int32_t out_dtype,
+                                             int32_t *selected, int32_t *dev_status,
+                                             kvq_stream_t stream);
+
+/*
  * kv_attend_decode_static -- the decode case of kv_attend (one query row per
  * sequence and head, 8 query heads per KV head, D = 128, bf16 or no window)
  * for callers that cannot allocate device memory: a serving runtime that has

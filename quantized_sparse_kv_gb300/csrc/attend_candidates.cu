@@ -37,6 +37,8 @@ struct CandArgs {
   void *out;
   int out_dtype;
   float scale_log2;
+  int top_k, Cp;       // exact top-k inside the list (0: attend every listed key); Cp = pow2 >= C
+  int32_t *selected;   // [rows][top_k] kept positions, or nullptr
   KernelCtl ctl;
 };
 
@@ -329,11 +331,150 @@ void launch_f(const CandArgs &a, int B, cudaStream_t s) {
   cand_kernel<F><<<grid, kWarps * 32, smem, s>>>(a);
 }
 
+// Exact top-k inside the candidates (MiniCPM study, section 6: the predictor's
+// top-C list, then the true top-32 inside it by exact score). One CTA per
+// (query row, query head, sequence): warp w scores candidates w, w + 8, ...
+// into shared memory (lane l owns features l*F ..), the (score, list
+// position) pairs are sorted by a bitonic sort (higher score first, ties to
+// the position listed first), and the first top_k keys are attended: warp w
+// takes kept keys w, w + 8, ... against the common maximum (the first sorted
+// score), and the warps' sums meet in shared memory.
+template <int F>
+__global__ void __launch_bounds__(kWarps * 32) cand_topk_kernel(const CandArgs a) {
+  constexpr int D = F * 32;
+  __shared__ float red_o[kWarps][D];
+  __shared__ float red_l[kWarps];
+  extern __shared__ float sc[];                       // [Cp] scores
+  int32_t *pos = reinterpret_cast<int32_t *>(sc + a.Cp);  // [Cp] list positions
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int i = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const long u = static_cast<long>(b) * a.Hkv + h / a.group;
+  const long row = (static_cast<long>(b) * a.Hq + h) * a.n_q + i;
+  const int32_t *cand = a.idx + row * a.C;
+  const int d0 = lane * F;
+
+  float q[F];
+#pragma unroll
+  for (int k = 0; k < F; ++k) {
+    const long gi = row * D + d0 + k;
+    q[k] = (a.q_dtype == KVQ_F32 ? static_cast<const float *>(a.q)[gi]
+                                 : bf16_to_f32(static_cast<const uint16_t *>(a.q)[gi])) *
+           a.scale_log2;
+  }
+  for (int c = a.C + threadIdx.x; c < a.Cp; c += blockDim.x) {
+    sc[c] = -CUDART_INF_F;
+    pos[c] = 0x7fffffff;
+  }
+  // scores of every listed key (an index outside [0, N) scores -inf)
+  for (int c = warp; c < a.C; c += kWarps) {
+    const int t = cand[c];
+    float s = -CUDART_INF_F;
+    if (t >= 0 && t < a.N) {
+      float part = 0.0f;
+      if (t < a.cut) {
+        const int g = t / kGroup, r = t % kGroup;
+        const uint8_t *kc = a.k_codes + ((u * a.Gs + g) * kGroup + r) * (D / 2);
+        const float *ks = a.k_scales + (u * a.Gs + g) * D;
+#pragma unroll
+        for (int k = 0; k < F; ++k) {
+          const int d = d0 + k;
+          const uint8_t kb = kc[d >> 1];
+          part = fmaf(q[k],
+                      static_cast<float>(static_cast<int>((d & 1) ? (kb >> 4) : (kb & 15)) - 8) *
+                          ks[d],
+                      part);
+        }
+      } else {
+        const long wr = u * a.Ws + (t - a.cut);
+#pragma unroll
+        for (int k = 0; k < F; ++k) part = fmaf(q[k], wval(a.k_window, a.kwin, wr * D + d0 + k), part);
+      }
+      s = warp_sum(part);
+    } else if (lane == 0) {
+      flag_error(a.ctl, KVQ_DEV_INDEX);
+    }
+    if (lane == 0) {
+      sc[c] = s;
+      pos[c] = c;
+    }
+  }
+  __syncthreads();
+  // sort: element x before y when its score is higher, or equal and listed first
+  for (int k = 2; k <= a.Cp; k <<= 1)
+    for (int jj = k >> 1; jj > 0; jj >>= 1) {
+      for (int e = threadIdx.x; e < a.Cp; e += blockDim.x) {
+        const int f = e ^ jj;
+        if (f > e) {
+          const float se = sc[e], sf = sc[f];
+          const int pe = pos[e], pf = pos[f];
+          const bool f_first = sf > se || (sf == se && pf < pe);
+          if (((e & k) == 0) == f_first) {
+            sc[e] = sf;
+            sc[f] = se;
+            pos[e] = pf;
+            pos[f] = pe;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  const int kk = min(a.top_k, a.C);
+  const float mx = sc[0];
+  float l = 0.0f, o[F];
+#pragma unroll
+  for (int k = 0; k < F; ++k) o[k] = 0.0f;
+  for (int r = warp; r < kk; r += kWarps) {
+    if (sc[r] == -CUDART_INF_F) break;  // fewer valid keys than top_k
+    const int t = cand[pos[r]];
+    const float p = exp2f(sc[r] - mx);
+    l += p;
+    if (t < a.cut) {
+      const uint8_t *vc = a.v_codes + (u * a.Vs + t) * (D / 2);
+      const float *vs = a.v_scales + (u * a.Vs + t) * (D / 32);
+#pragma unroll
+      for (int k = 0; k < F; ++k) {
+        const int d = d0 + k;
+        const uint8_t vb = vc[d >> 1];
+        o[k] = fmaf(p, static_cast<float>(static_cast<int>((d & 1) ? (vb >> 4) : (vb & 15)) - 8) *
+                           vs[d / 32], o[k]);
+      }
+    } else {
+      const long wr = u * a.Ws + (t - a.cut);
+#pragma unroll
+      for (int k = 0; k < F; ++k) o[k] = fmaf(p, wval(a.v_window, a.vwin, wr * D + d0 + k), o[k]);
+    }
+  }
+  if (lane == 0) red_l[warp] = l;
+#pragma unroll
+  for (int k = 0; k < F; ++k) red_o[warp][d0 + k] = o[k];
+  if (a.selected)
+    for (int r = threadIdx.x; r < a.top_k; r += blockDim.x)
+      a.selected[row * a.top_k + r] =
+          (r < kk && sc[r] != -CUDART_INF_F) ? cand[pos[r]] : -1;
+  __syncthreads();
+  float ls = 0.0f;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) ls += red_l[w];
+  for (int d = threadIdx.x; d < D; d += blockDim.x) {
+    float acc = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) acc += red_o[w][d];
+    const float x = acc / ls;
+    if (a.out_dtype == KVQ_F32)
+      static_cast<float *>(a.out)[row * D + d] = x;
+    else
+      static_cast<__nv_bfloat16 *>(a.out)[row * D + d] = __float2bfloat16_rn(x);
+  }
+}
+
 }  // namespace
+
+int candidates_topk_max() { return 4096; }
 
 int launch_attend_candidates(const kvq_cache &c, const void *q, int q_dtype, int Hq, int n_q,
                              const int32_t *idx, int n_cand, int validate, float scale_log2,
-                             void *out, int out_dtype, const KernelCtl &ctl, cudaStream_t s) {
+                             void *out, int out_dtype, const KernelCtl &ctl, cudaStream_t s,
+                             int top_k, int32_t *selected) {
   const CacheDims d = dims_of(c);
   CandArgs a;
   a.k_codes = c.k_codes;
@@ -364,6 +505,34 @@ int launch_attend_candidates(const kvq_cache &c, const void *q, int q_dtype, int
   a.out_dtype = out_dtype;
   a.scale_log2 = scale_log2;
   a.ctl = ctl;
+  a.top_k = top_k;
+  a.selected = selected;
+  a.Cp = 1;
+  while (a.Cp < n_cand) a.Cp <<= 1;
+  if (top_k > 0) {
+    const size_t smem = static_cast<size_t>(a.Cp) * (sizeof(float) + sizeof(int32_t));
+    const dim3 grid(n_q, Hq, d.B);
+    switch (d.D / 32) {
+#define KVQ_TOPK_CASE(F)                                                                      \
+  case F:                                                                                     \
+    cudaFuncSetAttribute(cand_topk_kernel<F>, cudaFuncAttributeMaxDynamicSharedMemorySize,   \
+                         static_cast<int>(smem));                                             \
+    cand_topk_kernel<F><<<grid, kWarps * 32, smem, s>>>(a);                                   \
+    break;
+      KVQ_TOPK_CASE(1)
+      KVQ_TOPK_CASE(2)
+      KVQ_TOPK_CASE(3)
+      KVQ_TOPK_CASE(4)
+      KVQ_TOPK_CASE(5)
+      KVQ_TOPK_CASE(6)
+      KVQ_TOPK_CASE(7)
+      KVQ_TOPK_CASE(8)
+#undef KVQ_TOPK_CASE
+      default:
+        return -1;
+    }
+    return 1;
+  }
   if (d.D == 128) {
     cand128_kernel<<<dim3(n_q, Hq, d.B), kWarps * 32, sizeof(int32_t) * n_cand, s>>>(a);
     return 1;

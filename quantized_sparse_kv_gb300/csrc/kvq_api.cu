@@ -309,6 +309,33 @@ kvq_status kv_attend_candidates(const kvq_cache *cache, const void *q, int32_t q
   return finish(n, "candidates");
 }
 
+kvq_status kv_attend_candidates_topk(const kvq_cache *cache, const void *q, int32_t q_dtype,
+                                     int32_t q_heads, int32_t n_q, const int32_t *idx,
+                                     int32_t n_cand, int32_t top_k, float sm_scale, void *out,
+                                     int32_t out_dtype, int32_t *selected, int32_t *dev_status,
+                                     kvq_stream_t stream) {
+  kvq_status st = check_cache(cache);
+  if (st != KVQ_OK) return st;
+  if (q_heads < 1 || q_heads % cache->kv_heads || n_q < 1 || n_cand < 1) return KVQ_ERR_ARG;
+  if (top_k < 1 || top_k > n_cand) return KVQ_ERR_ARG;
+  if ((q_dtype != KVQ_F32 && q_dtype != KVQ_BF16) ||
+      (out_dtype != KVQ_F32 && out_dtype != KVQ_BF16))
+    return KVQ_ERR_ARG;
+  if (!q || !out || !idx) return KVQ_ERR_ARG;
+  if (cache->recent > 0 && cache->kwin_dtype == KVQ_MXFP8) return KVQ_ERR_UNSUPPORTED;
+  if (n_cand > kvq::candidates_topk_max() || q_heads > 65535 || cache->batch > 65535)
+    return KVQ_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(out) || !aligned16(idx) || (selected && !aligned16(selected)) ||
+      (dev_status && !aligned16(dev_status)))
+    return KVQ_ERR_ALIGN;
+  const float scale = resolve_scale(sm_scale, cache->head_dim);
+  const int n = kvq::launch_attend_candidates(
+      *cache, q, q_dtype, q_heads, n_q, idx, n_cand, 0, static_cast<float>(scale * kLog2e), out,
+      out_dtype, make_ctl(dev_status), reinterpret_cast<cudaStream_t>(stream), top_k, selected);
+  if (n < 0) return KVQ_ERR_UNSUPPORTED;
+  return finish(n, "candidates_topk");
+}
+
 kvq_status kv_attend_decode_static(const kvq_cache *cache, const void *q, int32_t q_dtype,
                                    int32_t q_heads, float sm_scale, void *out,
                                    int32_t out_dtype, int32_t *dev_status, kvq_stream_t stream) {

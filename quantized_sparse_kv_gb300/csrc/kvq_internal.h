@@ -77,9 +77,13 @@ size_t decode_static_scratch_limit();
 cudaError_t decode_static_scratch(void **ptr);
 
 // attend_candidates.cu
+// top_k > 0: attend only the top_k listed keys by exact score (selected, if
+// not null, receives their positions); n_cand <= candidates_topk_max() then.
 int launch_attend_candidates(const kvq_cache &c, const void *q, int q_dtype, int Hq, int n_q,
                              const int32_t *idx, int n_cand, int validate, float scale_log2,
-                             void *out, int out_dtype, const KernelCtl &ctl, cudaStream_t s);
+                             void *out, int out_dtype, const KernelCtl &ctl, cudaStream_t s,
+                             int top_k = 0, int32_t *selected = nullptr);
+int candidates_topk_max();
 
 // attend_chunk.cu: tcgen05 chunk attention over an all-window bf16 / MXFP8 cache.
 bool chunk_supported(const kvq_cache &c, int q_dtype, int Hq, int n_q);

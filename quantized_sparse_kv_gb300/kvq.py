@@ -71,6 +71,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.kv_append.restype = i32
     lib.kv_attend_stats.argtypes = [cp, vp, i32, i32, i32, f32, vp, vp, vp, vp]
     lib.kv_attend_stats.restype = i32
+    lib.kv_attend_candidates_topk.argtypes = [cp, vp, i32, i32, i32, vp, i32, i32, f32, vp, i32,
+                                              vp, vp, vp]
+    lib.kv_attend_candidates_topk.restype = i32
     lib.kvq_cache_bytes.argtypes = [i32, i32, i32, i32, i32, i32, i32]
     lib.kvq_cache_bytes.restype = sz
     lib.kv_pack.argtypes = [vp, vp, i32, cp, vp, vp]
@@ -382,3 +385,27 @@ def attend_stats(cache: PackedCache, q: torch.Tensor, signs: torch.Tensor | None
                                _ptr(status) if status is not None else None, _stream()),
            "kv_attend_stats")
     return out
+
+
+def attend_candidates_topk(cache: PackedCache, q: torch.Tensor, idx: torch.Tensor, top_k: int,
+                           sm_scale: float = 0.0, out_dtype=None):
+    """kv_attend_candidates_topk: attend only the top_k of each row's listed
+    keys by exact score. Returns (out, selected positions, status tensor)."""
+    q = q.contiguous()
+    if q.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("q must be float32 or bfloat16")
+    idx = idx.to(torch.int32).contiguous()
+    b, hq, nq, d = q.shape
+    if tuple(idx.shape[:3]) != (b, hq, nq):
+        raise ValueError("idx must be (batch, q_heads, n_q, C)")
+    q_dt = F32 if q.dtype == torch.float32 else BF16
+    out_dt = _dtype(out_dtype) if out_dtype is not None else q_dt
+    out = torch.empty((b, hq, nq, d), dtype=TORCH_OF[out_dt], device=q.device)
+    selected = torch.empty((b, hq, nq, top_k), dtype=torch.int32, device=q.device)
+    status = new_status(q.device)
+    lib = load_library()
+    _check(lib.kv_attend_candidates_topk(cache.ref, _ptr(q), q_dt, hq, nq, _ptr(idx),
+                                         idx.shape[3], top_k, float(sm_scale or 0.0), _ptr(out),
+                                         out_dt, _ptr(selected), _ptr(status), _stream()),
+           "kv_attend_candidates_topk")
+    return out, selected, status
