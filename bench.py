@@ -350,6 +350,40 @@ def row_candidates_topk(kvq, synth, torch, steps, warmup, pk, context, c, top_k)
             "launches": 1}
 
 
+def row_candidates_block(kvq, synth, torch, steps, warmup, pk):
+    """Candidate prefill with block-shared lists: L = 4096 query rows of one
+    sequence (16 query heads over 2 KV heads, D = 128) over its own int4 +
+    bf16 R=128 cache, one list of C = 256 keys per 128-row block, against
+    dense kv_attend of the same rows on the same cache."""
+    import numpy as np
+    L, c, bq, hq = 4096, 256, 128, 16
+    q, k, v = synth.decode_inputs_torch(71, 1, L, "cuda")
+    q = synth.normal_torch(72, (1, hq, L, 128), torch.bfloat16, "cuda")
+    cache = kvq.pack(k, v, 128, "bf16")
+    del k, v
+    nb = L // bq
+    rng = np.random.default_rng(8)
+    idx = np.stack([np.stack([np.sort(rng.choice(L, c, replace=False)) for _ in range(nb)])
+                    for _ in range(hq)])[None].astype(np.int32)
+    blk = kvq.AttendCandidatesBlock(cache, q, torch.from_numpy(idx).cuda(), bq, out_dtype="bf16")
+    blk.run()
+    dense = kvq.Attend(cache, q, out_dtype="bf16")
+    dense.run()
+    ms = time_steps(blk.run, steps, warmup)
+    ms_dense = time_steps(dense.run, steps, warmup)
+    flops = 4.0 * hq * L * c * 128
+    tf = flops / (ms * 1e-3) / 1e12
+    return {"workload": "candidate prefill, block-shared lists: 4096 rows x 16 heads, one list of "
+                        "C=256 keys per 128 rows, int4 + bf16 R=128 cache of 4096 tokens",
+            "ms": ms, "keys_per_s": hq * L * c / (ms * 1e-3), "path": blk.path,
+            "dense_ms": ms_dense, "dense_path": dense.path,
+            "speedup_vs_dense": ms_dense / ms,
+            "roofline": {"bound": "tensor", "achieved": tf, "peak": pk["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": tf / pk["bf16_tflops"], "traffic": None,
+                         "note": "gather of the lists (bf16) included; 4 x rows x C x 128 flops"},
+            "launches": 2}
+
+
 def row_decode(kvq, synth, torch, steps, warmup, pk, batch, context):
     """The decode step at another (batch, context) of the decode workload."""
     d = dict(DECODE, batch=batch, context=context)
@@ -669,6 +703,8 @@ ROWS = {
         row_candidates(kvq, synth, torch, st, w, pk, 131072, 256),
     "candidates_L32768_C96": lambda kvq, synth, torch, st, w, pk:
         row_candidates(kvq, synth, torch, st, w, pk, 32768, 96),
+    "candidates_block_prefill_L4096_C256": lambda kvq, synth, torch, st, w, pk:
+        row_candidates_block(kvq, synth, torch, st, w, pk),
     "candidates_top32_of_C256_L131072": lambda kvq, synth, torch, st, w, pk:
         row_candidates_topk(kvq, synth, torch, st, w, pk, 131072, 256, 32),
     "chunk_bf16": lambda kvq, synth, torch, st, w, pk: row_chunk(kvq, synth, torch, st, w, pk, "bf16"),

@@ -273,6 +273,29 @@ KVQ_API kvq_status kv_attend_candidates_topk(const kvq_cache *cache, const void 
                                              kvq_stream_t stream);
 
 /*
+ * kv_attend_candidates_block -- candidate attention for many query rows
+ * (prefill) with one candidate list per block of block_q consecutive query
+ * rows of a head. The MiniCPM5-2B study (section 9) found its prefill kernel,
+ * which gathered a head's candidate rows again for every query block, slower
+ * than dense attention, and names the fix: a block-shared candidate layout
+ * with the rows tiled through on-chip memory. Row i of head h of sequence b
+ * attends exactly over the keys of list idx[b][h][i / block_q][0 .. n_cand).
+ * idx: device int32 [batch][q_heads][ceil(n_q / block_q)][n_cand] of distinct
+ *   positions in [0, N) (others are flagged KVQ_DEV_INDEX; such a list's rows
+ *   are then invalid). q, out as kv_attend.
+ * With D = 128, bf16 q, block_q a multiple of 128 and no MXFP8 K window,
+ * every list's K and V rows are gathered once into workspace as bf16 and the
+ * rows attend them on the tensor cores; otherwise the fp32 candidate kernel
+ * runs with the shared lists (no workspace). workspace/ws_bytes as kv_attend.
+ */
+KVQ_API kvq_status kv_attend_candidates_block(const kvq_cache *cache, const void *q,
+                                              int32_t q_dtype, int32_t q_heads, int32_t n_q,
+                                              const int32_t *idx, int32_t n_cand, int32_t block_q,
+                                              float sm_scale, void *out, int32_t out_dtype,
+                                              void *workspace, size_t *ws_bytes,
+                                              int32_t *dev_status, kvq_stream_t stream);
+
+/*
  * kv_attend_decode_static -- the decode case of kv_attend (one query row per
  * sequence and head, 8 query heads per KV head, D = 128, bf16 or no window)
  * for callers that cannot allocate device memory: a serving runtime that has

@@ -38,6 +38,7 @@ struct CandArgs {
   int out_dtype;
   float scale_log2;
   int top_k, Cp;       // exact top-k inside the list (0: attend every listed key); Cp = pow2 >= C
+  int block_q, lists_per_head;  // rows [k*block_q, (k+1)*block_q) of a head share list k
   int32_t *selected;   // [rows][top_k] kept positions, or nullptr
   KernelCtl ctl;
 };
@@ -58,7 +59,8 @@ __global__ void __launch_bounds__(kWarps * 32) cand_kernel(const CandArgs a) {
   const int i = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const long u = static_cast<long>(b) * a.Hkv + h / a.group;
   const long row = (static_cast<long>(b) * a.Hq + h) * a.n_q + i;
-  const int32_t *cand = a.idx + row * a.C;
+  const int32_t *cand =
+      a.idx + ((static_cast<long>(b) * a.Hq + h) * a.lists_per_head + i / a.block_q) * a.C;
   const int d0 = lane * F;
 
   float q[F];
@@ -170,7 +172,8 @@ __global__ void __launch_bounds__(kWarps * 32) cand128_kernel(const CandArgs a) 
   const int i = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const long u = static_cast<long>(b) * a.Hkv + h / a.group;
   const long row = (static_cast<long>(b) * a.Hq + h) * a.n_q + i;
-  const int32_t *cand = a.idx + row * a.C;
+  const int32_t *cand =
+      a.idx + ((static_cast<long>(b) * a.Hq + h) * a.lists_per_head + i / a.block_q) * a.C;
   for (int j = threadIdx.x; j < a.C; j += blockDim.x) list[j] = cand[j];
 
   float q[4];
@@ -350,7 +353,8 @@ __global__ void __launch_bounds__(kWarps * 32) cand_topk_kernel(const CandArgs a
   const int i = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const long u = static_cast<long>(b) * a.Hkv + h / a.group;
   const long row = (static_cast<long>(b) * a.Hq + h) * a.n_q + i;
-  const int32_t *cand = a.idx + row * a.C;
+  const int32_t *cand =
+      a.idx + ((static_cast<long>(b) * a.Hq + h) * a.lists_per_head + i / a.block_q) * a.C;
   const int d0 = lane * F;
 
   float q[F];
@@ -474,7 +478,7 @@ int candidates_topk_max() { return 4096; }
 int launch_attend_candidates(const kvq_cache &c, const void *q, int q_dtype, int Hq, int n_q,
                              const int32_t *idx, int n_cand, int validate, float scale_log2,
                              void *out, int out_dtype, const KernelCtl &ctl, cudaStream_t s,
-                             int top_k, int32_t *selected) {
+                             int top_k, int32_t *selected, int block_q) {
   const CacheDims d = dims_of(c);
   CandArgs a;
   a.k_codes = c.k_codes;
@@ -507,6 +511,8 @@ int launch_attend_candidates(const kvq_cache &c, const void *q, int q_dtype, int
   a.ctl = ctl;
   a.top_k = top_k;
   a.selected = selected;
+  a.block_q = block_q;
+  a.lists_per_head = (n_q + block_q - 1) / block_q;
   a.Cp = 1;
   while (a.Cp < n_cand) a.Cp <<= 1;
   if (top_k > 0) {

@@ -67,6 +67,9 @@ static_assert(sizeof(MergeState) <= kTileBytes, "merge state fits a K stage");
 
 struct ChunkArgs {
   int n_q, n_kv, q_heads, kv_group, n_tiles;
+  // block-shared candidate lists: 0, or the 128-row query tiles per list;
+  // K/V row set of CTA (x, y) is then list y * lists_per_head + x / tiles_per_list
+  int tiles_per_list, lists_per_head;
   float scale_log2;
   void *out;
   int out_dtype;
@@ -376,7 +379,9 @@ __global__ void __launch_bounds__(384, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q0 = blockIdx.x * kBM;
   const int hq = blockIdx.y;                 // b * q_heads + h
-  const int hkv = (hq / a.q_heads) * (a.q_heads / a.kv_group) + (hq % a.q_heads) / a.kv_group;
+  const int hkv = a.tiles_per_list
+                      ? hq * a.lists_per_head + static_cast<int>(blockIdx.x) / a.tiles_per_list
+                      : (hq / a.q_heads) * (a.q_heads / a.kv_group) + (hq % a.q_heads) / a.kv_group;
   const int nt = a.n_tiles;
 
   if (threadIdx.x == 0) {
@@ -831,6 +836,74 @@ __global__ void __launch_bounds__(256) history_to_bf16_kernel(const HistArgs a) 
   *reinterpret_cast<uint4 *>(a.v_out + o) = vo;
 }
 
+// ------------------------------------------------------------------ block-shared candidate lists
+// Candidate prefill with one list per block of query rows (MiniCPM study,
+// section 9: its prefill kernel re-gathered a head's candidate rows for every
+// query block and lost to dense attention; the fix it names is a
+// block-shared candidate layout with the rows tiled through on-chip memory).
+// Every list's K and V rows are gathered once, dequantized to bf16, into
+// workspace [list][C][128]; the tensor-core kernel then runs each 128-row
+// query tile against its list as if it were a cache of C tokens.
+struct ListArgs {
+  const uint8_t *k_codes;
+  const float *k_scales;
+  const uint8_t *v_codes;
+  const float *v_scales;
+  const void *k_window, *v_window;
+  int kwin, vwin;
+  const int32_t *idx;  // [lists][C]
+  uint16_t *k_out, *v_out;  // [lists][C][128] bf16
+  int N, cut, Gs, Vs, Ws, Hkv, Hq, group, lists_per_head, C;
+  KernelCtl ctl;
+};
+
+__device__ __forceinline__ float win_value(const void *w, int dt, long i) {
+  return dt == KVQ_F32 ? static_cast<const float *>(w)[i]
+                       : __uint_as_float(static_cast<uint32_t>(static_cast<const uint16_t *>(w)[i]) << 16);
+}
+
+// One thread per (listed key, 8 features) of list blockIdx.y.
+__global__ void __launch_bounds__(256) gather_lists_bf16_kernel(const ListArgs a) {
+  const int i = blockIdx.x * 256 + threadIdx.x;
+  if (i >= a.C * 16) return;
+  const long l = blockIdx.y;
+  const int c = i >> 4, q8 = i & 15;
+  const long bh = l / a.lists_per_head;  // b * Hq + h
+  const long u = (bh / a.Hq) * a.Hkv + (bh % a.Hq) / a.group;
+  const int t = a.idx[l * a.C + c];
+  float kx[8], vx[8];
+  if (t < 0 || t >= a.N) {
+    if (q8 == 0) flag_error(a.ctl, KVQ_DEV_INDEX);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) kx[e] = vx[e] = 0.0f;
+  } else if (t < a.cut) {
+    const long grp = u * a.Gs + (t >> 5);
+    const uint32_t kc =
+        *reinterpret_cast<const uint32_t *>(a.k_codes + (grp * 32 + (t & 31)) * 64 + 4 * q8);
+    const uint32_t vc = *reinterpret_cast<const uint32_t *>(a.v_codes + (u * a.Vs + t) * 64 + 4 * q8);
+    const float vs = a.v_scales[(u * a.Vs + t) * 4 + (q8 >> 2)];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      kx[e] = nib(kc, e) * a.k_scales[grp * 128 + 8 * q8 + e];
+      vx[e] = nib(vc, e) * vs;
+    }
+  } else {
+    const long w = (u * a.Ws + (t - a.cut)) * 128 + 8 * q8;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      kx[e] = win_value(a.k_window, a.kwin, w + e);
+      vx[e] = win_value(a.v_window, a.vwin, w + e);
+    }
+  }
+  const long o = (l * a.C + c) * 128 + 8 * q8;
+  *reinterpret_cast<uint4 *>(a.k_out + o) =
+      make_uint4(pack_bf16x2(kx[0], kx[1]), pack_bf16x2(kx[2], kx[3]), pack_bf16x2(kx[4], kx[5]),
+                 pack_bf16x2(kx[6], kx[7]));
+  *reinterpret_cast<uint4 *>(a.v_out + o) =
+      make_uint4(pack_bf16x2(vx[0], vx[1]), pack_bf16x2(vx[2], vx[3]), pack_bf16x2(vx[4], vx[5]),
+                 pack_bf16x2(vx[6], vx[7]));
+}
+
 // ------------------------------------------------------------------ host side
 using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
@@ -964,6 +1037,8 @@ int launch_attend_chunk(const kvq_cache &c, const void *q, int Hq, int n_q, floa
   a.mass = mass;
   a.reg = make_regions(bounds, n_regions);
   a.ctl = ctl;
+  a.tiles_per_list = 0;
+  a.lists_per_head = 0;
   static_assert(sizeof(ChunkSmem) + 1024 <= 232448, "chunk kernel shared memory");
   const size_t smem = sizeof(ChunkSmem) + 1024;
   cudaFuncSetAttribute(chunk_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -971,6 +1046,78 @@ int launch_attend_chunk(const kvq_cache &c, const void *q, int Hq, int n_q, floa
   dim3 grid((n_q + kBM - 1) / kBM, c.batch * Hq);
   chunk_bf16_kernel<<<grid, 384, smem, s>>>(tq, tk, tv, a);
   return launches;
+}
+
+// Tensor-core path of kv_attend_candidates_block: D = 128, bf16 q, lists of
+// block_q (a multiple of 128) query rows.
+bool candidate_lists_supported(const kvq_cache &c, int q_dtype, int block_q) {
+  return c.head_dim == kDim && q_dtype == KVQ_BF16 && block_q % kBM == 0 &&
+         c.kwin_dtype != KVQ_MXFP8 && encoder() != nullptr;
+}
+
+size_t candidate_lists_workspace_bytes(long lists, int C) {
+  const size_t kb = static_cast<size_t>(lists) * C * kDim * 2;
+  return 2 * ((kb + 255) & ~size_t(255));
+}
+
+int launch_candidate_lists(const kvq_cache &c, const void *q, int Hq, int n_q,
+                           const int32_t *idx, int C, int block_q, float scale_log2, void *out,
+                           int out_dtype, void *ws, const KernelCtl &ctl, cudaStream_t s) {
+  const CacheDims d = dims_of(c);
+  const int lists_per_head = (n_q + block_q - 1) / block_q;
+  const long lists = static_cast<long>(d.B) * Hq * lists_per_head;
+  const size_t kb = (static_cast<size_t>(lists) * C * kDim * 2 + 255) & ~size_t(255);
+  ListArgs g;
+  g.k_codes = c.k_codes;
+  g.k_scales = c.k_scales;
+  g.v_codes = c.v_codes;
+  g.v_scales = c.v_scales;
+  g.k_window = c.k_window;
+  g.v_window = c.v_window;
+  g.kwin = c.kwin_dtype;
+  g.vwin = c.vwin_dtype;
+  g.idx = idx;
+  g.k_out = static_cast<uint16_t *>(ws);
+  g.v_out = reinterpret_cast<uint16_t *>(static_cast<uint8_t *>(ws) + kb);
+  g.N = d.N;
+  g.cut = d.cut;
+  g.Gs = d.Gs;
+  g.Vs = d.Vs;
+  g.Ws = d.Ws;
+  g.Hkv = d.Hkv;
+  g.Hq = Hq;
+  g.group = Hq / d.Hkv;
+  g.lists_per_head = lists_per_head;
+  g.C = C;
+  g.ctl = ctl;
+  gather_lists_bf16_kernel<<<dim3(static_cast<unsigned>((C * 16 + 255) / 256),
+                                  static_cast<unsigned>(lists)),
+                             256, 0, s>>>(g);
+  CUtensorMap tq, tk, tv;
+  if (!make_map(&tq, q, n_q, d.B * Hq, n_q) ||
+      !make_map(&tk, g.k_out, C, static_cast<int>(lists), C) ||
+      !make_map(&tv, g.v_out, C, static_cast<int>(lists), C))
+    return -1;
+  ChunkArgs a;
+  a.n_q = n_q;
+  a.n_kv = C;
+  a.q_heads = Hq;
+  a.kv_group = 1;
+  a.n_tiles = (C + kBN - 1) / kBN;
+  a.scale_log2 = scale_log2;
+  a.out = out;
+  a.out_dtype = out_dtype;
+  a.mass = nullptr;
+  a.reg = make_regions(nullptr, 0);
+  a.ctl = ctl;
+  a.tiles_per_list = block_q / kBM;
+  a.lists_per_head = lists_per_head;
+  const size_t smem = sizeof(ChunkSmem) + 1024;
+  cudaFuncSetAttribute(chunk_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       static_cast<int>(smem));
+  dim3 grid((n_q + kBM - 1) / kBM, d.B * Hq);
+  chunk_bf16_kernel<<<grid, 384, smem, s>>>(tq, tk, tv, a);
+  return 2;
 }
 
 }  // namespace kvq

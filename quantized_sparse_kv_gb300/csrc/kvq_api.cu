@@ -336,6 +336,48 @@ kvq_status kv_attend_candidates_topk(const kvq_cache *cache, const void *q, int3
   return finish(n, "candidates_topk");
 }
 
+kvq_status kv_attend_candidates_block(const kvq_cache *cache, const void *q, int32_t q_dtype,
+                                      int32_t q_heads, int32_t n_q, const int32_t *idx,
+                                      int32_t n_cand, int32_t block_q, float sm_scale, void *out,
+                                      int32_t out_dtype, void *workspace, size_t *ws_bytes,
+                                      int32_t *dev_status, kvq_stream_t stream) {
+  kvq_status st = check_cache(cache);
+  if (st != KVQ_OK) return st;
+  if (!ws_bytes) return KVQ_ERR_ARG;
+  if (q_heads < 1 || q_heads % cache->kv_heads || n_q < 1 || n_cand < 1 || block_q < 1)
+    return KVQ_ERR_ARG;
+  if ((q_dtype != KVQ_F32 && q_dtype != KVQ_BF16) ||
+      (out_dtype != KVQ_F32 && out_dtype != KVQ_BF16))
+    return KVQ_ERR_ARG;
+  if (cache->recent > 0 && cache->kwin_dtype == KVQ_MXFP8) return KVQ_ERR_UNSUPPORTED;
+  if (n_cand > 65536 || q_heads > 65535 || cache->batch > 65535) return KVQ_ERR_UNSUPPORTED;
+  const long lists = static_cast<long>(cache->batch) * q_heads * ((n_q + block_q - 1) / block_q);
+  const bool tensor = kvq::candidate_lists_supported(*cache, q_dtype, block_q) && lists <= 65535;
+  const size_t need = tensor ? kvq::candidate_lists_workspace_bytes(lists, n_cand) : 0;
+  if (!workspace) {
+    *ws_bytes = need;
+    return KVQ_OK;
+  }
+  if (*ws_bytes < need) return KVQ_ERR_WORKSPACE;
+  if (!q || !out || !idx) return KVQ_ERR_ARG;
+  if (!aligned16(q) || !aligned16(out) || !aligned16(idx) || !aligned16(workspace) ||
+      (dev_status && !aligned16(dev_status)))
+    return KVQ_ERR_ALIGN;
+  const float scale = resolve_scale(sm_scale, cache->head_dim);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (tensor) {
+    const int n = kvq::launch_candidate_lists(*cache, q, q_heads, n_q, idx, n_cand, block_q,
+                                              static_cast<float>(scale * kLog2e), out, out_dtype,
+                                              workspace, make_ctl(dev_status), s);
+    if (n < 0) return KVQ_ERR_CUDA;
+    return finish(n, "candidates_block_tensor");
+  }
+  const int n = kvq::launch_attend_candidates(*cache, q, q_dtype, q_heads, n_q, idx, n_cand, 0,
+                                              static_cast<float>(scale * kLog2e), out, out_dtype,
+                                              make_ctl(dev_status), s, 0, nullptr, block_q);
+  return finish(n, "candidates_block");
+}
+
 kvq_status kv_attend_decode_static(const kvq_cache *cache, const void *q, int32_t q_dtype,
                                    int32_t q_heads, float sm_scale, void *out,
                                    int32_t out_dtype, int32_t *dev_status, kvq_stream_t stream) {

@@ -82,8 +82,16 @@ cudaError_t decode_static_scratch(void **ptr);
 int launch_attend_candidates(const kvq_cache &c, const void *q, int q_dtype, int Hq, int n_q,
                              const int32_t *idx, int n_cand, int validate, float scale_log2,
                              void *out, int out_dtype, const KernelCtl &ctl, cudaStream_t s,
-                             int top_k = 0, int32_t *selected = nullptr);
+                             int top_k = 0, int32_t *selected = nullptr, int block_q = 1);
 int candidates_topk_max();
+
+// attend_chunk.cu: kv_attend_candidates_block on the tensor cores (lists of
+// block_q query rows gathered once to bf16 in workspace).
+bool candidate_lists_supported(const kvq_cache &c, int q_dtype, int block_q);
+size_t candidate_lists_workspace_bytes(long lists, int C);
+int launch_candidate_lists(const kvq_cache &c, const void *q, int Hq, int n_q,
+                           const int32_t *idx, int C, int block_q, float scale_log2, void *out,
+                           int out_dtype, void *ws, const KernelCtl &ctl, cudaStream_t s);
 
 // attend_chunk.cu: tcgen05 chunk attention over an all-window bf16 / MXFP8 cache.
 bool chunk_supported(const kvq_cache &c, int q_dtype, int Hq, int n_q);

@@ -74,6 +74,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.kv_attend_candidates_topk.argtypes = [cp, vp, i32, i32, i32, vp, i32, i32, f32, vp, i32,
                                               vp, vp, vp]
     lib.kv_attend_candidates_topk.restype = i32
+    lib.kv_attend_candidates_block.argtypes = [cp, vp, i32, i32, i32, vp, i32, i32, f32, vp, i32,
+                                               vp, ctypes.POINTER(sz), vp, vp]
+    lib.kv_attend_candidates_block.restype = i32
     lib.kvq_cache_bytes.argtypes = [i32, i32, i32, i32, i32, i32, i32]
     lib.kvq_cache_bytes.restype = sz
     lib.kv_pack.argtypes = [vp, vp, i32, cp, vp, vp]
@@ -409,3 +412,43 @@ def attend_candidates_topk(cache: PackedCache, q: torch.Tensor, idx: torch.Tenso
                                          out_dt, _ptr(selected), _ptr(status), _stream()),
            "kv_attend_candidates_topk")
     return out, selected, status
+
+
+class AttendCandidatesBlock:
+    """A prepared kv_attend_candidates_block call: rows [k*block_q, (k+1)*block_q)
+    of a head attend over list k of idx (batch, q_heads, ceil(n_q / block_q), C)."""
+
+    def __init__(self, cache: PackedCache, q: torch.Tensor, idx: torch.Tensor, block_q: int,
+                 sm_scale: float = 0.0, out_dtype=None):
+        self.lib = load_library()
+        self.cache = cache
+        self.q = q.contiguous()
+        if self.q.dtype not in (torch.float32, torch.bfloat16):
+            raise TypeError("q must be float32 or bfloat16")
+        self.idx = idx.to(torch.int32).contiguous()
+        b, hq, nq, d = self.q.shape
+        if tuple(self.idx.shape[:3]) != (b, hq, -(-nq // block_q)):
+            raise ValueError("idx must be (batch, q_heads, ceil(n_q / block_q), C)")
+        self.block_q = block_q
+        self.q_dt = F32 if self.q.dtype == torch.float32 else BF16
+        self.out_dt = _dtype(out_dtype) if out_dtype is not None else self.q_dt
+        self.out = torch.empty((b, hq, nq, d), dtype=TORCH_OF[self.out_dt], device=self.q.device)
+        self.hq, self.nq, self.sm_scale = hq, nq, float(sm_scale or 0.0)
+        self.status = new_status(self.q.device)
+        need = ctypes.c_size_t(0)
+        self._call(None, need)
+        self.ws = torch.empty(max(int(need.value), 256), dtype=torch.uint8, device=self.q.device)
+        self.ws_bytes = ctypes.c_size_t(self.ws.numel())
+        self.path = None
+
+    def _call(self, ws, ws_bytes):
+        st = self.lib.kv_attend_candidates_block(
+            self.cache.ref, _ptr(self.q), self.q_dt, self.hq, self.nq, _ptr(self.idx),
+            self.idx.shape[3], self.block_q, self.sm_scale, _ptr(self.out), self.out_dt, ws,
+            ctypes.byref(ws_bytes), _ptr(self.status), _stream())
+        _check(st, "kv_attend_candidates_block")
+
+    def run(self) -> torch.Tensor:
+        self._call(_ptr(self.ws), self.ws_bytes)
+        self.path = self.lib.kvq_last_path().decode()
+        return self.out
