@@ -249,6 +249,26 @@ def candidate_topk_attention(q, k_hat, v_hat, idx, top_k: int, sm_scale: float |
     return candidate_attention(q, k_hat, v_hat, keep, sm_scale)
 
 
+def region_drop_keys(region_bounds, drop) -> np.ndarray:
+    """Positions of the keys outside the dropped regions (Catnip study,
+    recommended local output ablation: drop sink, drop recent, drop all
+    history, renormalise P): region r is [b_r, b_{r+1}); drop lists region
+    numbers."""
+    keep = [np.arange(region_bounds[r], region_bounds[r + 1])
+            for r in range(len(region_bounds) - 1) if r not in set(drop)]
+    return np.concatenate(keep) if keep else np.zeros(0, dtype=np.int64)
+
+
+def output_change(o, o_ref) -> tuple[np.ndarray, np.ndarray]:
+    """Per-row relative L2 ||o - o_ref|| / ||o_ref|| and cosine similarity."""
+    o = np.asarray(o, dtype=np.float64)
+    o_ref = np.asarray(o_ref, dtype=np.float64)
+    nr = np.linalg.norm(o_ref, axis=-1)
+    rel = np.linalg.norm(o - o_ref, axis=-1) / nr
+    cos = (o * o_ref).sum(-1) / (np.linalg.norm(o, axis=-1) * nr)
+    return rel, cos
+
+
 # --------------------------------------------------------------------------------------
 # Batched forms over (batch, head) in the library's tensor layout
 # --------------------------------------------------------------------------------------

@@ -554,3 +554,28 @@ def test_topk_ties_go_to_the_key_listed_first():
     q[0, 0] = 1.0
     keep, _ = O.candidate_topk_select(q, k, np.array([[4, 1, 2, 0]]), 2)
     assert list(keep[0]) == [4, 1]
+
+
+# ------------------------------------------------------------------ region-drop ablation
+
+def test_full_output_is_the_mass_weighted_mix_of_region_outputs():
+    # softmax over a union of disjoint key sets: O = sum_r mass_r * O_r, where
+    # O_r attends region r alone -- ties the dropped-region outputs to the
+    # region masses without retyping either
+    rng = np.random.default_rng(21)
+    bounds = [0, 39, 100, 160]
+    q, k, v = rng.standard_normal((4, 32)), rng.standard_normal((160, 32)), rng.standard_normal((160, 32))
+    o, _, mass = O.attention(q, k, v, region_bounds=bounds)
+    mix = np.zeros_like(o)
+    for r in range(3):
+        keep = O.region_drop_keys(bounds, [x for x in range(3) if x != r])
+        o_r = O.candidate_attention(q, k, v, np.tile(keep, (4, 1)))
+        mix += mass[:, r:r + 1] * o_r
+    assert np.allclose(mix, o)
+    # dropping nothing is dense attention; the kept positions are exact
+    assert np.array_equal(O.region_drop_keys(bounds, []), np.arange(160))
+    assert np.array_equal(O.region_drop_keys(bounds, [0, 2]), np.arange(39, 100))
+    rel, cos = O.output_change(o, o)
+    assert np.all(rel == 0) and np.allclose(cos, 1)
+    rel, cos = O.output_change(-o, o)
+    assert np.allclose(rel, 2) and np.allclose(cos, -1)
