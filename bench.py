@@ -384,6 +384,33 @@ def row_candidates_block(kvq, synth, torch, steps, warmup, pk):
             "launches": 2}
 
 
+def row_region_drop(kvq, synth, torch, steps, warmup, pk):
+    """The local output ablation on the video chunk: drop the sink region
+    (1,560 keys); time, and the median output change of every variant."""
+    c = CHUNK
+    q, k, v = synth.chunk_inputs_torch(81, "cuda", concentrated=4.0)
+    cache = kvq.pack(k, v, c["n_kv"], "bf16")
+    full = kvq.attend(cache, q, out_dtype="f32")[0]
+    change = {}
+    for name, drop in (("drop_sink", [0]), ("drop_recent", [1]), ("drop_history", [0, 1])):
+        o = kvq.AttendRegionDrop(cache, q, c["bounds"], drop, out_dtype="f32").run()
+        rel = (o - full).norm(dim=-1) / full.norm(dim=-1)
+        cos = (o * full).sum(-1) / (o.norm(dim=-1) * full.norm(dim=-1))
+        change[name] = {"median_rel_l2": float(rel.median()), "median_cosine": float(cos.median())}
+    a = kvq.AttendRegionDrop(cache, q, c["bounds"], [0], out_dtype="bf16")
+    ms = time_steps(a.run, steps, warmup)
+    kept = c["n_kv"] - c["bounds"][1]
+    flops = 4.0 * c["heads"] * c["n_q"] * kept * 128
+    tf = flops / (ms * 1e-3) / 1e12
+    return {"workload": "region-drop ablation on the video chunk (32 heads, 2340 queries, "
+                        "[1560 | 2340 | 2340] keys, concentrated rows): sink dropped",
+            "ms": ms, "output_change": change,
+            "roofline": {"bound": "tensor", "achieved": tf, "peak": pk["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": tf / pk["bf16_tflops"], "traffic": None,
+                         "note": "gather of the kept rows included"},
+            "launches": 2}
+
+
 def row_decode(kvq, synth, torch, steps, warmup, pk, batch, context):
     """The decode step at another (batch, context) of the decode workload."""
     d = dict(DECODE, batch=batch, context=context)
@@ -713,6 +740,8 @@ ROWS = {
     "chunk_int4_history": lambda kvq, synth, torch, st, w, pk:
         row_chunk(kvq, synth, torch, st, w, pk, "int4"),
     "stats_chunk_96q": lambda kvq, synth, torch, st, w, pk: row_stats(kvq, synth, torch, st, w, pk),
+    "region_drop_chunk": lambda kvq, synth, torch, st, w, pk:
+        row_region_drop(kvq, synth, torch, st, w, pk),
 }
 
 

@@ -296,6 +296,26 @@ KVQ_API kvq_status kv_attend_candidates_block(const kvq_cache *cache, const void
                                               int32_t *dev_status, kvq_stream_t stream);
 
 /*
+ * kv_attend_region_drop -- the local output ablation the Catnip study
+ * recommends ("Catnip Week 10 KV Cache Attention Study", section
+ * 当前判断与下一步优化空间: drop sink, drop recent or drop all history,
+ * renormalise P, compare the attention output): O over the keys of the regions
+ * NOT set in drop_mask only, the softmax renormalised over them.
+ * region_bounds: HOST array of n_regions + 1 increasing positions from 0 to N
+ * (n_regions <= 16); bit r of drop_mask drops region r (at least one key must
+ * remain). q, out, workspace/ws_bytes as kv_attend. The kept keys of every
+ * (sequence, KV head) are gathered once to bf16 in workspace and attended on
+ * the tensor cores: D = 128, bf16 q and no MXFP8 K window, else
+ * KVQ_ERR_UNSUPPORTED.
+ */
+KVQ_API kvq_status kv_attend_region_drop(const kvq_cache *cache, const void *q, int32_t q_dtype,
+                                         int32_t q_heads, int32_t n_q, float sm_scale,
+                                         const int32_t *region_bounds, int32_t n_regions,
+                                         uint32_t drop_mask, void *out, int32_t out_dtype,
+                                         void *workspace, size_t *ws_bytes, int32_t *dev_status,
+                                         kvq_stream_t stream);
+
+/*
  * kv_attend_decode_static -- the decode case of kv_attend (one query row per
  * sequence and head, 8 query heads per KV head, D = 128, bf16 or no window)
  * for callers that cannot allocate device memory: a serving runtime that has

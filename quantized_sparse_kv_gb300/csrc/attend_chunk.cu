@@ -851,11 +851,23 @@ struct ListArgs {
   const float *v_scales;
   const void *k_window, *v_window;
   int kwin, vwin;
-  const int32_t *idx;  // [lists][C]
+  const int32_t *idx;  // [lists][C], or nullptr: the kept ranges below, one list per unit
   uint16_t *k_out, *v_out;  // [lists][C][128] bf16
   int N, cut, Gs, Vs, Ws, Hkv, Hq, group, lists_per_head, C;
+  int n_ranges;
+  int range_lo[16], range_hi[16];  // kept key ranges, in order
   KernelCtl ctl;
 };
+
+// Position of the c-th kept key when the list is a set of key ranges.
+__device__ __forceinline__ int kept_position(const ListArgs &a, int c) {
+  for (int r = 0; r < a.n_ranges; ++r) {
+    const int len = a.range_hi[r] - a.range_lo[r];
+    if (c < len) return a.range_lo[r] + c;
+    c -= len;
+  }
+  return -1;
+}
 
 __device__ __forceinline__ float win_value(const void *w, int dt, long i) {
   return dt == KVQ_F32 ? static_cast<const float *>(w)[i]
@@ -869,8 +881,8 @@ __global__ void __launch_bounds__(256) gather_lists_bf16_kernel(const ListArgs a
   const long l = blockIdx.y;
   const int c = i >> 4, q8 = i & 15;
   const long bh = l / a.lists_per_head;  // b * Hq + h
-  const long u = (bh / a.Hq) * a.Hkv + (bh % a.Hq) / a.group;
-  const int t = a.idx[l * a.C + c];
+  const long u = a.idx ? (bh / a.Hq) * a.Hkv + (bh % a.Hq) / a.group : l;
+  const int t = a.idx ? a.idx[l * a.C + c] : kept_position(a, c);
   float kx[8], vx[8];
   if (t < 0 || t >= a.N) {
     if (q8 == 0) flag_error(a.ctl, KVQ_DEV_INDEX);
@@ -1112,6 +1124,86 @@ int launch_candidate_lists(const kvq_cache &c, const void *q, int Hq, int n_q,
   a.ctl = ctl;
   a.tiles_per_list = block_q / kBM;
   a.lists_per_head = lists_per_head;
+  const size_t smem = sizeof(ChunkSmem) + 1024;
+  cudaFuncSetAttribute(chunk_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       static_cast<int>(smem));
+  dim3 grid((n_q + kBM - 1) / kBM, d.B * Hq);
+  chunk_bf16_kernel<<<grid, 384, smem, s>>>(tq, tk, tv, a);
+  return 2;
+}
+
+// kv_attend_region_drop: every (sequence, KV head)'s keys outside the dropped
+// regions gathered once to bf16 (a list of C keys per unit), then the chunk
+// kernel over them with the usual GQA mapping.
+size_t region_drop_workspace_bytes(const kvq_cache &c, int kept) {
+  return candidate_lists_workspace_bytes(static_cast<long>(c.batch) * c.kv_heads, kept);
+}
+
+int launch_region_drop(const kvq_cache &c, const void *q, int Hq, int n_q, const int32_t *bounds,
+                       int n_regions, uint32_t drop_mask, float scale_log2, void *out,
+                       int out_dtype, void *ws, const KernelCtl &ctl, cudaStream_t s) {
+  const CacheDims d = dims_of(c);
+  const long units = static_cast<long>(d.B) * d.Hkv;
+  ListArgs g;
+  g.n_ranges = 0;
+  int C = 0;
+  for (int r = 0; r < n_regions && r < 16; ++r) {
+    if (drop_mask & (1u << r)) continue;
+    if (g.n_ranges > 0 && g.range_hi[g.n_ranges - 1] == bounds[r]) {
+      g.range_hi[g.n_ranges - 1] = bounds[r + 1];  // adjacent kept regions: one range
+    } else {
+      g.range_lo[g.n_ranges] = bounds[r];
+      g.range_hi[g.n_ranges] = bounds[r + 1];
+      ++g.n_ranges;
+    }
+    C += bounds[r + 1] - bounds[r];
+  }
+  if (C == 0) return -1;
+  const size_t kb = (static_cast<size_t>(units) * C * kDim * 2 + 255) & ~size_t(255);
+  g.k_codes = c.k_codes;
+  g.k_scales = c.k_scales;
+  g.v_codes = c.v_codes;
+  g.v_scales = c.v_scales;
+  g.k_window = c.k_window;
+  g.v_window = c.v_window;
+  g.kwin = c.kwin_dtype;
+  g.vwin = c.vwin_dtype;
+  g.idx = nullptr;
+  g.k_out = static_cast<uint16_t *>(ws);
+  g.v_out = reinterpret_cast<uint16_t *>(static_cast<uint8_t *>(ws) + kb);
+  g.N = d.N;
+  g.cut = d.cut;
+  g.Gs = d.Gs;
+  g.Vs = d.Vs;
+  g.Ws = d.Ws;
+  g.Hkv = d.Hkv;
+  g.Hq = Hq;
+  g.group = Hq / d.Hkv;
+  g.lists_per_head = 1;
+  g.C = C;
+  g.ctl = ctl;
+  gather_lists_bf16_kernel<<<dim3(static_cast<unsigned>((C * 16 + 255) / 256),
+                                  static_cast<unsigned>(units)),
+                             256, 0, s>>>(g);
+  CUtensorMap tq, tk, tv;
+  if (!make_map(&tq, q, n_q, d.B * Hq, n_q) ||
+      !make_map(&tk, g.k_out, C, static_cast<int>(units), C) ||
+      !make_map(&tv, g.v_out, C, static_cast<int>(units), C))
+    return -1;
+  ChunkArgs a;
+  a.n_q = n_q;
+  a.n_kv = C;
+  a.q_heads = Hq;
+  a.kv_group = Hq / d.Hkv;
+  a.n_tiles = (C + kBN - 1) / kBN;
+  a.scale_log2 = scale_log2;
+  a.out = out;
+  a.out_dtype = out_dtype;
+  a.mass = nullptr;
+  a.reg = make_regions(nullptr, 0);
+  a.ctl = ctl;
+  a.tiles_per_list = 0;
+  a.lists_per_head = 0;
   const size_t smem = sizeof(ChunkSmem) + 1024;
   cudaFuncSetAttribute(chunk_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        static_cast<int>(smem));

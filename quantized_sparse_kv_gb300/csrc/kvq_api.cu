@@ -378,6 +378,47 @@ kvq_status kv_attend_candidates_block(const kvq_cache *cache, const void *q, int
   return finish(n, "candidates_block");
 }
 
+kvq_status kv_attend_region_drop(const kvq_cache *cache, const void *q, int32_t q_dtype,
+                                 int32_t q_heads, int32_t n_q, float sm_scale,
+                                 const int32_t *region_bounds, int32_t n_regions,
+                                 uint32_t drop_mask, void *out, int32_t out_dtype,
+                                 void *workspace, size_t *ws_bytes, int32_t *dev_status,
+                                 kvq_stream_t stream) {
+  kvq_status st = check_cache(cache);
+  if (st != KVQ_OK) return st;
+  if (!ws_bytes || !region_bounds) return KVQ_ERR_ARG;
+  if (q_heads < 1 || q_heads % cache->kv_heads || n_q < 1) return KVQ_ERR_ARG;
+  if (n_regions < 1 || n_regions > 16) return KVQ_ERR_ARG;
+  if (region_bounds[0] != 0 || region_bounds[n_regions] != cache->n_tokens) return KVQ_ERR_ARG;
+  for (int i = 0; i < n_regions; ++i)
+    if (region_bounds[i + 1] <= region_bounds[i]) return KVQ_ERR_ARG;
+  if (out_dtype != KVQ_F32 && out_dtype != KVQ_BF16) return KVQ_ERR_ARG;
+  int kept = 0;
+  for (int r = 0; r < n_regions; ++r)
+    if (!(drop_mask & (1u << r))) kept += region_bounds[r + 1] - region_bounds[r];
+  if (kept == 0 || (drop_mask >> n_regions) != 0) return KVQ_ERR_ARG;
+  if (!kvq::candidate_lists_supported(*cache, q_dtype, 128) || q_heads > 65535 ||
+      static_cast<long>(cache->batch) * cache->kv_heads > 65535)
+    return KVQ_ERR_UNSUPPORTED;
+  const size_t need = kvq::region_drop_workspace_bytes(*cache, kept);
+  if (!workspace) {
+    *ws_bytes = need;
+    return KVQ_OK;
+  }
+  if (*ws_bytes < need) return KVQ_ERR_WORKSPACE;
+  if (!q || !out) return KVQ_ERR_ARG;
+  if (!aligned16(q) || !aligned16(out) || !aligned16(workspace) ||
+      (dev_status && !aligned16(dev_status)))
+    return KVQ_ERR_ALIGN;
+  const float scale = resolve_scale(sm_scale, cache->head_dim);
+  const int n = kvq::launch_region_drop(*cache, q, q_heads, n_q, region_bounds, n_regions,
+                                        drop_mask, static_cast<float>(scale * kLog2e), out,
+                                        out_dtype, workspace, make_ctl(dev_status),
+                                        reinterpret_cast<cudaStream_t>(stream));
+  if (n < 0) return KVQ_ERR_CUDA;
+  return finish(n, "region_drop");
+}
+
 kvq_status kv_attend_decode_static(const kvq_cache *cache, const void *q, int32_t q_dtype,
                                    int32_t q_heads, float sm_scale, void *out,
                                    int32_t out_dtype, int32_t *dev_status, kvq_stream_t stream) {

@@ -92,6 +92,11 @@ size_t candidate_lists_workspace_bytes(long lists, int C);
 int launch_candidate_lists(const kvq_cache &c, const void *q, int Hq, int n_q,
                            const int32_t *idx, int C, int block_q, float scale_log2, void *out,
                            int out_dtype, void *ws, const KernelCtl &ctl, cudaStream_t s);
+// kv_attend_region_drop (same conditions as the block lists, block_q = any).
+size_t region_drop_workspace_bytes(const kvq_cache &c, int kept);
+int launch_region_drop(const kvq_cache &c, const void *q, int Hq, int n_q, const int32_t *bounds,
+                       int n_regions, uint32_t drop_mask, float scale_log2, void *out,
+                       int out_dtype, void *ws, const KernelCtl &ctl, cudaStream_t s);
 
 // attend_chunk.cu: tcgen05 chunk attention over an all-window bf16 / MXFP8 cache.
 bool chunk_supported(const kvq_cache &c, int q_dtype, int Hq, int n_q);

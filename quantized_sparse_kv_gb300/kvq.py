@@ -77,6 +77,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.kv_attend_candidates_block.argtypes = [cp, vp, i32, i32, i32, vp, i32, i32, f32, vp, i32,
                                                vp, ctypes.POINTER(sz), vp, vp]
     lib.kv_attend_candidates_block.restype = i32
+    lib.kv_attend_region_drop.argtypes = [cp, vp, i32, i32, i32, f32, ctypes.POINTER(i32), i32,
+                                          ctypes.c_uint32, vp, i32, vp, ctypes.POINTER(sz), vp,
+                                          vp]
+    lib.kv_attend_region_drop.restype = i32
     lib.kvq_cache_bytes.argtypes = [i32, i32, i32, i32, i32, i32, i32]
     lib.kvq_cache_bytes.restype = sz
     lib.kv_pack.argtypes = [vp, vp, i32, cp, vp, vp]
@@ -451,4 +455,44 @@ class AttendCandidatesBlock:
     def run(self) -> torch.Tensor:
         self._call(_ptr(self.ws), self.ws_bytes)
         self.path = self.lib.kvq_last_path().decode()
+        return self.out
+
+
+class AttendRegionDrop:
+    """A prepared kv_attend_region_drop call: attention over the keys of the
+    regions not listed in ``drop`` (region r = [bounds[r], bounds[r + 1]))."""
+
+    def __init__(self, cache: PackedCache, q: torch.Tensor, region_bounds, drop,
+                 sm_scale: float = 0.0, out_dtype=None):
+        self.lib = load_library()
+        self.cache = cache
+        self.q = q.contiguous()
+        if self.q.dtype not in (torch.float32, torch.bfloat16):
+            raise TypeError("q must be float32 or bfloat16")
+        rb = [int(x) for x in region_bounds]
+        self.n_regions = len(rb) - 1
+        self.bounds = (ctypes.c_int32 * len(rb))(*rb)
+        self.mask = 0
+        for r in drop:
+            self.mask |= 1 << int(r)
+        b, hq, nq, d = self.q.shape
+        self.q_dt = F32 if self.q.dtype == torch.float32 else BF16
+        self.out_dt = _dtype(out_dtype) if out_dtype is not None else self.q_dt
+        self.out = torch.empty((b, hq, nq, d), dtype=TORCH_OF[self.out_dt], device=self.q.device)
+        self.hq, self.nq, self.sm_scale = hq, nq, float(sm_scale or 0.0)
+        self.status = new_status(self.q.device)
+        need = ctypes.c_size_t(0)
+        self._call(None, need)
+        self.ws = torch.empty(max(int(need.value), 256), dtype=torch.uint8, device=self.q.device)
+        self.ws_bytes = ctypes.c_size_t(self.ws.numel())
+
+    def _call(self, ws, ws_bytes):
+        st = self.lib.kv_attend_region_drop(
+            self.cache.ref, _ptr(self.q), self.q_dt, self.hq, self.nq, self.sm_scale, self.bounds,
+            self.n_regions, self.mask, _ptr(self.out), self.out_dt, ws, ctypes.byref(ws_bytes),
+            _ptr(self.status), _stream())
+        _check(st, "kv_attend_region_drop")
+
+    def run(self) -> torch.Tensor:
+        self._call(_ptr(self.ws), self.ws_bytes)
         return self.out
