@@ -487,11 +487,13 @@ def row_stats(kvq, synth, torch, steps, warmup, pk):
     peak = 152 * 128 * 2 * 2.07e9 / 1e12                  # fp32 FMA issue rate at 2.07 GHz
     tf = flops / (ms * 1e-3) / 1e12
     return {"workload": "kv_attend_stats: 32 heads x 96 sampled queries over 6240 bf16 keys, "
-                        "signed-H128 MXFP8 Q/K path, MXFP8 P path, top-k by sort",
+                        "signed-H128 MXFP8 Q/K path, MXFP8 P path, top-k by radix select",
             "ms": ms, "rows_per_s": rows / (ms * 1e-3),
             "roofline": {"bound": "alu", "achieved": tf, "peak": peak, "unit": "TFLOP/s",
                          "frac": tf / peak, "traffic": None,
-                         "peak_note": "fp32 FMA: 152 SMs x 128 lanes x 2 flop x 2.07 GHz"},
+                         "peak_note": "fp32 FMA: 152 SMs x 128 lanes x 2 flop x 2.07 GHz",
+                         "note": "each query row re-reads its head's two fp32 key copies "
+                                 "(6.4 MB) from L2: bound by L2 traffic, not the ALUs"},
             "launches": 1}
 
 

@@ -227,13 +227,15 @@ enum {
  * q: [batch][q_heads][n_q][D] in q_dtype (F32 or BF16), device; typically a
  *   sample of query rows. hadamard_signs: device float [D] of +-1, or NULL.
  * stats: device float [batch][q_heads][n_q][KVQ_N_STATS], see KVQ_STAT_*.
+ * workspace/ws_bytes as kv_attend (it holds every key twice in fp32: as
+ * attention reads it and on the MXFP8 Q/K path).
  * Restrictions (else KVQ_ERR_UNSUPPORTED): D in {32, 64, 128, 256},
- * N <= 16384. No workspace is needed.
+ * N <= 16384.
  */
 KVQ_API kvq_status kv_attend_stats(const kvq_cache *cache, const void *q, int32_t q_dtype,
                                    int32_t q_heads, int32_t n_q, float sm_scale,
-                                   const float *hadamard_signs, float *stats,
-                                   int32_t *dev_status, kvq_stream_t stream);
+                                   const float *hadamard_signs, float *stats, void *workspace,
+                                   size_t *ws_bytes, int32_t *dev_status, kvq_stream_t stream);
 
 /*
  * kv_attend_candidates -- exact attention of each query row over its own

@@ -15,12 +15,17 @@
 //     E4M3 with one E8M0 scale per 32 along D; the total variation between its
 //     softmax and p, and whether both rows have the same argmax.
 //
-// One CTA (8 warps) per query row. Scores: warp w takes keys w, w + 8, ...;
-// lane l holds features l*E .. l*E + E - 1 (E = D / 32) of the key, dequantized
-// as the attention kernels read it, and the Hadamard transform runs as E-wide
-// in-thread butterflies followed by five lane-exchange stages. Both score rows
-// stay in shared memory; the statistics are block reductions over them, and
-// the top-k masses come from a bitonic sort of p (padded to a power of two).
+// Two kernels. keys_kernel writes, once per (sequence, KV head), every key
+// twice to workspace in fp32: as attention reads it (int4 part dequantized,
+// window as stored) and on the MXFP8 Q/K path (rotated, rounded); warp per
+// key, lane l holding features l*E .. l*E + E - 1 (E = D / 32), the Hadamard
+// transform as E-wide in-thread butterflies followed by five lane-exchange
+// stages. stats_kernel: one CTA (8 warps) per query row; warp w scores keys
+// w, w + 8, ... on both paths from the workspace rows (whole rows per load,
+// shuffle reductions); both score rows stay in shared memory, the statistics
+// are block reductions over them, and each top-k mass takes the k-th largest
+// probability from a radix select over the float bits.
+
 #include <cuda_fp8.h>
 #include <math_constants.h>
 
@@ -38,14 +43,17 @@ struct StatsArgs {
   const void *k_window;
   const uint8_t *k_e8m0;
   int kwin;
-  int Hkv, N, D, cut, Gs, Ws, Np;
+  int Hkv, N, D, cut, Gs, Ws;
   int Hq, group, n_q;
   const void *q;
   int q_dtype;
   float sm_scale;
   const float *signs;  // [D] +-1, or nullptr: no rotation
   float *stats;        // [rows][KVQ_N_STATS]
+  float *k_ref;        // workspace [units][N][D]: keys as attention reads them
+  float *k_mx;         // workspace [units][N][D]: keys on the MXFP8 Q/K path
 };
+
 
 __device__ __forceinline__ float key_value(const StatsArgs &a, long u, int j, int d) {
   if (j < a.cut) {
@@ -114,6 +122,26 @@ __device__ __forceinline__ void mxfp8_round_row(float (&x)[E]) {
   }
 }
 
+// Both workspace copies of key blockIdx.x * 8 + warp of unit blockIdx.y.
+template <int E>
+__global__ void __launch_bounds__(kThreads) keys_kernel(const StatsArgs a) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int j = blockIdx.x * kWarps + warp;
+  if (j >= a.N) return;
+  const long u = blockIdx.y;
+  const long o = (u * a.N + j) * a.D + lane * E;
+  float x[E];
+#pragma unroll
+  for (int t = 0; t < E; ++t) {
+    x[t] = key_value(a, u, j, lane * E + t);
+    a.k_ref[o + t] = x[t];
+  }
+  if (a.signs) signed_hadamard<E>(x, a.signs, lane);
+  mxfp8_round_row<E>(x);
+#pragma unroll
+  for (int t = 0; t < E; ++t) a.k_mx[o + t] = x[t];
+}
+
 __device__ __forceinline__ float block_sum(float x, float *red) {
   x = warp_sum(x);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -173,13 +201,49 @@ __device__ __forceinline__ int block_argmax(const float *s, int n, float *red, i
   return bi;
 }
 
+// Bits of the k-th largest of x[0, n) (all x >= 0, 1 <= k <= n): four rounds
+// of a 256-bucket histogram over the next 8 bits of the keys that still
+// match the chosen prefix.
+__device__ uint32_t kth_largest_bits(const float *x, int n, int k, uint32_t *hist,
+                                     uint32_t *sel) {
+  uint32_t prefix = 0u, mask = 0u;
+#pragma unroll 1
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int i = threadIdx.x; i < 256; i += kThreads) hist[i] = 0u;
+    __syncthreads();
+    for (int i = threadIdx.x; i < n; i += kThreads) {
+      const uint32_t b = __float_as_uint(x[i]);
+      if ((b & mask) == prefix) atomicAdd(&hist[(b >> shift) & 255u], 1u);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      uint32_t cum = 0u, d = 255u;
+      for (;; --d) {
+        if (cum + hist[d] >= static_cast<uint32_t>(k) || d == 0u) break;
+        cum += hist[d];
+      }
+      sel[0] = d;
+      sel[1] = static_cast<uint32_t>(k) - cum;
+    }
+    __syncthreads();
+    prefix |= sel[0] << shift;
+    mask |= 255u << shift;
+    k = static_cast<int>(sel[1]);
+    __syncthreads();
+  }
+  return prefix;
+}
+
 template <int E>
 __global__ void __launch_bounds__(kThreads) stats_kernel(const StatsArgs a) {
   extern __shared__ float sm[];
-  float *s_ref = sm;                 // [Np]: scores, then p, then p sorted
-  float *s_mx = sm + a.Np;           // [Np]: scores of the MXFP8 Q/K path
-  __shared__ float qf[256], qm[256], red[kWarps];
+  float *s_ref = sm;                 // [N]: scores, then p
+  float *s_mx = sm + a.N;            // [N]: scores of the MXFP8 Q/K path
+  __shared__ __align__(16) float qf[256];
+  __shared__ __align__(16) float qm[256];
+  __shared__ float red[kWarps];
   __shared__ int redi[kWarps];
+  __shared__ uint32_t hist[256], sel[2];
   const long row = blockIdx.x;       // (b * Hq + h) * n_q + i
   const long bh = row / a.n_q;
   const int h = static_cast<int>(bh % a.Hq);
@@ -202,26 +266,42 @@ __global__ void __launch_bounds__(kThreads) stats_kernel(const StatsArgs a) {
   }
   __syncthreads();
 
-  // scores of both paths, one key per warp at a time
-  for (int j = warp; j < a.N; j += kWarps) {
-    float x[E];
-    float dot = 0.0f;
+  // scores of both paths: warp w takes keys w, w + 8, ..., two at a time;
+  // lane l reads features l*E .. l*E + E - 1 of each (whole rows per load)
+  float qa[E], qb[E];
 #pragma unroll
-    for (int t = 0; t < E; ++t) {
-      x[t] = key_value(a, u, j, lane * E + t);
-      dot = fmaf(qf[lane * E + t], x[t], dot);
-    }
-    if (a.signs) signed_hadamard<E>(x, a.signs, lane);
-    mxfp8_round_row<E>(x);
-    float dm = 0.0f;
+  for (int t = 0; t < E; ++t) {
+    qa[t] = qf[lane * E + t];
+    qb[t] = qm[lane * E + t];
+  }
+  for (int j0 = 2 * warp; j0 < a.N; j0 += 2 * kWarps) {
+    float dr[2], dm[2];
 #pragma unroll
-    for (int t = 0; t < E; ++t) dm = fmaf(qm[lane * E + t], x[t], dm);
-    dot = warp_sum(dot);
-    dm = warp_sum(dm);
-    if (lane == 0) {
-      s_ref[j] = a.sm_scale * dot;
-      s_mx[j] = a.sm_scale * dm;
+    for (int x = 0; x < 2; ++x) {
+      const int j = min(j0 + x, a.N - 1);
+      const float *kr = a.k_ref + (u * a.N + j) * D + lane * E;
+      const float *km = a.k_mx + (u * a.N + j) * D + lane * E;
+      dr[x] = dm[x] = 0.0f;
+#pragma unroll
+      for (int t = 0; t < E; ++t) {
+        dr[x] = fmaf(qa[t], __ldg(kr + t), dr[x]);
+        dm[x] = fmaf(qb[t], __ldg(km + t), dm[x]);
+      }
     }
+#pragma unroll
+    for (int o = 16; o; o >>= 1)
+#pragma unroll
+      for (int x = 0; x < 2; ++x) {
+        dr[x] += __shfl_xor_sync(0xffffffffu, dr[x], o);
+        dm[x] += __shfl_xor_sync(0xffffffffu, dm[x], o);
+      }
+    if (lane == 0)
+#pragma unroll
+      for (int x = 0; x < 2; ++x)
+        if (j0 + x < a.N) {
+          s_ref[j0 + x] = a.sm_scale * dr[x];
+          s_mx[j0 + x] = a.sm_scale * dm[x];
+        }
   }
   __syncthreads();
 
@@ -269,34 +349,27 @@ __global__ void __launch_bounds__(kThreads) stats_kernel(const StatsArgs a) {
   p_tv = block_sum(p_tv, red);
   p_sum = block_sum(p_sum, red);
 
-  // top-k masses: p sorted ascending (padding -1 goes first), sum the last k
-  for (int j = a.N + threadIdx.x; j < a.Np; j += kThreads) s_ref[j] = -1.0f;
-  __syncthreads();
-  for (int k = 2; k <= a.Np; k <<= 1)
-    for (int jj = k >> 1; jj > 0; jj >>= 1) {
-      for (int i = threadIdx.x; i < a.Np; i += kThreads) {
-        const int ixj = i ^ jj;
-        if (ixj > i) {
-          const float x = s_ref[i], y = s_ref[ixj];
-          if (((i & k) == 0) ? (x > y) : (x < y)) {
-            s_ref[i] = y;
-            s_ref[ixj] = x;
-          }
-        }
+  // top-k masses: the k-th largest probability t by a radix select on the
+  // float bits (monotone for p >= 0), then mass = sum(p > t) + (k - #(p > t)) t
+  const int kk[3] = {(a.N + 99) / 100, (a.N * 5 + 99) / 100, (a.N * 10 + 99) / 100};
+  float top[3];
+#pragma unroll 1
+  for (int which = 0; which < 3; ++which) {
+    const uint32_t t = kth_largest_bits(s_ref, a.N, kk[which], hist, sel);
+    const float tv = __uint_as_float(t);
+    float sum = 0.0f, cnt = 0.0f;
+    for (int j = threadIdx.x; j < a.N; j += kThreads) {
+      const float p = s_ref[j];
+      if (__float_as_uint(p) > t) {
+        sum += p;
+        cnt += 1.0f;
       }
-      __syncthreads();
     }
-  const int k1 = (a.N + 99) / 100, k5 = (a.N * 5 + 99) / 100, k10 = (a.N * 10 + 99) / 100;
-  float t1 = 0.0f, t5 = 0.0f, t10 = 0.0f;
-  for (int r = threadIdx.x; r < k10; r += kThreads) {
-    const float p = s_ref[a.Np - 1 - r];
-    t10 += p;
-    t5 += r < k5 ? p : 0.0f;
-    t1 += r < k1 ? p : 0.0f;
+    sum = block_sum(sum, red);
+    cnt = block_sum(cnt, red);
+    top[which] = sum + (static_cast<float>(kk[which]) - cnt) * tv;
   }
-  t1 = block_sum(t1, red);
-  t5 = block_sum(t5, red);
-  t10 = block_sum(t10, red);
+  const float t1 = top[0], t5 = top[1], t10 = top[2];
 
   if (threadIdx.x == 0) {
     float *o = a.stats + row * KVQ_N_STATS;
@@ -315,18 +388,20 @@ __global__ void __launch_bounds__(kThreads) stats_kernel(const StatsArgs a) {
   }
 }
 
-int pow2_at_least(int n) {
-  int p = 1;
-  while (p < n) p <<= 1;
-  return p;
-}
 
 }  // namespace
 
 int stats_max_tokens() { return 16384; }
 
+size_t stats_workspace_bytes(const kvq_cache &c) {
+  const size_t one = sizeof(float) * static_cast<size_t>(c.batch) * c.kv_heads * c.n_tokens *
+                     c.head_dim;
+  return 2 * ((one + 255) & ~size_t(255));
+}
+
 int launch_attend_stats(const kvq_cache &c, const void *q, int q_dtype, int Hq, int n_q,
-                        float sm_scale, const float *signs, float *stats, cudaStream_t s) {
+                        float sm_scale, const float *signs, float *stats, void *ws,
+                        cudaStream_t s) {
   const CacheDims d = dims_of(c);
   StatsArgs a;
   a.k_codes = c.k_codes;
@@ -340,7 +415,6 @@ int launch_attend_stats(const kvq_cache &c, const void *q, int q_dtype, int Hq, 
   a.cut = d.cut;
   a.Gs = d.Gs;
   a.Ws = d.Ws;
-  a.Np = pow2_at_least(d.N);
   a.Hq = Hq;
   a.group = Hq / d.Hkv;
   a.n_q = n_q;
@@ -349,12 +423,19 @@ int launch_attend_stats(const kvq_cache &c, const void *q, int q_dtype, int Hq, 
   a.sm_scale = sm_scale;
   a.signs = signs;
   a.stats = stats;
-  const size_t smem = sizeof(float) * 2 * static_cast<size_t>(a.Np);
+  const size_t one = (sizeof(float) * static_cast<size_t>(d.B) * d.Hkv * d.N * d.D + 255) &
+                     ~size_t(255);
+  a.k_ref = static_cast<float *>(ws);
+  a.k_mx = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + one);
+  const dim3 kgrid(static_cast<unsigned>((d.N + kWarps - 1) / kWarps),
+                   static_cast<unsigned>(d.B * d.Hkv));
+  const size_t smem = sizeof(float) * 2 * static_cast<size_t>(d.N);
   const long rows = static_cast<long>(d.B) * Hq * n_q;
   const dim3 grid(static_cast<unsigned>(rows));
   switch (d.D / 32) {
 #define KVQ_STATS_CASE(E)                                                                     \
   case E:                                                                                     \
+    keys_kernel<E><<<kgrid, kThreads, 0, s>>>(a);                                             \
     cudaFuncSetAttribute(stats_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize,       \
                          static_cast<int>(smem));                                             \
     stats_kernel<E><<<grid, kThreads, smem, s>>>(a);                                          \
@@ -367,7 +448,7 @@ int launch_attend_stats(const kvq_cache &c, const void *q, int q_dtype, int Hq, 
     default:
       return -1;
   }
-  return 1;
+  return 2;
 }
 
 }  // namespace kvq

@@ -259,22 +259,29 @@ kvq_status kv_attend(const kvq_cache *cache, const void *q, int32_t q_dtype, int
 
 kvq_status kv_attend_stats(const kvq_cache *cache, const void *q, int32_t q_dtype,
                            int32_t q_heads, int32_t n_q, float sm_scale,
-                           const float *hadamard_signs, float *stats, int32_t *dev_status,
-                           kvq_stream_t stream) {
+                           const float *hadamard_signs, float *stats, void *workspace,
+                           size_t *ws_bytes, int32_t *dev_status, kvq_stream_t stream) {
   const kvq_status st = check_cache(cache);
   if (st != KVQ_OK) return st;
+  if (!ws_bytes) return KVQ_ERR_ARG;
   if (q_heads < 1 || q_heads % cache->kv_heads || n_q < 1) return KVQ_ERR_ARG;
   if (q_dtype != KVQ_F32 && q_dtype != KVQ_BF16) return KVQ_ERR_ARG;
-  if (!q || !stats) return KVQ_ERR_ARG;
   const int d = cache->head_dim;
   if ((d & (d - 1)) != 0 || cache->n_tokens > kvq::stats_max_tokens()) return KVQ_ERR_UNSUPPORTED;
   if (static_cast<long>(cache->batch) * q_heads * n_q > 0x7fffffffL) return KVQ_ERR_UNSUPPORTED;
-  if (!aligned16(q) || !aligned16(stats) || (hadamard_signs && !aligned16(hadamard_signs)) ||
-      (dev_status && !aligned16(dev_status)))
+  const size_t need = kvq::stats_workspace_bytes(*cache);
+  if (!workspace) {
+    *ws_bytes = need;
+    return KVQ_OK;
+  }
+  if (*ws_bytes < need) return KVQ_ERR_WORKSPACE;
+  if (!q || !stats) return KVQ_ERR_ARG;
+  if (!aligned16(q) || !aligned16(stats) || !aligned16(workspace) ||
+      (hadamard_signs && !aligned16(hadamard_signs)) || (dev_status && !aligned16(dev_status)))
     return KVQ_ERR_ALIGN;
   const float scale = resolve_scale(sm_scale, d);
   const int n = kvq::launch_attend_stats(*cache, q, q_dtype, q_heads, n_q, scale, hadamard_signs,
-                                         stats, reinterpret_cast<cudaStream_t>(stream));
+                                         stats, workspace, reinterpret_cast<cudaStream_t>(stream));
   if (n < 0) return KVQ_ERR_UNSUPPORTED;
   return finish(n, "stats");
 }

@@ -69,7 +69,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.kvq_cache_sizes_reserved.restype = i32
     lib.kv_append.argtypes = [cp, vp, vp, i32, i32, i32, vp, vp]
     lib.kv_append.restype = i32
-    lib.kv_attend_stats.argtypes = [cp, vp, i32, i32, i32, f32, vp, vp, vp, vp]
+    lib.kv_attend_stats.argtypes = [cp, vp, i32, i32, i32, f32, vp, vp, vp, ctypes.POINTER(sz),
+                                    vp, vp]
     lib.kv_attend_stats.restype = i32
     lib.kv_attend_candidates_topk.argtypes = [cp, vp, i32, i32, i32, vp, i32, i32, f32, vp, i32,
                                               vp, vp, vp]
@@ -387,8 +388,15 @@ def attend_stats(cache: PackedCache, q: torch.Tensor, signs: torch.Tensor | None
         if sg.shape != (d,):
             raise ValueError("signs must have head_dim entries")
     lib = load_library()
-    _check(lib.kv_attend_stats(cache.ref, _ptr(q), F32 if q.dtype == torch.float32 else BF16, hq,
-                               nq, float(sm_scale or 0.0), _ptr(sg), _ptr(out),
+    q_dt = F32 if q.dtype == torch.float32 else BF16
+    need = ctypes.c_size_t(0)
+    _check(lib.kv_attend_stats(cache.ref, _ptr(q), q_dt, hq, nq, float(sm_scale or 0.0), _ptr(sg),
+                               _ptr(out), None, ctypes.byref(need), None, _stream()),
+           "kv_attend_stats")
+    ws = torch.empty(max(int(need.value), 256), dtype=torch.uint8, device=q.device)
+    ws_bytes = ctypes.c_size_t(ws.numel())
+    _check(lib.kv_attend_stats(cache.ref, _ptr(q), q_dt, hq, nq, float(sm_scale or 0.0), _ptr(sg),
+                               _ptr(out), _ptr(ws), ctypes.byref(ws_bytes),
                                _ptr(status) if status is not None else None, _stream()),
            "kv_attend_stats")
     return out
