@@ -1,0 +1,77 @@
+"""Argument rules of the newer entry points (observer statistics, top-k and
+block-shared candidates, region drop), checked on the host: every case here
+returns before anything is enqueued, so no GPU is needed and nothing runs on
+the placeholder addresses."""
+import ctypes
+
+import pytest
+
+
+@pytest.fixture(scope="module")
+def k():
+    import os
+    from quantized_sparse_kv_gb300 import build, kvq
+    if not os.path.exists(kvq.LIB_PATH):
+        build.build()
+    kvq.load_library()
+    return kvq
+
+
+ADDR = ctypes.c_void_p(1 << 20)   # 16-byte aligned placeholder, never dereferenced
+
+
+def cache(k, n=256, d=128, recent=256, kwin=1, hkv=2, b=1):
+    return k.KvqCacheStruct(b, hkv, n, d, recent, kwin, 1, ADDR, ADDR, ADDR, ADDR, ADDR, ADDR, ADDR,
+                            (ctypes.c_uint32 * 4)(0, 0, 0, 0), 0, 0)
+
+
+def test_stats_rules(k):
+    lib = k.load_library()
+    sz = ctypes.c_size_t(0)
+    c = cache(k)
+    # the workspace query answers with two fp32 copies of every key
+    assert lib.kv_attend_stats(ctypes.byref(c), ADDR, 1, 4, 8, 0.0, None, ADDR, None,
+                               ctypes.byref(sz), None, None) == 0
+    assert sz.value >= 2 * 2 * 256 * 128 * 4
+    c96 = cache(k, d=96)
+    assert lib.kv_attend_stats(ctypes.byref(c96), ADDR, 1, 4, 8, 0.0, None, ADDR, None,
+                               ctypes.byref(sz), None, None) == 3       # D not a power of two
+    big = cache(k, n=20000, recent=20000)
+    assert lib.kv_attend_stats(ctypes.byref(big), ADDR, 1, 4, 8, 0.0, None, ADDR, None,
+                               ctypes.byref(sz), None, None) == 3       # N > 16384
+    assert lib.kv_attend_stats(ctypes.byref(c), ADDR, 1, 3, 8, 0.0, None, ADDR, None,
+                               ctypes.byref(sz), None, None) == 1       # 3 q-heads over 2
+    small = ctypes.c_size_t(16)
+    assert lib.kv_attend_stats(ctypes.byref(c), ADDR, 1, 4, 8, 0.0, None, ADDR, ADDR,
+                               ctypes.byref(small), None, None) == 4    # workspace too small
+
+
+def test_topk_rules(k):
+    lib = k.load_library()
+    c = cache(k, recent=128)
+    call = lambda cc, C, top: lib.kv_attend_candidates_topk(  # noqa: E731
+        ctypes.byref(cc), ADDR, 1, 16, 1, ADDR, C, top, 0.0, ADDR, 1, None, None, None)
+    assert call(c, 64, 0) == 1           # top_k < 1
+    assert call(c, 64, 65) == 1          # top_k > C
+    assert call(c, 5000, 32) == 3        # C beyond the sort's 4,096
+    mx = cache(k, recent=128, kwin=2)
+    assert call(mx, 64, 32) == 3         # MXFP8 K window
+
+
+def test_block_and_region_drop_rules(k):
+    lib = k.load_library()
+    c = cache(k)
+    sz = ctypes.c_size_t(0)
+    assert lib.kv_attend_candidates_block(ctypes.byref(c), ADDR, 1, 4, 300, ADDR, 64, 0, 0.0,
+                                          ADDR, 1, None, ctypes.byref(sz), None, None) == 1
+    bounds = (ctypes.c_int32 * 4)(0, 60, 200, 256)
+    drop = lambda mask, b=bounds, n=3: lib.kv_attend_region_drop(  # noqa: E731
+        ctypes.byref(c), ADDR, 1, 4, 300, 0.0, b, n, mask, ADDR, 1, None, ctypes.byref(sz), None,
+        None)
+    assert drop(0b111) == 1              # nothing left
+    assert drop(0b1000) == 1             # a region that does not exist
+    bad = (ctypes.c_int32 * 4)(0, 60, 200, 250)
+    assert drop(0b001, bad) == 1         # bounds must end at N
+    d64 = cache(k, d=64)
+    assert lib.kv_attend_region_drop(ctypes.byref(d64), ADDR, 1, 4, 300, 0.0, bounds, 3, 1, ADDR,
+                                     1, None, ctypes.byref(sz), None, None) == 3
