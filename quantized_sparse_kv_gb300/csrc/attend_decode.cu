@@ -459,6 +459,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const Deco
     fence_mbar_init();
   }
   __syncthreads();
+  // This grid is itself a programmatic dependent launch: it may be placed
+  // while the previous kernel on the stream drains (for instance the last
+  // call's combine, which reads the partial slots this grid rewrites, or a
+  // kv_pack writing the cache), so nothing in global memory is touched before
+  // that kernel has completed and its writes are visible.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   if (warp == kConsumers) {
     // ---------------- loader: one lane walks the CTA's items in order
@@ -720,17 +726,24 @@ int launch_attend_decode(const kvq_cache &c, const void *q, int q_dtype, float s
   const size_t smem = sizeof(DecodeSmem);
   cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        static_cast<int>(smem));
-  decode_kernel<<<p.num_ctas, kThreads, smem, s>>>(a);
-  // The combine kernel is a programmatic dependent launch: its blocks may be
-  // placed while the decode grid drains and wait for it on the device.
+  // Both kernels are programmatic dependent launches: the blocks of each may
+  // be placed while the kernel before it drains, and wait for it on the device.
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t dcfg = {};
+  dcfg.gridDim = dim3(static_cast<unsigned>(p.num_ctas));
+  dcfg.blockDim = dim3(kThreads);
+  dcfg.dynamicSmemBytes = smem;
+  dcfg.stream = s;
+  dcfg.attrs = attr;
+  dcfg.numAttrs = 1;
+  cudaLaunchKernelEx(&dcfg, decode_kernel, a);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(p.units));
   cfg.blockDim = dim3(kHeads * 32);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (out_dtype == KVQ_F32)
