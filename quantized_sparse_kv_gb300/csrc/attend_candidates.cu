@@ -50,6 +50,8 @@ __device__ __forceinline__ float wval(const void *w, int dtype, long i) {
 
 template <int F>
 __global__ void __launch_bounds__(kWarps * 32) cand_kernel(const CandArgs a) {
+  wait_prior_grid();
+  allow_next_grid();
   constexpr int D = F * 32;
   __shared__ float red_o[kWarps][D];
   __shared__ float red_m[kWarps], red_l[kWarps];
@@ -163,6 +165,8 @@ __global__ void __launch_bounds__(kWarps * 32) cand_kernel(const CandArgs a) {
 constexpr int kUnroll = 4;
 
 __global__ void __launch_bounds__(kWarps * 32) cand128_kernel(const CandArgs a) {
+  wait_prior_grid();
+  allow_next_grid();
   constexpr int D = 128;
   __shared__ float red_o[kWarps][D];
   __shared__ float red_m[kWarps], red_l[kWarps];
@@ -331,7 +335,7 @@ template <int F>
 void launch_f(const CandArgs &a, int B, cudaStream_t s) {
   dim3 grid(a.n_q, a.Hq, B);
   const size_t smem = a.validate ? sizeof(int32_t) * a.C : 0;
-  cand_kernel<F><<<grid, kWarps * 32, smem, s>>>(a);
+  launch_dependent(cand_kernel<F>, grid, dim3(kWarps * 32), smem, s, a);
 }
 
 // Exact top-k inside the candidates (MiniCPM study, section 6: the predictor's
@@ -344,6 +348,8 @@ void launch_f(const CandArgs &a, int B, cudaStream_t s) {
 // score), and the warps' sums meet in shared memory.
 template <int F>
 __global__ void __launch_bounds__(kWarps * 32) cand_topk_kernel(const CandArgs a) {
+  wait_prior_grid();
+  allow_next_grid();
   constexpr int D = F * 32;
   __shared__ float red_o[kWarps][D];
   __shared__ float red_l[kWarps];
@@ -523,7 +529,7 @@ int launch_attend_candidates(const kvq_cache &c, const void *q, int q_dtype, int
   case F:                                                                                     \
     cudaFuncSetAttribute(cand_topk_kernel<F>, cudaFuncAttributeMaxDynamicSharedMemorySize,   \
                          static_cast<int>(smem));                                             \
-    cand_topk_kernel<F><<<grid, kWarps * 32, smem, s>>>(a);                                   \
+    launch_dependent(cand_topk_kernel<F>, grid, dim3(kWarps * 32), smem, s, a);               \
     break;
       KVQ_TOPK_CASE(1)
       KVQ_TOPK_CASE(2)
@@ -540,7 +546,8 @@ int launch_attend_candidates(const kvq_cache &c, const void *q, int q_dtype, int
     return 1;
   }
   if (d.D == 128) {
-    cand128_kernel<<<dim3(n_q, Hq, d.B), kWarps * 32, sizeof(int32_t) * n_cand, s>>>(a);
+    launch_dependent(cand128_kernel, dim3(n_q, Hq, d.B), dim3(kWarps * 32),
+                     sizeof(int32_t) * n_cand, s, a);
     return 1;
   }
   switch (d.D / 32) {

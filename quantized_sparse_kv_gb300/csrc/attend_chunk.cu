@@ -413,6 +413,10 @@ __global__ void __launch_bounds__(384, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // The barriers and TMEM are set up while the previous kernel drains; its
+  // outputs (the expanded or gathered K and V rows) are read only after this.
+  wait_prior_grid();
+  allow_next_grid();
   const uint32_t tmem = sm.tmem_base;
   // group g: S at columns 256g, O at 256g + 128
   auto t_s = [&](int g) { return tmem + 256u * g; };
@@ -711,6 +715,8 @@ __device__ __forceinline__ float e8m0_scale(uint32_t e) {
 __global__ void mxfp8_to_bf16_kernel(const uint8_t *__restrict__ codes,
                                      const uint8_t *__restrict__ e8m0, long n16,
                                      __nv_bfloat16 *__restrict__ out) {
+  wait_prior_grid();
+  allow_next_grid();
   for (long i = blockIdx.x * static_cast<long>(blockDim.x) + threadIdx.x; i < n16;
        i += static_cast<long>(gridDim.x) * blockDim.x) {
     const uint4 c = reinterpret_cast<const uint4 *>(codes)[i];
@@ -742,6 +748,8 @@ __global__ void mxfp8_to_bf16_kernel(const uint8_t *__restrict__ codes,
 __global__ void __launch_bounds__(256) q_mxfp8_round_kernel(const __nv_bfloat16 *__restrict__ q,
                                                             long blocks,
                                                             __nv_bfloat16 *__restrict__ out) {
+  wait_prior_grid();
+  allow_next_grid();
   const long tid = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const bool live = (tid >> 2) < blocks;
   const uint4 u = live ? reinterpret_cast<const uint4 *>(q)[tid] : make_uint4(0, 0, 0, 0);
@@ -803,6 +811,8 @@ __device__ __forceinline__ float nib(uint32_t w, int e) {
 
 // One thread per (token, 8 features) of unit blockIdx.y: 16-byte stores.
 __global__ void __launch_bounds__(256) history_to_bf16_kernel(const HistArgs a) {
+  wait_prior_grid();
+  allow_next_grid();
   const int i = blockIdx.x * 256 + threadIdx.x;
   if (i >= a.N * 16) return;
   const long u = blockIdx.y;
@@ -876,6 +886,8 @@ __device__ __forceinline__ float win_value(const void *w, int dt, long i) {
 
 // One thread per (listed key, 8 features) of list blockIdx.y.
 __global__ void __launch_bounds__(256) gather_lists_bf16_kernel(const ListArgs a) {
+  wait_prior_grid();
+  allow_next_grid();
   const int i = blockIdx.x * 256 + threadIdx.x;
   if (i >= a.C * 16) return;
   const long l = blockIdx.y;
@@ -1009,7 +1021,7 @@ int launch_attend_chunk(const kvq_cache &c, const void *q, int Hq, int n_q, floa
     h.Ws = d.Ws;
     const dim3 grid(static_cast<unsigned>((d.N * 16 + 255) / 256),
                     static_cast<unsigned>(d.B * d.Hkv));
-    history_to_bf16_kernel<<<grid, 256, 0, s>>>(h);
+    launch_dependent(history_to_bf16_kernel, grid, dim3(256), 0, s, h);
     kptr = h.k_out;
     vptr = h.v_out;
     launches += 1;
@@ -1019,11 +1031,11 @@ int launch_attend_chunk(const kvq_cache &c, const void *q, int Hq, int n_q, floa
     __nv_bfloat16 *kb = static_cast<__nv_bfloat16 *>(ws);
     __nv_bfloat16 *qb = reinterpret_cast<__nv_bfloat16 *>(static_cast<uint8_t *>(ws) +
                                                           ((kn * 2 + 255) & ~255L));
-    mxfp8_to_bf16_kernel<<<static_cast<unsigned>(std::min<long>((kn / 16 + 255) / 256, 1L << 20)),
-                           256, 0, s>>>(static_cast<const uint8_t *>(c.k_window), c.k_window_e8m0,
-                                        kn / 16, kb);
-    q_mxfp8_round_kernel<<<static_cast<unsigned>((qn / 8 + 255) / 256), 256, 0, s>>>(
-        static_cast<const __nv_bfloat16 *>(q), qn / 32, qb);
+    const unsigned kblocks = static_cast<unsigned>(std::min<long>((kn / 16 + 255) / 256, 1L << 20));
+    launch_dependent(mxfp8_to_bf16_kernel, dim3(kblocks), dim3(256), 0, s,
+                     static_cast<const uint8_t *>(c.k_window), c.k_window_e8m0, kn / 16, kb);
+    launch_dependent(q_mxfp8_round_kernel, dim3(static_cast<unsigned>((qn / 8 + 255) / 256)),
+                     dim3(256), 0, s, static_cast<const __nv_bfloat16 *>(q), qn / 32, qb);
     kptr = kb;
     qptr = qb;
     launches += 2;
@@ -1056,7 +1068,7 @@ int launch_attend_chunk(const kvq_cache &c, const void *q, int Hq, int n_q, floa
   cudaFuncSetAttribute(chunk_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        static_cast<int>(smem));
   dim3 grid((n_q + kBM - 1) / kBM, c.batch * Hq);
-  chunk_bf16_kernel<<<grid, 384, smem, s>>>(tq, tk, tv, a);
+  launch_dependent(chunk_bf16_kernel, grid, dim3(384), smem, s, tq, tk, tv, a);
   return launches;
 }
 
@@ -1102,9 +1114,9 @@ int launch_candidate_lists(const kvq_cache &c, const void *q, int Hq, int n_q,
   g.lists_per_head = lists_per_head;
   g.C = C;
   g.ctl = ctl;
-  gather_lists_bf16_kernel<<<dim3(static_cast<unsigned>((C * 16 + 255) / 256),
-                                  static_cast<unsigned>(lists)),
-                             256, 0, s>>>(g);
+  launch_dependent(gather_lists_bf16_kernel,
+                   dim3(static_cast<unsigned>((C * 16 + 255) / 256), static_cast<unsigned>(lists)),
+                   dim3(256), 0, s, g);
   CUtensorMap tq, tk, tv;
   if (!make_map(&tq, q, n_q, d.B * Hq, n_q) ||
       !make_map(&tk, g.k_out, C, static_cast<int>(lists), C) ||
@@ -1128,7 +1140,7 @@ int launch_candidate_lists(const kvq_cache &c, const void *q, int Hq, int n_q,
   cudaFuncSetAttribute(chunk_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        static_cast<int>(smem));
   dim3 grid((n_q + kBM - 1) / kBM, d.B * Hq);
-  chunk_bf16_kernel<<<grid, 384, smem, s>>>(tq, tk, tv, a);
+  launch_dependent(chunk_bf16_kernel, grid, dim3(384), smem, s, tq, tk, tv, a);
   return 2;
 }
 
@@ -1182,9 +1194,9 @@ int launch_region_drop(const kvq_cache &c, const void *q, int Hq, int n_q, const
   g.lists_per_head = 1;
   g.C = C;
   g.ctl = ctl;
-  gather_lists_bf16_kernel<<<dim3(static_cast<unsigned>((C * 16 + 255) / 256),
-                                  static_cast<unsigned>(units)),
-                             256, 0, s>>>(g);
+  launch_dependent(gather_lists_bf16_kernel,
+                   dim3(static_cast<unsigned>((C * 16 + 255) / 256), static_cast<unsigned>(units)),
+                   dim3(256), 0, s, g);
   CUtensorMap tq, tk, tv;
   if (!make_map(&tq, q, n_q, d.B * Hq, n_q) ||
       !make_map(&tk, g.k_out, C, static_cast<int>(units), C) ||
@@ -1208,7 +1220,7 @@ int launch_region_drop(const kvq_cache &c, const void *q, int Hq, int n_q, const
   cudaFuncSetAttribute(chunk_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        static_cast<int>(smem));
   dim3 grid((n_q + kBM - 1) / kBM, d.B * Hq);
-  chunk_bf16_kernel<<<grid, 384, smem, s>>>(tq, tk, tv, a);
+  launch_dependent(chunk_bf16_kernel, grid, dim3(384), smem, s, tq, tk, tv, a);
   return 2;
 }
 

@@ -448,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const Deco
 
   // The combine launch may start placing its blocks as this grid drains; it
   // waits for the whole grid before reading any partial.
-  asm volatile("griddepcontrol.launch_dependents;");
+  allow_next_grid();
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -459,12 +459,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const Deco
     fence_mbar_init();
   }
   __syncthreads();
-  // This grid is itself a programmatic dependent launch: it may be placed
-  // while the previous kernel on the stream drains (for instance the last
-  // call's combine, which reads the partial slots this grid rewrites, or a
-  // kv_pack writing the cache), so nothing in global memory is touched before
-  // that kernel has completed and its writes are visible.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // The previous kernel may still be running (the last call's combine reads
+  // the partial slots this grid rewrites; a kv_pack may be writing the cache).
+  wait_prior_grid();
 
   if (warp == kConsumers) {
     // ---------------- loader: one lane walks the CTA's items in order
@@ -603,7 +600,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const Deco
 // sixteen at a time with all loads of a batch in flight together.
 template <typename OT>
 __global__ void __launch_bounds__(256) combine_kernel(const DecodeArgs a, OT *__restrict__ out) {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  wait_prior_grid();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int u = blockIdx.x;
   const int h = warp;
@@ -726,31 +723,15 @@ int launch_attend_decode(const kvq_cache &c, const void *q, int q_dtype, float s
   const size_t smem = sizeof(DecodeSmem);
   cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        static_cast<int>(smem));
-  // Both kernels are programmatic dependent launches: the blocks of each may
-  // be placed while the kernel before it drains, and wait for it on the device.
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cudaLaunchConfig_t dcfg = {};
-  dcfg.gridDim = dim3(static_cast<unsigned>(p.num_ctas));
-  dcfg.blockDim = dim3(kThreads);
-  dcfg.dynamicSmemBytes = smem;
-  dcfg.stream = s;
-  dcfg.attrs = attr;
-  dcfg.numAttrs = 1;
-  cudaLaunchKernelEx(&dcfg, decode_kernel, a);
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(p.units));
-  cfg.blockDim = dim3(kHeads * 32);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = s;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  // The combine grid's blocks may be placed while the decode grid drains; they
+  // wait for it on the device.
+  launch_dependent(decode_kernel, dim3(p.num_ctas), dim3(kThreads), smem, s, a);
   if (out_dtype == KVQ_F32)
-    cudaLaunchKernelEx(&cfg, combine_kernel<float>, a, static_cast<float *>(out));
+    launch_dependent(combine_kernel<float>, dim3(p.units), dim3(kHeads * 32), 0, s, a,
+                     static_cast<float *>(out));
   else
-    cudaLaunchKernelEx(&cfg, combine_kernel<__nv_bfloat16>, a,
-                       static_cast<__nv_bfloat16 *>(out));
+    launch_dependent(combine_kernel<__nv_bfloat16>, dim3(p.units), dim3(kHeads * 32), 0, s, a,
+                     static_cast<__nv_bfloat16 *>(out));
   return 2;
 }
 

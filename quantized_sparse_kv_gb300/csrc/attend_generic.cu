@@ -56,6 +56,8 @@ __device__ __forceinline__ float window_value(const void *w, int dtype, long i) 
 
 template <int DPL>
 __global__ void __launch_bounds__(kWarps * 32) generic_attend_kernel(GenericArgs a) {
+  wait_prior_grid();
+  allow_next_grid();
   constexpr int D = DPL * 32;
   extern __shared__ float sm[];
   float *Ks = sm;                        // [32][D+1]
@@ -202,6 +204,8 @@ constexpr int kSmallRegions = 4;
 
 template <int D>
 __global__ void __launch_bounds__(kSmallWarps * 32) small_attend_kernel(GenericArgs a, long rows) {
+  wait_prior_grid();
+  allow_next_grid();
   __shared__ float red[kSmallWarps][32][D + 1];
   __shared__ float wm[kSmallWarps], wl[kSmallWarps], wr[kSmallWarps][kSmallRegions];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -355,7 +359,7 @@ void launch_dpl(const GenericArgs &a, int B, cudaStream_t s) {
   cudaFuncSetAttribute(generic_attend_kernel<DPL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        static_cast<int>(smem));
   dim3 grid((a.n_q + kRowsPerCta - 1) / kRowsPerCta, a.Hq, B);
-  generic_attend_kernel<DPL><<<grid, kWarps * 32, smem, s>>>(a);
+  launch_dependent(generic_attend_kernel<DPL>, grid, dim3(kWarps * 32), smem, s, a);
 }
 
 }  // namespace
@@ -395,7 +399,8 @@ int launch_attend_generic(const kvq_cache &c, const void *q, int q_dtype, int Hq
   a.reg = make_regions(bounds, n_regions);
   if (d.D == 32 && c.kwin_dtype != KVQ_MXFP8 && a.reg.n <= kSmallRegions) {
     const long rows = static_cast<long>(d.B) * Hq * n_q;  // one CTA per query row
-    small_attend_kernel<32><<<static_cast<unsigned>(rows), kSmallWarps * 32, 0, s>>>(a, rows);
+    launch_dependent(small_attend_kernel<32>, dim3(static_cast<unsigned>(rows)),
+                     dim3(kSmallWarps * 32), 0, s, a, rows);
     return 1;
   }
   switch (d.D / 32) {

@@ -125,6 +125,8 @@ __device__ __forceinline__ void mxfp8_round_row(float (&x)[E]) {
 // Both workspace copies of key blockIdx.x * 8 + warp of unit blockIdx.y.
 template <int E>
 __global__ void __launch_bounds__(kThreads) keys_kernel(const StatsArgs a) {
+  wait_prior_grid();
+  allow_next_grid();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int j = blockIdx.x * kWarps + warp;
   if (j >= a.N) return;
@@ -236,6 +238,8 @@ __device__ uint32_t kth_largest_bits(const float *x, int n, int k, uint32_t *his
 
 template <int E>
 __global__ void __launch_bounds__(kThreads) stats_kernel(const StatsArgs a) {
+  wait_prior_grid();
+  allow_next_grid();
   extern __shared__ float sm[];
   float *s_ref = sm;                 // [N]: scores, then p
   float *s_mx = sm + a.N;            // [N]: scores of the MXFP8 Q/K path
@@ -435,10 +439,10 @@ int launch_attend_stats(const kvq_cache &c, const void *q, int q_dtype, int Hq, 
   switch (d.D / 32) {
 #define KVQ_STATS_CASE(E)                                                                     \
   case E:                                                                                     \
-    keys_kernel<E><<<kgrid, kThreads, 0, s>>>(a);                                             \
+    launch_dependent(keys_kernel<E>, dim3(kgrid), dim3(kThreads), 0, s, a);                   \
     cudaFuncSetAttribute(stats_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize,       \
                          static_cast<int>(smem));                                             \
-    stats_kernel<E><<<grid, kThreads, smem, s>>>(a);                                          \
+    launch_dependent(stats_kernel<E>, dim3(grid), dim3(kThreads), smem, s, a);                \
     break;
     KVQ_STATS_CASE(1)
     KVQ_STATS_CASE(2)

@@ -51,6 +51,8 @@ __global__ void __launch_bounds__(256) pack_k128_kernel(const T *__restrict__ k,
                                                         int Gs, long u0,
                                                         uint8_t *__restrict__ k_codes,
                                                         float *__restrict__ k_scales) {
+  wait_prior_grid();
+  allow_next_grid();
   constexpr int D = 128;
   __shared__ __align__(16) float part[8][D];
   __shared__ __align__(16) float scale[D];
@@ -128,6 +130,8 @@ __global__ void __launch_bounds__(256) pack_k_kernel(const T *__restrict__ k, lo
                                                      int D, int cut, int Gk, int Gs,
                                                      uint8_t *__restrict__ k_codes,
                                                      float *__restrict__ k_scales) {
+  wait_prior_grid();
+  allow_next_grid();
   const long task = blockIdx.x * static_cast<long>(blockDim.x) + threadIdx.x;
   if (task >= tasks) return;
   const int pairs = D / 2;
@@ -169,6 +173,8 @@ __global__ void __launch_bounds__(256) pack_v_kernel(const T *__restrict__ v, lo
                                                      int nt, int N, int D, int Vs,
                                                      uint8_t *__restrict__ v_codes,
                                                      float *__restrict__ v_scales) {
+  wait_prior_grid();
+  allow_next_grid();
   const int groups = D / kGroup;
   const unsigned task = blockIdx.x * blockDim.x + threadIdx.x;  // (token, group) in the slice
   if (task >= static_cast<unsigned>(nt) * groups) return;
@@ -204,6 +210,8 @@ __global__ void __launch_bounds__(256) pack_v_kernel(const T *__restrict__ v, lo
 template <typename TI, typename TO>
 __global__ void window_copy_kernel(const TI *__restrict__ x, long rows, int N, int D, int R,
                                    int Ws, TO *__restrict__ w) {
+  wait_prior_grid();
+  allow_next_grid();
   const long n = rows * D;
   for (long i = blockIdx.x * static_cast<long>(blockDim.x) + threadIdx.x; i < n;
        i += static_cast<long>(gridDim.x) * blockDim.x) {
@@ -221,6 +229,8 @@ __global__ void __launch_bounds__(256) window_mxfp8_kernel(const TI *__restrict_
                                                            int N, int D, int R, int Ws,
                                                            uint8_t *__restrict__ codes,
                                                            uint8_t *__restrict__ e8m0) {
+  wait_prior_grid();
+  allow_next_grid();
   const int groups = D / kGroup;
   const long task = static_cast<long>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32;
   if (task >= rows * groups) return;
@@ -252,14 +262,14 @@ int pack_typed(const T *k, const T *v, const kvq_cache &c, cudaStream_t s) {
     if (d.D == 128) {
       for (long u0 = 0; u0 < units; u0 += 65535) {  // grid.y holds at most 65,535 units
         const unsigned nu = static_cast<unsigned>(std::min<long>(65535, units - u0));
-        pack_k128_kernel<T><<<dim3(d.Gk, nu), 256, 0, s>>>(k, d.N, d.cut, d.Gs, u0, c.k_codes,
-                                                           c.k_scales);
+        launch_dependent(pack_k128_kernel<T>, dim3(d.Gk, nu), dim3(256), 0, s, k, d.N, d.cut, d.Gs,
+                         u0, c.k_codes, c.k_scales);
         ++launches;
       }
     } else {
       const long ktasks = units * d.Gk * (d.D / 2);
-      pack_k_kernel<T><<<static_cast<unsigned>((ktasks + 255) / 256), 256, 0, s>>>(
-          k, ktasks, d.N, d.D, d.cut, d.Gk, d.Gs, c.k_codes, c.k_scales);
+      const unsigned kblocks = static_cast<unsigned>((ktasks + 255) / 256);
+      launch_dependent(pack_k_kernel<T>, dim3(kblocks), dim3(256), 0, s, k, ktasks, d.N, d.D, d.cut, d.Gk, d.Gs, c.k_codes, c.k_scales);
       ++launches;
     }
     // V: per launch at most 65,535 units (grid.y) and 2^24 tokens of each,
@@ -270,8 +280,8 @@ int pack_typed(const T *k, const T *v, const kvq_cache &c, cudaStream_t s) {
       for (int t0 = 0; t0 < d.cut; t0 += kSlice) {
         const int nt = std::min(kSlice, d.cut - t0);
         const long vthreads = static_cast<long>(nt) * (d.D / kGroup);
-        pack_v_kernel<T><<<dim3(static_cast<unsigned>((vthreads + 255) / 256), nu), 256, 0, s>>>(
-            v, u0, t0, nt, d.N, d.D, d.Vs, c.v_codes, c.v_scales);
+        launch_dependent(pack_v_kernel<T>, dim3(static_cast<unsigned>((vthreads + 255) / 256), nu),
+                         dim3(256), 0, s, v, u0, t0, nt, d.N, d.D, d.Vs, c.v_codes, c.v_scales);
         ++launches;
       }
     }
@@ -282,20 +292,21 @@ int pack_typed(const T *k, const T *v, const kvq_cache &c, cudaStream_t s) {
         static_cast<unsigned>(std::min<long>((rows * d.D + 255) / 256, 1L << 20));
     if (c.kwin_dtype == KVQ_MXFP8) {
       const long tasks = rows * (d.D / kGroup);
-      window_mxfp8_kernel<T><<<static_cast<unsigned>((tasks + 7) / 8), 256, 0, s>>>(
-          k, rows, d.N, d.D, d.R, d.Ws, static_cast<uint8_t *>(c.k_window), c.k_window_e8m0);
+      launch_dependent(window_mxfp8_kernel<T>, dim3(static_cast<unsigned>((tasks + 7) / 8)),
+                       dim3(256), 0, s, k, rows, d.N, d.D, d.R, d.Ws,
+                       static_cast<uint8_t *>(c.k_window), c.k_window_e8m0);
     } else if (c.kwin_dtype == KVQ_F32) {
-      window_copy_kernel<T, float><<<blocks, 256, 0, s>>>(k, rows, d.N, d.D, d.R, d.Ws,
-                                                          static_cast<float *>(c.k_window));
+      launch_dependent(window_copy_kernel<T, float>, dim3(blocks), dim3(256), 0, s, k, rows, d.N,
+                       d.D, d.R, d.Ws, static_cast<float *>(c.k_window));
     } else {
-      window_copy_kernel<T, __nv_bfloat16><<<blocks, 256, 0, s>>>(
+      launch_dependent(window_copy_kernel<T, __nv_bfloat16>, dim3(blocks), dim3(256), 0, s,
           k, rows, d.N, d.D, d.R, d.Ws, static_cast<__nv_bfloat16 *>(c.k_window));
     }
     if (c.vwin_dtype == KVQ_F32) {
-      window_copy_kernel<T, float><<<blocks, 256, 0, s>>>(v, rows, d.N, d.D, d.R, d.Ws,
-                                                          static_cast<float *>(c.v_window));
+      launch_dependent(window_copy_kernel<T, float>, dim3(blocks), dim3(256), 0, s, v, rows, d.N,
+                       d.D, d.R, d.Ws, static_cast<float *>(c.v_window));
     } else {
-      window_copy_kernel<T, __nv_bfloat16><<<blocks, 256, 0, s>>>(
+      launch_dependent(window_copy_kernel<T, __nv_bfloat16>, dim3(blocks), dim3(256), 0, s,
           v, rows, d.N, d.D, d.R, d.Ws, static_cast<__nv_bfloat16 *>(c.v_window));
     }
     launches += 2;
@@ -335,6 +346,8 @@ __device__ __forceinline__ float seq_at(const AppendArgs &a, const void *win, co
 // shared memory as floats ([32][D], K then V); K takes one thread per channel
 // pair, V one thread per (token, 32-feature block).
 __global__ void __launch_bounds__(128) append_migrate_kernel(const AppendArgs a) {
+  wait_prior_grid();
+  allow_next_grid();
   extern __shared__ float xs[];
   const int gi = blockIdx.x;
   const long u = blockIdx.y;
@@ -392,6 +405,8 @@ __device__ __forceinline__ void store_as(void *base, long i, int dt, float x) {
 // before the barrier; with m = 0 the old rows stay and only new ones are
 // written.
 __global__ void __launch_bounds__(256) append_window_kernel(const AppendArgs a, int R_new) {
+  wait_prior_grid();
+  allow_next_grid();
   const long u = blockIdx.x;
   const int D = a.D;
   for (int r0 = a.m == 0 ? a.R_old : 0; r0 < R_new; r0 += kGroup) {
@@ -446,11 +461,13 @@ int launch_append(const kvq_cache &c, const void *k_new, const void *v_new, int 
   a.Ws = d.Ws;
   int launches = 0;
   if (m > 0) {
-    append_migrate_kernel<<<dim3(static_cast<unsigned>(m), static_cast<unsigned>(units)), 128,
-                            sizeof(float) * kGroup * d.D, s>>>(a);
+    launch_dependent(append_migrate_kernel,
+                     dim3(static_cast<unsigned>(m), static_cast<unsigned>(units)), dim3(128),
+                     sizeof(float) * kGroup * d.D, s, a);
     ++launches;
   }
-  append_window_kernel<<<static_cast<unsigned>(units), 256, 0, s>>>(a, R_new);
+  launch_dependent(append_window_kernel, dim3(static_cast<unsigned>(units)), dim3(256), 0, s, a,
+                   R_new);
   return launches + 1;
 }
 
