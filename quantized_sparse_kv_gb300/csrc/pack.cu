@@ -331,53 +331,125 @@ struct AppendArgs {
   int D, T, R_old, m, Gk_old, cut_old, Gs, Vs, Ws;
 };
 
-__device__ __forceinline__ float load_as(const void *base, long i, int dt) {
-  return dt == KVQ_F32 ? static_cast<const float *>(base)[i]
-                       : load_f32(static_cast<const __nv_bfloat16 *>(base) + i);
+// Eight consecutive elements from element e0 of a window or of the new rows,
+// as floats: one 16-byte load for bf16, two for fp32 (e0 is a multiple of 8
+// and every row starts on a 16-byte boundary).
+__device__ __forceinline__ void load8_as(const void *base, long e0, int dt, float (&x)[8]) {
+  if (dt == KVQ_F32) {
+    const float4 lo = *reinterpret_cast<const float4 *>(static_cast<const float *>(base) + e0);
+    const float4 hi = *reinterpret_cast<const float4 *>(static_cast<const float *>(base) + e0 + 4);
+    x[0] = lo.x, x[1] = lo.y, x[2] = lo.z, x[3] = lo.w;
+    x[4] = hi.x, x[5] = hi.y, x[6] = hi.z, x[7] = hi.w;
+  } else {
+    const uint4 w = *reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(base) + e0);
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      x[2 * i] = __uint_as_float(ws[i] << 16);
+      x[2 * i + 1] = __uint_as_float(ws[i] & 0xffff0000u);
+    }
+  }
 }
 
-__device__ __forceinline__ float seq_at(const AppendArgs &a, const void *win, const void *fresh,
-                                        int win_dt, long u, int i, int d) {
-  if (i < a.R_old) return load_as(win, (u * a.Ws + i) * a.D + d, win_dt);
-  return load_as(fresh, (u * a.T + (i - a.R_old)) * a.D + d, a.in_dtype);
+__device__ __forceinline__ void store8_as(void *base, long e0, int dt, const float (&x)[8]) {
+  if (dt == KVQ_F32) {
+    float *o = static_cast<float *>(base) + e0;
+    *reinterpret_cast<float4 *>(o) = make_float4(x[0], x[1], x[2], x[3]);
+    *reinterpret_cast<float4 *>(o + 4) = make_float4(x[4], x[5], x[6], x[7]);
+  } else {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      __nv_bfloat162 b = __floats2bfloat162_rn(x[2 * i], x[2 * i + 1]);
+      w[i] = *reinterpret_cast<uint32_t *>(&b);
+    }
+    *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(base) + e0) =
+        make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+// Elements d0 .. d0 + 7 of token i of the append sequence S.
+__device__ __forceinline__ void seq8(const AppendArgs &a, const void *win, const void *fresh,
+                                     int win_dt, long u, int i, int d0, float (&x)[8]) {
+  if (i < a.R_old)
+    load8_as(win, (u * a.Ws + i) * a.D + d0, win_dt, x);
+  else
+    load8_as(fresh, (u * a.T + (i - a.R_old)) * a.D + d0, a.in_dtype, x);
+}
+
+constexpr int kAppendThreads = 256;
+// 8-element pieces of a 32-token group per thread: 32 * D / 8 / 256, D <= 256
+constexpr int kStagePieces = 4;
+
+// The group's 32 tokens of S into shared memory as floats, rows of D + 1
+// (the padding spreads a column over the banks). Every load of a thread is
+// issued before its first store.
+__device__ __forceinline__ void stage_group(const AppendArgs &a, const void *win,
+                                            const void *fresh, int win_dt, long u, int gi,
+                                            float *xs) {
+  const int D = a.D, pieces = kGroup * D / 8;
+  float x[kStagePieces][8];
+#pragma unroll
+  for (int k = 0; k < kStagePieces; ++k) {
+    const int pc = threadIdx.x + k * kAppendThreads;
+    if (pc < pieces) seq8(a, win, fresh, win_dt, u, kGroup * gi + pc * 8 / D, pc * 8 % D, x[k]);
+  }
+#pragma unroll
+  for (int k = 0; k < kStagePieces; ++k) {
+    const int pc = threadIdx.x + k * kAppendThreads;
+    if (pc < pieces) {
+      float *row = xs + (pc * 8 / D) * (D + 1) + pc * 8 % D;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) row[e] = x[k][e];
+    }
+  }
 }
 
 // One CTA per (migrated group gi, unit). The group's 32 tokens are staged in
-// shared memory as floats ([32][D], K then V); K takes one thread per channel
-// pair, V one thread per (token, 32-feature block).
-__global__ void __launch_bounds__(128) append_migrate_kernel(const AppendArgs a) {
+// shared memory as floats, K then V; K takes a thread per channel pair and
+// token slice, V one thread per (token, 32-feature block).
+__global__ void __launch_bounds__(kAppendThreads) append_migrate_kernel(const AppendArgs a) {
   wait_prior_grid();
   allow_next_grid();
-  extern __shared__ float xs[];
+  extern __shared__ float xs[];  // [32][D + 1]
   const int gi = blockIdx.x;
   const long u = blockIdx.y;
   const long grp = u * a.Gs + a.Gk_old + gi;
-  const int D = a.D;
-  for (int e = threadIdx.x; e < kGroup * D; e += blockDim.x)
-    xs[e] = seq_at(a, a.k_window, a.k_new, a.kwin, u, kGroup * gi + e / D, e % D);
+  const int D = a.D, ld = D + 1;
+  stage_group(a, a.k_window, a.k_new, a.kwin, u, gi, xs);
   __syncthreads();
-  for (int p = threadIdx.x; p < D / 2; p += blockDim.x) {
-    float a0 = 0.0f, a1 = 0.0f;
-    for (int t = 0; t < kGroup; ++t) {
-      a0 = fmaxf(a0, fabsf(xs[t * D + 2 * p]));
-      a1 = fmaxf(a1, fabsf(xs[t * D + 2 * p + 1]));
-    }
-    const float s0 = int4_scale(a0), s1 = int4_scale(a1);
+  // K: thread (pair p, slice q) takes channels 2p, 2p + 1 over tokens
+  // q * tq .. q * tq + tq - 1; the per-channel maxima meet in shared memory.
+  __shared__ float2 kmax[kAppendThreads];
+  const int np = D / 2, nq = kAppendThreads / np, tq = kGroup / nq;
+  const int p = threadIdx.x % np, q = threadIdx.x / np;
+  float a0 = 0.0f, a1 = 0.0f;
+  for (int t = q * tq; t < q * tq + tq; ++t) {
+    a0 = fmaxf(a0, fabsf(xs[t * ld + 2 * p]));
+    a1 = fmaxf(a1, fabsf(xs[t * ld + 2 * p + 1]));
+  }
+  kmax[threadIdx.x] = make_float2(a0, a1);
+  __syncthreads();
+  for (int r = 0; r < nq; ++r) {
+    a0 = fmaxf(a0, kmax[r * np + p].x);
+    a1 = fmaxf(a1, kmax[r * np + p].y);
+  }
+  const float s0 = int4_scale(a0), s1 = int4_scale(a1);
+  if (q == 0) {
     a.k_scales[grp * D + 2 * p] = s0;
     a.k_scales[grp * D + 2 * p + 1] = s1;
-    for (int t = 0; t < kGroup; ++t)
-      a.k_codes[(grp * kGroup + t) * (D / 2) + p] = static_cast<uint8_t>(
-          (int4_code(xs[t * D + 2 * p], s0) + 8) | ((int4_code(xs[t * D + 2 * p + 1], s1) + 8) << 4));
   }
+  for (int t = q * tq; t < q * tq + tq; ++t)
+    a.k_codes[(grp * kGroup + t) * (D / 2) + p] = static_cast<uint8_t>(
+        (int4_code(xs[t * ld + 2 * p], s0) + 8) | ((int4_code(xs[t * ld + 2 * p + 1], s1) + 8) << 4));
   __syncthreads();
-  for (int e = threadIdx.x; e < kGroup * D; e += blockDim.x)
-    xs[e] = seq_at(a, a.v_window, a.v_new, a.vwin, u, kGroup * gi + e / D, e % D);
+  stage_group(a, a.v_window, a.v_new, a.vwin, u, gi, xs);
   __syncthreads();
   const int blocks = D / kGroup;
   for (int task = threadIdx.x; task < kGroup * blocks; task += blockDim.x) {
     const int t = task / blocks, j = task % blocks;
     const long row = u * a.Vs + a.cut_old + kGroup * gi + t;
-    const float *x = xs + t * D + kGroup * j;
+    const float *x = xs + t * ld + kGroup * j;
     float amax = 0.0f;
 #pragma unroll
     for (int e = 0; e < kGroup; ++e) amax = fmaxf(amax, fabsf(x[e]));
@@ -392,33 +464,38 @@ __global__ void __launch_bounds__(128) append_migrate_kernel(const AppendArgs a)
   }
 }
 
-__device__ __forceinline__ void store_as(void *base, long i, int dt, float x) {
-  if (dt == KVQ_F32)
-    static_cast<float *>(base)[i] = x;
-  else
-    store_from_f32(static_cast<__nv_bfloat16 *>(base) + i, x);
-}
-
 // The new window, rows [0, R_new) = S[32m ..], one CTA per unit, 32 rows per
 // step with a barrier between steps. With m > 0 a step reads rows at least 32
 // above those it writes, and a row written at step s was read at step s - m,
 // before the barrier; with m = 0 the old rows stay and only new ones are
-// written.
-__global__ void __launch_bounds__(256) append_window_kernel(const AppendArgs a, int R_new) {
+// written. A step moves 8-element pieces, all of a thread's loads before its
+// stores.
+__global__ void __launch_bounds__(kAppendThreads) append_window_kernel(const AppendArgs a,
+                                                                       int R_new) {
   wait_prior_grid();
   allow_next_grid();
   const long u = blockIdx.x;
   const int D = a.D;
   for (int r0 = a.m == 0 ? a.R_old : 0; r0 < R_new; r0 += kGroup) {
-    const int rows = min(kGroup, R_new - r0);
-    for (int e = threadIdx.x; e < rows * D; e += blockDim.x) {
-      const int r = r0 + e / D, d = e % D;
-      const int i = kGroup * a.m + r;
-      const float kx = seq_at(a, a.k_window, a.k_new, a.kwin, u, i, d);
-      const float vx = seq_at(a, a.v_window, a.v_new, a.vwin, u, i, d);
-      const long o = (u * a.Ws + r) * D + d;
-      store_as(a.k_window, o, a.kwin, kx);
-      store_as(a.v_window, o, a.vwin, vx);
+    const int pieces = min(kGroup, R_new - r0) * D / 8;
+    float kx[kStagePieces][8], vx[kStagePieces][8];
+#pragma unroll
+    for (int k = 0; k < kStagePieces; ++k) {
+      const int pc = threadIdx.x + k * kAppendThreads;
+      if (pc < pieces) {
+        const int i = kGroup * a.m + r0 + pc * 8 / D, d0 = pc * 8 % D;
+        seq8(a, a.k_window, a.k_new, a.kwin, u, i, d0, kx[k]);
+        seq8(a, a.v_window, a.v_new, a.vwin, u, i, d0, vx[k]);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kStagePieces; ++k) {
+      const int pc = threadIdx.x + k * kAppendThreads;
+      if (pc < pieces) {
+        const long o = (u * a.Ws + r0 + pc * 8 / D) * D + pc * 8 % D;
+        store8_as(a.k_window, o, a.kwin, kx[k]);
+        store8_as(a.v_window, o, a.vwin, vx[k]);
+      }
     }
     __syncthreads();
   }
@@ -461,13 +538,14 @@ int launch_append(const kvq_cache &c, const void *k_new, const void *v_new, int 
   a.Ws = d.Ws;
   int launches = 0;
   if (m > 0) {
+    const size_t smem = sizeof(float) * kGroup * (d.D + 1);
     launch_dependent(append_migrate_kernel,
-                     dim3(static_cast<unsigned>(m), static_cast<unsigned>(units)), dim3(128),
-                     sizeof(float) * kGroup * d.D, s, a);
+                     dim3(static_cast<unsigned>(m), static_cast<unsigned>(units)),
+                     dim3(kAppendThreads), smem, s, a);
     ++launches;
   }
-  launch_dependent(append_window_kernel, dim3(static_cast<unsigned>(units)), dim3(256), 0, s, a,
-                   R_new);
+  launch_dependent(append_window_kernel, dim3(static_cast<unsigned>(units)),
+                   dim3(kAppendThreads), 0, s, a, R_new);
   return launches + 1;
 }
 

@@ -134,6 +134,7 @@ def to_dev(x, dtype):
     (1, 3, 64, 16, "f32", 48, [1] * 20 + [33, 2, 70]),
     (2, 1, 128, 128, "bf16", 160, [1] * 36 + [100, 1]),
     (1, 2, 32, 0, "f32", 64, [1] * 33 + [7, 40]),
+    (1, 2, 256, 32, "bf16", 40, [1] * 34 + [9, 50, 1]),
 ])
 def test_append_equals_pack_of_the_whole_sequence(kvq, b, h, d, window, dtype, n0, steps):
     total = n0 + sum(steps)
