@@ -492,9 +492,11 @@ def row_stats(kvq, synth, torch, steps, warmup, pk):
             "roofline": {"bound": "alu", "achieved": tf, "peak": peak, "unit": "TFLOP/s",
                          "frac": tf / peak, "traffic": None,
                          "peak_note": "fp32 FMA: 152 SMs x 128 lanes x 2 flop x 2.07 GHz",
-                         "note": "each query row re-reads its head's two fp32 key copies "
-                                 "(6.4 MB) from L2: bound by L2 traffic, not the ALUs"},
-            "launches": 1}
+                         "note": "three kernels: keys once per head into 32-key tiles, "
+                                 "scores of 16 rows per CTA (lane = key), per-row "
+                                 "statistics; flops counted are the two score dot products "
+                                 "only, the statistics passes take about 40 % of the time"},
+            "launches": 3}
 
 
 # ---------------------------------------------------------------- oracle (CPU) arm

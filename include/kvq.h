@@ -227,8 +227,10 @@ enum {
  * q: [batch][q_heads][n_q][D] in q_dtype (F32 or BF16), device; typically a
  *   sample of query rows. hadamard_signs: device float [D] of +-1, or NULL.
  * stats: device float [batch][q_heads][n_q][KVQ_N_STATS], see KVQ_STAT_*.
- * workspace/ws_bytes as kv_attend (it holds every key twice in fp32: as
- * attention reads it and on the MXFP8 Q/K path).
+ * workspace/ws_bytes as kv_attend (it holds every key twice in fp32, as
+ * attention reads it and on the MXFP8 Q/K path, and both score rows of
+ * every query row: about 8 x B x Hkv x N x D + 8 x B x q_heads x n_q x N
+ * bytes).
  * Restrictions (else KVQ_ERR_UNSUPPORTED): D in {32, 64, 128, 256},
  * N <= 16384.
  */

@@ -15,19 +15,25 @@
 //     E4M3 with one E8M0 scale per 32 along D; the total variation between its
 //     softmax and p, and whether both rows have the same argmax.
 //
-// Two kernels. keys_kernel writes, once per (sequence, KV head), every key
+// Three kernels. keys_kernel writes, once per (sequence, KV head), every key
 // twice to workspace in fp32: as attention reads it (int4 part dequantized,
 // window as stored) and on the MXFP8 Q/K path (rotated, rounded); warp per
 // key, lane l holding features l*E .. l*E + E - 1 (E = D / 32), the Hadamard
 // transform as E-wide in-thread butterflies followed by five lane-exchange
-// stages. stats_kernel: one CTA (8 warps) per query row; warp w scores keys
-// w, w + 8, ... on both paths from the workspace rows (whole rows per load,
-// shuffle reductions); both score rows stay in shared memory, the statistics
-// are block reductions over them, and each top-k mass takes the k-th largest
+// stages. Both copies are stored in tiles of 32 keys, feature-major
+// ([unit][tile][D][32]), transposed through shared memory. scores_kernel: one
+// CTA per 16 query rows of a head and a range of key tiles; lane = key, so
+// every tile row is one 128-byte load, read once for all 16 rows, and each
+// lane keeps the 16 rows' dot products on both paths (q from shared memory,
+// four features per broadcast load). stats_kernel: one CTA per query row;
+// both score rows come from workspace into shared memory, the statistics are
+// block reductions over them, and each top-k mass takes the k-th largest
 // probability from a radix select over the float bits.
 
 #include <cuda_fp8.h>
 #include <math_constants.h>
+
+#include <algorithm>
 
 #include "kvq_internal.h"
 
@@ -50,9 +56,15 @@ struct StatsArgs {
   float sm_scale;
   const float *signs;  // [D] +-1, or nullptr: no rotation
   float *stats;        // [rows][KVQ_N_STATS]
-  float *k_ref;        // workspace [units][N][D]: keys as attention reads them
-  float *k_mx;         // workspace [units][N][D]: keys on the MXFP8 Q/K path
+  float *k_ref;        // workspace [units][T][D][32]: keys as attention reads them
+  float *k_mx;         // workspace [units][T][D][32]: keys on the MXFP8 Q/K path
+  float *s_ref;        // workspace [rows][N]: sm_scale * q k on the reference path
+  float *s_mx;         // workspace [rows][N]: the same on the MXFP8 Q/K path
+  int T;               // key tiles of 32 per unit
+  int key_splits;      // scores_kernel CTAs per group of rows
 };
+
+constexpr int kRows = 16;  // query rows per scores_kernel CTA
 
 
 __device__ __forceinline__ float key_value(const StatsArgs &a, long u, int j, int d) {
@@ -122,26 +134,135 @@ __device__ __forceinline__ void mxfp8_round_row(float (&x)[E]) {
   }
 }
 
-// Both workspace copies of key blockIdx.x * 8 + warp of unit blockIdx.y.
+// Both workspace copies of the 32 keys of tile blockIdx.x of unit
+// blockIdx.y: warp w computes keys 4w .. 4w + 3 of the tile (zeros past N)
+// into shared memory [2][D][33], then the CTA stores both [D][32] tiles with
+// whole-row writes.
 template <int E>
 __global__ void __launch_bounds__(kThreads) keys_kernel(const StatsArgs a) {
   wait_prior_grid();
   allow_next_grid();
+  extern __shared__ float tile[];  // [2][D][33]
+  constexpr int D = 32 * E;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int j = blockIdx.x * kWarps + warp;
-  if (j >= a.N) return;
   const long u = blockIdx.y;
-  const long o = (u * a.N + j) * a.D + lane * E;
-  float x[E];
+  for (int kk = 0; kk < 4; ++kk) {
+    const int c = 4 * warp + kk;  // key within the tile
+    const int j = blockIdx.x * 32 + c;
+    float x[E];
+    if (j < a.N) {
 #pragma unroll
-  for (int t = 0; t < E; ++t) {
-    x[t] = key_value(a, u, j, lane * E + t);
-    a.k_ref[o + t] = x[t];
+      for (int t = 0; t < E; ++t) x[t] = key_value(a, u, j, lane * E + t);
+    } else {
+#pragma unroll
+      for (int t = 0; t < E; ++t) x[t] = 0.0f;
+    }
+#pragma unroll
+    for (int t = 0; t < E; ++t) tile[(lane * E + t) * 33 + c] = x[t];
+    if (j < a.N) {
+      if (a.signs) signed_hadamard<E>(x, a.signs, lane);
+      mxfp8_round_row<E>(x);
+    }
+#pragma unroll
+    for (int t = 0; t < E; ++t) tile[(D + lane * E + t) * 33 + c] = x[t];
   }
-  if (a.signs) signed_hadamard<E>(x, a.signs, lane);
-  mxfp8_round_row<E>(x);
+  __syncthreads();
+  const long o = (u * a.T + blockIdx.x) * D * 32;
+  for (int i = threadIdx.x; i < D * 32; i += kThreads) {
+    a.k_ref[o + i] = tile[(i >> 5) * 33 + (i & 31)];
+    a.k_mx[o + i] = tile[(D + (i >> 5)) * 33 + (i & 31)];
+  }
+}
+
+// Scores of query rows i0 .. i0 + 15 of head blockIdx.y (sequence b, query
+// head h) on both paths against the key tiles of split blockIdx.z. Rows past
+// n_q are computed as zeros and not stored.
+template <int E>
+__global__ void __launch_bounds__(kThreads) scores_kernel(const StatsArgs a) {
+  wait_prior_grid();
+  allow_next_grid();
+  constexpr int D = 32 * E;
+  __shared__ __align__(16) float qf[kRows][D];
+  __shared__ __align__(16) float qm[kRows][D];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long bh = blockIdx.y;  // b * Hq + h
+  const int h = static_cast<int>(bh % a.Hq);
+  const long u = (bh / a.Hq) * a.Hkv + h / a.group;
+  const int i0 = blockIdx.x * kRows;
+  const int nr = min(kRows, a.n_q - i0);
+  const long row0 = bh * a.n_q + i0;
+  for (int e = threadIdx.x; e < kRows * D; e += kThreads) {
+    const int r = e / D, d = e % D;
+    const long gi = (row0 + r) * D + d;
+    qf[r][d] = r >= nr ? 0.0f
+               : a.q_dtype == KVQ_F32 ? static_cast<const float *>(a.q)[gi]
+                                      : load_f32(static_cast<const __nv_bfloat16 *>(a.q) + gi);
+  }
+  __syncthreads();
+  for (int r = warp; r < kRows; r += kWarps) {
+    float x[E];
 #pragma unroll
-  for (int t = 0; t < E; ++t) a.k_mx[o + t] = x[t];
+    for (int t = 0; t < E; ++t) x[t] = qf[r][lane * E + t];
+    if (a.signs) signed_hadamard<E>(x, a.signs, lane);
+    mxfp8_round_row<E>(x);
+#pragma unroll
+    for (int t = 0; t < E; ++t) qm[r][lane * E + t] = x[t];
+  }
+  __syncthreads();
+
+  const int per = (a.T + a.key_splits - 1) / a.key_splits;
+  const int t_lo = blockIdx.z * per, t_hi = min(a.T, t_lo + per);
+  // a warp takes two tiles per step (lane = key in each): every q load from
+  // shared memory feeds both
+  for (int t0 = t_lo + warp; t0 < t_hi; t0 += 2 * kWarps) {
+    const int t1 = t0 + kWarps < t_hi ? t0 + kWarps : t0;
+    const float *kr0 = a.k_ref + (u * a.T + t0) * D * 32 + lane;
+    const float *km0 = a.k_mx + (u * a.T + t0) * D * 32 + lane;
+    const float *kr1 = a.k_ref + (u * a.T + t1) * D * 32 + lane;
+    const float *km1 = a.k_mx + (u * a.T + t1) * D * 32 + lane;
+    float ar[2][kRows], am[2][kRows];
+#pragma unroll
+    for (int r = 0; r < kRows; ++r) ar[0][r] = am[0][r] = ar[1][r] = am[1][r] = 0.0f;
+#pragma unroll 1
+    for (int d = 0; d < D; d += 4) {
+      float xr[2][4], xm[2][4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        xr[0][e] = __ldg(kr0 + (d + e) * 32);
+        xm[0][e] = __ldg(km0 + (d + e) * 32);
+        xr[1][e] = __ldg(kr1 + (d + e) * 32);
+        xm[1][e] = __ldg(km1 + (d + e) * 32);
+      }
+#pragma unroll
+      for (int r = 0; r < kRows; ++r) {
+        const float4 f = *reinterpret_cast<const float4 *>(&qf[r][d]);
+        const float4 g = *reinterpret_cast<const float4 *>(&qm[r][d]);
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+          ar[x][r] = fmaf(f.x, xr[x][0], ar[x][r]);
+          ar[x][r] = fmaf(f.y, xr[x][1], ar[x][r]);
+          ar[x][r] = fmaf(f.z, xr[x][2], ar[x][r]);
+          ar[x][r] = fmaf(f.w, xr[x][3], ar[x][r]);
+          am[x][r] = fmaf(g.x, xm[x][0], am[x][r]);
+          am[x][r] = fmaf(g.y, xm[x][1], am[x][r]);
+          am[x][r] = fmaf(g.z, xm[x][2], am[x][r]);
+          am[x][r] = fmaf(g.w, xm[x][3], am[x][r]);
+        }
+      }
+    }
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {
+      const int j = (x ? t1 : t0) * 32 + lane;
+      if ((x == 0 || t1 != t0) && j < a.N) {
+#pragma unroll
+        for (int r = 0; r < kRows; ++r)
+          if (r < nr) {
+            a.s_ref[(row0 + r) * a.N + j] = a.sm_scale * ar[x][r];
+            a.s_mx[(row0 + r) * a.N + j] = a.sm_scale * am[x][r];
+          }
+      }
+    }
+  }
 }
 
 __device__ __forceinline__ float block_sum(float x, float *red) {
@@ -153,18 +274,6 @@ __device__ __forceinline__ float block_sum(float x, float *red) {
   float t = 0.0f;
 #pragma unroll
   for (int w = 0; w < kWarps; ++w) t += red[w];
-  return t;
-}
-
-__device__ __forceinline__ float block_max(float x, float *red) {
-  x = warp_max(x);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  __syncthreads();
-  if (lane == 0) red[warp] = x;
-  __syncthreads();
-  float t = -CUDART_INF_F;
-#pragma unroll
-  for (int w = 0; w < kWarps; ++w) t = fmaxf(t, red[w]);
   return t;
 }
 
@@ -218,14 +327,44 @@ __device__ uint32_t kth_largest_bits(const float *x, int n, int k, uint32_t *his
       if ((b & mask) == prefix) atomicAdd(&hist[(b >> shift) & 255u], 1u);
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-      uint32_t cum = 0u, d = 255u;
-      for (;; --d) {
-        if (cum + hist[d] >= static_cast<uint32_t>(k) || d == 0u) break;
-        cum += hist[d];
+    if (threadIdx.x < 32) {
+      // the bucket d holding the k-th largest: count above d < k <= count
+      // above d + hist[d]; lane l owns buckets 8l .. 8l + 7
+      const int lane = threadIdx.x;
+      const uint32_t kk = static_cast<uint32_t>(k);
+      uint32_t hb[8], tot = 0u;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        hb[e] = hist[8 * lane + e];
+        tot += hb[e];
       }
-      sel[0] = d;
-      sel[1] = static_cast<uint32_t>(k) - cum;
+      uint32_t above = tot;  // inclusive suffix sum over lanes >= lane
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t v = __shfl_down_sync(0xffffffffu, above, o);
+        if (lane + o < 32) above += v;
+      }
+      const uint32_t all = __shfl_sync(0xffffffffu, above, 0);
+      uint32_t cum = above - tot;  // buckets of the lanes above
+      bool found = false;
+      uint32_t fd = 0u, fk = 0u;
+#pragma unroll
+      for (int e = 7; e >= 0; --e) {
+        if (!found && cum < kk && cum + hb[e] >= kk) {
+          found = true;
+          fd = 8u * lane + e;
+          fk = kk - cum;
+        }
+        cum += hb[e];
+      }
+      if (found) {
+        sel[0] = fd;
+        sel[1] = fk;
+      }
+      if (__ballot_sync(0xffffffffu, found) == 0u && lane == 0) {
+        sel[0] = 0u;
+        sel[1] = kk - (all - hb[0]);
+      }
     }
     __syncthreads();
     prefix |= sel[0] << shift;
@@ -236,88 +375,26 @@ __device__ uint32_t kth_largest_bits(const float *x, int n, int k, uint32_t *his
   return prefix;
 }
 
-template <int E>
 __global__ void __launch_bounds__(kThreads) stats_kernel(const StatsArgs a) {
   wait_prior_grid();
   allow_next_grid();
   extern __shared__ float sm[];
   float *s_ref = sm;                 // [N]: scores, then p
   float *s_mx = sm + a.N;            // [N]: scores of the MXFP8 Q/K path
-  __shared__ __align__(16) float qf[256];
-  __shared__ __align__(16) float qm[256];
   __shared__ float red[kWarps];
   __shared__ int redi[kWarps];
   __shared__ uint32_t hist[256], sel[2];
   const long row = blockIdx.x;       // (b * Hq + h) * n_q + i
-  const long bh = row / a.n_q;
-  const int h = static_cast<int>(bh % a.Hq);
-  const long u = (bh / a.Hq) * a.Hkv + h / a.group;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int D = a.D;
-
-  for (int d = threadIdx.x; d < D; d += kThreads)
-    qf[d] = a.q_dtype == KVQ_F32 ? static_cast<const float *>(a.q)[row * D + d]
-                                 : load_f32(static_cast<const __nv_bfloat16 *>(a.q) + row * D + d);
-  __syncthreads();
-  if (warp == 0) {
-    float x[E];
-#pragma unroll
-    for (int t = 0; t < E; ++t) x[t] = qf[lane * E + t];
-    if (a.signs) signed_hadamard<E>(x, a.signs, lane);
-    mxfp8_round_row<E>(x);
-#pragma unroll
-    for (int t = 0; t < E; ++t) qm[lane * E + t] = x[t];
-  }
-  __syncthreads();
-
-  // scores of both paths: warp w takes keys w, w + 8, ..., two at a time;
-  // lane l reads features l*E .. l*E + E - 1 of each (whole rows per load)
-  float qa[E], qb[E];
-#pragma unroll
-  for (int t = 0; t < E; ++t) {
-    qa[t] = qf[lane * E + t];
-    qb[t] = qm[lane * E + t];
-  }
-  for (int j0 = 2 * warp; j0 < a.N; j0 += 2 * kWarps) {
-    float dr[2], dm[2];
-#pragma unroll
-    for (int x = 0; x < 2; ++x) {
-      const int j = min(j0 + x, a.N - 1);
-      const float *kr = a.k_ref + (u * a.N + j) * D + lane * E;
-      const float *km = a.k_mx + (u * a.N + j) * D + lane * E;
-      dr[x] = dm[x] = 0.0f;
-#pragma unroll
-      for (int t = 0; t < E; ++t) {
-        dr[x] = fmaf(qa[t], __ldg(kr + t), dr[x]);
-        dm[x] = fmaf(qb[t], __ldg(km + t), dm[x]);
-      }
-    }
-#pragma unroll
-    for (int o = 16; o; o >>= 1)
-#pragma unroll
-      for (int x = 0; x < 2; ++x) {
-        dr[x] += __shfl_xor_sync(0xffffffffu, dr[x], o);
-        dm[x] += __shfl_xor_sync(0xffffffffu, dm[x], o);
-      }
-    if (lane == 0)
-#pragma unroll
-      for (int x = 0; x < 2; ++x)
-        if (j0 + x < a.N) {
-          s_ref[j0 + x] = a.sm_scale * dr[x];
-          s_mx[j0 + x] = a.sm_scale * dm[x];
-        }
+  for (int j = threadIdx.x; j < a.N; j += kThreads) {
+    s_ref[j] = a.s_ref[row * a.N + j];
+    s_mx[j] = a.s_mx[row * a.N + j];
   }
   __syncthreads();
 
   const int am_ref = block_argmax(s_ref, a.N, red, redi);
   const int am_mx = block_argmax(s_mx, a.N, red, redi);
-  float mx_ref = -CUDART_INF_F, mx_mx = -CUDART_INF_F;
-  for (int j = threadIdx.x; j < a.N; j += kThreads) {
-    mx_ref = fmaxf(mx_ref, s_ref[j]);
-    mx_mx = fmaxf(mx_mx, s_mx[j]);
-  }
-  mx_ref = block_max(mx_ref, red);
-  mx_mx = block_max(mx_mx, red);
+  const float mx_ref = s_ref[am_ref], mx_mx = s_mx[am_mx];
   float l_ref = 0.0f, l_mx = 0.0f;
   for (int j = threadIdx.x; j < a.N; j += kThreads) {
     l_ref += expf(s_ref[j] - mx_ref);
@@ -397,10 +474,16 @@ __global__ void __launch_bounds__(kThreads) stats_kernel(const StatsArgs a) {
 
 int stats_max_tokens() { return 16384; }
 
-size_t stats_workspace_bytes(const kvq_cache &c) {
-  const size_t one = sizeof(float) * static_cast<size_t>(c.batch) * c.kv_heads * c.n_tokens *
-                     c.head_dim;
-  return 2 * ((one + 255) & ~size_t(255));
+namespace {
+size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+}  // namespace
+
+// Key tiles (both paths) and score rows (both paths).
+size_t stats_workspace_bytes(const kvq_cache &c, int Hq, int n_q) {
+  const size_t tiles = sizeof(float) * static_cast<size_t>(c.batch) * c.kv_heads *
+                       ((c.n_tokens + 31) / 32) * 32 * c.head_dim;
+  const size_t scores = sizeof(float) * static_cast<size_t>(c.batch) * Hq * n_q * c.n_tokens;
+  return 2 * round256(tiles) + 2 * round256(scores);
 }
 
 int launch_attend_stats(const kvq_cache &c, const void *q, int q_dtype, int Hq, int n_q,
@@ -427,22 +510,31 @@ int launch_attend_stats(const kvq_cache &c, const void *q, int q_dtype, int Hq, 
   a.sm_scale = sm_scale;
   a.signs = signs;
   a.stats = stats;
-  const size_t one = (sizeof(float) * static_cast<size_t>(d.B) * d.Hkv * d.N * d.D + 255) &
-                     ~size_t(255);
-  a.k_ref = static_cast<float *>(ws);
-  a.k_mx = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + one);
-  const dim3 kgrid(static_cast<unsigned>((d.N + kWarps - 1) / kWarps),
-                   static_cast<unsigned>(d.B * d.Hkv));
+  a.T = (d.N + 31) / 32;
+  const size_t tiles = round256(sizeof(float) * static_cast<size_t>(d.B) * d.Hkv * a.T * 32 * d.D);
+  const size_t scores = round256(sizeof(float) * static_cast<size_t>(d.B) * Hq * n_q * d.N);
+  uint8_t *w = static_cast<uint8_t *>(ws);
+  a.k_ref = reinterpret_cast<float *>(w);
+  a.k_mx = reinterpret_cast<float *>(w + tiles);
+  a.s_ref = reinterpret_cast<float *>(w + 2 * tiles);
+  a.s_mx = reinterpret_cast<float *>(w + 2 * tiles + scores);
+  // about a thousand scoring CTAs, each over at least 8 key tiles
+  const long row_blocks = static_cast<long>(d.B) * Hq * ((n_q + kRows - 1) / kRows);
+  a.key_splits = static_cast<int>(
+      std::max<long>(1, std::min<long>({(1024 + row_blocks - 1) / row_blocks, a.T / 8, 65535L})));
+  const dim3 kgrid(static_cast<unsigned>(a.T), static_cast<unsigned>(d.B * d.Hkv));
+  const size_t ksmem = sizeof(float) * 2 * d.D * 33;
+  const dim3 sgrid(static_cast<unsigned>((n_q + kRows - 1) / kRows),
+                   static_cast<unsigned>(d.B * Hq), static_cast<unsigned>(a.key_splits));
   const size_t smem = sizeof(float) * 2 * static_cast<size_t>(d.N);
   const long rows = static_cast<long>(d.B) * Hq * n_q;
-  const dim3 grid(static_cast<unsigned>(rows));
   switch (d.D / 32) {
 #define KVQ_STATS_CASE(E)                                                                     \
   case E:                                                                                     \
-    launch_dependent(keys_kernel<E>, dim3(kgrid), dim3(kThreads), 0, s, a);                   \
-    cudaFuncSetAttribute(stats_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize,       \
-                         static_cast<int>(smem));                                             \
-    launch_dependent(stats_kernel<E>, dim3(grid), dim3(kThreads), smem, s, a);                \
+    cudaFuncSetAttribute(keys_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize,        \
+                         static_cast<int>(ksmem));                                            \
+    launch_dependent(keys_kernel<E>, kgrid, dim3(kThreads), ksmem, s, a);                     \
+    launch_dependent(scores_kernel<E>, sgrid, dim3(kThreads), 0, s, a);                       \
     break;
     KVQ_STATS_CASE(1)
     KVQ_STATS_CASE(2)
@@ -452,7 +544,10 @@ int launch_attend_stats(const kvq_cache &c, const void *q, int q_dtype, int Hq, 
     default:
       return -1;
   }
-  return 2;
+  cudaFuncSetAttribute(stats_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       static_cast<int>(smem));
+  launch_dependent(stats_kernel, dim3(static_cast<unsigned>(rows)), dim3(kThreads), smem, s, a);
+  return 3;
 }
 
 }  // namespace kvq

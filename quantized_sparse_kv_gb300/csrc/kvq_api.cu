@@ -269,7 +269,7 @@ kvq_status kv_attend_stats(const kvq_cache *cache, const void *q, int32_t q_dtyp
   const int d = cache->head_dim;
   if ((d & (d - 1)) != 0 || cache->n_tokens > kvq::stats_max_tokens()) return KVQ_ERR_UNSUPPORTED;
   if (static_cast<long>(cache->batch) * q_heads * n_q > 0x7fffffffL) return KVQ_ERR_UNSUPPORTED;
-  const size_t need = kvq::stats_workspace_bytes(*cache);
+  const size_t need = kvq::stats_workspace_bytes(*cache, q_heads, n_q);
   if (!workspace) {
     *ws_bytes = need;
     return KVQ_OK;

@@ -108,7 +108,7 @@ int launch_attend_chunk(const kvq_cache &c, const void *q, int Hq, int n_q, floa
 
 // attend_stats.cu: observer statistics of attention rows (kv_attend_stats).
 int stats_max_tokens();
-size_t stats_workspace_bytes(const kvq_cache &c);
+size_t stats_workspace_bytes(const kvq_cache &c, int Hq, int n_q);
 int launch_attend_stats(const kvq_cache &c, const void *q, int q_dtype, int Hq, int n_q,
                         float sm_scale, const float *signs, float *stats, void *ws,
                         cudaStream_t s);
