@@ -70,6 +70,10 @@ struct ChunkArgs {
   // block-shared candidate lists: 0, or the 128-row query tiles per list;
   // K/V row set of CTA (x, y) is then list y * lists_per_head + x / tiles_per_list
   int tiles_per_list, lists_per_head;
+  // key tiles below hist_tiles come from the K/V maps; the later ones from
+  // the window maps, at row key - win_off (an int4-history cache whose
+  // expanded history is followed by its bf16 window read in place)
+  int hist_tiles, win_off;
   float scale_log2;
   void *out;
   int out_dtype;
@@ -371,7 +375,9 @@ __device__ __forceinline__ void softmax_pass_head(uint32_t taddr, int valid, int
 __global__ void __launch_bounds__(384, 1)
     chunk_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
-                      const __grid_constant__ CUtensorMap tm_v, const ChunkArgs a) {
+                      const __grid_constant__ CUtensorMap tm_v,
+                      const __grid_constant__ CUtensorMap tm_kw,
+                      const __grid_constant__ CUtensorMap tm_vw, const ChunkArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // dynamic shared memory is only 16-byte aligned: round up to 1024
   const uint32_t base = smem_u32(smem_raw);
@@ -437,8 +443,11 @@ __global__ void __launch_bounds__(384, 1)
         if (cta_aborted(sm)) break;
         const uint32_t fb = smem_u32(&sm.k_full[st]);
         mbar_arrive_expect_tx(fb, kTileBytes);
-        tma_load_3d(smem_u32(sm.k[st]), &tm_k, 0, kj * kBN, hkv, fb);
-        tma_load_3d(smem_u32(sm.k[st]) + kHalfBytes, &tm_k, 64, kj * kBN, hkv, fb);
+        const bool hist = kj < a.hist_tiles;
+        const CUtensorMap *mk = hist ? &tm_k : &tm_kw;
+        const int ky = hist ? kj * kBN : kj * kBN - a.win_off;
+        tma_load_3d(smem_u32(sm.k[st]), mk, 0, ky, hkv, fb);
+        tma_load_3d(smem_u32(sm.k[st]) + kHalfBytes, mk, 64, ky, hkv, fb);
       }
       // drain: the copies of the last stages must land before the CTA exits
       mbar_wait(qb, 0, 2000000000ull);
@@ -455,8 +464,11 @@ __global__ void __launch_bounds__(384, 1)
         if (cta_aborted(sm)) break;
         const uint32_t fb = smem_u32(&sm.v_full[st]);
         mbar_arrive_expect_tx(fb, kTileBytes);
-        tma_load_3d(smem_u32(sm.v[st]), &tm_v, 0, vj * kBN, hkv, fb);
-        tma_load_3d(smem_u32(sm.v[st]) + kHalfBytes, &tm_v, 64, vj * kBN, hkv, fb);
+        const bool hist = vj < a.hist_tiles;
+        const CUtensorMap *mv = hist ? &tm_v : &tm_vw;
+        const int vy = hist ? vj * kBN : vj * kBN - a.win_off;
+        tma_load_3d(smem_u32(sm.v[st]), mv, 0, vy, hkv, fb);
+        tma_load_3d(smem_u32(sm.v[st]) + kHalfBytes, mv, 64, vy, hkv, fb);
       }
       for (int d = (vj > kVStages ? vj - kVStages : 0); d < vj; ++d)
         mbar_wait(smem_u32(&sm.v_full[d % kVStages]), (d / kVStages) & 1, 2000000000ull);
@@ -790,10 +802,13 @@ __global__ void __launch_bounds__(256) q_mxfp8_round_kernel(const __nv_bfloat16 
 // ------------------------------------------------------------------ int4 history
 // A cache whose older tokens are grouped int4 (residual-window page, section
 // 固定預算) and whose last R tokens are a bf16 window -- the layout of the
-// Catnip study's cache with the sink and recent regions compressed -- is
-// first expanded to contiguous bf16 K and V rows [unit][N][128] in workspace:
-// x = code * s, exact in fp32, rounded once to bf16 (the precision the tensor
-// cores take anyway). The chunk kernel then reads one key range.
+// Catnip study's cache with the sink and recent regions compressed -- has the
+// key tiles that hold int4 tokens expanded to contiguous bf16 K and V rows
+// [unit][N][128] in workspace (N here: the history rounded up to whole
+// 128-key tiles, the first window rows of the last one included): x = code * s,
+// exact in fp32, rounded once to bf16 (the precision the tensor cores take
+// anyway). The chunk kernel reads those tiles from workspace and the later
+// ones from the window in place.
 struct HistArgs {
   const uint8_t *k_codes;   // [unit][Gk][32][64]
   const float *k_scales;    // [unit][Gk][128]
@@ -801,7 +816,7 @@ struct HistArgs {
   const float *v_scales;    // [unit][cut][4]
   const uint16_t *k_window, *v_window;  // [unit][R][128] bf16
   uint16_t *k_out, *v_out;  // [unit][N][128] bf16
-  int N, R, cut, Gk;
+  int N, R, cut, Gk;        // N: rows expanded
   int Gs, Vs, Ws;  // per-unit strides: K groups, V rows, window rows
 };
 
@@ -980,11 +995,19 @@ bool chunk_supported(const kvq_cache &c, int q_dtype, int Hq, int n_q) {
 
 static bool has_history(const kvq_cache &c) { return c.recent < c.n_tokens; }
 
+// Rows of an int4-history cache expanded to bf16: the key tiles that hold an
+// int4 token, i.e. the history rounded up to whole tiles (the first window
+// rows of the last such tile included); later tiles are read from the window.
+static int expanded_rows(const kvq_cache &c) {
+  const int cut = c.n_tokens - c.recent;
+  return std::min(c.n_tokens, (cut + kBN - 1) / kBN * kBN);
+}
+
 // MXFP8: bf16 copies of K and of the MXFP8-rounded Q, each 256-byte aligned.
-// int4 history: bf16 K and V of every token.
+// int4 history: bf16 K and V of the expanded rows.
 size_t chunk_workspace_bytes(const kvq_cache &c, int Hq, int n_q) {
   if (has_history(c)) {
-    const size_t kb = static_cast<size_t>(c.batch) * c.kv_heads * c.n_tokens * kDim * 2;
+    const size_t kb = static_cast<size_t>(c.batch) * c.kv_heads * expanded_rows(c) * kDim * 2;
     return 2 * ((kb + 255) & ~size_t(255));
   }
   if (c.kwin_dtype != KVQ_MXFP8) return 0;
@@ -1000,9 +1023,12 @@ int launch_attend_chunk(const kvq_cache &c, const void *q, int Hq, int n_q, floa
                         float *mass, void *ws, const KernelCtl &ctl, cudaStream_t s) {
   int launches = 1;
   const void *kptr = c.k_window, *vptr = c.v_window, *qptr = q;
+  int hist_rows = 0;  // rows read from the expanded history (0: none)
   if (has_history(c)) {
     const CacheDims d = dims_of(c);
-    const size_t kb = (static_cast<size_t>(d.B) * d.Hkv * d.N * kDim * 2 + 255) & ~size_t(255);
+    hist_rows = expanded_rows(c);
+    const size_t kb =
+        (static_cast<size_t>(d.B) * d.Hkv * hist_rows * kDim * 2 + 255) & ~size_t(255);
     HistArgs h;
     h.k_codes = c.k_codes;
     h.k_scales = c.k_scales;
@@ -1012,14 +1038,14 @@ int launch_attend_chunk(const kvq_cache &c, const void *q, int Hq, int n_q, floa
     h.v_window = static_cast<const uint16_t *>(c.v_window);
     h.k_out = static_cast<uint16_t *>(ws);
     h.v_out = reinterpret_cast<uint16_t *>(static_cast<uint8_t *>(ws) + kb);
-    h.N = d.N;
+    h.N = hist_rows;
     h.R = d.R;
     h.cut = d.cut;
     h.Gk = d.Gk;
     h.Gs = d.Gs;
     h.Vs = d.Vs;
     h.Ws = d.Ws;
-    const dim3 grid(static_cast<unsigned>((d.N * 16 + 255) / 256),
+    const dim3 grid(static_cast<unsigned>((hist_rows * 16 + 255) / 256),
                     static_cast<unsigned>(d.B * d.Hkv));
     launch_dependent(history_to_bf16_kernel, grid, dim3(256), 0, s, h);
     kptr = h.k_out;
@@ -1040,15 +1066,27 @@ int launch_attend_chunk(const kvq_cache &c, const void *q, int Hq, int n_q, floa
     qptr = qb;
     launches += 2;
   }
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, tkw, tvw;
   // expanded K and V (history, MXFP8) are tight; an all-window cache keeps
   // its window stride
-  const long k_rows = kptr == c.k_window ? dims_of(c).Ws : c.n_tokens;
-  const long v_rows = vptr == c.v_window ? dims_of(c).Ws : c.n_tokens;
+  const int Ws = dims_of(c).Ws;
+  const int rows = hist_rows ? hist_rows : c.n_tokens;
+  const long k_rows = kptr == c.k_window ? Ws : rows;
+  const long v_rows = vptr == c.v_window ? Ws : rows;
   if (!make_map(&tq, qptr, n_q, c.batch * Hq, n_q) ||
-      !make_map(&tk, kptr, c.n_tokens, c.batch * c.kv_heads, k_rows) ||
-      !make_map(&tv, vptr, c.n_tokens, c.batch * c.kv_heads, v_rows))
+      !make_map(&tk, kptr, rows, c.batch * c.kv_heads, k_rows) ||
+      !make_map(&tv, vptr, rows, c.batch * c.kv_heads, v_rows))
     return -1;
+  // the window of an int4-history cache, read in place after the expanded tiles
+  const bool split = hist_rows > 0 && hist_rows < c.n_tokens;
+  if (split) {
+    if (!make_map(&tkw, c.k_window, c.recent, c.batch * c.kv_heads, Ws) ||
+        !make_map(&tvw, c.v_window, c.recent, c.batch * c.kv_heads, Ws))
+      return -1;
+  } else {
+    tkw = tk;
+    tvw = tv;
+  }
   ChunkArgs a;
   a.n_q = n_q;
   a.n_kv = c.n_tokens;
@@ -1063,12 +1101,14 @@ int launch_attend_chunk(const kvq_cache &c, const void *q, int Hq, int n_q, floa
   a.ctl = ctl;
   a.tiles_per_list = 0;
   a.lists_per_head = 0;
+  a.hist_tiles = split ? hist_rows / kBN : 0x7fffffff;
+  a.win_off = split ? c.n_tokens - c.recent : 0;
   static_assert(sizeof(ChunkSmem) + 1024 <= 232448, "chunk kernel shared memory");
   const size_t smem = sizeof(ChunkSmem) + 1024;
   cudaFuncSetAttribute(chunk_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        static_cast<int>(smem));
   dim3 grid((n_q + kBM - 1) / kBM, c.batch * Hq);
-  launch_dependent(chunk_bf16_kernel, grid, dim3(384), smem, s, tq, tk, tv, a);
+  launch_dependent(chunk_bf16_kernel, grid, dim3(384), smem, s, tq, tk, tv, tkw, tvw, a);
   return launches;
 }
 
@@ -1122,6 +1162,7 @@ int launch_candidate_lists(const kvq_cache &c, const void *q, int Hq, int n_q,
       !make_map(&tk, g.k_out, C, static_cast<int>(lists), C) ||
       !make_map(&tv, g.v_out, C, static_cast<int>(lists), C))
     return -1;
+  const CUtensorMap tkw = tk, tvw = tv;  // no window read in place
   ChunkArgs a;
   a.n_q = n_q;
   a.n_kv = C;
@@ -1136,11 +1177,13 @@ int launch_candidate_lists(const kvq_cache &c, const void *q, int Hq, int n_q,
   a.ctl = ctl;
   a.tiles_per_list = block_q / kBM;
   a.lists_per_head = lists_per_head;
+  a.hist_tiles = 0x7fffffff;
+  a.win_off = 0;
   const size_t smem = sizeof(ChunkSmem) + 1024;
   cudaFuncSetAttribute(chunk_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        static_cast<int>(smem));
   dim3 grid((n_q + kBM - 1) / kBM, d.B * Hq);
-  launch_dependent(chunk_bf16_kernel, grid, dim3(384), smem, s, tq, tk, tv, a);
+  launch_dependent(chunk_bf16_kernel, grid, dim3(384), smem, s, tq, tk, tv, tkw, tvw, a);
   return 2;
 }
 
@@ -1202,6 +1245,7 @@ int launch_region_drop(const kvq_cache &c, const void *q, int Hq, int n_q, const
       !make_map(&tk, g.k_out, C, static_cast<int>(units), C) ||
       !make_map(&tv, g.v_out, C, static_cast<int>(units), C))
     return -1;
+  const CUtensorMap tkw = tk, tvw = tv;  // no window read in place
   ChunkArgs a;
   a.n_q = n_q;
   a.n_kv = C;
@@ -1216,11 +1260,13 @@ int launch_region_drop(const kvq_cache &c, const void *q, int Hq, int n_q, const
   a.ctl = ctl;
   a.tiles_per_list = 0;
   a.lists_per_head = 0;
+  a.hist_tiles = 0x7fffffff;
+  a.win_off = 0;
   const size_t smem = sizeof(ChunkSmem) + 1024;
   cudaFuncSetAttribute(chunk_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        static_cast<int>(smem));
   dim3 grid((n_q + kBM - 1) / kBM, d.B * Hq);
-  launch_dependent(chunk_bf16_kernel, grid, dim3(384), smem, s, tq, tk, tv, a);
+  launch_dependent(chunk_bf16_kernel, grid, dim3(384), smem, s, tq, tk, tv, tkw, tvw, a);
   return 2;
 }
 

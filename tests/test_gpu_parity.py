@@ -366,6 +366,7 @@ def history_reference(q, k, v, recent, bounds):
     (2, 2, 200, 600, 250, [0, 150, 350, 600], 0.0),
     (4, 2, 130, 1000, 0, [0, 390, 999, 1000], 0.0),
     (2, 1, 333, 777, 100, None, 3.0),
+    (2, 2, 130, 640, 256, [0, 100, 384, 640], 0.0),   # window starts on a key tile
 ])
 def test_chunk_int4_history_matches_oracle(kvq, hq, hkv, n_q, n_kv, recent, bounds, conc):
     # int4 groups for the older tokens (a ragged last K group where N - R is
