@@ -57,13 +57,13 @@ struct __align__(1024) ChunkSmem {
   int abort_flag;
 };
 
-// Group B's row state for the final merge, laid over K stage 0, which no copy
-// or MMA touches any more once group B has seen its last PV complete.
+// The two groups' row states for the final merge, laid over K stage 0, which
+// no copy or MMA touches any more once a group has seen its last PV complete.
 struct MergeState {
   float m[kBM], l[kBM];
   float r[kMaxRegions][kBM];
 };
-static_assert(sizeof(MergeState) <= kTileBytes, "merge state fits a K stage");
+static_assert(2 * sizeof(MergeState) <= kTileBytes, "merge states fit a K stage");
 
 struct ChunkArgs {
   int n_q, n_kv, q_heads, kv_group, n_tiles;
@@ -636,38 +636,38 @@ __global__ void __launch_bounds__(384, 1)
         }
       }
     }
-    // ---- epilogue: group B hands its row state to group A, A merges and stores
-    const bool last_ok =
-        ok && my_tiles > 0 &&
-        wait_or_abort(sm, smem_u32(&sm.o_done[g]), (my_tiles - 1) & 1, a.ctl);
-    // only after its last PV completed may group B write over K stage 0 (a
-    // group B without tiles writes nothing; group A then ignores it)
-    MergeState &ms = *reinterpret_cast<MergeState *>(sm.k[0]);
-    if (g == 1 && last_ok) {
-      ms.m[row] = m_used;
-      ms.l[row] = l;
+    // ---- epilogue: each group leaves its row state in shared memory, then
+    // merges both groups' O for half of the columns (group g: 64g .. 64g + 63)
+    const bool mine_ok =
+        ok && (my_tiles == 0 ||
+               wait_or_abort(sm, smem_u32(&sm.o_done[g]), (my_tiles - 1) & 1, a.ctl));
+    // A group's last PV is issued after the last QK, so once it has completed
+    // no MMA reads K stage 0 any more and the group may write over it.
+    MergeState *ms = reinterpret_cast<MergeState *>(sm.k[0]);
+    if (mine_ok && my_tiles > 0) {
+      ms[g].m[row] = m_used;
+      ms[g].l[row] = l;
 #pragma unroll
-      for (int k = 0; k < kMaxRegions; ++k) ms.r[k][row] = rsum[k];
+      for (int k = 0; k < kMaxRegions; ++k) ms[g].r[k][row] = rsum[k];
     }
     tc_fence_before();
     asm volatile("bar.sync 2, 256;" ::: "memory");
-    const int tiles_b = nt >> 1;
-    if (g == 0 && last_ok &&
-        (tiles_b == 0 ||
-         wait_or_abort(sm, smem_u32(&sm.o_done[1]), (tiles_b - 1) & 1, a.ctl))) {
+    const int other = 1 - g;
+    const int other_tiles = (nt - other + 1) >> 1;
+    if (mine_ok &&
+        (other_tiles == 0 ||
+         wait_or_abort(sm, smem_u32(&sm.o_done[other]), (other_tiles - 1) & 1, a.ctl))) {
       tc_fence_after();
-      const bool have_b = nt > 1;  // group B processed at least one tile
-      const float mb = have_b ? ms.m[row] : -CUDART_INF_F;
-      const float mm = fmaxf(m_used, mb);
-      const float fa = exp2f(m_used - mm);
+      const bool have_b = nt > 1;  // group B processed at least one tile (group A always)
+      const float ma = ms[0].m[row], mb = have_b ? ms[1].m[row] : -CUDART_INF_F;
+      const float mm = fmaxf(ma, mb);
+      const float fa = exp2f(ma - mm);
       const float fb = have_b ? exp2f(mb - mm) : 0.0f;
-      const float lt = fa * l + (have_b ? fb * ms.l[row] : 0.0f);
-      const float inv = 1.0f / lt;
-      const float oa = fa, ob = have_b ? fb : 0.0f;
+      const float inv = 1.0f / (fa * ms[0].l[row] + (have_b ? fb * ms[1].l[row] : 0.0f));
       const int qrow = q0 + row;
       const long obase = (static_cast<long>(hq) * a.n_q + qrow) * kDim;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 2 * g; c < 2 * g + 2; ++c) {
         float va[32], vb[32];
         tmem_ld32(t_o(0) + lane_off + 32u * c, va);
         if (have_b) tmem_ld32(t_o(1) + lane_off + 32u * c, vb);
@@ -675,7 +675,7 @@ __global__ void __launch_bounds__(384, 1)
         reg_fence(va);
         if (have_b) reg_fence(vb);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) va[e] = (oa * va[e] + (have_b ? ob * vb[e] : 0.0f)) * inv;
+        for (int e = 0; e < 32; ++e) va[e] = (fa * va[e] + (have_b ? fb * vb[e] : 0.0f)) * inv;
         if (qrow < a.n_q) {
           if (a.out_dtype == KVQ_F32) {
             float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(a.out) + obase + 32 * c);
@@ -694,10 +694,10 @@ __global__ void __launch_bounds__(384, 1)
           }
         }
       }
-      if (a.mass && qrow < a.n_q)
+      if (g == 0 && a.mass && qrow < a.n_q)
         for (int k = 0; k < a.reg.n && k < kMaxRegions; ++k)
           a.mass[(static_cast<long>(hq) * a.n_q + qrow) * a.reg.n + k] =
-              (fa * rsum[k] + (have_b ? fb * ms.r[k][row] : 0.0f)) * inv;
+              (fa * ms[0].r[k][row] + (have_b ? fb * ms[1].r[k][row] : 0.0f)) * inv;
     }
   }
   tc_fence_before();
