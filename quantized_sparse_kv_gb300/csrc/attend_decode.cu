@@ -395,6 +395,45 @@ __device__ __forceinline__ void load_q(const DecodeArgs &a, int u, int g, int t,
     for (int j = 0; j < 4; ++j) qh[i][j] = pack_h2(qr[8 * i + j], qr[8 * i + 4 + j]);
 }
 
+// A bf16 query slice (this lane's 32 features of head g) as loaded, so that
+// the next unit's loads can be issued before the current unit's merge and
+// their latency hidden by it.
+struct QRaw {
+  uint4 w[4];
+};
+
+__device__ __forceinline__ void load_q_raw(const DecodeArgs &a, int u, int g, int t, QRaw &r) {
+  if (a.q_dtype == KVQ_F32) return;  // fp32 rows are loaded when converted
+  const long row = static_cast<long>(u) * kHeads + g;
+  const uint4 *p = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(a.q) + row * kD +
+                                                   32 * t);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) r.w[i] = p[i];
+}
+
+// load_q from a prefetched bf16 slice (the same values).
+__device__ __forceinline__ void q_from_raw(const DecodeArgs &a, int u, int g, int t,
+                                           const QRaw &r, uint32_t (&qh)[4][4]) {
+  if (a.q_dtype == KVQ_F32) {
+    load_q(a, u, g, t, qh);
+    return;
+  }
+  float qr[32];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t w[4] = {r.w[i].x, r.w[i].y, r.w[i].z, r.w[i].w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      qr[8 * i + 2 * j] = __uint_as_float(w[j] << 16) * a.scale_log2;
+      qr[8 * i + 2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u) * a.scale_log2;
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) qh[i][j] = pack_h2(qr[8 * i + j], qr[8 * i + 4 + j]);
+}
+
 __device__ __forceinline__ bool aborted_flag(DecodeSmem &sm) {
   return *reinterpret_cast<volatile int *>(&sm.abort_flag) != 0;
 }
@@ -499,10 +538,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const Deco
   const int g = lane >> 2, t = lane & 3;
   WarpState st;
   uint32_t qh[4][4];
+  QRaw qraw;
+  load_q_raw(a, u_first, g, t, qraw);
   int k = 0;  // CTA-relative item index
   for (int u = u_first; u * a.ipu < hi; ++u) {
     state_reset(st);
-    load_q(a, u, g, t, qh);
+    q_from_raw(a, u, g, t, qraw, qh);
     const int u_end = min(hi, (u + 1) * a.ipu) - lo;  // CTA-relative end of unit u
     int j = lo + k - u * a.ipu;                        // item index within unit u
     bool aborted = false;
@@ -542,6 +583,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const Deco
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&sm.empty[s]));
     }
+    // the next unit's query rows are in flight during the merge
+    if ((u + 1) * a.ipu < hi) load_q_raw(a, u + 1, g, t, qraw);
     // ---- merge the 4 warps' states for unit u and write one partial
     float l0 = st.l[0], l1 = st.l[1];
 #pragma unroll
