@@ -371,6 +371,8 @@ struct __align__(16) DecodeSmem {
   float red_o[kConsumers][kHeads / 2][kD];  // one half of the heads at a time
   float red_m[kConsumers][kHeads];
   float red_l[kConsumers][kHeads];
+  float red_c[kConsumers][kHeads];  // merge weight of warp w's state for head h
+  float red_mx[kHeads], red_ls[kHeads];
   uint64_t full[kStages];
   uint64_t empty[kStages];
   int abort_flag;
@@ -598,37 +600,50 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const Deco
       sm.red_l[warp][2 * t] = l0;
       sm.red_l[warp][2 * t + 1] = l1;
     }
+    asm volatile("bar.sync 1, %0;" ::"n"(kConsumers * 32));
+    // per head: the maximum over the warps, each warp's weight and the sum
+    if (threadIdx.x < kHeads) {
+      const int h = threadIdx.x;
+      float mx = -CUDART_INF_F;
+#pragma unroll
+      for (int w = 0; w < kConsumers; ++w) mx = fmaxf(mx, sm.red_m[w][h]);
+      float lsum = 0.0f;
+#pragma unroll
+      for (int w = 0; w < kConsumers; ++w) {
+        const float c = (sm.red_m[w][h] == -CUDART_INF_F) ? 0.0f : exp2f(sm.red_m[w][h] - mx);
+        sm.red_c[w][h] = c;
+        lsum += c * sm.red_l[w][h];
+      }
+      sm.red_mx[h] = mx;
+      sm.red_ls[h] = lsum;
+    }
     // heads 0-3 live in lanes with t < 2, heads 4-7 in lanes with t >= 2:
     // merge one half at a time through red_o
+    float *part = partial_of(a, u, cta - cta_of_item(a, u * a.ipu));
     for (int half = 0; half < 2; ++half) {
       if ((t >> 1) == half) {
         const int h0 = 2 * t - 4 * half;
-#pragma unroll
-        for (int f = 0; f < 8; ++f) {
-          sm.red_o[warp][h0][16 * g + f] = st.o[f][0];
-          sm.red_o[warp][h0 + 1][16 * g + f] = st.o[f][1];
-          sm.red_o[warp][h0][16 * g + 8 + f] = st.o[f][2];
-          sm.red_o[warp][h0 + 1][16 * g + 8 + f] = st.o[f][3];
-        }
+        float4 *ra = reinterpret_cast<float4 *>(&sm.red_o[warp][h0][16 * g]);
+        float4 *rb = reinterpret_cast<float4 *>(&sm.red_o[warp][h0 + 1][16 * g]);
+        ra[0] = make_float4(st.o[0][0], st.o[1][0], st.o[2][0], st.o[3][0]);
+        ra[1] = make_float4(st.o[4][0], st.o[5][0], st.o[6][0], st.o[7][0]);
+        ra[2] = make_float4(st.o[0][2], st.o[1][2], st.o[2][2], st.o[3][2]);
+        ra[3] = make_float4(st.o[4][2], st.o[5][2], st.o[6][2], st.o[7][2]);
+        rb[0] = make_float4(st.o[0][1], st.o[1][1], st.o[2][1], st.o[3][1]);
+        rb[1] = make_float4(st.o[4][1], st.o[5][1], st.o[6][1], st.o[7][1]);
+        rb[2] = make_float4(st.o[0][3], st.o[1][3], st.o[2][3], st.o[3][3]);
+        rb[3] = make_float4(st.o[4][3], st.o[5][3], st.o[6][3], st.o[7][3]);
       }
       asm volatile("bar.sync 1, %0;" ::"n"(kConsumers * 32));
-      float *part = partial_of(a, u, cta - cta_of_item(a, u * a.ipu));
       for (int i = threadIdx.x; i < (kHeads / 2) * kD; i += kConsumers * 32) {
         const int hh = i / kD, d = i % kD, h = 4 * half + hh;
-        float mx = -CUDART_INF_F;
+        float acc = 0.0f;
 #pragma unroll
-        for (int w = 0; w < kConsumers; ++w) mx = fmaxf(mx, sm.red_m[w][h]);
-        float acc = 0.0f, lsum = 0.0f;
-#pragma unroll
-        for (int w = 0; w < kConsumers; ++w) {
-          const float c = (sm.red_m[w][h] == -CUDART_INF_F) ? 0.0f : exp2f(sm.red_m[w][h] - mx);
-          acc += c * sm.red_o[w][hh][d];
-          lsum += c * sm.red_l[w][h];
-        }
+        for (int w = 0; w < kConsumers; ++w) acc += sm.red_c[w][h] * sm.red_o[w][hh][d];
         part[h * kPartFloats + d] = acc;
         if (d == 0) {
-          part[h * kPartFloats + kD] = mx;
-          part[h * kPartFloats + kD + 1] = lsum;
+          part[h * kPartFloats + kD] = sm.red_mx[h];
+          part[h * kPartFloats + kD + 1] = sm.red_ls[h];
         }
       }
       asm volatile("bar.sync 1, %0;" ::"n"(kConsumers * 32));
