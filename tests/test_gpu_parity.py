@@ -102,6 +102,27 @@ def test_pack_edge_values_bitexact(kvq):
     assert_pack_bitexact(cache, ref)
 
 
+def test_pack_near_ties_and_tiny_scales_bitexact(kvq):
+    # quotients on and a hair off half-integers (scale 1 and 2^-20), groups
+    # whose scale is subnormal (its reciprocal large or infinite), and the
+    # largest finite values
+    k = np.zeros((1, 1, 192, 32), np.float32)
+    base = np.array([2.5, 3.5, -2.5, -0.5, 0.5, 6.5, -6.5, 1.5], np.float32)
+    col = np.concatenate([base, np.nextafter(base, np.float32(np.inf)),
+                          np.nextafter(base, np.float32(-np.inf)), [7.0] * 8]).astype(np.float32)
+    k[0, 0, :32, 0] = col
+    k[0, 0, 32:64, 1] = col * np.float32(2.0 ** -20)
+    k[0, 0, 64:96, 2] = col * np.float32(2.0 ** -130)     # scale 2^-130: subnormal
+    k[0, 0, 96:128, 3] = col * np.float32(1e-44 / 7.0)    # scale rounds to the smallest subnormal
+    k[0, 0, 128:160, 4] = np.float32(3.4e38) * np.linspace(-1, 1, 32, dtype=np.float32)
+    k[0, 0, 160:, 5] = synth.normal_numpy(14, (32,)) * np.float32(1e-38)
+    v = np.ascontiguousarray(np.swapaxes(k, 2, 3)[:, :, :, :192].repeat(1, axis=2))
+    v = np.ascontiguousarray(np.tile(v[:, :, :, :32], (1, 1, 6, 1))[:, :, :192])
+    cache = kvq.pack(torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda(), 0, "f32")
+    _, ref = oracle_pack(k, v, 0, "f32")
+    assert_pack_bitexact(cache, ref)
+
+
 def test_pack_mxfp8_window_bitexact(kvq):
     shape = (1, 2, 70, 128)
     k = O.round_to_bf16(synth.normal_numpy(12, shape) * np.logspace(-3, 3, 128, dtype=np.float32))
