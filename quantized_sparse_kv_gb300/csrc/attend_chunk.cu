@@ -756,7 +756,14 @@ __global__ void mxfp8_to_bf16_kernel(const uint8_t *__restrict__ codes,
 // Q: bf16 -> MXFP8 rounding -> bf16. Four lanes per 32-feature block, 8
 // values each (16-byte loads and stores); the block maximum takes two
 // shuffles, after which every value follows the rule kv_pack applies to an
-// MXFP8 K window (mxfp8_round_warp gives the same values with a lane each).
+// MXFP8 K window (mxfp8_round_warp gives the same values with a lane each),
+// in exact steps: the block exponent ex = floor(log2 amax) - 8 from the float
+// bits (frexpf for a zero, subnormal or non-finite maximum); y = x * 2^-ex,
+// exact while normal (the power of two is always normal here, ex <= 119) and
+// rounded like ldexpf below that, where the code is 0 anyway; E4M3 with
+// saturation, two values per conversion; back through the exact E4M3 -> f16
+// conversion and a multiplication by 2^ex, exact since an E4M3 value has at
+// most 4 significant bits and the result stays above 2^-136.
 __global__ void __launch_bounds__(256) q_mxfp8_round_kernel(const __nv_bfloat16 *__restrict__ q,
                                                             long blocks,
                                                             __nv_bfloat16 *__restrict__ out) {
@@ -778,23 +785,30 @@ __global__ void __launch_bounds__(256) q_mxfp8_round_kernel(const __nv_bfloat16 
   amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
   amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
   if (!live) return;
-  int ex = -127;
-  if (amax > 0.0f) {
-    int f;
-    frexpf(amax, &f);
-    ex = max(-127, min(127, f - 1 - 8));
+  const int be = static_cast<int>(__float_as_uint(amax) >> 23);  // biased exponent (amax >= 0)
+  int ex;
+  if (be >= 1 && be <= 254) {
+    ex = max(-127, be - 135);  // frexp exponent be - 126, minus 1 and 8
+  } else {
+    ex = -127;
+    if (amax > 0.0f) {
+      int f;
+      frexpf(amax, &f);
+      ex = max(-127, min(127, f - 1 - 8));
+    }
   }
+  const float down = __uint_as_float(static_cast<uint32_t>(127 - ex) << 23);  // 2^-ex
+  const float up = e8m0_scale(static_cast<uint32_t>(ex + 127));             // 2^ex
   uint32_t o[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    float r[2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const uint8_t c = static_cast<uint8_t>(
-          __nv_cvt_float_to_fp8(ldexpf(x[2 * j + h], -ex), __NV_SATFINITE, __NV_E4M3));
-      r[h] = mxfp8_value(c, static_cast<uint8_t>(ex + 127));
-    }
-    o[j] = pack_bf16x2(r[0], r[1]);
+    const __nv_fp8x2_storage_t c = __nv_cvt_float2_to_fp8x2(
+        make_float2(__fmul_rn(x[2 * j], down), __fmul_rn(x[2 * j + 1], down)), __NV_SATFINITE,
+        __NV_E4M3);
+    uint32_t f16x2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(f16x2) : "h"(static_cast<unsigned short>(c)));
+    const float2 f = __half22float2(*reinterpret_cast<__half2 *>(&f16x2));
+    o[j] = pack_bf16x2(__fmul_rn(f.x, up), __fmul_rn(f.y, up));
   }
   reinterpret_cast<uint4 *>(out)[tid] = make_uint4(o[0], o[1], o[2], o[3]);
 }
