@@ -756,14 +756,8 @@ __global__ void mxfp8_to_bf16_kernel(const uint8_t *__restrict__ codes,
 // Q: bf16 -> MXFP8 rounding -> bf16. Four lanes per 32-feature block, 8
 // values each (16-byte loads and stores); the block maximum takes two
 // shuffles, after which every value follows the rule kv_pack applies to an
-// MXFP8 K window (mxfp8_round_warp gives the same values with a lane each),
-// in exact steps: the block exponent ex = floor(log2 amax) - 8 from the float
-// bits (frexpf for a zero, subnormal or non-finite maximum); y = x * 2^-ex,
-// exact while normal (the power of two is always normal here, ex <= 119) and
-// rounded like ldexpf below that, where the code is 0 anyway; E4M3 with
-// saturation, two values per conversion; back through the exact E4M3 -> f16
-// conversion and a multiplication by 2^ex, exact since an E4M3 value has at
-// most 4 significant bits and the result stays above 2^-136.
+// MXFP8 K window in the exact steps of mxfp8_round_warp, two values per E4M3
+// conversion.
 __global__ void __launch_bounds__(256) q_mxfp8_round_kernel(const __nv_bfloat16 *__restrict__ q,
                                                             long blocks,
                                                             __nv_bfloat16 *__restrict__ out) {
@@ -785,20 +779,8 @@ __global__ void __launch_bounds__(256) q_mxfp8_round_kernel(const __nv_bfloat16 
   amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
   amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
   if (!live) return;
-  const int be = static_cast<int>(__float_as_uint(amax) >> 23);  // biased exponent (amax >= 0)
-  int ex;
-  if (be >= 1 && be <= 254) {
-    ex = max(-127, be - 135);  // frexp exponent be - 126, minus 1 and 8
-  } else {
-    ex = -127;
-    if (amax > 0.0f) {
-      int f;
-      frexpf(amax, &f);
-      ex = max(-127, min(127, f - 1 - 8));
-    }
-  }
-  const float down = __uint_as_float(static_cast<uint32_t>(127 - ex) << 23);  // 2^-ex
-  const float up = e8m0_scale(static_cast<uint32_t>(ex + 127));             // 2^ex
+  const int ex = mxfp8_block_exp(amax);
+  const float down = pow2_of(-ex), up = pow2_of(ex);
   uint32_t o[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) {

@@ -120,18 +120,10 @@ __device__ __forceinline__ void mxfp8_round_row(float (&x)[E]) {
   for (int t = 0; t < E; ++t) amax = fmaxf(amax, fabsf(x[t]));
 #pragma unroll
   for (int o = 1; o < 32 / E; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-  int e = -127;
-  if (amax > 0.0f) {
-    int ex;
-    frexpf(amax, &ex);
-    e = max(-127, min(127, ex - 1 - 8));
-  }
+  const int e = mxfp8_block_exp(amax);
+  const float down = pow2_of(-e), up = pow2_of(e);
 #pragma unroll
-  for (int t = 0; t < E; ++t) {
-    const uint8_t c = static_cast<uint8_t>(
-        __nv_cvt_float_to_fp8(ldexpf(x[t], -e), __NV_SATFINITE, __NV_E4M3));
-    x[t] = mxfp8_value(c, static_cast<uint8_t>(e + 127));
-  }
+  for (int t = 0; t < E; ++t) x[t] = __fmul_rn(e4m3_value(mxfp8_code(x[t], down)), up);
 }
 
 // Both workspace copies of the 32 keys of tile blockIdx.x of unit

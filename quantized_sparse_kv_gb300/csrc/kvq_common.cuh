@@ -194,19 +194,40 @@ __device__ __forceinline__ float mxfp8_value(uint8_t code, uint8_t e8m0) {
   return ldexpf((code & 0x80) ? -mag : mag, static_cast<int>(e8m0) - 127);
 }
 
+// MXFP8 (E4M3 elements, one E8M0 scale 2^e per 32-value block, the OCP MX
+// rule): e = clamp(floor(log2 amax) - 8, -127, 127), -127 for a zero block.
+// The exponent is read from the float bits when amax is normal (frexpf for a
+// subnormal or non-finite maximum), so every step below is exact: x * 2^-e
+// (the power of two is normal since e <= 119; a product below the normal
+// range, rounded as ldexpf would, has code 0), the saturating conversion to
+// E4M3, the exact E4M3 -> f16 conversion back, and the product with 2^e (an
+// E4M3 value has at most 4 significant bits and the result stays above 2^-136).
+__device__ __forceinline__ int mxfp8_block_exp(float amax) {
+  const int be = static_cast<int>(__float_as_uint(amax) >> 23);  // biased exponent, amax >= 0
+  if (be >= 1 && be <= 254) return max(-127, be - 135);       // frexp exponent be - 126
+  if (!(amax > 0.0f)) return -127;
+  int f;
+  frexpf(amax, &f);
+  return max(-127, min(127, f - 1 - 8));
+}
+__device__ __forceinline__ float pow2_of(int e) {  // 2^e for e in [-127, 127]
+  return e > -127 ? __uint_as_float(static_cast<uint32_t>(e + 127) << 23)
+                  : __uint_as_float(0x00400000u);
+}
+__device__ __forceinline__ uint8_t mxfp8_code(float x, float down) {  // down = 2^-e
+  return static_cast<uint8_t>(__nv_cvt_float_to_fp8(__fmul_rn(x, down), __NV_SATFINITE, __NV_E4M3));
+}
+__device__ __forceinline__ float e4m3_value(uint8_t c) {
+  uint32_t f16x2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(f16x2) : "h"(static_cast<unsigned short>(c)));
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(f16x2 & 0xffffu)));
+}
+
 // Round x to MXFP8 inside a warp (lane = position in the 32-block) and return
 // the dequantized value: the same rule kv_pack applies to an MXFP8 K window.
 __device__ __forceinline__ float mxfp8_round_warp(float x) {
-  const float amax = warp_max(fabsf(x));
-  int e = -127;
-  if (amax > 0.0f) {
-    int ex;
-    frexpf(amax, &ex);
-    e = max(-127, min(127, ex - 1 - 8));
-  }
-  const uint8_t c =
-      static_cast<uint8_t>(__nv_cvt_float_to_fp8(ldexpf(x, -e), __NV_SATFINITE, __NV_E4M3));
-  return mxfp8_value(c, static_cast<uint8_t>(e + 127));
+  const int e = mxfp8_block_exp(warp_max(fabsf(x)));
+  return __fmul_rn(e4m3_value(mxfp8_code(x, pow2_of(-e))), pow2_of(e));
 }
 
 }  // namespace kvq

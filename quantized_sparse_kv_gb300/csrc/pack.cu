@@ -239,17 +239,9 @@ __global__ void __launch_bounds__(256) window_mxfp8_kernel(const TI *__restrict_
   const int j = static_cast<int>(task % groups);
   const long u = row / R, t = row % R;
   const float val = load_f32(x + (u * N + (N - R) + t) * D + j * kGroup + lane);
-  const float amax = warp_max(fabsf(val));
-  int e = -127;
-  if (amax > 0.0f) {
-    int ex;
-    frexpf(amax, &ex);  // amax = f * 2^ex, f in [0.5, 1)
-    e = max(-127, min(127, ex - 1 - 8));
-  }
-  const float y = ldexpf(val, -e);
-  const __nv_fp8_storage_t c = __nv_cvt_float_to_fp8(y, __NV_SATFINITE, __NV_E4M3);
+  const int e = mxfp8_block_exp(warp_max(fabsf(val)));
   const long dst = u * Ws + t;
-  codes[dst * D + j * kGroup + lane] = static_cast<uint8_t>(c);
+  codes[dst * D + j * kGroup + lane] = mxfp8_code(val, pow2_of(-e));
   if (lane == 0) e8m0[dst * groups + j] = static_cast<uint8_t>(e + 127);
 }
 
