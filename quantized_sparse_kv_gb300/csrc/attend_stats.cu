@@ -304,67 +304,86 @@ __device__ __forceinline__ int block_argmax(const float *s, int n, float *red, i
   return bi;
 }
 
-// Bits of the k-th largest of x[0, n) (all x >= 0, 1 <= k <= n): four rounds
-// of a 256-bucket histogram over the next 8 bits of the keys that still
-// match the chosen prefix.
-__device__ uint32_t kth_largest_bits(const float *x, int n, int k, uint32_t *hist,
-                                     uint32_t *sel) {
-  uint32_t prefix = 0u, mask = 0u;
-#pragma unroll 1
-  for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int i = threadIdx.x; i < 256; i += kThreads) hist[i] = 0u;
-    __syncthreads();
-    for (int i = threadIdx.x; i < n; i += kThreads) {
-      const uint32_t b = __float_as_uint(x[i]);
-      if ((b & mask) == prefix) atomicAdd(&hist[(b >> shift) & 255u], 1u);
-    }
-    __syncthreads();
-    if (threadIdx.x < 32) {
-      // the bucket d holding the k-th largest: count above d < k <= count
-      // above d + hist[d]; lane l owns buckets 8l .. 8l + 7
-      const int lane = threadIdx.x;
-      const uint32_t kk = static_cast<uint32_t>(k);
-      uint32_t hb[8], tot = 0u;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        hb[e] = hist[8 * lane + e];
-        tot += hb[e];
-      }
-      uint32_t above = tot;  // inclusive suffix sum over lanes >= lane
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t v = __shfl_down_sync(0xffffffffu, above, o);
-        if (lane + o < 32) above += v;
-      }
-      const uint32_t all = __shfl_sync(0xffffffffu, above, 0);
-      uint32_t cum = above - tot;  // buckets of the lanes above
-      bool found = false;
-      uint32_t fd = 0u, fk = 0u;
-#pragma unroll
-      for (int e = 7; e >= 0; --e) {
-        if (!found && cum < kk && cum + hb[e] >= kk) {
-          found = true;
-          fd = 8u * lane + e;
-          fk = kk - cum;
-        }
-        cum += hb[e];
-      }
-      if (found) {
-        sel[0] = fd;
-        sel[1] = fk;
-      }
-      if (__ballot_sync(0xffffffffu, found) == 0u && lane == 0) {
-        sel[0] = 0u;
-        sel[1] = kk - (all - hb[0]);
-      }
-    }
-    __syncthreads();
-    prefix |= sel[0] << shift;
-    mask |= 255u << shift;
-    k = static_cast<int>(sel[1]);
-    __syncthreads();
+// 256-bucket histogram of bits [shift, shift + 8) of the keys of x[0, n)
+// whose bits under `mask` equal `prefix`.
+__device__ __forceinline__ void bucket_histogram(const float *x, int n, uint32_t prefix,
+                                                 uint32_t mask, int shift, uint32_t *hist) {
+  for (int i = threadIdx.x; i < 256; i += kThreads) hist[i] = 0u;
+  __syncthreads();
+  for (int i = threadIdx.x; i < n; i += kThreads) {
+    const uint32_t b = __float_as_uint(x[i]);
+    if ((b & mask) == prefix) atomicAdd(&hist[(b >> shift) & 255u], 1u);
   }
-  return prefix;
+  __syncthreads();
+}
+
+// The bucket d holding the k-th largest key: count above d < k <= count above
+// d + hist[d]. Warp 0 scans (lane l owns buckets 8l .. 8l + 7) and leaves
+// {d, k - count above d} in sel; every thread reads it after the barrier.
+__device__ __forceinline__ void pick_bucket(const uint32_t *hist, int k, uint32_t *sel) {
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    const uint32_t kk = static_cast<uint32_t>(k);
+    uint32_t hb[8], tot = 0u;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      hb[e] = hist[8 * lane + e];
+      tot += hb[e];
+    }
+    uint32_t above = tot;  // inclusive suffix sum over lanes >= lane
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t v = __shfl_down_sync(0xffffffffu, above, o);
+      if (lane + o < 32) above += v;
+    }
+    const uint32_t all = __shfl_sync(0xffffffffu, above, 0);
+    uint32_t cum = above - tot;  // buckets of the lanes above
+    bool found = false;
+    uint32_t fd = 0u, fk = 0u;
+#pragma unroll
+    for (int e = 7; e >= 0; --e) {
+      if (!found && cum < kk && cum + hb[e] >= kk) {
+        found = true;
+        fd = 8u * lane + e;
+        fk = kk - cum;
+      }
+      cum += hb[e];
+    }
+    if (found) {
+      sel[0] = fd;
+      sel[1] = fk;
+    }
+    if (__ballot_sync(0xffffffffu, found) == 0u && lane == 0) {
+      sel[0] = 0u;
+      sel[1] = kk - (all - hb[0]);
+    }
+  }
+  __syncthreads();
+}
+
+// Bits of the k-th largest of x[0, n) (all x >= 0, 1 <= k <= n) for three
+// values of k: a radix select of four rounds of 8 bits each, the first
+// round's histogram (all keys) shared by the three.
+__device__ void kth_largest_bits3(const float *x, int n, const int (&k3)[3], uint32_t (&bits)[3],
+                                  uint32_t *hist, uint32_t *hist_top, uint32_t *sel) {
+  bucket_histogram(x, n, 0u, 0u, 24, hist_top);
+#pragma unroll 1
+  for (int which = 0; which < 3; ++which) {
+    pick_bucket(hist_top, k3[which], sel);
+    uint32_t prefix = sel[0] << 24, mask = 0xFF000000u;
+    int k = static_cast<int>(sel[1]);
+    __syncthreads();
+#pragma unroll 1
+    for (int shift = 16; shift >= 0; shift -= 8) {
+      bucket_histogram(x, n, prefix, mask, shift, hist);
+      pick_bucket(hist, k, sel);
+      prefix |= sel[0] << shift;
+      mask |= 255u << shift;
+      k = static_cast<int>(sel[1]);
+      __syncthreads();
+    }
+    bits[which] = prefix;
+  }
 }
 
 __global__ void __launch_bounds__(kThreads) stats_kernel(const StatsArgs a) {
@@ -375,7 +394,7 @@ __global__ void __launch_bounds__(kThreads) stats_kernel(const StatsArgs a) {
   float *s_mx = sm + a.N;            // [N]: scores of the MXFP8 Q/K path
   __shared__ float red[kWarps];
   __shared__ int redi[kWarps];
-  __shared__ uint32_t hist[256], sel[2];
+  __shared__ uint32_t hist[256], hist_top[256], sel[2];
   const long row = blockIdx.x;       // (b * Hq + h) * n_q + i
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int j = threadIdx.x; j < a.N; j += kThreads) {
@@ -425,22 +444,24 @@ __global__ void __launch_bounds__(kThreads) stats_kernel(const StatsArgs a) {
   // top-k masses: the k-th largest probability t by a radix select on the
   // float bits (monotone for p >= 0), then mass = sum(p > t) + (k - #(p > t)) t
   const int kk[3] = {(a.N + 99) / 100, (a.N * 5 + 99) / 100, (a.N * 10 + 99) / 100};
+  uint32_t tb[3];
+  kth_largest_bits3(s_ref, a.N, kk, tb, hist, hist_top, sel);
+  float sum[3] = {0.0f, 0.0f, 0.0f}, cnt[3] = {0.0f, 0.0f, 0.0f};
+  for (int j = threadIdx.x; j < a.N; j += kThreads) {
+    const float p = s_ref[j];
+    const uint32_t pb = __float_as_uint(p);
+#pragma unroll
+    for (int w = 0; w < 3; ++w)
+      if (pb > tb[w]) {
+        sum[w] += p;
+        cnt[w] += 1.0f;
+      }
+  }
   float top[3];
 #pragma unroll 1
-  for (int which = 0; which < 3; ++which) {
-    const uint32_t t = kth_largest_bits(s_ref, a.N, kk[which], hist, sel);
-    const float tv = __uint_as_float(t);
-    float sum = 0.0f, cnt = 0.0f;
-    for (int j = threadIdx.x; j < a.N; j += kThreads) {
-      const float p = s_ref[j];
-      if (__float_as_uint(p) > t) {
-        sum += p;
-        cnt += 1.0f;
-      }
-    }
-    sum = block_sum(sum, red);
-    cnt = block_sum(cnt, red);
-    top[which] = sum + (static_cast<float>(kk[which]) - cnt) * tv;
+  for (int w = 0; w < 3; ++w) {
+    const float sw = block_sum(sum[w], red), cw = block_sum(cnt[w], red);
+    top[w] = sw + (static_cast<float>(kk[w]) - cw) * __uint_as_float(tb[w]);
   }
   const float t1 = top[0], t5 = top[1], t10 = top[2];
 
