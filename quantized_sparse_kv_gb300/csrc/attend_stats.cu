@@ -269,39 +269,52 @@ __device__ __forceinline__ float block_sum(float x, float *red) {
   return t;
 }
 
-// Index of the first maximum of s[0, n).
-__device__ __forceinline__ int block_argmax(const float *s, int n, float *red, int *redi) {
-  float best = -CUDART_INF_F;
-  int bi = 0x7fffffff;
-  for (int j = threadIdx.x; j < n; j += kThreads)
-    if (s[j] > best) {
-      best = s[j];
-      bi = j;
+// Indices of the first maxima of a[0, n) and b[0, n) in one pass.
+__device__ __forceinline__ void block_argmax2(const float *a, const float *b, int n, float *red,
+                                              int *redi, int &ia, int &ib) {
+  float best[2] = {-CUDART_INF_F, -CUDART_INF_F};
+  int bi[2] = {0x7fffffff, 0x7fffffff};
+  for (int j = threadIdx.x; j < n; j += kThreads) {
+    if (a[j] > best[0]) {
+      best[0] = a[j];
+      bi[0] = j;
     }
-#pragma unroll
-  for (int o = 16; o; o >>= 1) {
-    const float ob = __shfl_xor_sync(0xffffffffu, best, o);
-    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-    if (ob > best || (ob == best && oi < bi)) {
-      best = ob;
-      bi = oi;
+    if (b[j] > best[1]) {
+      best[1] = b[j];
+      bi[1] = j;
     }
   }
+#pragma unroll
+  for (int o = 16; o; o >>= 1)
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {
+      const float ob = __shfl_xor_sync(0xffffffffu, best[x], o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi[x], o);
+      if (ob > best[x] || (ob == best[x] && oi < bi[x])) {
+        best[x] = ob;
+        bi[x] = oi;
+      }
+    }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   __syncthreads();
-  if (lane == 0) {
-    red[warp] = best;
-    redi[warp] = bi;
-  }
-  __syncthreads();
-  best = red[0];
-  bi = redi[0];
-  for (int w = 1; w < kWarps; ++w)
-    if (red[w] > best || (red[w] == best && redi[w] < bi)) {
-      best = red[w];
-      bi = redi[w];
+  if (lane == 0)
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {
+      red[x * kWarps + warp] = best[x];
+      redi[x * kWarps + warp] = bi[x];
     }
-  return bi;
+  __syncthreads();
+#pragma unroll
+  for (int x = 0; x < 2; ++x) {
+    float bb = red[x * kWarps];
+    int ii = redi[x * kWarps];
+    for (int w = 1; w < kWarps; ++w)
+      if (red[x * kWarps + w] > bb || (red[x * kWarps + w] == bb && redi[x * kWarps + w] < ii)) {
+        bb = red[x * kWarps + w];
+        ii = redi[x * kWarps + w];
+      }
+    (x == 0 ? ia : ib) = ii;
+  }
 }
 
 // 256-bucket histogram of bits [shift, shift + 8) of the keys of x[0, n)
@@ -392,8 +405,8 @@ __global__ void __launch_bounds__(kThreads) stats_kernel(const StatsArgs a) {
   extern __shared__ float sm[];
   float *s_ref = sm;                 // [N]: scores, then p
   float *s_mx = sm + a.N;            // [N]: scores of the MXFP8 Q/K path
-  __shared__ float red[kWarps];
-  __shared__ int redi[kWarps];
+  __shared__ float red[2 * kWarps];
+  __shared__ int redi[2 * kWarps];
   __shared__ uint32_t hist[256], hist_top[256], sel[2];
   const long row = blockIdx.x;       // (b * Hq + h) * n_q + i
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -403,13 +416,18 @@ __global__ void __launch_bounds__(kThreads) stats_kernel(const StatsArgs a) {
   }
   __syncthreads();
 
-  const int am_ref = block_argmax(s_ref, a.N, red, redi);
-  const int am_mx = block_argmax(s_mx, a.N, red, redi);
+  int am_ref, am_mx;
+  block_argmax2(s_ref, s_mx, a.N, red, redi, am_ref, am_mx);
   const float mx_ref = s_ref[am_ref], mx_mx = s_mx[am_mx];
+  __syncthreads();  // both maxima read before the rows are overwritten
+  // the exponentials, kept in place of the scores
   float l_ref = 0.0f, l_mx = 0.0f;
   for (int j = threadIdx.x; j < a.N; j += kThreads) {
-    l_ref += expf(s_ref[j] - mx_ref);
-    l_mx += expf(s_mx[j] - mx_mx);
+    const float er = expf(s_ref[j] - mx_ref), em = expf(s_mx[j] - mx_mx);
+    s_ref[j] = er;
+    s_mx[j] = em;
+    l_ref += er;
+    l_mx += em;
   }
   l_ref = block_sum(l_ref, red);
   l_mx = block_sum(l_mx, red);
@@ -417,8 +435,8 @@ __global__ void __launch_bounds__(kThreads) stats_kernel(const StatsArgs a) {
   // p, structural zeros, entropy, Q/K-path TV
   float zeros = 0.0f, plogp = 0.0f, qk_tv = 0.0f;
   for (int j = threadIdx.x; j < a.N; j += kThreads) {
-    const float p = expf(s_ref[j] - mx_ref) * inv_ref;
-    const float p2 = expf(s_mx[j] - mx_mx) * inv_mx;
+    const float p = s_ref[j] * inv_ref;
+    const float p2 = s_mx[j] * inv_mx;
     s_ref[j] = p;
     zeros += p == 0.0f ? 1.0f : 0.0f;
     plogp += p > 0.0f ? p * logf(p) : 0.0f;
