@@ -724,13 +724,12 @@ __device__ __forceinline__ float e8m0_scale(uint32_t e) {
 
 // K window: E4M3 codes + E8M0 block bytes -> bf16, 16 codes (one half block)
 // per thread. cvt from e4m3x2 to f16x2 is exact; the power of two is exact.
-__global__ void mxfp8_to_bf16_kernel(const uint8_t *__restrict__ codes,
-                                     const uint8_t *__restrict__ e8m0, long n16,
-                                     __nv_bfloat16 *__restrict__ out) {
-  wait_prior_grid();
-  allow_next_grid();
-  for (long i = blockIdx.x * static_cast<long>(blockDim.x) + threadIdx.x; i < n16;
-       i += static_cast<long>(gridDim.x) * blockDim.x) {
+__device__ __forceinline__ void mxfp8_to_bf16(const uint8_t *__restrict__ codes,
+                                              const uint8_t *__restrict__ e8m0, long n16,
+                                              __nv_bfloat16 *__restrict__ out, long block,
+                                              long blocks) {
+  for (long i = block * static_cast<long>(blockDim.x) + threadIdx.x; i < n16;
+       i += blocks * blockDim.x) {
     const uint4 c = reinterpret_cast<const uint4 *>(codes)[i];
     const float sc = e8m0_scale(e8m0[i >> 1]);
     const uint32_t w[4] = {c.x, c.y, c.z, c.w};
@@ -758,12 +757,9 @@ __global__ void mxfp8_to_bf16_kernel(const uint8_t *__restrict__ codes,
 // shuffles, after which every value follows the rule kv_pack applies to an
 // MXFP8 K window in the exact steps of mxfp8_round_warp, two values per E4M3
 // conversion.
-__global__ void __launch_bounds__(256) q_mxfp8_round_kernel(const __nv_bfloat16 *__restrict__ q,
-                                                            long blocks,
-                                                            __nv_bfloat16 *__restrict__ out) {
-  wait_prior_grid();
-  allow_next_grid();
-  const long tid = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x;
+__device__ __forceinline__ void q_mxfp8_round(const __nv_bfloat16 *__restrict__ q, long blocks,
+                                              __nv_bfloat16 *__restrict__ out, long block) {
+  const long tid = block * blockDim.x + threadIdx.x;
   const bool live = (tid >> 2) < blocks;
   const uint4 u = live ? reinterpret_cast<const uint4 *>(q)[tid] : make_uint4(0, 0, 0, 0);
   const uint32_t w[4] = {u.x, u.y, u.z, u.w};
@@ -793,6 +789,21 @@ __global__ void __launch_bounds__(256) q_mxfp8_round_kernel(const __nv_bfloat16 
     o[j] = pack_bf16x2(__fmul_rn(f.x, up), __fmul_rn(f.y, up));
   }
   reinterpret_cast<uint4 *>(out)[tid] = make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// The MXFP8 prologue as one grid: blocks [0, k_blocks) expand the K window,
+// the rest round Q; the two parts are independent, so neither waits for the
+// other as two dependent launches would.
+__global__ void __launch_bounds__(256) mxfp8_prologue_kernel(
+    const uint8_t *__restrict__ codes, const uint8_t *__restrict__ e8m0, long n16,
+    __nv_bfloat16 *__restrict__ k_out, unsigned k_blocks, const __nv_bfloat16 *__restrict__ q,
+    long q_blocks, __nv_bfloat16 *__restrict__ q_out) {
+  wait_prior_grid();
+  allow_next_grid();
+  if (blockIdx.x < k_blocks)
+    mxfp8_to_bf16(codes, e8m0, n16, k_out, blockIdx.x, k_blocks);
+  else
+    q_mxfp8_round(q, q_blocks, q_out, blockIdx.x - k_blocks);
 }
 
 // ------------------------------------------------------------------ int4 history
@@ -1054,13 +1065,13 @@ int launch_attend_chunk(const kvq_cache &c, const void *q, int Hq, int n_q, floa
     __nv_bfloat16 *qb = reinterpret_cast<__nv_bfloat16 *>(static_cast<uint8_t *>(ws) +
                                                           ((kn * 2 + 255) & ~255L));
     const unsigned kblocks = static_cast<unsigned>(std::min<long>((kn / 16 + 255) / 256, 1L << 20));
-    launch_dependent(mxfp8_to_bf16_kernel, dim3(kblocks), dim3(256), 0, s,
-                     static_cast<const uint8_t *>(c.k_window), c.k_window_e8m0, kn / 16, kb);
-    launch_dependent(q_mxfp8_round_kernel, dim3(static_cast<unsigned>((qn / 8 + 255) / 256)),
-                     dim3(256), 0, s, static_cast<const __nv_bfloat16 *>(q), qn / 32, qb);
+    const unsigned qblocks = static_cast<unsigned>((qn / 8 + 255) / 256);
+    launch_dependent(mxfp8_prologue_kernel, dim3(kblocks + qblocks), dim3(256), 0, s,
+                     static_cast<const uint8_t *>(c.k_window), c.k_window_e8m0, kn / 16, kb,
+                     kblocks, static_cast<const __nv_bfloat16 *>(q), qn / 32, qb);
     kptr = kb;
     qptr = qb;
-    launches += 2;
+    launches += 1;
   }
   CUtensorMap tq, tk, tv, tkw, tvw;
   // expanded K and V (history, MXFP8) are tight; an all-window cache keeps
