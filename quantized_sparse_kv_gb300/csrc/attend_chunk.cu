@@ -330,13 +330,15 @@ __device__ __forceinline__ void softmax_chunk(float (&v)[32], int c, int valid, 
 // chunk: chunks 0-2 are exponentiated and stored while the TMEM load of the
 // next is in flight; chunk 3 is left raw in v3, and mx is its raw maximum, so
 // that the caller can release S before finishing it. cs[c]: sum of chunk c;
-// part: region sums (kSplit only).
+// part: region sums (kSplit only). With set_ref (a group's first tile) the
+// reference is taken from chunk 0's maximum, stored in *set_ref, and used
+// for the whole tile.
 template <bool kSplit>
 __device__ __forceinline__ void softmax_pass_head(uint32_t taddr, int valid, int t0, float scale,
                                                   float neg_m, const Regions &reg, uint8_t *p,
                                                   int row, float (&cs)[4],
                                                   float (&part)[kMaxRegions], float (&v3)[32],
-                                                  float &mx) {
+                                                  float &mx, float *set_ref) {
 #pragma unroll
   for (int k = 0; k < kMaxRegions; ++k) part[k] = 0.0f;
   float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F;
@@ -345,6 +347,17 @@ __device__ __forceinline__ void softmax_pass_head(uint32_t taddr, int valid, int
   tmem_wait_ld();
   reg_fence(va);
   tmem_ld32(taddr + 32u, v3);
+  if (set_ref) {  // chunk 0 holds at least one valid key
+    float r0 = -CUDART_INF_F, r1 = -CUDART_INF_F;
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) {
+      r0 = fmaxf(r0, e < valid ? va[e] : -CUDART_INF_F);
+      r1 = fmaxf(r1, e + 1 < valid ? va[e + 1] : -CUDART_INF_F);
+    }
+    const float ref = fmaxf(r0, r1) * scale;  // scale > 0 keeps the order
+    *set_ref = ref;
+    neg_m = -ref;
+  }
   softmax_chunk<kSplit, false>(va, 0, valid, t0, scale, neg_m, reg, p, row, cs[0], part, mx0, mx1);
   tmem_wait_ld();
   reg_fence(v3);
@@ -536,7 +549,7 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t s_row = t_s(g) + lane_off, o_row = t_o(g) + lane_off;
     const int my_tiles = (nt - g + 1) >> 1;  // tiles g, g+2, ...
     // Row state: P is taken against a reference m_used, set from the row's
-    // maximum over its first tile and kept while P stays below
+    // maximum over the first 32 scores of its first tile and kept while P stays below
     // 2^kRedoThreshold (bf16 P and the fp32 sums have the range for it, so no
     // running maximum is kept); a tile that would pass that bound raises the
     // reference to its maximum and is redone.
@@ -558,7 +571,6 @@ __global__ void __launch_bounds__(384, 1)
         ok = false;
         break;
       }
-      if (i == 0) m_used = row_max(s_row, valid) * a.scale_log2;  // scale > 0 keeps the order
       // regions: chunk c of the tile lies in region kc[c], unless the tile
       // has a chunk across a bound (split: sums taken per element)
       int kc[4] = {0, 0, 0, 0};
@@ -574,14 +586,16 @@ __global__ void __launch_bounds__(384, 1)
           split |= start < end && end > a.reg.b[kc[c] + 1];
         }
       }
-      // one pass: P = 2^(s * scale - m_used) -> shared memory, sums
+      // one pass: P = 2^(s * scale - m_used) -> shared memory, sums; the
+      // group's first tile sets m_used from its first 32 scores
       float cs[4], part[kMaxRegions], v3[32], mx, dummy0 = 0.0f, dummy1 = 0.0f;
+      float *const set_ref = i == 0 ? &m_used : nullptr;
       if (split)
         softmax_pass_head<true>(s_row, valid, t0, a.scale_log2, -m_used, a.reg, sm.p[g], row, cs,
-                                part, v3, mx);
+                                part, v3, mx, set_ref);
       else
         softmax_pass_head<false>(s_row, valid, t0, a.scale_log2, -m_used, a.reg, sm.p[g], row, cs,
-                                 part, v3, mx);
+                                 part, v3, mx, set_ref);
       // A chunk sum bounds each of its P values: chunks 0-2 are checked by
       // their sums, chunk 3 by its raw maximum.
       const float big = fmaxf(fmaxf(cs[0], cs[1]), cs[2]);
@@ -601,10 +615,10 @@ __global__ void __launch_bounds__(384, 1)
         }
         if (split)
           softmax_pass_head<true>(s_row, valid, t0, a.scale_log2, -m_used, a.reg, sm.p[g], row, cs,
-                                  part, v3, mx);
+                                  part, v3, mx, nullptr);
         else
           softmax_pass_head<false>(s_row, valid, t0, a.scale_log2, -m_used, a.reg, sm.p[g], row,
-                                   cs, part, v3, mx);
+                                   cs, part, v3, mx, nullptr);
       }
       // every score of the tile is in registers: S_g may take the next tile
       tc_fence_before();
