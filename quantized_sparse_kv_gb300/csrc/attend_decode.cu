@@ -659,6 +659,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const Deco
 template <typename OT>
 __global__ void __launch_bounds__(256) combine_kernel(const DecodeArgs a, OT *__restrict__ out) {
   wait_prior_grid();
+  allow_next_grid();  // the next call's decode grid may be placed while this one runs
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int u = blockIdx.x;
   const int h = warp;
