@@ -29,10 +29,17 @@ def test_stats_rules(k):
     lib = k.load_library()
     sz = ctypes.c_size_t(0)
     c = cache(k)
-    # the workspace query answers with two fp32 copies of every key
-    assert lib.kv_attend_stats(ctypes.byref(c), ADDR, 1, 4, 8, 0.0, None, ADDR, None,
-                               ctypes.byref(sz), None, None) == 0
-    assert sz.value >= 2 * 2 * 256 * 128 * 4
+    # the workspace query answers with two fp32 copies of every key, in
+    # 32-key tiles, and both fp32 score rows of every query row, each of the
+    # four arrays rounded up to 256 bytes
+    round256 = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    for (b, hkv, n, d, hq, nq) in ((1, 2, 256, 128, 4, 8), (2, 1, 700, 64, 3, 5), (1, 4, 33, 32, 8, 1)):
+        cc = cache(k, n=n, d=d, recent=n, hkv=hkv, b=b)
+        assert lib.kv_attend_stats(ctypes.byref(cc), ADDR, 1, hq, nq, 0.0, None, ADDR, None,
+                                   ctypes.byref(sz), None, None) == 0
+        tiles = 4 * b * hkv * (-(-n // 32)) * 32 * d
+        scores = 4 * b * hq * nq * n
+        assert sz.value == 2 * round256(tiles) + 2 * round256(scores)
     c96 = cache(k, d=96)
     assert lib.kv_attend_stats(ctypes.byref(c96), ADDR, 1, 4, 8, 0.0, None, ADDR, None,
                                ctypes.byref(sz), None, None) == 3       # D not a power of two
