@@ -186,9 +186,11 @@ KVQ_API kvq_status kv_append(kvq_cache *cache, const void *k_new, const void *v_
  *   (enqueueing nothing); to run, pass a non-NULL workspace even when the
  *   required size is 0.
  * Kernel choice: one query row per (sequence, head) with 8 query heads per KV
- *   head and D = 128 runs the split-K decode kernels; a bf16 or MXFP8 window
- *   covering all tokens with many queries runs the tensor-core chunk kernel;
- *   everything else runs the fp32 kernel.
+ *   head and D = 128 runs the split-K decode kernels; with bf16 q, D = 128
+ *   and at least 64 query rows, a bf16 or MXFP8 window covering all tokens,
+ *   or an int4 part followed by a bf16 window (the key tiles holding int4
+ *   tokens are expanded to bf16 in the workspace, the others read in place),
+ *   runs the tensor-core chunk kernel; everything else runs the fp32 kernel.
  */
 KVQ_API kvq_status kv_attend(const kvq_cache *cache, const void *q, int32_t q_dtype,
                              int32_t q_heads, int32_t n_q, float sm_scale, void *out,
