@@ -190,7 +190,9 @@ KVQ_API kvq_status kv_append(kvq_cache *cache, const void *k_new, const void *v_
  *   and at least 64 query rows, a bf16 or MXFP8 window covering all tokens,
  *   or an int4 part followed by a bf16 window (the key tiles holding int4
  *   tokens are expanded to bf16 in the workspace, the others read in place),
- *   runs the tensor-core chunk kernel; everything else runs the fp32 kernel.
+ *   runs the tensor-core chunk kernel (when batch * q_heads <= 65,535);
+ *   everything else runs the fp32 kernel, which needs q_heads and batch
+ *   <= 65,535 (else KVQ_ERR_UNSUPPORTED).
  */
 KVQ_API kvq_status kv_attend(const kvq_cache *cache, const void *q, int32_t q_dtype,
                              int32_t q_heads, int32_t n_q, float sm_scale, void *out,
@@ -234,7 +236,7 @@ enum {
  * every query row: about 8 x B x Hkv x N x D + 8 x B x q_heads x n_q x N
  * bytes).
  * Restrictions (else KVQ_ERR_UNSUPPORTED): D in {32, 64, 128, 256},
- * N <= 16384.
+ * N <= 16384, batch * q_heads <= 65,535.
  */
 KVQ_API kvq_status kv_attend_stats(const kvq_cache *cache, const void *q, int32_t q_dtype,
                                    int32_t q_heads, int32_t n_q, float sm_scale,
@@ -248,8 +250,8 @@ KVQ_API kvq_status kv_attend_stats(const kvq_cache *cache, const void *q, int32_
  * other key. Lists hold distinct positions in any order. An index outside
  * [0, N) is skipped and flagged KVQ_DEV_INDEX; with validate != 0 duplicate
  * positions are flagged KVQ_DEV_DUP (the output of that row is then invalid).
- * An MXFP8 K window is not supported here (KVQ_ERR_UNSUPPORTED). Other
- * arguments as for kv_attend.
+ * An MXFP8 K window, n_cand > 65,536 and q_heads or batch above 65,535 are
+ * not supported (KVQ_ERR_UNSUPPORTED). Other arguments as for kv_attend.
  */
 KVQ_API kvq_status kv_attend_candidates(const kvq_cache *cache, const void *q, int32_t q_dtype,
                                         int32_t q_heads, int32_t n_q, const int32_t *idx,

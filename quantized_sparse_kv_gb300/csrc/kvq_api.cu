@@ -217,11 +217,15 @@ kvq_status kv_attend(const kvq_cache *cache, const void *q, int32_t q_dtype, int
   const int sms = sm_count();
 
   enum { GENERIC, DECODE, CHUNK } path = GENERIC;
+  // the chunk kernel's grid is (query tiles, batch * q_heads)
   if (kvq::chunk_supported(*cache, q_dtype, q_heads, n_q) &&
+      static_cast<long>(cache->batch) * q_heads <= 65535 &&
       (!regions || n_regions <= kvq::chunk_max_regions()))
     path = CHUNK;
   else if (!regions && kvq::decode_supported(*cache, q_dtype, q_heads, n_q))
     path = DECODE;
+  // the fp32 kernel's grid is (row blocks, q_heads, batch)
+  if (path == GENERIC && (q_heads > 65535 || cache->batch > 65535)) return KVQ_ERR_UNSUPPORTED;
   size_t need = 0;
   if (path == DECODE) need = kvq::decode_workspace_bytes(*cache, q_heads, sms);
   if (path == CHUNK) need = kvq::chunk_workspace_bytes(*cache, q_heads, n_q);
@@ -269,6 +273,7 @@ kvq_status kv_attend_stats(const kvq_cache *cache, const void *q, int32_t q_dtyp
   const int d = cache->head_dim;
   if ((d & (d - 1)) != 0 || cache->n_tokens > kvq::stats_max_tokens()) return KVQ_ERR_UNSUPPORTED;
   if (static_cast<long>(cache->batch) * q_heads * n_q > 0x7fffffffL) return KVQ_ERR_UNSUPPORTED;
+  if (static_cast<long>(cache->batch) * q_heads > 65535) return KVQ_ERR_UNSUPPORTED;  // grid.y
   const size_t need = kvq::stats_workspace_bytes(*cache, q_heads, n_q);
   if (!workspace) {
     *ws_bytes = need;
@@ -299,7 +304,8 @@ kvq_status kv_attend_candidates(const kvq_cache *cache, const void *q, int32_t q
       (out_dtype != KVQ_F32 && out_dtype != KVQ_BF16))
     return KVQ_ERR_ARG;
   if (cache->recent > 0 && cache->kwin_dtype == KVQ_MXFP8) return KVQ_ERR_UNSUPPORTED;
-  if (n_cand > 65536) return KVQ_ERR_UNSUPPORTED;
+  // the grid is (query rows, q_heads, batch)
+  if (n_cand > 65536 || q_heads > 65535 || cache->batch > 65535) return KVQ_ERR_UNSUPPORTED;
   if (!workspace) {
     *ws_bytes = 0;
     return KVQ_OK;

@@ -82,3 +82,20 @@ def test_block_and_region_drop_rules(k):
     d64 = cache(k, d=64)
     assert lib.kv_attend_region_drop(ctypes.byref(d64), ADDR, 1, 4, 300, 0.0, bounds, 3, 1, ADDR,
                                      1, None, ctypes.byref(sz), None, None) == 3
+
+
+def test_grid_limits_are_argument_errors(k):
+    # shapes whose launch grids would pass CUDA's 65,535 limit on y or z are
+    # refused before anything is enqueued
+    lib = k.load_library()
+    sz = ctypes.c_size_t(0)
+    c1 = cache(k, n=256, d=128, recent=256, hkv=1)
+    assert lib.kv_attend(ctypes.byref(c1), ADDR, 1, 65536, 1, 0.0, ADDR, 1, None, 0, None, None,
+                         ctypes.byref(sz), None, None) == 3
+    assert lib.kv_attend_stats(ctypes.byref(c1), ADDR, 1, 65536, 1, 0.0, None, ADDR, None,
+                               ctypes.byref(sz), None, None) == 3
+    assert lib.kv_attend_candidates(ctypes.byref(c1), ADDR, 1, 65536, 1, ADDR, 8, 0, 0.0, ADDR,
+                                    1, None, ctypes.byref(sz), None, None) == 3
+    # a large but valid head count still answers the workspace query
+    assert lib.kv_attend(ctypes.byref(c1), ADDR, 1, 64, 1, 0.0, ADDR, 1, None, 0, None, None,
+                         ctypes.byref(sz), None, None) == 0
