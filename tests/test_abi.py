@@ -105,3 +105,19 @@ def test_binding_struct_matches_header():
         for part in decl.split(","):
             names.append(re.findall(r"(\w+)\s*(?:\[\d+\])?\s*$", part.strip())[0])
     assert names == [f[0] for f in k.KvqCacheStruct._fields_]
+
+
+def test_binding_fails_loudly_without_the_library():
+    # no fallback path: a missing libkvq.so is an error at the first call
+    import subprocess
+    import sys
+    code = ("from quantized_sparse_kv_gb300 import kvq\n"
+            "try:\n"
+            "    kvq.load_library('/nonexistent/libkvq.so')\n"
+            "except RuntimeError as e:\n"
+            "    print('raised', 'missing' in str(e))\n")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = subprocess.run([sys.executable, "-c", code], cwd=root, capture_output=True, text=True,
+                         timeout=300)
+    assert out.returncode == 0, out.stderr[-2000:]
+    assert out.stdout.strip() == "raised True"
