@@ -203,8 +203,12 @@ def make_flush():
 
 def rotation(touched_bytes, cap=16):
     """How many independent input sets keep every reuse of a set at least two
-    L2 sizes of other traffic away (so a call never finds its inputs in L2)."""
-    return max(1, min(cap, math.ceil(2 * L2_BYTES / max(1, touched_bytes))))
+    L2 sizes of other traffic away (so a call never finds its inputs in L2):
+    one set when a call alone touches twice L2, else enough others that
+    (n - 1) sets cover twice L2."""
+    if touched_bytes >= 2 * L2_BYTES:
+        return 1
+    return max(1, min(cap, 1 + math.ceil(2 * L2_BYTES / max(1, touched_bytes))))
 
 
 def cycling(calls):
@@ -259,10 +263,13 @@ def row_small(kvq, synth, torch, steps, warmup, pk):
             "launches": a.launches(), "note": "latency-bound: 0.8 MB per call"}
 
 
-def row_chunk(kvq, synth, torch, steps, warmup, pk, kwin):
+def row_chunk(kvq, synth, torch, steps, warmup, pk, kwin, bounds=None):
     """kwin "bf16" / "mxfp8": every key in the window; "int4": the sink and
-    recent regions (3,900 tokens) as int4 groups, the current 2,340 in bf16."""
+    recent regions (3,900 tokens) as int4 groups, the current 2,340 in bf16.
+    bounds: the region bounds (default [sink | recent | current]; the 16
+    latent frames for the heatmap row)."""
     c = CHUNK
+    bounds = list(bounds or c["bounds"])
     recent = c["n_kv"] if kwin != "int4" else c["n_kv"] - c["bounds"][2]
     touched = 2 * c["heads"] * c["head_dim"] * (2 * c["n_q"] + 2 * c["n_kv"])
     n = rotation(touched)
@@ -271,7 +278,7 @@ def row_chunk(kvq, synth, torch, steps, warmup, pk, kwin):
         q, k, v = synth.chunk_inputs_torch(21 + 5 * i, "cuda")
         cache = kvq.pack(k, v, recent, "bf16" if kwin == "int4" else kwin, "bf16")
         del k, v
-        attends.append(kvq.Attend(cache, q, out_dtype="bf16", region_bounds=c["bounds"]))
+        attends.append(kvq.Attend(cache, q, out_dtype="bf16", region_bounds=bounds))
     a = attends[0]
     ms = time_steps(cycling([x.run for x in attends]), steps, warmup)
     flops = 4.0 * c["heads"] * c["n_q"] * c["n_kv"] * c["head_dim"]
@@ -281,8 +288,10 @@ def row_chunk(kvq, synth, torch, steps, warmup, pk, kwin):
     keys = c["heads"] * c["n_q"] * c["n_kv"]
     what = {"bf16": "bf16 Q/K", "mxfp8": "mxfp8 Q/K",
             "int4": "bf16 Q, int4 K/V for sink+recent (3900 tokens) and bf16 current window"}[kwin]
+    regions = ("[sink 1560 | recent 2340 | current 2340]" if len(bounds) == 4
+               else f"{len(bounds) - 1} regions (one per 390-key latent frame)")
     return {"workload": f"chunk attention {what}, 32 heads, 2340 queries over 6240 keys "
-                        "[sink 1560 | recent 2340 | current 2340], D=128, region mass",
+                        f"{regions}, D=128, region mass",
             "ms": ms, "keys_per_s": keys / (ms * 1e-3), "path": a.path, "l2": l2_note(n, touched),
             "roofline": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s",
                          "frac": tf / peak,
@@ -739,6 +748,8 @@ ROWS = {
     "candidates_top32_of_C256_L131072": lambda kvq, synth, torch, st, w, pk:
         row_candidates_topk(kvq, synth, torch, st, w, pk, 131072, 256, 32),
     "chunk_bf16": lambda kvq, synth, torch, st, w, pk: row_chunk(kvq, synth, torch, st, w, pk, "bf16"),
+    "chunk_bf16_16frames": lambda kvq, synth, torch, st, w, pk:
+        row_chunk(kvq, synth, torch, st, w, pk, "bf16", synth.CHUNK_LF_BOUNDS),
     "chunk_mxfp8": lambda kvq, synth, torch, st, w, pk:
         row_chunk(kvq, synth, torch, st, w, pk, "mxfp8"),
     "chunk_int4_history": lambda kvq, synth, torch, st, w, pk:

@@ -339,9 +339,17 @@ KVQ_API kvq_status kv_attend_region_drop(const kvq_cache *cache, const void *q, 
  * 152-SM GPU) returns KVQ_ERR_WORKSPACE and enqueues nothing; other
  * unsupported shapes return KVQ_ERR_UNSUPPORTED. Nothing is allocated, by
  * the library or by any library it calls.
- * The first call on a device looks up the scratch array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call
- * before any stream capture. Every call reads scratch it wrote itself in the
+ * The array's device address is looked up (cudaGetSymbolAddress) once per
+ * device, with that device current, by the first kv_pack or kv_append on the
+ * device, or else by the first call of this entry point; make that first call
+ * before any stream capture. The lookup loads the library's decode module on
+ * the device (CUDA loads modules lazily by default), and that load is what
+ * takes the 8 MiB: a runtime that hands all free HBM to its KV-cache pool
+ * should pack (or append to) a cache first, as it must before decoding anyway.
+ * If the lookup fails, the call returns KVQ_ERR_CUDA with the CUDA error
+ * cleared. The looked-up address is kept for the life of the process: do not
+ * use the library across a cudaDeviceReset on that device.
+ * Every call reads scratch it wrote itself in the
  * same call, so nothing needs clearing between calls, but all calls share
  * the one array: calls that overlap on the GPU (different streams, no
  * ordering between them) race and corrupt each other's results.

@@ -18,7 +18,7 @@ what the hot path computes, written from these pages:
 * the MiniCPM5-2B attention-predictor study (bjdmk.com.cn/news/5855973) --
   exact attention restricted to top-C candidate keys (sections 6 and 9).
 
-Readings where the pages are silent (each restated in the design notes):
+Readings where the pages are silent:
 int4 scale = fp32(amax / 7) with codes clamped to [-7, 7] and rounded half to
 even; a zero scale gives all-zero codes; nibble = code + 8, even element in the
 low nibble; K groups are aligned at token 0 and the last one is zero padded; V

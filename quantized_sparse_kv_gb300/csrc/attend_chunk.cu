@@ -17,10 +17,16 @@
 // a P buffer in shared memory; its chain per tile is S = Q K^T (MMA) ->
 // softmax (thread r owns query row r = TMEM lane r) -> O_g += P V (MMA, V as
 // the MN-major operand), and the two groups' chains interleave so the tensor
-// core works on one group while the other exponentiates. A group's running
-// max only moves when it grows by more than 8 (then O_g and its sums are
-// rescaled). At the end group A merges both (max, sum, O, region sums)
-// states of its rows, normalises and stores O and the region masses.
+// core works on one group while the other exponentiates. P is taken against
+// a fixed reference per row and group, set from the first 32 scores the
+// group sees; a tile that would push P past 2^64 raises the reference,
+// rescales O_g and the sums, and is redone from its scores (still in TMEM).
+// Region masses (up to 16 regions) are summed per row as the keys stream by:
+// one running sum for the region under the current key, the finished
+// regions' sums kept per thread. At the end each group leaves its row state
+// (reference, sum, region sums) in shared memory and merges both groups' O
+// for half of the columns, normalises and stores them; group A stores the
+// region masses.
 // Every mbarrier wait is bounded; on timeout the CTA flags KVQ_DEV_TIMEOUT,
 // stops, drains its copies and MMAs and frees TMEM.
 #include <cuda.h>
@@ -39,7 +45,7 @@ constexpr int kBN = 128;          // keys per tile
 constexpr int kDim = 128;         // head dim
 constexpr int kKStages = 2;
 constexpr int kVStages = 2;
-constexpr int kMaxRegions = 4;
+constexpr int kMaxRegions = 16;
 constexpr uint32_t kTileBytes = kBN * kDim * 2;  // 32 KB, one K or V tile (bf16)
 constexpr uint32_t kHalfBytes = kTileBytes / 2;  // 16 KB: 128 rows x 64 features
 constexpr float kRedoThreshold = 64.0f;           // log2 units: P stays below 2^64
@@ -55,6 +61,7 @@ struct __align__(1024) ChunkSmem {
   uint64_t s_full[2], s_free[2], p_full[2], o_done[2], mma_done;
   uint32_t tmem_base;
   int abort_flag;
+  int rb[kMaxRegions + 1];                  // region bounds (a copy of ChunkArgs::reg.b)
 };
 
 // The two groups' row states for the final merge, laid over K stage 0, which
@@ -258,15 +265,50 @@ __device__ __forceinline__ void add2(float &a0, float &a1, float x0, float x1) {
       : "f"(x0), "f"(x1));
 }
 
+// Running region sums of one row. The keys a softmax group sees arrive in
+// increasing order, so the region under the current key only moves forward:
+// `cur` sums region k, and a region that has been left is stored in done[]
+// (indexed at run time, so it lives in local memory; it is written once per
+// region, not per key). k is the same in every thread of a group.
+struct RegionAcc {
+  int k;
+  float cur;
+  float *done;
+};
+
+// Move to the region holding key `pos`, storing the sums of those passed.
+__device__ __forceinline__ void region_seek(RegionAcc &r, const int *rb, int n, int pos) {
+  while (r.k + 1 < n && rb[r.k + 1] <= pos) {
+    r.done[r.k] = r.cur;
+    r.cur = 0.0f;
+    ++r.k;
+  }
+}
+
+// Sum of v[e] for lo <= e < hi.
+__device__ __forceinline__ float range_sum(const float (&v)[32], int lo, int hi) {
+  float a = 0.0f, b = 0.0f;
+#pragma unroll
+  for (int e = 0; e < 32; e += 2) {
+    a += (e >= lo && e < hi) ? v[e] : 0.0f;
+    b += (e + 1 >= lo && e + 1 < hi) ? v[e + 1] : 0.0f;
+  }
+  return a + b;
+}
+
 // 32 columns of the pass: P = 2^(s * scale + neg_m) for the valid ones (0
 // beyond), raw maximum, P to shared memory as bf16, the chunk's sum. Region
-// sums are left to the caller unless kSplit (the tile straddles a region
-// bound), when they are taken here element by element.
+// sums: byte c of offs is the offset of the one region bound inside chunk c
+// (32: none); psum then receives the sum of the chunk's keys before it, and
+// the caller does the accounting once P is handed over. With kSplit (some
+// chunk of the tile holds two or more bounds) the chunk's keys are added to
+// the region sums here instead, split at every bound inside the chunk.
 template <bool kSplit, bool kMax = true>
 __device__ __forceinline__ void softmax_chunk(float (&v)[32], int c, int valid, int t0,
-                                              float scale, float neg_m, const Regions &reg,
-                                              uint8_t *p, int row, float &cs,
-                                              float (&part)[kMaxRegions], float &mx0, float &mx1) {
+                                              float scale, float neg_m, const int *rb, int nreg,
+                                              uint32_t offs, uint8_t *p, int row, float &cs,
+                                              float &psum, RegionAcc &racc, float &mx0,
+                                              float &mx1) {
   float ps4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
   if (32 * c + 32 <= valid) {
     if (kMax) {
@@ -311,36 +353,37 @@ __device__ __forceinline__ void softmax_chunk(float (&v)[32], int c, int valid, 
     *reinterpret_cast<uint4 *>(p + (chunk >> 3) * kHalfBytes + swz(row, chunk & 7)) = w;
   }
   cs = (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
-  if (kSplit) {
+  if (!kSplit) {
+    const int off = static_cast<int>((offs >> (8 * c)) & 0xffu);
+    if (off < 32) psum = range_sum(v, 0, off);
+  } else {
     const int start = t0 + 32 * c;
-#pragma unroll
-    for (int k = 0; k < kMaxRegions; ++k) {
-      if (k >= reg.n) break;
-      const int lo = reg.b[k] - start, hi = reg.b[k + 1] - start;
-      if (hi <= 0 || lo >= 32) continue;
-      float pk = 0.0f;
-#pragma unroll
-      for (int e = 0; e < 32; ++e) pk += (e >= lo && e < hi) ? v[e] : 0.0f;
-      part[k] += pk;
+    region_seek(racc, rb, nreg, start);
+    int lo = 0;
+    while (racc.k + 1 < nreg && rb[racc.k + 1] < start + 32) {  // a bound inside the chunk
+      const int o = rb[racc.k + 1] - start;
+      racc.done[racc.k] = racc.cur + range_sum(v, lo, o);
+      racc.cur = 0.0f;
+      ++racc.k;
+      lo = o;
     }
+    racc.cur += lo == 0 ? cs : range_sum(v, lo, 32);
   }
 }
 
 // The pass over the 128 score columns of this thread's row, up to the last
 // chunk: chunks 0-2 are exponentiated and stored while the TMEM load of the
 // next is in flight; chunk 3 is left raw in v3, and mx is its raw maximum, so
-// that the caller can release S before finishing it. cs[c]: sum of chunk c;
-// part: region sums (kSplit only). With set_ref (a group's first tile) the
-// reference is taken from chunk 0's maximum, stored in *set_ref, and used
-// for the whole tile.
+// that the caller can release S before finishing it. cs[c]: sum of chunk c.
+// With set_ref (a group's first tile) the reference is taken from chunk 0's
+// maximum, stored in *set_ref, and used for the whole tile.
 template <bool kSplit>
 __device__ __forceinline__ void softmax_pass_head(uint32_t taddr, int valid, int t0, float scale,
-                                                  float neg_m, const Regions &reg, uint8_t *p,
-                                                  int row, float (&cs)[4],
-                                                  float (&part)[kMaxRegions], float (&v3)[32],
-                                                  float &mx, float *set_ref) {
-#pragma unroll
-  for (int k = 0; k < kMaxRegions; ++k) part[k] = 0.0f;
+                                                  float neg_m, const int *rb, int nreg,
+                                                  uint32_t offs, uint8_t *p, int row,
+                                                  float (&cs)[4], float (&psum)[4],
+                                                  RegionAcc &racc, float (&v3)[32], float &mx,
+                                                  float *set_ref) {
   float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F;
   float va[32];
   tmem_ld32(taddr, va);
@@ -358,15 +401,18 @@ __device__ __forceinline__ void softmax_pass_head(uint32_t taddr, int valid, int
     *set_ref = ref;
     neg_m = -ref;
   }
-  softmax_chunk<kSplit, false>(va, 0, valid, t0, scale, neg_m, reg, p, row, cs[0], part, mx0, mx1);
+  softmax_chunk<kSplit, false>(va, 0, valid, t0, scale, neg_m, rb, nreg, offs, p, row, cs[0],
+                               psum[0], racc, mx0, mx1);
   tmem_wait_ld();
   reg_fence(v3);
   tmem_ld32(taddr + 64u, va);
-  softmax_chunk<kSplit, false>(v3, 1, valid, t0, scale, neg_m, reg, p, row, cs[1], part, mx0, mx1);
+  softmax_chunk<kSplit, false>(v3, 1, valid, t0, scale, neg_m, rb, nreg, offs, p, row, cs[1],
+                               psum[1], racc, mx0, mx1);
   tmem_wait_ld();
   reg_fence(va);
   tmem_ld32(taddr + 96u, v3);
-  softmax_chunk<kSplit, false>(va, 2, valid, t0, scale, neg_m, reg, p, row, cs[2], part, mx0, mx1);
+  softmax_chunk<kSplit, false>(va, 2, valid, t0, scale, neg_m, rb, nreg, offs, p, row, cs[2],
+                               psum[2], racc, mx0, mx1);
   tmem_wait_ld();
   reg_fence(v3);
   if (valid == kBN) {
@@ -421,6 +467,8 @@ __global__ void __launch_bounds__(384, 1)
     }
     mbar_init(smem_u32(&sm.mma_done), 1);
     sm.abort_flag = 0;
+#pragma unroll
+    for (int i = 0; i <= kMaxRegions; ++i) sm.rb[i] = a.reg.b[i];
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -554,7 +602,13 @@ __global__ void __launch_bounds__(384, 1)
     // running maximum is kept); a tile that would pass that bound raises the
     // reference to its maximum and is redone.
     float m_used = -CUDART_INF_F, l = 0.0f;
-    float rsum[kMaxRegions] = {0.0f, 0.0f, 0.0f, 0.0f};
+    const int nreg = a.reg.n;
+    const int *rb = sm.rb;
+    float done[kMaxRegions];
+    RegionAcc racc;
+    racc.k = 0;
+    racc.cur = 0.0f;
+    racc.done = done;
     bool ok = true;
     for (int i = 0; i < my_tiles; ++i) {
       const int j = 2 * i + g;
@@ -571,31 +625,36 @@ __global__ void __launch_bounds__(384, 1)
         ok = false;
         break;
       }
-      // regions: chunk c of the tile lies in region kc[c], unless the tile
-      // has a chunk across a bound (split: sums taken per element)
-      int kc[4] = {0, 0, 0, 0};
-      bool split = false;
-      if (a.reg.n > 0) {
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int start = t0 + 32 * c;
-#pragma unroll
-          for (int k = 1; k < kMaxRegions; ++k)
-            kc[c] += (k < a.reg.n && a.reg.b[k] <= start) ? 1 : 0;
-          const int end = min(start + 32, t0 + valid);
-          split |= start < end && end > a.reg.b[kc[c] + 1];
+      // Regions of the tile (the same for every row of the group): `whole`
+      // when it lies inside one region; otherwise offs holds, per 32-key
+      // chunk, the offset of the one bound strictly inside it (32: none),
+      // and `split` is set when some chunk holds two or more (tiny regions:
+      // accounted key by key during the pass, from a state kept so that a
+      // redone tile is counted once).
+      bool whole = true, split = false;
+      uint32_t offs = 0x20202020u;
+      if (nreg > 0) {
+        region_seek(racc, rb, nreg, t0);
+        for (int b = racc.k + 1; b < nreg && rb[b] < t0 + valid; ++b) {
+          whole = false;
+          const int o = rb[b] - t0, c = o >> 5, oc = o & 31;
+          if (oc == 0) continue;  // a bound on a chunk start needs no split
+          if (((offs >> (8 * c)) & 0xffu) != 32u) split = true;
+          offs = (offs & ~(0xffu << (8 * c))) | (static_cast<uint32_t>(oc) << (8 * c));
         }
       }
+      const int k_before = racc.k;
+      const float cur_before = racc.cur;
       // one pass: P = 2^(s * scale - m_used) -> shared memory, sums; the
       // group's first tile sets m_used from its first 32 scores
-      float cs[4], part[kMaxRegions], v3[32], mx, dummy0 = 0.0f, dummy1 = 0.0f;
+      float cs[4], psum[4], v3[32], mx, dummy0 = 0.0f, dummy1 = 0.0f;
       float *const set_ref = i == 0 ? &m_used : nullptr;
       if (split)
-        softmax_pass_head<true>(s_row, valid, t0, a.scale_log2, -m_used, a.reg, sm.p[g], row, cs,
-                                part, v3, mx, set_ref);
+        softmax_pass_head<true>(s_row, valid, t0, a.scale_log2, -m_used, rb, nreg, offs, sm.p[g],
+                                row, cs, psum, racc, v3, mx, set_ref);
       else
-        softmax_pass_head<false>(s_row, valid, t0, a.scale_log2, -m_used, a.reg, sm.p[g], row, cs,
-                                 part, v3, mx, set_ref);
+        softmax_pass_head<false>(s_row, valid, t0, a.scale_log2, -m_used, rb, nreg, offs, sm.p[g],
+                                 row, cs, psum, racc, v3, mx, set_ref);
       // A chunk sum bounds each of its P values: chunks 0-2 are checked by
       // their sums, chunk 3 by its raw maximum.
       const float big = fmaxf(fmaxf(cs[0], cs[1]), cs[2]);
@@ -607,46 +666,50 @@ __global__ void __launch_bounds__(384, 1)
         const float f = fast_exp2(m_used - m_new);
         m_used = m_new;
         l *= f;
-#pragma unroll
-        for (int k = 0; k < kMaxRegions; ++k) rsum[k] *= f;
+        racc.k = k_before;
+        racc.cur = cur_before * f;
+        for (int k = 0; k < k_before; ++k) done[k] *= f;
         if (i >= 1) {
           tc_fence_after();
           scale_tmem_row(o_row, f);
         }
         if (split)
-          softmax_pass_head<true>(s_row, valid, t0, a.scale_log2, -m_used, a.reg, sm.p[g], row, cs,
-                                  part, v3, mx, nullptr);
+          softmax_pass_head<true>(s_row, valid, t0, a.scale_log2, -m_used, rb, nreg, offs,
+                                  sm.p[g], row, cs, psum, racc, v3, mx, nullptr);
         else
-          softmax_pass_head<false>(s_row, valid, t0, a.scale_log2, -m_used, a.reg, sm.p[g], row,
-                                   cs, part, v3, mx, nullptr);
+          softmax_pass_head<false>(s_row, valid, t0, a.scale_log2, -m_used, rb, nreg, offs,
+                                   sm.p[g], row, cs, psum, racc, v3, mx, nullptr);
       }
       // every score of the tile is in registers: S_g may take the next tile
       tc_fence_before();
       mbar_arrive(smem_u32(&sm.s_free[g]));
       if (split)
-        softmax_chunk<true, false>(v3, 3, valid, t0, a.scale_log2, -m_used, a.reg, sm.p[g], row,
-                                   cs[3], part, dummy0, dummy1);
+        softmax_chunk<true, false>(v3, 3, valid, t0, a.scale_log2, -m_used, rb, nreg, offs,
+                                   sm.p[g], row, cs[3], psum[3], racc, dummy0, dummy1);
       else
-        softmax_chunk<false, false>(v3, 3, valid, t0, a.scale_log2, -m_used, a.reg, sm.p[g], row,
-                                    cs[3], part, dummy0, dummy1);
+        softmax_chunk<false, false>(v3, 3, valid, t0, a.scale_log2, -m_used, rb, nreg, offs,
+                                    sm.p[g], row, cs[3], psum[3], racc, dummy0, dummy1);
       // P is complete: hand it to the MMA warp, then do the bookkeeping
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       tc_fence_before();
       mbar_arrive(smem_u32(&sm.p_full[g]));
       const float tile_sum = (cs[0] + cs[1]) + (cs[2] + cs[3]);
       l += tile_sum;
-      if (a.reg.n > 0) {
-        if (split) {
-#pragma unroll
-          for (int k = 0; k < kMaxRegions; ++k) rsum[k] += part[k];
-        } else if (kc[0] == kc[3]) {  // the whole tile in one region
-#pragma unroll
-          for (int k = 0; k < kMaxRegions; ++k) rsum[k] += (kc[0] == k) ? tile_sum : 0.0f;
+      if (nreg > 0 && !split) {
+        if (whole) {
+          racc.cur += tile_sum;
         } else {
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
-#pragma unroll
-            for (int k = 0; k < kMaxRegions; ++k) rsum[k] += (kc[c] == k) ? cs[c] : 0.0f;
+          for (int c = 0; c < 4; ++c) {
+            region_seek(racc, rb, nreg, t0 + 32 * c);
+            if (((offs >> (8 * c)) & 0xffu) < 32u) {  // the chunk ends one region
+              done[racc.k] = racc.cur + psum[c];
+              racc.cur = cs[c] - psum[c];
+              ++racc.k;
+            } else {
+              racc.cur += cs[c];
+            }
+          }
         }
       }
     }
@@ -661,8 +724,11 @@ __global__ void __launch_bounds__(384, 1)
     if (mine_ok && my_tiles > 0) {
       ms[g].m[row] = m_used;
       ms[g].l[row] = l;
-#pragma unroll
-      for (int k = 0; k < kMaxRegions; ++k) ms[g].r[k][row] = rsum[k];
+      if (nreg > 0) {
+        region_seek(racc, rb, nreg, a.n_kv);  // store the open regions' sums
+        done[racc.k] = racc.cur;
+        for (int k = 0; k < nreg; ++k) ms[g].r[k][row] = done[k];
+      }
     }
     tc_fence_before();
     asm volatile("bar.sync 2, 256;" ::: "memory");
@@ -709,7 +775,7 @@ __global__ void __launch_bounds__(384, 1)
         }
       }
       if (g == 0 && a.mass && qrow < a.n_q)
-        for (int k = 0; k < a.reg.n && k < kMaxRegions; ++k)
+        for (int k = 0; k < nreg; ++k)
           a.mass[(static_cast<long>(hq) * a.n_q + qrow) * a.reg.n + k] =
               (fa * ms[0].r[k][row] + (have_b ? fb * ms[1].r[k][row] : 0.0f)) * inv;
     }

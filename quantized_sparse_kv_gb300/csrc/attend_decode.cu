@@ -799,7 +799,8 @@ int launch_attend_decode(const kvq_cache &c, const void *q, int q_dtype, float s
 // file-scope device array instead of a caller-provided workspace. Every GPU
 // that loads this module keeps the array until the process exits.
 namespace {
-constexpr size_t kStaticScratchBytes = size_t(8) << 20;  // 8 MiB
+constexpr size_t kStaticScratchBytes = KVQ_DECODE_STATIC_SCRATCH_BYTES;  // 8 MiB
+static_assert(kStaticScratchBytes == (size_t(8) << 20), "the header states 8 MiB");
 static __device__ __align__(256) unsigned char g_decode_scratch[kStaticScratchBytes];
 std::mutex g_scratch_mu;
 void *g_scratch_addr[64] = {};
@@ -809,16 +810,26 @@ size_t decode_static_scratch_limit() { return kStaticScratchBytes; }
 
 // In host code `g_decode_scratch` is only a host-side stand-in; the kernel
 // needs its device address, resolved once per device with that device current.
+// Resolving it loads this file's module on that device (with lazy module
+// loading, the CUDA default, nothing is loaded before), which is when the
+// 8 MiB are reserved. A failure leaves no sticky error behind: the runtime's
+// last error is cleared so the caller's next successful call reports success.
 cudaError_t decode_static_scratch(void **ptr) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return e;
+  }
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
   if (!g_scratch_addr[dev]) {
     void *p = nullptr;
     e = cudaGetSymbolAddress(&p, g_decode_scratch);
-    if (e != cudaSuccess) return e;
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return e;
+    }
     g_scratch_addr[dev] = p;
   }
   *ptr = g_scratch_addr[dev];

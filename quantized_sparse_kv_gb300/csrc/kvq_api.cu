@@ -81,6 +81,16 @@ kvq_status finish(int launches, const char *path) {
   return KVQ_OK;
 }
 
+// The calls that fill a cache (kv_pack, kv_append) come before any decode,
+// so they reserve the static decode scratch of the current device (loading
+// its module) before a runtime hands the rest of HBM to its own pool. A
+// failure here is not the caller's: it is cleared and kv_attend_decode_static
+// retries, returning KVQ_ERR_CUDA if the array still cannot be had.
+void reserve_static_scratch() {
+  void *p = nullptr;
+  (void)kvq::decode_static_scratch(&p);
+}
+
 float resolve_scale(float sm_scale, int head_dim) {
   return sm_scale > 0.0f ? sm_scale
                          : static_cast<float>(1.0 / sqrt(static_cast<double>(head_dim)));
@@ -153,6 +163,7 @@ kvq_status kv_pack(const void *k, const void *v, int32_t in_dtype, kvq_cache *ca
   cache->header[1] = static_cast<uint32_t>(cache->head_dim);
   cache->header[2] = static_cast<uint32_t>(cache->recent);
   cache->header[3] = 32u;
+  reserve_static_scratch();
   const int n = kvq::launch_pack(k, v, in_dtype, *cache, make_ctl(dev_status),
                                  reinterpret_cast<cudaStream_t>(stream));
   return finish(n, "pack");
@@ -180,6 +191,7 @@ kvq_status kv_append(kvq_cache *cache, const void *k_new, const void *v_new, int
   if (cut2 / 32 > cache->cap_groups || r2 > cache->cap_window) return KVQ_ERR_WORKSPACE;
   if (m > 0 && static_cast<long>(cache->batch) * cache->kv_heads > 65535)
     return KVQ_ERR_UNSUPPORTED;
+  reserve_static_scratch();
   const int n = kvq::launch_append(*cache, k_new, v_new, in_dtype, n_new, m, r2,
                                    reinterpret_cast<cudaStream_t>(stream));
   const kvq_status done = finish(n, "append");

@@ -5,7 +5,7 @@ structure of the workloads (focus variants, candidate index lists). It does
 none of the method's arithmetic (no quantization, no attention), so the
 oracle and the CUDA path can both be fed from it without sharing any code.
 
-Recipes (each is restated in the design notes):
+Recipes:
 
 * ``residual_window_inputs`` -- "KV residual window" page (huhohoo.com,
   kv-residual-window), section on where the attention mass lands: one head,
@@ -32,6 +32,9 @@ import numpy as np
 CHUNK_TOKENS_PER_LF = 390
 CHUNK_REGION_BOUNDS = (0, 4 * 390, 10 * 390, 16 * 390)  # (0, 1560, 3900, 6240)
 CHUNK_N_Q = 6 * 390  # 2340
+# One region per latent frame: the 16 key-LF columns of the page's temporal
+# attention heatmap (each query row's 16 masses sum to 100 %).
+CHUNK_LF_BOUNDS = tuple(390 * i for i in range(17))  # (0, 390, ..., 6240)
 
 
 def residual_window_inputs(seed: int, n: int, *, variant: str = "clean",

@@ -162,6 +162,19 @@ def test_attend_region_mass_fp32(kvq):
     np.testing.assert_allclose(to_np(mass).sum(-1), 1.0, atol=1e-5)
 
 
+def test_attend_sixteen_regions_fp32(kvq):
+    # the fp32 kernel with the largest region count the call takes
+    q, k, v = synth.residual_window_batch(5, 512, 4, variant="early")
+    bounds = [0, 1, 2, 5, 16, 17, 40, 64, 100, 128, 200, 255, 256, 300, 480, 511, 512]
+    cache = kvq.pack(torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda(), 64, "f32")
+    out, mass, path = kvq.attend(cache, torch.from_numpy(q).cuda(), out_dtype="f32",
+                                 region_bounds=bounds)
+    assert path == "generic"
+    ref, ref_mass = O.attend(q, O.pack(k, v, 64, "f32"), region_bounds=bounds)
+    assert O.rel_l2(to_np(out), ref) <= TOL_F32
+    np.testing.assert_allclose(to_np(mass), ref_mass, atol=TOL_MASS, rtol=0)
+
+
 # ------------------------------------------------------------------ decode (int4 + bf16 window)
 
 
@@ -361,6 +374,67 @@ def test_chunk_bf16_full_size_sampled_heads(kvq):
     np.testing.assert_allclose(to_np(mass).sum(-1), 1.0, atol=1e-4)
 
 
+@pytest.mark.parametrize("hq,hkv,n_q,n_kv,bounds,conc", [
+    # 16 regions of one latent frame each (390 keys), as the page's heatmap
+    (2, 1, 200, 6240, list(synth.CHUNK_LF_BOUNDS), 3.0),
+    # tiny regions: several bounds inside one 32-key chunk, a region of one
+    # key, bounds on tile and chunk edges, a ragged last tile
+    (2, 2, 130, 700, [0, 1, 2, 3, 31, 32, 33, 64, 100, 127, 128, 129, 300, 301, 640, 699, 700],
+     0.0),
+    # five regions (one more than the kernel once carried)
+    (4, 2, 128, 1000, [0, 200, 390, 512, 999, 1000], 2.0),
+])
+def test_chunk_bf16_many_regions(kvq, hq, hkv, n_q, n_kv, bounds, conc):
+    q, k, v = chunk_case(100 + len(bounds), hq, hkv, n_q, n_kv, conc)
+    cache = kvq.pack(bf16_cuda(k), bf16_cuda(v), n_kv, "bf16")
+    out, mass, path = kvq.attend(cache, bf16_cuda(q), out_dtype="f32", region_bounds=bounds)
+    assert path == "chunk_bf16"
+    ref, ref_mass = O.attend(q, O.pack(k, v, n_kv, "bf16"), region_bounds=bounds)
+    assert O.rel_l2(to_np(out), ref) <= TOL_BF16
+    np.testing.assert_allclose(to_np(mass), ref_mass, atol=TOL_MASS, rtol=0)
+    np.testing.assert_allclose(to_np(mass).sum(-1), 1.0, atol=1e-4)
+
+
+def test_chunk_bf16_many_regions_with_redone_tile(kvq):
+    # the spike of the growing-scores case inside a run of 16 small regions:
+    # the tile that holds it is redone with a new reference, and the region
+    # sums counted during the first pass of that tile must not count twice
+    rng = np.random.default_rng(12)
+    n_q, n_kv = 130, 1100
+    u = rng.standard_normal(128)
+    u /= np.linalg.norm(u)
+    q = rng.standard_normal((1, 2, n_q, 128))
+    q += (3.0 - q @ u)[..., None] * u
+    k = rng.standard_normal((1, 1, n_kv, 128)) * (1.0 + 6.0 * np.arange(n_kv) / n_kv)[:, None]
+    k[0, 0, 900:910] = 300.0 * u + 0.1 * rng.standard_normal((10, 128))
+    v = rng.standard_normal((1, 1, n_kv, 128))
+    q, k, v = (O.round_to_bf16(x.astype(np.float32)) for x in (q, k, v))
+    bounds = [0, 100, 200, 300, 400, 500, 600, 700, 800, 896, 901, 903, 905, 908, 960, 1024, n_kv]
+    cache = kvq.pack(bf16_cuda(k), bf16_cuda(v), n_kv, "bf16")
+    out, mass, path = kvq.attend(cache, bf16_cuda(q), out_dtype="f32", region_bounds=bounds)
+    assert path == "chunk_bf16"
+    ref, ref_mass = O.attend(q, O.pack(k, v, n_kv, "bf16"), region_bounds=bounds)
+    assert O.rel_l2(to_np(out), ref) <= TOL_BF16
+    np.testing.assert_allclose(to_np(mass), ref_mass, atol=TOL_MASS, rtol=0)
+    assert (ref_mass[..., 9:14].sum(-1) > 0.99).all()
+
+
+def test_chunk_bf16_full_size_sixteen_frames(kvq):
+    # the video chunk with one region per latent frame: each query row's 16
+    # key-LF masses (the page's temporal heatmap), sampled heads
+    bounds = list(synth.CHUNK_LF_BOUNDS)
+    q, k, v = synth.chunk_inputs_torch(13, "cuda", concentrated=4.0)
+    cache = kvq.pack(k, v, bounds[-1], "bf16")
+    out, mass, path = kvq.attend(cache, q, out_dtype="f32", region_bounds=bounds)
+    assert path == "chunk_bf16"
+    qn, kn, vn = to_np(q), to_np(k), to_np(v)
+    for h in (0, 17, 31):
+        ref, _, ref_mass = O.attention(qn[0, h], kn[0, h], vn[0, h], region_bounds=bounds)
+        assert O.rel_l2(to_np(out)[0, h], ref) <= TOL_BF16
+        np.testing.assert_allclose(to_np(mass)[0, h], ref_mass, atol=TOL_MASS, rtol=0)
+    np.testing.assert_allclose(to_np(mass).sum(-1), 1.0, atol=1e-4)
+
+
 def history_reference(q, k, v, recent, bounds):
     """Oracle attention over an int4 history + bf16 window, two ways: with the
     dequantized history exact (fp64), and with it rounded once to bf16, which is
@@ -447,6 +521,29 @@ def test_chunk_mxfp8_matches_oracle(kvq, hq, hkv, n_q, n_kv, bounds):
     out_g, _, path_g = kvq.attend(cache_g, bf16_cuda(q[:, :, :63]), out_dtype="f32")
     assert path_g == "generic"
     assert O.rel_l2(to_np(out_g), to_np(out)[:, :, :63]) <= TOL_BF16
+
+
+def test_chunk_mxfp8_full_size_sampled_heads(kvq):
+    # the video chunk on the MXFP8 Q/K path at full size (32 heads, 2,340
+    # queries over 6,240 keys), three sampled heads against the oracle on
+    # MXFP8-rounded Q and K
+    bounds = list(synth.CHUNK_REGION_BOUNDS)
+    q, k, v = synth.chunk_inputs_torch(21, "cuda")
+    cache = kvq.pack(k, v, bounds[-1], "mxfp8", "bf16")
+    out, mass, path = kvq.attend(cache, q, out_dtype="f32", region_bounds=bounds)
+    assert path == "chunk_mxfp8"
+    heads = (0, 17, 31)
+    qn = to_np(q)[0, heads].astype(np.float64)
+    kn = to_np(k)[0, heads].astype(np.float64)
+    vn = to_np(v)[0, heads]
+    qh = O.mxfp8_dequantize(*O.mxfp8_quantize(qn))
+    kh = O.mxfp8_dequantize(*O.mxfp8_quantize(kn))
+    got, got_mass = to_np(out), to_np(mass)
+    for i, h in enumerate(heads):
+        ref, _, ref_mass = O.attention(qh[i], kh[i], vn[i], region_bounds=bounds)
+        assert O.rel_l2(got[0, h], ref) <= TOL_BF16
+        np.testing.assert_allclose(got_mass[0, h], ref_mass, atol=TOL_MASS, rtol=0)
+    np.testing.assert_allclose(got_mass.sum(-1), 1.0, atol=1e-4)
 
 
 def test_chunk_mxfp8_changes_probabilities_little(kvq):
