@@ -41,21 +41,48 @@ namespace kvq {
 namespace {
 
 constexpr int kBM = 128;          // query rows per CTA
-constexpr int kBN = 128;          // keys per tile
 constexpr int kDim = 128;         // head dim
-constexpr int kKStages = 2;
-constexpr int kVStages = 2;
 constexpr int kMaxRegions = 16;
-constexpr uint32_t kTileBytes = kBN * kDim * 2;  // 32 KB, one K or V tile (bf16)
-constexpr uint32_t kHalfBytes = kTileBytes / 2;  // 16 KB: 128 rows x 64 features
+constexpr uint32_t kHalfBytes = 128u * 128u;     // 16 KB: 128 rows x 128 B (P, bf16 Q and K)
 constexpr float kRedoThreshold = 64.0f;           // log2 units: P stays below 2^64
 constexpr float kRedoBound = 18446744073709551616.0f;  // 2^64
 
+// Tile geometry of the two variants. bf16 Q/K: 128-key tiles, Q and K tiles
+// as two 64-feature halves of 128 B rows. MXFP8 Q/K: E4M3 rows of 128 B
+// (one swizzle row per token), 112-key tiles: S then takes 112 TMEM columns
+// per group, which leaves columns 496-511 free for the E8M0 scale vectors.
+template <bool kMx>
+struct Tile {
+  static constexpr int BN = kMx ? 112 : 128;                         // keys per tile
+  static constexpr int KStages = kMx ? 3 : 2;                        // K tile ring
+  static constexpr int VStages = kMx ? 3 : 2;                        // V tile ring
+  static constexpr uint32_t QBytes = kMx ? 128u * 128u : 2u * kHalfBytes;
+  static constexpr uint32_t KBytes = kMx ? BN * 128u : 2u * kHalfBytes;
+  static constexpr uint32_t VHalf = BN * 128u;                       // 64 features x BN rows
+  static constexpr uint32_t VBytes = 2u * VHalf;
+};
+
+// Scale-factor block of a 128-row (or key) MXFP8 tile as the tensor core reads
+// it from TMEM: byte (r % 32) * 16 + (r / 32) * 4 + b holds the E8M0 scale of
+// row r and 32-feature block b. tcgen05.cp (32 rows x 16 B, replicated to the
+// four lane quadrants) moves it to four TMEM columns: lane r % 32 (+ 32 q),
+// column r / 32, byte b; the MMA picks byte b through its scale-factor ids.
+__host__ __device__ constexpr uint32_t sf_offset(int r, int b) {
+  return static_cast<uint32_t>((r % 32) * 16 + (r / 32) * 4 + b);
+}
+
+constexpr int kBN = Tile<false>::BN;  // key tile of the bf16 variant (int4 history, lists)
+
+template <bool kMx>
 struct __align__(1024) ChunkSmem {
-  uint8_t q[kTileBytes];                    // 2 x [128 rows][128 B], swizzled
-  uint8_t k[kKStages][kTileBytes];
-  uint8_t v[kVStages][kTileBytes];
-  uint8_t p[2][kTileBytes];                 // P (bf16) of group A and B, K-major A operand
+  static constexpr int kKStages = Tile<kMx>::KStages;
+  static constexpr int kVStages = Tile<kMx>::VStages;
+  uint8_t q[Tile<kMx>::QBytes];             // bf16: 2 x [128 rows][128 B]; MXFP8: [128][128 B]
+  uint8_t k[kKStages][Tile<kMx>::KBytes];   // swizzled like q, BN rows
+  uint8_t v[kVStages][Tile<kMx>::VBytes];   // 2 x [BN rows][128 B] (64 features each)
+  uint8_t p[2][2 * kHalfBytes];             // P (bf16) of group A and B, K-major A operand
+  uint8_t sfa[kMx ? 512 : 16];              // MXFP8: Q scale block
+  uint8_t sfb[kKStages][kMx ? 512 : 16];    // MXFP8: K scale block per stage
   uint64_t q_full;
   uint64_t k_full[kKStages], k_empty[kKStages], v_full[kVStages], v_empty[kVStages];
   uint64_t s_full[2], s_free[2], p_full[2], o_done[2], mma_done;
@@ -64,13 +91,16 @@ struct __align__(1024) ChunkSmem {
   int rb[kMaxRegions + 1];                  // region bounds (a copy of ChunkArgs::reg.b)
 };
 
-// The two groups' row states for the final merge, laid over K stage 0, which
-// no copy or MMA touches any more once a group has seen its last PV complete.
+// The two groups' row states for the final merge, laid over the Q tile and
+// the first K stage (contiguous), which no copy or MMA touches any more once
+// a group has seen its last PV complete: every QK MMA was issued before it.
 struct MergeState {
   float m[kBM], l[kBM];
   float r[kMaxRegions][kBM];
 };
-static_assert(2 * sizeof(MergeState) <= kTileBytes, "merge states fit a K stage");
+static_assert(2 * sizeof(MergeState) <= Tile<false>::QBytes + Tile<false>::KBytes &&
+                  2 * sizeof(MergeState) <= Tile<true>::QBytes + Tile<true>::KBytes,
+              "merge states fit over Q and K stage 0");
 
 struct ChunkArgs {
   int n_q, n_kv, q_heads, kv_group, n_tiles;
@@ -87,6 +117,11 @@ struct ChunkArgs {
   float *mass;
   Regions reg;
   KernelCtl ctl;
+  // MXFP8 only: Q scale blocks [hq][q tiles][512 B]; K window scales
+  // [unit][Ws][4] (E8M0 bytes) with Ws rows per unit
+  const uint8_t *q_sf;
+  const uint8_t *k_e8m0;
+  int k_ws;
 };
 
 // ------------------------------------------------------------------ PTX wrappers
@@ -119,6 +154,38 @@ __device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t a_desc, uin
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
+}
+
+// Block-scaled E4M3 x E4M3 MMA: the E8M0 scale vectors of A (rows) and B
+// (keys) are read from TMEM at sfa / sfb; the byte used (the 32-feature block)
+// is chosen by the scale-factor ids in the instruction descriptor.
+__device__ __forceinline__ void tc_mma_mx(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t sfa, uint32_t sfb,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], "
+      "[%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+      : "memory");
+}
+
+// Shared-memory descriptor without swizzle (rows of 16 B, 8-row groups 128 B
+// apart): the source of a scale-block copy.
+__device__ __forceinline__ uint64_t smem_desc_plain(uint32_t addr) {
+  uint64_t d = static_cast<uint64_t>((addr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(16u >> 4) << 16;
+  d |= static_cast<uint64_t>(128u >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  return d;
+}
+
+// A 512-byte scale block (32 rows x 16 B) to four TMEM columns, replicated to
+// all four lane quadrants; ordered before the MMAs this thread issues next.
+__device__ __forceinline__ void tc_copy_sf(uint32_t taddr, uint32_t src) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr),
+               "l"(smem_desc_plain(src))
+               : "memory");
 }
 
 // 32 consecutive TMEM columns of this thread's lane.
@@ -186,21 +253,28 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
 }
 
 // Instruction descriptor, kind::f16: bf16 A and B, fp32 accumulator, M=128,
-// N=128, A K-major, B K-major (b_mn_major = 0) or MN-major (1).
-__host__ __device__ constexpr uint32_t idesc_bf16(uint32_t b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | (b_mn_major << 16) | ((128u >> 3) << 17) |
+// N=n, A K-major, B K-major (b_mn_major = 0) or MN-major (1).
+__host__ __device__ constexpr uint32_t idesc_bf16(uint32_t b_mn_major, uint32_t n = 128) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (b_mn_major << 16) | ((n >> 3) << 17) |
          ((128u >> 4) << 24);
 }
 
-__device__ __forceinline__ bool cta_aborted(ChunkSmem &sm) {
-  return *reinterpret_cast<volatile int *>(&sm.abort_flag) != 0;
+// Instruction descriptor, kind::mxf8f6f4 block-scaled: E4M3 A and B (format
+// 0), both K-major, N=n, UE8M0 scales (bit 23), M=128; the scale-factor ids of
+// B (bits 4-5) and A (bits 29-30) select byte `blk` of the scale vectors.
+__host__ __device__ constexpr uint32_t idesc_mx(uint32_t n, uint32_t blk) {
+  return (blk << 4) | ((n >> 3) << 17) | (1u << 23) | ((128u >> 4) << 24) | (blk << 29);
 }
 
-__device__ __forceinline__ bool wait_or_abort(ChunkSmem &sm, uint32_t bar, uint32_t parity,
+__device__ __forceinline__ bool cta_aborted(int *abort_flag) {
+  return *reinterpret_cast<volatile int *>(abort_flag) != 0;
+}
+
+__device__ __forceinline__ bool wait_or_abort(int *abort_flag, uint32_t bar, uint32_t parity,
                                               const KernelCtl &ctl) {
   if (mbar_wait(bar, parity, ctl.wait_limit_ns)) return true;
   flag_error(ctl, KVQ_DEV_TIMEOUT);
-  *reinterpret_cast<volatile int *>(&sm.abort_flag) = 1;
+  *reinterpret_cast<volatile int *>(abort_flag) = 1;
   return false;
 }
 
@@ -328,6 +402,27 @@ __device__ __forceinline__ void softmax_chunk(float (&v)[32], int c, int valid, 
       else
         add2(ps4[0], ps4[1], v[e], v[e + 1]);
     }
+  } else if (32 * c + 16 == valid) {
+    // exactly 16 keys (the last chunk of a 112-key tile)
+    if (kMax) {
+#pragma unroll
+      for (int e = 0; e < 16; e += 2) {
+        mx0 = fmaxf(mx0, v[e]);
+        mx1 = fmaxf(mx1, v[e + 1]);
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 16; e += 2) {
+      fma2(v[e], v[e + 1], v[e], v[e + 1], scale, neg_m);
+      v[e] = fast_exp2(v[e]);
+      v[e + 1] = fast_exp2(v[e + 1]);
+      if (e & 2)
+        add2(ps4[2], ps4[3], v[e], v[e + 1]);
+      else
+        add2(ps4[0], ps4[1], v[e], v[e + 1]);
+    }
+#pragma unroll
+    for (int e = 16; e < 32; ++e) v[e] = 0.0f;
   } else {
 #pragma unroll
     for (int e = 0; e < 32; ++e) {
@@ -376,14 +471,14 @@ __device__ __forceinline__ void softmax_chunk(float (&v)[32], int c, int valid, 
 // next is in flight; chunk 3 is left raw in v3, and mx is its raw maximum, so
 // that the caller can release S before finishing it. cs[c]: sum of chunk c.
 // With set_ref (a group's first tile) the reference is taken from chunk 0's
-// maximum, stored in *set_ref, and used for the whole tile.
+// maximum, stored in ref_out, and used for the whole tile.
 template <bool kSplit>
 __device__ __forceinline__ void softmax_pass_head(uint32_t taddr, int valid, int t0, float scale,
                                                   float neg_m, const int *rb, int nreg,
                                                   uint32_t offs, uint8_t *p, int row,
                                                   float (&cs)[4], float (&psum)[4],
                                                   RegionAcc &racc, float (&v3)[32], float &mx,
-                                                  float *set_ref) {
+                                                  bool set_ref, float &ref_out) {
   float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F;
   float va[32];
   tmem_ld32(taddr, va);
@@ -398,7 +493,7 @@ __device__ __forceinline__ void softmax_pass_head(uint32_t taddr, int valid, int
       r1 = fmaxf(r1, e + 1 < valid ? va[e + 1] : -CUDART_INF_F);
     }
     const float ref = fmaxf(r0, r1) * scale;  // scale > 0 keeps the order
-    *set_ref = ref;
+    ref_out = ref;
     neg_m = -ref;
   }
   softmax_chunk<kSplit, false>(va, 0, valid, t0, scale, neg_m, rb, nreg, offs, p, row, cs[0],
@@ -415,9 +510,15 @@ __device__ __forceinline__ void softmax_pass_head(uint32_t taddr, int valid, int
                                psum[2], racc, mx0, mx1);
   tmem_wait_ld();
   reg_fence(v3);
-  if (valid == kBN) {
+  if (valid >= 128) {
 #pragma unroll
     for (int e = 0; e < 32; e += 2) {
+      mx0 = fmaxf(mx0, v3[e]);
+      mx1 = fmaxf(mx1, v3[e + 1]);
+    }
+  } else if (valid == 112) {
+#pragma unroll
+    for (int e = 0; e < 16; e += 2) {
       mx0 = fmaxf(mx0, v3[e]);
       mx1 = fmaxf(mx1, v3[e + 1]);
     }
@@ -431,16 +532,21 @@ __device__ __forceinline__ void softmax_pass_head(uint32_t taddr, int valid, int
   mx = fmaxf(mx0, mx1);
 }
 
-__global__ void __launch_bounds__(384, 1)
-    chunk_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
-                      const __grid_constant__ CUtensorMap tm_k,
-                      const __grid_constant__ CUtensorMap tm_v,
-                      const __grid_constant__ CUtensorMap tm_kw,
-                      const __grid_constant__ CUtensorMap tm_vw, const ChunkArgs a) {
+// The kernel body, for bf16 Q/K (kind::f16 QK) and MXFP8 Q/K (block-scaled
+// kind::mxf8f6f4 QK); PV is a bf16 kind::f16 MMA in both.
+template <bool kMx>
+__device__ __forceinline__ void chunk_body(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
+                                           const CUtensorMap &tm_v, const CUtensorMap &tm_kw,
+                                           const CUtensorMap &tm_vw, const ChunkArgs &a) {
+  using T = Tile<kMx>;
+  constexpr int BN = T::BN;
+  constexpr int kKStages = T::KStages, kVStages = T::VStages;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // dynamic shared memory is only 16-byte aligned: round up to 1024
   const uint32_t base = smem_u32(smem_raw);
-  ChunkSmem &sm = *reinterpret_cast<ChunkSmem *>(smem_raw + (((base + 1023u) & ~1023u) - base));
+  ChunkSmem<kMx> &sm =
+      *reinterpret_cast<ChunkSmem<kMx> *>(smem_raw + (((base + 1023u) & ~1023u) - base));
+  int *const abort_flag = &sm.abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q0 = blockIdx.x * kBM;
   const int hq = blockIdx.y;                 // b * q_heads + h
@@ -450,9 +556,9 @@ __global__ void __launch_bounds__(384, 1)
   const int nt = a.n_tiles;
 
   if (threadIdx.x == 0) {
-    mbar_init(smem_u32(&sm.q_full), 1);
+    mbar_init(smem_u32(&sm.q_full), kMx ? 32 : 1);
     for (int s = 0; s < kKStages; ++s) {
-      mbar_init(smem_u32(&sm.k_full[s]), 1);
+      mbar_init(smem_u32(&sm.k_full[s]), kMx ? 32 : 1);
       mbar_init(smem_u32(&sm.k_empty[s]), 1);
     }
     for (int s = 0; s < kVStages; ++s) {
@@ -471,6 +577,12 @@ __global__ void __launch_bounds__(384, 1)
     for (int i = 0; i <= kMaxRegions; ++i) sm.rb[i] = a.reg.b[i];
     fence_mbar_init();
   }
+  if (kMx && warp == 3) {
+    // the scale slots of rows 112-127 of a key block are never written:
+    // give them a valid scale (1.0) once, so no byte is ever NaN
+    for (int i = lane; i < kKStages * 128; i += 32)
+      reinterpret_cast<uint32_t *>(sm.sfb)[i] = 0x7f7f7f7fu;
+  }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(
                      smem_u32(&sm.tmem_base))
@@ -481,36 +593,84 @@ __global__ void __launch_bounds__(384, 1)
   __syncthreads();
   tc_fence_after();
   // The barriers and TMEM are set up while the previous kernel drains; its
-  // outputs (the expanded or gathered K and V rows) are read only after this.
+  // outputs (the expanded or gathered K and V rows, the MXFP8 Q) are read
+  // only after this.
   wait_prior_grid();
   allow_next_grid();
   const uint32_t tmem = sm.tmem_base;
-  // group g: S at columns 256g, O at 256g + 128
-  auto t_s = [&](int g) { return tmem + 256u * g; };
-  auto t_o = [&](int g) { return tmem + 256u * g + 128u; };
+  // bf16: group g's S at columns 256g, O at 256g + 128. MXFP8: O at 128g, S
+  // (112 columns) at 256 + 128g, Q scales at 496, K scales of stage s at 500 + 4s.
+  auto t_s = [&](int g) { return tmem + (kMx ? 256u + 128u * g : 256u * g); };
+  auto t_o = [&](int g) { return tmem + (kMx ? 128u * g : 256u * g + 128u); };
+  const uint32_t t_sfa = tmem + 496u;
+  auto t_sfb = [&](int st) { return tmem + 500u + 4u * st; };
 
   if (warp == 0) {
     // ------------------------------------------------ TMA producer: Q, then K tiles
+    // With MXFP8 every lane also moves scale bytes into the stage's scale
+    // block and arrives on its barrier (32 arrivals); lane 0 posts the
+    // copy's byte count first so that the phase waits for the copy too.
+    const uint32_t qb = smem_u32(&sm.q_full);
     if (lane == 0) {
-      const uint32_t qb = smem_u32(&sm.q_full);
-      mbar_arrive_expect_tx(qb, kTileBytes);
+      if (kMx)
+        mbar_expect_tx(qb, T::QBytes);
+      else
+        mbar_arrive_expect_tx(qb, T::QBytes);
       tma_load_3d(smem_u32(sm.q), &tm_q, 0, q0, hq, qb);
-      tma_load_3d(smem_u32(sm.q) + kHalfBytes, &tm_q, 64, q0, hq, qb);
-      // a stage is reused once the MMA reading it has completed
-      int kj = 0;
-      for (; kj < nt; ++kj) {
-        const int st = kj % kKStages, use = kj / kKStages;
-        if (use > 0 && !wait_or_abort(sm, smem_u32(&sm.k_empty[st]), (use - 1) & 1, a.ctl)) break;
-        if (cta_aborted(sm)) break;
-        const uint32_t fb = smem_u32(&sm.k_full[st]);
-        mbar_arrive_expect_tx(fb, kTileBytes);
+      if (!kMx) tma_load_3d(smem_u32(sm.q) + kHalfBytes, &tm_q, 64, q0, hq, qb);
+    }
+    // MXFP8: the K scales of a tile are loaded into registers one tile ahead
+    // (lane l holds keys l, l + 32, l + 64, l + 96; 1.0 past the last key)
+    uint32_t sfw[4] = {0u, 0u, 0u, 0u};
+    auto load_sf = [&](int kj) {
+      const int valid = min(BN, a.n_kv - kj * BN);
+      const uint32_t *e8 = reinterpret_cast<const uint32_t *>(a.k_e8m0) +
+                           static_cast<long>(hkv) * a.k_ws + kj * BN;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) sfw[i] = lane + 32 * i < valid ? e8[lane + 32 * i] : 0x7f7f7f7fu;
+    };
+    if (kMx) {
+      // the Q tile's scale block, laid out by the prologue as the MMA reads it
+      const uint4 *src = reinterpret_cast<const uint4 *>(
+          a.q_sf + (static_cast<long>(hq) * gridDim.x + blockIdx.x) * 512);
+      reinterpret_cast<uint4 *>(sm.sfa)[lane] = src[lane];
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      mbar_arrive(qb);
+      if (nt > 0) load_sf(0);
+    }
+    // a stage is reused once the MMA reading it has completed
+    int kj = 0;
+    for (; kj < nt; ++kj) {
+      const int st = kj % kKStages, use = kj / kKStages;
+      // every lane waits: with MXFP8 every lane then writes the stage's scales
+      bool go = use == 0 ||
+                wait_or_abort(abort_flag, smem_u32(&sm.k_empty[st]), (use - 1) & 1, a.ctl);
+      go = __all_sync(0xffffffffu, go) && !cta_aborted(abort_flag);
+      if (!go) break;
+      const uint32_t fb = smem_u32(&sm.k_full[st]);
+      if (lane == 0) {
+        if (kMx)
+          mbar_expect_tx(fb, T::KBytes);
+        else
+          mbar_arrive_expect_tx(fb, T::KBytes);
         const bool hist = kj < a.hist_tiles;
         const CUtensorMap *mk = hist ? &tm_k : &tm_kw;
-        const int ky = hist ? kj * kBN : kj * kBN - a.win_off;
+        const int ky = hist ? kj * BN : kj * BN - a.win_off;
         tma_load_3d(smem_u32(sm.k[st]), mk, 0, ky, hkv, fb);
-        tma_load_3d(smem_u32(sm.k[st]) + kHalfBytes, mk, 64, ky, hkv, fb);
+        if (!kMx) tma_load_3d(smem_u32(sm.k[st]) + kHalfBytes, mk, 64, ky, hkv, fb);
       }
-      // drain: the copies of the last stages must land before the CTA exits
+      if (kMx) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          if (lane + 32 * i < BN)
+            *reinterpret_cast<uint32_t *>(sm.sfb[st] + sf_offset(lane + 32 * i, 0)) = sfw[i];
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_arrive(fb);
+        if (kj + 1 < nt) load_sf(kj + 1);
+      }
+    }
+    // drain: the copies of the last stages must land before the CTA exits
+    if (lane == 0) {
       mbar_wait(qb, 0, 2000000000ull);
       for (int d = (kj > kKStages ? kj - kKStages : 0); d < kj; ++d)
         mbar_wait(smem_u32(&sm.k_full[d % kKStages]), (d / kKStages) & 1, 2000000000ull);
@@ -521,15 +681,17 @@ __global__ void __launch_bounds__(384, 1)
       int vj = 0;
       for (; vj < nt; ++vj) {
         const int st = vj % kVStages, use = vj / kVStages;
-        if (use > 0 && !wait_or_abort(sm, smem_u32(&sm.v_empty[st]), (use - 1) & 1, a.ctl)) break;
-        if (cta_aborted(sm)) break;
+        if (use > 0 &&
+            !wait_or_abort(abort_flag, smem_u32(&sm.v_empty[st]), (use - 1) & 1, a.ctl))
+          break;
+        if (cta_aborted(abort_flag)) break;
         const uint32_t fb = smem_u32(&sm.v_full[st]);
-        mbar_arrive_expect_tx(fb, kTileBytes);
+        mbar_arrive_expect_tx(fb, T::VBytes);
         const bool hist = vj < a.hist_tiles;
         const CUtensorMap *mv = hist ? &tm_v : &tm_vw;
-        const int vy = hist ? vj * kBN : vj * kBN - a.win_off;
+        const int vy = hist ? vj * BN : vj * BN - a.win_off;
         tma_load_3d(smem_u32(sm.v[st]), mv, 0, vy, hkv, fb);
-        tma_load_3d(smem_u32(sm.v[st]) + kHalfBytes, mv, 64, vy, hkv, fb);
+        tma_load_3d(smem_u32(sm.v[st]) + T::VHalf, mv, 64, vy, hkv, fb);
       }
       for (int d = (vj > kVStages ? vj - kVStages : 0); d < vj; ++d)
         mbar_wait(smem_u32(&sm.v_full[d % kVStages]), (d / kVStages) & 1, 2000000000ull);
@@ -539,18 +701,31 @@ __global__ void __launch_bounds__(384, 1)
     if (lane == 0) {
       constexpr uint32_t id_qk = idesc_bf16(0), id_pv = idesc_bf16(1);
       const uint32_t qa = smem_u32(sm.q);
-      bool ok = wait_or_abort(sm, smem_u32(&sm.q_full), 0, a.ctl);
+      bool ok = wait_or_abort(abort_flag, smem_u32(&sm.q_full), 0, a.ctl);
+      if (kMx && ok) {
+        tc_fence_after();
+        tc_copy_sf(t_sfa, smem_u32(sm.sfa));
+      }
       // S_j = Q K_j^T into group j % 2's S
       auto issue_s = [&](int j) -> bool {
         const int st = j % kKStages, g = j & 1;
-        if (!wait_or_abort(sm, smem_u32(&sm.k_full[st]), (j / kKStages) & 1, a.ctl)) return false;
+        if (!wait_or_abort(abort_flag, smem_u32(&sm.k_full[st]), (j / kKStages) & 1, a.ctl))
+          return false;
         tc_fence_after();
         const uint32_t ka = smem_u32(sm.k[st]);
+        if (kMx) {
+          tc_copy_sf(t_sfb(st), smem_u32(sm.sfb[st]));
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32u;
-          tc_mma_f16(t_s(g), smem_desc(qa + off, 16, 1024), smem_desc(ka + off, 16, 1024), id_qk,
-                     kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < 4; ++kk)
+            tc_mma_mx(t_s(g), smem_desc(qa + 32u * kk, 16, 1024), smem_desc(ka + 32u * kk, 16, 1024),
+                      idesc_mx(BN, kk), t_sfa, t_sfb(st), kk > 0 ? 1u : 0u);
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32u;
+            tc_mma_f16(t_s(g), smem_desc(qa + off, 16, 1024), smem_desc(ka + off, 16, 1024),
+                       id_qk, kk > 0 ? 1u : 0u);
+          }
         }
         tc_commit(smem_u32(&sm.s_full[g]));
         tc_commit(smem_u32(&sm.k_empty[st]));
@@ -562,23 +737,23 @@ __global__ void __launch_bounds__(384, 1)
         const int st = j % kVStages, g = j & 1, i = j >> 1;
         // S_g can take tile j + 2 as soon as group g holds tile j's scores in
         // registers, before its P is written
-        if (j + 2 < nt && (!wait_or_abort(sm, smem_u32(&sm.s_free[g]), i & 1, a.ctl) ||
-                           !issue_s(j + 2))) {
+        if (j + 2 < nt &&
+            (!wait_or_abort(abort_flag, smem_u32(&sm.s_free[g]), i & 1, a.ctl) || !issue_s(j + 2))) {
           ok = false;
           break;
         }
         // O_g += P_g V_j once group g has written P for tile j
-        if (!wait_or_abort(sm, smem_u32(&sm.p_full[g]), i & 1, a.ctl) ||
-            !wait_or_abort(sm, smem_u32(&sm.v_full[st]), (j / kVStages) & 1, a.ctl)) {
+        if (!wait_or_abort(abort_flag, smem_u32(&sm.p_full[g]), i & 1, a.ctl) ||
+            !wait_or_abort(abort_flag, smem_u32(&sm.v_full[st]), (j / kVStages) & 1, a.ctl)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t pa = smem_u32(sm.p[g]), va = smem_u32(sm.v[st]);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
+        for (int kk = 0; kk < BN / 16; ++kk) {
           const uint64_t ad = smem_desc(pa + (kk >> 2) * kHalfBytes + (kk & 3) * 32u, 16, 1024);
-          const uint64_t bd = smem_desc(va + kk * 2048u, kHalfBytes, 1024);
+          const uint64_t bd = smem_desc(va + kk * 2048u, T::VHalf, 1024);
           tc_mma_f16(t_o(g), ad, bd, id_pv, (i > 0 || kk > 0) ? 1u : 0u);
         }
         tc_commit(smem_u32(&sm.o_done[g]));
@@ -612,16 +787,16 @@ __global__ void __launch_bounds__(384, 1)
     bool ok = true;
     for (int i = 0; i < my_tiles; ++i) {
       const int j = 2 * i + g;
-      if (!wait_or_abort(sm, smem_u32(&sm.s_full[g]), i & 1, a.ctl)) {
+      if (!wait_or_abort(abort_flag, smem_u32(&sm.s_full[g]), i & 1, a.ctl)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const int valid = min(kBN, a.n_kv - j * kBN);
-      const int t0 = j * kBN;
+      const int valid = min(BN, a.n_kv - j * BN);
+      const int t0 = j * BN;
       // O_g += P V of the previous tile must be done before P_g is rewritten
       // or O_g is rescaled
-      if (i >= 1 && !wait_or_abort(sm, smem_u32(&sm.o_done[g]), (i - 1) & 1, a.ctl)) {
+      if (i >= 1 && !wait_or_abort(abort_flag, smem_u32(&sm.o_done[g]), (i - 1) & 1, a.ctl)) {
         ok = false;
         break;
       }
@@ -648,20 +823,25 @@ __global__ void __launch_bounds__(384, 1)
       // one pass: P = 2^(s * scale - m_used) -> shared memory, sums; the
       // group's first tile sets m_used from its first 32 scores
       float cs[4], psum[4], v3[32], mx, dummy0 = 0.0f, dummy1 = 0.0f;
-      float *const set_ref = i == 0 ? &m_used : nullptr;
-      if (split)
-        softmax_pass_head<true>(s_row, valid, t0, a.scale_log2, -m_used, rb, nreg, offs, sm.p[g],
-                                row, cs, psum, racc, v3, mx, set_ref);
-      else
-        softmax_pass_head<false>(s_row, valid, t0, a.scale_log2, -m_used, rb, nreg, offs, sm.p[g],
-                                 row, cs, psum, racc, v3, mx, set_ref);
-      // A chunk sum bounds each of its P values: chunks 0-2 are checked by
-      // their sums, chunk 3 by its raw maximum.
-      const float big = fmaxf(fmaxf(cs[0], cs[1]), cs[2]);
-      if (__any_sync(0xffffffffu, !(big <= kRedoBound) || mx * a.scale_log2 > m_used + kRedoThreshold)) {
+      bool set_ref = i == 0;
+      for (;;) {
+        if (split)
+          softmax_pass_head<true>(s_row, valid, t0, a.scale_log2, -m_used, rb, nreg, offs,
+                                  sm.p[g], row, cs, psum, racc, v3, mx, set_ref, m_used);
+        else
+          softmax_pass_head<false>(s_row, valid, t0, a.scale_log2, -m_used, rb, nreg, offs,
+                                   sm.p[g], row, cs, psum, racc, v3, mx, set_ref, m_used);
+        // A chunk sum bounds each of its P values: chunks 0-2 are checked by
+        // their sums, chunk 3 by its raw maximum.
+        const float big = fmaxf(fmaxf(cs[0], cs[1]), cs[2]);
+        if (!__any_sync(0xffffffffu,
+                        !(big <= kRedoBound) || mx * a.scale_log2 > m_used + kRedoThreshold))
+          break;
         // far above the reference for some row (P could overflow): the warp
         // takes the tile maxima now and redoes the tile from its scores, still
-        // in TMEM (TMEM access is warp-wide); O_g is idle, its last MMA is done
+        // in TMEM (TMEM access is warp-wide); O_g is idle, its last MMA is
+        // done. The new reference is the tile's maximum, so a second pass
+        // never redoes again.
         const float m_new = fmaxf(m_used, row_max(s_row, valid) * a.scale_log2);
         const float f = fast_exp2(m_used - m_new);
         m_used = m_new;
@@ -673,12 +853,7 @@ __global__ void __launch_bounds__(384, 1)
           tc_fence_after();
           scale_tmem_row(o_row, f);
         }
-        if (split)
-          softmax_pass_head<true>(s_row, valid, t0, a.scale_log2, -m_used, rb, nreg, offs,
-                                  sm.p[g], row, cs, psum, racc, v3, mx, nullptr);
-        else
-          softmax_pass_head<false>(s_row, valid, t0, a.scale_log2, -m_used, rb, nreg, offs,
-                                   sm.p[g], row, cs, psum, racc, v3, mx, nullptr);
+        set_ref = false;
       }
       // every score of the tile is in registers: S_g may take the next tile
       tc_fence_before();
@@ -717,10 +892,10 @@ __global__ void __launch_bounds__(384, 1)
     // merges both groups' O for half of the columns (group g: 64g .. 64g + 63)
     const bool mine_ok =
         ok && (my_tiles == 0 ||
-               wait_or_abort(sm, smem_u32(&sm.o_done[g]), (my_tiles - 1) & 1, a.ctl));
+               wait_or_abort(abort_flag, smem_u32(&sm.o_done[g]), (my_tiles - 1) & 1, a.ctl));
     // A group's last PV is issued after the last QK, so once it has completed
-    // no MMA reads K stage 0 any more and the group may write over it.
-    MergeState *ms = reinterpret_cast<MergeState *>(sm.k[0]);
+    // no MMA reads Q or K stage 0 any more and the group may write over them.
+    MergeState *ms = reinterpret_cast<MergeState *>(sm.q);
     if (mine_ok && my_tiles > 0) {
       ms[g].m[row] = m_used;
       ms[g].l[row] = l;
@@ -736,7 +911,7 @@ __global__ void __launch_bounds__(384, 1)
     const int other_tiles = (nt - other + 1) >> 1;
     if (mine_ok &&
         (other_tiles == 0 ||
-         wait_or_abort(sm, smem_u32(&sm.o_done[other]), (other_tiles - 1) & 1, a.ctl))) {
+         wait_or_abort(abort_flag, smem_u32(&sm.o_done[other]), (other_tiles - 1) & 1, a.ctl))) {
       tc_fence_after();
       const bool have_b = nt > 1;  // group B processed at least one tile (group A always)
       const float ma = ms[0].m[row], mb = have_b ? ms[1].m[row] : -CUDART_INF_F;
@@ -788,60 +963,49 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
-// ------------------------------------------------------------------ MXFP8 Q/K prologue
+__global__ void __launch_bounds__(384, 1)
+    chunk_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
+                      const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v,
+                      const __grid_constant__ CUtensorMap tm_kw,
+                      const __grid_constant__ CUtensorMap tm_vw, const ChunkArgs a) {
+  chunk_body<false>(tm_q, tm_k, tm_v, tm_kw, tm_vw, a);
+}
+
+__global__ void __launch_bounds__(384, 1)
+    chunk_mxfp8_kernel(const __grid_constant__ CUtensorMap tm_q,
+                       const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, const ChunkArgs a) {
+  chunk_body<true>(tm_q, tm_k, tm_v, tm_k, tm_v, a);
+}
+
+// ------------------------------------------------------------------ MXFP8 Q prologue
 // The MXFP8 path (Catnip study, section "Q/K 与 probability quantization 的影响":
-// E4M3 elements with an E8M0 scale per 32 features) rounds Q to MXFP8 with the
-// same rule kv_pack applies to the K window, and expands both to bf16. Every
-// MXFP8 value (at most 4 significant bits times a power of two) is exact in
-// bf16 unless its exponent falls below bf16's subnormal range, so the bf16
-// tensor-core products equal the E4M3 products and the fp32 accumulation is
-// the same.
-
-// 2^(e - 127) as an exact float for an E8M0 byte e (e = 255, NaN, is not produced by kv_pack).
-__device__ __forceinline__ float e8m0_scale(uint32_t e) {
-  return e ? __uint_as_float(e << 23) : __uint_as_float(0x00400000u);  // 2^-127 is subnormal
-}
-
-// K window: E4M3 codes + E8M0 block bytes -> bf16, 16 codes (one half block)
-// per thread. cvt from e4m3x2 to f16x2 is exact; the power of two is exact.
-__device__ __forceinline__ void mxfp8_to_bf16(const uint8_t *__restrict__ codes,
-                                              const uint8_t *__restrict__ e8m0, long n16,
-                                              __nv_bfloat16 *__restrict__ out, long block,
-                                              long blocks) {
-  for (long i = block * static_cast<long>(blockDim.x) + threadIdx.x; i < n16;
-       i += blocks * blockDim.x) {
-    const uint4 c = reinterpret_cast<const uint4 *>(codes)[i];
-    const float sc = e8m0_scale(e8m0[i >> 1]);
-    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
-    uint32_t o[8];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const unsigned short pair = static_cast<unsigned short>(w[k] >> (16 * h));
-        uint32_t f16x2;
-        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(f16x2) : "h"(pair));
-        const float2 f = __half22float2(*reinterpret_cast<__half2 *>(&f16x2));
-        __nv_bfloat162 b = __floats2bfloat162_rn(f.x * sc, f.y * sc);
-        o[2 * k + h] = *reinterpret_cast<uint32_t *>(&b);
-      }
-    }
-    uint4 *dst = reinterpret_cast<uint4 *>(out) + 2 * i;
-    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
-  }
-}
-
-// Q: bf16 -> MXFP8 rounding -> bf16. Four lanes per 32-feature block, 8
-// values each (16-byte loads and stores); the block maximum takes two
-// shuffles, after which every value follows the rule kv_pack applies to an
-// MXFP8 K window in the exact steps of mxfp8_round_warp, two values per E4M3
-// conversion.
-__device__ __forceinline__ void q_mxfp8_round(const __nv_bfloat16 *__restrict__ q, long blocks,
-                                              __nv_bfloat16 *__restrict__ out, long block) {
-  const long tid = block * blockDim.x + threadIdx.x;
-  const bool live = (tid >> 2) < blocks;
-  const uint4 u = live ? reinterpret_cast<const uint4 *>(q)[tid] : make_uint4(0, 0, 0, 0);
+// E4M3 elements with an E8M0 scale per 32 features) takes K as kv_pack stored
+// it (E4M3 window + E8M0 bytes) and rounds Q to MXFP8 with the same rule here:
+// E4M3 codes [hq][n_q][128] and, per 128-row query tile, the scale block in
+// the layout the tensor core reads (sf_offset). Rows of the last tile past
+// n_q get scale 1.0 (their codes are zero: the TMA fills rows past the end).
+// Four lanes per 32-value block, 8 values each (16-byte loads); the block
+// maximum takes two shuffles, after which every value follows the rule
+// kv_pack applies to an MXFP8 K window in the exact steps of
+// mxfp8_round_warp, two values per E4M3 conversion.
+__global__ void __launch_bounds__(256) q_mxfp8_kernel(const __nv_bfloat16 *__restrict__ q,
+                                                     int n_q, int q_tiles, long n_blocks,
+                                                     uint8_t *__restrict__ codes,
+                                                     uint8_t *__restrict__ sf) {
+  wait_prior_grid();
+  allow_next_grid();
+  const long tid = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long blk = tid >> 2;                   // (hq, padded row, 32-feature block)
+  const bool live = blk < n_blocks;
+  const int kb = static_cast<int>(blk & 3);
+  const long prow = blk >> 2;                  // hq * q_tiles * 128 + padded row
+  const int r = static_cast<int>(prow % (static_cast<long>(q_tiles) * kBM));
+  const long hq = prow / (static_cast<long>(q_tiles) * kBM);
+  const bool real = live && r < n_q;
+  const long src = (hq * n_q + r) * kDim + 32 * kb + 8 * (tid & 3);
+  const uint4 u = real ? *reinterpret_cast<const uint4 *>(q + src) : make_uint4(0, 0, 0, 0);
   const uint32_t w[4] = {u.x, u.y, u.z, u.w};
   float x[8];
 #pragma unroll
@@ -856,34 +1020,22 @@ __device__ __forceinline__ void q_mxfp8_round(const __nv_bfloat16 *__restrict__ 
   amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
   if (!live) return;
   const int ex = mxfp8_block_exp(amax);
-  const float down = pow2_of(-ex), up = pow2_of(ex);
-  uint32_t o[4];
+  if ((tid & 3) == 0) {
+    const int t = r / kBM;
+    sf[(hq * q_tiles + t) * 512 + sf_offset(r % kBM, kb)] =
+        static_cast<uint8_t>(real ? ex + 127 : 127);
+  }
+  if (!real) return;
+  const float down = pow2_of(-ex);
+  uint32_t o[2] = {0u, 0u};
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const __nv_fp8x2_storage_t c = __nv_cvt_float2_to_fp8x2(
         make_float2(__fmul_rn(x[2 * j], down), __fmul_rn(x[2 * j + 1], down)), __NV_SATFINITE,
         __NV_E4M3);
-    uint32_t f16x2;
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(f16x2) : "h"(static_cast<unsigned short>(c)));
-    const float2 f = __half22float2(*reinterpret_cast<__half2 *>(&f16x2));
-    o[j] = pack_bf16x2(__fmul_rn(f.x, up), __fmul_rn(f.y, up));
+    o[j >> 1] |= static_cast<uint32_t>(c) << (16 * (j & 1));
   }
-  reinterpret_cast<uint4 *>(out)[tid] = make_uint4(o[0], o[1], o[2], o[3]);
-}
-
-// The MXFP8 prologue as one grid: blocks [0, k_blocks) expand the K window,
-// the rest round Q; the two parts are independent, so neither waits for the
-// other as two dependent launches would.
-__global__ void __launch_bounds__(256) mxfp8_prologue_kernel(
-    const uint8_t *__restrict__ codes, const uint8_t *__restrict__ e8m0, long n16,
-    __nv_bfloat16 *__restrict__ k_out, unsigned k_blocks, const __nv_bfloat16 *__restrict__ q,
-    long q_blocks, __nv_bfloat16 *__restrict__ q_out) {
-  wait_prior_grid();
-  allow_next_grid();
-  if (blockIdx.x < k_blocks)
-    mxfp8_to_bf16(codes, e8m0, n16, k_out, blockIdx.x, k_blocks);
-  else
-    q_mxfp8_round(q, q_blocks, q_out, blockIdx.x - k_blocks);
+  *reinterpret_cast<uint2 *>(codes + src) = make_uint2(o[0], o[1]);
 }
 
 // ------------------------------------------------------------------ int4 history
@@ -1052,15 +1204,32 @@ EncodeTiled encoder() {
 
 // [heads][rows][128] bf16 as a 3-D map, box 64 features x 128 rows x 1 head;
 // consecutive heads are head_rows rows apart (>= rows).
-bool make_map(CUtensorMap *m, const void *ptr, int rows, int heads, long head_rows) {
+bool make_map(CUtensorMap *m, const void *ptr, int rows, int heads, long head_rows,
+              int box_rows = 128) {
   EncodeTiled enc = encoder();
   if (!enc) return false;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kDim), static_cast<cuuint64_t>(rows),
                               static_cast<cuuint64_t>(heads)};
   const cuuint64_t strides[2] = {kDim * 2ull, static_cast<cuuint64_t>(head_rows) * kDim * 2ull};
-  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// [heads][rows][128] bytes (E4M3) as a 3-D map, box 128 bytes x box_rows x 1:
+// one 128B-swizzled row per token.
+bool make_map_e4m3(CUtensorMap *m, const void *ptr, int rows, int heads, long head_rows,
+                   int box_rows) {
+  EncodeTiled enc = encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kDim), static_cast<cuuint64_t>(rows),
+                              static_cast<cuuint64_t>(heads)};
+  const cuuint64_t strides[2] = {kDim * 1ull, static_cast<cuuint64_t>(head_rows) * kDim};
+  const cuuint32_t box[3] = {128, static_cast<cuuint32_t>(box_rows), 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(ptr), dims, strides, box,
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -1070,10 +1239,8 @@ bool make_map(CUtensorMap *m, const void *ptr, int rows, int heads, long head_ro
 // All-window caches (bf16 K, or MXFP8 K) and int4-history caches whose window,
 // if any, is bf16.
 bool chunk_supported(const kvq_cache &c, int q_dtype, int Hq, int n_q) {
-  // (the MXFP8 expansion reads a tight window)
-  const bool all_window =
-      c.recent == c.n_tokens && c.vwin_dtype == KVQ_BF16 &&
-      (c.kwin_dtype == KVQ_BF16 || (c.kwin_dtype == KVQ_MXFP8 && dims_of(c).Ws == c.recent));
+  const bool all_window = c.recent == c.n_tokens && c.vwin_dtype == KVQ_BF16 &&
+                          (c.kwin_dtype == KVQ_BF16 || c.kwin_dtype == KVQ_MXFP8);
   const bool history = c.recent < c.n_tokens &&
                        (c.recent == 0 || (c.kwin_dtype == KVQ_BF16 && c.vwin_dtype == KVQ_BF16));
   return (all_window || history) && c.head_dim == kDim && q_dtype == KVQ_BF16 && n_q >= 64 &&
@@ -1090,20 +1257,73 @@ static int expanded_rows(const kvq_cache &c) {
   return std::min(c.n_tokens, (cut + kBN - 1) / kBN * kBN);
 }
 
-// MXFP8: bf16 copies of K and of the MXFP8-rounded Q, each 256-byte aligned.
-// int4 history: bf16 K and V of the expanded rows.
+// MXFP8: E4M3 codes of Q [hq][n_q][128] (256-byte aligned size), then the Q
+// scale blocks [hq][query tiles][512]. int4 history: bf16 K and V of the
+// expanded rows.
+static size_t q_codes_bytes(const kvq_cache &c, int Hq, int n_q) {
+  return (static_cast<size_t>(c.batch) * Hq * n_q * kDim + 255) & ~size_t(255);
+}
+
 size_t chunk_workspace_bytes(const kvq_cache &c, int Hq, int n_q) {
   if (has_history(c)) {
     const size_t kb = static_cast<size_t>(c.batch) * c.kv_heads * expanded_rows(c) * kDim * 2;
     return 2 * ((kb + 255) & ~size_t(255));
   }
   if (c.kwin_dtype != KVQ_MXFP8) return 0;
-  const size_t kb = static_cast<size_t>(c.batch) * c.kv_heads * c.n_tokens * kDim * 2;
-  const size_t qb = static_cast<size_t>(c.batch) * Hq * n_q * kDim * 2;
-  return ((kb + 255) & ~size_t(255)) + qb;
+  const size_t tiles = static_cast<size_t>((n_q + kBM - 1) / kBM);
+  return q_codes_bytes(c, Hq, n_q) + static_cast<size_t>(c.batch) * Hq * tiles * 512;
 }
 
 int chunk_max_regions() { return kMaxRegions; }
+
+// MXFP8 Q/K: Q rounded to E4M3 + E8M0 in workspace, then the block-scaled
+// kernel over the cache's E4M3 K window and bf16 V window in place.
+static int launch_chunk_mxfp8(const kvq_cache &c, const void *q, int Hq, int n_q,
+                              float scale_log2, void *out, int out_dtype, const int32_t *bounds,
+                              int n_regions, float *mass, void *ws, const KernelCtl &ctl,
+                              cudaStream_t s) {
+  using T = Tile<true>;
+  const int q_tiles = (n_q + kBM - 1) / kBM;
+  const long hq_rows = static_cast<long>(c.batch) * Hq;
+  uint8_t *codes = static_cast<uint8_t *>(ws);
+  uint8_t *sf = codes + q_codes_bytes(c, Hq, n_q);
+  const long n_blocks = hq_rows * q_tiles * kBM * 4;  // 32-feature blocks, padded rows
+  launch_dependent(q_mxfp8_kernel, dim3(static_cast<unsigned>((n_blocks * 4 + 255) / 256)),
+                   dim3(256), 0, s, static_cast<const __nv_bfloat16 *>(q), n_q, q_tiles,
+                   n_blocks, codes, sf);
+  const int Ws = dims_of(c).Ws;
+  CUtensorMap tq, tk, tv;
+  if (!make_map_e4m3(&tq, codes, n_q, static_cast<int>(hq_rows), n_q, kBM) ||
+      !make_map_e4m3(&tk, c.k_window, c.n_tokens, c.batch * c.kv_heads, Ws, T::BN) ||
+      !make_map(&tv, c.v_window, c.n_tokens, c.batch * c.kv_heads, Ws, T::BN))
+    return -1;
+  ChunkArgs a;
+  a.n_q = n_q;
+  a.n_kv = c.n_tokens;
+  a.q_heads = Hq;
+  a.kv_group = Hq / c.kv_heads;
+  a.n_tiles = (c.n_tokens + T::BN - 1) / T::BN;
+  a.scale_log2 = scale_log2;
+  a.out = out;
+  a.out_dtype = out_dtype;
+  a.mass = mass;
+  a.reg = make_regions(bounds, n_regions);
+  a.ctl = ctl;
+  a.tiles_per_list = 0;
+  a.lists_per_head = 0;
+  a.hist_tiles = 0x7fffffff;
+  a.win_off = 0;
+  a.q_sf = sf;
+  a.k_e8m0 = c.k_window_e8m0;
+  a.k_ws = Ws;
+  static_assert(sizeof(ChunkSmem<true>) + 1024 <= 232448, "chunk kernel shared memory");
+  const size_t smem = sizeof(ChunkSmem<true>) + 1024;
+  cudaFuncSetAttribute(chunk_mxfp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       static_cast<int>(smem));
+  dim3 grid(q_tiles, static_cast<unsigned>(hq_rows));
+  launch_dependent(chunk_mxfp8_kernel, grid, dim3(384), smem, s, tq, tk, tv, a);
+  return 2;
+}
 
 int launch_attend_chunk(const kvq_cache &c, const void *q, int Hq, int n_q, float scale_log2,
                         void *out, int out_dtype, const int32_t *bounds, int n_regions,
@@ -1139,19 +1359,8 @@ int launch_attend_chunk(const kvq_cache &c, const void *q, int Hq, int n_q, floa
     vptr = h.v_out;
     launches += 1;
   } else if (c.kwin_dtype == KVQ_MXFP8) {
-    const long kn = static_cast<long>(c.batch) * c.kv_heads * c.n_tokens * kDim;
-    const long qn = static_cast<long>(c.batch) * Hq * n_q * kDim;
-    __nv_bfloat16 *kb = static_cast<__nv_bfloat16 *>(ws);
-    __nv_bfloat16 *qb = reinterpret_cast<__nv_bfloat16 *>(static_cast<uint8_t *>(ws) +
-                                                          ((kn * 2 + 255) & ~255L));
-    const unsigned kblocks = static_cast<unsigned>(std::min<long>((kn / 16 + 255) / 256, 1L << 20));
-    const unsigned qblocks = static_cast<unsigned>((qn / 8 + 255) / 256);
-    launch_dependent(mxfp8_prologue_kernel, dim3(kblocks + qblocks), dim3(256), 0, s,
-                     static_cast<const uint8_t *>(c.k_window), c.k_window_e8m0, kn / 16, kb,
-                     kblocks, static_cast<const __nv_bfloat16 *>(q), qn / 32, qb);
-    kptr = kb;
-    qptr = qb;
-    launches += 1;
+    return launch_chunk_mxfp8(c, q, Hq, n_q, scale_log2, out, out_dtype, bounds, n_regions, mass,
+                              ws, ctl, s);
   }
   CUtensorMap tq, tk, tv, tkw, tvw;
   // expanded K and V (history, MXFP8) are tight; an all-window cache keeps
@@ -1190,8 +1399,11 @@ int launch_attend_chunk(const kvq_cache &c, const void *q, int Hq, int n_q, floa
   a.lists_per_head = 0;
   a.hist_tiles = split ? hist_rows / kBN : 0x7fffffff;
   a.win_off = split ? c.n_tokens - c.recent : 0;
-  static_assert(sizeof(ChunkSmem) + 1024 <= 232448, "chunk kernel shared memory");
-  const size_t smem = sizeof(ChunkSmem) + 1024;
+  a.q_sf = nullptr;
+  a.k_e8m0 = nullptr;
+  a.k_ws = 0;
+  static_assert(sizeof(ChunkSmem<false>) + 1024 <= 232448, "chunk kernel shared memory");
+  const size_t smem = sizeof(ChunkSmem<false>) + 1024;
   cudaFuncSetAttribute(chunk_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        static_cast<int>(smem));
   dim3 grid((n_q + kBM - 1) / kBM, c.batch * Hq);
@@ -1266,7 +1478,10 @@ int launch_candidate_lists(const kvq_cache &c, const void *q, int Hq, int n_q,
   a.lists_per_head = lists_per_head;
   a.hist_tiles = 0x7fffffff;
   a.win_off = 0;
-  const size_t smem = sizeof(ChunkSmem) + 1024;
+  a.q_sf = nullptr;
+  a.k_e8m0 = nullptr;
+  a.k_ws = 0;
+  const size_t smem = sizeof(ChunkSmem<false>) + 1024;
   cudaFuncSetAttribute(chunk_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        static_cast<int>(smem));
   dim3 grid((n_q + kBM - 1) / kBM, d.B * Hq);
@@ -1349,7 +1564,10 @@ int launch_region_drop(const kvq_cache &c, const void *q, int Hq, int n_q, const
   a.lists_per_head = 0;
   a.hist_tiles = 0x7fffffff;
   a.win_off = 0;
-  const size_t smem = sizeof(ChunkSmem) + 1024;
+  a.q_sf = nullptr;
+  a.k_e8m0 = nullptr;
+  a.k_ws = 0;
+  const size_t smem = sizeof(ChunkSmem<false>) + 1024;
   cudaFuncSetAttribute(chunk_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        static_cast<int>(smem));
   dim3 grid((n_q + kBM - 1) / kBM, d.B * Hq);

@@ -501,6 +501,13 @@ def test_chunk_int4_history_full_size_sampled_heads(kvq):
 @pytest.mark.parametrize("hq,hkv,n_q,n_kv,bounds", [
     (2, 2, 200, 300, [0, 100, 250, 300]),
     (4, 2, 130, 1000, [0, 390, 999, 1000]),
+    # fewer keys than one 112-key tile; one tile and one key; a ragged tail
+    (2, 1, 64, 100, [0, 50, 100]),
+    (1, 1, 128, 113, [0, 112, 113]),
+    (3, 3, 257, 1233, [0, 1, 112, 500, 1233]),
+    # 16 regions, bounds inside and on the edges of 112-key tiles
+    (2, 2, 190, 1800, [0, 1, 111, 112, 113, 224, 300, 336, 390, 700, 780, 1000, 1120, 1170,
+                       1500, 1799, 1800]),
 ])
 def test_chunk_mxfp8_matches_oracle(kvq, hq, hkv, n_q, n_kv, bounds):
     q, k, v = chunk_case(80 + n_kv, hq, hkv, n_q, n_kv, 2.0)
@@ -521,6 +528,31 @@ def test_chunk_mxfp8_matches_oracle(kvq, hq, hkv, n_q, n_kv, bounds):
     out_g, _, path_g = kvq.attend(cache_g, bf16_cuda(q[:, :, :63]), out_dtype="f32")
     assert path_g == "generic"
     assert O.rel_l2(to_np(out_g), to_np(out)[:, :, :63]) <= TOL_BF16
+
+
+def test_chunk_mxfp8_spiking_scores(kvq):
+    # a late block of keys far above the rest: the MXFP8 kernel redoes that
+    # tile with a new reference, as the bf16 one does
+    rng = np.random.default_rng(13)
+    n_q, n_kv = 130, 1100
+    u = rng.standard_normal(128)
+    u /= np.linalg.norm(u)
+    q = rng.standard_normal((1, 2, n_q, 128))
+    q += (3.0 - q @ u)[..., None] * u
+    k = rng.standard_normal((1, 1, n_kv, 128)) * (1.0 + 6.0 * np.arange(n_kv) / n_kv)[:, None]
+    k[0, 0, 900:910] = 300.0 * u + 0.1 * rng.standard_normal((10, 128))
+    v = rng.standard_normal((1, 1, n_kv, 128))
+    q, k, v = (O.round_to_bf16(x.astype(np.float32)) for x in (q, k, v))
+    bounds = [0, 500, 905, n_kv]
+    cache = kvq.pack(bf16_cuda(k), bf16_cuda(v), n_kv, "mxfp8", "bf16")
+    out, mass, path = kvq.attend(cache, bf16_cuda(q), out_dtype="f32", region_bounds=bounds)
+    assert path == "chunk_mxfp8"
+    qh = O.mxfp8_dequantize(*O.mxfp8_quantize(q.astype(np.float64)))
+    kh = O.mxfp8_dequantize(*O.mxfp8_quantize(k.astype(np.float64)))
+    for h in range(2):
+        ref, _, ref_mass = O.attention(qh[0, h], kh[0, 0], v[0, 0], region_bounds=bounds)
+        assert O.rel_l2(to_np(out)[0, h], ref) <= TOL_BF16
+        np.testing.assert_allclose(to_np(mass)[0, h], ref_mass, atol=TOL_MASS, rtol=0)
 
 
 def test_chunk_mxfp8_full_size_sampled_heads(kvq):
