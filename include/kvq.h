@@ -252,6 +252,13 @@ KVQ_API kvq_status kv_attend_stats(const kvq_cache *cache, const void *q, int32_
  * positions are flagged KVQ_DEV_DUP (the output of that row is then invalid).
  * An MXFP8 K window, n_cand > 65,536 and q_heads or batch above 65,535 are
  * not supported (KVQ_ERR_UNSUPPORTED). Other arguments as for kv_attend.
+ * Kernel choice: with D = 128, bf16 q, one query row, 8 query heads per KV
+ * head, a bf16 window (or none) and 8 x n_cand <= 4096, one pass per
+ * (sequence, KV head) covers the union of its 8 query heads' lists, reading
+ * each distinct row and K-scale group once and scoring it for all 8 heads on
+ * the tensor cores (bf16 operands, the int4 rows rounded once to bf16); it
+ * needs workspace for per-slice partials (query it with workspace == NULL).
+ * Other shapes run a per-row fp32 kernel and need none.
  */
 KVQ_API kvq_status kv_attend_candidates(const kvq_cache *cache, const void *q, int32_t q_dtype,
                                         int32_t q_heads, int32_t n_q, const int32_t *idx,

@@ -318,19 +318,29 @@ kvq_status kv_attend_candidates(const kvq_cache *cache, const void *q, int32_t q
   if (cache->recent > 0 && cache->kwin_dtype == KVQ_MXFP8) return KVQ_ERR_UNSUPPORTED;
   // the grid is (query rows, q_heads, batch)
   if (n_cand > 65536 || q_heads > 65535 || cache->batch > 65535) return KVQ_ERR_UNSUPPORTED;
+  const int sms = sm_count();
+  const bool uni = kvq::candidates_union_supported(*cache, q_dtype, q_heads, n_q, n_cand);
+  const size_t need = uni ? kvq::candidates_union_workspace_bytes(*cache, n_cand, sms) : 0;
   if (!workspace) {
-    *ws_bytes = 0;
+    *ws_bytes = need;
     return KVQ_OK;
   }
+  if (*ws_bytes < need) return KVQ_ERR_WORKSPACE;
   if (!q || !out || !idx) return KVQ_ERR_ARG;
-  if (!aligned16(q) || !aligned16(out) || !aligned16(idx) ||
+  if (!aligned16(q) || !aligned16(out) || !aligned16(idx) || !aligned16(workspace) ||
       (dev_status && !aligned16(dev_status)))
     return KVQ_ERR_ALIGN;
   const float scale = resolve_scale(sm_scale, cache->head_dim);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (uni) {
+    const int n = kvq::launch_candidates_union(*cache, q, idx, n_cand, validate,
+                                               static_cast<float>(scale * kLog2e), out, out_dtype,
+                                               workspace, make_ctl(dev_status), sms, s);
+    return finish(n, "candidates_union");
+  }
   const int n = kvq::launch_attend_candidates(*cache, q, q_dtype, q_heads, n_q, idx, n_cand,
                                               validate, static_cast<float>(scale * kLog2e), out,
-                                              out_dtype, make_ctl(dev_status),
-                                              reinterpret_cast<cudaStream_t>(stream));
+                                              out_dtype, make_ctl(dev_status), s);
   return finish(n, "candidates");
 }
 

@@ -189,6 +189,48 @@ __device__ __forceinline__ float warp_sum(float x) {
   return x;
 }
 
+// ------------------------------------------------------------------ warp MMA (mma.sync)
+// D += A B, m16n8k16, bf16 operands, fp32 accumulators. With g = lane / 4 and
+// t = lane % 4: a0 = A(g, 2t..2t+1), a1 = A(g+8, 2t..), a2 = A(g, 2t+8..),
+// a3 = A(g+8, 2t+8..); b0 = B(2t..2t+1, g), b1 = B(2t+8..2t+9, g);
+// c0, c1 = C(g, 2t..2t+1), c2, c3 = C(g+8, 2t..2t+1).
+__device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Transpose of an 8x8 matrix of 16-bit pairs held one row pair per lane.
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
+  __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&b);
+}
+
+// Four 8x8 16-bit matrices from shared memory: lane i gives the address of
+// row i % 8 of matrix i / 8; register j receives matrix j (transposed with
+// ldsm_x4_t).
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                        uint32_t &r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                          uint32_t &r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
 // Value of an E4M3 byte times 2^(e8m0 - 127), computed exactly in fp32
 // (E4M3 has 3 mantissa bits; the power of two is applied with ldexpf).
 __device__ __forceinline__ float mxfp8_value(uint8_t code, uint8_t e8m0) {

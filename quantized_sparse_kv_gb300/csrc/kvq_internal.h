@@ -85,6 +85,14 @@ int launch_attend_candidates(const kvq_cache &c, const void *q, int q_dtype, int
                              int top_k = 0, int32_t *selected = nullptr, int block_q = 1);
 int candidates_topk_max();
 
+// attend_candidates.cu: one pass per (sequence, KV head) over the union of its
+// 8 query heads' lists (D = 128, bf16 q, one query row, 8 x C <= 4096).
+bool candidates_union_supported(const kvq_cache &c, int q_dtype, int Hq, int n_q, int n_cand);
+size_t candidates_union_workspace_bytes(const kvq_cache &c, int n_cand, int num_sms);
+int launch_candidates_union(const kvq_cache &c, const void *q, const int32_t *idx, int n_cand,
+                            int validate, float scale_log2, void *out, int out_dtype, void *ws,
+                            const KernelCtl &ctl, int num_sms, cudaStream_t s);
+
 // attend_chunk.cu: kv_attend_candidates_block on the tensor cores (lists of
 // block_q query rows gathered once to bf16 in workspace).
 bool candidate_lists_supported(const kvq_cache &c, int q_dtype, int block_q);

@@ -78,4 +78,9 @@ def test_topk_of_all_keys_is_plain_candidate_attention(kvq):
     a, _, _ = kvq.attend_candidates_topk(cache, dev(q), torch.from_numpy(idx).cuda(), 96,
                                          out_dtype="f32")
     b, _ = kvq.attend_candidates(cache, dev(q), torch.from_numpy(idx).cuda(), out_dtype="f32")
-    assert O.rel_l2(to_np(a), to_np(b)) <= 1e-5
+    # the top-k path is fp32 throughout; plain candidate attention at this
+    # shape runs on bf16 tensor-core operands (the bf16 tolerance)
+    ref = O.attend_candidates(q, O.pack(k, v, 128, "bf16"), idx)
+    assert O.rel_l2(to_np(a), ref) <= 1e-5
+    assert O.rel_l2(to_np(b), ref) <= 1e-2
+    assert O.rel_l2(to_np(a), to_np(b)) <= 1e-2

@@ -229,6 +229,82 @@ def test_candidates_match_oracle(kvq, n, recent, c, sort):
     assert O.rel_l2(to_np(out), ref) <= TOL_BF16
 
 
+def _cand_run(kvq, cache, tq, idx, validate=False):
+    a = kvq.AttendCandidates(cache, tq, torch.from_numpy(idx).cuda(), out_dtype="f32",
+                             validate=validate)
+    a.run()
+    return a.out, a.status, a.lib.kvq_last_path().decode()
+
+
+@pytest.mark.parametrize("case", ["shared", "disjoint", "window_only", "sink_only", "c512",
+                                  "one_unit_many_slices"])
+def test_candidates_union_of_head_lists(kvq, case):
+    # the pass over the union of a KV head's 8 lists: heads listing the same
+    # keys, disjoint keys, only window keys, only the first 64 positions (every
+    # later slice empty), the largest list it takes (8 x 512 rows), and one
+    # (sequence, KV head) split into many slices
+    rng = np.random.default_rng(hash(case) % 1000)
+    batch, n, recent, c = 2, 3000, 128, 64
+    if case == "c512":
+        c = 512
+    if case == "one_unit_many_slices":
+        batch, n = 1, 20000
+    q, k, v = decode_case(50 + len(case), batch, n, hkv=2 if case != "one_unit_many_slices" else 1)
+    hq = q.shape[1]
+    idx = np.empty((batch, hq, 1, c), dtype=np.int32)
+    for b in range(batch):
+        for h in range(hq):
+            if case == "shared":
+                base = np.random.default_rng(b * 100 + h // 8).choice(n, c, replace=False)
+                idx[b, h, 0] = rng.permutation(base)
+            elif case == "disjoint":
+                idx[b, h, 0] = (h % 8) * c + rng.permutation(c)
+            elif case == "window_only":
+                idx[b, h, 0] = n - recent + rng.choice(recent, c, replace=False)
+            elif case == "sink_only":
+                idx[b, h, 0] = rng.permutation(64)[:c]
+            else:
+                idx[b, h, 0] = rng.choice(n, c, replace=False)
+    cache = kvq.pack(bf16_cuda(k), bf16_cuda(v), recent, "bf16")
+    out, status, path = _cand_run(kvq, cache, bf16_cuda(q), idx, validate=True)
+    assert path == "candidates_union"
+    assert kvq.read_status(status) == 0
+    ref = O.attend_candidates(q, O.pack(k, v, recent, "bf16"), idx)
+    assert O.rel_l2(to_np(out), ref) <= TOL_BF16
+
+
+def test_candidates_union_flags_and_skips_bad_indices(kvq):
+    # out-of-range positions are skipped and flagged; a duplicate within one
+    # head's list is flagged with validate; the other rows are still exact
+    q, k, v = decode_case(9, 2, 900)
+    cache = kvq.pack(bf16_cuda(k), bf16_cuda(v), 64, "bf16")
+    rng = np.random.default_rng(9)
+    idx = np.stack([np.stack([rng.choice(900, 48, replace=False) for _ in range(16)])
+                    for _ in range(2)])[:, :, None].astype(np.int32)
+    bad = idx.copy()
+    bad[1, 5, 0, 7] = -3
+    bad[0, 12, 0, 40] = 900
+    out, status, path = _cand_run(kvq, cache, bf16_cuda(q), bad)
+    assert path == "candidates_union"
+    assert kvq.read_status(status) == kvq.DEV_INDEX
+    packed = O.pack(k, v, 64, "bf16")
+    keep = [(b, h) for b in range(2) for h in range(16) if (b, h) not in ((1, 5), (0, 12))]
+    ref = O.attend_candidates(q, packed, idx)
+    got = to_np(out)
+    for b, h in keep:
+        assert O.rel_l2(got[b, h], ref[b, h]) <= TOL_BF16
+    # the flagged rows attend the remaining listed keys
+    for b, h, j in ((1, 5, 7), (0, 12, 40)):
+        rest = np.delete(idx[b, h, 0], j)
+        kh, vh = O.dequantize_head(packed[b][h // 8])
+        r = O.candidate_attention(q[b, h].astype(np.float64), kh, vh, rest[None])
+        assert O.rel_l2(got[b, h], r) <= TOL_BF16
+    dup = idx.copy()
+    dup[0, 3, 0, 9] = dup[0, 3, 0, 2]
+    _, status, _ = _cand_run(kvq, cache, bf16_cuda(q), dup, validate=True)
+    assert kvq.read_status(status) & kvq.DEV_DUP
+
+
 def test_candidates_over_all_keys_equal_dense(kvq):
     q, k, v = decode_case(7, 1, 700)
     cache = kvq.pack(bf16_cuda(k), bf16_cuda(v), 64, "bf16")
