@@ -578,6 +578,37 @@ def _oracle_unit_worker(args):
     return time.perf_counter() - t0
 
 
+def _oracle_pack_worker(args):
+    """Time the oracle's kv_pack of one (sequence, KV head) of the decode
+    workload (int4 groups of K per channel and of V per token, bf16 window)."""
+    seed, context, recent = args
+    from oracle import kvq_oracle as O
+    from quantized_sparse_kv_gb300 import synth
+    k = O.round_to_bf16(synth.normal_numpy(seed + 1, (context, 128)))
+    v = O.round_to_bf16(synth.normal_numpy(seed + 2, (context, 128)))
+    t0 = time.perf_counter()
+    O.pack_head(k, v, recent, "bf16")
+    return time.perf_counter() - t0
+
+
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), for the record."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part", "hardware")):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
 def oracle_pool(workers):
     import multiprocessing as mp
     for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
@@ -595,6 +626,46 @@ def oracle_sample(pool, units, workers, seed0=1000):
     cpu_s = sum(busy)
     # each worker is one core; input generation and packing are not timed
     return {"keys": keys, "wall_s": wall, "cpu_s": cpu_s, "keys_per_s": keys * workers / cpu_s}
+
+
+def oracle_pack_sample(pool, units, workers, seed0=5000):
+    d = DECODE
+    busy = pool.map(_oracle_pack_worker,
+                    [(seed0 + 3 * i, d["context"], d["recent"]) for i in range(units)])
+    tokens = units * d["context"]
+    return {"tokens": tokens, "cpu_s": sum(busy), "tokens_per_s": tokens * workers / sum(busy)}
+
+
+def cpu_baseline_record(workers):
+    """The fp64 oracle timed on the host cores (spawned before any GPU work):
+    attention of the decode workload's (sequence, KV head) units on all
+    workers and on one, and kv_pack of such units, each a bounded sample."""
+    d = DECODE
+    pool = oracle_pool(workers)
+    allc = oracle_sample(pool, 8 * workers, workers)
+    pack = oracle_pack_sample(pool, 2 * workers, workers)
+    pool.close()
+    one = oracle_pool(1)
+    single = oracle_sample(one, 4, 1, seed0=3000)
+    pack1 = oracle_pack_sample(one, 2, 1, seed0=6000)
+    one.close()
+    try:
+        nproc = len(os.sched_getaffinity(0))
+    except AttributeError:
+        nproc = os.cpu_count() or 1
+    return {"value": allc["keys_per_s"], "unit": "keys/s", "cores": workers, "kind": "oracle",
+            "sample": f"{8 * workers} (sequence, KV head) units of the decode workload "
+                      f"(8 query heads x L={d['context']} each), oracle dequantize + fp64 "
+                      f"attention, {allc['cpu_s']:.1f} s of CPU work",
+            "cpu_model": cpu_model(), "nproc": nproc,
+            "single_thread": {"value": single["keys_per_s"], "unit": "keys/s", "cores": 1,
+                              "sample": f"4 units, {single['cpu_s']:.1f} s"},
+            "pack": {"value": pack["tokens_per_s"], "unit": "tokens/s (x 1 KV head)",
+                     "cores": workers,
+                     "sample": f"{2 * workers} units of {d['context']} tokens packed "
+                               f"(int4 K per channel, V per token, bf16 window R={d['recent']}), "
+                               f"{pack['cpu_s']:.1f} s",
+                     "single_thread": pack1["tokens_per_s"]}}
 
 
 def cpu_workers():
@@ -659,7 +730,7 @@ def run_reference(args):
             "impl": "reference",
             "config": {"workload": "decode B=64 Hq=16 Hkv=2 D=128 L=32768 R=128 (sampled units)"},
             "cpu_baseline": {"value": value, "unit": "keys/s", "cores": workers, "kind": "oracle",
-                             "sample": sample},
+                             "sample": sample, "cpu_model": cpu_model()},
             "e2e": {"value": value, "unit": "keys/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
@@ -681,14 +752,7 @@ def run_kvq(args):
     # CPU oracle baseline first (spawned before heavy GPU work), rank 0 only
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
-        workers = cpu_workers()
-        pool = oracle_pool(workers)
-        s = oracle_sample(pool, 8 * workers, workers)
-        pool.close()
-        cpu = {"value": s["keys_per_s"], "unit": "keys/s", "cores": workers, "kind": "oracle",
-               "sample": f"{8 * workers} (sequence, KV head) units of the decode workload "
-                         f"(8 query heads x L={d['context']} each), oracle dequantize + fp64 "
-                         f"attention, {s['cpu_s']:.1f} s of CPU work"}
+        cpu = cpu_baseline_record(cpu_workers())
 
     q, k, v = synth.decode_inputs_torch(1 + rank, d["batch"], d["context"], "cuda")
     cache = kvq.pack(k, v, d["recent"], "bf16")
