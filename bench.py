@@ -431,7 +431,7 @@ def row_candidates(kvq, synth, torch, steps, warmup, pk, context, c):
             "ms": ms, "keys_per_s": keys / (ms * 1e-3), "l2": l2_note(n, nbytes),
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
                          "frac": gbs / pk["hbm_gbs"],
-                         "traffic": (profile_traffic("candidates_kernel_B32_L131072_C256.md")
+                         "traffic": (profile_traffic("candidates_union_kernels_B32_L131072_C256.md")
                                      if (context, c) == (131072, 256) else None),
                          "bytes_note": "distinct rows and K-scale groups per (sequence, KV head)"},
             "launches": a.launches()}
