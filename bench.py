@@ -862,7 +862,8 @@ def run_kvq(args):
            "unit": "keys/s", "h2d_bytes_per_step": q_hosts[0].numel() * q_hosts[0].element_size(),
            "d2h_bytes_per_step": o_hosts[0].numel() * o_hosts[0].element_size(),
            "note": "KV cache resident in HBM; per step the query rows go in from pinned host "
-                   "memory and the outputs come back out, on a copy stream, double-buffered, so "
+                   "memory and the outputs come back out, on one copy stream per direction, "
+                   "double-buffered, so "
                    "that step i's copies overlap the neighbouring steps' attention"}
 
     rows = {}
