@@ -61,7 +61,8 @@ enum {
   KVQ_DEV_INDEX = 1,   /* a candidate index outside [0, n_tokens) (that key is skipped) */
   KVQ_DEV_DUP = 2,     /* a candidate list holds the same index twice (validate only) */
   KVQ_DEV_TIMEOUT = 4, /* a bounded wait ran out; the outputs of that launch are invalid */
-  KVQ_DEV_BOUNDS = 8   /* an internal index check failed; outputs invalid */
+  KVQ_DEV_BOUNDS = 8   /* an address range a kernel derived lay outside the call's buffers
+                          (checked in the KVQ_DEBUG build, kvq_debug_checks); outputs invalid */
 };
 
 typedef enum { KVQ_F32 = 0, KVQ_BF16 = 1, KVQ_MXFP8 = 2 } kvq_dtype;
@@ -382,6 +383,21 @@ KVQ_API const char *kvq_last_path(void);
  * work item so that the wait on it can only run out. Used by the failure tests.
  */
 KVQ_API void kvq_debug_set(uint32_t wait_limit_ns, int32_t drop_item);
+
+/*
+ * 1 when this library was built with KVQ_DEBUG (libkvq_debug.so), else 0. In
+ * that build every kernel checks each global address range it derives from
+ * its indices (a row, a chunk, a bulk copy) against the device buffers the
+ * call passed -- the cache's arrays at the sizes its shape gives, q, the
+ * outputs, index lists and the workspace at the size given in *ws_bytes --
+ * and, for a range outside them, sets KVQ_DEV_BOUNDS in *dev_status and
+ * leaves the access out (a load reads zeros, a store is dropped, a bulk copy
+ * is neither issued nor waited for), so a wrong index is reported instead of
+ * faulting. TMA tile copies are bounded by their tensor maps. The checks cost
+ * time; the outputs of a call that reports no error are those of the other
+ * build.
+ */
+KVQ_API int32_t kvq_debug_checks(void);
 
 #ifdef __cplusplus
 }

@@ -45,6 +45,32 @@ struct CandArgs {
   KernelCtl ctl;
 };
 
+// Whether the rows a listed key t of unit u reads (int4: its K code row, K
+// scale group, V code row and V scales; window: its K and V rows) lie inside
+// the call's buffers (see in_bounds; always true outside debug builds).
+__device__ __forceinline__ bool cand_row_ok(const CandArgs &a, long u, int t, int D) {
+  if (t < a.cut) {
+    const long g = u * a.Gs + t / kGroup, vr = u * a.Vs + t;
+    return in_bounds(a.ctl, a.k_codes + (g * kGroup + t % kGroup) * (D / 2), D / 2) &&
+           in_bounds(a.ctl, a.k_scales + g * D, sizeof(float) * D) &&
+           in_bounds(a.ctl, a.v_codes + vr * (D / 2), D / 2) &&
+           in_bounds(a.ctl, a.v_scales + vr * (D / 32), sizeof(float) * (D / 32));
+  }
+  const long wr = (u * a.Ws + (t - a.cut)) * D;
+  const size_t kb = a.kwin == KVQ_F32 ? 4 : 2, vb = a.vwin == KVQ_F32 ? 4 : 2;
+  return in_bounds(a.ctl, static_cast<const uint8_t *>(a.k_window) + wr * kb, kb * D) &&
+         in_bounds(a.ctl, static_cast<const uint8_t *>(a.v_window) + wr * vb, vb * D);
+}
+
+// The row's list, q row and output row inside the call's buffers.
+__device__ __forceinline__ bool cand_io_ok(const CandArgs &a, const int32_t *cand, long row,
+                                           int D) {
+  const size_t qb = a.q_dtype == KVQ_F32 ? 4 : 2, ob = a.out_dtype == KVQ_F32 ? 4 : 2;
+  return in_bounds(a.ctl, cand, sizeof(int32_t) * a.C) &&
+         in_bounds(a.ctl, static_cast<const uint8_t *>(a.q) + row * D * qb, qb * D) &&
+         in_bounds(a.ctl, static_cast<const uint8_t *>(a.out) + row * D * ob, ob * D);
+}
+
 __device__ __forceinline__ float wval(const void *w, int dtype, long i) {
   return dtype == KVQ_F32 ? static_cast<const float *>(w)[i]
                           : bf16_to_f32(static_cast<const uint16_t *>(w)[i]);
@@ -66,6 +92,7 @@ __global__ void __launch_bounds__(kWarps * 32) cand_kernel(const CandArgs a) {
   const int32_t *cand =
       a.idx + ((static_cast<long>(b) * a.Hq + h) * a.lists_per_head + i / a.block_q) * a.C;
   const int d0 = lane * F;
+  if (!cand_io_ok(a, cand, row, D)) return;  // the same in every thread
 
   float q[F];
 #pragma unroll
@@ -99,6 +126,7 @@ __global__ void __launch_bounds__(kWarps * 32) cand_kernel(const CandArgs a) {
       if (lane == 0) flag_error(a.ctl, KVQ_DEV_INDEX);
       continue;
     }
+    if (!cand_row_ok(a, u, t, D)) continue;
     float kv[F], vv[F];
     if (t < a.cut) {
       const int g = t / kGroup, r = t % kGroup;
@@ -180,6 +208,7 @@ __global__ void __launch_bounds__(kWarps * 32) cand128_kernel(const CandArgs a) 
   const long row = (static_cast<long>(b) * a.Hq + h) * a.n_q + i;
   const int32_t *cand =
       a.idx + ((static_cast<long>(b) * a.Hq + h) * a.lists_per_head + i / a.block_q) * a.C;
+  if (!cand_io_ok(a, cand, row, D)) return;  // the same in every thread
   for (int j = threadIdx.x; j < a.C; j += blockDim.x) list[j] = cand[j];
 
   float q[4];
@@ -224,6 +253,7 @@ __global__ void __launch_bounds__(kWarps * 32) cand128_kernel(const CandArgs a) 
       tk[x] = c < a.C ? list[c] : -1;
       ok[x] = c < a.C && tk[x] >= 0 && tk[x] < a.N;
       if (c < a.C && !ok[x] && lane == 0) flag_error(a.ctl, KVQ_DEV_INDEX);
+      ok[x] = ok[x] && cand_row_ok(a, u, tk[x], D);
       any_win |= ok[x] && tk[x] >= a.cut;
     }
     // int4 rows for every slot, branch-free: out-of-range or window slots read
@@ -237,6 +267,12 @@ __global__ void __launch_bounds__(kWarps * 32) cand128_kernel(const CandArgs a) 
       for (int x = 0; x < kUnroll; ++x) {
         const int t = min(max(tk[x], 0), tq_max);
         const int g = t / kGroup, r = t % kGroup;
+        if (!cand_row_ok(a, u, t, D)) {  // debug builds only: the slot reads nothing
+          kb[x] = vb[x] = 0u;
+          ks[x] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+          vs[x] = 0.0f;
+          continue;
+        }
         kb[x] = reinterpret_cast<const uint16_t *>(kc_u + (static_cast<long>(g) * kGroup + r) * (D / 2))[lane];
         ks[x] = reinterpret_cast<const float4 *>(ks_u + static_cast<long>(g) * D)[lane];
         vb[x] = reinterpret_cast<const uint16_t *>(vc_u + static_cast<long>(t) * (D / 2))[lane];
@@ -364,6 +400,10 @@ __global__ void __launch_bounds__(kWarps * 32) cand_topk_kernel(const CandArgs a
   const int32_t *cand =
       a.idx + ((static_cast<long>(b) * a.Hq + h) * a.lists_per_head + i / a.block_q) * a.C;
   const int d0 = lane * F;
+  // the row's list, q, output and selected rows (the same in every thread)
+  if (!cand_io_ok(a, cand, row, D) ||
+      (a.selected && !in_bounds(a.ctl, a.selected + row * a.top_k, sizeof(int32_t) * a.top_k)))
+    return;
 
   float q[F];
 #pragma unroll
@@ -381,7 +421,7 @@ __global__ void __launch_bounds__(kWarps * 32) cand_topk_kernel(const CandArgs a
   for (int c = warp; c < a.C; c += kWarps) {
     const int t = cand[c];
     float s = -CUDART_INF_F;
-    if (t >= 0 && t < a.N) {
+    if (t >= 0 && t < a.N && cand_row_ok(a, u, t, D)) {
       float part = 0.0f;
       if (t < a.cut) {
         const int g = t / kGroup, r = t % kGroup;
@@ -402,7 +442,7 @@ __global__ void __launch_bounds__(kWarps * 32) cand_topk_kernel(const CandArgs a
         for (int k = 0; k < F; ++k) part = fmaf(q[k], wval(a.k_window, a.kwin, wr * D + d0 + k), part);
       }
       s = warp_sum(part);
-    } else if (lane == 0) {
+    } else if (lane == 0 && (t < 0 || t >= a.N)) {
       flag_error(a.ctl, KVQ_DEV_INDEX);
     }
     if (lane == 0) {
@@ -564,6 +604,13 @@ __global__ void __launch_bounds__(kUBuild) cand_union_build_kernel(const UnionAr
   const int b = u / a.Hkv, kvh = u % a.Hkv;
   const int32_t *lists = a.idx + (static_cast<long>(b) * a.Hkv * 8 + kvh * 8) * a.C;
   const int entries = 8 * a.C;
+  const long lbase = (static_cast<long>(u) * a.slices + slice) * entries;
+  // the 8 lists and this slice's outputs (the same in every thread)
+  const bool io_ok = in_bounds(a.ctl, lists, sizeof(int32_t) * entries) &&
+                     in_bounds(a.ctl, a.list_pos + lbase, sizeof(int32_t) * entries) &&
+                     in_bounds(a.ctl, a.list_heads + lbase, entries) &&
+                     in_bounds(a.ctl, a.count + static_cast<long>(u) * a.slices + slice, 4);
+  if (!io_ok) return;
   auto mark = [&](int e, int t) {
     if (t < 0 || t >= a.N) {
       if (slice == 0) flag_error(a.ctl, KVQ_DEV_INDEX);
@@ -640,7 +687,6 @@ __global__ void __launch_bounds__(kUBuild) cand_union_build_kernel(const UnionAr
     pos += w < warp ? sm.wsum[w] : 0;
     total += sm.wsum[w];
   }
-  const long lbase = (static_cast<long>(u) * a.slices + slice) * entries;
   for (int c = c0; c < c1; ++c) {
     const int ch = sm.chunks[c];
     const uint4 m4 = reinterpret_cast<const uint4 *>(sm.mask)[ch];
@@ -758,15 +804,21 @@ __device__ __forceinline__ void union_fetch(const UnionArgs &a, long u, int t, i
                                             RawSlot &r) {
   if (t < a.cut) {
     const long grp = u * a.Gs + (t >> 5);
+    const long vr = u * a.Vs + t;
+    if (!in_bounds(a.ctl, a.k_codes + (grp * 32 + (t & 31)) * 64 + 16 * cc, 16) ||
+        !in_bounds(a.ctl, a.k_scales + grp * 128 + 32 * cc, 128) ||
+        !in_bounds(a.ctl, a.v_codes + vr * 64 + 16 * cc, 16) ||
+        !in_bounds(a.ctl, a.v_scales + vr * 4 + cc, 4))
+      return;
     cp_async16(smem_u32(r.kc), a.k_codes + (grp * 32 + (t & 31)) * 64 + 16 * cc);
     const float *ks = a.k_scales + grp * 128 + 32 * cc;
 #pragma unroll
     for (int j = 0; j < 8; ++j) cp_async16(smem_u32(r.ks + 4 * j), ks + 4 * j);
-    const long vr = u * a.Vs + t;
     cp_async16(smem_u32(r.vc), a.v_codes + vr * 64 + 16 * cc);
     cp_async4(smem_u32(&r.vs), a.v_scales + vr * 4 + cc);
   } else {
     const long wr = (u * a.Ws + (t - a.cut)) * 128 + 32 * cc;
+    if (!in_bounds(a.ctl, a.k_window + wr, 64) || !in_bounds(a.ctl, a.v_window + wr, 64)) return;
     uint8_t *dst = reinterpret_cast<uint8_t *>(&r);  // K: bytes 0..63, V: bytes 64..127
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -836,6 +888,13 @@ __global__ void __launch_bounds__(kUThreads, 2) cand_union_kernel(const UnionArg
   // features 16k + 2t.. and 16k + 2t + 8..)
   const int g = lane >> 2, t4 = lane & 3;
   uint32_t qb[8][2];
+  // the unit's q rows, counts and lists (the same in every thread)
+  const long lists_at = static_cast<long>(u) * a.slices * 8 * a.C;
+  const bool io_ok = in_bounds(a.ctl, a.q + static_cast<long>(u) * 8 * 128, 8 * 128 * 2) &&
+                     in_bounds(a.ctl, a.count + static_cast<long>(u) * a.slices, 4 * a.slices) &&
+                     in_bounds(a.ctl, a.list_pos + lists_at, 4L * a.slices * 8 * a.C) &&
+                     in_bounds(a.ctl, a.list_heads + lists_at, 1L * a.slices * 8 * a.C);
+  if (!io_ok) return;
   if (warp < kUMma) {
     const uint32_t *qw =
         reinterpret_cast<const uint32_t *>(a.q + (static_cast<long>(u) * 8 + g) * 128);
@@ -984,11 +1043,16 @@ __global__ void __launch_bounds__(kUThreads, 2) cand_union_kernel(const UnionArg
       ls += c * sm.red_l[w][h];
     }
     float *part = a.partials + ((static_cast<long>(u) * a.pieces + piece) * 8 + h) * kUPart;
-    part[128] = mx;
-    part[129] = ls;
+    if (in_bounds(a.ctl, part, sizeof(float) * kUPart)) {
+      part[128] = mx;
+      part[129] = ls;
+    }
   }
   __syncthreads();
-  for (int i = tid; i < 8 * 128; i += kUThreads) {
+  const bool part_ok = in_bounds(
+      a.ctl, a.partials + (static_cast<long>(u) * a.pieces + piece) * 8 * kUPart,
+      sizeof(float) * 8 * kUPart);
+  for (int i = tid; part_ok && i < 8 * 128; i += kUThreads) {
     const int h = i >> 7, d = i & 127;
     float acc = 0.0f;
 #pragma unroll
@@ -1005,6 +1069,13 @@ __global__ void __launch_bounds__(256) cand_union_combine_kernel(const UnionArgs
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int u = blockIdx.x, h = warp;
   const float *base = a.partials + (static_cast<long>(u) * a.pieces * 8 + h) * kUPart;
+  const long o = (static_cast<long>(u) * 8 + h) * 128 + 4 * lane;
+  const size_t ob = a.out_dtype == KVQ_F32 ? 4 : 2;
+  // the unit's partials and this head's output row (the same in every lane)
+  if (!in_bounds(a.ctl, a.partials + static_cast<long>(u) * a.pieces * 8 * kUPart,
+                 sizeof(float) * a.pieces * 8 * kUPart) ||
+      !in_bounds(a.ctl, static_cast<uint8_t *>(a.out) + (o - 4 * lane) * ob, 128 * ob))
+    return;
   float m = -CUDART_INF_F, l = 0.0f;
   float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
   constexpr int kBatch = 8;  // pieces whose loads are in flight together
@@ -1041,7 +1112,6 @@ __global__ void __launch_bounds__(256) cand_union_combine_kernel(const UnionArgs
     m = nm;
   }
   const float inv = 1.0f / l;
-  const long o = (static_cast<long>(u) * 8 + h) * 128 + 4 * lane;
   if (a.out_dtype == KVQ_F32) {
     reinterpret_cast<float4 *>(static_cast<float *>(a.out) + o)[0] =
         make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);

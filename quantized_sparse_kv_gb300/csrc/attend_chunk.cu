@@ -627,13 +627,18 @@ __device__ __forceinline__ void chunk_body(const CUtensorMap &tm_q, const CUtens
       const uint32_t *e8 = reinterpret_cast<const uint32_t *>(a.k_e8m0) +
                            static_cast<long>(hkv) * a.k_ws + kj * BN;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) sfw[i] = lane + 32 * i < valid ? e8[lane + 32 * i] : 0x7f7f7f7fu;
+      for (int i = 0; i < 4; ++i)
+        sfw[i] = lane + 32 * i < valid && in_bounds(a.ctl, e8 + lane + 32 * i, 4)
+                     ? e8[lane + 32 * i]
+                     : 0x7f7f7f7fu;
     };
     if (kMx) {
       // the Q tile's scale block, laid out by the prologue as the MMA reads it
       const uint4 *src = reinterpret_cast<const uint4 *>(
           a.q_sf + (static_cast<long>(hq) * gridDim.x + blockIdx.x) * 512);
-      reinterpret_cast<uint4 *>(sm.sfa)[lane] = src[lane];
+      reinterpret_cast<uint4 *>(sm.sfa)[lane] =
+          in_bounds(a.ctl, src + lane, 16) ? src[lane] : make_uint4(0x7f7f7f7fu, 0x7f7f7f7fu,
+                                                                    0x7f7f7f7fu, 0x7f7f7f7fu);
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       mbar_arrive(qb);
       if (nt > 0) load_sf(0);
@@ -931,7 +936,9 @@ __device__ __forceinline__ void chunk_body(const CUtensorMap &tm_q, const CUtens
         if (have_b) reg_fence(vb);
 #pragma unroll
         for (int e = 0; e < 32; ++e) va[e] = (fa * va[e] + (have_b ? fb * vb[e] : 0.0f)) * inv;
-        if (qrow < a.n_q) {
+        const size_t ob = a.out_dtype == KVQ_F32 ? 4 : 2;
+        if (qrow < a.n_q &&
+            in_bounds(a.ctl, static_cast<uint8_t *>(a.out) + (obase + 32 * c) * ob, 32 * ob)) {
           if (a.out_dtype == KVQ_F32) {
             float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(a.out) + obase + 32 * c);
 #pragma unroll
@@ -949,7 +956,9 @@ __device__ __forceinline__ void chunk_body(const CUtensorMap &tm_q, const CUtens
           }
         }
       }
-      if (g == 0 && a.mass && qrow < a.n_q)
+      if (g == 0 && a.mass && qrow < a.n_q &&
+          in_bounds(a.ctl, a.mass + (static_cast<long>(hq) * a.n_q + qrow) * a.reg.n,
+                    sizeof(float) * nreg))
         for (int k = 0; k < nreg; ++k)
           a.mass[(static_cast<long>(hq) * a.n_q + qrow) * a.reg.n + k] =
               (fa * ms[0].r[k][row] + (have_b ? fb * ms[1].r[k][row] : 0.0f)) * inv;
@@ -993,7 +1002,8 @@ __global__ void __launch_bounds__(384, 1)
 __global__ void __launch_bounds__(256) q_mxfp8_kernel(const __nv_bfloat16 *__restrict__ q,
                                                      int n_q, int q_tiles, long n_blocks,
                                                      uint8_t *__restrict__ codes,
-                                                     uint8_t *__restrict__ sf) {
+                                                     uint8_t *__restrict__ sf,
+                                                     const KernelCtl ctl) {
   wait_prior_grid();
   allow_next_grid();
   const long tid = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -1005,7 +1015,8 @@ __global__ void __launch_bounds__(256) q_mxfp8_kernel(const __nv_bfloat16 *__res
   const long hq = prow / (static_cast<long>(q_tiles) * kBM);
   const bool real = live && r < n_q;
   const long src = (hq * n_q + r) * kDim + 32 * kb + 8 * (tid & 3);
-  const uint4 u = real ? *reinterpret_cast<const uint4 *>(q + src) : make_uint4(0, 0, 0, 0);
+  const uint4 u = real && in_bounds(ctl, q + src, 16) ? *reinterpret_cast<const uint4 *>(q + src)
+                                                     : make_uint4(0, 0, 0, 0);
   const uint32_t w[4] = {u.x, u.y, u.z, u.w};
   float x[8];
 #pragma unroll
@@ -1022,8 +1033,8 @@ __global__ void __launch_bounds__(256) q_mxfp8_kernel(const __nv_bfloat16 *__res
   const int ex = mxfp8_block_exp(amax);
   if ((tid & 3) == 0) {
     const int t = r / kBM;
-    sf[(hq * q_tiles + t) * 512 + sf_offset(r % kBM, kb)] =
-        static_cast<uint8_t>(real ? ex + 127 : 127);
+    uint8_t *dst = sf + (hq * q_tiles + t) * 512 + sf_offset(r % kBM, kb);
+    if (in_bounds(ctl, dst, 1)) *dst = static_cast<uint8_t>(real ? ex + 127 : 127);
   }
   if (!real) return;
   const float down = pow2_of(-ex);
@@ -1035,7 +1046,7 @@ __global__ void __launch_bounds__(256) q_mxfp8_kernel(const __nv_bfloat16 *__res
         __NV_E4M3);
     o[j >> 1] |= static_cast<uint32_t>(c) << (16 * (j & 1));
   }
-  *reinterpret_cast<uint2 *>(codes + src) = make_uint2(o[0], o[1]);
+  if (in_bounds(ctl, codes + src, 8)) *reinterpret_cast<uint2 *>(codes + src) = make_uint2(o[0], o[1]);
 }
 
 // ------------------------------------------------------------------ int4 history
@@ -1057,6 +1068,7 @@ struct HistArgs {
   uint16_t *k_out, *v_out;  // [unit][N][128] bf16
   int N, R, cut, Gk;        // N: rows expanded
   int Gs, Vs, Ws;  // per-unit strides: K groups, V rows, window rows
+  KernelCtl ctl;
 };
 
 __device__ __forceinline__ float nib(uint32_t w, int e) {
@@ -1071,9 +1083,15 @@ __global__ void __launch_bounds__(256) history_to_bf16_kernel(const HistArgs a) 
   if (i >= a.N * 16) return;
   const long u = blockIdx.y;
   const int t = i >> 4, q = i & 15;  // token, feature slice 8q..8q+7
-  uint4 ko, vo;
+  uint4 ko = make_uint4(0u, 0u, 0u, 0u), vo = ko;
   if (t < a.cut) {
     const long grp = u * a.Gs + (t >> 5);
+    const long row = u * a.Vs + t;
+    if (!in_bounds(a.ctl, a.k_codes + (grp * 32 + (t & 31)) * 64 + 4 * q, 4) ||
+        !in_bounds(a.ctl, a.k_scales + grp * 128 + 8 * q, 32) ||
+        !in_bounds(a.ctl, a.v_codes + row * 64 + 4 * q, 4) ||
+        !in_bounds(a.ctl, a.v_scales + row * 4 + (q >> 2), 4))
+      return;
     // byte j of the slice holds features 8q + 2j (low nibble) and 8q + 2j + 1
     const uint32_t kc =
         *reinterpret_cast<const uint32_t *>(a.k_codes + (grp * 32 + (t & 31)) * 64 + 4 * q);
@@ -1083,7 +1101,6 @@ __global__ void __launch_bounds__(256) history_to_bf16_kernel(const HistArgs a) 
                     pack_bf16x2(nib(kc, 2) * s0.z, nib(kc, 3) * s0.w),
                     pack_bf16x2(nib(kc, 4) * s1.x, nib(kc, 5) * s1.y),
                     pack_bf16x2(nib(kc, 6) * s1.z, nib(kc, 7) * s1.w));
-    const long row = u * a.Vs + t;
     const uint32_t vc = *reinterpret_cast<const uint32_t *>(a.v_codes + row * 64 + 4 * q);
     const float vs = a.v_scales[row * 4 + (q >> 2)];
     vo = make_uint4(pack_bf16x2(nib(vc, 0) * vs, nib(vc, 1) * vs),
@@ -1092,12 +1109,12 @@ __global__ void __launch_bounds__(256) history_to_bf16_kernel(const HistArgs a) 
                     pack_bf16x2(nib(vc, 6) * vs, nib(vc, 7) * vs));
   } else {
     const long w = (u * a.Ws + (t - a.cut)) * 128 + 8 * q;
-    ko = *reinterpret_cast<const uint4 *>(a.k_window + w);
-    vo = *reinterpret_cast<const uint4 *>(a.v_window + w);
+    if (in_bounds(a.ctl, a.k_window + w, 16)) ko = *reinterpret_cast<const uint4 *>(a.k_window + w);
+    if (in_bounds(a.ctl, a.v_window + w, 16)) vo = *reinterpret_cast<const uint4 *>(a.v_window + w);
   }
   const long o = (u * a.N + t) * 128 + 8 * q;
-  *reinterpret_cast<uint4 *>(a.k_out + o) = ko;
-  *reinterpret_cast<uint4 *>(a.v_out + o) = vo;
+  if (in_bounds(a.ctl, a.k_out + o, 16)) *reinterpret_cast<uint4 *>(a.k_out + o) = ko;
+  if (in_bounds(a.ctl, a.v_out + o, 16)) *reinterpret_cast<uint4 *>(a.v_out + o) = vo;
 }
 
 // ------------------------------------------------------------------ block-shared candidate lists
@@ -1148,14 +1165,26 @@ __global__ void __launch_bounds__(256) gather_lists_bf16_kernel(const ListArgs a
   const int c = i >> 4, q8 = i & 15;
   const long bh = l / a.lists_per_head;  // b * Hq + h
   const long u = a.idx ? (bh / a.Hq) * a.Hkv + (bh % a.Hq) / a.group : l;
-  const int t = a.idx ? a.idx[l * a.C + c] : kept_position(a, c);
+  const int t = a.idx ? (in_bounds(a.ctl, a.idx + l * a.C + c, 4) ? a.idx[l * a.C + c] : -1)
+                     : kept_position(a, c);
   float kx[8], vx[8];
-  if (t < 0 || t >= a.N) {
-    if (q8 == 0) flag_error(a.ctl, KVQ_DEV_INDEX);
+  const long grp = u * a.Gs + (t >> 5);
+  const long wrow = (u * a.Ws + (t - a.cut)) * 128 + 8 * q8;
+  const size_t kwb = a.kwin == KVQ_F32 ? 4 : 2, vwb = a.vwin == KVQ_F32 ? 4 : 2;
+  const bool in_ok =
+      t >= 0 && t < a.N &&
+      (t < a.cut
+           ? in_bounds(a.ctl, a.k_codes + (grp * 32 + (t & 31)) * 64 + 4 * q8, 4) &&
+                 in_bounds(a.ctl, a.v_codes + (u * a.Vs + t) * 64 + 4 * q8, 4) &&
+                 in_bounds(a.ctl, a.v_scales + (u * a.Vs + t) * 4 + (q8 >> 2), 4) &&
+                 in_bounds(a.ctl, a.k_scales + grp * 128 + 8 * q8, 32)
+           : in_bounds(a.ctl, static_cast<const uint8_t *>(a.k_window) + wrow * kwb, 8 * kwb) &&
+                 in_bounds(a.ctl, static_cast<const uint8_t *>(a.v_window) + wrow * vwb, 8 * vwb));
+  if (t < 0 || t >= a.N || !in_ok) {
+    if (q8 == 0 && (t < 0 || t >= a.N)) flag_error(a.ctl, KVQ_DEV_INDEX);
 #pragma unroll
     for (int e = 0; e < 8; ++e) kx[e] = vx[e] = 0.0f;
   } else if (t < a.cut) {
-    const long grp = u * a.Gs + (t >> 5);
     const uint32_t kc =
         *reinterpret_cast<const uint32_t *>(a.k_codes + (grp * 32 + (t & 31)) * 64 + 4 * q8);
     const uint32_t vc = *reinterpret_cast<const uint32_t *>(a.v_codes + (u * a.Vs + t) * 64 + 4 * q8);
@@ -1166,14 +1195,14 @@ __global__ void __launch_bounds__(256) gather_lists_bf16_kernel(const ListArgs a
       vx[e] = nib(vc, e) * vs;
     }
   } else {
-    const long w = (u * a.Ws + (t - a.cut)) * 128 + 8 * q8;
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      kx[e] = win_value(a.k_window, a.kwin, w + e);
-      vx[e] = win_value(a.v_window, a.vwin, w + e);
+      kx[e] = win_value(a.k_window, a.kwin, wrow + e);
+      vx[e] = win_value(a.v_window, a.vwin, wrow + e);
     }
   }
   const long o = (l * a.C + c) * 128 + 8 * q8;
+  if (!in_bounds(a.ctl, a.k_out + o, 16) || !in_bounds(a.ctl, a.v_out + o, 16)) return;
   *reinterpret_cast<uint4 *>(a.k_out + o) =
       make_uint4(pack_bf16x2(kx[0], kx[1]), pack_bf16x2(kx[2], kx[3]), pack_bf16x2(kx[4], kx[5]),
                  pack_bf16x2(kx[6], kx[7]));
@@ -1290,7 +1319,7 @@ static int launch_chunk_mxfp8(const kvq_cache &c, const void *q, int Hq, int n_q
   const long n_blocks = hq_rows * q_tiles * kBM * 4;  // 32-feature blocks, padded rows
   launch_dependent(q_mxfp8_kernel, dim3(static_cast<unsigned>((n_blocks * 4 + 255) / 256)),
                    dim3(256), 0, s, static_cast<const __nv_bfloat16 *>(q), n_q, q_tiles,
-                   n_blocks, codes, sf);
+                   n_blocks, codes, sf, ctl);
   const int Ws = dims_of(c).Ws;
   CUtensorMap tq, tk, tv;
   if (!make_map_e4m3(&tq, codes, n_q, static_cast<int>(hq_rows), n_q, kBM) ||
@@ -1352,6 +1381,7 @@ int launch_attend_chunk(const kvq_cache &c, const void *q, int Hq, int n_q, floa
     h.Gs = d.Gs;
     h.Vs = d.Vs;
     h.Ws = d.Ws;
+    h.ctl = ctl;
     const dim3 grid(static_cast<unsigned>((hist_rows * 16 + 255) / 256),
                     static_cast<unsigned>(d.B * d.Hkv));
     launch_dependent(history_to_bf16_kernel, grid, dim3(256), 0, s, h);

@@ -365,12 +365,14 @@ __device__ __forceinline__ void load_q(const DecodeArgs &a, int u, int g, int t,
   float qr[32];
   if (a.q_dtype == KVQ_F32) {
     const float *q = static_cast<const float *>(a.q) + row * kD + 32 * t;
+    const bool ok = in_bounds(a.ctl, q, 32 * sizeof(float));
 #pragma unroll
-    for (int i = 0; i < 32; ++i) qr[i] = q[i] * a.scale_log2;
+    for (int i = 0; i < 32; ++i) qr[i] = ok ? q[i] * a.scale_log2 : 0.0f;
   } else {
     const uint16_t *q = static_cast<const uint16_t *>(a.q) + row * kD + 32 * t;
+    const bool ok = in_bounds(a.ctl, q, 32 * sizeof(uint16_t));
 #pragma unroll
-    for (int i = 0; i < 32; ++i) qr[i] = bf16_to_f32(q[i]) * a.scale_log2;
+    for (int i = 0; i < 32; ++i) qr[i] = ok ? bf16_to_f32(q[i]) * a.scale_log2 : 0.0f;
   }
 #pragma unroll
   for (int i = 0; i < 4; ++i)
@@ -390,8 +392,9 @@ __device__ __forceinline__ void load_q_raw(const DecodeArgs &a, int u, int g, in
   const long row = static_cast<long>(u) * kHeads + g;
   const uint4 *p = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(a.q) + row * kD +
                                                    32 * t);
+  const bool ok = in_bounds(a.ctl, p, 4 * sizeof(uint4));
 #pragma unroll
-  for (int i = 0; i < 4; ++i) r.w[i] = p[i];
+  for (int i = 0; i < 4; ++i) r.w[i] = ok ? p[i] : make_uint4(0u, 0u, 0u, 0u);
 }
 
 // load_q from a prefetched bf16 slice (the same values).
@@ -432,19 +435,26 @@ __device__ __forceinline__ void load_item(const DecodeArgs &a, int u, int j, uin
     const long gi = static_cast<long>(u) * a.Gs + g0;
     const long ti = static_cast<long>(u) * a.Vs + t0;
     const uint32_t kb = 2048u * ng, sb = 512u * ng, vb = 64u * nt, wb = 16u * nt;
-    mbar_arrive_expect_tx(bar, kb + sb + vb + wb);
-    bulk_g2s(dst, a.k_codes + gi * 2048, kb, bar);
-    bulk_g2s(dst + kOffKScale, a.k_scales + gi * 128, sb, bar);
-    bulk_g2s(dst + kOffVCode, a.v_codes + ti * 64, vb, bar);
-    bulk_g2s(dst + kOffVScale, a.v_scales + ti * 4, wb, bar);
+    // a copy whose source fails the bounds check is neither issued nor expected
+    const bool ok0 = in_bounds(a.ctl, a.k_codes + gi * 2048, kb);
+    const bool ok1 = in_bounds(a.ctl, a.k_scales + gi * 128, sb);
+    const bool ok2 = in_bounds(a.ctl, a.v_codes + ti * 64, vb);
+    const bool ok3 = in_bounds(a.ctl, a.v_scales + ti * 4, wb);
+    mbar_arrive_expect_tx(bar, (ok0 ? kb : 0u) + (ok1 ? sb : 0u) + (ok2 ? vb : 0u) + (ok3 ? wb : 0u));
+    if (ok0) bulk_g2s(dst, a.k_codes + gi * 2048, kb, bar);
+    if (ok1) bulk_g2s(dst + kOffKScale, a.k_scales + gi * 128, sb, bar);
+    if (ok2) bulk_g2s(dst + kOffVCode, a.v_codes + ti * 64, vb, bar);
+    if (ok3) bulk_g2s(dst + kOffVScale, a.v_scales + ti * 4, wb, bar);
   } else {
     const int w0 = kWinItem * (j - a.Gi);
     const int nt = min(kWinItem, a.R - w0);
     const long wi = static_cast<long>(u) * a.Ws + w0;
     const uint32_t bytes = 256u * nt;
-    mbar_arrive_expect_tx(bar, 2u * bytes);
-    bulk_g2s(dst, a.k_window + wi * 128, bytes, bar);
-    bulk_g2s(dst + kOffVWin, a.v_window + wi * 128, bytes, bar);
+    const bool ok0 = in_bounds(a.ctl, a.k_window + wi * 128, bytes);
+    const bool ok1 = in_bounds(a.ctl, a.v_window + wi * 128, bytes);
+    mbar_arrive_expect_tx(bar, (ok0 ? bytes : 0u) + (ok1 ? bytes : 0u));
+    if (ok0) bulk_g2s(dst, a.k_window + wi * 128, bytes, bar);
+    if (ok1) bulk_g2s(dst + kOffVWin, a.v_window + wi * 128, bytes, bar);
   }
 }
 
@@ -601,6 +611,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const Deco
     // heads 0-3 live in lanes with t < 2, heads 4-7 in lanes with t >= 2:
     // merge one half at a time through red_o
     float *part = partial_of(a, u, cta - cta_of_item(a, u * a.ipu));
+    const bool part_ok = in_bounds(a.ctl, part, sizeof(float) * kHeads * kPartFloats);
     for (int half = 0; half < 2; ++half) {
       if ((t >> 1) == half) {
         const int h0 = 2 * t - 4 * half;
@@ -621,6 +632,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const Deco
         float acc = 0.0f;
 #pragma unroll
         for (int w = 0; w < kConsumers; ++w) acc += sm.red_c[w][h] * sm.red_o[w][hh][d];
+        if (!part_ok) continue;
         part[h * kPartFloats + d] = acc;
         if (d == 0) {
           part[h * kPartFloats + kD] = sm.red_mx[h];
@@ -647,6 +659,12 @@ __global__ void __launch_bounds__(256) combine_kernel(const DecodeArgs a, OT *__
   const int n = cta_of_item(a, (u + 1) * a.ipu - 1) - cta_of_item(a, u * a.ipu) + 1;
   const float *base = partial_of(a, u, 0) + h * kPartFloats;
   constexpr int kSlot = kHeads * kPartFloats;
+#ifdef KVQ_DEBUG
+  // the unit's partial slots and this head's output row (the same in every lane)
+  if (!in_bounds(a.ctl, base - h * kPartFloats, sizeof(float) * n * kSlot) ||
+      !in_bounds(a.ctl, out + (static_cast<long>(u) * kHeads + h) * kD, kD * sizeof(OT)))
+    return;
+#endif
   constexpr int kBatch = 16;
   float m = -CUDART_INF_F, l = 0.0f;
   float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);

@@ -43,7 +43,25 @@ struct GenericArgs {
   float *mass;
   float sm_scale;
   Regions reg;
+  KernelCtl ctl;
 };
+
+// Whether the int4 bytes and scales of element d of token t (unit u) lie in
+// the call's buffers (see in_bounds; true outside debug builds).
+__device__ __forceinline__ bool elem_ok(const GenericArgs &a, long u, int t, int d, int D) {
+  const long g = u * a.Gs + t / kGroup, vr = u * a.Vs + t;
+  return in_bounds(a.ctl, a.k_codes + (g * kGroup + t % kGroup) * (D / 2) + d / 2, 1) &&
+         in_bounds(a.ctl, a.k_scales + g * D + d, sizeof(float)) &&
+         in_bounds(a.ctl, a.v_codes + vr * (D / 2) + d / 2, 1) &&
+         in_bounds(a.ctl, a.v_scales + vr * (D / 32) + d / 32, sizeof(float));
+}
+__device__ __forceinline__ bool win_elem_ok(const GenericArgs &a, long wi, long ei) {
+  const size_t kb = a.kwin == KVQ_F32 ? 4 : a.kwin == KVQ_BF16 ? 2 : 1;
+  const size_t vb = a.vwin == KVQ_F32 ? 4 : 2;
+  return in_bounds(a.ctl, static_cast<const uint8_t *>(a.k_window) + wi * kb, kb) &&
+         in_bounds(a.ctl, static_cast<const uint8_t *>(a.v_window) + wi * vb, vb) &&
+         (a.kwin != KVQ_MXFP8 || in_bounds(a.ctl, a.k_e8m0 + ei, 1));
+}
 
 __device__ __forceinline__ float nib(uint8_t byte, int odd) {
   return static_cast<float>(static_cast<int>(odd ? (byte >> 4) : (byte & 15)) - 8);
@@ -74,8 +92,10 @@ __global__ void __launch_bounds__(kWarps * 32) generic_attend_kernel(GenericArgs
   for (int i = tid; i < kRowsPerCta * D; i += blockDim.x) {
     const int r = i / D, d = i % D;
     float x = 0.0f;
-    if (q0 + r < a.n_q) {
-      const long gi = (qbase + q0 + r) * D + d;
+    const long gi = (qbase + q0 + r) * D + d;
+    if (q0 + r < a.n_q &&
+        in_bounds(a.ctl, static_cast<const uint8_t *>(a.q) + gi * (a.q_dtype == KVQ_F32 ? 4 : 2),
+                  a.q_dtype == KVQ_F32 ? 4 : 2)) {
       x = a.q_dtype == KVQ_F32 ? static_cast<const float *>(a.q)[gi]
                                : bf16_to_f32(static_cast<const uint16_t *>(a.q)[gi]);
     }
@@ -109,20 +129,23 @@ __global__ void __launch_bounds__(kWarps * 32) generic_attend_kernel(GenericArgs
         const int g = t / kGroup, r = t % kGroup;
         const long kb = ((u * a.Gs + g) * kGroup + r) * (D / 2) + d / 2;
         const long vb = (u * a.Vs + t) * (D / 2) + d / 2;
-        Ks[j * (D + 1) + d] = nib(a.k_codes[kb], d & 1) * a.k_scales[(u * a.Gs + g) * D + d];
-        Vs[j * D + d] = nib(a.v_codes[vb], d & 1) * a.v_scales[(u * a.Vs + t) * (D / 32) + d / 32];
+        const bool ok = elem_ok(a, u, t, d, D);
+        Ks[j * (D + 1) + d] = ok ? nib(a.k_codes[kb], d & 1) * a.k_scales[(u * a.Gs + g) * D + d] : 0.0f;
+        Vs[j * D + d] = ok ? nib(a.v_codes[vb], d & 1) * a.v_scales[(u * a.Vs + t) * (D / 32) + d / 32] : 0.0f;
       }
     } else
     for (int i = tid; i < kTileKeys * D; i += blockDim.x) {
       const int j = i / D, d = i % D, t = t0 + j;
       float kv = 0.0f, vv = 0.0f;
-      if (t < a.cut) {
+      if (t < a.cut && elem_ok(a, u, t, d, D)) {
         const int g = t / kGroup, r = t % kGroup;
         const long kb = ((u * a.Gs + g) * kGroup + r) * (D / 2) + d / 2;
         kv = nib(a.k_codes[kb], d & 1) * a.k_scales[(u * a.Gs + g) * D + d];
         const long vb = (u * a.Vs + t) * (D / 2) + d / 2;
         vv = nib(a.v_codes[vb], d & 1) * a.v_scales[(u * a.Vs + t) * (D / 32) + d / 32];
-      } else if (t < a.N) {
+      } else if (t >= a.cut && t < a.N &&
+                 win_elem_ok(a, (u * a.Ws + (t - a.cut)) * D + d,
+                             (u * a.Ws + (t - a.cut)) * (D / 32) + d / 32)) {
         const long wi = (u * a.Ws + (t - a.cut)) * D + d;
         if (a.kwin == KVQ_MXFP8)
           kv = mxfp8_value(static_cast<const uint8_t *>(a.k_window)[wi],
@@ -180,6 +203,11 @@ __global__ void __launch_bounds__(kWarps * 32) generic_attend_kernel(GenericArgs
     if (row >= a.n_q) continue;
     const float inv = 1.0f / l[r];
     const long ob = (qbase + row) * D;
+    if (!in_bounds(a.ctl,
+                   static_cast<uint8_t *>(a.out) + ob * (a.out_dtype == KVQ_F32 ? 4 : 2),
+                   D * (a.out_dtype == KVQ_F32 ? 4 : 2)) ||
+        (a.mass && !in_bounds(a.ctl, a.mass + (qbase + row) * a.reg.n, sizeof(float) * a.reg.n)))
+      continue;
 #pragma unroll
     for (int k = 0; k < DPL; ++k) {
       const float x = o[r][k] * inv;
@@ -214,6 +242,12 @@ __global__ void __launch_bounds__(kSmallWarps * 32) small_attend_kernel(GenericA
   const int h = static_cast<int>(bh % a.Hq);
   const long b = bh / a.Hq;
   const long u = b * a.Hkv + h / a.group;
+  const size_t qe = a.q_dtype == KVQ_F32 ? 4 : 2, oe = a.out_dtype == KVQ_F32 ? 4 : 2;
+  // this row's q, output and masses (the same in every thread)
+  if (!in_bounds(a.ctl, static_cast<const uint8_t *>(a.q) + row * D * qe, D * qe) ||
+      !in_bounds(a.ctl, static_cast<uint8_t *>(a.out) + row * D * oe, D * oe) ||
+      (a.mass && !in_bounds(a.ctl, a.mass + row * a.reg.n, sizeof(float) * a.reg.n)))
+    return;
 
   float q[D];
 #pragma unroll
@@ -236,7 +270,19 @@ __global__ void __launch_bounds__(kSmallWarps * 32) small_attend_kernel(GenericA
 
   for (int t0 = 32 * warp; t0 < a.N; t0 += 32 * kSmallWarps) {
     const int t = t0 + lane;
-    const bool in_codes = t < a.cut, in_win = !in_codes && t < a.N;
+    bool in_codes = t < a.cut, in_win = !in_codes && t < a.N;
+    if (in_codes) {  // the token's code rows, scale group and V scales
+      const long g = u * a.Gs + t / kGroup, vr = u * a.Vs + t;
+      in_codes = in_bounds(a.ctl, a.k_codes + (g * kGroup + t % kGroup) * (D / 2), D / 2) &&
+                 in_bounds(a.ctl, a.v_codes + vr * (D / 2), D / 2) &&
+                 in_bounds(a.ctl, a.v_scales + vr * (D / 32), sizeof(float) * (D / 32)) &&
+                 in_bounds(a.ctl, a.k_scales + g * D, sizeof(float) * D);
+    } else if (in_win) {  // its window rows
+      const long wr = (u * a.Ws + (t - a.cut)) * D;
+      const size_t kb = a.kwin == KVQ_F32 ? 4 : 2, vb = a.vwin == KVQ_F32 ? 4 : 2;
+      in_win = in_bounds(a.ctl, static_cast<const uint8_t *>(a.k_window) + wr * kb, D * kb) &&
+               in_bounds(a.ctl, static_cast<const uint8_t *>(a.v_window) + wr * vb, D * vb);
+    }
     // the key's K and V nibbles stay packed until used (8 registers, not 2D)
     uint32_t kw[D / 8], vw[D / 8];
     const float *ks = a.k_scales;
@@ -366,7 +412,7 @@ void launch_dpl(const GenericArgs &a, int B, cudaStream_t s) {
 
 int launch_attend_generic(const kvq_cache &c, const void *q, int q_dtype, int Hq, int n_q,
                           float sm_scale, void *out, int out_dtype, const int32_t *bounds,
-                          int n_regions, float *mass, const KernelCtl &, cudaStream_t s) {
+                          int n_regions, float *mass, const KernelCtl &ctl, cudaStream_t s) {
   const CacheDims d = dims_of(c);
   GenericArgs a;
   a.k_codes = c.k_codes;
@@ -397,6 +443,7 @@ int launch_attend_generic(const kvq_cache &c, const void *q, int q_dtype, int Hq
   a.mass = mass;
   a.sm_scale = sm_scale;
   a.reg = make_regions(bounds, n_regions);
+  a.ctl = ctl;
   if (d.D == 32 && c.kwin_dtype != KVQ_MXFP8 && a.reg.n <= kSmallRegions) {
     const long rows = static_cast<long>(d.B) * Hq * n_q;  // one CTA per query row
     launch_dependent(small_attend_kernel<32>, dim3(static_cast<unsigned>(rows)),

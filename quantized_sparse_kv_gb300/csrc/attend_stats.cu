@@ -62,6 +62,7 @@ struct StatsArgs {
   float *s_mx;         // workspace [rows][N]: the same on the MXFP8 Q/K path
   int T;               // key tiles of 32 per unit
   int key_splits;      // scores_kernel CTAs per group of rows
+  KernelCtl ctl;
 };
 
 constexpr int kRows = 16;  // query rows per scores_kernel CTA
@@ -70,11 +71,19 @@ constexpr int kRows = 16;  // query rows per scores_kernel CTA
 __device__ __forceinline__ float key_value(const StatsArgs &a, long u, int j, int d) {
   if (j < a.cut) {
     const long g = u * a.Gs + (j >> 5);
+    if (!in_bounds(a.ctl, a.k_codes + (g * kGroup + (j & 31)) * (a.D / 2) + d / 2, 1) ||
+        !in_bounds(a.ctl, a.k_scales + g * a.D + d, sizeof(float)))
+      return 0.0f;
     const uint8_t byte = a.k_codes[(g * kGroup + (j & 31)) * (a.D / 2) + d / 2];
     const int code = static_cast<int>((d & 1) ? (byte >> 4) : (byte & 15)) - 8;
     return static_cast<float>(code) * a.k_scales[g * a.D + d];
   }
   const long row = u * a.Ws + (j - a.cut);
+  const size_t eb = a.kwin == KVQ_F32 ? 4 : a.kwin == KVQ_BF16 ? 2 : 1;
+  if (!in_bounds(a.ctl, static_cast<const uint8_t *>(a.k_window) + (row * a.D + d) * eb, eb) ||
+      (a.kwin == KVQ_MXFP8 &&
+       !in_bounds(a.ctl, a.k_e8m0 + row * (a.D / kGroup) + d / kGroup, 1)))
+    return 0.0f;
   if (a.kwin == KVQ_F32) return static_cast<const float *>(a.k_window)[row * a.D + d];
   if (a.kwin == KVQ_BF16)
     return load_f32(static_cast<const __nv_bfloat16 *>(a.k_window) + row * a.D + d);
@@ -138,6 +147,12 @@ __global__ void __launch_bounds__(kThreads) keys_kernel(const StatsArgs a) {
   constexpr int D = 32 * E;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long u = blockIdx.y;
+  const long o = (u * a.T + blockIdx.x) * D * 32;
+  // the signs and this tile's two outputs (the same in every thread)
+  if ((a.signs && !in_bounds(a.ctl, a.signs, sizeof(float) * D)) ||
+      !in_bounds(a.ctl, a.k_ref + o, sizeof(float) * D * 32) ||
+      !in_bounds(a.ctl, a.k_mx + o, sizeof(float) * D * 32))
+    return;
   for (int kk = 0; kk < 4; ++kk) {
     const int c = 4 * warp + kk;  // key within the tile
     const int j = blockIdx.x * 32 + c;
@@ -159,7 +174,6 @@ __global__ void __launch_bounds__(kThreads) keys_kernel(const StatsArgs a) {
     for (int t = 0; t < E; ++t) tile[(D + lane * E + t) * 33 + c] = x[t];
   }
   __syncthreads();
-  const long o = (u * a.T + blockIdx.x) * D * 32;
   for (int i = threadIdx.x; i < D * 32; i += kThreads) {
     a.k_ref[o + i] = tile[(i >> 5) * 33 + (i & 31)];
     a.k_mx[o + i] = tile[(D + (i >> 5)) * 33 + (i & 31)];
@@ -183,6 +197,13 @@ __global__ void __launch_bounds__(kThreads) scores_kernel(const StatsArgs a) {
   const int i0 = blockIdx.x * kRows;
   const int nr = min(kRows, a.n_q - i0);
   const long row0 = bh * a.n_q + i0;
+  const size_t qe = a.q_dtype == KVQ_F32 ? 4 : 2;
+  // q rows, signs and score rows of the block (the same in every thread)
+  if (!in_bounds(a.ctl, static_cast<const uint8_t *>(a.q) + row0 * D * qe, qe * D * nr) ||
+      (a.signs && !in_bounds(a.ctl, a.signs, sizeof(float) * D)) ||
+      !in_bounds(a.ctl, a.s_ref + row0 * a.N, sizeof(float) * a.N * nr) ||
+      !in_bounds(a.ctl, a.s_mx + row0 * a.N, sizeof(float) * a.N * nr))
+    return;
   for (int e = threadIdx.x; e < kRows * D; e += kThreads) {
     const int r = e / D, d = e % D;
     const long gi = (row0 + r) * D + d;
@@ -208,6 +229,11 @@ __global__ void __launch_bounds__(kThreads) scores_kernel(const StatsArgs a) {
   // shared memory feeds both
   for (int t0 = t_lo + warp; t0 < t_hi; t0 += 2 * kWarps) {
     const int t1 = t0 + kWarps < t_hi ? t0 + kWarps : t0;
+    if (!in_bounds(a.ctl, a.k_ref + (u * a.T + t0) * D * 32, sizeof(float) * D * 32) ||
+        !in_bounds(a.ctl, a.k_mx + (u * a.T + t0) * D * 32, sizeof(float) * D * 32) ||
+        !in_bounds(a.ctl, a.k_ref + (u * a.T + t1) * D * 32, sizeof(float) * D * 32) ||
+        !in_bounds(a.ctl, a.k_mx + (u * a.T + t1) * D * 32, sizeof(float) * D * 32))
+      continue;
     const float *kr0 = a.k_ref + (u * a.T + t0) * D * 32 + lane;
     const float *km0 = a.k_mx + (u * a.T + t0) * D * 32 + lane;
     const float *kr1 = a.k_ref + (u * a.T + t1) * D * 32 + lane;
@@ -410,6 +436,11 @@ __global__ void __launch_bounds__(kThreads) stats_kernel(const StatsArgs a) {
   __shared__ uint32_t hist[256], hist_top[256], sel[2];
   const long row = blockIdx.x;       // (b * Hq + h) * n_q + i
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // the row's two score rows and its statistics (the same in every thread)
+  if (!in_bounds(a.ctl, a.s_ref + row * a.N, sizeof(float) * a.N) ||
+      !in_bounds(a.ctl, a.s_mx + row * a.N, sizeof(float) * a.N) ||
+      !in_bounds(a.ctl, a.stats + row * KVQ_N_STATS, sizeof(float) * KVQ_N_STATS))
+    return;
   for (int j = threadIdx.x; j < a.N; j += kThreads) {
     s_ref[j] = a.s_ref[row * a.N + j];
     s_mx[j] = a.s_mx[row * a.N + j];
@@ -519,9 +550,10 @@ size_t stats_workspace_bytes(const kvq_cache &c, int Hq, int n_q) {
 
 int launch_attend_stats(const kvq_cache &c, const void *q, int q_dtype, int Hq, int n_q,
                         float sm_scale, const float *signs, float *stats, void *ws,
-                        cudaStream_t s) {
+                        const KernelCtl &ctl, cudaStream_t s) {
   const CacheDims d = dims_of(c);
   StatsArgs a;
+  a.ctl = ctl;
   a.k_codes = c.k_codes;
   a.k_scales = c.k_scales;
   a.k_window = c.k_window;

@@ -33,7 +33,31 @@ kvq::KernelCtl make_ctl(int32_t *dev_status) {
   c.dev_status = dev_status;
   c.wait_limit_ns = g_wait_limit_ns ? g_wait_limit_ns : kDefaultWaitNs;
   c.drop_item = g_drop_item;
+#ifdef KVQ_DEBUG
+  c.n_bufs = 0;
+#endif
   return c;
+}
+
+// The bounds-check table of a KVQ_DEBUG build: each device buffer of the
+// call, as [p, p + bytes). Other builds keep no table and these do nothing.
+void ctl_add(kvq::KernelCtl &c, const void *p, size_t bytes) {
+#ifdef KVQ_DEBUG
+  if (!p || bytes == 0 || c.n_bufs >= kvq::kMaxBufs) return;
+  c.buf_lo[c.n_bufs] = reinterpret_cast<uintptr_t>(p);
+  c.buf_hi[c.n_bufs] = reinterpret_cast<uintptr_t>(p) + bytes;
+  ++c.n_bufs;
+#else
+  (void)c;
+  (void)p;
+  (void)bytes;
+#endif
+}
+
+// Bytes of rows x d elements of type dt.
+size_t rows_bytes(long rows, int d, int32_t dt) {
+  return static_cast<size_t>(rows) * static_cast<size_t>(d) *
+         (dt == KVQ_F32 ? 4u : dt == KVQ_BF16 ? 2u : 1u);
 }
 
 bool shape_ok(int32_t batch, int32_t kv_heads, int32_t n_tokens, int32_t head_dim, int32_t recent,
@@ -94,6 +118,30 @@ void reserve_static_scratch() {
 float resolve_scale(float sm_scale, int head_dim) {
   return sm_scale > 0.0f ? sm_scale
                          : static_cast<float>(1.0 / sqrt(static_cast<double>(head_dim)));
+}
+
+// The cache's arrays, at the sizes its shape (and reserved room) gives.
+void ctl_add_cache(kvq::KernelCtl &c, const kvq_cache &k) {
+#ifdef KVQ_DEBUG
+  size_t sz[8];
+  const kvq_status st =
+      k.cap_groups > 0
+          ? kvq_cache_sizes_reserved(k.batch, k.kv_heads, k.head_dim, k.kwin_dtype, k.vwin_dtype,
+                                     k.cap_groups, k.cap_window, sz)
+          : kvq_cache_sizes(k.batch, k.kv_heads, k.n_tokens, k.head_dim, k.recent, k.kwin_dtype,
+                            k.vwin_dtype, sz);
+  if (st != KVQ_OK) return;
+  ctl_add(c, k.k_codes, sz[0]);
+  ctl_add(c, k.k_scales, sz[1]);
+  ctl_add(c, k.v_codes, sz[2]);
+  ctl_add(c, k.v_scales, sz[3]);
+  ctl_add(c, k.k_window, sz[4]);
+  ctl_add(c, k.v_window, sz[5]);
+  ctl_add(c, k.k_window_e8m0, sz[6]);
+#else
+  (void)c;
+  (void)k;
+#endif
 }
 
 }  // namespace
@@ -164,7 +212,12 @@ kvq_status kv_pack(const void *k, const void *v, int32_t in_dtype, kvq_cache *ca
   cache->header[2] = static_cast<uint32_t>(cache->recent);
   cache->header[3] = 32u;
   reserve_static_scratch();
-  const int n = kvq::launch_pack(k, v, in_dtype, *cache, make_ctl(dev_status),
+  kvq::KernelCtl ctl = make_ctl(dev_status);
+  ctl_add_cache(ctl, *cache);
+  const long units = static_cast<long>(cache->batch) * cache->kv_heads;
+  ctl_add(ctl, k, rows_bytes(units * cache->n_tokens, cache->head_dim, in_dtype));
+  ctl_add(ctl, v, rows_bytes(units * cache->n_tokens, cache->head_dim, in_dtype));
+  const int n = kvq::launch_pack(k, v, in_dtype, *cache, ctl,
                                  reinterpret_cast<cudaStream_t>(stream));
   return finish(n, "pack");
 }
@@ -192,7 +245,12 @@ kvq_status kv_append(kvq_cache *cache, const void *k_new, const void *v_new, int
   if (m > 0 && static_cast<long>(cache->batch) * cache->kv_heads > 65535)
     return KVQ_ERR_UNSUPPORTED;
   reserve_static_scratch();
-  const int n = kvq::launch_append(*cache, k_new, v_new, in_dtype, n_new, m, r2,
+  kvq::KernelCtl ctl = make_ctl(dev_status);
+  ctl_add_cache(ctl, *cache);
+  const long units = static_cast<long>(cache->batch) * cache->kv_heads;
+  ctl_add(ctl, k_new, rows_bytes(units * n_new, cache->head_dim, in_dtype));
+  ctl_add(ctl, v_new, rows_bytes(units * n_new, cache->head_dim, in_dtype));
+  const int n = kvq::launch_append(*cache, k_new, v_new, in_dtype, n_new, m, r2, ctl,
                                    reinterpret_cast<cudaStream_t>(stream));
   const kvq_status done = finish(n, "append");
   if (done != KVQ_OK) return done;
@@ -251,7 +309,15 @@ kvq_status kv_attend(const kvq_cache *cache, const void *q, int32_t q_dtype, int
       (dev_status && !aligned16(dev_status)))
     return KVQ_ERR_ALIGN;
 
-  const kvq::KernelCtl ctl = make_ctl(dev_status);
+  kvq::KernelCtl ctl = make_ctl(dev_status);
+  {
+    const long rows = static_cast<long>(cache->batch) * q_heads * n_q;
+    ctl_add_cache(ctl, *cache);
+    ctl_add(ctl, q, rows_bytes(rows, cache->head_dim, q_dtype));
+    ctl_add(ctl, out, rows_bytes(rows, cache->head_dim, out_dtype));
+    if (regions) ctl_add(ctl, region_mass, rows_bytes(rows, n_regions, KVQ_F32));
+    ctl_add(ctl, workspace, *ws_bytes);
+  }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (path == CHUNK) {
     const int n = kvq::launch_attend_chunk(*cache, q, q_heads, n_q,
@@ -297,8 +363,18 @@ kvq_status kv_attend_stats(const kvq_cache *cache, const void *q, int32_t q_dtyp
       (hadamard_signs && !aligned16(hadamard_signs)) || (dev_status && !aligned16(dev_status)))
     return KVQ_ERR_ALIGN;
   const float scale = resolve_scale(sm_scale, d);
+  kvq::KernelCtl ctl = make_ctl(dev_status);
+  {
+    const long rows = static_cast<long>(cache->batch) * q_heads * n_q;
+    ctl_add_cache(ctl, *cache);
+    ctl_add(ctl, q, rows_bytes(rows, d, q_dtype));
+    ctl_add(ctl, stats, rows_bytes(rows, KVQ_N_STATS, KVQ_F32));
+    ctl_add(ctl, hadamard_signs, rows_bytes(1, d, KVQ_F32));
+    ctl_add(ctl, workspace, *ws_bytes);
+  }
   const int n = kvq::launch_attend_stats(*cache, q, q_dtype, q_heads, n_q, scale, hadamard_signs,
-                                         stats, workspace, reinterpret_cast<cudaStream_t>(stream));
+                                         stats, workspace, ctl,
+                                         reinterpret_cast<cudaStream_t>(stream));
   if (n < 0) return KVQ_ERR_UNSUPPORTED;
   return finish(n, "stats");
 }
@@ -332,15 +408,24 @@ kvq_status kv_attend_candidates(const kvq_cache *cache, const void *q, int32_t q
     return KVQ_ERR_ALIGN;
   const float scale = resolve_scale(sm_scale, cache->head_dim);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  kvq::KernelCtl ctl = make_ctl(dev_status);
+  {
+    const long rows = static_cast<long>(cache->batch) * q_heads * n_q;
+    ctl_add_cache(ctl, *cache);
+    ctl_add(ctl, q, rows_bytes(rows, cache->head_dim, q_dtype));
+    ctl_add(ctl, out, rows_bytes(rows, cache->head_dim, out_dtype));
+    ctl_add(ctl, idx, rows_bytes(rows, n_cand, KVQ_F32));
+    ctl_add(ctl, workspace, *ws_bytes);
+  }
   if (uni) {
     const int n = kvq::launch_candidates_union(*cache, q, idx, n_cand, validate,
                                                static_cast<float>(scale * kLog2e), out, out_dtype,
-                                               workspace, make_ctl(dev_status), sms, s);
+                                               workspace, ctl, sms, s);
     return finish(n, "candidates_union");
   }
   const int n = kvq::launch_attend_candidates(*cache, q, q_dtype, q_heads, n_q, idx, n_cand,
                                               validate, static_cast<float>(scale * kLog2e), out,
-                                              out_dtype, make_ctl(dev_status), s);
+                                              out_dtype, ctl, s);
   return finish(n, "candidates");
 }
 
@@ -364,9 +449,18 @@ kvq_status kv_attend_candidates_topk(const kvq_cache *cache, const void *q, int3
       (dev_status && !aligned16(dev_status)))
     return KVQ_ERR_ALIGN;
   const float scale = resolve_scale(sm_scale, cache->head_dim);
+  kvq::KernelCtl ctl = make_ctl(dev_status);
+  {
+    const long rows = static_cast<long>(cache->batch) * q_heads * n_q;
+    ctl_add_cache(ctl, *cache);
+    ctl_add(ctl, q, rows_bytes(rows, cache->head_dim, q_dtype));
+    ctl_add(ctl, out, rows_bytes(rows, cache->head_dim, out_dtype));
+    ctl_add(ctl, idx, rows_bytes(rows, n_cand, KVQ_F32));
+    ctl_add(ctl, selected, rows_bytes(rows, top_k, KVQ_F32));
+  }
   const int n = kvq::launch_attend_candidates(
       *cache, q, q_dtype, q_heads, n_q, idx, n_cand, 0, static_cast<float>(scale * kLog2e), out,
-      out_dtype, make_ctl(dev_status), reinterpret_cast<cudaStream_t>(stream), top_k, selected);
+      out_dtype, ctl, reinterpret_cast<cudaStream_t>(stream), top_k, selected);
   if (n < 0) return KVQ_ERR_UNSUPPORTED;
   return finish(n, "candidates_topk");
 }
@@ -400,16 +494,25 @@ kvq_status kv_attend_candidates_block(const kvq_cache *cache, const void *q, int
     return KVQ_ERR_ALIGN;
   const float scale = resolve_scale(sm_scale, cache->head_dim);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  kvq::KernelCtl ctl = make_ctl(dev_status);
+  {
+    const long rows = static_cast<long>(cache->batch) * q_heads * n_q;
+    ctl_add_cache(ctl, *cache);
+    ctl_add(ctl, q, rows_bytes(rows, cache->head_dim, q_dtype));
+    ctl_add(ctl, out, rows_bytes(rows, cache->head_dim, out_dtype));
+    ctl_add(ctl, idx, rows_bytes(lists, n_cand, KVQ_F32));
+    ctl_add(ctl, workspace, *ws_bytes);
+  }
   if (tensor) {
     const int n = kvq::launch_candidate_lists(*cache, q, q_heads, n_q, idx, n_cand, block_q,
                                               static_cast<float>(scale * kLog2e), out, out_dtype,
-                                              workspace, make_ctl(dev_status), s);
+                                              workspace, ctl, s);
     if (n < 0) return KVQ_ERR_CUDA;
     return finish(n, "candidates_block_tensor");
   }
   const int n = kvq::launch_attend_candidates(*cache, q, q_dtype, q_heads, n_q, idx, n_cand, 0,
                                               static_cast<float>(scale * kLog2e), out, out_dtype,
-                                              make_ctl(dev_status), s, 0, nullptr, block_q);
+                                              ctl, s, 0, nullptr, block_q);
   return finish(n, "candidates_block");
 }
 
@@ -446,9 +549,17 @@ kvq_status kv_attend_region_drop(const kvq_cache *cache, const void *q, int32_t 
       (dev_status && !aligned16(dev_status)))
     return KVQ_ERR_ALIGN;
   const float scale = resolve_scale(sm_scale, cache->head_dim);
+  kvq::KernelCtl ctl = make_ctl(dev_status);
+  {
+    const long rows = static_cast<long>(cache->batch) * q_heads * n_q;
+    ctl_add_cache(ctl, *cache);
+    ctl_add(ctl, q, rows_bytes(rows, cache->head_dim, q_dtype));
+    ctl_add(ctl, out, rows_bytes(rows, cache->head_dim, out_dtype));
+    ctl_add(ctl, workspace, *ws_bytes);
+  }
   const int n = kvq::launch_region_drop(*cache, q, q_heads, n_q, region_bounds, n_regions,
                                         drop_mask, static_cast<float>(scale * kLog2e), out,
-                                        out_dtype, workspace, make_ctl(dev_status),
+                                        out_dtype, workspace, ctl,
                                         reinterpret_cast<cudaStream_t>(stream));
   if (n < 0) return KVQ_ERR_CUDA;
   return finish(n, "region_drop");
@@ -473,8 +584,16 @@ kvq_status kv_attend_decode_static(const kvq_cache *cache, const void *q, int32_
   void *scratch = nullptr;
   if (kvq::decode_static_scratch(&scratch) != cudaSuccess) return KVQ_ERR_CUDA;
   const float scale = resolve_scale(sm_scale, cache->head_dim);
+  kvq::KernelCtl ctl = make_ctl(dev_status);
+  {
+    const long rows = static_cast<long>(cache->batch) * q_heads;
+    ctl_add_cache(ctl, *cache);
+    ctl_add(ctl, q, rows_bytes(rows, cache->head_dim, q_dtype));
+    ctl_add(ctl, out, rows_bytes(rows, cache->head_dim, out_dtype));
+    ctl_add(ctl, scratch, kvq::decode_static_scratch_limit());
+  }
   const int n = kvq::launch_attend_decode(*cache, q, q_dtype, static_cast<float>(scale * kLog2e),
-                                          out, out_dtype, scratch, make_ctl(dev_status), sms,
+                                          out, out_dtype, scratch, ctl, sms,
                                           reinterpret_cast<cudaStream_t>(stream));
   return finish(n, "decode_static");
 }
@@ -482,6 +601,14 @@ kvq_status kv_attend_decode_static(const kvq_cache *cache, const void *q, int32_
 int32_t kvq_last_launch_count(void) { return g_last_launches; }
 
 const char *kvq_last_path(void) { return g_last_path; }
+
+int32_t kvq_debug_checks(void) {
+#ifdef KVQ_DEBUG
+  return 1;
+#else
+  return 0;
+#endif
+}
 
 void kvq_debug_set(uint32_t wait_limit_ns, int32_t drop_item) {
   g_wait_limit_ns = wait_limit_ns;

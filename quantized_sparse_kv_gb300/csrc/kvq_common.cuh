@@ -14,15 +14,53 @@ namespace kvq {
 
 constexpr int kGroup = 32;
 
+#ifdef KVQ_DEBUG
+constexpr int kMaxBufs = 16;  // buffers one call may register for the bounds checks
+#endif
+
 // Launch-wide settings every kernel receives by value.
 struct KernelCtl {
   int32_t *dev_status;      // may be nullptr
   uint64_t wait_limit_ns;   // bound of every mbarrier wait
   int32_t drop_item;        // test hook: loader skips this work item (-1: none)
+#ifdef KVQ_DEBUG
+  // The device buffers of the call ([lo, hi) byte ranges): the cache's
+  // arrays, q, the outputs, index lists, workspace.
+  int32_t n_bufs;
+  uintptr_t buf_lo[kMaxBufs], buf_hi[kMaxBufs];
+#endif
 };
 
-__device__ __forceinline__ void flag_error(const KernelCtl &ctl, int bit) {
+__host__ __device__ __forceinline__ void flag_error(const KernelCtl &ctl, int bit) {
+#ifdef __CUDA_ARCH__
   if (ctl.dev_status) atomicOr(ctl.dev_status, bit);
+#else
+  if (ctl.dev_status) *ctl.dev_status |= bit;  // host: the check's own tests
+#endif
+}
+
+// Bounds check of a global access. In a build with KVQ_DEBUG defined: true
+// when the bytes [p, p + bytes) lie inside one buffer of the call; otherwise
+// KVQ_DEV_BOUNDS is set and the caller leaves the access out (a load reads
+// zeros, a store is dropped, a bulk copy is not issued and not expected), so
+// a wrong index is reported instead of touching memory. Every kernel checks
+// each contiguous range it derives from its indices (a row, a chunk, a copy)
+// before the accesses inside it. Other builds: true, and the check
+// compiles away.
+__host__ __device__ __forceinline__ bool in_bounds(const KernelCtl &ctl, const void *p,
+                                                   size_t bytes) {
+#ifdef KVQ_DEBUG
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p), b = a + bytes;
+  for (int i = 0; i < ctl.n_bufs; ++i)
+    if (a >= ctl.buf_lo[i] && b <= ctl.buf_hi[i] && b >= a) return true;
+  flag_error(ctl, KVQ_DEV_BOUNDS);
+  return false;
+#else
+  (void)ctl;
+  (void)p;
+  (void)bytes;
+  return true;
+#endif
 }
 
 __device__ __forceinline__ uint64_t global_ns() {

@@ -57,7 +57,7 @@ int launch_pack(const void *k, const void *v, int in_dtype, const kvq_cache &c,
 // (sequence, head) after the current ones; m groups of the oldest window
 // tokens become int4 and the window becomes R_new rows.
 int launch_append(const kvq_cache &c, const void *k_new, const void *v_new, int in_dtype,
-                  int n_new, int m, int R_new, cudaStream_t s);
+                  int n_new, int m, int R_new, const KernelCtl &ctl, cudaStream_t s);
 
 // attend_generic.cu: fp32 CUDA-core attention for any supported shape.
 int launch_attend_generic(const kvq_cache &c, const void *q, int q_dtype, int Hq, int n_q,
@@ -119,6 +119,6 @@ int stats_max_tokens();
 size_t stats_workspace_bytes(const kvq_cache &c, int Hq, int n_q);
 int launch_attend_stats(const kvq_cache &c, const void *q, int q_dtype, int Hq, int n_q,
                         float sm_scale, const float *signs, float *stats, void *ws,
-                        cudaStream_t s);
+                        const KernelCtl &ctl, cudaStream_t s);
 
 }  // namespace kvq

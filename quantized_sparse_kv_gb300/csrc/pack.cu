@@ -50,7 +50,8 @@ template <typename T>
 __global__ void __launch_bounds__(256) pack_k128_kernel(const T *__restrict__ k, int N, int cut,
                                                         int Gs, long u0,
                                                         uint8_t *__restrict__ k_codes,
-                                                        float *__restrict__ k_scales) {
+                                                        float *__restrict__ k_scales,
+                                                        const KernelCtl ctl) {
   wait_prior_grid();
   allow_next_grid();
   constexpr int D = 128;
@@ -67,7 +68,7 @@ __global__ void __launch_bounds__(256) pack_k128_kernel(const T *__restrict__ k,
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int t = 4 * warp + i;
-    if (t < valid)
+    if (t < valid && in_bounds(ctl, src + static_cast<long>(t) * D, 4 * sizeof(T)))
       load4(src + static_cast<long>(t) * D, x[i]);
     else
       x[i][0] = x[i][1] = x[i][2] = x[i][3] = 0.0f;
@@ -82,7 +83,8 @@ __global__ void __launch_bounds__(256) pack_k128_kernel(const T *__restrict__ k,
     for (int w = 1; w < 8; ++w) mx = fmaxf(mx, part[w][threadIdx.x]);
     const float sc = int4_scale(mx);
     scale[threadIdx.x] = sc;
-    k_scales[ug * D + threadIdx.x] = sc;
+    if (in_bounds(ctl, k_scales + ug * D + threadIdx.x, sizeof(float)))
+      k_scales[ug * D + threadIdx.x] = sc;
   }
   __syncthreads();
   const float4 sc = *reinterpret_cast<const float4 *>(&scale[4 * lane]);
@@ -92,8 +94,8 @@ __global__ void __launch_bounds__(256) pack_k128_kernel(const T *__restrict__ k,
     uint32_t w = 0u;
 #pragma unroll
     for (int e = 0; e < 4; ++e) w |= static_cast<uint32_t>(int4_code(x[i][e], s4[e]) + 8) << (4 * e);
-    *reinterpret_cast<uint16_t *>(k_codes + (ug * kGroup + 4 * warp + i) * (D / 2) + 2 * lane) =
-        static_cast<uint16_t>(w);
+    uint8_t *dst = k_codes + (ug * kGroup + 4 * warp + i) * (D / 2) + 2 * lane;
+    if (in_bounds(ctl, dst, 2)) *reinterpret_cast<uint16_t *>(dst) = static_cast<uint16_t>(w);
   }
 }
 
@@ -129,7 +131,8 @@ template <typename T>
 __global__ void __launch_bounds__(256) pack_k_kernel(const T *__restrict__ k, long tasks, int N,
                                                      int D, int cut, int Gk, int Gs,
                                                      uint8_t *__restrict__ k_codes,
-                                                     float *__restrict__ k_scales) {
+                                                     float *__restrict__ k_scales,
+                                                     const KernelCtl ctl) {
   wait_prior_grid();
   allow_next_grid();
   const long task = blockIdx.x * static_cast<long>(blockDim.x) + threadIdx.x;
@@ -145,7 +148,7 @@ __global__ void __launch_bounds__(256) pack_k_kernel(const T *__restrict__ k, lo
   typename PairOf<T>::type x[kGroup];
 #pragma unroll
   for (int t = 0; t < kGroup; ++t) {
-    if (t < valid)
+    if (t < valid && in_bounds(ctl, src + static_cast<long>(t) * D, 2 * sizeof(T)))
       x[t].load(src + static_cast<long>(t) * D);
     else
       x[t].zero();
@@ -157,8 +160,10 @@ __global__ void __launch_bounds__(256) pack_k_kernel(const T *__restrict__ k, lo
     a1 = fmaxf(a1, fabsf(x[t].hi()));
   }
   const float s0 = int4_scale(a0), s1 = int4_scale(a1);
-  *reinterpret_cast<float2 *>(k_scales + ug * D + 2 * p) = make_float2(s0, s1);
+  if (in_bounds(ctl, k_scales + ug * D + 2 * p, 2 * sizeof(float)))
+    *reinterpret_cast<float2 *>(k_scales + ug * D + 2 * p) = make_float2(s0, s1);
   uint8_t *dst = k_codes + ug * (kGroup * D / 2) + p;
+  if (!in_bounds(ctl, dst, (kGroup - 1) * (D / 2) + 1)) return;
 #pragma unroll
   for (int t = 0; t < kGroup; ++t)
     dst[t * (D / 2)] =
@@ -172,7 +177,8 @@ template <typename T>
 __global__ void __launch_bounds__(256) pack_v_kernel(const T *__restrict__ v, long u0, int t0,
                                                      int nt, int N, int D, int Vs,
                                                      uint8_t *__restrict__ v_codes,
-                                                     float *__restrict__ v_scales) {
+                                                     float *__restrict__ v_scales,
+                                                     const KernelCtl ctl) {
   wait_prior_grid();
   allow_next_grid();
   const int groups = D / kGroup;
@@ -183,11 +189,12 @@ __global__ void __launch_bounds__(256) pack_v_kernel(const T *__restrict__ v, lo
   const long u = u0 + blockIdx.y;
   const long row = u * Vs + t;  // Vs: V rows per (sequence, head) in the arrays
   const T *src = v + (u * N + t) * D + j * kGroup;
+  const bool src_ok = in_bounds(ctl, src, kGroup * sizeof(T));
   float x[kGroup];
 #pragma unroll
   for (int i = 0; i < kGroup / 4; ++i) {
-    float f[4];
-    load4(src + 4 * i, f);
+    float f[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    if (src_ok) load4(src + 4 * i, f);
     x[4 * i] = f[0];
     x[4 * i + 1] = f[1];
     x[4 * i + 2] = f[2];
@@ -201,15 +208,16 @@ __global__ void __launch_bounds__(256) pack_v_kernel(const T *__restrict__ v, lo
 #pragma unroll
   for (int e = 0; e < kGroup; ++e)
     w[e >> 3] |= static_cast<uint32_t>(int4_code(x[e], s) + 8) << (4 * (e & 7));
-  *reinterpret_cast<uint4 *>(v_codes + row * (D / 2) + j * (kGroup / 2)) = make_uint4(w[0], w[1], w[2], w[3]);
-  v_scales[row * groups + j] = s;
+  uint8_t *cd = v_codes + row * (D / 2) + j * (kGroup / 2);
+  if (in_bounds(ctl, cd, 16)) *reinterpret_cast<uint4 *>(cd) = make_uint4(w[0], w[1], w[2], w[3]);
+  if (in_bounds(ctl, v_scales + row * groups + j, sizeof(float))) v_scales[row * groups + j] = s;
 }
 
 // Window copy with dtype change (fp32 <-> bf16, nearest even).
 // Ws: window rows per (sequence, head) in the arrays.
 template <typename TI, typename TO>
 __global__ void window_copy_kernel(const TI *__restrict__ x, long rows, int N, int D, int R,
-                                   int Ws, TO *__restrict__ w) {
+                                   int Ws, TO *__restrict__ w, const KernelCtl ctl) {
   wait_prior_grid();
   allow_next_grid();
   const long n = rows * D;
@@ -217,7 +225,10 @@ __global__ void window_copy_kernel(const TI *__restrict__ x, long rows, int N, i
        i += static_cast<long>(gridDim.x) * blockDim.x) {
     const long row = i / D, d = i % D;
     const long u = row / R, t = row % R;
-    store_from_f32(w + (u * Ws + t) * D + d, load_f32(x + (u * N + (N - R) + t) * D + d));
+    const TI *src = x + (u * N + (N - R) + t) * D + d;
+    TO *dst = w + (u * Ws + t) * D + d;
+    if (in_bounds(ctl, src, sizeof(TI)) && in_bounds(ctl, dst, sizeof(TO)))
+      store_from_f32(dst, load_f32(src));
   }
 }
 
@@ -228,7 +239,8 @@ template <typename TI>
 __global__ void __launch_bounds__(256) window_mxfp8_kernel(const TI *__restrict__ x, long rows,
                                                            int N, int D, int R, int Ws,
                                                            uint8_t *__restrict__ codes,
-                                                           uint8_t *__restrict__ e8m0) {
+                                                           uint8_t *__restrict__ e8m0,
+                                                           const KernelCtl ctl) {
   wait_prior_grid();
   allow_next_grid();
   const int groups = D / kGroup;
@@ -238,15 +250,18 @@ __global__ void __launch_bounds__(256) window_mxfp8_kernel(const TI *__restrict_
   const long row = task / groups;
   const int j = static_cast<int>(task % groups);
   const long u = row / R, t = row % R;
-  const float val = load_f32(x + (u * N + (N - R) + t) * D + j * kGroup + lane);
+  const TI *src = x + (u * N + (N - R) + t) * D + j * kGroup + lane;
+  const float val = in_bounds(ctl, src, sizeof(TI)) ? load_f32(src) : 0.0f;
   const int e = mxfp8_block_exp(warp_max(fabsf(val)));
   const long dst = u * Ws + t;
-  codes[dst * D + j * kGroup + lane] = mxfp8_code(val, pow2_of(-e));
-  if (lane == 0) e8m0[dst * groups + j] = static_cast<uint8_t>(e + 127);
+  if (in_bounds(ctl, codes + dst * D + j * kGroup + lane, 1))
+    codes[dst * D + j * kGroup + lane] = mxfp8_code(val, pow2_of(-e));
+  if (lane == 0 && in_bounds(ctl, e8m0 + dst * groups + j, 1))
+    e8m0[dst * groups + j] = static_cast<uint8_t>(e + 127);
 }
 
 template <typename T>
-int pack_typed(const T *k, const T *v, const kvq_cache &c, cudaStream_t s) {
+int pack_typed(const T *k, const T *v, const kvq_cache &c, const KernelCtl &ctl, cudaStream_t s) {
   const CacheDims d = dims_of(c);
   const long units = static_cast<long>(d.B) * d.Hkv;
   int launches = 0;
@@ -255,13 +270,13 @@ int pack_typed(const T *k, const T *v, const kvq_cache &c, cudaStream_t s) {
       for (long u0 = 0; u0 < units; u0 += 65535) {  // grid.y holds at most 65,535 units
         const unsigned nu = static_cast<unsigned>(std::min<long>(65535, units - u0));
         launch_dependent(pack_k128_kernel<T>, dim3(d.Gk, nu), dim3(256), 0, s, k, d.N, d.cut, d.Gs,
-                         u0, c.k_codes, c.k_scales);
+                         u0, c.k_codes, c.k_scales, ctl);
         ++launches;
       }
     } else {
       const long ktasks = units * d.Gk * (d.D / 2);
       const unsigned kblocks = static_cast<unsigned>((ktasks + 255) / 256);
-      launch_dependent(pack_k_kernel<T>, dim3(kblocks), dim3(256), 0, s, k, ktasks, d.N, d.D, d.cut, d.Gk, d.Gs, c.k_codes, c.k_scales);
+      launch_dependent(pack_k_kernel<T>, dim3(kblocks), dim3(256), 0, s, k, ktasks, d.N, d.D, d.cut, d.Gk, d.Gs, c.k_codes, c.k_scales, ctl);
       ++launches;
     }
     // V: per launch at most 65,535 units (grid.y) and 2^24 tokens of each,
@@ -273,7 +288,8 @@ int pack_typed(const T *k, const T *v, const kvq_cache &c, cudaStream_t s) {
         const int nt = std::min(kSlice, d.cut - t0);
         const long vthreads = static_cast<long>(nt) * (d.D / kGroup);
         launch_dependent(pack_v_kernel<T>, dim3(static_cast<unsigned>((vthreads + 255) / 256), nu),
-                         dim3(256), 0, s, v, u0, t0, nt, d.N, d.D, d.Vs, c.v_codes, c.v_scales);
+                         dim3(256), 0, s, v, u0, t0, nt, d.N, d.D, d.Vs, c.v_codes, c.v_scales,
+                         ctl);
         ++launches;
       }
     }
@@ -286,20 +302,20 @@ int pack_typed(const T *k, const T *v, const kvq_cache &c, cudaStream_t s) {
       const long tasks = rows * (d.D / kGroup);
       launch_dependent(window_mxfp8_kernel<T>, dim3(static_cast<unsigned>((tasks + 7) / 8)),
                        dim3(256), 0, s, k, rows, d.N, d.D, d.R, d.Ws,
-                       static_cast<uint8_t *>(c.k_window), c.k_window_e8m0);
+                       static_cast<uint8_t *>(c.k_window), c.k_window_e8m0, ctl);
     } else if (c.kwin_dtype == KVQ_F32) {
       launch_dependent(window_copy_kernel<T, float>, dim3(blocks), dim3(256), 0, s, k, rows, d.N,
-                       d.D, d.R, d.Ws, static_cast<float *>(c.k_window));
+                       d.D, d.R, d.Ws, static_cast<float *>(c.k_window), ctl);
     } else {
       launch_dependent(window_copy_kernel<T, __nv_bfloat16>, dim3(blocks), dim3(256), 0, s,
-          k, rows, d.N, d.D, d.R, d.Ws, static_cast<__nv_bfloat16 *>(c.k_window));
+          k, rows, d.N, d.D, d.R, d.Ws, static_cast<__nv_bfloat16 *>(c.k_window), ctl);
     }
     if (c.vwin_dtype == KVQ_F32) {
       launch_dependent(window_copy_kernel<T, float>, dim3(blocks), dim3(256), 0, s, v, rows, d.N,
-                       d.D, d.R, d.Ws, static_cast<float *>(c.v_window));
+                       d.D, d.R, d.Ws, static_cast<float *>(c.v_window), ctl);
     } else {
       launch_dependent(window_copy_kernel<T, __nv_bfloat16>, dim3(blocks), dim3(256), 0, s,
-          v, rows, d.N, d.D, d.R, d.Ws, static_cast<__nv_bfloat16 *>(c.v_window));
+          v, rows, d.N, d.D, d.R, d.Ws, static_cast<__nv_bfloat16 *>(c.v_window), ctl);
     }
     launches += 2;
   }
@@ -321,6 +337,7 @@ struct AppendArgs {
   float *v_scales;
   void *k_window, *v_window;
   int D, T, R_old, m, Gk_old, cut_old, Gs, Vs, Ws;
+  KernelCtl ctl;
 };
 
 // Eight consecutive elements from element e0 of a window or of the new rows,
@@ -363,10 +380,24 @@ __device__ __forceinline__ void store8_as(void *base, long e0, int dt, const flo
 // Elements d0 .. d0 + 7 of token i of the append sequence S.
 __device__ __forceinline__ void seq8(const AppendArgs &a, const void *win, const void *fresh,
                                      int win_dt, long u, int i, int d0, float (&x)[8]) {
-  if (i < a.R_old)
-    load8_as(win, (u * a.Ws + i) * a.D + d0, win_dt, x);
-  else
-    load8_as(fresh, (u * a.T + (i - a.R_old)) * a.D + d0, a.in_dtype, x);
+  // (debug builds: a row outside the call's buffers reads as zeros)
+  if (i < a.R_old) {
+    const long e0 = (u * a.Ws + i) * a.D + d0;
+    const size_t eb = win_dt == KVQ_F32 ? 4 : 2;
+    if (in_bounds(a.ctl, static_cast<const uint8_t *>(win) + e0 * eb, 8 * eb)) {
+      load8_as(win, e0, win_dt, x);
+      return;
+    }
+  } else {
+    const long e0 = (u * a.T + (i - a.R_old)) * a.D + d0;
+    const size_t eb = a.in_dtype == KVQ_F32 ? 4 : 2;
+    if (in_bounds(a.ctl, static_cast<const uint8_t *>(fresh) + e0 * eb, 8 * eb)) {
+      load8_as(fresh, e0, a.in_dtype, x);
+      return;
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < 8; ++e) x[e] = 0.0f;
 }
 
 constexpr int kAppendThreads = 256;
@@ -427,12 +458,13 @@ __global__ void __launch_bounds__(kAppendThreads) append_migrate_kernel(const Ap
     a1 = fmaxf(a1, kmax[r * np + p].y);
   }
   const float s0 = int4_scale(a0), s1 = int4_scale(a1);
-  if (q == 0) {
+  if (q == 0 && in_bounds(a.ctl, a.k_scales + grp * D + 2 * p, 2 * sizeof(float))) {
     a.k_scales[grp * D + 2 * p] = s0;
     a.k_scales[grp * D + 2 * p + 1] = s1;
   }
   for (int t = q * tq; t < q * tq + tq; ++t)
-    a.k_codes[(grp * kGroup + t) * (D / 2) + p] = static_cast<uint8_t>(
+    if (in_bounds(a.ctl, a.k_codes + (grp * kGroup + t) * (D / 2) + p, 1))
+      a.k_codes[(grp * kGroup + t) * (D / 2) + p] = static_cast<uint8_t>(
         (int4_code(xs[t * ld + 2 * p], s0) + 8) | ((int4_code(xs[t * ld + 2 * p + 1], s1) + 8) << 4));
   __syncthreads();
   stage_group(a, a.v_window, a.v_new, a.vwin, u, gi, xs);
@@ -450,9 +482,10 @@ __global__ void __launch_bounds__(kAppendThreads) append_migrate_kernel(const Ap
 #pragma unroll
     for (int e = 0; e < kGroup; ++e)
       w[e >> 3] |= static_cast<uint32_t>(int4_code(x[e], sc) + 8) << (4 * (e & 7));
-    *reinterpret_cast<uint4 *>(a.v_codes + row * (D / 2) + j * (kGroup / 2)) =
-        make_uint4(w[0], w[1], w[2], w[3]);
-    a.v_scales[row * blocks + j] = sc;
+    uint8_t *cd = a.v_codes + row * (D / 2) + j * (kGroup / 2);
+    if (in_bounds(a.ctl, cd, 16)) *reinterpret_cast<uint4 *>(cd) = make_uint4(w[0], w[1], w[2], w[3]);
+    if (in_bounds(a.ctl, a.v_scales + row * blocks + j, sizeof(float)))
+      a.v_scales[row * blocks + j] = sc;
   }
 }
 
@@ -485,8 +518,11 @@ __global__ void __launch_bounds__(kAppendThreads) append_window_kernel(const App
       const int pc = threadIdx.x + k * kAppendThreads;
       if (pc < pieces) {
         const long o = (u * a.Ws + r0 + pc * 8 / D) * D + pc * 8 % D;
-        store8_as(a.k_window, o, a.kwin, kx[k]);
-        store8_as(a.v_window, o, a.vwin, vx[k]);
+        const size_t kb = a.kwin == KVQ_F32 ? 4 : 2, vb = a.vwin == KVQ_F32 ? 4 : 2;
+        if (in_bounds(a.ctl, static_cast<uint8_t *>(a.k_window) + o * kb, 8 * kb))
+          store8_as(a.k_window, o, a.kwin, kx[k]);
+        if (in_bounds(a.ctl, static_cast<uint8_t *>(a.v_window) + o * vb, 8 * vb))
+          store8_as(a.v_window, o, a.vwin, vx[k]);
       }
     }
     __syncthreads();
@@ -496,15 +532,15 @@ __global__ void __launch_bounds__(kAppendThreads) append_window_kernel(const App
 }  // namespace
 
 int launch_pack(const void *k, const void *v, int in_dtype, const kvq_cache &c,
-                const KernelCtl &, cudaStream_t s) {
+                const KernelCtl &ctl, cudaStream_t s) {
   if (in_dtype == KVQ_F32)
-    return pack_typed(static_cast<const float *>(k), static_cast<const float *>(v), c, s);
+    return pack_typed(static_cast<const float *>(k), static_cast<const float *>(v), c, ctl, s);
   return pack_typed(static_cast<const __nv_bfloat16 *>(k), static_cast<const __nv_bfloat16 *>(v),
-                    c, s);
+                    c, ctl, s);
 }
 
 int launch_append(const kvq_cache &c, const void *k_new, const void *v_new, int in_dtype,
-                  int n_new, int m, int R_new, cudaStream_t s) {
+                  int n_new, int m, int R_new, const KernelCtl &ctl, cudaStream_t s) {
   const CacheDims d = dims_of(c);
   const long units = static_cast<long>(d.B) * d.Hkv;
   AppendArgs a;
@@ -528,6 +564,7 @@ int launch_append(const kvq_cache &c, const void *k_new, const void *v_new, int 
   a.Gs = d.Gs;
   a.Vs = d.Vs;
   a.Ws = d.Ws;
+  a.ctl = ctl;
   int launches = 0;
   if (m > 0) {
     const size_t smem = sizeof(float) * kGroup * (d.D + 1);

@@ -26,6 +26,8 @@ STATS = ("entropy", "support", "top1", "top5", "top10", "zero", "p_zero", "p_tv"
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libkvq.so")
+# the same library built with every kernel's access ranges checked (KVQ_DEBUG)
+DEBUG_LIB_PATH = os.path.join(_HERE, "libkvq_debug.so")
 HEADER = os.path.join(os.path.dirname(_HERE), "include", "kvq.h")
 
 
@@ -98,6 +100,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.kvq_last_path.restype = ctypes.c_char_p
     lib.kvq_debug_set.argtypes = [ctypes.c_uint32, i32]
     lib.kvq_debug_set.restype = None
+    lib.kvq_debug_checks.argtypes = []
+    lib.kvq_debug_checks.restype = i32
     _lib = lib
     return lib
 
