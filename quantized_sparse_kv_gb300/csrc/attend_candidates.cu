@@ -1195,13 +1195,11 @@ int launch_candidates_union(const kvq_cache &c, const void *q, const int32_t *id
   a.out_dtype = out_dtype;
   a.ctl = ctl;
   const size_t build_smem = sizeof(BuildSmem);
-  cudaFuncSetAttribute(cand_union_build_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       static_cast<int>(build_smem));
+  opt_in_smem(cand_union_build_kernel, build_smem);
   launch_dependent(cand_union_build_kernel, dim3(p.slices, static_cast<unsigned>(p.units)),
                    dim3(kUBuild), build_smem, s, a);
   const size_t smem = sizeof(UnionSmem);
-  cudaFuncSetAttribute(cand_union_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       static_cast<int>(smem));
+  opt_in_smem(cand_union_kernel, smem);
   launch_dependent(cand_union_kernel, dim3(p.pieces, static_cast<unsigned>(p.units)),
                    dim3(kUThreads), smem, s, a);
   launch_dependent(cand_union_combine_kernel, dim3(static_cast<unsigned>(p.units)), dim3(256), 0,
@@ -1257,8 +1255,7 @@ int launch_attend_candidates(const kvq_cache &c, const void *q, int q_dtype, int
     switch (d.D / 32) {
 #define KVQ_TOPK_CASE(F)                                                                      \
   case F:                                                                                     \
-    cudaFuncSetAttribute(cand_topk_kernel<F>, cudaFuncAttributeMaxDynamicSharedMemorySize,   \
-                         static_cast<int>(smem));                                             \
+    opt_in_smem(cand_topk_kernel<F>, smem);                                             \
     launch_dependent(cand_topk_kernel<F>, grid, dim3(kWarps * 32), smem, s, a);               \
     break;
       KVQ_TOPK_CASE(1)

@@ -1347,8 +1347,7 @@ static int launch_chunk_mxfp8(const kvq_cache &c, const void *q, int Hq, int n_q
   a.k_ws = Ws;
   static_assert(sizeof(ChunkSmem<true>) + 1024 <= 232448, "chunk kernel shared memory");
   const size_t smem = sizeof(ChunkSmem<true>) + 1024;
-  cudaFuncSetAttribute(chunk_mxfp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       static_cast<int>(smem));
+  opt_in_smem(chunk_mxfp8_kernel, smem);
   dim3 grid(q_tiles, static_cast<unsigned>(hq_rows));
   launch_dependent(chunk_mxfp8_kernel, grid, dim3(384), smem, s, tq, tk, tv, a);
   return 2;
@@ -1434,8 +1433,7 @@ int launch_attend_chunk(const kvq_cache &c, const void *q, int Hq, int n_q, floa
   a.k_ws = 0;
   static_assert(sizeof(ChunkSmem<false>) + 1024 <= 232448, "chunk kernel shared memory");
   const size_t smem = sizeof(ChunkSmem<false>) + 1024;
-  cudaFuncSetAttribute(chunk_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       static_cast<int>(smem));
+  opt_in_smem(chunk_bf16_kernel, smem);
   dim3 grid((n_q + kBM - 1) / kBM, c.batch * Hq);
   launch_dependent(chunk_bf16_kernel, grid, dim3(384), smem, s, tq, tk, tv, tkw, tvw, a);
   return launches;
@@ -1512,8 +1510,7 @@ int launch_candidate_lists(const kvq_cache &c, const void *q, int Hq, int n_q,
   a.k_e8m0 = nullptr;
   a.k_ws = 0;
   const size_t smem = sizeof(ChunkSmem<false>) + 1024;
-  cudaFuncSetAttribute(chunk_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       static_cast<int>(smem));
+  opt_in_smem(chunk_bf16_kernel, smem);
   dim3 grid((n_q + kBM - 1) / kBM, d.B * Hq);
   launch_dependent(chunk_bf16_kernel, grid, dim3(384), smem, s, tq, tk, tv, tkw, tvw, a);
   return 2;
@@ -1598,8 +1595,7 @@ int launch_region_drop(const kvq_cache &c, const void *q, int Hq, int n_q, const
   a.k_e8m0 = nullptr;
   a.k_ws = 0;
   const size_t smem = sizeof(ChunkSmem<false>) + 1024;
-  cudaFuncSetAttribute(chunk_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       static_cast<int>(smem));
+  opt_in_smem(chunk_bf16_kernel, smem);
   dim3 grid((n_q + kBM - 1) / kBM, d.B * Hq);
   launch_dependent(chunk_bf16_kernel, grid, dim3(384), smem, s, tq, tk, tv, tkw, tvw, a);
   return 2;

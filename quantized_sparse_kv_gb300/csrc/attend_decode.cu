@@ -779,8 +779,7 @@ int launch_attend_decode(const kvq_cache &c, const void *q, int q_dtype, float s
   a.partials = static_cast<float *>(ws);
   a.ctl = ctl;
   const size_t smem = sizeof(DecodeSmem);
-  cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       static_cast<int>(smem));
+  opt_in_smem(decode_kernel, smem);
   // The combine grid's blocks may be placed while the decode grid drains; they
   // wait for it on the device.
   launch_dependent(decode_kernel, dim3(p.num_ctas), dim3(kThreads), smem, s, a);

@@ -402,8 +402,7 @@ void launch_dpl(const GenericArgs &a, int B, cudaStream_t s) {
   constexpr int D = DPL * 32;
   const size_t smem = sizeof(float) * (kTileKeys * (D + 1) + kTileKeys * D + kRowsPerCta * D +
                                        kRowsPerCta * kTileKeys);
-  cudaFuncSetAttribute(generic_attend_kernel<DPL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       static_cast<int>(smem));
+  opt_in_smem(generic_attend_kernel<DPL>, smem);
   dim3 grid((a.n_q + kRowsPerCta - 1) / kRowsPerCta, a.Hq, B);
   launch_dependent(generic_attend_kernel<DPL>, grid, dim3(kWarps * 32), smem, s, a);
 }

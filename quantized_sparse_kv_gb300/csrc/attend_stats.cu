@@ -594,8 +594,7 @@ int launch_attend_stats(const kvq_cache &c, const void *q, int q_dtype, int Hq, 
   switch (d.D / 32) {
 #define KVQ_STATS_CASE(E)                                                                     \
   case E:                                                                                     \
-    cudaFuncSetAttribute(keys_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize,        \
-                         static_cast<int>(ksmem));                                            \
+    opt_in_smem(keys_kernel<E>, ksmem);                                            \
     launch_dependent(keys_kernel<E>, kgrid, dim3(kThreads), ksmem, s, a);                     \
     launch_dependent(scores_kernel<E>, sgrid, dim3(kThreads), 0, s, a);                       \
     break;
@@ -607,8 +606,7 @@ int launch_attend_stats(const kvq_cache &c, const void *q, int q_dtype, int Hq, 
     default:
       return -1;
   }
-  cudaFuncSetAttribute(stats_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       static_cast<int>(smem));
+  opt_in_smem(stats_kernel, smem);
   launch_dependent(stats_kernel, dim3(static_cast<unsigned>(rows)), dim3(kThreads), smem, s, a);
   return 3;
 }

@@ -8,6 +8,10 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+#include <tuple>
+#include <vector>
+
 #include "../../include/kvq.h"
 
 namespace kvq {
@@ -314,6 +318,25 @@ __device__ __forceinline__ float e4m3_value(uint8_t c) {
 __device__ __forceinline__ float mxfp8_round_warp(float x) {
   const int e = mxfp8_block_exp(warp_max(fabsf(x)));
   return __fmul_rn(e4m3_value(mxfp8_code(x, pow2_of(-e))), pow2_of(e));
+}
+
+// Let `kernel` take `bytes` of dynamic shared memory on the current device.
+// The attribute is set once per (kernel, device) and size, so a call that
+// launches the kernel again costs a lookup, not a driver call.
+template <typename Kernel>
+inline cudaError_t opt_in_smem(Kernel *kernel, size_t bytes) {
+  static std::mutex mu;
+  static std::vector<std::tuple<const void *, int, size_t>> done;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+  const void *fn = reinterpret_cast<const void *>(kernel);
+  std::lock_guard<std::mutex> lock(mu);
+  for (const auto &d : done)
+    if (std::get<0>(d) == fn && std::get<1>(d) == dev && std::get<2>(d) >= bytes) return cudaSuccess;
+  const cudaError_t r = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(bytes));
+  if (r == cudaSuccess) done.emplace_back(fn, dev, bytes);
+  return r;
 }
 
 }  // namespace kvq
