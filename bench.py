@@ -394,8 +394,9 @@ def row_chunk(kvq, synth, torch, steps, warmup, pk, kwin, bounds=None):
             "ms": ms, "keys_per_s": keys / (ms * 1e-3), "path": a.path, "l2": l2_note(n, touched),
             "roofline": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s",
                          "frac": tf / peak,
-                         "traffic": (profile_traffic("chunk_bf16_kernel_H32_Q2340_K6240.md")
-                                     if kwin == "bf16" else None),
+                         "traffic": {"bf16": profile_traffic("chunk_bf16_kernel_H32_Q2340_K6240.md"),
+                                     "mxfp8": profile_traffic("chunk_mxfp8_kernel_H32_Q2340_K6240.md"),
+                                     }.get(kwin),
                          "frac_of_bf16_peak": tf / pk["bf16_tflops"],
                          "peak_note": {"bf16": "bf16 measured",
                                        "mxfp8": "half fp8 / half bf16 flops: "
