@@ -579,3 +579,18 @@ def test_full_output_is_the_mass_weighted_mix_of_region_outputs():
     assert np.all(rel == 0) and np.allclose(cos, 1)
     rel, cos = O.output_change(-o, o)
     assert np.allclose(rel, 2) and np.allclose(cos, -1)
+
+
+def test_rel_l2_closed_forms():
+    # ||a - b|| / ||b|| over the whole array: a 3-4-5 triangle gives exact
+    # values, the reference is the second argument, scaling both leaves it
+    # unchanged, and a flattening or per-row mean would give other numbers
+    ref = np.array([[3.0, 4.0], [0.0, 0.0]])
+    assert O.rel_l2(ref, ref) == 0.0
+    assert O.rel_l2(ref + np.array([[0.0, 1.0], [0.0, 0.0]]), ref) == pytest.approx(0.2, abs=0)
+    assert O.rel_l2(np.zeros_like(ref), ref) == 1.0
+    assert O.rel_l2(2.0 * ref, ref) == 1.0
+    assert O.rel_l2(ref, 2.0 * ref) == 0.5           # the second argument is the reference
+    got = ref + np.array([[0.0, 0.0], [3.0, 4.0]])   # the error sits in the zero row
+    assert O.rel_l2(got, ref) == 1.0
+    assert O.rel_l2(7.0 * got, 7.0 * ref) == pytest.approx(1.0, rel=1e-15)
