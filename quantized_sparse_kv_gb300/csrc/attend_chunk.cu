@@ -6,11 +6,18 @@
 // chunk of 2,340 queries (6 latent frames) over 6,240 keys laid out [sink 1560
 // | recent 2340 | current 2340] (section "KV Cache 的实际作用"), no mask.
 //
+// Variants of the same kernel body: bf16 Q/K over 128-key tiles (an
+// all-window cache; an int4-history cache, whose history tiles are first
+// expanded to bf16 in workspace; block-shared candidate lists gathered to
+// bf16), and MXFP8 Q/K over 112-key tiles (QK^T as a block-scaled MMA).
+//
 // One CTA per (128 query rows, query head); 12 warps:
-//   warp 0      TMA producer: Q once, then 128-key K tiles (one slot: K is
-//               free once its QK MMA ends) and V tiles (two slots), all
+//   warp 0      TMA producer: Q once, then the K tiles (a ring of two stages,
+//               three with MXFP8; a stage is refilled once its QK MMA ends),
 //               128B-swizzled in 64-feature boxes;
 //   warp 1      allocates 512 TMEM columns and one lane issues the MMAs;
+//   warp 2      TMA producer: the V tiles (the same ring sizes; a stage is
+//               refilled once its PV MMA ends);
 //   warps 4-7   softmax group A: key tiles 0, 2, 4, ...
 //   warps 8-11  softmax group B: key tiles 1, 3, 5, ...
 // Each softmax group g owns TMEM S_g (128 columns) and O_g (128 columns) and
