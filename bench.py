@@ -880,7 +880,9 @@ def run_kvq(args):
         "metric": "attended keys/s (GQA decode over int4 KV cache)",
         "value": value, "unit": "keys/s", "n_gpus": world, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": ms_max, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "int4 KV, bf16 Q/window, f16/f32 MMA",
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "dtype_note": "int4 KV codes and bf16 Q/window in; the MMAs take f16 operands (bf16 "
+                      "for the window tiles) and accumulate in f32",
         "data": "synthetic N(0,1) bf16 Q/K/V, seeded",
         "config": {"workload": f"decode: B={d['batch']} sequences, 16 query heads over 2 KV heads, "
                                "D=128, L=32768, last R=128 tokens bf16, int4 groups of 32",
