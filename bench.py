@@ -762,6 +762,17 @@ def max_over_ranks(x, world):
     return float(t.item())
 
 
+def decode_config(world):
+    """The headline workload, as both arms report it."""
+    d = DECODE
+    nbytes = decode_bytes(d["batch"], d["kv_heads"], d["context"], d["recent"])
+    return {"workload": f"decode: B={d['batch']} sequences, 16 query heads over 2 KV heads, "
+                        "D=128, L=32768, last R=128 tokens bf16, int4 groups of 32",
+            "batch": d["batch"], "context": d["context"], "recent": d["recent"],
+            "l2": f"inputs larger than L2 ({nbytes / 1e6:.0f} MB per step), no flush",
+            "parallelism": f"replicas x{world}, each its own batch"}
+
+
 def run_reference(args):
     world, rank, _ = dist_setup()
     if rank != 0:
@@ -785,7 +796,7 @@ def run_reference(args):
             "ms_per_step": 1e3 * wall / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic N(0,1), bf16-rounded",
             "impl": "reference",
-            "config": {"workload": "decode B=64 Hq=16 Hkv=2 D=128 L=32768 R=128 (sampled units)"},
+            "config": decode_config(world),
             "cpu_baseline": {"value": value, "unit": "keys/s", "cores": workers, "kind": "oracle",
                              "sample": sample, "cpu_model": cpu_model()},
             "e2e": {"value": value, "unit": "keys/s", "h2d_bytes_per_step": 0,
@@ -884,11 +895,7 @@ def run_kvq(args):
         "dtype_note": "int4 KV codes and bf16 Q/window in; the MMAs take f16 operands (bf16 "
                       "for the window tiles) and accumulate in f32",
         "data": "synthetic N(0,1) bf16 Q/K/V, seeded",
-        "config": {"workload": f"decode: B={d['batch']} sequences, 16 query heads over 2 KV heads, "
-                               "D=128, L=32768, last R=128 tokens bf16, int4 groups of 32",
-                   "batch": d["batch"], "context": d["context"], "recent": d["recent"],
-                   "l2": f"inputs larger than L2 ({nbytes / 1e6:.0f} MB per step), no flush",
-                   "parallelism": f"replicas x{world}, each its own batch"},
+        "config": decode_config(world),
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
                      "frac": gbs / pk["hbm_gbs"],
                      "traffic": (profile_traffic("decode_kernel_B16_L32768.md")
