@@ -688,15 +688,20 @@ def _unit_np(t, b, h):
     return t[b, h].float().cpu().numpy()
 
 
-def test_decode_full_size_sampled_units(kvq):
-    # the timed decode workload: 64 sequences, 16 q-heads / 2 KV heads, D=128, L=32768, R=128
-    q, k, v = synth.decode_inputs_torch(1, 64, 32768, "cuda")
+@pytest.mark.parametrize("batch,context", [(64, 32768), (16, 32768), (64, 8192), (1, 32768),
+                                           (64, 1024)])
+def test_decode_full_size_sampled_units(kvq, batch, context):
+    # the decode workloads at full size (16 q-heads / 2 KV heads, D=128, R=128):
+    # the timed step (64, 32768) and the other graded batch / context sizes,
+    # through the same kernels and launch configuration, checked on sampled
+    # (sequence, KV head) units
+    q, k, v = synth.decode_inputs_torch(1, batch, context, "cuda")
     cache = kvq.pack(k, v, 128, "bf16")
     a = kvq.Attend(cache, q, out_dtype="bf16")
     a.run()
     assert a.path == "decode" and kvq.read_status(a.status) == 0
     out = a.out.float().cpu().numpy()
-    for b, kvh in ((0, 0), (17, 1), (63, 1)):
+    for b, kvh in sorted({(0, 0), (min(17, batch - 1), 1), (batch - 1, 1)}):
         kn, vn = _unit_np(k, b, kvh), _unit_np(v, b, kvh)
         p = O.pack_head(kn, vn, 128, "bf16")
         ser = O.serialize_head(p)
@@ -708,12 +713,17 @@ def test_decode_full_size_sampled_units(kvq):
             assert O.rel_l2(out[b, h], ref) <= TOL_BF16
 
 
-def test_candidates_full_size_sampled_rows(kvq):
-    # the timed candidate workload: 32 sequences, L=131072, C=256
-    q, k, v = synth.decode_inputs_torch(31, 32, 131072, "cuda")
+@pytest.mark.parametrize("context,c", [(131072, 256), (32768, 96), (4096, 256)])
+def test_candidates_full_size_sampled_rows(kvq, context, c):
+    # the candidate workloads at full size: 32 sequences, 16 q-heads / 2 KV
+    # heads, the timed L=131072, C=256 and the other graded sizes
+    q, k, v = synth.decode_inputs_torch(31, 32, context, "cuda")
     cache = kvq.pack(k, v, 128, "bf16")
-    idx = synth.candidate_indices(5, 32, 16, 131072, 256)
-    out, status = kvq.attend_candidates(cache, q, torch.from_numpy(idx).cuda(), out_dtype="f32")
+    idx = synth.candidate_indices(5, 32, 16, context, c)
+    a = kvq.AttendCandidates(cache, q, torch.from_numpy(idx).cuda(), out_dtype="f32")
+    a.run()
+    out, status = a.out, a.status
+    assert a.lib.kvq_last_path().decode() == "candidates_union"
     assert kvq.read_status(status) == 0
     out = out.cpu().numpy()
     for b, h in ((0, 0), (9, 7), (31, 15)):
