@@ -3,11 +3,11 @@
 python tests/debug_build_cases.py LIB OUT.npz
 
 Loads LIB (libkvq.so or libkvq_debug.so), runs small seeded cases of pack,
-append, decode, the fp32 kernels, chunk attention (bf16, MXFP8, int4
-history, with region masses), candidate attention (union, per row, top-k,
-block lists), region drop and the observer statistics, and saves every output
-(as raw bytes) and every status word. test_debug_build compares the files of
-the two builds.
+append, decode (with a workspace and with the library-owned scratch), the
+fp32 kernels, chunk attention (bf16, MXFP8, int4 history, with region
+masses), candidate attention (union, per row, top-k, block lists), region
+drop and the observer statistics, and saves every output (as raw bytes) and
+every status word. test_debug_build compares the files of the two builds.
 """
 import os
 import sys
@@ -65,6 +65,20 @@ def main(lib_path: str, out_path: str) -> None:
     assert a.path == "decode", a.path
     keep("decode_out", a.out)
     status("decode", a.status)
+    # the same decode with the library-owned scratch (kv_attend_decode_static)
+    import ctypes
+    fn = lib.kv_attend_decode_static
+    fn.argtypes = [ctypes.POINTER(kvq.KvqCacheStruct), ctypes.c_void_p, ctypes.c_int32,
+                   ctypes.c_int32, ctypes.c_float, ctypes.c_void_p, ctypes.c_int32,
+                   ctypes.c_void_p, ctypes.c_void_p]
+    fn.restype = ctypes.c_int32
+    out_s = torch.empty_like(a.out)
+    s = kvq.new_status()
+    rc = fn(cd.ref, qd.data_ptr(), kvq.BF16, 16, 0.0, out_s.data_ptr(), kvq.F32, s.data_ptr(),
+            ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert rc == 0, rc
+    keep("decode_static_out", out_s)
+    status("decode_static", s)
     idx = torch.from_numpy(synth.candidate_indices(0, 2, 16, 600, 96)).to(dev)
     out, s = kvq.attend_candidates(cd, qd, idx, out_dtype="f32")
     keep("cand_union_out", out)
