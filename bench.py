@@ -337,8 +337,9 @@ def row_pack(kvq, synth, torch, steps, warmup, pk):
     return {"workload": "kv_pack int4 K/V, 64 x 2 KV heads x 32768 tokens x 128, bf16 in, R=128",
             "ms": ms, "tokens_per_s": tokens / (ms * 1e-3),
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                         "frac": gbs / pk["hbm_gbs"], "traffic": None},
-            "launches": 4}
+                         "frac": gbs / pk["hbm_gbs"],
+                         "traffic": profile_traffic("pack_kv128_bf16_kernel_B64_L32768.md")},
+            "launches": 3}
 
 
 def row_small(kvq, synth, torch, steps, warmup, pk):

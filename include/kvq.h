@@ -379,8 +379,9 @@ KVQ_API const char *kvq_last_path(void);
 /*
  * Test hook: bound every mbarrier wait of the next launches on this thread to
  * `wait_limit_ns` nanoseconds (0 restores the default of one second), and,
- * when drop_item >= 0, make the decode kernel's loader skip the copy of that
- * work item so that the wait on it can only run out. Used by the failure tests.
+ * when drop_item >= 0, make the loader of the decode kernel and of the bf16
+ * kv_pack kernel skip the copy of that work item so that the wait on it can
+ * only run out. Used by the failure tests.
  */
 KVQ_API void kvq_debug_set(uint32_t wait_limit_ns, int32_t drop_item);
 

@@ -217,7 +217,7 @@ kvq_status kv_pack(const void *k, const void *v, int32_t in_dtype, kvq_cache *ca
   const long units = static_cast<long>(cache->batch) * cache->kv_heads;
   ctl_add(ctl, k, rows_bytes(units * cache->n_tokens, cache->head_dim, in_dtype));
   ctl_add(ctl, v, rows_bytes(units * cache->n_tokens, cache->head_dim, in_dtype));
-  const int n = kvq::launch_pack(k, v, in_dtype, *cache, ctl,
+  const int n = kvq::launch_pack(k, v, in_dtype, *cache, ctl, sm_count(),
                                  reinterpret_cast<cudaStream_t>(stream));
   return finish(n, "pack");
 }

@@ -51,7 +51,7 @@ inline Regions make_regions(const int32_t *bounds, int n) {
 
 // pack.cu
 int launch_pack(const void *k, const void *v, int in_dtype, const kvq_cache &c,
-                const KernelCtl &ctl, cudaStream_t s);
+                const KernelCtl &ctl, int num_sms, cudaStream_t s);
 
 // pack.cu: kv_append on a cache with reserved room: n_new tokens per
 // (sequence, head) after the current ones; m groups of the oldest window

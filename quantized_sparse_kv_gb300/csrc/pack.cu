@@ -12,6 +12,7 @@
 
 #include <algorithm>
 
+#include "int4_round.cuh"
 #include "kvq_internal.h"
 
 namespace kvq {
@@ -213,6 +214,275 @@ __global__ void __launch_bounds__(256) pack_v_kernel(const T *__restrict__ v, lo
   if (in_bounds(ctl, v_scales + row * groups + j, sizeof(float))) v_scales[row * groups + j] = s;
 }
 
+// ------------------------------------------------------------------ bf16, D = 128
+// The int4 part of a bf16 cache with D = 128 in one persistent kernel. A work
+// item is one 32-token group of one (sequence, head): its K rows and its V
+// rows are two contiguous 8 KB tiles. One loader lane streams both tiles of
+// each item into a ring of shared-memory stages with 1-D bulk copies; warps
+// 0-3 quantize the K tile (warp w: tokens 8w..8w+7, lane l: channels
+// 4l..4l+3, so each shared-memory load of a warp is one whole row; the four
+// warps' per-channel maxima meet in shared memory behind an mbarrier) and
+// warps 4-7 the V tile (lane: one token and one 32-feature group).
+//
+// Same codes and scales as the kernels above, without a division per
+// element (int4_round.cuh: a reciprocal and one correction step, exact on
+// bf16 inputs for the groups recip_ok admits); other groups take the
+// division.
+constexpr int kPkStages = 6;
+constexpr int kPkTile = kGroup * 128 * 2;  // bytes of one tile: 32 rows of 128 bf16
+constexpr int kPkWorkers = 8;              // warps 0-3 K, 4-7 V; warp 8 loads
+constexpr int kPkThreads = 32 * (kPkWorkers + 1);
+constexpr int kPkCtasPerSm = 2;
+
+struct PackSmem {
+  uint8_t k[kPkStages][kPkTile];
+  uint8_t v[kPkStages][kPkTile];
+  uint64_t full[kPkStages], empty[kPkStages];
+  int abort_flag;
+};
+
+__device__ __forceinline__ uint32_t max_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// One code byte by the division (the groups recip_ok leaves out).
+__device__ __forceinline__ uint32_t code_byte_div(uint32_t w, float s_lo, float s_hi) {
+  return static_cast<uint32_t>(int4_code(bf_hi(w), s_hi) + 8) * 16u +
+         static_cast<uint32_t>(int4_code(bf_lo(w), s_lo) + 8);
+}
+
+// The division path of one K lane (out of line, reading its column of the
+// tile again: rare).
+__device__ __noinline__ void pack_k_quarter_div(const uint8_t *src, int h, int valid, float a0,
+                                                float a1, float *scales, uint8_t *dst,
+                                                const KernelCtl ctl) {
+  const float s0 = int4_scale(a0), s1 = int4_scale(a1);
+  if (h == 0 && in_bounds(ctl, scales, 2 * sizeof(float)))
+    *reinterpret_cast<float2 *>(scales) = make_float2(s0, s1);
+#pragma unroll 1
+  for (int i = 0; i < 16; ++i) {
+    const uint32_t x = 16 * h + i < valid ? *reinterpret_cast<const uint32_t *>(src + i * 256) : 0u;
+    if (in_bounds(ctl, dst + i * 64, 1)) dst[i * 64] = static_cast<uint8_t>(code_byte_div(x, s0, s1));
+  }
+}
+
+// K warp kw of one item: channels 32kw..32kw+31 of the tile. Lane (w, h) =
+// (lane % 16, lane / 16) holds the channel pair 32kw + 2w, +1 of rows
+// 16h..16h+15 in registers; one lane exchange joins the two halves' maxima.
+template <bool kRagged>
+__device__ __forceinline__ void pack_k_quarter(const uint8_t *tile, int kw, int lane, int valid,
+                                               long ug, uint8_t *__restrict__ k_codes,
+                                               float *__restrict__ k_scales,
+                                               const KernelCtl &ctl) {
+  const int w = lane & 15, h = lane >> 4;
+  const uint8_t *src = tile + 16 * h * 256 + 64 * kw + 4 * w;
+  uint32_t x[16];
+  uint32_t m = 0u;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    x[i] = *reinterpret_cast<const uint32_t *>(src + i * 256);
+    if (kRagged && 16 * h + i >= valid) x[i] = 0u;  // rows past the cut
+    m = max_bf16x2(m, x[i] & 0x7fff7fffu);
+  }
+  m = max_bf16x2(m, __shfl_xor_sync(~0u, m, 16));
+  const float a0 = bf_lo(m), a1 = bf_hi(m);
+  float *scales = k_scales + ug * 128 + 32 * kw + 2 * w;
+  uint8_t *dst = k_codes + (ug * kGroup + 16 * h) * 64 + 16 * kw + w;
+  if (!(recip_ok(a0) && recip_ok(a1))) {
+    pack_k_quarter_div(src, h, valid, a0, a1, scales, dst, ctl);
+    return;
+  }
+  const float s0 = scale_recip(a0), s1 = scale_recip(a1);
+  const float r0 = recip_of(s0), r1 = recip_of(s1);
+  if (h == 0 && in_bounds(ctl, scales, 2 * sizeof(float)))
+    *reinterpret_cast<float2 *>(scales) = make_float2(s0, s1);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const uint32_t b = code_byte_recip(x[i], -s0, -s1, r0, r1);
+    if (in_bounds(ctl, dst + i * 64, 1)) dst[i * 64] = static_cast<uint8_t>(b);
+  }
+}
+
+// One V lane's group by the division (out of line, reading its 64 bytes of
+// shared memory again: rare).
+__device__ __noinline__ void pack_v_group_div(const uint8_t *src, float amax, bool store,
+                                              uint8_t *dst, float *scale, const KernelCtl ctl) {
+  const float s = int4_scale(amax);
+  uint32_t o[4];
+#pragma unroll 1
+  for (int i = 0; i < 4; ++i) {
+    const uint4 w = *reinterpret_cast<const uint4 *>(src + 16 * i);
+    const uint32_t e[4] = {w.x, w.y, w.z, w.w};
+    uint32_t b[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) b[q] = code_byte_div(e[q], s, s);
+    o[i] = __byte_perm(__byte_perm(b[0], b[1], 0x0040), __byte_perm(b[2], b[3], 0x0040), 0x5410);
+  }
+  if (!store) return;
+  if (in_bounds(ctl, dst, 16)) *reinterpret_cast<uint4 *>(dst) = make_uint4(o[0], o[1], o[2], o[3]);
+  if (in_bounds(ctl, scale, sizeof(float))) *scale = s;
+}
+
+// V warp vw of one item: lane (token 8 vw + lane / 4, feature group lane % 4).
+// Its four 16-byte loads are taken in a rotated order so that the eight lanes
+// of each shared-memory phase hit eight different bank quads.
+__device__ __forceinline__ void pack_v_tile(const uint8_t *tile, int vw, int lane, int valid,
+                                            long row0, uint8_t *__restrict__ v_codes,
+                                            float *__restrict__ v_scales, const KernelCtl &ctl) {
+  const int t = 8 * vw + (lane >> 2), j = lane & 3;
+  const int rot = ((j >> 1) + 2 * (t & 1)) & 3;
+  const uint8_t *src = tile + t * 256 + 64 * j;
+  uint4 w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) w[i] = *reinterpret_cast<const uint4 *>(src + 16 * ((i + rot) & 3));
+  uint32_t m[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    m[i] = max_bf16x2(max_bf16x2(w[i].x & 0x7fff7fffu, w[i].y & 0x7fff7fffu),
+                      max_bf16x2(w[i].z & 0x7fff7fffu, w[i].w & 0x7fff7fffu));
+  const uint32_t mm = max_bf16x2(max_bf16x2(m[0], m[1]), max_bf16x2(m[2], m[3]));
+  const float amax = fmaxf(bf_lo(mm), bf_hi(mm));
+  const long row = row0 + t;
+  uint8_t *dst = v_codes + row * 64 + 16 * j;
+  float *scale = v_scales + row * 4 + j;
+  if (!recip_ok(amax)) {
+    pack_v_group_div(src, amax, t < valid, dst, scale, ctl);
+    return;
+  }
+  const float s = scale_recip(amax), r = recip_of(s);
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t e[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
+    uint32_t b[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) b[q] = code_byte_recip(e[q], -s, -s, r, r);
+    o[i] = __byte_perm(__byte_perm(b[0], b[1], 0x0040), __byte_perm(b[2], b[3], 0x0040), 0x5410);
+  }
+  // o[i] holds 16-byte piece (i + rot) & 3: rotate back by rot
+  uint32_t p[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) p[c] = (rot & 1) ? o[(c + 3) & 3] : o[c];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) o[c] = (rot & 2) ? p[(c + 2) & 3] : p[c];
+  if (t >= valid) return;  // rows past the cut belong to the window
+  if (in_bounds(ctl, dst, 16)) *reinterpret_cast<uint4 *>(dst) = make_uint4(o[0], o[1], o[2], o[3]);
+  if (in_bounds(ctl, scale, sizeof(float))) *scale = s;
+}
+
+// The items of a CTA: it = blockIdx.x + n * gridDim.x, as (unit u, group g)
+// advanced without a division (du, dg: gridDim.x = du * Gk + dg).
+struct ItemWalk {
+  int u, g;
+  __device__ __forceinline__ void start(int Gk) {
+    u = static_cast<int>(blockIdx.x) / Gk;
+    g = static_cast<int>(blockIdx.x) - u * Gk;
+  }
+  __device__ __forceinline__ void next(int Gk, int du, int dg) {
+    u += du;
+    g += dg;
+    if (g >= Gk) {
+      g -= Gk;
+      ++u;
+    }
+  }
+};
+
+// Every worker warp takes part in every item of the CTA, in order (so each
+// waits on each phase of a stage's barrier and none can run a phase ahead):
+// K warp w a quarter of the channels of the K tile, V warp w a quarter of
+// the rows of the V tile; a stage is free again after the eight arrivals.
+__global__ void __launch_bounds__(kPkThreads, kPkCtasPerSm)
+    pack_kv128_bf16_kernel(const __nv_bfloat16 *__restrict__ k,
+                           const __nv_bfloat16 *__restrict__ v, int N, int cut, int Gk, int Gs,
+                           int Vs, int items, int du, int dg, uint8_t *__restrict__ k_codes,
+                           float *__restrict__ k_scales, uint8_t *__restrict__ v_codes,
+                           float *__restrict__ v_scales, const KernelCtl ctl) {
+  extern __shared__ __align__(128) uint8_t pk_smem_raw[];
+  PackSmem &sm = *reinterpret_cast<PackSmem *>(pk_smem_raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  allow_next_grid();
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kPkStages; ++s) {
+      mbar_init(smem_u32(&sm.full[s]), 1);
+      mbar_init(smem_u32(&sm.empty[s]), kPkWorkers);
+    }
+    sm.abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  wait_prior_grid();  // the previous kernel may still be reading the cache
+  ItemWalk at;
+  at.start(Gk);
+
+  if (warp == kPkWorkers) {
+    // ---------------- loader
+    if (lane == 0) {
+      int n = 0;
+      for (int it = blockIdx.x; it < items; it += gridDim.x, ++n, at.next(Gk, du, dg)) {
+        const int st = n % kPkStages;
+        if (n >= kPkStages &&
+            !mbar_wait(smem_u32(&sm.empty[st]), static_cast<uint32_t>((n / kPkStages - 1) & 1),
+                       ctl.wait_limit_ns)) {
+          flag_error(ctl, KVQ_DEV_TIMEOUT);
+          *reinterpret_cast<volatile int *>(&sm.abort_flag) = 1;
+          break;
+        }
+        if (*reinterpret_cast<volatile int *>(&sm.abort_flag)) break;
+        if (it == ctl.drop_item) continue;  // test hook: a dropped stage is never filled
+        const uint32_t bytes = static_cast<uint32_t>(min(kGroup, cut - at.g * kGroup)) * 256u;
+        const long e0 = (static_cast<long>(at.u) * N + static_cast<long>(at.g) * kGroup) * 128;
+        const bool ok_k = in_bounds(ctl, k + e0, bytes), ok_v = in_bounds(ctl, v + e0, bytes);
+        mbar_arrive_expect_tx(smem_u32(&sm.full[st]), (ok_k + ok_v) * bytes);
+        if (ok_k) bulk_g2s(smem_u32(sm.k[st]), k + e0, bytes, smem_u32(&sm.full[st]));
+        if (ok_v) bulk_g2s(smem_u32(sm.v[st]), v + e0, bytes, smem_u32(&sm.full[st]));
+      }
+      // drain: copies still in flight must land before the CTA exits
+      for (int d = max(0, n - kPkStages); d < n; ++d) {
+        if (static_cast<long>(blockIdx.x) + static_cast<long>(d) * gridDim.x == ctl.drop_item)
+          continue;
+        mbar_wait(smem_u32(&sm.full[d % kPkStages]), static_cast<uint32_t>((d / kPkStages) & 1),
+                  2000000000ull);
+      }
+    }
+    return;
+  }
+
+  // ---------------- workers (every decision on a wait is taken by the whole warp)
+  const bool is_k = warp < 4;
+  int n = 0;
+  for (int it = blockIdx.x; it < items; it += gridDim.x, ++n, at.next(Gk, du, dg)) {
+    const int st = n % kPkStages;
+    if (__any_sync(~0u, *reinterpret_cast<volatile int *>(&sm.abort_flag) != 0)) break;
+    if (!__all_sync(~0u, mbar_wait(smem_u32(&sm.full[st]),
+                                   static_cast<uint32_t>((n / kPkStages) & 1), ctl.wait_limit_ns))) {
+      if (lane == 0) {
+        flag_error(ctl, KVQ_DEV_TIMEOUT);
+        *reinterpret_cast<volatile int *>(&sm.abort_flag) = 1;
+      }
+      break;
+    }
+    const int valid = min(kGroup, cut - at.g * kGroup);
+    if (is_k) {
+      const long ug = static_cast<long>(at.u) * Gs + at.g;
+      if (valid == kGroup)
+        pack_k_quarter<false>(sm.k[st], warp, lane, valid, ug, k_codes, k_scales, ctl);
+      else
+        pack_k_quarter<true>(sm.k[st], warp, lane, valid, ug, k_codes, k_scales, ctl);
+    } else {
+      pack_v_tile(sm.v[st], warp - 4, lane, valid,
+                  static_cast<long>(at.u) * Vs + static_cast<long>(at.g) * kGroup, v_codes,
+                  v_scales, ctl);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&sm.empty[st]));
+  }
+}
+
 // Window copy with dtype change (fp32 <-> bf16, nearest even).
 // Ws: window rows per (sequence, head) in the arrays.
 template <typename TI, typename TO>
@@ -260,12 +530,39 @@ __global__ void __launch_bounds__(256) window_mxfp8_kernel(const TI *__restrict_
     e8m0[dst * groups + j] = static_cast<uint8_t>(e + 127);
 }
 
+bool aligned16_ptr(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// The fused bf16 kernel for the int4 part, when the cache takes it: D = 128,
+// every array on a 16-byte boundary (the bulk copies and the vector stores).
+bool pack_fused(const __nv_bfloat16 *k, const __nv_bfloat16 *v, const kvq_cache &c,
+                const CacheDims &d, const KernelCtl &ctl, int num_sms, cudaStream_t s) {
+  const long items = static_cast<long>(d.B) * d.Hkv * d.Gk;
+  if (d.D != 128 || items >= (1L << 30) || !aligned16_ptr(k) || !aligned16_ptr(v) ||
+      !aligned16_ptr(c.k_codes) || !aligned16_ptr(c.k_scales) || !aligned16_ptr(c.v_codes) ||
+      !aligned16_ptr(c.v_scales))
+    return false;
+  const size_t smem = sizeof(PackSmem);
+  if (opt_in_smem(pack_kv128_bf16_kernel, smem) != cudaSuccess) return false;
+  const int grid = static_cast<int>(std::min<long>(items, static_cast<long>(kPkCtasPerSm) * num_sms));
+  launch_dependent(pack_kv128_bf16_kernel, dim3(grid), dim3(kPkThreads), smem, s, k, v, d.N, d.cut,
+                   d.Gk, d.Gs, d.Vs, static_cast<int>(items), grid / d.Gk, grid % d.Gk, c.k_codes,
+                   c.k_scales, c.v_codes, c.v_scales, ctl);
+  return true;
+}
+bool pack_fused(const float *, const float *, const kvq_cache &, const CacheDims &,
+                const KernelCtl &, int, cudaStream_t) {
+  return false;
+}
+
 template <typename T>
-int pack_typed(const T *k, const T *v, const kvq_cache &c, const KernelCtl &ctl, cudaStream_t s) {
+int pack_typed(const T *k, const T *v, const kvq_cache &c, const KernelCtl &ctl, int num_sms,
+               cudaStream_t s) {
   const CacheDims d = dims_of(c);
   const long units = static_cast<long>(d.B) * d.Hkv;
   int launches = 0;
-  if (d.cut > 0) {
+  if (d.cut > 0 && pack_fused(k, v, c, d, ctl, num_sms, s)) {
+    ++launches;
+  } else if (d.cut > 0) {
     if (d.D == 128) {
       for (long u0 = 0; u0 < units; u0 += 65535) {  // grid.y holds at most 65,535 units
         const unsigned nu = static_cast<unsigned>(std::min<long>(65535, units - u0));
@@ -532,11 +829,12 @@ __global__ void __launch_bounds__(kAppendThreads) append_window_kernel(const App
 }  // namespace
 
 int launch_pack(const void *k, const void *v, int in_dtype, const kvq_cache &c,
-                const KernelCtl &ctl, cudaStream_t s) {
+                const KernelCtl &ctl, int num_sms, cudaStream_t s) {
   if (in_dtype == KVQ_F32)
-    return pack_typed(static_cast<const float *>(k), static_cast<const float *>(v), c, ctl, s);
+    return pack_typed(static_cast<const float *>(k), static_cast<const float *>(v), c, ctl,
+                      num_sms, s);
   return pack_typed(static_cast<const __nv_bfloat16 *>(k), static_cast<const __nv_bfloat16 *>(v),
-                    c, ctl, s);
+                    c, ctl, num_sms, s);
 }
 
 int launch_append(const kvq_cache &c, const void *k_new, const void *v_new, int in_dtype,

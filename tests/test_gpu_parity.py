@@ -89,6 +89,72 @@ def test_pack_ragged_bf16_bitexact(kvq, shape, recent):
     assert_pack_bitexact(cache, ref)
 
 
+def tie_heavy_bf16(seed, shape, scale=1.0):
+    # normal values rounded to quarters: group maxima are small multiples of
+    # 1/4, so x / scale lands on half-integers often (and a hair off them)
+    return O.round_to_bf16(np.round(synth.normal_numpy(seed, shape) * 4) / 4 * scale)
+
+
+@pytest.mark.parametrize("shape,recent", [((2, 2, 1100, 128), 76), ((1, 3, 333, 128), 0),
+                                          ((3, 1, 40, 128), 8), ((1, 1, 31, 128), 0),
+                                          ((4, 2, 4100, 128), 4), ((4, 2, 16400, 128), 16)])
+@pytest.mark.parametrize("data", ["normal", "ties"])
+def test_pack_bf16_d128_bitexact(kvq, shape, recent, data):
+    # the fused bf16 kernel: whole and ragged last groups, one group, and
+    # 4 x 2 x 512 items, so that each CTA of the grid reuses its ring of
+    # shared-memory stages several times
+    if data == "normal":
+        k = O.round_to_bf16(synth.normal_numpy(30, shape) * 3)
+        v = O.round_to_bf16(synth.normal_numpy(31, shape))
+    else:
+        k, v = tie_heavy_bf16(32, shape), tie_heavy_bf16(33, shape, 2.0 ** -5)
+    cache = kvq.pack(bf16_cuda(k), bf16_cuda(v), recent, "bf16")
+    _, ref = oracle_pack(k, v, recent, "bf16")
+    assert_pack_bitexact(cache, ref)
+
+
+def test_pack_bf16_d128_edge_groups_bitexact(kvq):
+    # groups the reciprocal path leaves to the division (maxima below 2^-100,
+    # subnormal bf16), next to zero groups, exact .5 quotients and the largest
+    # finite bf16 values; one channel of a lane's four on its own
+    k = np.zeros((1, 1, 160, 128), np.float32)
+    k[0, 0, :32, 0] = np.arange(-16, 16) * 0.5
+    k[0, 0, :32, 1] = synth.normal_numpy(40, (32,)) * np.float32(2.0 ** -110)
+    k[0, 0, 32:64, 2] = synth.normal_numpy(41, (32,)) * np.float32(1e-39)   # subnormal
+    k[0, 0, 32:64, 3] = np.float32(3.38e38) * np.linspace(-1, 1, 32, dtype=np.float32)
+    k[0, 0, 64:96, 4:64] = synth.normal_numpy(42, (32, 60)) * np.float32(2.0 ** -99)
+    k[0, 0, 96:128, 64:] = tie_heavy_bf16(43, (32, 64), 2.0 ** -120)
+    k[0, 0, 128:, 5] = np.float32(2.0 ** -100)
+    k[0, 0, 128:, 6] = np.float32(-(2.0 ** -101))
+    k = O.round_to_bf16(k)
+    v = np.ascontiguousarray(np.swapaxes(k[:, :, :128], 2, 3)).repeat(2, axis=2)[:, :, :160]
+    v = O.round_to_bf16(np.ascontiguousarray(v))
+    cache = kvq.pack(bf16_cuda(k), bf16_cuda(v), 0, "bf16")
+    _, ref = oracle_pack(k, v, 0, "bf16")
+    assert_pack_bitexact(cache, ref)
+
+
+def test_pack_wait_runs_out_and_reports_timeout(kvq):
+    # the bf16 pack loader skips one item, so the wait on it can only end by
+    # its limit; afterwards a normal call packs the same cache bit-exactly
+    shape = (2, 2, 700, 128)
+    k = O.round_to_bf16(synth.normal_numpy(44, shape))
+    v = O.round_to_bf16(synth.normal_numpy(45, shape))
+    st = kvq.new_status()
+    try:
+        kvq.debug_set(wait_limit_ns=2_000_000, drop_item=3)
+        cache = kvq.pack(bf16_cuda(k), bf16_cuda(v), 64, "bf16", status=st)
+        code = kvq.read_status(st)
+    finally:
+        kvq.debug_set(0, -1)
+    assert code & kvq.DEV_TIMEOUT
+    st.zero_()
+    kvq.pack(bf16_cuda(k), bf16_cuda(v), 64, "bf16", out=cache, status=st)
+    assert kvq.read_status(st) == 0
+    _, ref = oracle_pack(k, v, 64, "bf16")
+    assert_pack_bitexact(cache, ref)
+
+
 def test_pack_edge_values_bitexact(kvq):
     # zero groups, exact .5 quotients, a negative amax, tiny and huge groups
     k = np.zeros((1, 1, 96, 32), np.float32)
@@ -705,8 +771,10 @@ def test_decode_full_size_sampled_units(kvq, batch, context):
         kn, vn = _unit_np(k, b, kvh), _unit_np(v, b, kvh)
         p = O.pack_head(kn, vn, 128, "bf16")
         ser = O.serialize_head(p)
-        np.testing.assert_array_equal(cache.k_codes[b, kvh].cpu().numpy().reshape(-1), ser["k_codes"].reshape(-1))
-        np.testing.assert_array_equal(cache.v_scales[b, kvh].cpu().numpy(), ser["v_scales"])
+        for key in ("k_codes", "k_scales", "v_codes", "v_scales"):
+            got = getattr(cache, key)[b, kvh].cpu().numpy()
+            np.testing.assert_array_equal(got.reshape(-1)[:ser[key].size],
+                                          ser[key].reshape(-1), err_msg=key)
         kh, vh = O.dequantize_head(p)
         for h in range(8 * kvh, 8 * kvh + 8):
             ref, _, _ = O.attention(q[b, h].float().cpu().numpy(), kh, vh)
