@@ -26,9 +26,10 @@
 // every tile row is one 128-byte load, read once for all 16 rows, and each
 // lane keeps the 16 rows' dot products on both paths (q from shared memory,
 // four features per broadcast load). stats_kernel: one CTA per query row;
-// both score rows come from workspace into shared memory, the statistics are
-// block reductions over them, and each top-k mass takes the k-th largest
-// probability from a radix select over the float bits.
+// both score rows come from workspace into shared memory (for N up to
+// kStagedTokens; longer rows are swept where they lie in the workspace, from
+// L2), the statistics are block reductions over them, and each top-k mass
+// takes the k-th largest probability from a radix select over the float bits.
 
 #include <cuda_fp8.h>
 #include <math_constants.h>
@@ -425,25 +426,32 @@ __device__ void kth_largest_bits3(const float *x, int n, const int (&k3)[3], uin
   }
 }
 
+// Rows of up to this many keys are staged in shared memory (2 x 64 KB).
+constexpr int kStagedTokens = 16384;
+
+template <bool kStaged>
 __global__ void __launch_bounds__(kThreads) stats_kernel(const StatsArgs a) {
   wait_prior_grid();
   allow_next_grid();
   extern __shared__ float sm[];
-  float *s_ref = sm;                 // [N]: scores, then p
-  float *s_mx = sm + a.N;            // [N]: scores of the MXFP8 Q/K path
+  const long row = blockIdx.x;       // (b * Hq + h) * n_q + i
+  // [N] each: scores, then p (reference path); scores of the MXFP8 Q/K path
+  float *s_ref = kStaged ? sm : a.s_ref + row * a.N;
+  float *s_mx = kStaged ? sm + a.N : a.s_mx + row * a.N;
   __shared__ float red[2 * kWarps];
   __shared__ int redi[2 * kWarps];
   __shared__ uint32_t hist[256], hist_top[256], sel[2];
-  const long row = blockIdx.x;       // (b * Hq + h) * n_q + i
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // the row's two score rows and its statistics (the same in every thread)
   if (!in_bounds(a.ctl, a.s_ref + row * a.N, sizeof(float) * a.N) ||
       !in_bounds(a.ctl, a.s_mx + row * a.N, sizeof(float) * a.N) ||
       !in_bounds(a.ctl, a.stats + row * KVQ_N_STATS, sizeof(float) * KVQ_N_STATS))
     return;
-  for (int j = threadIdx.x; j < a.N; j += kThreads) {
-    s_ref[j] = a.s_ref[row * a.N + j];
-    s_mx[j] = a.s_mx[row * a.N + j];
+  if (kStaged) {
+    for (int j = threadIdx.x; j < a.N; j += kThreads) {
+      s_ref[j] = a.s_ref[row * a.N + j];
+      s_mx[j] = a.s_mx[row * a.N + j];
+    }
   }
   __syncthreads();
 
@@ -534,7 +542,7 @@ __global__ void __launch_bounds__(kThreads) stats_kernel(const StatsArgs a) {
 
 }  // namespace
 
-int stats_max_tokens() { return 16384; }
+int stats_max_tokens() { return 1 << 20; }
 
 namespace {
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -589,7 +597,8 @@ int launch_attend_stats(const kvq_cache &c, const void *q, int q_dtype, int Hq, 
   const size_t ksmem = sizeof(float) * 2 * d.D * 33;
   const dim3 sgrid(static_cast<unsigned>((n_q + kRows - 1) / kRows),
                    static_cast<unsigned>(d.B * Hq), static_cast<unsigned>(a.key_splits));
-  const size_t smem = sizeof(float) * 2 * static_cast<size_t>(d.N);
+  const bool staged = d.N <= kStagedTokens;
+  const size_t smem = staged ? sizeof(float) * 2 * static_cast<size_t>(d.N) : 0;
   const long rows = static_cast<long>(d.B) * Hq * n_q;
   switch (d.D / 32) {
 #define KVQ_STATS_CASE(E)                                                                     \
@@ -606,8 +615,14 @@ int launch_attend_stats(const kvq_cache &c, const void *q, int q_dtype, int Hq, 
     default:
       return -1;
   }
-  opt_in_smem(stats_kernel, smem);
-  launch_dependent(stats_kernel, dim3(static_cast<unsigned>(rows)), dim3(kThreads), smem, s, a);
+  if (staged) {
+    opt_in_smem(stats_kernel<true>, smem);
+    launch_dependent(stats_kernel<true>, dim3(static_cast<unsigned>(rows)), dim3(kThreads), smem,
+                     s, a);
+  } else {
+    launch_dependent(stats_kernel<false>, dim3(static_cast<unsigned>(rows)), dim3(kThreads), 0, s,
+                     a);
+  }
   return 3;
 }
 

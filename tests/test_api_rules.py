@@ -43,9 +43,12 @@ def test_stats_rules(k):
     c96 = cache(k, d=96)
     assert lib.kv_attend_stats(ctypes.byref(c96), ADDR, 1, 4, 8, 0.0, None, ADDR, None,
                                ctypes.byref(sz), None, None) == 3       # D not a power of two
-    big = cache(k, n=20000, recent=20000)
+    long_rows = cache(k, n=20000, recent=20000)   # rows past shared memory: swept in place
+    assert lib.kv_attend_stats(ctypes.byref(long_rows), ADDR, 1, 4, 8, 0.0, None, ADDR, None,
+                               ctypes.byref(sz), None, None) == 0
+    big = cache(k, n=(1 << 20) + 32, recent=128)
     assert lib.kv_attend_stats(ctypes.byref(big), ADDR, 1, 4, 8, 0.0, None, ADDR, None,
-                               ctypes.byref(sz), None, None) == 3       # N > 16384
+                               ctypes.byref(sz), None, None) == 3       # N > 2^20
     assert lib.kv_attend_stats(ctypes.byref(c), ADDR, 1, 3, 8, 0.0, None, ADDR, None,
                                ctypes.byref(sz), None, None) == 1       # 3 q-heads over 2
     small = ctypes.c_size_t(16)

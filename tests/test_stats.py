@@ -72,6 +72,7 @@ def cache_case(kvq, seed, b, hkv, n, d, recent, kwin, spike=0.0):
     (1, 2, 4, 700, 128, 300, "bf16", True, 0.0),     # int4 history + bf16 window, signed-H128
     (2, 1, 2, 129, 32, 129, "f32", False, 0.0),      # ragged last block of 32 keys
     (1, 2, 2, 256, 64, 256, "mxfp8", True, 0.0),     # MXFP8 K window
+    (1, 1, 2, 20000, 128, 500, "bf16", True, 0.0),   # rows past shared memory, swept in place
 ])
 def test_stats_match_oracle(kvq, b, hkv, hq, n, d, recent, kwin, use_signs, spike):
     cache, khat = cache_case(kvq, 500 + n + d, b, hkv, n, d, recent, kwin, spike)
