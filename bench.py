@@ -544,11 +544,19 @@ def row_decode(kvq, synth, torch, steps, warmup, pk, batch, context):
     ms = time_steps(cycling([x.run for x in attends]), steps, warmup)
     gbs = nbytes / (ms * 1e-3) / 1e9
     keys = batch * d["q_heads"] * context
+    # the decode profile's traffic (full-size launch) scaled by this row's
+    # algorithmic bytes: the kernel's traffic tracks them (1.02x at every size
+    # captured), so the scaling is by the units of work each launch processes
+    full = profile_traffic("decode_kernel_B16_L32768.md")
+    full_bytes = decode_bytes(DECODE["batch"], d["kv_heads"], DECODE["context"], d["recent"])
+    traffic = None if full is None else int(round(full * nbytes / full_bytes))
     return {"workload": f"decode: B={batch}, 16 query heads over 2 KV heads, D=128, L={context}, "
                         "R=128 bf16, int4 groups of 32",
             "ms": ms, "keys_per_s": keys / (ms * 1e-3), "path": a.path, "l2": l2_note(n, nbytes),
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                         "frac": gbs / pk["hbm_gbs"], "traffic": None,
+                         "frac": gbs / pk["hbm_gbs"], "traffic": traffic,
+                         "traffic_note": "ncu DRAM bytes of the B=16, L=32768 decode launch, "
+                                         "scaled by algorithmic bytes",
                          "algorithmic_bytes": nbytes,
                          "kernel": "decode_kernel + combine_kernel (one kv_attend call)"},
             "launches": a.launches()}
