@@ -533,6 +533,11 @@ def row_decode(kvq, synth, torch, steps, warmup, pk, batch, context):
     d = dict(DECODE, batch=batch, context=context)
     nbytes = decode_bytes(batch, d["kv_heads"], context, d["recent"])
     n = rotation(nbytes)
+    flush = None
+    if n > 1 and (n - 1) * nbytes < 2 * L2_BYTES:
+        # too small for the rotation to keep two L2 sizes between reuses:
+        # one input set, L2 flushed before every call
+        n, flush = 1, make_flush()
     attends = []
     for i in range(n):
         q, k, v = synth.decode_inputs_torch(1 + 7 * i, batch, context, "cuda")
@@ -541,7 +546,7 @@ def row_decode(kvq, synth, torch, steps, warmup, pk, batch, context):
         attends.append(kvq.Attend(cache, q, out_dtype="bf16"))
     a = attends[0]
     a.run()
-    ms = time_steps(cycling([x.run for x in attends]), steps, warmup)
+    ms = time_steps(cycling([x.run for x in attends]), steps, warmup, flush=flush)
     gbs = nbytes / (ms * 1e-3) / 1e9
     keys = batch * d["q_heads"] * context
     # the decode profile's traffic (full-size launch) scaled by this row's
@@ -552,7 +557,9 @@ def row_decode(kvq, synth, torch, steps, warmup, pk, batch, context):
     traffic = None if full is None else int(round(full * nbytes / full_bytes))
     return {"workload": f"decode: B={batch}, 16 query heads over 2 KV heads, D=128, L={context}, "
                         "R=128 bf16, int4 groups of 32",
-            "ms": ms, "keys_per_s": keys / (ms * 1e-3), "path": a.path, "l2": l2_note(n, nbytes),
+            "ms": ms, "keys_per_s": keys / (ms * 1e-3), "path": a.path,
+            "l2": (f"L2 flushed before every call ({nbytes / 1e6:.1f} MB per call)" if flush
+                   else l2_note(n, nbytes)),
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
                          "frac": gbs / pk["hbm_gbs"], "traffic": traffic,
                          "traffic_note": "ncu DRAM bytes of the B=16, L=32768 decode launch, "
@@ -928,6 +935,16 @@ ROWS = {
         row_decode(kvq, synth, torch, st, w, pk, 64, 8192),
     "decode_B64_L1024": lambda kvq, synth, torch, st, w, pk:
         row_decode(kvq, synth, torch, st, w, pk, 64, 1024),
+    "decode_B16_L8192": lambda kvq, synth, torch, st, w, pk:
+        row_decode(kvq, synth, torch, st, w, pk, 16, 8192),
+    "decode_B16_L1024": lambda kvq, synth, torch, st, w, pk:
+        row_decode(kvq, synth, torch, st, w, pk, 16, 1024),
+    "decode_B1_L32768": lambda kvq, synth, torch, st, w, pk:
+        row_decode(kvq, synth, torch, st, w, pk, 1, 32768),
+    "decode_B1_L8192": lambda kvq, synth, torch, st, w, pk:
+        row_decode(kvq, synth, torch, st, w, pk, 1, 8192),
+    "decode_B1_L1024": lambda kvq, synth, torch, st, w, pk:
+        row_decode(kvq, synth, torch, st, w, pk, 1, 1024),
     "pack": lambda kvq, synth, torch, st, w, pk: row_pack(kvq, synth, torch, st, w, pk),
     "append": lambda kvq, synth, torch, st, w, pk: row_append(kvq, synth, torch, st, w, pk),
     "small_d_fp32": lambda kvq, synth, torch, st, w, pk: row_small(kvq, synth, torch, st, w, pk),

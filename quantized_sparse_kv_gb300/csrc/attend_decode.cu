@@ -708,6 +708,95 @@ __global__ void __launch_bounds__(256) combine_kernel(const DecodeArgs a, OT *__
   store_from_f32(o + 3, acc.w * inv);
 }
 
+// The same merge for units whose partials come from many CTAs (small
+// batches, where each unit spans a large share of the grid): one block per
+// (unit, query head), warp w merging slots w, w + 8, ..., then the eight
+// warps' states merged through shared memory.
+constexpr int kWideCombineAbove = 32;  // slots per unit above which it is used
+
+template <typename OT>
+__global__ void __launch_bounds__(256) combine_wide_kernel(const DecodeArgs a,
+                                                           OT *__restrict__ out) {
+  wait_prior_grid();
+  allow_next_grid();
+  __shared__ float sm_m[8], sm_l[8];
+  __shared__ float4 sm_acc[8][32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int u = blockIdx.x, h = blockIdx.y;
+  const int n = cta_of_item(a, (u + 1) * a.ipu - 1) - cta_of_item(a, u * a.ipu) + 1;
+  const float *base = partial_of(a, u, 0) + h * kPartFloats;
+  constexpr int kSlot = kHeads * kPartFloats;
+#ifdef KVQ_DEBUG
+  if (!in_bounds(a.ctl, base - h * kPartFloats, sizeof(float) * n * kSlot) ||
+      !in_bounds(a.ctl, out + (static_cast<long>(u) * kHeads + h) * kD, kD * sizeof(OT)))
+    return;
+#endif
+  constexpr int kBatch = 8;
+  float m = -CUDART_INF_F, l = 0.0f;
+  float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  for (int c0 = warp; c0 < n; c0 += 8 * kBatch) {
+    float pm[kBatch], pl[kBatch];
+    float4 po[kBatch];
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      const int c = c0 + 8 * i;
+      const float *p = base + static_cast<long>(min(c, n - 1)) * kSlot;
+      const float2 ml = *reinterpret_cast<const float2 *>(p + kD);
+      pm[i] = c < n ? ml.x : -CUDART_INF_F;
+      pl[i] = ml.y;
+      po[i] = *reinterpret_cast<const float4 *>(p + 4 * lane);
+    }
+    float nm = m;
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) nm = fmaxf(nm, pm[i]);
+    if (nm == -CUDART_INF_F) continue;
+    const float r = exp2f(m - nm);  // 0 while m is -inf
+    l *= r;
+    acc.x *= r;
+    acc.y *= r;
+    acc.z *= r;
+    acc.w *= r;
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      const float w = exp2f(pm[i] - nm);  // 0 for empty and padded slots
+      l += w * pl[i];
+      acc.x += w * po[i].x;
+      acc.y += w * po[i].y;
+      acc.z += w * po[i].z;
+      acc.w += w * po[i].w;
+    }
+    m = nm;
+  }
+  sm_acc[warp][lane] = acc;
+  if (lane == 0) {
+    sm_m[warp] = m;
+    sm_l[warp] = l;
+  }
+  __syncthreads();
+  if (warp != 0) return;
+  float mx = -CUDART_INF_F;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) mx = fmaxf(mx, sm_m[w]);
+  float ls = 0.0f;
+  float4 o4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    const float c = sm_m[w] == -CUDART_INF_F ? 0.0f : exp2f(sm_m[w] - mx);
+    const float4 x = sm_acc[w][lane];
+    ls += c * sm_l[w];
+    o4.x += c * x.x;
+    o4.y += c * x.y;
+    o4.z += c * x.z;
+    o4.w += c * x.w;
+  }
+  const float inv = 1.0f / ls;
+  OT *o = out + (static_cast<long>(u) * kHeads + h) * kD + 4 * lane;
+  store_from_f32(o + 0, o4.x * inv);
+  store_from_f32(o + 1, o4.y * inv);
+  store_from_f32(o + 2, o4.z * inv);
+  store_from_f32(o + 3, o4.w * inv);
+}
+
 struct Plan {
   int total_items;
   int ipu, Gi, Wt, num_ctas, max_ctas_per_unit;
@@ -783,12 +872,21 @@ int launch_attend_decode(const kvq_cache &c, const void *q, int q_dtype, float s
   // The combine grid's blocks may be placed while the decode grid drains; they
   // wait for it on the device.
   launch_dependent(decode_kernel, dim3(p.num_ctas), dim3(kThreads), smem, s, a);
-  if (out_dtype == KVQ_F32)
+  if (p.max_ctas_per_unit > kWideCombineAbove) {
+    const dim3 grid(static_cast<unsigned>(p.units), kHeads);
+    if (out_dtype == KVQ_F32)
+      launch_dependent(combine_wide_kernel<float>, grid, dim3(256), 0, s, a,
+                       static_cast<float *>(out));
+    else
+      launch_dependent(combine_wide_kernel<__nv_bfloat16>, grid, dim3(256), 0, s, a,
+                       static_cast<__nv_bfloat16 *>(out));
+  } else if (out_dtype == KVQ_F32) {
     launch_dependent(combine_kernel<float>, dim3(p.units), dim3(kHeads * 32), 0, s, a,
                      static_cast<float *>(out));
-  else
+  } else {
     launch_dependent(combine_kernel<__nv_bfloat16>, dim3(p.units), dim3(kHeads * 32), 0, s, a,
                      static_cast<__nv_bfloat16 *>(out));
+  }
   return 2;
 }
 

@@ -755,7 +755,7 @@ def _unit_np(t, b, h):
 
 
 @pytest.mark.parametrize("batch,context", [(64, 32768), (16, 32768), (64, 8192), (1, 32768),
-                                           (64, 1024)])
+                                           (64, 1024), (1, 8192), (16, 1024)])
 def test_decode_full_size_sampled_units(kvq, batch, context):
     # the decode workloads at full size (16 q-heads / 2 KV heads, D=128, R=128):
     # the timed step (64, 32768) and the other graded batch / context sizes,
