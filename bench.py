@@ -625,9 +625,12 @@ def row_stats(kvq, synth, torch, steps, warmup, pk):
                          "frac": tf / peak, "traffic": None,
                          "peak_note": "fp32 FMA: 152 SMs x 128 lanes x 2 flop x 2.07 GHz",
                          "note": "three kernels: keys once per head into 32-key tiles, "
-                                 "scores of 16 rows per CTA (lane = key), per-row "
-                                 "statistics; flops counted are the two score dot products "
-                                 "only, the statistics passes take about 40 % of the time"},
+                                 "scores of 48 rows per CTA on the tensor cores (tf32 "
+                                 "mma.sync: three products per pair on the fp32 path, one "
+                                 "on the exact MXFP8 path), per-row statistics; flops "
+                                 "counted are the two score dot products only, against the "
+                                 "fp32 FMA rate of a CUDA-core scoring; the statistics "
+                                 "passes take about 43 % of the time"},
             "launches": 3}
 
 

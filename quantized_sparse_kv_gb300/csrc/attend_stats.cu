@@ -284,6 +284,150 @@ __global__ void __launch_bounds__(kThreads) scores_kernel(const StatsArgs a) {
   }
 }
 
+// ---- the same scores on the tensor cores (D = 128)
+// mma.sync m16n8k8 with tf32 operands: 16 query rows are M, 8 keys of a tile
+// N, 8 features K; a CTA takes 48 query rows, so that each key fragment read
+// from L2 feeds three m-tiles (the key tiles are read once per 48 rows instead
+// of once per 16). Reference path: each operand split into a tf32 high
+// part and a tf32 low part (x = hi + lo to about 2^-22 of |x|), the product
+// taken as hi.hi + hi.lo + lo.hi (three MMAs; the lo.lo term and the split
+// residuals are below 2^-21 of a product). MXFP8 Q/K path: E4M3 values times
+// a power of two have at most four significant bits, exact in tf32, so one
+// MMA gives the exact products. Accumulation in fp32.
+__device__ __forceinline__ uint32_t tf32_hi(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
+__device__ __forceinline__ void mma_tf32(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+constexpr int kQPad = 132;  // floats per staged q row: lanes (g, t) read banks 4g + t
+constexpr int kTcRows = 48;  // query rows per CTA: three m-tiles share each key fragment
+
+struct ScoresTcSmem {
+  float qf[kTcRows][128];
+  uint32_t q_hi[kTcRows][kQPad], q_lo[kTcRows][kQPad], q_mx[kTcRows][kQPad];
+};
+
+__global__ void __launch_bounds__(kThreads) scores_tc_kernel(const StatsArgs a) {
+  wait_prior_grid();
+  allow_next_grid();
+  constexpr int D = 128, E = 4, kM = kTcRows / 16;
+  extern __shared__ __align__(16) uint8_t tc_smem_raw[];
+  ScoresTcSmem &sm = *reinterpret_cast<ScoresTcSmem *>(tc_smem_raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long bh = blockIdx.y;  // b * Hq + h
+  const int h = static_cast<int>(bh % a.Hq);
+  const long u = (bh / a.Hq) * a.Hkv + h / a.group;
+  const int i0 = blockIdx.x * kTcRows;
+  const int nr = min(kTcRows, a.n_q - i0);
+  const long row0 = bh * a.n_q + i0;
+  const size_t qe = a.q_dtype == KVQ_F32 ? 4 : 2;
+  if (!in_bounds(a.ctl, static_cast<const uint8_t *>(a.q) + row0 * D * qe, qe * D * nr) ||
+      (a.signs && !in_bounds(a.ctl, a.signs, sizeof(float) * D)) ||
+      !in_bounds(a.ctl, a.s_ref + row0 * a.N, sizeof(float) * a.N * nr) ||
+      !in_bounds(a.ctl, a.s_mx + row0 * a.N, sizeof(float) * a.N * nr))
+    return;
+  for (int e = threadIdx.x; e < kTcRows * D; e += kThreads) {
+    const int r = e / D, d = e % D;
+    const long gi = (row0 + r) * D + d;
+    const float x = r >= nr ? 0.0f
+                    : a.q_dtype == KVQ_F32 ? static_cast<const float *>(a.q)[gi]
+                                           : load_f32(static_cast<const __nv_bfloat16 *>(a.q) + gi);
+    sm.qf[r][d] = x;
+    const uint32_t hi = tf32_hi(x);
+    sm.q_hi[r][d] = hi;
+    sm.q_lo[r][d] = tf32_hi(x - __uint_as_float(hi));
+  }
+  __syncthreads();
+  for (int r = warp; r < kTcRows; r += kWarps) {
+    float x[E];
+#pragma unroll
+    for (int t = 0; t < E; ++t) x[t] = sm.qf[r][lane * E + t];
+    if (a.signs) signed_hadamard<E>(x, a.signs, lane);
+    mxfp8_round_row<E>(x);
+#pragma unroll
+    for (int t = 0; t < E; ++t) sm.q_mx[r][lane * E + t] = __float_as_uint(x[t]);
+  }
+  __syncthreads();
+
+  const int g = lane >> 2, t4 = lane & 3;
+  const int per = (a.T + a.key_splits - 1) / a.key_splits;
+  const int t_lo = blockIdx.z * per, t_hi = min(a.T, t_lo + per);
+  for (int tile = t_lo + warp; tile < t_hi; tile += kWarps) {
+    const float *kr = a.k_ref + (u * a.T + tile) * D * 32;
+    const float *km = a.k_mx + (u * a.T + tile) * D * 32;
+    if (!in_bounds(a.ctl, kr, sizeof(float) * D * 32) ||
+        !in_bounds(a.ctl, km, sizeof(float) * D * 32))
+      continue;
+#pragma unroll 1
+    for (int half = 0; half < 2; ++half) {  // keys 16 half .. 16 half + 15 of the tile
+      float cr[kM][2][4], cm[kM][2][4];  // [m-tile][key group of 8][fragment]
+#pragma unroll
+      for (int m = 0; m < kM; ++m)
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) cr[m][n][j] = cm[m][n][j] = 0.0f;
+#pragma unroll 2
+      for (int k0 = 0; k0 < D; k0 += 8) {
+        uint32_t bh[2][2], bl[2][2], bm[2][2];
+#pragma unroll
+        for (int n = 0; n < 2; ++n) {
+          // B[k][key]: features k0 + t4 and k0 + t4 + 4 of key 16 half + 8n + g
+          const int key = 16 * half + 8 * n + g;
+          const float x0 = __ldg(kr + (k0 + t4) * 32 + key);
+          const float x1 = __ldg(kr + (k0 + t4 + 4) * 32 + key);
+          bm[n][0] = __float_as_uint(__ldg(km + (k0 + t4) * 32 + key));
+          bm[n][1] = __float_as_uint(__ldg(km + (k0 + t4 + 4) * 32 + key));
+          bh[n][0] = tf32_hi(x0);
+          bh[n][1] = tf32_hi(x1);
+          bl[n][0] = tf32_hi(x0 - __uint_as_float(bh[n][0]));
+          bl[n][1] = tf32_hi(x1 - __uint_as_float(bh[n][1]));
+        }
+#pragma unroll
+        for (int m = 0; m < kM; ++m) {
+          const int ra = 16 * m + g, rb = ra + 8;
+          const uint32_t ah[4] = {sm.q_hi[ra][k0 + t4], sm.q_hi[rb][k0 + t4],
+                                  sm.q_hi[ra][k0 + t4 + 4], sm.q_hi[rb][k0 + t4 + 4]};
+          const uint32_t al[4] = {sm.q_lo[ra][k0 + t4], sm.q_lo[rb][k0 + t4],
+                                  sm.q_lo[ra][k0 + t4 + 4], sm.q_lo[rb][k0 + t4 + 4]};
+          const uint32_t am[4] = {sm.q_mx[ra][k0 + t4], sm.q_mx[rb][k0 + t4],
+                                  sm.q_mx[ra][k0 + t4 + 4], sm.q_mx[rb][k0 + t4 + 4]};
+#pragma unroll
+          for (int n = 0; n < 2; ++n) {
+            mma_tf32(cr[m][n], al[0], al[1], al[2], al[3], bh[n][0], bh[n][1]);
+            mma_tf32(cr[m][n], ah[0], ah[1], ah[2], ah[3], bl[n][0], bl[n][1]);
+            mma_tf32(cr[m][n], ah[0], ah[1], ah[2], ah[3], bh[n][0], bh[n][1]);
+            mma_tf32(cm[m][n], am[0], am[1], am[2], am[3], bm[n][0], bm[n][1]);
+          }
+        }
+      }
+      // C fragment: rows 16m + g (+ 8); keys 16 half + 8n + 2t4 (+ 1)
+#pragma unroll
+      for (int m = 0; m < kM; ++m)
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int r = 16 * m + g + 8 * (j >> 1);
+            const int key = tile * 32 + 16 * half + 8 * n + 2 * t4 + (j & 1);
+            if (r < nr && key < a.N) {
+              a.s_ref[(row0 + r) * a.N + key] = a.sm_scale * cr[m][n][j];
+              a.s_mx[(row0 + r) * a.N + key] = a.sm_scale * cm[m][n][j];
+            }
+          }
+    }
+  }
+}
+
 __device__ __forceinline__ float block_sum(float x, float *red) {
   x = warp_sum(x);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -609,9 +753,21 @@ int launch_attend_stats(const kvq_cache &c, const void *q, int q_dtype, int Hq, 
     break;
     KVQ_STATS_CASE(1)
     KVQ_STATS_CASE(2)
-    KVQ_STATS_CASE(4)
     KVQ_STATS_CASE(8)
 #undef KVQ_STATS_CASE
+    case 4: {  // D = 128: the scores on the tensor cores, 48 query rows per CTA
+      opt_in_smem(keys_kernel<4>, ksmem);
+      launch_dependent(keys_kernel<4>, kgrid, dim3(kThreads), ksmem, s, a);
+      StatsArgs at = a;
+      const long tc_blocks = static_cast<long>(d.B) * Hq * ((n_q + kTcRows - 1) / kTcRows);
+      at.key_splits = static_cast<int>(std::max<long>(
+          1, std::min<long>({(1024 + tc_blocks - 1) / tc_blocks, at.T / 8, 65535L})));
+      const dim3 tgrid(static_cast<unsigned>((n_q + kTcRows - 1) / kTcRows),
+                       static_cast<unsigned>(d.B * Hq), static_cast<unsigned>(at.key_splits));
+      opt_in_smem(scores_tc_kernel, sizeof(ScoresTcSmem));
+      launch_dependent(scores_tc_kernel, tgrid, dim3(kThreads), sizeof(ScoresTcSmem), s, at);
+      break;
+    }
     default:
       return -1;
   }
