@@ -237,8 +237,9 @@ enum {
  * every query row: about 8 x B x Hkv x N x D + 8 x B x q_heads x n_q x N
  * bytes).
  * Restrictions (else KVQ_ERR_UNSUPPORTED): D in {32, 64, 128, 256},
- * N <= 1,048,576, batch * q_heads <= 65,535. Rows of up to 16,384 keys are
- * swept in shared memory; longer ones in place in the workspace (slower).
+ * N <= 1,048,576, batch * q_heads <= 65,535. A row's reference scores are
+ * swept in shared memory up to 16,384 keys, longer rows in place in the
+ * workspace (slower).
  */
 KVQ_API kvq_status kv_attend_stats(const kvq_cache *cache, const void *q, int32_t q_dtype,
                                    int32_t q_heads, int32_t n_q, float sm_scale,

@@ -26,10 +26,12 @@
 // every tile row is one 128-byte load, read once for all 16 rows, and each
 // lane keeps the 16 rows' dot products on both paths (q from shared memory,
 // four features per broadcast load). stats_kernel: one CTA per query row;
-// both score rows come from workspace into shared memory (for N up to
-// kStagedTokens; longer rows are swept where they lie in the workspace, from
-// L2), the statistics are block reductions over them, and each top-k mass
-// takes the k-th largest probability from a radix select over the float bits.
+// the reference score row comes from workspace into shared memory (for N up
+// to kStagedTokens; longer rows are swept where they lie in the workspace,
+// from L2), the MXFP8 Q/K row, which three passes read, stays in the
+// workspace; the statistics are block reductions over them, and each top-k
+// mass takes the k-th largest probability from a radix select over the
+// float bits.
 
 #include <cuda_fp8.h>
 #include <math_constants.h>
@@ -570,7 +572,7 @@ __device__ void kth_largest_bits3(const float *x, int n, const int (&k3)[3], uin
   }
 }
 
-// Rows of up to this many keys are staged in shared memory (2 x 64 KB).
+// Rows of up to this many keys are staged in shared memory (64 KB).
 constexpr int kStagedTokens = 16384;
 
 template <bool kStaged>
@@ -579,9 +581,10 @@ __global__ void __launch_bounds__(kThreads) stats_kernel(const StatsArgs a) {
   allow_next_grid();
   extern __shared__ float sm[];
   const long row = blockIdx.x;       // (b * Hq + h) * n_q + i
-  // [N] each: scores, then p (reference path); scores of the MXFP8 Q/K path
+  // [N] each: scores, then p (reference path; staged in shared memory when it
+  // fits) and the scores of the MXFP8 Q/K path (three passes read it: from L2)
   float *s_ref = kStaged ? sm : a.s_ref + row * a.N;
-  float *s_mx = kStaged ? sm + a.N : a.s_mx + row * a.N;
+  float *s_mx = a.s_mx + row * a.N;
   __shared__ float red[2 * kWarps];
   __shared__ int redi[2 * kWarps];
   __shared__ uint32_t hist[256], hist_top[256], sel[2];
@@ -591,12 +594,8 @@ __global__ void __launch_bounds__(kThreads) stats_kernel(const StatsArgs a) {
       !in_bounds(a.ctl, a.s_mx + row * a.N, sizeof(float) * a.N) ||
       !in_bounds(a.ctl, a.stats + row * KVQ_N_STATS, sizeof(float) * KVQ_N_STATS))
     return;
-  if (kStaged) {
-    for (int j = threadIdx.x; j < a.N; j += kThreads) {
-      s_ref[j] = a.s_ref[row * a.N + j];
-      s_mx[j] = a.s_mx[row * a.N + j];
-    }
-  }
+  if (kStaged)
+    for (int j = threadIdx.x; j < a.N; j += kThreads) s_ref[j] = a.s_ref[row * a.N + j];
   __syncthreads();
 
   int am_ref, am_mx;
@@ -742,7 +741,7 @@ int launch_attend_stats(const kvq_cache &c, const void *q, int q_dtype, int Hq, 
   const dim3 sgrid(static_cast<unsigned>((n_q + kRows - 1) / kRows),
                    static_cast<unsigned>(d.B * Hq), static_cast<unsigned>(a.key_splits));
   const bool staged = d.N <= kStagedTokens;
-  const size_t smem = staged ? sizeof(float) * 2 * static_cast<size_t>(d.N) : 0;
+  const size_t smem = staged ? sizeof(float) * static_cast<size_t>(d.N) : 0;
   const long rows = static_cast<long>(d.B) * Hq * n_q;
   switch (d.D / 32) {
 #define KVQ_STATS_CASE(E)                                                                     \
