@@ -138,10 +138,10 @@ KVQ_API size_t kvq_cache_bytes(int32_t batch, int32_t kv_heads, int32_t n_tokens
  * narrower; E4M3 with an E8M0 scale per 32 features for an MXFP8 K window).
  * int4 rule: scale = amax / 7 rounded to fp32, code = clamp(rint(x / scale),
  * -7, 7) with the division correctly rounded in fp32 and ties to even; a zero
- * scale gives all-zero codes. Inputs are expected finite: a group holding an
- * infinity follows the rule above, but the code of a NaN element is
- * unspecified. The cache's shape fields and array pointers are read;
- * header[] is written. dev_status may be NULL.
+ * scale gives all-zero codes. Inputs are expected finite: the code of a NaN
+ * or infinite element is unspecified (the group's other elements follow the
+ * rule; a NaN does not enter amax). The cache's shape fields and array
+ * pointers are read; header[] is written. dev_status may be NULL.
  */
 KVQ_API kvq_status kv_pack(const void *k, const void *v, int32_t in_dtype, kvq_cache *cache,
                            int32_t *dev_status, kvq_stream_t stream);
